@@ -1,0 +1,245 @@
+/*
+ * CPU oracle for the routed-expert RVQ MoE step.  TEST INFRASTRUCTURE ONLY:
+ * only the tests, the package's smoke check and the benchmark's CPU-baseline
+ * leg may load it.  It shares no code, header or table with the CUDA
+ * library, and the library never calls it.
+ *
+ * Plain, slow, single-threaded C.  Inputs are the fp32 / uint8 arrays the
+ * method stores; every sum is carried in double.  Each function states the
+ * passage it follows.  Sources (web pages about the WASTE engine):
+ *   [fr]  "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s"
+ *   [vi]  "Chạy Kimi K3 ở 0.50 tok/s với 29GB RAM"  (same text, Vietnamese)
+ * Where the pages leave a step open, the reading taken is stated at the
+ * function.
+ *
+ * Logical code layout used throughout (one matrix with n_out rows and
+ * n_in = 8*nv inputs): codes[r][s][j], r < n_out, s < 3 stages, j < nv,
+ * i.e. byte (r*3 + s)*nv + j.  Vector j of row r covers inputs 8j..8j+7.
+ * Codebooks of one matrix: cb[s][c][v], s < 3, c < 256, v < 8, fp32.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_STAGES 3
+#define OR_K 256
+#define OR_V 8
+
+static size_t code_index(int nv, int r, int s, int j) {
+    return ((size_t)r * OR_STAGES + (size_t)s) * (size_t)nv + (size_t)j;
+}
+
+static double cb_at(const float *cb, int s, int c, int v) {
+    return (double)cb[((size_t)s * OR_K + (size_t)c) * OR_V + (size_t)v];
+}
+
+/*
+ * Dequantise one matrix ([fr] "Quantification et exactitude": residual
+ * vector quantisation in 3 stages, 256-entry codebooks of 8-dimensional
+ * vectors).  Reading: the stages are residuals, so a weight vector is the
+ * sum of the three selected codebook vectors; the sum is taken in double
+ * (exact for three fp32 addends of these magnitudes up to rounding at 2^-53).
+ * W is row-major [n_out][n_in].
+ */
+void oracle_dequant(int n_out, int n_in, const float *cb, const uint8_t *codes, double *W) {
+    int nv = n_in / OR_V;
+    for (int r = 0; r < n_out; ++r)
+        for (int j = 0; j < nv; ++j)
+            for (int v = 0; v < OR_V; ++v) {
+                double w = 0.0;
+                for (int s = 0; s < OR_STAGES; ++s)
+                    w += cb_at(cb, s, codes[code_index(nv, r, s, j)], v);
+                W[(size_t)r * n_in + (size_t)j * OR_V + v] = w;
+            }
+}
+
+/* y = W x, plain row-by-row dot products in double. */
+void oracle_matvec_dense(int n_out, int n_in, const double *W, const double *x, double *y) {
+    for (int r = 0; r < n_out; ++r) {
+        double acc = 0.0;
+        for (int i = 0; i < n_in; ++i) acc += W[(size_t)r * n_in + i] * x[i];
+        y[r] = acc;
+    }
+}
+
+/*
+ * The pages' product without rebuilding the matrix ([fr] "Quantification et
+ * exactitude": a table of partial dot products is built, then every row
+ * costs 3 table lookups and 2 additions per vector).  Table entry
+ * T[s][j][c] = <cb[s][c][:], x[8j..8j+7]>; row r accumulates
+ * T[0][j][c0] + T[1][j][c1] + T[2][j][c2] over its vectors j.
+ */
+void oracle_matvec_lut(int n_out, int n_in, const float *cb, const uint8_t *codes,
+                       const double *x, double *y) {
+    int nv = n_in / OR_V;
+    double *T = (double *)malloc(sizeof(double) * (size_t)OR_STAGES * (size_t)nv * OR_K);
+    if (!T) return;
+    for (int s = 0; s < OR_STAGES; ++s)
+        for (int j = 0; j < nv; ++j)
+            for (int c = 0; c < OR_K; ++c) {
+                double t = 0.0;
+                for (int v = 0; v < OR_V; ++v) t += cb_at(cb, s, c, v) * x[(size_t)j * OR_V + v];
+                T[((size_t)s * nv + j) * OR_K + c] = t;
+            }
+    for (int r = 0; r < n_out; ++r) {
+        double acc = 0.0;
+        for (int j = 0; j < nv; ++j) {
+            double t0 = T[((size_t)0 * nv + j) * OR_K + codes[code_index(nv, r, 0, j)]];
+            double t1 = T[((size_t)1 * nv + j) * OR_K + codes[code_index(nv, r, 1, j)]];
+            double t2 = T[((size_t)2 * nv + j) * OR_K + codes[code_index(nv, r, 2, j)]];
+            acc += t0 + t1 + t2;
+        }
+        y[r] = acc;
+    }
+    free(T);
+}
+
+/*
+ * Router logits l[e] = sum_i W_r[e][i] h[i] + b[e] ([fr] "Lecture anticipée
+ * et prédiction du routeur": the router of a layer decides the expert IDs).
+ * bias may be NULL (no bias).
+ */
+void oracle_router(int n_experts, int d, const float *Wr, const float *bias, const double *h,
+                   double *logits) {
+    for (int e = 0; e < n_experts; ++e) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += (double)Wr[(size_t)e * d + i] * h[i];
+        logits[e] = acc + (bias ? (double)bias[e] : 0.0);
+    }
+}
+
+/* true when expert a ranks before expert b: larger logit first, lower index on ties */
+static int ranks_before(const double *l, int a, int b) {
+    if (l[a] > l[b]) return 1;
+    if (l[a] < l[b]) return 0;
+    return a < b;
+}
+
+/*
+ * Top-k selection and gate normalisation.  The pages give 16 expert IDs per
+ * token and layer ([fr] "Lecture anticipée ..."); the order (logit
+ * descending, lowest index first on equal logits) and the softmax over the
+ * k selected logits are the readings taken where the pages are silent.
+ * Selection is a plain k-pass scan; idx comes out in rank order.
+ */
+void oracle_topk_softmax(int n_experts, int k, const double *logits, int32_t *idx, double *gate) {
+    unsigned char *taken = (unsigned char *)calloc((size_t)n_experts, 1);
+    if (!taken) return;
+    for (int i = 0; i < k; ++i) {
+        int best = -1;
+        for (int e = 0; e < n_experts; ++e) {
+            if (taken[e]) continue;
+            if (best < 0 || ranks_before(logits, e, best)) best = e;
+        }
+        taken[best] = 1;
+        idx[i] = best;
+    }
+    double lmax = logits[idx[0]];
+    double z = 0.0;
+    for (int i = 0; i < k; ++i) z += exp(logits[idx[i]] - lmax);
+    for (int i = 0; i < k; ++i) gate[i] = exp(logits[idx[i]] - lmax) / z;
+    free(taken);
+}
+
+/* silu(z) = z / (1 + e^-z) */
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/*
+ * One expert's FFN on one token: a = silu(G x) * (U x), y = D a.  The three
+ * matrices gate, up and down are the ones the pages store side by side in
+ * one record ([fr] "Architecture de streaming depuis le disque"); SwiGLU is
+ * the reading taken for how they combine.  cb holds the expert's codebooks
+ * [3 matrices: gate, up, down][3][256][8]; use_lut selects the table form
+ * (1) or dequantise-then-multiply (0).
+ */
+void oracle_expert_ffn(int d, int f, const float *cb, const uint8_t *gate_codes,
+                       const uint8_t *up_codes, const uint8_t *down_codes, const double *x,
+                       double *y, int use_lut) {
+    const size_t cb_mat = (size_t)OR_STAGES * OR_K * OR_V;
+    double *zg = (double *)malloc(sizeof(double) * (size_t)f);
+    double *zu = (double *)malloc(sizeof(double) * (size_t)f);
+    double *a = (double *)malloc(sizeof(double) * (size_t)f);
+    if (!zg || !zu || !a) { free(zg); free(zu); free(a); return; }
+    if (use_lut) {
+        oracle_matvec_lut(f, d, cb + 0 * cb_mat, gate_codes, x, zg);
+        oracle_matvec_lut(f, d, cb + 1 * cb_mat, up_codes, x, zu);
+    } else {
+        double *W = (double *)malloc(sizeof(double) * (size_t)f * (size_t)d);
+        if (!W) { free(zg); free(zu); free(a); return; }
+        oracle_dequant(f, d, cb + 0 * cb_mat, gate_codes, W);
+        oracle_matvec_dense(f, d, W, x, zg);
+        oracle_dequant(f, d, cb + 1 * cb_mat, up_codes, W);
+        oracle_matvec_dense(f, d, W, x, zu);
+        free(W);
+    }
+    for (int r = 0; r < f; ++r) a[r] = oracle_silu(zg[r]) * zu[r];
+    if (use_lut) {
+        oracle_matvec_lut(d, f, cb + 2 * cb_mat, down_codes, a, y);
+    } else {
+        double *W = (double *)malloc(sizeof(double) * (size_t)d * (size_t)f);
+        if (!W) { free(zg); free(zu); free(a); return; }
+        oracle_dequant(d, f, cb + 2 * cb_mat, down_codes, W);
+        oracle_matvec_dense(d, f, W, a, y);
+        free(W);
+    }
+    free(zg); free(zu); free(a);
+}
+
+/*
+ * Gate-weighted combine of the k expert outputs of one token:
+ * out[i] = base[i] + sum_k gate[k] * ys[k][i], k in rank order.  base may be
+ * NULL (zero).  The residual form h + combine is the reading taken for how a
+ * layer's output feeds the next layer.
+ */
+void oracle_combine(int d, int k, const double *gate, const double *ys, const double *base,
+                    double *out) {
+    for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int t = 0; t < k; ++t) acc += gate[t] * ys[(size_t)t * d + i];
+        out[i] = (base ? base[i] : 0.0) + acc;
+    }
+}
+
+/*
+ * One MoE layer over T tokens with every expert's arrays in memory:
+ * per token, router -> top-k + softmax -> k expert FFNs -> combine.
+ * h [T][d] (double), cbs [E][3][3][256][8], codes in the logical layout per
+ * expert: gate/up [E][f][3][d/8], down [E][d][3][f/8].  residual != 0 adds
+ * h to the output.  logits [T][E], idx [T][k], gate [T][k] are outputs.
+ */
+void oracle_moe_layer(int T, int d, int f, int n_experts, int k, const float *Wr,
+                      const float *bias, const float *cbs, const uint8_t *gate_codes,
+                      const uint8_t *up_codes, const uint8_t *down_codes, const double *h,
+                      int residual, int use_lut, double *out, double *logits, int32_t *idx,
+                      double *gate) {
+    const size_t cb_exp = (size_t)3 * OR_STAGES * OR_K * OR_V;
+    const size_t gu_exp = (size_t)f * OR_STAGES * (size_t)(d / OR_V);
+    const size_t dn_exp = (size_t)d * OR_STAGES * (size_t)(f / OR_V);
+    double *ys = (double *)malloc(sizeof(double) * (size_t)k * (size_t)d);
+    if (!ys) return;
+    for (int t = 0; t < T; ++t) {
+        const double *ht = h + (size_t)t * d;
+        double *lt = logits + (size_t)t * n_experts;
+        oracle_router(n_experts, d, Wr, bias, ht, lt);
+        oracle_topk_softmax(n_experts, k, lt, idx + (size_t)t * k, gate + (size_t)t * k);
+        for (int i = 0; i < k; ++i) {
+            int e = idx[(size_t)t * k + i];
+            oracle_expert_ffn(d, f, cbs + (size_t)e * cb_exp, gate_codes + (size_t)e * gu_exp,
+                              up_codes + (size_t)e * gu_exp, down_codes + (size_t)e * dn_exp, ht,
+                              ys + (size_t)i * d, use_lut);
+        }
+        oracle_combine(d, k, gate + (size_t)t * k, ys, residual ? ht : NULL,
+                       out + (size_t)t * d);
+    }
+    free(ys);
+}
+
+/*
+ * Bytes of codes per expert: 3 matrices (gate, up, down) of d*f weights at
+ * 3 stages x 1 byte per 8 weights = 3.00 bits per weight ([fr]
+ * "Quantification et exactitude").
+ */
+uint64_t oracle_expert_code_bytes(int d, int f) {
+    return (uint64_t)3 * (uint64_t)OR_STAGES * (uint64_t)d * (uint64_t)f / OR_V;
+}

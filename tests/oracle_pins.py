@@ -1,0 +1,275 @@
+"""Pins of the CPU oracle to facts other than the oracle itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with
+a value fixed by the pages or by mathematics: the hand-worked example in
+``golden/hand_2expert.txt``, closed forms, invariants, library routines
+(numpy matmul, Python's stable sort) and brute force on tiny inputs.  The
+set is chosen so that a plausible slip anywhere in the oracle (a dropped
+stage or term, a wrong sign, index or tie order, a transposed operand)
+fails at least one of them; ``test_oracle_mutants.py`` plants such slips in
+a copy of the oracle and checks that they are caught.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------- fixtures
+
+def load_hand_example():
+    """Parse golden/hand_2expert.txt into arrays (d = f = 8, E = 2)."""
+    d = f = 8
+    E = 2
+    cb_one = np.zeros((3, 256, 8), np.float32)
+    codes = {m: np.zeros((E, 8, 3, 1), np.uint8) for m in range(3)}
+    Wr = np.zeros((E, d), np.float32)
+    h = None
+    expect = {}
+    with open(os.path.join(GOLDEN, "hand_2expert.txt")) as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            tok = line.split()
+            if tok[0] == "codebook":
+                s, c = int(tok[1]), int(tok[2])
+                cb_one[s, c] = [float(v) for v in tok[3:11]]
+            elif tok[0] == "code":
+                e, m, r = int(tok[1]), int(tok[2]), int(tok[3])
+                codes[m][e, r, :, 0] = [int(v) for v in tok[4:7]]
+            elif tok[0] == "router":
+                Wr[int(tok[1])] = [float(v) for v in tok[2:10]]
+            elif tok[0] == "hidden":
+                h = np.array([float(v) for v in tok[1:9]], np.float64)
+            elif tok[0] == "expect":
+                expect[tok[1]] = np.array([float(v) for v in tok[2:]], np.float64)
+    cbs = np.broadcast_to(cb_one, (E, 3, 3, 256, 8)).copy()
+    return dict(d=d, f=f, E=E, cbs=cbs, codes=(codes[0], codes[1], codes[2]), Wr=Wr, h=h,
+                expect=expect)
+
+
+def _rand_matrix(rng, n_out, n_in):
+    cb = (rng.standard_normal((3, 256, 8)) * np.array([0.02, 0.01, 0.005])[:, None, None]
+          ).astype(np.float32)
+    codes = rng.integers(0, 256, (n_out, 3, n_in // 8), dtype=np.uint8)
+    return cb, codes
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(np.asarray(a) - np.asarray(b)) / max(np.linalg.norm(b), 1e-300))
+
+
+# ---------------------------------------------------------------- pins
+
+def pin_hand_example_layer():
+    """Hand-worked 2-expert example: exact tie, k = 2 and k = 1, both product forms."""
+    ex = load_hand_example()
+    for use_lut in (True, False):
+        for k in (2, 1):
+            r = oracle.moe_layer(ex["h"][None], ex["Wr"], None, ex["cbs"], ex["codes"], k,
+                                 use_lut=use_lut)
+            np.testing.assert_allclose(r["logits"][0], ex["expect"]["logits"], rtol=0, atol=0)
+            np.testing.assert_array_equal(r["idx"][0], ex["expect"][f"idx_k{k}"].astype(np.int32))
+            np.testing.assert_allclose(r["gate"][0], ex["expect"][f"gate_k{k}"], rtol=0, atol=1e-15)
+            np.testing.assert_allclose(r["out"][0], ex["expect"][f"out_k{k}"], rtol=1e-14, atol=1e-14)
+
+
+def pin_hand_example_experts():
+    """Each expert of the hand example on its own matches the worked values."""
+    ex = load_hand_example()
+    for e in range(2):
+        for use_lut in (True, False):
+            y = oracle.expert_ffn(ex["cbs"][e], ex["codes"][0][e], ex["codes"][1][e],
+                                  ex["codes"][2][e], ex["h"], use_lut)
+            np.testing.assert_allclose(y, ex["expect"][f"y_expert{e}"], rtol=1e-14, atol=1e-14)
+
+
+def pin_dequant_stage_placement():
+    """Closed form: with stage-s codebook entry c equal to c * 256**s on component s
+    (zero elsewhere), W[r][8j+s] is code_s(r, j) * 256**s and every other weight is 0."""
+    rng = np.random.default_rng(1)
+    n_out, n_in = 24, 40
+    cb = np.zeros((3, 256, 8), np.float32)
+    for s in range(3):
+        cb[s, :, s] = np.arange(256, dtype=np.float32) * float(256 ** s)
+    codes = rng.integers(0, 256, (n_out, 3, n_in // 8), dtype=np.uint8)
+    W = oracle.dequant(cb, codes)
+    expect = np.zeros((n_out, n_in))
+    for r in range(n_out):
+        for j in range(n_in // 8):
+            for s in range(3):
+                expect[r, 8 * j + s] = float(codes[r, s, j]) * 256.0 ** s
+    np.testing.assert_array_equal(W, expect)
+
+
+def pin_dequant_residual_sum():
+    """Residual stages add: W from all three stages equals the sum of W from each stage alone."""
+    rng = np.random.default_rng(2)
+    cb, codes = _rand_matrix(rng, 16, 32)
+    parts = []
+    for s in range(3):
+        cb_s = np.zeros_like(cb)
+        cb_s[s] = cb[s]
+        parts.append(oracle.dequant(cb_s, codes))
+    np.testing.assert_allclose(oracle.dequant(cb, codes), parts[0] + parts[1] + parts[2],
+                               rtol=1e-15, atol=1e-18)
+
+
+def pin_matvec_dense_library():
+    """Dense product against numpy's matmul."""
+    rng = np.random.default_rng(3)
+    W = rng.standard_normal((37, 53))
+    x = rng.standard_normal(53)
+    np.testing.assert_allclose(oracle.matvec_dense(W, x), W @ x, rtol=1e-12, atol=1e-12)
+
+
+def pin_lut_equals_dequant():
+    """The pages' table form equals dequantise-then-multiply (numpy matmul) on tiny shapes."""
+    rng = np.random.default_rng(4)
+    for n_out, n_in in ((8, 8), (16, 16), (5, 64), (33, 256), (64, 8)):
+        cb, codes = _rand_matrix(rng, n_out, n_in)
+        x = rng.standard_normal(n_in)
+        W = oracle.dequant(cb, codes)
+        assert _rel(oracle.matvec_lut(cb, codes, x), W @ x) < 1e-12
+
+
+def pin_lut_unit_vectors():
+    """Brute force: the table form applied to unit vector e_i returns column i of W."""
+    rng = np.random.default_rng(5)
+    cb, codes = _rand_matrix(rng, 7, 24)
+    W = oracle.dequant(cb, codes)
+    for i in range(24):
+        x = np.zeros(24)
+        x[i] = 1.0
+        np.testing.assert_allclose(oracle.matvec_lut(cb, codes, x), W[:, i], rtol=1e-13, atol=1e-16)
+
+
+def pin_router_library():
+    """Router logits against numpy: W_r h + b, with and without bias."""
+    rng = np.random.default_rng(6)
+    Wr = rng.standard_normal((11, 40)).astype(np.float32)
+    b = rng.standard_normal(11).astype(np.float32)
+    h = rng.standard_normal(40)
+    np.testing.assert_allclose(oracle.router(Wr, None, h), Wr.astype(np.float64) @ h, rtol=1e-12)
+    np.testing.assert_allclose(oracle.router(Wr, b, h), Wr.astype(np.float64) @ h + b, rtol=1e-12)
+
+
+def pin_topk_against_sort():
+    """Top-k against Python's stable sort on key (-logit, index), ties and +-0 included."""
+    rng = np.random.default_rng(7)
+    cases = [rng.standard_normal(8), rng.integers(-2, 3, 16).astype(np.float64),
+             np.array([0.0, -0.0, 0.0, -0.0, 1.0, 1.0, -1.0]), np.ones(5),
+             rng.standard_normal(64)]
+    for l in cases:
+        order = sorted(range(len(l)), key=lambda e: (-l[e], e))
+        for k in range(1, len(l) + 1):
+            idx, _ = oracle.topk_softmax(l, k)
+            assert idx.tolist() == order[:k], (l, k)
+
+
+def pin_topk_exhaustive_small():
+    """Brute force over all 2-subsets of 8 experts: the chosen pair is the one whose
+    smaller logit beats every logit outside it."""
+    rng = np.random.default_rng(8)
+    for _ in range(20):
+        l = rng.standard_normal(8)
+        best = [S for S in itertools.combinations(range(8), 2)
+                if min(l[list(S)]) > max(l[[e for e in range(8) if e not in S]])]
+        assert len(best) == 1
+        idx, _ = oracle.topk_softmax(l, 2)
+        assert sorted(idx.tolist()) == list(best[0])
+        assert l[idx[0]] >= l[idx[1]]
+
+
+def pin_gate_invariants():
+    """Gates sum to 1; k = 1 gives exactly 1; equal logits give 1/k; ratios are exp of gaps."""
+    rng = np.random.default_rng(9)
+    l = rng.standard_normal(32) * 3
+    idx, g = oracle.topk_softmax(l, 6)
+    assert abs(g.sum() - 1.0) < 1e-15
+    for a in range(6):
+        for b in range(6):
+            assert abs(g[a] / g[b] - math.exp(l[idx[a]] - l[idx[b]])) < 1e-12 * max(1, g[a] / g[b])
+    _, g1 = oracle.topk_softmax(l, 1)
+    assert g1[0] == 1.0
+    _, geq = oracle.topk_softmax(np.full(9, 0.25), 4)
+    np.testing.assert_allclose(geq, np.full(4, 0.25), rtol=0, atol=1e-16)
+    assert np.all(np.diff(g) <= 0)
+
+
+def pin_silu_closed_forms():
+    """silu(0) = 0; silu(x) - silu(-x) = x; silu(ln 3) = 0.75 ln 3; silu(x) -> x for large x."""
+    assert oracle.silu(0.0) == 0.0
+    for x in (0.1, 0.7, 2.5, 9.0):
+        assert abs(oracle.silu(x) - oracle.silu(-x) - x) < 1e-14 * max(1, x)
+    assert abs(oracle.silu(math.log(3.0)) - 0.75 * math.log(3.0)) < 1e-15
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12
+
+
+def pin_swiglu_roles():
+    """Gate and up play different roles: with U = 0 the output is 0 whatever G is, and
+    with the gate matrix zero the output is 0 too (silu(0) = 0)."""
+    rng = np.random.default_rng(10)
+    d, f = 16, 8
+    cb = np.stack([_rand_matrix(rng, 1, 8)[0] for _ in range(3)])
+    gc = rng.integers(0, 256, (f, 3, d // 8), dtype=np.uint8)
+    uc = rng.integers(0, 256, (f, 3, d // 8), dtype=np.uint8)
+    dc = rng.integers(0, 256, (d, 3, f // 8), dtype=np.uint8)
+    x = rng.standard_normal(d)
+    for zero_mat in (0, 1):
+        cbz = cb.copy()
+        cbz[zero_mat] = 0
+        assert np.all(oracle.expert_ffn(cbz, gc, uc, dc, x) == 0.0)
+    # and the full product against a numpy composition of the dequantised matrices
+    G = oracle.dequant(cb[0], gc)
+    U = oracle.dequant(cb[1], uc)
+    D = oracle.dequant(cb[2], dc)
+    zg = G @ x
+    a = zg / (1 + np.exp(-zg)) * (U @ x)
+    assert _rel(oracle.expert_ffn(cb, gc, uc, dc, x), D @ a) < 1e-12
+
+
+def pin_down_linearity():
+    """Doubling the down codebooks doubles the expert output exactly."""
+    rng = np.random.default_rng(11)
+    d, f = 24, 16
+    cb = np.stack([_rand_matrix(rng, 1, 8)[0] for _ in range(3)])
+    gc = rng.integers(0, 256, (f, 3, d // 8), dtype=np.uint8)
+    uc = rng.integers(0, 256, (f, 3, d // 8), dtype=np.uint8)
+    dc = rng.integers(0, 256, (d, 3, f // 8), dtype=np.uint8)
+    x = rng.standard_normal(d)
+    cb2 = cb.copy()
+    cb2[2] *= 2
+    np.testing.assert_array_equal(oracle.expert_ffn(cb2, gc, uc, dc, x),
+                                  2 * oracle.expert_ffn(cb, gc, uc, dc, x))
+
+
+def pin_combine():
+    """Combine: k = 1 with gate 1 returns y; the base is added; gates weight the outputs."""
+    rng = np.random.default_rng(12)
+    ys = rng.standard_normal((3, 10))
+    base = rng.standard_normal(10)
+    np.testing.assert_array_equal(oracle.combine([1.0], ys[:1]), ys[0])
+    np.testing.assert_allclose(oracle.combine([0.2, 0.3, 0.5], ys, base),
+                               base + 0.2 * ys[0] + 0.3 * ys[1] + 0.5 * ys[2], rtol=1e-14)
+
+
+def pin_code_bytes_match_pages():
+    """Per-token expert bytes: 16 experts x 92 layers of 3-bit codes at K3's shapes
+    (d = 7168, f = 1536) come to 16.98 GiB, the pages' "17.0 GB" per token; one expert's
+    codes fill exactly 3024 pages of 4 KiB."""
+    b = oracle.expert_code_bytes(7168, 1536)
+    assert b == 12_386_304
+    assert b % 4096 == 0 and b // 4096 == 3024
+    assert abs(16 * 92 * b / 2 ** 30 - 17.0) < 0.05
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
