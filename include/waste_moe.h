@@ -1,0 +1,256 @@
+/*
+ * waste_moe.h -- C ABI of the routed-expert RVQ MoE step for NVIDIA GB300 (sm_103a).
+ *
+ * One handle serves one MoE layer.  Per token the layer
+ *   1. computes router logits  l = W_r h (+ b),
+ *   2. keeps the top-k experts (logit descending, lowest index first on equal
+ *      logits) and normalises their gates with a softmax over the k selected
+ *      logits,
+ *   3. applies each selected expert's gate/up/down matrices straight from
+ *      their residual-vector-quantised codes (3 stages, 256-entry codebooks of
+ *      8-weight vectors, one uint8 code per vector and stage = 3.00 bits per
+ *      weight), a = silu(G h) * (U h), y = D a, and
+ *   4. adds the gate-weighted sum of the k expert outputs into the output.
+ * A lookahead call runs the NEXT layer's router on the current hidden state
+ * and prefetches the experts it predicts into L2; it never changes outputs.
+ *
+ * Sources (web pages about the WASTE engine; page titles and sections):
+ *   "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s"
+ *     - "Quantification et exactitude": 3-stage RVQ, 256 entries, 8-dim
+ *       vectors, 3.00 bits/weight; the matrix is never rebuilt: a table of
+ *       partial dot products is built and each row costs 3 lookups + 2 adds.
+ *     - "Architecture de streaming depuis le disque": one record per expert,
+ *       aligned to 4 KiB, gate/up/down contiguous so one read fetches an
+ *       expert; magic, expert ID and offset range are always checked;
+ *       codebooks carry no checksum.
+ *     - "Lecture anticipée et prédiction du routeur": 16 expert IDs per token
+ *       and layer; the resident next-layer router runs on the current hidden
+ *       state to prefetch 6 experts; the real router still decides, so the
+ *       output is exact; total bytes read do not change; WASTE_LOOKAHEAD=0
+ *       turns it off.
+ *   "Chạy Kimi K3 ở 0.50 tok/s với 29GB RAM" -- the same text in Vietnamese.
+ * Readings taken where the pages are silent: SwiGLU for how gate/up/down
+ * combine, softmax over the selected logits, lowest-index tie-break,
+ * codebooks per (expert, matrix) in fp32, the residual update h + combine.
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* are CUDA device pointers; the caller owns every
+ *     buffer.  A handle BORROWS the router, records and codebooks: they must
+ *     outlive it.  It owns only the workspace that create allocates and
+ *     destroy frees.
+ *   - Calls that take a stream only enqueue work on it and return; none
+ *     synchronises the device (create and waste_moe_pack_records/stats do
+ *     short synchronous copies, see each).  route/forward/prefetch allocate
+ *     nothing and may be captured in a CUDA graph.
+ *   - Return value: WASTE_OK (0) or a negative waste_status; the message of
+ *     the last failure on the calling thread is waste_moe_last_error().
+ *     Arguments are checked on the host before anything is launched; a
+ *     failed check launches nothing.  Expert indices passed to forward are
+ *     checked again on the device: an index outside [0, E) contributes zero
+ *     and sets a sticky device error reported by waste_moe_stats as
+ *     WASTE_EINVAL.
+ *   - A handle is not safe for concurrent use from two host threads.
+ */
+#ifndef WASTE_MOE_H
+#define WASTE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WASTE_MOE_ABI_VERSION 1u
+
+/* CUDA stream handle; ABI-identical to cudaStream_t. NULL = legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *waste_stream_t;
+
+typedef struct waste_moe waste_moe; /* opaque; one handle per MoE layer */
+
+typedef enum {
+    WASTE_OK = 0,
+    WASTE_EINVAL = -1,   /* bad argument (null pointer, size out of range, bad config) */
+    WASTE_ENOMEM = -2,   /* device workspace could not be allocated */
+    WASTE_ECUDA = -3,    /* a CUDA call or launch failed */
+    WASTE_ELAYOUT = -4,  /* record header: bad magic / version / expert id / offset / alignment */
+    WASTE_ECRC = -5,     /* record payload crc32 mismatch (WASTE_FLAG_VERIFY_CRC) */
+    WASTE_ETIMEOUT = -6, /* a bounded device wait gave up */
+    WASTE_ENOTIMPL = -7  /* combination not supported by this build */
+} waste_status;
+
+enum { WASTE_ACT_F32 = 0, WASTE_ACT_BF16 = 1 };
+
+enum {
+    WASTE_FLAG_VERIFY_CRC = 1u << 0,    /* create: check every record's payload crc32 */
+    WASTE_FLAG_FORCE_GEMV = 1u << 2,    /* forward: table-lookup path for every slot */
+    WASTE_FLAG_FORCE_MMA = 1u << 3,     /* forward: grouped dequant + tensor-core path when T > 1 */
+    WASTE_FLAG_K2_RECONSTRUCT = 1u << 4 /* forward: rebuild each 8-weight vector from the
+                                           3 codebook entries in registers instead of the
+                                           partial-dot-product table */
+};
+
+/* Layer configuration.  d % 8 == 0, f % 8 == 0, 1 <= top_k <= n_experts <= 4096,
+ * top_k <= 32, 1 <= max_tokens.  lookahead = experts predicted per token by
+ * waste_moe_prefetch when its n_prefetch is negative (the pages use 6; 0 = off);
+ * the environment variable WASTE_LOOKAHEAD, when set, overrides it at create. */
+typedef struct {
+    uint32_t abi_version; /* must equal WASTE_MOE_ABI_VERSION */
+    int32_t d;            /* hidden size */
+    int32_t f;            /* expert FFN width */
+    int32_t n_experts;    /* E */
+    int32_t top_k;        /* k */
+    int32_t act_dtype;    /* WASTE_ACT_F32 or WASTE_ACT_BF16: dtype of the hidden states h */
+    int32_t max_tokens;   /* largest T passed to route/forward/prefetch (sizes the workspace) */
+    int32_t lookahead;    /* default prefetch count */
+    uint32_t flags;       /* WASTE_FLAG_* */
+    int32_t layer;        /* layer id expected in the record headers; -1 = do not check */
+} waste_moe_config;
+
+/* ---- record format -------------------------------------------------------------------
+ * The experts of a layer form a bank of records of equal stride (a multiple of
+ * 4096 B), record e at byte e * stride of the bank, the bank 4096-aligned.  A record
+ * is a 4096 B header followed by three sections (gate, up, down), each starting on a
+ * 4096 B boundary, holding that matrix's codes in the tiled order below.
+ *
+ * Code tiling of one matrix with n_out rows and n_in = 8 nv inputs (vector j of row r
+ * covers inputs 8j .. 8j+7; codes code[r][s][j], s = stage):
+ *   segments  sigma = 0 .. ceil(nv/32)-1  (32 vectors each),
+ *   row groups g    = 0 .. ceil(n_out/16)-1 (16 rows each),
+ *   16-byte chunk (sigma, g, s, jj) at byte ((sigma*G + g)*3 + s)*512 + jj*16,
+ *   byte q of that chunk = code[16g + ((jj ^ q) & 15)][s][32 sigma + jj]
+ *   (0 where the row or vector is past the end).
+ * The xor spreads each lane's 16 rows so the table-lookup kernel can reduce
+ * across lanes without selects; the order is a fixed part of the format. */
+#define WASTE_RECORD_MAGIC 0x454F4D57u /* bytes "WMOE" */
+#define WASTE_RECORD_VERSION 1u
+#define WASTE_RECORD_ALIGN 4096u
+#define WASTE_LAYOUT_TILED16X 1u
+
+typedef struct {
+    uint32_t magic;              /* WASTE_RECORD_MAGIC */
+    uint32_t version;            /* WASTE_RECORD_VERSION */
+    int32_t layer;               /* layer id written by pack */
+    int32_t expert_id;           /* must equal the record's index in the bank */
+    int32_t d, f;                /* shapes the codes were written for */
+    int32_t n_stages;            /* 3 */
+    int32_t codebook_size;       /* 256 */
+    int32_t vec;                 /* 8 */
+    uint32_t layout_id;          /* WASTE_LAYOUT_TILED16X */
+    uint64_t section_offset[3];  /* gate, up, down: byte offset from the record start */
+    uint64_t section_bytes[3];   /* bytes of each section (multiple of 4096) */
+    uint64_t record_bytes;       /* stride the record was written for */
+    uint32_t payload_crc32;      /* crc32 (IEEE, reflected 0xEDB88320) of the three
+                                    sections in order; 0 = not computed */
+    uint32_t reserved;
+} waste_record_header;
+
+/* Layout of one record for cfg: the minimal stride and the three sections.
+ * Pure host arithmetic; any output pointer may be NULL. */
+int waste_moe_record_layout(const waste_moe_config *cfg, size_t *record_stride,
+                            size_t section_offset[3], size_t section_bytes[3]);
+
+/* Write records [expert_begin, expert_begin + n_experts) of a bank from codes in
+ * the logical layout (the converter's last step):
+ *   d_gate_codes, d_up_codes: [n_experts][f][3][d/8] uint8,
+ *   d_down_codes:             [n_experts][d][3][f/8] uint8  (device, read only).
+ * d_records is the bank base (4096-aligned); record_stride as above.  Headers
+ * carry `layer`; with compute_crc != 0 the payload crc32 is computed on the device
+ * and stored (one small synchronous copy per record).  Enqueued on stream. */
+int waste_moe_pack_records(const waste_moe_config *cfg, int32_t layer, int32_t expert_begin,
+                           int32_t n_experts, const uint8_t *d_gate_codes,
+                           const uint8_t *d_up_codes, const uint8_t *d_down_codes,
+                           uint8_t *d_records, size_t record_stride, int32_t compute_crc,
+                           waste_stream_t stream);
+
+/* Create a handle for one layer.
+ *   d_router_w    [E][d] fp32 router weights (borrowed)
+ *   d_router_bias [E] fp32 or NULL (borrowed)
+ *   d_records     bank of E records, 4096-aligned base, stride record_stride (borrowed)
+ *   d_codebooks   [E][3 matrices: gate, up, down][3 stages][256][8] fp32 (borrowed)
+ * Checks every record header (magic, version, expert id, layer, shapes, section
+ * offsets inside the stride and 4096-aligned, sizes) with one synchronous copy of
+ * the headers, and the payload crc32 with WASTE_FLAG_VERIFY_CRC.  On any failure
+ * returns < 0 and sets *out = NULL (the layer is refused rather than run on
+ * suspect weights).  Allocates the workspace (sized by max_tokens). */
+int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
+                     const float *d_router_bias, const uint8_t *d_records,
+                     size_t record_stride, const float *d_codebooks, waste_moe **out);
+
+/* Route T tokens (0 <= T <= max_tokens; T == 0 does nothing).
+ *   d_h      [T][d] hidden states, fp32 or bf16 per act_dtype
+ *   d_idx    [T][k] int32 out: selected experts in rank order
+ *   d_gate   [T][k] fp32 out: softmax of the selected logits
+ *   d_logits [T][E] fp32 out, or NULL (then kept in the workspace)
+ * If waste_moe_prefetch ran for this layer (ordered before this call by the
+ * caller), the number of predicted experts among the selected ones is added to
+ * the prediction_hits statistic. */
+int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
+                    float *d_logits, waste_stream_t stream);
+
+/* Apply the selected experts and combine (0 <= T <= max_tokens).
+ *   d_h      [T][d] hidden states (fp32 or bf16 per act_dtype)
+ *   d_idx    [T][k] int32, d_gate [T][k] fp32 (usually route's outputs)
+ *   d_out    [T][d] fp32
+ *   mode 0: out  = sum_i gate_i * y_i
+ *   mode 1: out += sum_i gate_i * y_i   (residual already in out)
+ *   mode 2: out  = h + sum_i gate_i * y_i (fp32 h only; out may equal h)
+ * Deterministic: the same inputs give bit-identical outputs (fixed summation
+ * order, no floating-point atomics). */
+int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d_idx,
+                      const float *d_gate, float *d_out, int32_t mode, waste_stream_t stream);
+
+/* Lookahead: run next_layer's router on the current hidden states d_h [T][d],
+ * take its top n_prefetch experts per token (n_prefetch < 0: the handle's
+ * lookahead; 0: nothing) and prefetch their records into L2.  Writes no
+ * user-visible buffer and never changes any output.  The caller orders it after
+ * d_h is ready and before next_layer's route (events), and must not overwrite
+ * d_h until it has run. */
+int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_t n_prefetch,
+                       waste_stream_t side);
+
+/* Free the workspace and the handle (NULL is ignored).  Synchronises the device. */
+void waste_moe_destroy(waste_moe *h);
+
+typedef struct {
+    uint64_t demand_code_bytes;     /* code bytes the expert kernels read (algorithmic) */
+    uint64_t codebook_bytes;        /* codebook bytes used by the expert kernels */
+    uint64_t router_bytes;          /* router weight bytes read by route */
+    uint64_t prefetch_issued_bytes; /* record bytes named in L2 prefetches */
+    uint64_t prefetch_experts;      /* (token, expert) prefetches issued */
+    uint64_t prediction_hits;       /* routed experts that had been predicted */
+    uint64_t routed_slots;          /* (token, expert) slots routed */
+    uint64_t forward_slots;         /* (token, expert) slots applied by forward */
+} waste_moe_stats_t;
+
+/* Copy the handle's counters (one synchronous copy on the legacy stream after a
+ * device synchronise).  Returns WASTE_EINVAL if a kernel saw an expert index out
+ * of range since create, else WASTE_OK. */
+int waste_moe_stats(const waste_moe *h, waste_moe_stats_t *out);
+
+/* Zero the counters (synchronous). */
+int waste_moe_reset_stats(waste_moe *h);
+
+/* Per-kernel timing of the following route/forward calls with CUDA events recorded
+ * on the call's stream (enable != 0 creates the events, 0 drops them; do not enable
+ * while a stream is being captured into a graph). */
+int waste_moe_set_profiling(waste_moe *h, int32_t enable);
+
+/* Milliseconds of each kernel of the last profiled route and forward:
+ * ms[0] router, ms[1] top-k, ms[2] gate/up, ms[3] down, ms[4] combine
+ * (-1 where no call was profiled).  Waits for the events. */
+int waste_moe_read_profile(const waste_moe *h, float ms[5]);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char *waste_moe_last_error(void);
+
+/* Top-k + softmax of given logits (the routing step alone; used by tests to
+ * drive exact ties).  d_logits [T][E] fp32, d_idx/d_gate [T][k]. */
+int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int32_t k,
+                               int32_t *d_idx, float *d_gate, waste_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WASTE_MOE_H */

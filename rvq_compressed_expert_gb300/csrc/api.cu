@@ -1,0 +1,455 @@
+// Host side of the C ABI declared in waste_moe.h: argument and record checks,
+// workspace, statistics, error strings, and the launch sequence of each call.
+#include "common.cuh"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace wm;
+
+struct waste_moe {
+    waste_moe_config cfg;
+    LayerView L;
+    Workspace W;
+    int num_sms;
+    int lookahead;
+    int max_slots;
+    int pred_P; // experts per token of the last prefetch into this layer
+    bool profiling;
+    Timing route_tm, fwd_tm;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int ok() {
+    g_err.clear();
+    return WASTE_OK;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(WASTE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_config(const waste_moe_config *c) {
+    if (!c) return fail(WASTE_EINVAL, "config is NULL");
+    if (c->abi_version != WASTE_MOE_ABI_VERSION)
+        return fail(WASTE_EINVAL, "abi_version %u, library speaks %u", c->abi_version, WASTE_MOE_ABI_VERSION);
+    if (c->d <= 0 || c->d % kVec) return fail(WASTE_EINVAL, "d = %d must be a positive multiple of 8", c->d);
+    if (c->f <= 0 || c->f % kVec) return fail(WASTE_EINVAL, "f = %d must be a positive multiple of 8", c->f);
+    if (c->n_experts < 1 || c->n_experts > kMaxExperts)
+        return fail(WASTE_EINVAL, "n_experts = %d outside [1, %d]", c->n_experts, kMaxExperts);
+    if (c->top_k < 1 || c->top_k > c->n_experts || c->top_k > kMaxTopK)
+        return fail(WASTE_EINVAL, "top_k = %d outside [1, min(n_experts, %d)]", c->top_k, kMaxTopK);
+    if (c->act_dtype != WASTE_ACT_F32 && c->act_dtype != WASTE_ACT_BF16)
+        return fail(WASTE_EINVAL, "act_dtype = %d", c->act_dtype);
+    if (c->max_tokens < 1) return fail(WASTE_EINVAL, "max_tokens = %d", c->max_tokens);
+    if (c->lookahead < 0 || c->lookahead > kMaxTopK || c->lookahead > c->n_experts)
+        return fail(WASTE_EINVAL, "lookahead = %d outside [0, min(n_experts, %d)]", c->lookahead, kMaxTopK);
+    const uint32_t known = WASTE_FLAG_VERIFY_CRC | WASTE_FLAG_FORCE_GEMV | WASTE_FLAG_FORCE_MMA |
+                           WASTE_FLAG_K2_RECONSTRUCT;
+    if (c->flags & ~known) return fail(WASTE_EINVAL, "unknown flags 0x%x", c->flags & ~known);
+    return WASTE_OK;
+}
+
+void layout(const waste_moe_config *c, size_t *stride, size_t off[3], size_t bytes[3]) {
+    const MatGeom gu = mat_geom(c->f, c->d), dn = mat_geom(c->d, c->f);
+    bytes[0] = bytes[1] = round_up(gu.chunk_bytes(), WASTE_RECORD_ALIGN);
+    bytes[2] = round_up(dn.chunk_bytes(), WASTE_RECORD_ALIGN);
+    off[0] = WASTE_RECORD_ALIGN;
+    off[1] = off[0] + bytes[0];
+    off[2] = off[1] + bytes[1];
+    *stride = off[2] + bytes[2];
+}
+
+} // namespace
+
+namespace wm {
+int device_sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+} // namespace wm
+
+extern "C" {
+
+const char *waste_moe_last_error(void) { return g_err.c_str(); }
+
+int waste_moe_record_layout(const waste_moe_config *cfg, size_t *record_stride,
+                            size_t section_offset[3], size_t section_bytes[3]) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    size_t st, off[3], by[3];
+    layout(cfg, &st, off, by);
+    if (record_stride) *record_stride = st;
+    for (int m = 0; m < 3; ++m) {
+        if (section_offset) section_offset[m] = off[m];
+        if (section_bytes) section_bytes[m] = by[m];
+    }
+    return ok();
+}
+
+int waste_moe_pack_records(const waste_moe_config *cfg, int32_t layer, int32_t expert_begin,
+                           int32_t n_experts, const uint8_t *d_gate_codes,
+                           const uint8_t *d_up_codes, const uint8_t *d_down_codes,
+                           uint8_t *d_records, size_t record_stride, int32_t compute_crc,
+                           waste_stream_t stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (n_experts < 0 || expert_begin < 0 || expert_begin + n_experts > cfg->n_experts)
+        return fail(WASTE_EINVAL, "experts [%d, %d) outside [0, %d)", expert_begin,
+                    expert_begin + n_experts, cfg->n_experts);
+    if (n_experts == 0) return ok();
+    if (!d_gate_codes || !d_up_codes || !d_down_codes || !d_records)
+        return fail(WASTE_EINVAL, "NULL code or record pointer");
+    if (!aligned(d_records, WASTE_RECORD_ALIGN))
+        return fail(WASTE_ELAYOUT, "record bank base %p is not 4096-aligned", (const void *)d_records);
+    size_t st, off[3], by[3];
+    layout(cfg, &st, off, by);
+    if (record_stride < st || record_stride % WASTE_RECORD_ALIGN)
+        return fail(WASTE_ELAYOUT, "record stride %zu: needs a multiple of 4096 >= %zu", record_stride, st);
+    if (compute_crc) return fail(WASTE_ENOTIMPL, "payload crc32 is not computed by this build");
+    waste_record_header hdr;
+    memset(&hdr, 0, sizeof hdr);
+    hdr.magic = WASTE_RECORD_MAGIC;
+    hdr.version = WASTE_RECORD_VERSION;
+    hdr.layer = layer;
+    hdr.d = cfg->d;
+    hdr.f = cfg->f;
+    hdr.n_stages = kStages;
+    hdr.codebook_size = kCodes;
+    hdr.vec = kVec;
+    hdr.layout_id = WASTE_LAYOUT_TILED16X;
+    for (int m = 0; m < 3; ++m) {
+        hdr.section_offset[m] = off[m];
+        hdr.section_bytes[m] = by[m];
+    }
+    hdr.record_bytes = record_stride;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *first = d_records + (size_t)expert_begin * record_stride;
+    cudaError_t e = launch_headers(first, record_stride, n_experts, hdr, expert_begin, s);
+    if (e != cudaSuccess) return cuda_fail(e, "header kernel");
+    e = launch_pack(mat_geom(cfg->f, cfg->d), mat_geom(cfg->d, cfg->f), n_experts, d_gate_codes,
+                    d_up_codes, d_down_codes, first, record_stride, off, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pack kernel");
+    return ok();
+}
+
+int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
+                     const float *d_router_bias, const uint8_t *d_records, size_t record_stride,
+                     const float *d_codebooks, waste_moe **out) {
+    if (!out) return fail(WASTE_EINVAL, "out is NULL");
+    *out = nullptr;
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (!d_router_w || !d_records || !d_codebooks)
+        return fail(WASTE_EINVAL, "NULL router, record or codebook pointer");
+    if (!aligned(d_router_w, 16) || !aligned(d_codebooks, 16) ||
+        (d_router_bias && !aligned(d_router_bias, 4)))
+        return fail(WASTE_EINVAL, "router / codebook pointers must be 16-byte aligned");
+    if (!aligned(d_records, WASTE_RECORD_ALIGN))
+        return fail(WASTE_ELAYOUT, "record bank base %p is not 4096-aligned", (const void *)d_records);
+    size_t st, off[3], by[3];
+    layout(cfg, &st, off, by);
+    if (record_stride < st || record_stride % WASTE_RECORD_ALIGN)
+        return fail(WASTE_ELAYOUT, "record stride %zu: needs a multiple of 4096 >= %zu", record_stride, st);
+    if (cfg->flags & WASTE_FLAG_VERIFY_CRC)
+        return fail(WASTE_ENOTIMPL, "payload crc32 verification is not in this build");
+
+    // ---- record headers: one strided copy, then every field checked
+    const int E = cfg->n_experts;
+    std::vector<waste_record_header> hdrs((size_t)E);
+    cudaError_t ce = cudaMemcpy2D(hdrs.data(), sizeof(waste_record_header), d_records, record_stride,
+                                  sizeof(waste_record_header), (size_t)E, cudaMemcpyDeviceToHost);
+    if (ce != cudaSuccess) return cuda_fail(ce, "copying record headers");
+    for (int e = 0; e < E; ++e) {
+        const waste_record_header &h = hdrs[(size_t)e];
+        if (h.magic != WASTE_RECORD_MAGIC)
+            return fail(WASTE_ELAYOUT, "record %d: bad magic 0x%08x", e, h.magic);
+        if (h.version != WASTE_RECORD_VERSION)
+            return fail(WASTE_ELAYOUT, "record %d: version %u", e, h.version);
+        if (h.expert_id != e) return fail(WASTE_ELAYOUT, "record %d holds expert id %d", e, h.expert_id);
+        if (cfg->layer >= 0 && h.layer != cfg->layer)
+            return fail(WASTE_ELAYOUT, "record %d: layer %d, expected %d", e, h.layer, cfg->layer);
+        if (h.d != cfg->d || h.f != cfg->f || h.n_stages != kStages || h.codebook_size != kCodes ||
+            h.vec != kVec)
+            return fail(WASTE_ELAYOUT, "record %d: shapes (d %d, f %d, %d x %d x %d) do not match", e, h.d,
+                        h.f, h.n_stages, h.codebook_size, h.vec);
+        if (h.layout_id != WASTE_LAYOUT_TILED16X)
+            return fail(WASTE_ELAYOUT, "record %d: unknown code layout %u", e, h.layout_id);
+        for (int m = 0; m < 3; ++m) {
+            if (h.section_offset[m] % WASTE_RECORD_ALIGN || h.section_offset[m] < WASTE_RECORD_ALIGN ||
+                h.section_bytes[m] < by[m] || h.section_offset[m] + h.section_bytes[m] > record_stride ||
+                h.section_offset[m] != off[m])
+                return fail(WASTE_ELAYOUT, "record %d: section %d at %llu (+%llu) outside the record", e, m,
+                            (unsigned long long)h.section_offset[m], (unsigned long long)h.section_bytes[m]);
+        }
+    }
+
+    waste_moe *H = new (std::nothrow) waste_moe();
+    if (!H) return fail(WASTE_ENOMEM, "host allocation");
+    H->cfg = *cfg;
+    H->num_sms = device_sm_count();
+    H->lookahead = cfg->lookahead;
+    if (const char *env = getenv("WASTE_LOOKAHEAD")) {
+        const int v = atoi(env);
+        if (v >= 0 && v <= kMaxTopK && v <= E) H->lookahead = v;
+    }
+    H->max_slots = cfg->max_tokens * cfg->top_k;
+    H->pred_P = 0;
+    H->profiling = false;
+    LayerView &L = H->L;
+    L.router_w = d_router_w;
+    L.router_b = d_router_bias;
+    L.records = d_records;
+    L.stride = record_stride;
+    for (int m = 0; m < 3; ++m) L.sec_off[m] = off[m];
+    L.codebooks = d_codebooks;
+    L.d = cfg->d;
+    L.f = cfg->f;
+    L.E = E;
+    L.k = cfg->top_k;
+    L.act_bf16 = cfg->act_dtype == WASTE_ACT_BF16;
+    L.gu = mat_geom(cfg->f, cfg->d);
+    L.dn = mat_geom(cfg->d, cfg->f);
+
+    // ---- workspace, one allocation carved into 256-byte aligned pieces
+    const size_t T = (size_t)cfg->max_tokens, S = (size_t)H->max_slots;
+    const size_t npair = (size_t)(L.dn.nseg + 1) / 2;
+    size_t sizes[] = {
+        T * E * 4,                                  // logits
+        T * E * 4,                                  // pred_logits
+        T * kMaxTopK * 4,                           // pred_idx
+        T * 4,                                      // pred_count
+        T * kMaxTopK * 4,                           // pred_gate_sel
+        S * (size_t)L.gu.nseg * 2 * (size_t)L.f * 4, // part_gu
+        S * npair * (size_t)L.d * 4,                // part_dn
+        kStatCount * 8,                             // stats
+        4,                                          // err
+    };
+    const int n_parts = (int)(sizeof sizes / sizeof sizes[0]);
+    size_t offs[16], total = 0;
+    for (int i = 0; i < n_parts; ++i) {
+        offs[i] = total;
+        total += round_up(sizes[i], 256);
+    }
+    void *base = nullptr;
+    ce = cudaMalloc(&base, total);
+    if (ce != cudaSuccess) {
+        cudaGetLastError();
+        delete H;
+        return fail(WASTE_ENOMEM, "workspace of %zu bytes: %s", total, cudaGetErrorString(ce));
+    }
+    char *b = static_cast<char *>(base);
+    Workspace &W = H->W;
+    W.base = base;
+    W.bytes = total;
+    W.logits = reinterpret_cast<float *>(b + offs[0]);
+    W.pred_logits = reinterpret_cast<float *>(b + offs[1]);
+    W.pred_idx = reinterpret_cast<int32_t *>(b + offs[2]);
+    W.pred_count = reinterpret_cast<int32_t *>(b + offs[3]);
+    W.pred_gate_sel = reinterpret_cast<float *>(b + offs[4]);
+    W.pred_idx_sel = W.pred_idx;
+    W.part_gu = reinterpret_cast<float *>(b + offs[5]);
+    W.part_dn = reinterpret_cast<float *>(b + offs[6]);
+    W.stats = reinterpret_cast<unsigned long long *>(b + offs[7]);
+    W.err = reinterpret_cast<uint32_t *>(b + offs[8]);
+    ce = cudaMemset(base, 0, total);
+    if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
+    if (ce != cudaSuccess) {
+        cudaFree(base);
+        delete H;
+        return cuda_fail(ce, "clearing the workspace");
+    }
+    *out = H;
+    return ok();
+}
+
+static void drop_events(waste_moe *h) {
+    if (!h->profiling) return;
+    for (int i = 0; i < 8; ++i) {
+        cudaEventDestroy(h->route_tm.ev[i]);
+        cudaEventDestroy(h->fwd_tm.ev[i]);
+    }
+    h->profiling = false;
+}
+
+void waste_moe_destroy(waste_moe *h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    drop_events(h);
+    cudaFree(h->W.base);
+    delete h;
+}
+
+int waste_moe_set_profiling(waste_moe *h, int32_t enable) {
+    if (!h) return fail(WASTE_EINVAL, "NULL handle");
+    if (!enable) {
+        cudaDeviceSynchronize();
+        drop_events(h);
+        return ok();
+    }
+    if (h->profiling) return ok();
+    for (int i = 0; i < 8; ++i) {
+        cudaError_t e = cudaEventCreate(&h->route_tm.ev[i]);
+        if (e == cudaSuccess) e = cudaEventCreate(&h->fwd_tm.ev[i]);
+        if (e != cudaSuccess) return cuda_fail(e, "creating profiling events");
+    }
+    h->route_tm.n = h->fwd_tm.n = 0;
+    h->profiling = true;
+    return ok();
+}
+
+int waste_moe_read_profile(const waste_moe *h, float ms[5]) {
+    if (!h || !ms) return fail(WASTE_EINVAL, "NULL handle or output");
+    if (!h->profiling) return fail(WASTE_EINVAL, "profiling is not enabled");
+    for (int i = 0; i < 5; ++i) ms[i] = -1.f;
+    const Timing *t[2] = {&h->route_tm, &h->fwd_tm};
+    int o = 0;
+    for (int j = 0; j < 2; ++j) {
+        const int n = j == 0 ? 3 : 4;
+        if (t[j]->n == n) {
+            cudaError_t e = cudaEventSynchronize(t[j]->ev[n - 1]);
+            if (e != cudaSuccess) return cuda_fail(e, "waiting for profiling events");
+            for (int i = 0; i + 1 < n; ++i) {
+                e = cudaEventElapsedTime(&ms[o + i], t[j]->ev[i], t[j]->ev[i + 1]);
+                if (e != cudaSuccess) return cuda_fail(e, "reading profiling events");
+            }
+        }
+        o += n - 1;
+    }
+    return ok();
+}
+
+static int check_tokens(const waste_moe *h, int32_t T, const void *d_h) {
+    if (!h) return fail(WASTE_EINVAL, "handle is NULL");
+    if (T < 0 || T > h->cfg.max_tokens)
+        return fail(WASTE_EINVAL, "T = %d outside [0, max_tokens = %d]", T, h->cfg.max_tokens);
+    if (T > 0 && !d_h) return fail(WASTE_EINVAL, "hidden states pointer is NULL");
+    if (d_h && !aligned(d_h, 16)) return fail(WASTE_EINVAL, "hidden states must be 16-byte aligned");
+    return WASTE_OK;
+}
+
+int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
+                    float *d_logits, waste_stream_t stream) {
+    int rc = check_tokens(h, T, d_h);
+    if (rc) return rc;
+    if (T == 0) return ok();
+    if (!d_idx || !d_gate) return fail(WASTE_EINVAL, "NULL idx or gate output");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float *logits = d_logits ? d_logits : h->W.logits;
+    if (h->profiling) cudaEventRecord(h->route_tm.ev[0], s);
+    cudaError_t e = launch_router(h->L, d_h, T, logits, s);
+    if (e != cudaSuccess) return cuda_fail(e, "router kernel");
+    if (h->profiling) cudaEventRecord(h->route_tm.ev[1], s);
+    e = launch_topk(logits, T, h->L.E, h->L.k, d_idx, d_gate, h->W.pred_idx,
+                    h->W.pred_count, h->pred_P > 0 ? h->pred_P : 1, h->W.stats,
+                    (unsigned long long)h->L.E * (unsigned long long)h->L.d * 4ull, s);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k kernel");
+    if (h->profiling) {
+        cudaEventRecord(h->route_tm.ev[2], s);
+        h->route_tm.n = 3;
+    }
+    return ok();
+}
+
+int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d_idx,
+                      const float *d_gate, float *d_out, int32_t mode, waste_stream_t stream) {
+    int rc = check_tokens(h, T, d_h);
+    if (rc) return rc;
+    if (mode < 0 || mode > 2) return fail(WASTE_EINVAL, "mode = %d", mode);
+    if (mode == 2 && h->cfg.act_dtype != WASTE_ACT_F32)
+        return fail(WASTE_EINVAL, "mode 2 (out = h + y) needs fp32 hidden states");
+    if (T == 0) return ok();
+    if (!d_idx || !d_gate || !d_out) return fail(WASTE_EINVAL, "NULL idx, gate or out");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool recon = (h->cfg.flags & WASTE_FLAG_K2_RECONSTRUCT) != 0;
+    cudaError_t e = launch_lut_forward(h->L, h->W, d_h, T, d_idx, d_gate, d_out, mode, recon,
+                                       h->num_sms, s, h->profiling ? &h->fwd_tm : nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "expert kernels");
+    return ok();
+}
+
+int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_t n_prefetch,
+                       waste_stream_t side) {
+    int rc = check_tokens(next_layer, T, d_h);
+    if (rc) return rc;
+    waste_moe *h = next_layer;
+    const int P = n_prefetch < 0 ? h->lookahead : n_prefetch;
+    if (P > h->L.E || P > kMaxTopK)
+        return fail(WASTE_EINVAL, "n_prefetch = %d above min(n_experts, %d)", P, kMaxTopK);
+    if (T == 0 || P == 0) return ok();
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(side);
+    cudaError_t e = launch_router(h->L, d_h, T, h->W.pred_logits, s);
+    if (e != cudaSuccess) return cuda_fail(e, "lookahead router");
+    e = launch_topk(h->W.pred_logits, T, h->L.E, P, h->W.pred_idx, h->W.pred_gate_sel, nullptr,
+                    nullptr, 1, nullptr, 0, s);
+    if (e != cudaSuccess) return cuda_fail(e, "lookahead top-k");
+    h->pred_P = P;
+    e = launch_prefetch_l2(h->L, h->W.pred_idx, P, T, P, h->W.pred_count, h->W.stats, s);
+    if (e != cudaSuccess) return cuda_fail(e, "L2 prefetch");
+    return ok();
+}
+
+int waste_moe_stats(const waste_moe *h, waste_moe_stats_t *out) {
+    if (!h || !out) return fail(WASTE_EINVAL, "NULL handle or output");
+    unsigned long long v[kStatCount];
+    uint32_t err = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(v, h->W.stats, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(&err, h->W.err, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading statistics");
+    out->demand_code_bytes = v[kStatDemandCode];
+    out->codebook_bytes = v[kStatCodebook];
+    out->router_bytes = v[kStatRouter];
+    out->prefetch_issued_bytes = v[kStatPrefetchBytes];
+    out->prefetch_experts = v[kStatPrefetchExperts];
+    out->prediction_hits = v[kStatPredHits];
+    out->routed_slots = v[kStatRoutedSlots];
+    out->forward_slots = v[kStatForwardSlots];
+    if (err & kErrBadExpert) return fail(WASTE_EINVAL, "forward saw an expert index outside [0, %d)", h->L.E);
+    return ok();
+}
+
+int waste_moe_reset_stats(waste_moe *h) {
+    if (!h) return fail(WASTE_EINVAL, "NULL handle");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemset(h->W.stats, 0, kStatCount * 8);
+    if (e == cudaSuccess) e = cudaMemset(h->W.err, 0, 4);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "resetting statistics");
+    return ok();
+}
+
+int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int32_t k,
+                               int32_t *d_idx, float *d_gate, waste_stream_t stream) {
+    if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > E || k > kMaxTopK)
+        return fail(WASTE_EINVAL, "T = %d, E = %d, k = %d out of range", T, E, k);
+    if (T == 0) return ok();
+    if (!d_logits || !d_idx || !d_gate) return fail(WASTE_EINVAL, "NULL pointer");
+    cudaError_t e = launch_topk(d_logits, T, E, k, d_idx, d_gate, nullptr, nullptr, 1, nullptr, 0,
+                                reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "top-k kernel");
+    return ok();
+}
+
+} // extern "C"

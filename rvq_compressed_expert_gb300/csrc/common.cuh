@@ -1,0 +1,116 @@
+// Internal declarations shared by the translation units of libwaste_moe.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "waste_moe.h"
+
+namespace wm {
+
+constexpr int kStages = 3;
+constexpr int kCodes = 256;
+constexpr int kVec = 8;
+constexpr int kSegVec = 32;    // vectors per segment (one per lane)
+constexpr int kGroupRows = 16; // rows per 16-byte chunk
+constexpr int kMaxExperts = 4096;
+constexpr int kMaxTopK = 32;
+
+// Sticky device error bits.
+enum : uint32_t { kErrBadExpert = 1u };
+
+// Device counters, indices into the handle's uint64 counter array.
+enum {
+    kStatDemandCode = 0,
+    kStatCodebook,
+    kStatRouter,
+    kStatPrefetchBytes,
+    kStatPrefetchExperts,
+    kStatPredHits,
+    kStatRoutedSlots,
+    kStatForwardSlots,
+    kStatCount
+};
+
+// Geometry of one tiled matrix section.
+struct MatGeom {
+    int n_out, n_in;
+    int nv;     // vectors per row
+    int nseg;   // 32-vector segments
+    int groups; // 16-row groups
+    __host__ __device__ size_t chunk_bytes() const { return (size_t)nseg * groups * kStages * 512; }
+};
+
+inline MatGeom mat_geom(int n_out, int n_in) {
+    MatGeom g;
+    g.n_out = n_out;
+    g.n_in = n_in;
+    g.nv = n_in / kVec;
+    g.nseg = (g.nv + kSegVec - 1) / kSegVec;
+    g.groups = (n_out + kGroupRows - 1) / kGroupRows;
+    return g;
+}
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Everything a kernel needs to reach one layer's weights.
+struct LayerView {
+    const float *router_w;
+    const float *router_b;
+    const uint8_t *records;
+    size_t stride;
+    size_t sec_off[3];
+    const float *codebooks; // [E][3][3][256][8]
+    int d, f, E, k;
+    int act_bf16;
+    MatGeom gu;   // gate / up geometry (f rows, d inputs)
+    MatGeom dn;   // down geometry (d rows, f inputs)
+};
+
+struct Workspace {
+    float *logits;       // [max_T][E]
+    float *pred_logits;  // [max_T][E]
+    int32_t *pred_idx;   // [max_T][kMaxTopK]
+    int32_t *pred_count; // [max_T]
+    int32_t *pred_idx_sel; // scratch for prefetch top-k
+    float *pred_gate_sel;  // scratch (unused gates of the prediction)
+    float *part_gu;      // [max_slots][gu.nseg][2][f]
+    float *part_dn;      // [max_slots][npair][d]
+    unsigned long long *stats; // [kStatCount]
+    uint32_t *err;       // sticky error bits
+    void *base;
+    size_t bytes;
+};
+
+// ---- launchers (each returns cudaGetLastError() of its launches) ----
+cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
+                          cudaStream_t s);
+cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *gate,
+                        const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
+                        unsigned long long *stats, unsigned long long router_bytes,
+                        cudaStream_t s);
+// Optional per-kernel timing: events[i] is recorded after the i-th kernel (events[0] before
+// the first); null = no timing.
+struct Timing {
+    cudaEvent_t ev[8];
+    int n;
+};
+cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
+                               const int32_t *idx, const float *gate, float *out, int mode,
+                               bool reconstruct, int num_sms, cudaStream_t s, Timing *tm);
+cudaError_t launch_prefetch_l2(const LayerView &L, const int32_t *pred_idx, int pred_stride,
+                               int T, int P, int32_t *pred_count, unsigned long long *stats,
+                               cudaStream_t s);
+cudaError_t launch_pack(const MatGeom &gu, const MatGeom &dn, int n_experts,
+                        const uint8_t *gate_codes, const uint8_t *up_codes,
+                        const uint8_t *down_codes, uint8_t *records, size_t stride,
+                        const size_t sec_off[3], cudaStream_t s);
+
+cudaError_t launch_headers(uint8_t *records, size_t stride, int n, const waste_record_header &hdr,
+                           int expert_begin, cudaStream_t s);
+
+int device_sm_count();
+
+} // namespace wm

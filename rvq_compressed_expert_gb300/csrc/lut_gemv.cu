@@ -1,0 +1,434 @@
+// Expert matrices applied straight from their RVQ codes, one (token, expert)
+// slot at a time: the decode path.
+//
+// Method (page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section
+// "Quantification et exactitude"): the weights are stored as 3 residual stages
+// of 256-entry codebooks over 8-weight vectors, and the product is taken
+// without rebuilding the matrix -- a table of partial dot products
+// T[s][j][c] = <C_s[c], x_j> is built, then each row costs 3 lookups and 2
+// additions per vector.
+//
+// GB300 mapping.  A CTA (512 threads, one per SM, persistent) owns a "unit":
+// one slot and one 32-vector segment of the input (two matrices' worth: gate
+// and up at the same segment, or two consecutive segments of down).  It builds
+// the unit's tables in shared memory -- T[s][c][part][lane], 3 x 64 KiB, so
+// that lane l always reads bank l whatever the code -- then streams all rows'
+// codes of that segment with 128-bit loads.  Each lane owns one vector column
+// and 16 rows per 16-byte chunk; the chunk's bytes are pre-permuted (row
+// (lane ^ q) & 15 at byte q) so the cross-lane reduction of 32 row partials is
+// a select-free butterfly.  One PRMT turns a code byte plus the lane's column
+// offset into the table address, so a lookup costs PRMT + LDS + FADD.
+// Partials of each segment go to a scratch buffer; the down kernel reduces the
+// gate/up partials in a fixed order, applies SwiGLU and builds its own tables;
+// a last kernel combines the k expert outputs with their gates.  Every sum has a
+// fixed order: results are bit-reproducible.
+//
+// The K2_RECONSTRUCT variant instead stages the codebooks in shared memory and
+// rebuilds each 8-weight vector in registers (3 codebook rows summed) before an
+// 8-term dot product.
+#include "common.cuh"
+
+namespace wm {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTabStage = 65536;             // bytes per stage: 256 codes x 256 B
+constexpr int kTabBytes = kStages * kTabStage; // 192 KiB
+constexpr int kXsFloats = 512;               // down input staging (64 vectors x 8)
+constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
+
+struct LutArgs {
+    const uint8_t *records;
+    size_t stride;
+    const float *codebooks;
+    const int32_t *idx;
+    const void *h;
+    int E, k, slots;
+    // gate / up
+    MatGeom gu;
+    size_t off_gate, off_up;
+    float *part_gu; // [slot][gu.nseg][2][f]
+    // down
+    MatGeom dn;
+    size_t off_down;
+    int npair, nrb, rb_groups;
+    float *part_dn; // [slot][npair][d]
+    unsigned long long *stats;
+    uint32_t *err;
+};
+
+__device__ __forceinline__ uint32_t comp(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void load_x8(const void *h, size_t elem, float *xv) {
+    if constexpr (kBf16) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(h) + elem);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+            float2 f2 = __bfloat1622float2(b2);
+            xv[2 * i] = f2.x;
+            xv[2 * i + 1] = f2.y;
+        }
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(h) + elem);
+        const float4 a = p[0], b = p[1];
+        xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+        xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ float dot8(const float *__restrict__ c, const float *xv) {
+    const float4 c0 = __ldg(reinterpret_cast<const float4 *>(c));
+    const float4 c1 = __ldg(reinterpret_cast<const float4 *>(c) + 1);
+    float t = c0.x * xv[0];
+    t = fmaf(c0.y, xv[1], t);
+    t = fmaf(c0.z, xv[2], t);
+    t = fmaf(c0.w, xv[3], t);
+    t = fmaf(c1.x, xv[4], t);
+    t = fmaf(c1.y, xv[5], t);
+    t = fmaf(c1.z, xv[6], t);
+    t = fmaf(c1.w, xv[7], t);
+    return t;
+}
+
+__device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes, int lane) {
+    constexpr size_t kPiece = 32768;
+    for (size_t off = (size_t)lane * kPiece; off < bytes; off += 32 * kPiece) {
+        const uint32_t n = (uint32_t)min(kPiece, bytes - off);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + off), "r"(n) : "memory");
+    }
+}
+
+// Decode a unit index into (slot, first segment, part bases, row-group range).
+struct Unit {
+    int slot, e, seg0, g0, g1;
+    const uint8_t *base[2]; // chunk (seg, g=0, s=0, jj=0) of each part, or null
+};
+
+template <bool kDown>
+__device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
+    Unit U;
+    if constexpr (!kDown) {
+        U.slot = u / A.gu.nseg;
+        U.seg0 = u % A.gu.nseg;
+        U.g0 = 0;
+        U.g1 = A.gu.groups;
+    } else {
+        const int per_slot = A.npair * A.nrb;
+        U.slot = u / per_slot;
+        const int rem = u % per_slot;
+        U.seg0 = 2 * (rem / A.nrb);
+        const int rb = rem % A.nrb;
+        U.g0 = rb * A.rb_groups;
+        U.g1 = min(A.dn.groups, U.g0 + A.rb_groups);
+    }
+    U.e = A.idx[U.slot];
+    U.base[0] = U.base[1] = nullptr;
+    if (U.e >= 0 && U.e < A.E) {
+        const uint8_t *rec = A.records + (size_t)U.e * A.stride;
+        if constexpr (!kDown) {
+            const size_t so = (size_t)U.seg0 * A.gu.groups * (kStages * 512);
+            U.base[0] = rec + A.off_gate + so;
+            U.base[1] = rec + A.off_up + so;
+        } else {
+            for (int p = 0; p < 2; ++p)
+                if (U.seg0 + p < A.dn.nseg)
+                    U.base[p] = rec + A.off_down + (size_t)(U.seg0 + p) * A.dn.groups * (kStages * 512);
+        }
+    }
+    return U;
+}
+
+template <bool kDown, bool kRecon, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    // LUT variant: smem = tables [3][256][2][32] fp32 (192 KiB) + xs
+    // reconstruct variant: smem = codebooks [2][3][256][8] fp32 (48 KiB) + xs
+    float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kTabBytes));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b4 = lane >> 4;
+    const MatGeom &G = kDown ? A.dn : A.gu;
+    const int units = kDown ? A.slots * A.npair * A.nrb : A.slots * A.gu.nseg;
+    // table column byte offset of register-part p: column (p ^ b4), lane l
+    const uint32_t colb0 = ((uint32_t)(0 ^ b4) << 7) | ((uint32_t)lane << 2);
+    const uint32_t colb1 = ((uint32_t)(1 ^ b4) << 7) | ((uint32_t)lane << 2);
+
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const Unit U = decode_unit<kDown>(A, u);
+        const bool valid = U.base[0] != nullptr;
+        // warm L2 with the next unit's codes while this one builds its tables
+        if (warp == 0 && u + (int)gridDim.x < units) {
+            const Unit N = decode_unit<kDown>(A, u + gridDim.x);
+            for (int p = 0; p < 2; ++p)
+                if (N.base[p])
+                    prefetch_l2_range(N.base[p] + (size_t)N.g0 * (kStages * 512),
+                                      (size_t)(N.g1 - N.g0) * (kStages * 512), lane);
+        }
+        if (!valid) {
+            if (threadIdx.x == 0) atomicOr(A.err, kErrBadExpert);
+        }
+        const int t = U.slot / A.k;
+        // ---- input vectors of this lane's column(s)
+        float xv[2][kVec];
+        if constexpr (!kDown) {
+            const int j = U.seg0 * kSegVec + lane;
+            if (j < G.nv) load_x8<kBf16>(A.h, (size_t)t * A.gu.n_in + (size_t)j * kVec, xv[0]);
+            else {
+#pragma unroll
+                for (int v = 0; v < kVec; ++v) xv[0][v] = 0.f;
+            }
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) xv[1][v] = xv[0][v];
+        } else {
+            // a = silu(gate) * up for the 64 vectors of this unit, reduced over the
+            // gate/up segments in a fixed order
+            __syncthreads(); // xs may still be read by the previous unit
+            {
+                const int r = U.seg0 * kSegVec * kVec + threadIdx.x; // index into f
+                float a = 0.f;
+                if (valid && r < A.gu.n_out) {
+                    const float *pg = A.part_gu + (size_t)U.slot * A.gu.nseg * 2 * A.gu.n_out;
+                    float zg = 0.f, zu = 0.f;
+                    for (int sg = 0; sg < A.gu.nseg; ++sg) {
+                        zg += pg[((size_t)sg * 2 + 0) * A.gu.n_out + r];
+                        zu += pg[((size_t)sg * 2 + 1) * A.gu.n_out + r];
+                    }
+                    a = zg / (1.0f + expf(-zg)) * zu;
+                }
+                xs[threadIdx.x] = a;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+                for (int v = 0; v < kVec; ++v) xv[p][v] = xs[p * kSegVec * kVec + lane * kVec + v];
+        }
+        // x of register-part p (column p ^ b4), for the reconstruct variant
+        float xr[2][kVec];
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) xr[p][v] = b4 ? xv[p ^ 1][v] : xv[p][v];
+        __syncthreads(); // previous unit's lookups are done with the tables
+        const float *cb_e = A.codebooks + (size_t)(valid ? U.e : 0) * 3 * kCbFloats;
+        const float *cb_p0 = cb_e + (kDown ? 2 : 0) * kCbFloats;
+        const float *cb_p1 = cb_e + (kDown ? 2 : 1) * kCbFloats;
+        if constexpr (!kRecon) {
+            // ---- tables T[s][c][part][lane]
+            float *tab = reinterpret_cast<float *>(smem);
+            for (int combo = warp; combo < kStages * kCodes; combo += kWarps) {
+                const int s = combo >> 8, c = combo & 255;
+                const size_t o = (size_t)s * kCodes * kVec + (size_t)c * kVec;
+                const float t0 = valid ? dot8(cb_p0 + o, xv[0]) : 0.f;
+                const float t1 = valid ? dot8(cb_p1 + o, xv[1]) : 0.f;
+                tab[(size_t)combo * 64 + lane] = t0;
+                tab[(size_t)combo * 64 + 32 + lane] = t1;
+            }
+        } else {
+            // ---- codebooks of both parts [2][3][256][8]
+            float4 *cbs = reinterpret_cast<float4 *>(smem);
+            for (int i = threadIdx.x; i < 2 * kCbFloats / 4; i += kThreads) {
+                const float *src = (i < kCbFloats / 4) ? cb_p0 : cb_p1;
+                const int ii = i % (kCbFloats / 4);
+                cbs[i] = __ldg(reinterpret_cast<const float4 *>(src) + ii);
+            }
+        }
+        __syncthreads();
+
+        // ---- stream the codes of rows [g0, g1) x this unit's segment(s)
+        const uint8_t *pb0 = b4 ? U.base[1] : U.base[0];
+        const uint8_t *pb1 = b4 ? U.base[0] : U.base[1];
+        const unsigned char *tabb = smem;
+        for (int g = U.g0 + warp; g < U.g1; g += kWarps) {
+            uint4 cw[2][kStages];
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+                const size_t co = ((size_t)g * kStages + s) * 512 + (size_t)lane * 16;
+                cw[0][s] = pb0 ? __ldg(reinterpret_cast<const uint4 *>(pb0 + co)) : make_uint4(0, 0, 0, 0);
+                cw[1][s] = pb1 ? __ldg(reinterpret_cast<const uint4 *>(pb1 + co)) : make_uint4(0, 0, 0, 0);
+            }
+            float acc[32];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const uint32_t colb = p ? colb1 : colb0;
+#pragma unroll
+                for (int wd = 0; wd < 4; ++wd) {
+                    const uint32_t w0 = comp(cw[p][0], wd), w1 = comp(cw[p][1], wd), w2 = comp(cw[p][2], wd);
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        if constexpr (!kRecon) {
+                            const uint32_t sel = 0x7604u | ((uint32_t)b << 4);
+                            const uint32_t a0 = __byte_perm(w0, colb, sel);
+                            const uint32_t a1 = __byte_perm(w1, colb, sel);
+                            const uint32_t a2 = __byte_perm(w2, colb, sel);
+                            const float t0 = *reinterpret_cast<const float *>(tabb + a0);
+                            const float t1 = *reinterpret_cast<const float *>(tabb + kTabStage + a1);
+                            const float t2 = *reinterpret_cast<const float *>(tabb + 2 * kTabStage + a2);
+                            acc[16 * p + 4 * wd + b] = (t0 + t1) + t2;
+                        } else {
+                            const int part = p ^ b4;
+                            const float *cbs = reinterpret_cast<const float *>(smem) + part * kCbFloats;
+                            const int c0 = (w0 >> (8 * b)) & 255, c1 = (w1 >> (8 * b)) & 255,
+                                      c2 = (w2 >> (8 * b)) & 255;
+                            const float4 *r0 = reinterpret_cast<const float4 *>(cbs + c0 * kVec);
+                            const float4 *r1 = reinterpret_cast<const float4 *>(cbs + kCodes * kVec + c1 * kVec);
+                            const float4 *r2 = reinterpret_cast<const float4 *>(cbs + 2 * kCodes * kVec + c2 * kVec);
+                            const float4 a0 = r0[0], a1 = r0[1], b0 = r1[0], b1 = r1[1], d0 = r2[0], d1 = r2[1];
+                            const float *x = xr[p];
+                            float sacc = ((a0.x + b0.x) + d0.x) * x[0];
+                            sacc = fmaf((a0.y + b0.y) + d0.y, x[1], sacc);
+                            sacc = fmaf((a0.z + b0.z) + d0.z, x[2], sacc);
+                            sacc = fmaf((a0.w + b0.w) + d0.w, x[3], sacc);
+                            sacc = fmaf((a1.x + b1.x) + d1.x, x[4], sacc);
+                            sacc = fmaf((a1.y + b1.y) + d1.y, x[5], sacc);
+                            sacc = fmaf((a1.z + b1.z) + d1.z, x[6], sacc);
+                            sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
+                            acc[16 * p + 4 * wd + b] = sacc;
+                        }
+                    }
+                }
+            }
+            // slot i of lane l holds row (l ^ i) of the 32 (part, row) pairs: reduce-scatter
+#pragma unroll
+            for (int n = 16; n >= 1; n >>= 1)
+#pragma unroll
+                for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
+            const int row = g * kGroupRows + (lane & 15);
+            if constexpr (!kDown) {
+                if (row < G.n_out)
+                    A.part_gu[(((size_t)U.slot * A.gu.nseg + U.seg0) * 2 + b4) * G.n_out + row] = acc[0];
+            } else {
+                const float v = acc[0] + __shfl_xor_sync(0xffffffffu, acc[0], 16);
+                if (lane < 16 && row < G.n_out)
+                    A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = v;
+            }
+        }
+        // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
+        // and the slot's codebooks once
+        if (threadIdx.x == 0 && valid && A.stats) {
+            unsigned long long vecs = 0;
+            for (int p = 0; p < 2; ++p) {
+                const int seg = kDown ? U.seg0 + p : U.seg0;
+                if (seg < G.nseg) vecs += (unsigned long long)min(kSegVec, G.nv - seg * kSegVec);
+            }
+            const int rows = min(G.n_out, U.g1 * kGroupRows) - U.g0 * kGroupRows;
+            atomicAdd(A.stats + kStatDemandCode, vecs * (unsigned long long)rows * kStages);
+            const bool first = kDown ? (U.seg0 == 0 && U.g0 == 0) : (U.seg0 == 0);
+            if (first)
+                atomicAdd(A.stats + kStatCodebook,
+                          (unsigned long long)(kDown ? 1 : 2) * kCbFloats * sizeof(float));
+        }
+    }
+}
+
+// out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair]
+__global__ void combine_kernel(const float *__restrict__ part_dn, const int32_t *__restrict__ idx,
+                               const float *__restrict__ gate, const float *__restrict__ h,
+                               float *__restrict__ out, int d, int k, int E, int npair,
+                               int mode, unsigned long long *stats, unsigned long long slots) {
+    const int t = blockIdx.y;
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (stats && r == 0 && t == 0) atomicAdd(stats + kStatForwardSlots, slots);
+    if (r >= d) return;
+    float y = 0.f;
+    for (int i = 0; i < k; ++i) {
+        const int e = idx[(size_t)t * k + i];
+        if (e < 0 || e >= E) continue;
+        const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
+        float s = 0.f;
+        for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
+        y = fmaf(gate[(size_t)t * k + i], s, y);
+    }
+    const size_t o = (size_t)t * d + r;
+    if (mode == 0) out[o] = y;
+    else if (mode == 1) out[o] = out[o] + y;
+    else out[o] = h[o] + y;
+}
+
+template <bool kDown, bool kRecon, bool kBf16>
+cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
+    const size_t smem = (kRecon ? 2 * kCbFloats * 4 : kTabBytes) + kXsFloats * 4;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(lut_kernel<kDown, kRecon, kBf16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int grid = units < num_sms ? units : num_sms;
+    lut_kernel<kDown, kRecon, kBf16><<<grid, kThreads, smem, s>>>(A);
+    return cudaGetLastError();
+}
+
+template <bool kDown>
+cudaError_t launch_var(const LutArgs &A, int units, bool recon, bool bf16, int num_sms, cudaStream_t s) {
+    if (recon) return bf16 ? launch_one<kDown, true, true>(A, units, num_sms, s)
+                           : launch_one<kDown, true, false>(A, units, num_sms, s);
+    return bf16 ? launch_one<kDown, false, true>(A, units, num_sms, s)
+                : launch_one<kDown, false, false>(A, units, num_sms, s);
+}
+
+} // namespace
+
+// Row blocks of the down matrix per (slot, segment pair): enough units to fill
+// the SMs, but at least 64 row groups per unit so the table build stays small
+// next to the rows it serves.
+static int down_row_blocks(int slots, int npair, int groups, int num_sms) {
+    const int base = slots * npair;
+    int nrb = (num_sms + base / 2) / base;
+    const int max_rb = groups / 64 > 1 ? groups / 64 : 1;
+    if (nrb > max_rb) nrb = max_rb;
+    if (nrb < 1) nrb = 1;
+    return nrb;
+}
+
+cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
+                               const int32_t *idx, const float *gate, float *out, int mode,
+                               bool reconstruct, int num_sms, cudaStream_t s, Timing *tm) {
+    LutArgs A;
+    A.records = L.records;
+    A.stride = L.stride;
+    A.codebooks = L.codebooks;
+    A.idx = idx;
+    A.h = h;
+    A.E = L.E;
+    A.k = L.k;
+    A.slots = T * L.k;
+    A.gu = L.gu;
+    A.off_gate = L.sec_off[0];
+    A.off_up = L.sec_off[1];
+    A.part_gu = W.part_gu;
+    A.dn = L.dn;
+    A.off_down = L.sec_off[2];
+    A.npair = (L.dn.nseg + 1) / 2;
+    A.nrb = down_row_blocks(A.slots, A.npair, L.dn.groups, num_sms);
+    A.rb_groups = (L.dn.groups + A.nrb - 1) / A.nrb;
+    A.part_dn = W.part_dn;
+    A.stats = W.stats;
+    A.err = W.err;
+    const bool bf16 = L.act_bf16 != 0;
+    if (tm) cudaEventRecord(tm->ev[0], s);
+    cudaError_t e = launch_var<false>(A, A.slots * A.gu.nseg, reconstruct, bf16, num_sms, s);
+    if (e != cudaSuccess) return e;
+    if (tm) cudaEventRecord(tm->ev[1], s);
+    e = launch_var<true>(A, A.slots * A.npair * A.nrb, reconstruct, bf16, num_sms, s);
+    if (e != cudaSuccess) return e;
+    if (tm) cudaEventRecord(tm->ev[2], s);
+    dim3 grid((L.d + 255) / 256, T);
+    combine_kernel<<<grid, 256, 0, s>>>(W.part_dn, idx, gate, reinterpret_cast<const float *>(h), out,
+                                        L.d, L.k, L.E, A.npair, mode, W.stats,
+                                        (unsigned long long)A.slots);
+    if (tm) {
+        cudaEventRecord(tm->ev[3], s);
+        tm->n = 4;
+    }
+    return cudaGetLastError();
+}
+
+} // namespace wm
