@@ -177,34 +177,44 @@ def run_decode(args, dev, out):
     layer = MoELayer(w, seed=0, layer=0, device=dev)
     pool = [synth.hidden(100 + i, 1, w.d, "f32", dev) for i in range(DECODE_POOL)]
     idx, gate, logits, y = layer.alloc_outputs(1)
+    h_in = torch.empty(1, w.d, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(i):
-        layer.route(pool[i % DECODE_POOL], 1, idx, gate, logits)
-        layer.forward(pool[i % DECODE_POOL], 1, idx, gate, y, 0)
-
-    for i in range(args.warmup):
-        flush.zero_()
-        step(i)
-    torch.cuda.synchronize()
-    B.waste_moe_set_profiling(layer.handle, True)
-    layer.reset_stats()
     K = args.steps
+
+    def step():
+        layer.route(h_in, 1, idx, gate, logits)
+        layer.forward(h_in, 1, idx, gate, y, 0)
+
+    # the decode step as a CUDA graph (route + forward: 5 kernels), replayed per token
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(3):
+            h_in.copy_(pool[i])
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        h_in.copy_(pool[i % DECODE_POOL])
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    layer.reset_stats()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    prof = []
     if args.world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_start = time.time()
     for i in range(K):
+        h_in.copy_(pool[i % DECODE_POOL])
         flush.zero_()
         ev[i][0].record(stream)
-        step(i)
+        graph.replay()
         ev[i][1].record(stream)
-        if i % 8 == 7 or i == K - 1:  # read the per-kernel events of this step
-            torch.cuda.synchronize()
-            prof.append(B.waste_moe_read_profile(layer.handle))
     torch.cuda.synchronize()
     t_end = time.time()
     if args.world > 1:
@@ -217,6 +227,21 @@ def run_decode(args, dev, out):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     st = layer.stats()
+
+    # per-kernel device times: the same step launched directly with CUDA events between
+    # its kernels, queued behind a short spin kernel so launches never starve the GPU
+    B.waste_moe_set_profiling(layer.handle, True)
+    prof = []
+    n_prof = max(8, min(K, 200))
+    t_start = time.time()
+    for i in range(n_prof):
+        h_in.copy_(pool[i % DECODE_POOL])
+        flush.zero_()
+        torch.cuda._sleep(100_000)
+        step()
+        prof.append(B.waste_moe_read_profile(layer.handle))
+    torch.cuda.synchronize()
+    args.sampler.mark(t_start, time.time())
     B.waste_moe_set_profiling(layer.handle, False)
 
     step_bytes, gu_bytes, dn_bytes = decode_algorithmic_bytes(w)
@@ -226,27 +251,36 @@ def run_decode(args, dev, out):
                          gate_up_bytes=gu_bytes, down_bytes=dn_bytes,
                          hbm_gbs_step=step_bytes / (ms_per_step * 1e-3) / 1e9,
                          median_step_ms=statistics.median(step_ms),
-                         launches_per_step=5)
+                         launches_per_step=5, profiled_steps=n_prof)
 
-    # ---- end to end through the C ABI with host buffers
-    h_host = [p.cpu().pin_memory() for p in pool[:8]]
+    # ---- end to end through the C ABI with host buffers: h2d copy of the token from
+    # pinned memory, route, forward, d2h copy of the result -- one graph per step
+    h_host = torch.empty(1, w.d, dtype=torch.float32).pin_memory()
     y_host = torch.empty(1, w.d, dtype=torch.float32).pin_memory()
-    h_dev = torch.empty(1, w.d, dtype=torch.float32, device=dev)
-    for i in range(args.warmup):
-        h_dev.copy_(h_host[i % 8], non_blocking=True)
-        layer.route(h_dev, 1, idx, gate, logits)
-        layer.forward(h_dev, 1, idx, gate, y, 0)
+    host_pool = [p.cpu() for p in pool[:8]]
+    with torch.cuda.stream(side):
+        for i in range(3):
+            h_in.copy_(h_host, non_blocking=True)
+            step()
+            y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        h_in.copy_(h_host, non_blocking=True)
+        step()
         y_host.copy_(y, non_blocking=True)
+    for i in range(args.warmup):
+        h_host.copy_(host_pool[i % 8])
+        g2.replay()
     torch.cuda.synchronize()
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start = time.time()
     for i in range(K):
+        torch.cuda.current_stream().synchronize()  # the host buffer is free again
+        h_host.copy_(host_pool[i % 8])
         flush.zero_()
         ev2[i][0].record(stream)
-        h_dev.copy_(h_host[i % 8], non_blocking=True)
-        layer.route(h_dev, 1, idx, gate, logits)
-        layer.forward(h_dev, 1, idx, gate, y, 0)
-        y_host.copy_(y, non_blocking=True)
+        g2.replay()
         ev2[i][1].record(stream)
     torch.cuda.synchronize()
     args.sampler.mark(t_start, time.time())

@@ -237,6 +237,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     const size_t npair = (size_t)(L.dn.nseg + 1) / 2;
     size_t sizes[] = {
         T * E * 4,                                  // logits
+        T * E * 4,                                  // logits_lo
         T * E * 4,                                  // pred_logits
         T * kMaxTopK * 4,                           // pred_idx
         T * 4,                                      // pred_count
@@ -264,15 +265,16 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     W.base = base;
     W.bytes = total;
     W.logits = reinterpret_cast<float *>(b + offs[0]);
-    W.pred_logits = reinterpret_cast<float *>(b + offs[1]);
-    W.pred_idx = reinterpret_cast<int32_t *>(b + offs[2]);
-    W.pred_count = reinterpret_cast<int32_t *>(b + offs[3]);
-    W.pred_gate_sel = reinterpret_cast<float *>(b + offs[4]);
+    W.logits_lo = reinterpret_cast<float *>(b + offs[1]);
+    W.pred_logits = reinterpret_cast<float *>(b + offs[2]);
+    W.pred_idx = reinterpret_cast<int32_t *>(b + offs[3]);
+    W.pred_count = reinterpret_cast<int32_t *>(b + offs[4]);
+    W.pred_gate_sel = reinterpret_cast<float *>(b + offs[5]);
     W.pred_idx_sel = W.pred_idx;
-    W.part_gu = reinterpret_cast<float *>(b + offs[5]);
-    W.part_dn = reinterpret_cast<float *>(b + offs[6]);
-    W.stats = reinterpret_cast<unsigned long long *>(b + offs[7]);
-    W.err = reinterpret_cast<uint32_t *>(b + offs[8]);
+    W.part_gu = reinterpret_cast<float *>(b + offs[6]);
+    W.part_dn = reinterpret_cast<float *>(b + offs[7]);
+    W.stats = reinterpret_cast<unsigned long long *>(b + offs[8]);
+    W.err = reinterpret_cast<uint32_t *>(b + offs[9]);
     ce = cudaMemset(base, 0, total);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
@@ -358,10 +360,10 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *logits = d_logits ? d_logits : h->W.logits;
     if (h->profiling) cudaEventRecord(h->route_tm.ev[0], s);
-    cudaError_t e = launch_router(h->L, d_h, T, logits, s);
+    cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s);
     if (e != cudaSuccess) return cuda_fail(e, "router kernel");
     if (h->profiling) cudaEventRecord(h->route_tm.ev[1], s);
-    e = launch_topk(logits, T, h->L.E, h->L.k, d_idx, d_gate, h->W.pred_idx,
+    e = launch_topk(logits, h->W.logits_lo, T, h->L.E, h->L.k, d_idx, d_gate, h->W.pred_idx,
                     h->W.pred_count, h->pred_P > 0 ? h->pred_P : 1, h->W.stats,
                     (unsigned long long)h->L.E * (unsigned long long)h->L.d * 4ull, s);
     if (e != cudaSuccess) return cuda_fail(e, "top-k kernel");
@@ -399,9 +401,9 @@ int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_
         return fail(WASTE_EINVAL, "n_prefetch = %d above min(n_experts, %d)", P, kMaxTopK);
     if (T == 0 || P == 0) return ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(side);
-    cudaError_t e = launch_router(h->L, d_h, T, h->W.pred_logits, s);
+    cudaError_t e = launch_router(h->L, d_h, T, h->W.pred_logits, nullptr, s);
     if (e != cudaSuccess) return cuda_fail(e, "lookahead router");
-    e = launch_topk(h->W.pred_logits, T, h->L.E, P, h->W.pred_idx, h->W.pred_gate_sel, nullptr,
+    e = launch_topk(h->W.pred_logits, nullptr, T, h->L.E, P, h->W.pred_idx, h->W.pred_gate_sel, nullptr,
                     nullptr, 1, nullptr, 0, s);
     if (e != cudaSuccess) return cuda_fail(e, "lookahead top-k");
     h->pred_P = P;
@@ -446,7 +448,7 @@ int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int3
         return fail(WASTE_EINVAL, "T = %d, E = %d, k = %d out of range", T, E, k);
     if (T == 0) return ok();
     if (!d_logits || !d_idx || !d_gate) return fail(WASTE_EINVAL, "NULL pointer");
-    cudaError_t e = launch_topk(d_logits, T, E, k, d_idx, d_gate, nullptr, nullptr, 1, nullptr, 0,
+    cudaError_t e = launch_topk(d_logits, nullptr, T, E, k, d_idx, d_gate, nullptr, nullptr, 1, nullptr, 0,
                                 reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "top-k kernel");
     return ok();

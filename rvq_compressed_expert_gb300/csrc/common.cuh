@@ -71,6 +71,7 @@ struct LayerView {
 
 struct Workspace {
     float *logits;       // [max_T][E]
+    float *logits_lo;    // [max_T][E]
     float *pred_logits;  // [max_T][E]
     int32_t *pred_idx;   // [max_T][kMaxTopK]
     int32_t *pred_count; // [max_T]
@@ -85,12 +86,14 @@ struct Workspace {
 };
 
 // ---- launchers (each returns cudaGetLastError() of its launches) ----
+// logits_lo (optional): exact remainder of adding the router bias, so that
+// logits + logits_lo equals W_r h + b exactly given the fp32 dot product.
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
-                          cudaStream_t s);
-cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *gate,
-                        const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
-                        unsigned long long *stats, unsigned long long router_bytes,
-                        cudaStream_t s);
+                          float *logits_lo, cudaStream_t s);
+cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int E, int k,
+                        int32_t *idx, float *gate, const int32_t *pred_idx, int32_t *pred_count,
+                        int pred_stride, unsigned long long *stats,
+                        unsigned long long router_bytes, cudaStream_t s);
 // Optional per-kernel timing: events[i] is recorded after the i-th kernel (events[0] before
 // the first); null = no timing.
 struct Timing {

@@ -38,6 +38,8 @@ constexpr int kTabStage = 65536;             // bytes per stage: 256 codes x 256
 constexpr int kTabBytes = kStages * kTabStage; // 192 KiB
 constexpr int kXsFloats = 512;               // down input staging (64 vectors x 8)
 constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
+constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' codebooks
+constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
 
 struct LutArgs {
     const uint8_t *records;
@@ -145,12 +147,56 @@ __device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
     return U;
 }
 
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Codebook rows of one stage for both parts -> smem [part][256][8] (16 KiB), as
+// one cp.async group.
+__device__ __forceinline__ void issue_stage(float *dst, const float *cb_p0, const float *cb_p1, int s) {
+    for (int i = threadIdx.x; i < 1024; i += kThreads) {
+        const int part = i >> 9, ii = i & 511;
+        const float *src = (part ? cb_p1 : cb_p0) + (size_t)s * kCodes * kVec + (size_t)ii * 4;
+        cp_async16(dst + part * kCodes * kVec + ii * 4, src);
+    }
+    cp_async_commit();
+}
+
+template <bool kDown>
+__device__ __forceinline__ void unit_codebooks(const LutArgs &A, const Unit &U, const float *&p0,
+                                               const float *&p1) {
+    const int e = (U.e >= 0 && U.e < A.E) ? U.e : 0;
+    const float *cb_e = A.codebooks + (size_t)e * 3 * kCbFloats;
+    p0 = cb_e + (kDown ? 2 : 0) * kCbFloats;
+    p1 = cb_e + (kDown ? 2 : 1) * kCbFloats;
+}
+
+__device__ __forceinline__ float dot8s(const float *__restrict__ c, const float *xv) {
+    const float4 c0 = reinterpret_cast<const float4 *>(c)[0];
+    const float4 c1 = reinterpret_cast<const float4 *>(c)[1];
+    float t = c0.x * xv[0];
+    t = fmaf(c0.y, xv[1], t);
+    t = fmaf(c0.z, xv[2], t);
+    t = fmaf(c0.w, xv[3], t);
+    t = fmaf(c1.x, xv[4], t);
+    t = fmaf(c1.y, xv[5], t);
+    t = fmaf(c1.z, xv[6], t);
+    t = fmaf(c1.w, xv[7], t);
+    return t;
+}
+
 template <bool kDown, bool kRecon, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
     extern __shared__ __align__(16) unsigned char smem[];
-    // LUT variant: smem = tables [3][256][2][32] fp32 (192 KiB) + xs
-    // reconstruct variant: smem = codebooks [2][3][256][8] fp32 (48 KiB) + xs
-    float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kTabBytes));
+    // table variant: tables [3][256][2][32] fp32 (192 KiB) | 2 codebook stage buffers
+    //                [2][256][8] fp32 (2 x 16 KiB) | xs
+    // reconstruct variant: codebooks [2][3][256][8] fp32 (48 KiB) | xs
+    float *cbuf = reinterpret_cast<float *>(smem + kTabBytes);
+    float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kTabBytes + 2 * kStageBuf));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b4 = lane >> 4;
     const MatGeom &G = kDown ? A.dn : A.gu;
@@ -159,20 +205,29 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
     const uint32_t colb0 = ((uint32_t)(0 ^ b4) << 7) | ((uint32_t)lane << 2);
     const uint32_t colb1 = ((uint32_t)(1 ^ b4) << 7) | ((uint32_t)lane << 2);
 
+    int par = 0; // stage buffer holding the current unit's stage 0
+    if (!kRecon && (int)blockIdx.x < units) {
+        const Unit U0 = decode_unit<kDown>(A, blockIdx.x);
+        const float *p0, *p1;
+        unit_codebooks<kDown>(A, U0, p0, p1);
+        issue_stage(cbuf, p0, p1, 0);
+        issue_stage(cbuf + kStageFloats, p0, p1, 1);
+    }
+
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const Unit U = decode_unit<kDown>(A, u);
         const bool valid = U.base[0] != nullptr;
+        const bool has_next = u + (int)gridDim.x < units;
+        Unit N;
+        if (has_next) N = decode_unit<kDown>(A, u + gridDim.x);
         // warm L2 with the next unit's codes while this one builds its tables
-        if (warp == 0 && u + (int)gridDim.x < units) {
-            const Unit N = decode_unit<kDown>(A, u + gridDim.x);
+        if (warp == 0 && has_next) {
             for (int p = 0; p < 2; ++p)
                 if (N.base[p])
                     prefetch_l2_range(N.base[p] + (size_t)N.g0 * (kStages * 512),
                                       (size_t)(N.g1 - N.g0) * (kStages * 512), lane);
         }
-        if (!valid) {
-            if (threadIdx.x == 0) atomicOr(A.err, kErrBadExpert);
-        }
+        if (!valid && threadIdx.x == 0) atomicOr(A.err, kErrBadExpert);
         const int t = U.slot / A.k;
         // ---- input vectors of this lane's column(s)
         float xv[2][kVec];
@@ -216,43 +271,62 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
 #pragma unroll
             for (int v = 0; v < kVec; ++v) xr[p][v] = b4 ? xv[p ^ 1][v] : xv[p][v];
         __syncthreads(); // previous unit's lookups are done with the tables
-        const float *cb_e = A.codebooks + (size_t)(valid ? U.e : 0) * 3 * kCbFloats;
-        const float *cb_p0 = cb_e + (kDown ? 2 : 0) * kCbFloats;
-        const float *cb_p1 = cb_e + (kDown ? 2 : 1) * kCbFloats;
         if constexpr (!kRecon) {
-            // ---- tables T[s][c][part][lane]
+            // ---- tables T[s][c][part][lane], one stage at a time from the staged codebooks;
+            // the cp.async groups in flight are always the next two stage loads
             float *tab = reinterpret_cast<float *>(smem);
-            for (int combo = warp; combo < kStages * kCodes; combo += kWarps) {
-                const int s = combo >> 8, c = combo & 255;
-                const size_t o = (size_t)s * kCodes * kVec + (size_t)c * kVec;
-                const float t0 = valid ? dot8(cb_p0 + o, xv[0]) : 0.f;
-                const float t1 = valid ? dot8(cb_p1 + o, xv[1]) : 0.f;
-                tab[(size_t)combo * 64 + lane] = t0;
-                tab[(size_t)combo * 64 + 32 + lane] = t1;
+            const float *p0, *p1, *n0 = nullptr, *n1 = nullptr;
+            unit_codebooks<kDown>(A, U, p0, p1);
+            if (has_next) unit_codebooks<kDown>(A, N, n0, n1);
+#pragma unroll 1
+            for (int s = 0; s < kStages; ++s) {
+                if (s < 2 || has_next) cp_async_wait<1>();
+                else cp_async_wait<0>();
+                __syncthreads();
+                const float *buf = cbuf + ((s == 1) ? (par ^ 1) : par) * kStageFloats;
+                for (int c = warp; c < kCodes; c += kWarps) {
+                    const float t0 = valid ? dot8s(buf + c * kVec, xv[0]) : 0.f;
+                    const float t1 = valid ? dot8s(buf + kCodes * kVec + c * kVec, xv[1]) : 0.f;
+                    tab[((size_t)s * kCodes + c) * 64 + lane] = t0;
+                    tab[((size_t)s * kCodes + c) * 64 + 32 + lane] = t1;
+                }
+                __syncthreads(); // buffer consumed: refill it
+                if (s == 0) issue_stage(cbuf + par * kStageFloats, p0, p1, 2);
+                else if (s == 1 && has_next) issue_stage(cbuf + (par ^ 1) * kStageFloats, n0, n1, 0);
+                else if (s == 2 && has_next) issue_stage(cbuf + par * kStageFloats, n0, n1, 1);
             }
+            par ^= 1;
         } else {
             // ---- codebooks of both parts [2][3][256][8]
+            const float *p0, *p1;
+            unit_codebooks<kDown>(A, U, p0, p1);
             float4 *cbs = reinterpret_cast<float4 *>(smem);
             for (int i = threadIdx.x; i < 2 * kCbFloats / 4; i += kThreads) {
-                const float *src = (i < kCbFloats / 4) ? cb_p0 : cb_p1;
+                const float *src = (i < kCbFloats / 4) ? p0 : p1;
                 const int ii = i % (kCbFloats / 4);
                 cbs[i] = __ldg(reinterpret_cast<const float4 *>(src) + ii);
             }
+            __syncthreads();
         }
-        __syncthreads();
 
-        // ---- stream the codes of rows [g0, g1) x this unit's segment(s)
+        // ---- stream the codes of rows [g0, g1) x this unit's segment(s); the next row
+        // group's codes are loaded before the current one is consumed
         const uint8_t *pb0 = b4 ? U.base[1] : U.base[0];
         const uint8_t *pb1 = b4 ? U.base[0] : U.base[1];
         const unsigned char *tabb = smem;
-        for (int g = U.g0 + warp; g < U.g1; g += kWarps) {
-            uint4 cw[2][kStages];
+        uint4 cw[2][kStages], nw[2][kStages];
+        auto load = [&](int g, uint4 (&w)[2][kStages]) {
 #pragma unroll
             for (int s = 0; s < kStages; ++s) {
                 const size_t co = ((size_t)g * kStages + s) * 512 + (size_t)lane * 16;
-                cw[0][s] = pb0 ? __ldg(reinterpret_cast<const uint4 *>(pb0 + co)) : make_uint4(0, 0, 0, 0);
-                cw[1][s] = pb1 ? __ldg(reinterpret_cast<const uint4 *>(pb1 + co)) : make_uint4(0, 0, 0, 0);
+                w[0][s] = pb0 ? __ldg(reinterpret_cast<const uint4 *>(pb0 + co)) : make_uint4(0, 0, 0, 0);
+                w[1][s] = pb1 ? __ldg(reinterpret_cast<const uint4 *>(pb1 + co)) : make_uint4(0, 0, 0, 0);
             }
+        };
+        int g = U.g0 + warp;
+        if (g < U.g1) load(g, cw);
+        for (; g < U.g1; g += kWarps) {
+            if (g + kWarps < U.g1) load(g + kWarps, nw);
             float acc[32];
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
@@ -308,6 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
                 if (lane < 16 && row < G.n_out)
                     A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = v;
             }
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+                for (int s = 0; s < kStages; ++s) cw[p][s] = nw[p][s];
         }
         // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
         // and the slot's codebooks once
@@ -325,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
                           (unsigned long long)(kDown ? 1 : 2) * kCbFloats * sizeof(float));
         }
     }
+    if constexpr (!kRecon) cp_async_wait<0>();
 }
 
 // out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair]
@@ -353,7 +432,7 @@ __global__ void combine_kernel(const float *__restrict__ part_dn, const int32_t 
 
 template <bool kDown, bool kRecon, bool kBf16>
 cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
-    const size_t smem = (kRecon ? 2 * kCbFloats * 4 : kTabBytes) + kXsFloats * 4;
+    const size_t smem = (kRecon ? 2 * kCbFloats * 4 : kTabBytes + 2 * kStageBuf) + kXsFloats * 4;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(lut_kernel<kDown, kRecon, kBf16>,

@@ -34,6 +34,14 @@ __device__ __forceinline__ float load_h1(const void *h, size_t elem) {
     else return reinterpret_cast<const float *>(h)[elem];
 }
 
+// hi + lo == a + b exactly (Knuth's TwoSum); keeps the part of the dot product
+// that adding a large bias would round away, so gate ratios stay accurate.
+__device__ __forceinline__ void two_sum(float a, float b, float &hi, float &lo) {
+    hi = __fadd_rn(a, b);
+    const float bb = __fsub_rn(hi, a);
+    lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
+}
+
 // Small-T router: 4 experts per CTA, 4 warps per expert row (each takes every
 // 4th float4 of the row), up to 8 tokens per pass sharing each W_r load.
 constexpr int kRouterRows = 4;
@@ -44,7 +52,8 @@ __global__ void __launch_bounds__(512) router_small_kernel(const float *__restri
                                                            const float *__restrict__ bias,
                                                            const void *__restrict__ h, int T,
                                                            int E, int d,
-                                                           float *__restrict__ logits) {
+                                                           float *__restrict__ logits,
+                                                           float *__restrict__ logits_lo) {
     __shared__ float red[kRouterRows][4][kRouterTok];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_local = warp >> 2, sub = warp & 3;
@@ -84,8 +93,10 @@ __global__ void __launch_bounds__(512) router_small_kernel(const float *__restri
             const int r = blockIdx.x * kRouterRows + rl;
             if (r < E && t < nt) {
                 float v = ((red[rl][0][t] + red[rl][1][t]) + red[rl][2][t]) + red[rl][3][t];
-                if (bias) v += bias[r];
-                logits[(size_t)(t0 + t) * E + r] = v;
+                float hi = v, lo = 0.f;
+                if (bias) two_sum(v, bias[r], hi, lo);
+                logits[(size_t)(t0 + t) * E + r] = hi;
+                if (logits_lo) logits_lo[(size_t)(t0 + t) * E + r] = lo;
             }
         }
         __syncthreads();
@@ -101,7 +112,8 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const float *__restri
                                                            const float *__restrict__ bias,
                                                            const void *__restrict__ h, int T,
                                                            int E, int d,
-                                                           float *__restrict__ logits) {
+                                                           float *__restrict__ logits,
+                                                           float *__restrict__ logits_lo) {
     __shared__ float Hs[kTileK][kTileT + 4];
     __shared__ float Ws[kTileK][kTileE + 4];
     const int t0 = blockIdx.y * kTileT, e0 = blockIdx.x * kTileE;
@@ -142,19 +154,29 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const float *__restri
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             const int e = e0 + tx * 4 + b;
-            if (e < E) logits[(size_t)t * E + e] = acc[a][b] + (bias ? bias[e] : 0.f);
+            if (e < E) {
+                float hi = acc[a][b], lo = 0.f;
+                if (bias) two_sum(acc[a][b], bias[e], hi, lo);
+                logits[(size_t)t * E + e] = hi;
+                if (logits_lo) logits_lo[(size_t)t * E + e] = lo;
+            }
         }
     }
 }
 
-// (value, index) order used for routing: larger value first, lower index on ties.
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-    return va > vb || (va == vb && ia < ib);
+// Routing order: larger logit first (hi, then the exact remainder lo), lower
+// index on ties.
+__device__ __forceinline__ bool ranks_before(float ha, float la, int ia, float hb, float lb, int ib) {
+    if (ha != hb) return ha > hb;
+    if (la != lb) return la > lb;
+    return ia < ib;
 }
 
 // One warp per token.  Logits staged in shared memory; k rounds of a warp
-// arg-max that skips taken experts.
-__global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logits, int E, int k,
+// arg-max that skips taken experts; softmax over the k selected logits with
+// the differences taken as (hi_i - hi_0) + (lo_i - lo_0).
+__global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logits,
+                                                  const float *__restrict__ logits_lo, int E, int k,
                                                   int32_t *__restrict__ idx,
                                                   float *__restrict__ gate,
                                                   const int32_t *__restrict__ pred_idx,
@@ -164,50 +186,54 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
                                                   unsigned long long router_bytes) {
     extern __shared__ float smem_topk[];
     float *lv = smem_topk;
-    unsigned char *taken = reinterpret_cast<unsigned char *>(lv + E);
+    float *lw = lv + E;
+    unsigned char *taken = reinterpret_cast<unsigned char *>(lw + E);
     const int t = blockIdx.x, lane = threadIdx.x;
     for (int e = lane; e < E; e += 32) {
         lv[e] = logits[(size_t)t * E + e];
+        lw[e] = logits_lo ? logits_lo[(size_t)t * E + e] : 0.f;
         taken[e] = 0;
     }
     __syncwarp();
+    constexpr int kNone = 0x7fffffff;
     int my_idx = -1;
-    float my_val = 0.f;
+    float my_hi = 0.f, my_lo = 0.f;
     for (int r = 0; r < k; ++r) {
-        float bv = -FLT_MAX;
-        int bi = 0x7fffffff;
-        bool have = false;
+        float bh = 0.f, bl = 0.f;
+        int bi = kNone;
         for (int e = lane; e < E; e += 32) {
             if (taken[e]) continue;
-            float v = lv[e];
-            if (!have || ranks_before(v, e, bv, bi)) {
-                bv = v;
+            const float vh = lv[e], vl = lw[e];
+            if (bi == kNone || ranks_before(vh, vl, e, bh, bl, bi)) {
+                bh = vh;
+                bl = vl;
                 bi = e;
-                have = true;
             }
         }
-        if (!have) bi = 0x7fffffff;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            bool other_valid = oi != 0x7fffffff;
-            bool mine_valid = bi != 0x7fffffff;
-            if (other_valid && (!mine_valid || ranks_before(ov, oi, bv, bi))) {
-                bv = ov;
+            const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
+            const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != kNone && (bi == kNone || ranks_before(oh, ol, oi, bh, bl, bi))) {
+                bh = oh;
+                bl = ol;
                 bi = oi;
             }
         }
-        if (bi != 0x7fffffff && lane == (bi & 31)) taken[bi] = 1;
+        if (bi != kNone && lane == (bi & 31)) taken[bi] = 1;
         if (lane == r) {
             my_idx = bi;
-            my_val = bv;
+            my_hi = bh;
+            my_lo = bl;
         }
         __syncwarp();
     }
     // softmax over the selected logits; rank 0 holds the largest
-    const float lmax = __shfl_sync(0xffffffffu, my_val, 0);
-    float ex = (lane < k) ? expf(my_val - lmax) : 0.f;
+    const float h0 = __shfl_sync(0xffffffffu, my_hi, 0);
+    const float l0 = __shfl_sync(0xffffffffu, my_lo, 0);
+    const float diff = (lane == 0) ? 0.f : __fsub_rn(my_hi, h0) + __fsub_rn(my_lo, l0);
+    float ex = (lane < k) ? expf(diff) : 0.f;
     float sum = ex;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -265,36 +291,36 @@ __global__ void set_count_kernel(int32_t *count, int T, int P) {
 } // namespace
 
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
-                          cudaStream_t s) {
+                          float *logits_lo, cudaStream_t s) {
     if (T <= 16) {
         dim3 grid((L.E + kRouterRows - 1) / kRouterRows);
         if (L.act_bf16)
-            router_small_kernel<true><<<grid, 512, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits);
+            router_small_kernel<true><<<grid, 512, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
         else
-            router_small_kernel<false><<<grid, 512, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits);
+            router_small_kernel<false><<<grid, 512, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
     } else {
         dim3 grid((L.E + kTileE - 1) / kTileE, (T + kTileT - 1) / kTileT);
         if (L.act_bf16)
-            router_tiled_kernel<true><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits);
+            router_tiled_kernel<true><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
         else
-            router_tiled_kernel<false><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits);
+            router_tiled_kernel<false><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float *logits, int T, int E, int k, int32_t *idx, float *gate,
-                        const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
-                        unsigned long long *stats, unsigned long long router_bytes,
-                        cudaStream_t s) {
-    const size_t smem = (size_t)E * sizeof(float) + (size_t)E;
+cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int E, int k,
+                        int32_t *idx, float *gate, const int32_t *pred_idx, int32_t *pred_count,
+                        int pred_stride, unsigned long long *stats,
+                        unsigned long long router_bytes, cudaStream_t s) {
+    const size_t smem = (size_t)E * 2 * sizeof(float) + (size_t)E;
     static bool attr_set = false;
     if (!attr_set) {
         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)kMaxExperts * 5));
+                             (int)((size_t)kMaxExperts * 9));
         attr_set = true;
     }
-    topk_kernel<<<T, 32, smem, s>>>(logits, E, k, idx, gate, pred_idx, pred_count, pred_stride,
-                                    stats, router_bytes);
+    topk_kernel<<<T, 32, smem, s>>>(logits, logits_lo, E, k, idx, gate, pred_idx, pred_count,
+                                    pred_stride, stats, router_bytes);
     return cudaGetLastError();
 }
 

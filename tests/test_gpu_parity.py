@@ -63,7 +63,7 @@ def check_routing(g_idx, g_gate, ref_logits, k):
         ridx, rg = oracle.topk_softmax(l, k)
         if oracle.topk_margin(l, k) > tau:
             np.testing.assert_array_equal(g_idx[t], ridx, err_msg=f"token {t}")
-            np.testing.assert_allclose(g_gate[t], rg, rtol=2e-6, atol=2e-7)
+            np.testing.assert_allclose(g_gate[t], rg, rtol=1e-5, atol=1e-7)
             ok_tokens.append(t)
         else:
             kth = np.sort(l)[::-1][k - 1]
@@ -324,7 +324,7 @@ def test_decode_layer_full_size(seed):
         assert oracle.topk_margin(ref["logits"], w.top_k) > 1e-3
         np.testing.assert_allclose(g_logits[0], ref["logits"], rtol=1e-5, atol=1e-4)
         np.testing.assert_array_equal(g_idx[0], ref["idx"])
-        np.testing.assert_allclose(g_gate[0], ref["gate"], rtol=2e-6, atol=2e-7)
+        np.testing.assert_allclose(g_gate[0], ref["gate"], rtol=1e-5, atol=1e-7)
         assert_close(g_out[0], ref["out"])
         # reconstruct variant on the same weights gives the same answer within tolerance
         st = layer.stats()
