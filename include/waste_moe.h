@@ -250,6 +250,12 @@ const char *waste_moe_last_error(void);
 int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int32_t k,
                                int32_t *d_idx, float *d_gate, waste_stream_t stream);
 
+/* Weightless RMS normalisation of T rows of d floats: out = in / sqrt(mean(in^2) + 1e-6)
+ * (out may equal in).  Not one of the pages' operations: it stands in for the
+ * normalisation a model's trunk applies to each MoE layer's input, so that a stack of
+ * layers driven by h += combine keeps its inputs at unit scale. */
+int waste_moe_rmsnorm(const float *d_in, float *d_out, int32_t T, int32_t d, waste_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

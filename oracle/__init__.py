@@ -57,6 +57,7 @@ def _bind(lib):
     lib.oracle_combine.argtypes = [_i, _i, _dp, _dp, _dp, _dp]
     lib.oracle_moe_layer.argtypes = [_i, _i, _i, _i, _i, _fp, _fp, _fp, _u8p, _u8p, _u8p,
                                      _dp, _i, _i, _dp, _dp, _i32p, _dp]
+    lib.oracle_rmsnorm.argtypes = [_i, _dp, _dp]
     lib.oracle_expert_code_bytes.argtypes = [_i, _i]
     lib.oracle_expert_code_bytes.restype = ctypes.c_uint64
     return lib
@@ -170,6 +171,31 @@ def combine(gate, ys, base=None):
                            None if b is None else _ptr(b, ctypes.c_double),
                            _ptr(out, ctypes.c_double))
     return out
+
+
+def rmsnorm(x):
+    """x / sqrt(mean(x^2) + 1e-6) of one row (float64)."""
+    x = _np(x, np.float64)
+    out = np.empty_like(x)
+    _load().oracle_rmsnorm(x.shape[0], _ptr(x, ctypes.c_double), _ptr(out, ctypes.c_double))
+    return out
+
+
+def stack_chain(h0, layers, k, n_layers=None):
+    """Decode chain h <- h + MoE_L(rmsnorm(h)) over the given layers, per token.
+
+    layers: list of (Wr, bias, cbs, codes) with codes = (gate, up, down) for all experts.
+    Returns (final h [T,d], list of idx [T,k] per layer, list of logits [T,E] per layer).
+    """
+    h = _np(h0, np.float64).copy()
+    idxs, logits = [], []
+    for L, (Wr, bias, cbs, codes) in enumerate(layers[:n_layers]):
+        x = np.stack([rmsnorm(h[t]) for t in range(h.shape[0])])
+        r = moe_layer(x, Wr, bias, cbs, codes, k)
+        h = h + r["out"]
+        idxs.append(r["idx"])
+        logits.append(r["logits"])
+    return h, idxs, logits
 
 
 def expert_code_bytes(d: int, f: int) -> int:

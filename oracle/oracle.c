@@ -236,6 +236,19 @@ void oracle_moe_layer(int T, int d, int f, int n_experts, int k, const float *Wr
 }
 
 /*
+ * Weightless RMS normalisation out = in / sqrt(mean(in^2) + 1e-6).  Not one of
+ * the pages' operations: it stands in for the trunk's normalisation of each
+ * MoE layer's input when layers are chained as h <- h + MoE(norm(h)) (the
+ * plain chain h <- h + MoE(h) diverges at the test workloads' scales).
+ */
+void oracle_rmsnorm(int d, const double *in, double *out) {
+    double ss = 0.0;
+    for (int i = 0; i < d; ++i) ss += in[i] * in[i];
+    double scale = 1.0 / sqrt(ss / (double)d + 1e-6);
+    for (int i = 0; i < d; ++i) out[i] = in[i] * scale;
+}
+
+/*
  * Bytes of codes per expert: 3 matrices (gate, up, down) of d*f weights at
  * 3 stages x 1 byte per 8 weights = 3.00 bits per weight ([fr]
  * "Quantification et exactitude").

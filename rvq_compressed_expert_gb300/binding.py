@@ -31,7 +31,8 @@ STATUS = {0: "WASTE_OK", -1: "WASTE_EINVAL", -2: "WASTE_ENOMEM", -3: "WASTE_ECUD
 EXPORTED = ["waste_moe_record_layout", "waste_moe_pack_records", "waste_moe_create",
             "waste_moe_route", "waste_moe_forward", "waste_moe_prefetch", "waste_moe_destroy",
             "waste_moe_stats", "waste_moe_reset_stats", "waste_moe_last_error",
-            "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile"]
+            "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile",
+            "waste_moe_rmsnorm"]
 
 
 class waste_moe_config(ctypes.Structure):
@@ -95,6 +96,7 @@ def load(path: str = LIB_PATH):
     lib.waste_moe_topk_from_logits.argtypes = [vp, i32, i32, i32, vp, vp, vp]
     lib.waste_moe_set_profiling.argtypes = [vp, i32]
     lib.waste_moe_read_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_float)]
+    lib.waste_moe_rmsnorm.argtypes = [vp, vp, i32, i32, vp]
     for name in EXPORTED:
         if name not in ("waste_moe_destroy", "waste_moe_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -202,6 +204,10 @@ def waste_moe_read_profile(h) -> dict:
     ms = (ctypes.c_float * 5)()
     _check(load().waste_moe_read_profile(h, ms))
     return dict(zip(("router", "topk", "gate_up", "down", "combine"), list(ms)))
+
+
+def waste_moe_rmsnorm(d_in, d_out, T, d, stream=None):
+    return _check(load().waste_moe_rmsnorm(_ptr(d_in), _ptr(d_out), T, d, _stream(stream)))
 
 
 def aligned_bytes(nbytes: int, device="cuda", align: int = RECORD_ALIGN) -> torch.Tensor:

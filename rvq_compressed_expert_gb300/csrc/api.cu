@@ -454,4 +454,13 @@ int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int3
     return ok();
 }
 
+int waste_moe_rmsnorm(const float *d_in, float *d_out, int32_t T, int32_t d, waste_stream_t stream) {
+    if (T < 0 || d < 1) return fail(WASTE_EINVAL, "T = %d, d = %d out of range", T, d);
+    if (T == 0) return ok();
+    if (!d_in || !d_out) return fail(WASTE_EINVAL, "NULL pointer");
+    cudaError_t e = launch_rmsnorm(d_in, d_out, T, d, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "rmsnorm kernel");
+    return ok();
+}
+
 } // extern "C"

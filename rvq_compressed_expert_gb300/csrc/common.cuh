@@ -114,6 +114,8 @@ cudaError_t launch_pack(const MatGeom &gu, const MatGeom &dn, int n_experts,
 cudaError_t launch_headers(uint8_t *records, size_t stride, int n, const waste_record_header &hdr,
                            int expert_begin, cudaStream_t s);
 
+cudaError_t launch_rmsnorm(const float *in, float *out, int T, int d, cudaStream_t s);
+
 int device_sm_count();
 
 } // namespace wm

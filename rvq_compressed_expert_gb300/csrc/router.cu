@@ -190,8 +190,15 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
     unsigned char *taken = reinterpret_cast<unsigned char *>(lw + E);
     const int t = blockIdx.x, lane = threadIdx.x;
     for (int e = lane; e < E; e += 32) {
-        lv[e] = logits[(size_t)t * E + e];
-        lw[e] = logits_lo ? logits_lo[(size_t)t * E + e] : 0.f;
+        // canonical keys make the order total: -0 equals +0, and a NaN (outside the
+        // contract) ranks as -inf, so every lane agrees on each round's winner
+        float vh = logits[(size_t)t * E + e];
+        float vl = logits_lo ? logits_lo[(size_t)t * E + e] : 0.f;
+        if (vh != vh) vh = -INFINITY;
+        if (vh == 0.f) vh = 0.f;
+        if (vl != vl || vl == 0.f) vl = 0.f;
+        lv[e] = vh;
+        lw[e] = vl;
         taken[e] = 0;
     }
     __syncwarp();
@@ -283,6 +290,29 @@ __global__ void __launch_bounds__(128) prefetch_l2_kernel(const uint8_t *__restr
     }
 }
 
+// Weightless RMS normalisation of one token per CTA: out = in / sqrt(mean(in^2) + 1e-6),
+// with the sum of squares reduced in a fixed order.
+__global__ void __launch_bounds__(1024) rmsnorm_kernel(const float *__restrict__ in,
+                                                       float *__restrict__ out, int d) {
+    __shared__ float part[32];
+    const float *x = in + (size_t)blockIdx.x * d;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.f;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (threadIdx.x == 0) part[0] = v;
+    }
+    __syncthreads();
+    const float scale = 1.0f / sqrtf(part[0] / (float)d + 1e-6f);
+    for (int i = threadIdx.x; i < d; i += blockDim.x) out[(size_t)blockIdx.x * d + i] = x[i] * scale;
+}
+
 __global__ void set_count_kernel(int32_t *count, int T, int P) {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t < T) count[t] = P;
@@ -321,6 +351,11 @@ cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int 
     }
     topk_kernel<<<T, 32, smem, s>>>(logits, logits_lo, E, k, idx, gate, pred_idx, pred_count,
                                     pred_stride, stats, router_bytes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float *in, float *out, int T, int d, cudaStream_t s) {
+    rmsnorm_kernel<<<T, 1024, 0, s>>>(in, out, d);
     return cudaGetLastError();
 }
 

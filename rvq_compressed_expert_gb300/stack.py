@@ -1,0 +1,63 @@
+"""Decode through a stack of MoE layers with the pages' router lookahead.
+
+Per layer L, for one batch of tokens with residual h_L (page "Exécuter Kimi K3
+avec 29 Go de RAM à 0,50 tok/s", section "Lecture anticipée et prédiction du
+routeur"):
+  - x_L = rmsnorm(h_L)  (stand-in for the trunk's normalisation of the MoE
+    input; without it the chain h <- h + MoE(h) diverges at these scales),
+  - on a side stream, layer L+1's router runs on x_L and its top-P experts are
+    prefetched into L2 (waste_moe_prefetch),
+  - on the main stream layer L routes x_L and applies its experts:
+    h_{L+1} = h_L + combine (waste_moe_forward, mode 1, in place).
+The real router of each layer decides its experts, so the lookahead changes
+neither the outputs nor the demand bytes.  x alternates between two buffers so
+the side stream can still read x_L while x_{L+1} is written; layer L+1 routes
+only after its prefetch has finished (an event), which also keeps the next
+write of x_L's buffer behind the read.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class DecodeStack:
+    def __init__(self, layers, tokens: int, device="cuda"):
+        self.layers = layers
+        self.T = tokens
+        w = layers[0].w
+        self.d = w.d
+        self.h = torch.empty(tokens, w.d, dtype=torch.float32, device=device)
+        self.x = [torch.empty(tokens, w.d, dtype=torch.float32, device=device) for _ in range(2)]
+        self.idx = torch.empty(tokens, w.top_k, dtype=torch.int32, device=device)
+        self.gate = torch.empty(tokens, w.top_k, dtype=torch.float32, device=device)
+
+    def run(self, h0: torch.Tensor, lookahead: int, main: torch.cuda.Stream,
+            side: torch.cuda.Stream | None = None, on_layer=None) -> torch.Tensor:
+        """Enqueue one pass of h0 [T, d] fp32 through every layer on `main` (and `side` for
+        the lookahead); returns the buffer that holds the output once `main` is done."""
+        n = len(self.layers)
+        T = self.T
+        with torch.cuda.stream(main):
+            self.h.copy_(h0)
+        pending = None
+        for L in range(n):
+            x = self.x[L & 1]
+            B.waste_moe_rmsnorm(self.h, x, T, self.d, main)
+            ev = None
+            if lookahead and L + 1 < n:
+                side.wait_stream(main)  # x_L is ready
+                self.layers[L + 1].prefetch(x, T, lookahead, stream=side)
+                ev = torch.cuda.Event()
+                ev.record(side)
+            if pending is not None:
+                main.wait_event(pending)  # layer L's prediction is in place before it routes
+            self.layers[L].route(x, T, self.idx, self.gate, stream=main)
+            if on_layer is not None:
+                on_layer(L, self.idx, self.gate, main)
+            self.layers[L].forward(x, T, self.idx, self.gate, self.h, 1, stream=main)
+            pending = ev
+        if pending is not None:
+            main.wait_event(pending)
+        return self.h

@@ -272,4 +272,18 @@ def pin_code_bytes_match_pages():
     assert abs(16 * 92 * b / 2 ** 30 - 17.0) < 0.05
 
 
+def pin_rmsnorm():
+    """RMS normalisation: a constant vector c maps to sign(c) (up to the 1e-6 floor), the
+    output's mean square is 1 up to the floor, and scaling the input does not change it."""
+    for c in (3.0, -0.5):
+        out = oracle.rmsnorm(np.full(16, c))
+        np.testing.assert_allclose(out, np.sign(c) * abs(c) / math.sqrt(c * c + 1e-6), rtol=1e-14)
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal(100) * 5
+    out = oracle.rmsnorm(x)
+    ms = float(np.mean(x * x))
+    assert abs(float(np.mean(out * out)) - ms / (ms + 1e-6)) < 1e-13
+    np.testing.assert_allclose(oracle.rmsnorm(4 * x), out, rtol=1e-7)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

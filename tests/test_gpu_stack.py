@@ -1,0 +1,146 @@
+"""The decode stack with router lookahead: outputs and demand bytes do not depend on
+the lookahead, graph replay equals eager launches, and the chain matches the oracle.
+
+The pages state that the lookahead leaves the output exact (the real router still
+decides) and leaves the total bytes read unchanged (page "Exécuter Kimi K3 avec 29
+Go de RAM à 0,50 tok/s", section "Lecture anticipée et prédiction du routeur").
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rvq_compressed_expert_gb300 import binding as B
+from rvq_compressed_expert_gb300 import synth
+from rvq_compressed_expert_gb300.layer import MoELayer
+from rvq_compressed_expert_gb300.stack import DecodeStack
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rvq_compressed_expert_gb300 import _build
+    _build.build()
+    B.load()
+    oracle.build()
+
+
+SMALL = synth.Workload("small-stack", 512, 256, 16, 4, 2, "f32", "offsets", n_layers=6, lookahead=3)
+
+
+def make_layers(w, seed=0, device="cuda"):
+    layers = []
+    for L in range(w.n_layers):
+        li = synth.layer_inputs(w, seed, L, "cpu", with_codes=True)
+        layers.append((MoELayer(w, seed, L, device, inputs=li), li))
+    return layers
+
+
+def run_eager(stack, h0, P, record=None):
+    main = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    main.wait_stream(torch.cuda.current_stream())
+    out = stack.run(h0, P, main, side, on_layer=record)
+    torch.cuda.current_stream().wait_stream(main)
+    torch.cuda.synchronize()
+    return out.clone()
+
+
+def test_stack_lookahead_invariant_and_matches_oracle():
+    w = SMALL
+    pairs = make_layers(w)
+    layers = [p[0] for p in pairs]
+    try:
+        h0 = synth.hidden(3, w.tokens, w.d, "f32", "cpu")
+        hd = h0.cuda()
+        stack = DecodeStack(layers, w.tokens)
+        routed = {}
+
+        def record(L, idx, gate, main):
+            with torch.cuda.stream(main):
+                routed[L] = idx.clone()
+
+        outs = {}
+        for P in (0, w.lookahead):
+            for l in layers:
+                l.reset_stats()
+            outs[P] = run_eager(stack, hd, P, record if P == 0 else None)
+            sts = [l.stats() for l in layers]
+            outs[(P, "bytes")] = sum(s["demand_code_bytes"] for s in sts)
+            outs[(P, "hits")] = sum(s["prediction_hits"] for s in sts)
+            outs[(P, "prefetch")] = sum(s["prefetch_experts"] for s in sts)
+        assert torch.equal(outs[0], outs[w.lookahead]), "lookahead changed the output"
+        assert outs[(0, "bytes")] == outs[(w.lookahead, "bytes")]
+        assert outs[(0, "bytes")] == w.n_layers * w.tokens * w.top_k * oracle.expert_code_bytes(w.d, w.f)
+        assert outs[(w.lookahead, "prefetch")] == (w.n_layers - 1) * w.tokens * w.lookahead
+        assert outs[(0, "prefetch")] == 0 and outs[(0, "hits")] == 0
+        # the oracle runs the same chain from h0 on its own
+        ref_h, ref_idx, ref_logits = oracle.stack_chain(
+            h0, [(li.router_w, li.router_b, li.codebooks, li.codes) for _, li in pairs], w.top_k)
+        for L in range(w.n_layers):
+            for t in range(w.tokens):
+                assert oracle.topk_margin(ref_logits[L][t], w.top_k) > 1e-3
+            np.testing.assert_array_equal(routed[L].cpu().numpy(), ref_idx[L], err_msg=f"layer {L}")
+        got = outs[0].cpu().double().numpy()
+        rel = np.linalg.norm(got - ref_h) / np.linalg.norm(ref_h)
+        assert rel < 1e-5, rel
+    finally:
+        for l in layers:
+            l.close()
+
+
+def test_topk_survives_nonfinite_logits():
+    """NaN and infinite logits (outside the contract) still give k distinct valid indices."""
+    L = np.array([[np.nan, 1.0, np.inf, -np.inf, np.nan, 0.5, np.nan, -1.0] * 8], np.float32)
+    for k in (1, 4, 16, 32):
+        dl = torch.tensor(L).cuda()
+        idx = torch.empty(1, k, dtype=torch.int32, device="cuda")
+        gate = torch.empty(1, k, dtype=torch.float32, device="cuda")
+        B.waste_moe_topk_from_logits(dl, 1, L.shape[1], k, idx, gate)
+        torch.cuda.synchronize()
+        got = idx[0].cpu().numpy()
+        assert len(set(got.tolist())) == k
+        assert got.min() >= 0 and got.max() < L.shape[1]
+
+
+def test_rmsnorm_matches_oracle():
+    x = torch.randn(5, 1032, generator=torch.Generator().manual_seed(0)) * 7
+    y = torch.empty_like(x).cuda()
+    B.waste_moe_rmsnorm(x.cuda(), y, 5, 1032)
+    torch.cuda.synchronize()
+    for t in range(5):
+        ref = oracle.rmsnorm(x[t])
+        np.testing.assert_allclose(y[t].cpu().numpy(), ref, rtol=2e-6, atol=1e-7)
+
+
+def test_stack_graph_replay_equals_eager():
+    w = SMALL
+    pairs = make_layers(w, seed=1)
+    layers = [p[0] for p in pairs]
+    try:
+        hd = synth.hidden(4, w.tokens, w.d, "f32", "cpu").cuda()
+        stack = DecodeStack(layers, w.tokens)
+        ref = run_eager(stack, hd, w.lookahead)
+        for P in (0, w.lookahead):
+            main = torch.cuda.Stream()
+            side = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=main):
+                out = stack.run(hd, P, main, side)
+            for l in layers:
+                l.reset_stats()
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref), f"graph replay differs (lookahead {P})"
+            sts = [l.stats() for l in layers]  # raises if a kernel saw a bad expert index
+            assert sum(s["forward_slots"] for s in sts) == 3 * w.n_layers * w.tokens * w.top_k
+            if P:
+                assert sum(s["prefetch_experts"] for s in sts) == 3 * (w.n_layers - 1) * w.tokens * P
+            del g
+    finally:
+        for l in layers:
+            l.close()

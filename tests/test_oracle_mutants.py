@@ -33,6 +33,8 @@ MUTANTS = {
                           "acc += (double)Wr[(size_t)(i % n_experts) * d + (e % d)] * h[i];"),
     "dense_transposed": ("acc += W[(size_t)r * n_in + i] * x[i];",
                          "acc += W[(size_t)(i % n_out) * n_in + (r % n_in)] * x[i];"),
+    "rmsnorm_no_mean": ("double scale = 1.0 / sqrt(ss / (double)d + 1e-6);",
+                        "double scale = 1.0 / sqrt(ss + 1e-6);"),
     "code_bytes_wrong": ("return (uint64_t)3 * (uint64_t)OR_STAGES", "return (uint64_t)2 * (uint64_t)OR_STAGES"),
 }
 
