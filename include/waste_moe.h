@@ -256,6 +256,34 @@ int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int3
  * layers driven by h += combine keeps its inputs at unit scale. */
 int waste_moe_rmsnorm(const float *d_in, float *d_out, int32_t T, int32_t d, waste_stream_t stream);
 
+/* waste_moe_forward without a handle and without allocating anything.
+ *
+ * The pages have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory -- for example a host that only receives device pointers
+ * from an engine which owns all of the GPU's memory, or code running where
+ * cudaMalloc is not allowed.  It computes what waste_moe_forward computes for the
+ * same records, codebooks, hidden states, experts and gates, but keeps its
+ * partial sums in one fixed 8 MiB array inside the library's device image
+ * (every GPU that loads the library holds it until the process exits).
+ *   cfg          shapes and act_dtype (d, f, n_experts, top_k, act_dtype, flags as
+ *                for create; max_tokens, lookahead and layer are ignored)
+ *   d_records    bank of records, 4096-aligned; not re-validated here (validate
+ *                once, e.g. with waste_moe_create)
+ *   d_codebooks, d_h, d_idx, d_gate, d_out, mode: as for waste_moe_forward
+ * Limits: the T * top_k slots need (f * 2 * ceil(d/256) + d * ceil(f/512)) * 4 bytes
+ * of scratch each (about 0.43 MB at d = 7168, f = 1536, i.e. T * top_k <= 19 there);
+ * a call beyond 8 MiB in total is rejected with WASTE_EINVAL and launches nothing.
+ * No cudaMalloc, cudaFree or other allocating routine is called.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) once for that device; make that first call before any
+ * stream capture.  Every call shares the one array, so calls that overlap on the
+ * GPU (other streams, other threads) race and give wrong results: serialise them.
+ * An expert index outside [0, E) contributes zero; it is not reported here. */
+int waste_moe_forward_noalloc(const waste_moe_config *cfg, const uint8_t *d_records,
+                              size_t record_stride, const float *d_codebooks, const void *d_h,
+                              int32_t T, const int32_t *d_idx, const float *d_gate, float *d_out,
+                              int32_t mode, waste_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

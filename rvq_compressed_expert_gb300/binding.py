@@ -32,7 +32,7 @@ EXPORTED = ["waste_moe_record_layout", "waste_moe_pack_records", "waste_moe_crea
             "waste_moe_route", "waste_moe_forward", "waste_moe_prefetch", "waste_moe_destroy",
             "waste_moe_stats", "waste_moe_reset_stats", "waste_moe_last_error",
             "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile",
-            "waste_moe_rmsnorm"]
+            "waste_moe_rmsnorm", "waste_moe_forward_noalloc"]
 
 
 class waste_moe_config(ctypes.Structure):
@@ -97,6 +97,7 @@ def load(path: str = LIB_PATH):
     lib.waste_moe_set_profiling.argtypes = [vp, i32]
     lib.waste_moe_read_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_float)]
     lib.waste_moe_rmsnorm.argtypes = [vp, vp, i32, i32, vp]
+    lib.waste_moe_forward_noalloc.argtypes = [cfgp, vp, sz, vp, vp, i32, vp, vp, vp, i32, vp]
     for name in EXPORTED:
         if name not in ("waste_moe_destroy", "waste_moe_last_error"):
             getattr(lib, name).restype = ctypes.c_int
@@ -208,6 +209,14 @@ def waste_moe_read_profile(h) -> dict:
 
 def waste_moe_rmsnorm(d_in, d_out, T, d, stream=None):
     return _check(load().waste_moe_rmsnorm(_ptr(d_in), _ptr(d_out), T, d, _stream(stream)))
+
+
+def waste_moe_forward_noalloc(cfg, records, record_stride, codebooks, d_h, T, d_idx, d_gate, d_out,
+                              mode=0, stream=None):
+    """waste_moe_forward without a handle; its scratch is a fixed 8 MiB device array."""
+    return _check(load().waste_moe_forward_noalloc(
+        ctypes.byref(cfg), _ptr(records), record_stride, _ptr(codebooks), _ptr(d_h), T,
+        _ptr(d_idx), _ptr(d_gate), _ptr(d_out), mode, _stream(stream)))
 
 
 def aligned_bytes(nbytes: int, device="cuda", align: int = RECORD_ALIGN) -> torch.Tensor:

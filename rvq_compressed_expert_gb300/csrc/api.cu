@@ -82,6 +82,8 @@ void layout(const waste_moe_config *c, size_t *stride, size_t off[3], size_t byt
 } // namespace
 
 namespace wm {
+void set_last_error(const char *msg) { g_err = msg; }
+
 int device_sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
