@@ -536,6 +536,28 @@ def reference(args):
     print(json.dumps(line), flush=True)
 
 
+def profile_case(args):
+    """Small case for ncu captures: the decode step at full d, f and top-16 over 32 resident
+    experts (0.4 GB of records instead of 4.7 GB; the per-launch work is the same as the
+    full decode layer).  Runs `--warmup` then `--steps` plain launches, no timing."""
+    from rvq_compressed_expert_gb300 import _build
+    from rvq_compressed_expert_gb300 import binding as B
+    from rvq_compressed_expert_gb300 import synth
+    from rvq_compressed_expert_gb300.layer import MoELayer
+    _build.build()
+    B.load()
+    w = synth.Workload("decode-e32", 7168, 1536, 32, 16, 1, "f32", "offsets")
+    layer = MoELayer(w, seed=0, layer=0, device="cuda")
+    idx, gate, logits, y = layer.alloc_outputs(1)
+    for i in range(args.warmup + args.steps):
+        h = synth.hidden(100 + i, 1, w.d, "f32", "cuda")
+        layer.route(h, 1, idx, gate, logits)
+        layer.forward(h, 1, idx, gate, y, 0)
+    torch.cuda.synchronize()
+    layer.close()
+    print("profile case done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -544,9 +566,14 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run a small decode case for ncu captures and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.impl == "reference":
         reference(args)
     else:
