@@ -406,23 +406,43 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
     if constexpr (!kRecon) cp_async_wait<0>();
 }
 
-// out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair]
-__global__ void combine_kernel(const float *__restrict__ part_dn, const int32_t *__restrict__ idx,
-                               const float *__restrict__ gate, const float *__restrict__ h,
-                               float *__restrict__ out, int d, int k, int E, int npair,
-                               int mode, unsigned long long *stats, unsigned long long slots) {
+// out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair],
+// slots in rank order and pairs in order; the loads of 8 slots are issued together.
+__global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ part_dn,
+                                                      const int32_t *__restrict__ idx,
+                                                      const float *__restrict__ gate,
+                                                      const float *__restrict__ h,
+                                                      float *__restrict__ out, int d, int k, int E,
+                                                      int npair, int mode,
+                                                      unsigned long long *stats,
+                                                      unsigned long long slots) {
     const int t = blockIdx.y;
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (stats && r == 0 && t == 0) atomicAdd(stats + kStatForwardSlots, slots);
     if (r >= d) return;
     float y = 0.f;
-    for (int i = 0; i < k; ++i) {
-        const int e = idx[(size_t)t * k + i];
-        if (e < 0 || e >= E) continue;
-        const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
-        float s = 0.f;
-        for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
-        y = fmaf(gate[(size_t)t * k + i], s, y);
+    for (int i0 = 0; i0 < k; i0 += 8) {
+        float sv[8], gv[8];
+        bool ok[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u;
+            sv[u] = 0.f;
+            gv[u] = 0.f;
+            ok[u] = false;
+            if (i < k) {
+                const int e = idx[(size_t)t * k + i];
+                ok[u] = e >= 0 && e < E;
+                gv[u] = gate[(size_t)t * k + i];
+                const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
+                float s = 0.f;
+                for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
+                sv[u] = s;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (ok[u]) y = fmaf(gv[u], sv[u], y);
     }
     const size_t o = (size_t)t * d + r;
     if (mode == 0) out[o] = y;
@@ -499,8 +519,8 @@ cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const voi
     e = launch_var<true>(A, A.slots * A.npair * A.nrb, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[2], s);
-    dim3 grid((L.d + 255) / 256, T);
-    combine_kernel<<<grid, 256, 0, s>>>(W.part_dn, idx, gate, reinterpret_cast<const float *>(h), out,
+    dim3 grid((L.d + 127) / 128, T);
+    combine_kernel<<<grid, 128, 0, s>>>(W.part_dn, idx, gate, reinterpret_cast<const float *>(h), out,
                                         L.d, L.k, L.E, A.npair, mode, W.stats,
                                         (unsigned long long)A.slots);
     if (tm) {

@@ -42,13 +42,15 @@ __device__ __forceinline__ void two_sum(float a, float b, float &hi, float &lo) 
     lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
 }
 
-// Small-T router: 4 experts per CTA, 4 warps per expert row (each takes every
-// 4th float4 of the row), up to 8 tokens per pass sharing each W_r load.
-constexpr int kRouterRows = 4;
+// Small-T router: 2 experts per CTA, 4 warps per expert row (each takes every
+// 4th float4 of the row, 8 loads in flight per lane), up to 8 tokens per pass
+// sharing each W_r load.
+constexpr int kRouterRows = 2;
 constexpr int kRouterTok = 8;
+constexpr int kRouterBatch = 8;
 
 template <bool kBf16>
-__global__ void __launch_bounds__(512) router_small_kernel(const float *__restrict__ W,
+__global__ void __launch_bounds__(256) router_small_kernel(const float *__restrict__ W,
                                                            const float *__restrict__ bias,
                                                            const void *__restrict__ h, int T,
                                                            int E, int d,
@@ -59,6 +61,7 @@ __global__ void __launch_bounds__(512) router_small_kernel(const float *__restri
     const int row_local = warp >> 2, sub = warp & 3;
     const int row = blockIdx.x * kRouterRows + row_local;
     const int d4 = d >> 2;
+    const int per_lane = (d4 + 127) / 128;
     for (int t0 = 0; t0 < T; t0 += kRouterTok) {
         const int nt = min(kRouterTok, T - t0);
         float acc[kRouterTok];
@@ -66,16 +69,26 @@ __global__ void __launch_bounds__(512) router_small_kernel(const float *__restri
         for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.f;
         if (row < E) {
             const float4 *w4 = reinterpret_cast<const float4 *>(W + (size_t)row * d);
-            for (int i4 = sub * 32 + lane; i4 < d4; i4 += 128) {
-                float4 w = __ldg(w4 + i4);
+            for (int m0 = 0; m0 < per_lane; m0 += kRouterBatch) {
+                float4 w[kRouterBatch];
 #pragma unroll
-                for (int t = 0; t < kRouterTok; ++t) {
-                    if (t < nt) {
-                        float4 x = load_h4<kBf16>(h, (size_t)(t0 + t) * d + (size_t)i4 * 4);
-                        acc[t] = fmaf(w.x, x.x, acc[t]);
-                        acc[t] = fmaf(w.y, x.y, acc[t]);
-                        acc[t] = fmaf(w.z, x.z, acc[t]);
-                        acc[t] = fmaf(w.w, x.w, acc[t]);
+                for (int u = 0; u < kRouterBatch; ++u) {
+                    const int i4 = sub * 32 + lane + 128 * (m0 + u);
+                    w[u] = (i4 < d4) ? __ldg(w4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kRouterBatch; ++u) {
+                    const int i4 = sub * 32 + lane + 128 * (m0 + u);
+                    if (i4 >= d4) continue;
+#pragma unroll
+                    for (int t = 0; t < kRouterTok; ++t) {
+                        if (t < nt) {
+                            const float4 x = load_h4<kBf16>(h, (size_t)(t0 + t) * d + (size_t)i4 * 4);
+                            acc[t] = fmaf(w[u].x, x.x, acc[t]);
+                            acc[t] = fmaf(w[u].y, x.y, acc[t]);
+                            acc[t] = fmaf(w[u].z, x.z, acc[t]);
+                            acc[t] = fmaf(w[u].w, x.w, acc[t]);
+                        }
                     }
                 }
             }
@@ -203,20 +216,28 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
     }
     __syncwarp();
     constexpr int kNone = 0x7fffffff;
-    int my_idx = -1;
-    float my_hi = 0.f, my_lo = 0.f;
-    for (int r = 0; r < k; ++r) {
-        float bh = 0.f, bl = 0.f;
-        int bi = kNone;
+    // each lane keeps the best untaken expert of its stripe e = lane (mod 32); a round
+    // picks the best head across the warp, and only the owning lane rescans its stripe
+    float hh = 0.f, hl = 0.f;
+    int hidx = kNone;
+    auto rescan = [&]() {
+        hidx = kNone;
         for (int e = lane; e < E; e += 32) {
             if (taken[e]) continue;
             const float vh = lv[e], vl = lw[e];
-            if (bi == kNone || ranks_before(vh, vl, e, bh, bl, bi)) {
-                bh = vh;
-                bl = vl;
-                bi = e;
+            if (hidx == kNone || ranks_before(vh, vl, e, hh, hl, hidx)) {
+                hh = vh;
+                hl = vl;
+                hidx = e;
             }
         }
+    };
+    rescan();
+    int my_idx = -1;
+    float my_hi = 0.f, my_lo = 0.f;
+    for (int r = 0; r < k; ++r) {
+        float bh = hh, bl = hl;
+        int bi = hidx;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
             const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
@@ -228,13 +249,15 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
                 bi = oi;
             }
         }
-        if (bi != kNone && lane == (bi & 31)) taken[bi] = 1;
         if (lane == r) {
             my_idx = bi;
             my_hi = bh;
             my_lo = bl;
         }
-        __syncwarp();
+        if (bi != kNone && lane == (bi & 31)) {
+            taken[bi] = 1;
+            rescan();
+        }
     }
     // softmax over the selected logits; rank 0 holds the largest
     const float h0 = __shfl_sync(0xffffffffu, my_hi, 0);
@@ -325,9 +348,9 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
     if (T <= 16) {
         dim3 grid((L.E + kRouterRows - 1) / kRouterRows);
         if (L.act_bf16)
-            router_small_kernel<true><<<grid, 512, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
+            router_small_kernel<true><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
         else
-            router_small_kernel<false><<<grid, 512, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
+            router_small_kernel<false><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
     } else {
         dim3 grid((L.E + kTileE - 1) / kTileE, (T + kTileT - 1) / kTileT);
         if (L.act_bf16)
