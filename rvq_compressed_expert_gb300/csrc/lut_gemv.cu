@@ -40,6 +40,7 @@ constexpr int kXsFloats = 512;               // down input staging (64 vectors x
 constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
 constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' codebooks
 constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
+constexpr int kPrefetchRounds = 3;                 // L2 prefetch distance in row-group rounds
 
 struct LutArgs {
     const uint8_t *records;
@@ -99,6 +100,15 @@ __device__ __forceinline__ float dot8(const float *__restrict__ c, const float *
     return t;
 }
 
+// Streaming load of 16 code bytes: read once, so kept out of L1.
+__device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes, int lane) {
     constexpr size_t kPiece = 32768;
     for (size_t off = (size_t)lane * kPiece; off < bytes; off += 32 * kPiece) {
@@ -112,6 +122,19 @@ struct Unit {
     int slot, e, seg0, g0, g1;
     const uint8_t *base[2]; // chunk (seg, g=0, s=0, jj=0) of each part, or null
 };
+
+// Ask L2 for row group g of both parts of a unit: 2 parts x 3 stages x 512 B = 24 lines
+// of 128 B, one per lane 0..23, kept with evict_last priority until it is read.
+__device__ __forceinline__ void prefetch_group(const Unit &U, int g, int lane) {
+    if (lane < 24) {
+        const int part = lane / 12, rest = lane % 12;
+        const uint8_t *b = part ? U.base[1] : U.base[0];
+        if (b) {
+            const uint8_t *p = b + ((size_t)g * kStages + rest / 4) * 512 + (size_t)(rest % 4) * 128;
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+        }
+    }
+}
 
 template <bool kDown>
 __device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
@@ -220,12 +243,12 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
         const bool has_next = u + (int)gridDim.x < units;
         Unit N;
         if (has_next) N = decode_unit<kDown>(A, u + gridDim.x);
-        // warm L2 with the next unit's codes while this one builds its tables
-        if (warp == 0 && has_next) {
-            for (int p = 0; p < 2; ++p)
-                if (N.base[p])
-                    prefetch_l2_range(N.base[p] + (size_t)N.g0 * (kStages * 512),
-                                      (size_t)(N.g1 - N.g0) * (kStages * 512), lane);
+        // warm L2 with the first rounds of row groups this warp streams (the tail of the
+        // previous unit already asked for them, except on a CTA's first unit)
+#pragma unroll 1
+        for (int i = 0; i < kPrefetchRounds; ++i) {
+            const int g = U.g0 + warp + i * kWarps;
+            if (g < U.g1) prefetch_group(U, g, lane);
         }
         if (!valid && threadIdx.x == 0) atomicOr(A.err, kErrBadExpert);
         const int t = U.slot / A.k;
@@ -309,24 +332,30 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
             __syncthreads();
         }
 
-        // ---- stream the codes of rows [g0, g1) x this unit's segment(s); the next row
-        // group's codes are loaded before the current one is consumed
+        // ---- stream the codes of rows [g0, g1) x this unit's segment(s).  Registers hold
+        // the next row group's codes while the current one is consumed (ping-pong), and L2
+        // is asked for the row group kPrefetchRounds rounds ahead -- past the end of the
+        // unit, for the next unit's first row groups.
         const uint8_t *pb0 = b4 ? U.base[1] : U.base[0];
         const uint8_t *pb1 = b4 ? U.base[0] : U.base[1];
         const unsigned char *tabb = smem;
-        uint4 cw[2][kStages], nw[2][kStages];
         auto load = [&](int g, uint4 (&w)[2][kStages]) {
 #pragma unroll
             for (int s = 0; s < kStages; ++s) {
                 const size_t co = ((size_t)g * kStages + s) * 512 + (size_t)lane * 16;
-                w[0][s] = pb0 ? __ldg(reinterpret_cast<const uint4 *>(pb0 + co)) : make_uint4(0, 0, 0, 0);
-                w[1][s] = pb1 ? __ldg(reinterpret_cast<const uint4 *>(pb1 + co)) : make_uint4(0, 0, 0, 0);
+                w[0][s] = pb0 ? ld_stream(pb0 + co) : make_uint4(0, 0, 0, 0);
+                w[1][s] = pb1 ? ld_stream(pb1 + co) : make_uint4(0, 0, 0, 0);
             }
         };
-        int g = U.g0 + warp;
-        if (g < U.g1) load(g, cw);
-        for (; g < U.g1; g += kWarps) {
-            if (g + kWarps < U.g1) load(g + kWarps, nw);
+        auto ahead = [&](int g) {
+            const int ga = g + kPrefetchRounds * kWarps;
+            if (ga < U.g1) prefetch_group(U, ga, lane);
+            else if (has_next) {
+                const int gn = N.g0 + (ga - U.g1);
+                if (gn < N.g1) prefetch_group(N, gn, lane);
+            }
+        };
+        auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
             float acc[32];
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
@@ -382,10 +411,20 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
                 if (lane < 16 && row < G.n_out)
                     A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = v;
             }
-#pragma unroll
-            for (int p = 0; p < 2; ++p)
-#pragma unroll
-                for (int s = 0; s < kStages; ++s) cw[p][s] = nw[p][s];
+        };
+        uint4 wa[2][kStages], wb[2][kStages];
+        int g = U.g0 + warp;
+        if (g < U.g1) load(g, wa);
+        while (g < U.g1) {
+            if (g + kWarps < U.g1) load(g + kWarps, wb);
+            ahead(g);
+            consume(wa, g);
+            g += kWarps;
+            if (g >= U.g1) break;
+            if (g + kWarps < U.g1) load(g + kWarps, wa);
+            ahead(g);
+            consume(wb, g);
+            g += kWarps;
         }
         // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
         // and the slot's codebooks once
@@ -436,6 +475,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
                 gv[u] = gate[(size_t)t * k + i];
                 const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
                 float s = 0.f;
+#pragma unroll 4
                 for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
                 sv[u] = s;
             }

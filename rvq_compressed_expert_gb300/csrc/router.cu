@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
     float *lw = lv + E;
     unsigned char *taken = reinterpret_cast<unsigned char *>(lw + E);
     const int t = blockIdx.x, lane = threadIdx.x;
+#pragma unroll 8
     for (int e = lane; e < E; e += 32) {
         // canonical keys make the order total: -0 equals +0, and a NaN (outside the
         // contract) ranks as -inf, so every lane agrees on each round's winner
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
     int hidx = kNone;
     auto rescan = [&]() {
         hidx = kNone;
+#pragma unroll 4
         for (int e = lane; e < E; e += 32) {
             if (taken[e]) continue;
             const float vh = lv[e], vl = lw[e];
