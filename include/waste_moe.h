@@ -86,9 +86,11 @@ enum {
     WASTE_FLAG_VERIFY_CRC = 1u << 0,    /* create: check every record's payload crc32 */
     WASTE_FLAG_FORCE_GEMV = 1u << 2,    /* forward: table-lookup path for every slot */
     WASTE_FLAG_FORCE_MMA = 1u << 3,     /* forward: grouped dequant + tensor-core path when T > 1 */
-    WASTE_FLAG_K2_RECONSTRUCT = 1u << 4 /* forward: rebuild each 8-weight vector from the
-                                           3 codebook entries in registers instead of the
-                                           partial-dot-product table */
+    WASTE_FLAG_K2_RECONSTRUCT = 1u << 4, /* forward: rebuild each 8-weight vector from the
+                                            3 codebook entries in registers instead of the
+                                            partial-dot-product table */
+    WASTE_FLAG_UNFUSED = 1u << 5 /* run each phase as its own kernel instead of the one
+                                    persistent step kernel (same results, bit for bit) */
 };
 
 /* Layer configuration.  d % 8 == 0, f % 8 == 0, 1 <= top_k <= n_experts <= 4096,
@@ -201,6 +203,14 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
 int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d_idx,
                       const float *d_gate, float *d_out, int32_t mode, waste_stream_t stream);
 
+/* route + forward in one call: d_idx, d_gate (and d_logits if not NULL) receive the
+ * routing, d_out the combined output per mode (as waste_moe_forward).  Runs as one
+ * persistent kernel (router, top-k, expert units and combine claimed from a
+ * device-side queue) when the layer's shapes allow it, else as route then forward.
+ * Results are identical to route followed by forward. */
+int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
+                   float *d_logits, float *d_out, int32_t mode, waste_stream_t stream);
+
 /* Lookahead: run next_layer's router on the current hidden states d_h [T][d],
  * take its top n_prefetch experts per token (n_prefetch < 0: the handle's
  * lookahead; 0: nothing) and prefetch their records into L2.  Writes no
@@ -225,8 +235,9 @@ typedef struct {
 } waste_moe_stats_t;
 
 /* Copy the handle's counters (one synchronous copy on the legacy stream after a
- * device synchronise).  Returns WASTE_EINVAL if a kernel saw an expert index out
- * of range since create, else WASTE_OK. */
+ * device synchronise).  Returns WASTE_ETIMEOUT if a bounded device wait gave up,
+ * WASTE_EINVAL if a kernel saw an expert index out of range (since create or the
+ * last reset), else WASTE_OK. */
 int waste_moe_stats(const waste_moe *h, waste_moe_stats_t *out);
 
 /* Zero the counters (synchronous). */
@@ -237,10 +248,11 @@ int waste_moe_reset_stats(waste_moe *h);
  * while a stream is being captured into a graph). */
 int waste_moe_set_profiling(waste_moe *h, int32_t enable);
 
-/* Milliseconds of each kernel of the last profiled route and forward:
- * ms[0] router, ms[1] top-k, ms[2] gate/up, ms[3] down, ms[4] combine
- * (-1 where no call was profiled).  Waits for the events. */
-int waste_moe_read_profile(const waste_moe *h, float ms[5]);
+/* Milliseconds of each kernel of the last profiled calls: ms[0] router, ms[1] top-k
+ * (route); ms[2] gate/up, ms[3] down, ms[4] combine (forward as separate kernels);
+ * ms[5] the persistent step kernel (step, or forward when fused); -1 where the last
+ * call did not run that kernel.  Waits for the events. */
+int waste_moe_read_profile(const waste_moe *h, float ms[6]);
 
 /* Message of the last failure on the calling thread ("" if none). */
 const char *waste_moe_last_error(void);

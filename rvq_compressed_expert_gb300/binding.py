@@ -22,6 +22,7 @@ FLAG_VERIFY_CRC = 1 << 0
 FLAG_FORCE_GEMV = 1 << 2
 FLAG_FORCE_MMA = 1 << 3
 FLAG_K2_RECONSTRUCT = 1 << 4
+FLAG_UNFUSED = 1 << 5
 RECORD_ALIGN = 4096
 RECORD_MAGIC = 0x454F4D57
 
@@ -32,7 +33,7 @@ EXPORTED = ["waste_moe_record_layout", "waste_moe_pack_records", "waste_moe_crea
             "waste_moe_route", "waste_moe_forward", "waste_moe_prefetch", "waste_moe_destroy",
             "waste_moe_stats", "waste_moe_reset_stats", "waste_moe_last_error",
             "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile",
-            "waste_moe_rmsnorm", "waste_moe_forward_noalloc"]
+            "waste_moe_rmsnorm", "waste_moe_forward_noalloc", "waste_moe_step"]
 
 
 class waste_moe_config(ctypes.Structure):
@@ -97,6 +98,7 @@ def load(path: str = LIB_PATH):
     lib.waste_moe_set_profiling.argtypes = [vp, i32]
     lib.waste_moe_read_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_float)]
     lib.waste_moe_rmsnorm.argtypes = [vp, vp, i32, i32, vp]
+    lib.waste_moe_step.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, vp]
     lib.waste_moe_forward_noalloc.argtypes = [cfgp, vp, sz, vp, vp, i32, vp, vp, vp, i32, vp]
     for name in EXPORTED:
         if name not in ("waste_moe_destroy", "waste_moe_last_error"):
@@ -172,6 +174,11 @@ def waste_moe_forward(h, d_h, T, d_idx, d_gate, d_out, mode=0, stream=None):
                                            _ptr(d_out), mode, _stream(stream)))
 
 
+def waste_moe_step(h, d_h, T, d_idx, d_gate, d_logits, d_out, mode=0, stream=None):
+    return _check(load().waste_moe_step(h, _ptr(d_h), T, _ptr(d_idx), _ptr(d_gate), _ptr(d_logits),
+                                        _ptr(d_out), mode, _stream(stream)))
+
+
 def waste_moe_prefetch(next_layer, d_h, T, n_prefetch=-1, side=None):
     return _check(load().waste_moe_prefetch(next_layer, _ptr(d_h), T, n_prefetch, _stream(side)))
 
@@ -202,9 +209,9 @@ def waste_moe_set_profiling(h, enable=True):
 
 def waste_moe_read_profile(h) -> dict:
     """Milliseconds per kernel of the last profiled route and forward."""
-    ms = (ctypes.c_float * 5)()
+    ms = (ctypes.c_float * 6)()
     _check(load().waste_moe_read_profile(h, ms))
-    return dict(zip(("router", "topk", "gate_up", "down", "combine"), list(ms)))
+    return dict(zip(("router", "topk", "gate_up", "down", "combine", "step"), list(ms)))
 
 
 def waste_moe_rmsnorm(d_in, d_out, T, d, stream=None):

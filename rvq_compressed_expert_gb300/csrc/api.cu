@@ -20,7 +20,7 @@ struct waste_moe {
     int max_slots;
     int pred_P; // experts per token of the last prefetch into this layer
     bool profiling;
-    Timing route_tm, fwd_tm;
+    Timing route_tm, fwd_tm, step_tm;
 };
 
 namespace {
@@ -64,7 +64,7 @@ int check_config(const waste_moe_config *c) {
     if (c->lookahead < 0 || c->lookahead > kMaxTopK || c->lookahead > c->n_experts)
         return fail(WASTE_EINVAL, "lookahead = %d outside [0, min(n_experts, %d)]", c->lookahead, kMaxTopK);
     const uint32_t known = WASTE_FLAG_VERIFY_CRC | WASTE_FLAG_FORCE_GEMV | WASTE_FLAG_FORCE_MMA |
-                           WASTE_FLAG_K2_RECONSTRUCT;
+                           WASTE_FLAG_K2_RECONSTRUCT | WASTE_FLAG_UNFUSED;
     if (c->flags & ~known) return fail(WASTE_EINVAL, "unknown flags 0x%x", c->flags & ~known);
     return WASTE_OK;
 }
@@ -248,6 +248,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
         S * npair * (size_t)L.d * 4,                // part_dn
         kStatCount * 8,                             // stats
         4,                                          // err
+        (4 + S + kMaxFusedRowBlocks) * 4,           // sync
     };
     const int n_parts = (int)(sizeof sizes / sizeof sizes[0]);
     size_t offs[16], total = 0;
@@ -277,6 +278,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     W.part_dn = reinterpret_cast<float *>(b + offs[7]);
     W.stats = reinterpret_cast<unsigned long long *>(b + offs[8]);
     W.err = reinterpret_cast<uint32_t *>(b + offs[9]);
+    W.sync = reinterpret_cast<unsigned *>(b + offs[10]);
     ce = cudaMemset(base, 0, total);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
@@ -293,6 +295,7 @@ static void drop_events(waste_moe *h) {
     for (int i = 0; i < 8; ++i) {
         cudaEventDestroy(h->route_tm.ev[i]);
         cudaEventDestroy(h->fwd_tm.ev[i]);
+        cudaEventDestroy(h->step_tm.ev[i]);
     }
     h->profiling = false;
 }
@@ -316,21 +319,23 @@ int waste_moe_set_profiling(waste_moe *h, int32_t enable) {
     for (int i = 0; i < 8; ++i) {
         cudaError_t e = cudaEventCreate(&h->route_tm.ev[i]);
         if (e == cudaSuccess) e = cudaEventCreate(&h->fwd_tm.ev[i]);
+        if (e == cudaSuccess) e = cudaEventCreate(&h->step_tm.ev[i]);
         if (e != cudaSuccess) return cuda_fail(e, "creating profiling events");
     }
-    h->route_tm.n = h->fwd_tm.n = 0;
+    h->route_tm.n = h->fwd_tm.n = h->step_tm.n = 0;
     h->profiling = true;
     return ok();
 }
 
-int waste_moe_read_profile(const waste_moe *h, float ms[5]) {
+int waste_moe_read_profile(const waste_moe *h, float ms[6]) {
     if (!h || !ms) return fail(WASTE_EINVAL, "NULL handle or output");
     if (!h->profiling) return fail(WASTE_EINVAL, "profiling is not enabled");
-    for (int i = 0; i < 5; ++i) ms[i] = -1.f;
-    const Timing *t[2] = {&h->route_tm, &h->fwd_tm};
+    for (int i = 0; i < 6; ++i) ms[i] = -1.f;
+    const Timing *t[3] = {&h->route_tm, &h->fwd_tm, &h->step_tm};
+    const int count[3] = {3, 4, 2};
     int o = 0;
-    for (int j = 0; j < 2; ++j) {
-        const int n = j == 0 ? 3 : 4;
+    for (int j = 0; j < 3; ++j) {
+        const int n = count[j];
         if (t[j]->n == n) {
             cudaError_t e = cudaEventSynchronize(t[j]->ev[n - 1]);
             if (e != cudaSuccess) return cuda_fail(e, "waiting for profiling events");
@@ -387,9 +392,52 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
     if (!d_idx || !d_gate || !d_out) return fail(WASTE_EINVAL, "NULL idx, gate or out");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool recon = (h->cfg.flags & WASTE_FLAG_K2_RECONSTRUCT) != 0;
-    cudaError_t e = launch_lut_forward(h->L, h->W, d_h, T, d_idx, d_gate, d_out, mode, recon,
-                                       h->num_sms, s, h->profiling ? &h->fwd_tm : nullptr);
+    cudaError_t e;
+    if (!(h->cfg.flags & WASTE_FLAG_UNFUSED) && fused_eligible(h->L, T, false, h->num_sms)) {
+        if (h->profiling) cudaEventRecord(h->step_tm.ev[0], s);
+        e = launch_fused_step(h->L, h->W, d_h, T, false, const_cast<int32_t *>(d_idx),
+                              const_cast<float *>(d_gate), nullptr, nullptr, nullptr, 1, d_out, mode,
+                              recon, h->num_sms, s);
+        if (h->profiling) {
+            cudaEventRecord(h->step_tm.ev[1], s);
+            h->step_tm.n = 2;
+            h->fwd_tm.n = 0;
+        }
+    } else {
+        e = launch_lut_forward(h->L, h->W, d_h, T, d_idx, d_gate, d_out, mode, recon, h->num_sms, s,
+                               h->profiling ? &h->fwd_tm : nullptr);
+        if (h->profiling) h->step_tm.n = 0;
+    }
     if (e != cudaSuccess) return cuda_fail(e, "expert kernels");
+    return ok();
+}
+
+int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
+                   float *d_logits, float *d_out, int32_t mode, waste_stream_t stream) {
+    int rc = check_tokens(h, T, d_h);
+    if (rc) return rc;
+    if (mode < 0 || mode > 2) return fail(WASTE_EINVAL, "mode = %d", mode);
+    if (mode == 2 && h->cfg.act_dtype != WASTE_ACT_F32)
+        return fail(WASTE_EINVAL, "mode 2 (out = h + y) needs fp32 hidden states");
+    if (T == 0) return ok();
+    if (!d_idx || !d_gate || !d_out) return fail(WASTE_EINVAL, "NULL idx, gate or out");
+    if ((h->cfg.flags & WASTE_FLAG_UNFUSED) || !fused_eligible(h->L, T, true, h->num_sms)) {
+        rc = waste_moe_route(h, d_h, T, d_idx, d_gate, d_logits, stream);
+        if (rc) return rc;
+        return waste_moe_forward(h, d_h, T, d_idx, d_gate, d_out, mode, stream);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool recon = (h->cfg.flags & WASTE_FLAG_K2_RECONSTRUCT) != 0;
+    if (h->profiling) cudaEventRecord(h->step_tm.ev[0], s);
+    cudaError_t e = launch_fused_step(h->L, h->W, d_h, T, true, d_idx, d_gate,
+                                      d_logits ? d_logits : h->W.logits, h->W.pred_idx, h->W.pred_count,
+                                      h->pred_P > 0 ? h->pred_P : 1, d_out, mode, recon, h->num_sms, s);
+    if (h->profiling) {
+        cudaEventRecord(h->step_tm.ev[1], s);
+        h->step_tm.n = 2;
+        h->route_tm.n = h->fwd_tm.n = 0;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "fused step kernel");
     return ok();
 }
 
@@ -430,6 +478,8 @@ int waste_moe_stats(const waste_moe *h, waste_moe_stats_t *out) {
     out->prediction_hits = v[kStatPredHits];
     out->routed_slots = v[kStatRoutedSlots];
     out->forward_slots = v[kStatForwardSlots];
+    if (err & kErrTimeout) return fail(WASTE_ETIMEOUT, "a device wait of the fused step kernel gave up");
+    if (err & kErrTimeout) return fail(WASTE_ETIMEOUT, "a bounded device wait of the step kernel gave up");
     if (err & kErrBadExpert) return fail(WASTE_EINVAL, "forward saw an expert index outside [0, %d)", h->L.E);
     return ok();
 }

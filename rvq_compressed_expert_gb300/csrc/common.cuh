@@ -17,9 +17,10 @@ constexpr int kSegVec = 32;    // vectors per segment (one per lane)
 constexpr int kGroupRows = 16; // rows per 16-byte chunk
 constexpr int kMaxExperts = 4096;
 constexpr int kMaxTopK = 32;
+constexpr int kMaxFusedRowBlocks = 64; // down row blocks the fused step kernel can track
 
 // Sticky device error bits.
-enum : uint32_t { kErrBadExpert = 1u };
+enum : uint32_t { kErrBadExpert = 1u, kErrTimeout = 2u };
 
 // Device counters, indices into the handle's uint64 counter array.
 enum {
@@ -81,6 +82,7 @@ struct Workspace {
     float *part_dn;      // [max_slots][npair][d]
     unsigned long long *stats; // [kStatCount]
     uint32_t *err;       // sticky error bits
+    unsigned *sync;      // fused-step queue and counters [4 + max_slots + kMaxFusedRowBlocks], zero at rest
     void *base;
     size_t bytes;
 };
@@ -103,6 +105,16 @@ struct Timing {
 cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
                                const int32_t *idx, const float *gate, float *out, int mode,
                                bool reconstruct, int num_sms, cudaStream_t s, Timing *tm);
+// Row blocks of the down matrix per (slot, segment pair) for the lookup kernels.
+int down_row_blocks(int slots, int npair, int groups, int num_sms);
+// Whether the fused step kernel can run this call (else the per-phase kernels do).
+bool fused_eligible(const LayerView &L, int T, bool with_route, int num_sms);
+// Route (optional) and forward in one persistent kernel.
+cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void *h, int T,
+                              bool with_route, int32_t *idx, float *gate, float *logits,
+                              const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
+                              float *out, int mode, bool reconstruct, int num_sms,
+                              cudaStream_t s);
 cudaError_t launch_prefetch_l2(const LayerView &L, const int32_t *pred_idx, int pred_stride,
                                int T, int P, int32_t *pred_count, unsigned long long *stats,
                                cudaStream_t s);

@@ -1,0 +1,274 @@
+// One persistent kernel for a whole decode step of one MoE layer: router GEMV,
+// top-k + softmax, the table-lookup gate/up units, the down units and the
+// gate-weighted combine, in one launch.
+//
+// Work items are claimed from a device-side queue in a fixed order:
+//   [router items][top-k item][gate/up units][down units][combine items]
+// A CTA claims one item ahead of the one it runs, so the next unit's codes and
+// codebooks can be fetched while the current one streams.  An item waits only on
+// items that precede it in the queue (top-k on all router items, gate/up units on
+// the top-k, a down unit on the gate/up units of its slot, a combine item on the
+// down units of its rows), signalled by device counters with release/acquire
+// ordering.  Because every CTA runs its items in claim order, the smallest
+// unfinished item never waits on anything unfinished, so the queue always makes
+// progress whatever number of CTAs is resident; every wait is still bounded and
+// records kErrTimeout if it gives up.  The last CTA to leave resets the counters
+// for the next launch.  The arithmetic of each item is that of the per-phase
+// kernels, in the same order: results are bit-identical to them.
+#include "lut_dev.cuh"
+#include "route_dev.cuh"
+
+namespace wm {
+
+using namespace lut;
+using namespace route;
+
+namespace {
+
+constexpr int kRouterRowsPerItem = kThreads / 128; // 4 expert rows per router item
+constexpr int kCombineRows = 256;                   // output rows per combine item
+
+struct FusedArgs {
+    LutArgs A; // lookup units; A.idx is where the top-k item writes the routing
+    // routing
+    const float *router_w, *router_b;
+    float *logits, *logits_lo; // [T][E]
+    int32_t *idx_out;
+    float *gate_out;
+    const int32_t *pred_idx;
+    int32_t *pred_count;
+    int pred_stride;
+    unsigned long long router_bytes;
+    int with_route;
+    int T, d;
+    // combine
+    const float *gate, *h32;
+    float *out;
+    int mode;
+    // queue and counters (zero at rest):
+    // [0] next item, [1] CTAs that left, [2] router items done, [3] top-k done,
+    // [4, 4 + slots) gate/up units done per slot, then down units done per row block
+    unsigned *sync;
+    int n_router, n_topk, n_gu, n_dn, n_comb;
+};
+
+__device__ __forceinline__ void signal(unsigned *c) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(c, 1u);
+    }
+}
+
+__device__ __forceinline__ int claim(unsigned *q, int *slot) {
+    __syncthreads();
+    if (threadIdx.x == 0) *slot = (int)atomicAdd(q, 1u);
+    __syncthreads();
+    return *slot;
+}
+
+// combine rows [r0, r1) of every token from the down partials (same order as the
+// per-phase combine kernel)
+__device__ void combine_item(const FusedArgs &F, int r0, int r1) {
+    const LutArgs &A = F.A;
+    const int d = F.d, k = A.k;
+    for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+        for (int t = 0; t < F.T; ++t) {
+            float y = 0.f;
+            for (int i0 = 0; i0 < k; i0 += 8) {
+                float sv[8], gv[8];
+                bool ok[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u;
+                    sv[u] = 0.f;
+                    gv[u] = 0.f;
+                    ok[u] = false;
+                    if (i < k) {
+                        const int e = A.idx[(size_t)t * k + i];
+                        ok[u] = e >= 0 && e < A.E;
+                        gv[u] = F.gate[(size_t)t * k + i];
+                        const float *p = A.part_dn + ((size_t)t * k + i) * A.npair * d + r;
+                        float s = 0.f;
+#pragma unroll 4
+                        for (int q = 0; q < A.npair; ++q) s += p[(size_t)q * d];
+                        sv[u] = s;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (ok[u]) y = fmaf(gv[u], sv[u], y);
+            }
+            const size_t o = (size_t)t * d + r;
+            if (F.mode == 0) F.out[o] = y;
+            else if (F.mode == 1) F.out[o] = F.out[o] + y;
+            else F.out[o] = F.h32[o] + y;
+        }
+    }
+}
+
+template <bool kRecon, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs F) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ float red[kRouterRowsPerItem][4][kRouterTok];
+    __shared__ int claimed;
+    const LutArgs &A = F.A;
+    unsigned *queue = F.sync, *exited = F.sync + 1, *router_done = F.sync + 2,
+             *topk_done = F.sync + 3, *gu_done = F.sync + 4, *dn_done = F.sync + 4 + A.slots;
+    const int b_topk = F.n_router, b_gu = b_topk + F.n_topk, b_dn = b_gu + F.n_gu,
+              b_comb = b_dn + F.n_dn, total = b_comb + F.n_comb;
+    int par = 0;
+    bool primed = false;
+    int cur = claim(queue, &claimed);
+    int nxt = claim(queue, &claimed);
+    while (cur < total) {
+        if (cur < b_topk) {
+            // ---- router rows
+            router_block<kBf16>(F.router_w, F.router_b, A.h, F.T, A.E, F.d, cur * kRouterRowsPerItem,
+                                F.logits, F.logits_lo, red);
+            signal(router_done);
+        } else if (cur < b_gu) {
+            // ---- top-k + softmax of every token, one warp per token
+            wait_counter(router_done, (unsigned)F.n_router, A.err);
+            const int warp = threadIdx.x >> 5;
+            float *area = reinterpret_cast<float *>(smem) + (size_t)warp * ((A.E * 9 + 15) / 16 * 4);
+            for (int t = warp; t < F.T; t += kWarps)
+                topk_warp(F.logits, F.logits_lo, A.E, A.k, t, F.idx_out, F.gate_out, F.pred_idx,
+                          F.pred_count, F.pred_stride, A.stats, F.router_bytes, area);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomicExch(topk_done, 1u);
+            }
+        } else if (cur < b_dn) {
+            // ---- gate/up unit
+            if (F.with_route) wait_counter(topk_done, 1u, A.err);
+            const Unit U = decode_unit<false>(A, cur - b_gu);
+            const bool has_next = nxt >= b_gu && nxt < b_dn;
+            Unit N;
+            if (has_next) N = decode_unit<false>(A, nxt - b_gu);
+            run_unit<false, kRecon, kBf16>(A, U, has_next, N, par, primed, nullptr, 0, smem);
+            signal(gu_done + U.slot);
+        } else if (cur < b_comb) {
+            // ---- down unit (waits inside for the gate/up units of its slot)
+            if (F.with_route) wait_counter(topk_done, 1u, A.err);
+            const int u = cur - b_dn;
+            const Unit U = decode_unit<true>(A, u);
+            const bool has_next = nxt >= b_dn && nxt < b_comb;
+            Unit N;
+            if (has_next) N = decode_unit<true>(A, nxt - b_dn);
+            run_unit<true, kRecon, kBf16>(A, U, has_next, N, par, primed, gu_done + U.slot,
+                                          (unsigned)A.gu.nseg, smem);
+            signal(dn_done + (u % A.nrb));
+        } else {
+            // ---- combine rows [r0, r1) once every down unit over them is done
+            const int r0 = (cur - b_comb) * kCombineRows;
+            const int r1 = min(F.d, r0 + kCombineRows);
+            const int rb0 = (r0 / kGroupRows) / A.rb_groups;
+            const int rb1 = ((r1 - 1) / kGroupRows) / A.rb_groups;
+            for (int rb = rb0; rb <= rb1; ++rb)
+                wait_counter(dn_done + rb, (unsigned)(A.slots * A.npair), A.err);
+            combine_item(F, r0, r1);
+            if (cur == b_comb && threadIdx.x == 0 && A.stats)
+                atomicAdd(A.stats + kStatForwardSlots, (unsigned long long)A.slots);
+        }
+        cur = nxt;
+        nxt = claim(queue, &claimed);
+    }
+    if constexpr (!kRecon) cp_async_wait<0>();
+    // the last CTA to leave puts the queue and counters back to zero
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned left = atomicAdd(exited, 1u);
+        if (left == gridDim.x - 1) {
+            __threadfence();
+            const int n = 4 + A.slots + A.nrb;
+            for (int i = 0; i < n; ++i) F.sync[i] = 0u;
+            __threadfence();
+        }
+    }
+}
+
+template <bool kRecon, bool kBf16>
+cudaError_t launch_fused_t(const FusedArgs &F, int grid, cudaStream_t s) {
+    const size_t smem = unit_smem<kRecon>();
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(fused_step_kernel<kRecon, kBf16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    fused_step_kernel<kRecon, kBf16><<<grid, kThreads, smem, s>>>(F);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+bool fused_eligible(const LayerView &L, int T, bool with_route, int num_sms) {
+    const int slots = T * L.k;
+    const int npair = (L.dn.nseg + 1) / 2;
+    if (down_row_blocks(slots, npair, L.dn.groups, num_sms) > kMaxFusedRowBlocks) return false;
+    if (with_route && ((size_t)kWarps * ((L.E * 9 + 15) / 16 * 16) > (size_t)kTabBytes)) return false;
+    return true;
+}
+
+cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void *h, int T,
+                              bool with_route, int32_t *idx, float *gate, float *logits,
+                              const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
+                              float *out, int mode, bool reconstruct, int num_sms,
+                              cudaStream_t s) {
+    FusedArgs F;
+    LutArgs &A = F.A;
+    A.records = L.records;
+    A.stride = L.stride;
+    A.codebooks = L.codebooks;
+    A.idx = idx;
+    A.h = h;
+    A.E = L.E;
+    A.k = L.k;
+    A.slots = T * L.k;
+    A.gu = L.gu;
+    A.off_gate = L.sec_off[0];
+    A.off_up = L.sec_off[1];
+    A.part_gu = W.part_gu;
+    A.dn = L.dn;
+    A.off_down = L.sec_off[2];
+    A.npair = (L.dn.nseg + 1) / 2;
+    A.nrb = down_row_blocks(A.slots, A.npair, L.dn.groups, num_sms);
+    A.rb_groups = (L.dn.groups + A.nrb - 1) / A.nrb;
+    A.part_dn = W.part_dn;
+    A.stats = W.stats;
+    A.err = W.err;
+    F.router_w = L.router_w;
+    F.router_b = L.router_b;
+    F.logits = logits;
+    F.logits_lo = W.logits_lo;
+    F.idx_out = idx;
+    F.gate_out = gate;
+    F.pred_idx = pred_idx;
+    F.pred_count = pred_count;
+    F.pred_stride = pred_stride;
+    F.router_bytes = (unsigned long long)L.E * (unsigned long long)L.d * 4ull;
+    F.with_route = with_route ? 1 : 0;
+    F.T = T;
+    F.d = L.d;
+    F.gate = gate;
+    F.h32 = reinterpret_cast<const float *>(h);
+    F.out = out;
+    F.mode = mode;
+    F.sync = W.sync;
+    F.n_router = with_route ? (L.E + kRouterRowsPerItem - 1) / kRouterRowsPerItem : 0;
+    F.n_topk = with_route ? 1 : 0;
+    F.n_gu = A.slots * A.gu.nseg;
+    F.n_dn = A.slots * A.npair * A.nrb;
+    F.n_comb = (L.d + kCombineRows - 1) / kCombineRows;
+    const int total = F.n_router + F.n_topk + F.n_gu + F.n_dn + F.n_comb;
+    const int grid = total < num_sms ? total : num_sms;
+    const bool bf16 = L.act_bf16 != 0;
+    if (reconstruct) return bf16 ? launch_fused_t<true, true>(F, grid, s) : launch_fused_t<true, false>(F, grid, s);
+    return bf16 ? launch_fused_t<false, true>(F, grid, s) : launch_fused_t<false, false>(F, grid, s);
+}
+
+} // namespace wm

@@ -1,0 +1,447 @@
+// Device-side pieces of the table-lookup expert kernels, shared by the per-phase
+// kernels (lut_gemv.cu) and the fused decode-step kernel (fused.cu).
+#pragma once
+
+#include "common.cuh"
+
+
+namespace wm {
+namespace lut {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTabStage = 65536;             // bytes per stage: 256 codes x 256 B
+constexpr int kTabBytes = kStages * kTabStage; // 192 KiB
+constexpr int kXsFloats = 512;               // down input staging (64 vectors x 8)
+constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
+constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' codebooks
+constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
+constexpr int kPrefetchRounds = 3;                 // L2 prefetch distance in row-group rounds
+
+struct LutArgs {
+    const uint8_t *records;
+    size_t stride;
+    const float *codebooks;
+    const int32_t *idx;
+    const void *h;
+    int E, k, slots;
+    // gate / up
+    MatGeom gu;
+    size_t off_gate, off_up;
+    float *part_gu; // [slot][gu.nseg][2][f]
+    // down
+    MatGeom dn;
+    size_t off_down;
+    int npair, nrb, rb_groups;
+    float *part_dn; // [slot][npair][d]
+    unsigned long long *stats;
+    uint32_t *err;
+};
+
+__device__ __forceinline__ uint32_t comp(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void load_x8(const void *h, size_t elem, float *xv) {
+    if constexpr (kBf16) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(h) + elem);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+            float2 f2 = __bfloat1622float2(b2);
+            xv[2 * i] = f2.x;
+            xv[2 * i + 1] = f2.y;
+        }
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(h) + elem);
+        const float4 a = p[0], b = p[1];
+        xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+        xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ float dot8(const float *__restrict__ c, const float *xv) {
+    const float4 c0 = __ldg(reinterpret_cast<const float4 *>(c));
+    const float4 c1 = __ldg(reinterpret_cast<const float4 *>(c) + 1);
+    float t = c0.x * xv[0];
+    t = fmaf(c0.y, xv[1], t);
+    t = fmaf(c0.z, xv[2], t);
+    t = fmaf(c0.w, xv[3], t);
+    t = fmaf(c1.x, xv[4], t);
+    t = fmaf(c1.y, xv[5], t);
+    t = fmaf(c1.z, xv[6], t);
+    t = fmaf(c1.w, xv[7], t);
+    return t;
+}
+
+// Streaming load of 16 code bytes: read once, so kept out of L1.
+__device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes, int lane) {
+    constexpr size_t kPiece = 32768;
+    for (size_t off = (size_t)lane * kPiece; off < bytes; off += 32 * kPiece) {
+        const uint32_t n = (uint32_t)min(kPiece, bytes - off);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + off), "r"(n) : "memory");
+    }
+}
+
+// Decode a unit index into (slot, first segment, part bases, row-group range).
+struct Unit {
+    int slot, e, seg0, g0, g1;
+    const uint8_t *base[2]; // chunk (seg, g=0, s=0, jj=0) of each part, or null
+};
+
+// Ask L2 for row group g of both parts of a unit: 2 parts x 3 stages x 512 B = 24 lines
+// of 128 B, one per lane 0..23, kept with evict_last priority until it is read.
+__device__ __forceinline__ void prefetch_group(const Unit &U, int g, int lane) {
+    if (lane < 24) {
+        const int part = lane / 12, rest = lane % 12;
+        const uint8_t *b = part ? U.base[1] : U.base[0];
+        if (b) {
+            const uint8_t *p = b + ((size_t)g * kStages + rest / 4) * 512 + (size_t)(rest % 4) * 128;
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+        }
+    }
+}
+
+template <bool kDown>
+__device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
+    Unit U;
+    if constexpr (!kDown) {
+        U.slot = u / A.gu.nseg;
+        U.seg0 = u % A.gu.nseg;
+        U.g0 = 0;
+        U.g1 = A.gu.groups;
+    } else {
+        const int per_slot = A.npair * A.nrb;
+        U.slot = u / per_slot;
+        const int rem = u % per_slot;
+        U.seg0 = 2 * (rem / A.nrb);
+        const int rb = rem % A.nrb;
+        U.g0 = rb * A.rb_groups;
+        U.g1 = min(A.dn.groups, U.g0 + A.rb_groups);
+    }
+    U.e = A.idx[U.slot];
+    U.base[0] = U.base[1] = nullptr;
+    if (U.e >= 0 && U.e < A.E) {
+        const uint8_t *rec = A.records + (size_t)U.e * A.stride;
+        if constexpr (!kDown) {
+            const size_t so = (size_t)U.seg0 * A.gu.groups * (kStages * 512);
+            U.base[0] = rec + A.off_gate + so;
+            U.base[1] = rec + A.off_up + so;
+        } else {
+            for (int p = 0; p < 2; ++p)
+                if (U.seg0 + p < A.dn.nseg)
+                    U.base[p] = rec + A.off_down + (size_t)(U.seg0 + p) * A.dn.groups * (kStages * 512);
+        }
+    }
+    return U;
+}
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Codebook rows of one stage for both parts -> smem [part][256][8] (16 KiB), as
+// one cp.async group.
+__device__ __forceinline__ void issue_stage(float *dst, const float *cb_p0, const float *cb_p1, int s) {
+    for (int i = threadIdx.x; i < 1024; i += kThreads) {
+        const int part = i >> 9, ii = i & 511;
+        const float *src = (part ? cb_p1 : cb_p0) + (size_t)s * kCodes * kVec + (size_t)ii * 4;
+        cp_async16(dst + part * kCodes * kVec + ii * 4, src);
+    }
+    cp_async_commit();
+}
+
+template <bool kDown>
+__device__ __forceinline__ void unit_codebooks(const LutArgs &A, const Unit &U, const float *&p0,
+                                               const float *&p1) {
+    const int e = (U.e >= 0 && U.e < A.E) ? U.e : 0;
+    const float *cb_e = A.codebooks + (size_t)e * 3 * kCbFloats;
+    p0 = cb_e + (kDown ? 2 : 0) * kCbFloats;
+    p1 = cb_e + (kDown ? 2 : 1) * kCbFloats;
+}
+
+__device__ __forceinline__ float dot8s(const float *__restrict__ c, const float *xv) {
+    const float4 c0 = reinterpret_cast<const float4 *>(c)[0];
+    const float4 c1 = reinterpret_cast<const float4 *>(c)[1];
+    float t = c0.x * xv[0];
+    t = fmaf(c0.y, xv[1], t);
+    t = fmaf(c0.z, xv[2], t);
+    t = fmaf(c0.w, xv[3], t);
+    t = fmaf(c1.x, xv[4], t);
+    t = fmaf(c1.y, xv[5], t);
+    t = fmaf(c1.z, xv[6], t);
+    t = fmaf(c1.w, xv[7], t);
+    return t;
+}
+
+// Wait (thread 0 polls, the CTA then proceeds together) until *c >= target.  The wait
+// is bounded: after about a second it records kErrTimeout and gives up.
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target, uint32_t *err) {
+    if (threadIdx.x == 0) {
+        unsigned ns = 32;
+        for (long it = 0; ld_acquire(c) < target; ++it) {
+            if (it > (1l << 22)) {
+                atomicOr(err, kErrTimeout);
+                break;
+            }
+            __nanosleep(ns);
+            if (ns < 256) ns <<= 1;
+        }
+    }
+    __syncthreads();
+}
+
+// One unit: tables (or staged codebooks) for the unit's segment(s), then the stream of
+// its rows.  `par`/`primed` carry the codebook stage buffers across consecutive units of
+// one kind: when `has_next`, the next unit's stages 0 and 1 are already on their way
+// into the buffers when this one returns.  For a down unit, `dep` (if not null) is a
+// completion counter that must reach dep_target before the gate/up partials are read.
+template <bool kDown, bool kRecon, bool kBf16>
+__device__ __noinline__ void run_unit(const LutArgs &A, const Unit &U, bool has_next, const Unit &N,
+                                         int &par, bool &primed, const unsigned *dep,
+                                         unsigned dep_target, unsigned char *smem) {
+    float *cbuf = reinterpret_cast<float *>(smem + kTabBytes);
+    float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kTabBytes + 2 * kStageBuf));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b4 = lane >> 4;
+    const MatGeom &G = kDown ? A.dn : A.gu;
+    // table column byte offset of register-part p: column (p ^ b4), lane l
+    const uint32_t colb0 = ((uint32_t)(0 ^ b4) << 7) | ((uint32_t)lane << 2);
+    const uint32_t colb1 = ((uint32_t)(1 ^ b4) << 7) | ((uint32_t)lane << 2);
+    const bool valid = U.base[0] != nullptr;
+    if (!kRecon && !primed) {
+        const float *q0, *q1;
+        unit_codebooks<kDown>(A, U, q0, q1);
+        issue_stage(cbuf + par * kStageFloats, q0, q1, 0);
+        issue_stage(cbuf + (par ^ 1) * kStageFloats, q0, q1, 1);
+    }
+    // warm L2 with the first rounds of row groups this warp streams (the tail of the
+    // previous unit already asked for them, except on a CTA's first unit)
+#pragma unroll 1
+    for (int i = 0; i < kPrefetchRounds; ++i) {
+        const int g = U.g0 + warp + i * kWarps;
+        if (g < U.g1) prefetch_group(U, g, lane);
+    }
+    if (!valid && threadIdx.x == 0) atomicOr(A.err, kErrBadExpert);
+    const int t = U.slot / A.k;
+    // ---- input vectors of this lane's column(s)
+    float xv[2][kVec];
+    if constexpr (!kDown) {
+        const int j = U.seg0 * kSegVec + lane;
+        if (j < G.nv) load_x8<kBf16>(A.h, (size_t)t * A.gu.n_in + (size_t)j * kVec, xv[0]);
+        else {
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) xv[0][v] = 0.f;
+        }
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) xv[1][v] = xv[0][v];
+    } else {
+        // a = silu(gate) * up for the 64 vectors of this unit, reduced over the
+        // gate/up segments in a fixed order
+        __syncthreads(); // xs may still be read by the previous unit
+        if (dep) wait_counter(dep, dep_target, A.err);
+        {
+            const int r = U.seg0 * kSegVec * kVec + threadIdx.x; // index into f
+            float a = 0.f;
+            if (valid && r < A.gu.n_out) {
+                const float *pg = A.part_gu + (size_t)U.slot * A.gu.nseg * 2 * A.gu.n_out;
+                float zg = 0.f, zu = 0.f;
+                for (int sg = 0; sg < A.gu.nseg; ++sg) {
+                    zg += pg[((size_t)sg * 2 + 0) * A.gu.n_out + r];
+                    zu += pg[((size_t)sg * 2 + 1) * A.gu.n_out + r];
+                }
+                a = zg / (1.0f + expf(-zg)) * zu;
+            }
+            xs[threadIdx.x] = a;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) xv[p][v] = xs[p * kSegVec * kVec + lane * kVec + v];
+    }
+    // x of register-part p (column p ^ b4), for the reconstruct variant
+    float xr[2][kVec];
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) xr[p][v] = b4 ? xv[p ^ 1][v] : xv[p][v];
+    __syncthreads(); // previous unit's lookups are done with the tables
+    if constexpr (!kRecon) {
+        // ---- tables T[s][c][part][lane], one stage at a time from the staged codebooks;
+        // the cp.async groups in flight are always the next two stage loads
+        float *tab = reinterpret_cast<float *>(smem);
+        const float *p0, *p1, *n0 = nullptr, *n1 = nullptr;
+        unit_codebooks<kDown>(A, U, p0, p1);
+        if (has_next) unit_codebooks<kDown>(A, N, n0, n1);
+#pragma unroll 1
+        for (int s = 0; s < kStages; ++s) {
+            if (s < 2 || has_next) cp_async_wait<1>();
+            else cp_async_wait<0>();
+            __syncthreads();
+            const float *buf = cbuf + ((s == 1) ? (par ^ 1) : par) * kStageFloats;
+            for (int c = warp; c < kCodes; c += kWarps) {
+                const float t0 = valid ? dot8s(buf + c * kVec, xv[0]) : 0.f;
+                const float t1 = valid ? dot8s(buf + kCodes * kVec + c * kVec, xv[1]) : 0.f;
+                tab[((size_t)s * kCodes + c) * 64 + lane] = t0;
+                tab[((size_t)s * kCodes + c) * 64 + 32 + lane] = t1;
+            }
+            __syncthreads(); // buffer consumed: refill it
+            if (s == 0) issue_stage(cbuf + par * kStageFloats, p0, p1, 2);
+            else if (s == 1 && has_next) issue_stage(cbuf + (par ^ 1) * kStageFloats, n0, n1, 0);
+            else if (s == 2 && has_next) issue_stage(cbuf + par * kStageFloats, n0, n1, 1);
+        }
+        par ^= 1;
+        primed = has_next;
+    } else {
+        // ---- codebooks of both parts [2][3][256][8]
+        const float *p0, *p1;
+        unit_codebooks<kDown>(A, U, p0, p1);
+        float4 *cbs = reinterpret_cast<float4 *>(smem);
+        for (int i = threadIdx.x; i < 2 * kCbFloats / 4; i += kThreads) {
+            const float *src = (i < kCbFloats / 4) ? p0 : p1;
+            const int ii = i % (kCbFloats / 4);
+            cbs[i] = __ldg(reinterpret_cast<const float4 *>(src) + ii);
+        }
+        __syncthreads();
+    }
+
+    // ---- stream the codes of rows [g0, g1) x this unit's segment(s).  Registers hold
+    // the next row group's codes while the current one is consumed (ping-pong), and L2
+    // is asked for the row group kPrefetchRounds rounds ahead -- past the end of the
+    // unit, for the next unit's first row groups.
+    const uint8_t *pb0 = b4 ? U.base[1] : U.base[0];
+    const uint8_t *pb1 = b4 ? U.base[0] : U.base[1];
+    const unsigned char *tabb = smem;
+    auto load = [&](int g, uint4 (&w)[2][kStages]) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) {
+            const size_t co = ((size_t)g * kStages + s) * 512 + (size_t)lane * 16;
+            w[0][s] = pb0 ? ld_stream(pb0 + co) : make_uint4(0, 0, 0, 0);
+            w[1][s] = pb1 ? ld_stream(pb1 + co) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto ahead = [&](int g) {
+        const int ga = g + kPrefetchRounds * kWarps;
+        if (ga < U.g1) prefetch_group(U, ga, lane);
+        else if (has_next) {
+            const int gn = N.g0 + (ga - U.g1);
+            if (gn < N.g1) prefetch_group(N, gn, lane);
+        }
+    };
+    auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
+        float acc[32];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const uint32_t colb = p ? colb1 : colb0;
+#pragma unroll
+            for (int wd = 0; wd < 4; ++wd) {
+                const uint32_t w0 = comp(cw[p][0], wd), w1 = comp(cw[p][1], wd), w2 = comp(cw[p][2], wd);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if constexpr (!kRecon) {
+                        const uint32_t sel = 0x7604u | ((uint32_t)b << 4);
+                        const uint32_t a0 = __byte_perm(w0, colb, sel);
+                        const uint32_t a1 = __byte_perm(w1, colb, sel);
+                        const uint32_t a2 = __byte_perm(w2, colb, sel);
+                        const float t0 = *reinterpret_cast<const float *>(tabb + a0);
+                        const float t1 = *reinterpret_cast<const float *>(tabb + kTabStage + a1);
+                        const float t2 = *reinterpret_cast<const float *>(tabb + 2 * kTabStage + a2);
+                        acc[16 * p + 4 * wd + b] = (t0 + t1) + t2;
+                    } else {
+                        const int part = p ^ b4;
+                        const float *cbs = reinterpret_cast<const float *>(smem) + part * kCbFloats;
+                        const int c0 = (w0 >> (8 * b)) & 255, c1 = (w1 >> (8 * b)) & 255,
+                                  c2 = (w2 >> (8 * b)) & 255;
+                        const float4 *r0 = reinterpret_cast<const float4 *>(cbs + c0 * kVec);
+                        const float4 *r1 = reinterpret_cast<const float4 *>(cbs + kCodes * kVec + c1 * kVec);
+                        const float4 *r2 = reinterpret_cast<const float4 *>(cbs + 2 * kCodes * kVec + c2 * kVec);
+                        const float4 a0 = r0[0], a1 = r0[1], b0 = r1[0], b1 = r1[1], d0 = r2[0], d1 = r2[1];
+                        const float *x = xr[p];
+                        float sacc = ((a0.x + b0.x) + d0.x) * x[0];
+                        sacc = fmaf((a0.y + b0.y) + d0.y, x[1], sacc);
+                        sacc = fmaf((a0.z + b0.z) + d0.z, x[2], sacc);
+                        sacc = fmaf((a0.w + b0.w) + d0.w, x[3], sacc);
+                        sacc = fmaf((a1.x + b1.x) + d1.x, x[4], sacc);
+                        sacc = fmaf((a1.y + b1.y) + d1.y, x[5], sacc);
+                        sacc = fmaf((a1.z + b1.z) + d1.z, x[6], sacc);
+                        sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
+                        acc[16 * p + 4 * wd + b] = sacc;
+                    }
+                }
+            }
+        }
+        // slot i of lane l holds row (l ^ i) of the 32 (part, row) pairs: reduce-scatter
+#pragma unroll
+        for (int n = 16; n >= 1; n >>= 1)
+#pragma unroll
+            for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
+        const int row = g * kGroupRows + (lane & 15);
+        if constexpr (!kDown) {
+            if (row < G.n_out)
+                A.part_gu[(((size_t)U.slot * A.gu.nseg + U.seg0) * 2 + b4) * G.n_out + row] = acc[0];
+        } else {
+            const float v = acc[0] + __shfl_xor_sync(0xffffffffu, acc[0], 16);
+            if (lane < 16 && row < G.n_out)
+                A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = v;
+        }
+    };
+    uint4 wa[2][kStages], wb[2][kStages];
+    int g = U.g0 + warp;
+    if (g < U.g1) load(g, wa);
+    while (g < U.g1) {
+        if (g + kWarps < U.g1) load(g + kWarps, wb);
+        ahead(g);
+        consume(wa, g);
+        g += kWarps;
+        if (g >= U.g1) break;
+        if (g + kWarps < U.g1) load(g + kWarps, wa);
+        ahead(g);
+        consume(wb, g);
+        g += kWarps;
+    }
+    // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
+    // and the slot's codebooks once
+    if (threadIdx.x == 0 && valid && A.stats) {
+        unsigned long long vecs = 0;
+        for (int p = 0; p < 2; ++p) {
+            const int seg = kDown ? U.seg0 + p : U.seg0;
+            if (seg < G.nseg) vecs += (unsigned long long)min(kSegVec, G.nv - seg * kSegVec);
+        }
+        const int rows = min(G.n_out, U.g1 * kGroupRows) - U.g0 * kGroupRows;
+        atomicAdd(A.stats + kStatDemandCode, vecs * (unsigned long long)rows * kStages);
+        const bool first = kDown ? (U.seg0 == 0 && U.g0 == 0) : (U.seg0 == 0);
+        if (first)
+            atomicAdd(A.stats + kStatCodebook,
+                      (unsigned long long)(kDown ? 1 : 2) * kCbFloats * sizeof(float));
+    }
+}
+
+// Bytes of dynamic shared memory of a unit.
+template <bool kRecon>
+constexpr size_t unit_smem() {
+    return (kRecon ? 2 * kCbFloats * 4 : kTabBytes + 2 * kStageBuf) + kXsFloats * 4;
+}
+
+} // namespace lut
+} // namespace wm

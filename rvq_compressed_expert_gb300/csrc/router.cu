@@ -6,48 +6,16 @@
 // Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Lecture anticipée et
 // prédiction du routeur").  Order: logit descending, lowest index first on
 // equal logits; gates: softmax over the k selected logits.
-#include "common.cuh"
-
-#include <float.h>
+#include "route_dev.cuh"
 
 namespace wm {
 
+using namespace route;
+
 namespace {
 
-template <bool kBf16>
-__device__ __forceinline__ float4 load_h4(const void *h, size_t elem) {
-    if constexpr (kBf16) {
-        const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(h) + elem;
-        uint2 raw = *reinterpret_cast<const uint2 *>(p);
-        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&raw.x);
-        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&raw.y);
-        float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
-        return make_float4(fa.x, fa.y, fb.x, fb.y);
-    } else {
-        return *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(h) + elem);
-    }
-}
-
-template <bool kBf16>
-__device__ __forceinline__ float load_h1(const void *h, size_t elem) {
-    if constexpr (kBf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(h)[elem]);
-    else return reinterpret_cast<const float *>(h)[elem];
-}
-
-// hi + lo == a + b exactly (Knuth's TwoSum); keeps the part of the dot product
-// that adding a large bias would round away, so gate ratios stay accurate.
-__device__ __forceinline__ void two_sum(float a, float b, float &hi, float &lo) {
-    hi = __fadd_rn(a, b);
-    const float bb = __fsub_rn(hi, a);
-    lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
-}
-
-// Small-T router: 2 experts per CTA, 4 warps per expert row (each takes every
-// 4th float4 of the row, 8 loads in flight per lane), up to 8 tokens per pass
-// sharing each W_r load.
+// Small-T router: 2 experts per CTA of 256 threads.
 constexpr int kRouterRows = 2;
-constexpr int kRouterTok = 8;
-constexpr int kRouterBatch = 8;
 
 template <bool kBf16>
 __global__ void __launch_bounds__(256) router_small_kernel(const float *__restrict__ W,
@@ -57,63 +25,7 @@ __global__ void __launch_bounds__(256) router_small_kernel(const float *__restri
                                                            float *__restrict__ logits,
                                                            float *__restrict__ logits_lo) {
     __shared__ float red[kRouterRows][4][kRouterTok];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row_local = warp >> 2, sub = warp & 3;
-    const int row = blockIdx.x * kRouterRows + row_local;
-    const int d4 = d >> 2;
-    const int per_lane = (d4 + 127) / 128;
-    for (int t0 = 0; t0 < T; t0 += kRouterTok) {
-        const int nt = min(kRouterTok, T - t0);
-        float acc[kRouterTok];
-#pragma unroll
-        for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.f;
-        if (row < E) {
-            const float4 *w4 = reinterpret_cast<const float4 *>(W + (size_t)row * d);
-            for (int m0 = 0; m0 < per_lane; m0 += kRouterBatch) {
-                float4 w[kRouterBatch];
-#pragma unroll
-                for (int u = 0; u < kRouterBatch; ++u) {
-                    const int i4 = sub * 32 + lane + 128 * (m0 + u);
-                    w[u] = (i4 < d4) ? __ldg(w4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int u = 0; u < kRouterBatch; ++u) {
-                    const int i4 = sub * 32 + lane + 128 * (m0 + u);
-                    if (i4 >= d4) continue;
-#pragma unroll
-                    for (int t = 0; t < kRouterTok; ++t) {
-                        if (t < nt) {
-                            const float4 x = load_h4<kBf16>(h, (size_t)(t0 + t) * d + (size_t)i4 * 4);
-                            acc[t] = fmaf(w[u].x, x.x, acc[t]);
-                            acc[t] = fmaf(w[u].y, x.y, acc[t]);
-                            acc[t] = fmaf(w[u].z, x.z, acc[t]);
-                            acc[t] = fmaf(w[u].w, x.w, acc[t]);
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < kRouterTok; ++t) {
-            float v = acc[t];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) red[row_local][sub][t] = v;
-        }
-        __syncthreads();
-        if (threadIdx.x < kRouterRows * kRouterTok) {
-            const int rl = threadIdx.x / kRouterTok, t = threadIdx.x % kRouterTok;
-            const int r = blockIdx.x * kRouterRows + rl;
-            if (r < E && t < nt) {
-                float v = ((red[rl][0][t] + red[rl][1][t]) + red[rl][2][t]) + red[rl][3][t];
-                float hi = v, lo = 0.f;
-                if (bias) two_sum(v, bias[r], hi, lo);
-                logits[(size_t)(t0 + t) * E + r] = hi;
-                if (logits_lo) logits_lo[(size_t)(t0 + t) * E + r] = lo;
-            }
-        }
-        __syncthreads();
-    }
+    router_block<kBf16>(W, bias, h, T, E, d, blockIdx.x * kRouterRows, logits, logits_lo, red);
 }
 
 // Larger T: 64 tokens x 64 experts per CTA, 256 threads with 4x4 outputs each,
@@ -177,17 +89,7 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const float *__restri
     }
 }
 
-// Routing order: larger logit first (hi, then the exact remainder lo), lower
-// index on ties.
-__device__ __forceinline__ bool ranks_before(float ha, float la, int ia, float hb, float lb, int ib) {
-    if (ha != hb) return ha > hb;
-    if (la != lb) return la > lb;
-    return ia < ib;
-}
-
-// One warp per token.  Logits staged in shared memory; k rounds of a warp
-// arg-max that skips taken experts; softmax over the k selected logits with
-// the differences taken as (hi_i - hi_0) + (lo_i - lo_0).
+// One warp per token.
 __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logits,
                                                   const float *__restrict__ logits_lo, int E, int k,
                                                   int32_t *__restrict__ idx,
@@ -198,97 +100,8 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
                                                   unsigned long long *__restrict__ stats,
                                                   unsigned long long router_bytes) {
     extern __shared__ float smem_topk[];
-    float *lv = smem_topk;
-    float *lw = lv + E;
-    unsigned char *taken = reinterpret_cast<unsigned char *>(lw + E);
-    const int t = blockIdx.x, lane = threadIdx.x;
-#pragma unroll 8
-    for (int e = lane; e < E; e += 32) {
-        // canonical keys make the order total: -0 equals +0, and a NaN (outside the
-        // contract) ranks as -inf, so every lane agrees on each round's winner
-        float vh = logits[(size_t)t * E + e];
-        float vl = logits_lo ? logits_lo[(size_t)t * E + e] : 0.f;
-        if (vh != vh) vh = -INFINITY;
-        if (vh == 0.f) vh = 0.f;
-        if (vl != vl || vl == 0.f) vl = 0.f;
-        lv[e] = vh;
-        lw[e] = vl;
-        taken[e] = 0;
-    }
-    __syncwarp();
-    constexpr int kNone = 0x7fffffff;
-    // each lane keeps the best untaken expert of its stripe e = lane (mod 32); a round
-    // picks the best head across the warp, and only the owning lane rescans its stripe
-    float hh = 0.f, hl = 0.f;
-    int hidx = kNone;
-    auto rescan = [&]() {
-        hidx = kNone;
-#pragma unroll 4
-        for (int e = lane; e < E; e += 32) {
-            if (taken[e]) continue;
-            const float vh = lv[e], vl = lw[e];
-            if (hidx == kNone || ranks_before(vh, vl, e, hh, hl, hidx)) {
-                hh = vh;
-                hl = vl;
-                hidx = e;
-            }
-        }
-    };
-    rescan();
-    int my_idx = -1;
-    float my_hi = 0.f, my_lo = 0.f;
-    for (int r = 0; r < k; ++r) {
-        float bh = hh, bl = hl;
-        int bi = hidx;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
-            const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != kNone && (bi == kNone || ranks_before(oh, ol, oi, bh, bl, bi))) {
-                bh = oh;
-                bl = ol;
-                bi = oi;
-            }
-        }
-        if (lane == r) {
-            my_idx = bi;
-            my_hi = bh;
-            my_lo = bl;
-        }
-        if (bi != kNone && lane == (bi & 31)) {
-            taken[bi] = 1;
-            rescan();
-        }
-    }
-    // softmax over the selected logits; rank 0 holds the largest
-    const float h0 = __shfl_sync(0xffffffffu, my_hi, 0);
-    const float l0 = __shfl_sync(0xffffffffu, my_lo, 0);
-    const float diff = (lane == 0) ? 0.f : __fsub_rn(my_hi, h0) + __fsub_rn(my_lo, l0);
-    float ex = (lane < k) ? expf(diff) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane < k) {
-        idx[(size_t)t * k + lane] = my_idx;
-        gate[(size_t)t * k + lane] = ex / sum;
-    }
-    if (pred_count != nullptr) {
-        const int P = pred_count[t];
-        bool hit = false;
-        if (lane < k)
-            for (int p = 0; p < P; ++p) hit |= (pred_idx[(size_t)t * pred_stride + p] == my_idx);
-        const unsigned hits = __popc(__ballot_sync(0xffffffffu, hit));
-        __syncwarp();
-        if (lane == 0) {
-            if (P > 0) atomicAdd(stats + kStatPredHits, (unsigned long long)hits);
-            pred_count[t] = 0;
-        }
-    }
-    if (lane == 0 && stats) {
-        atomicAdd(stats + kStatRoutedSlots, (unsigned long long)k);
-        if (t == 0) atomicAdd(stats + kStatRouter, router_bytes);
-    }
+    topk_warp(logits, logits_lo, E, k, blockIdx.x, idx, gate, pred_idx, pred_count, pred_stride,
+              stats, router_bytes, smem_topk);
 }
 
 // L2 prefetch of predicted experts' records: one CTA per (token, rank);

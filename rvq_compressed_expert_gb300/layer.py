@@ -66,6 +66,9 @@ class MoELayer:
     def forward(self, h, T, idx, gate, out, mode=0, stream=None):
         B.waste_moe_forward(self.handle, h, T, idx, gate, out, mode, stream)
 
+    def step(self, h, T, idx, gate, out, mode=0, logits=None, stream=None):
+        B.waste_moe_step(self.handle, h, T, idx, gate, logits, out, mode, stream)
+
     def prefetch(self, h, T, n=-1, stream=None):
         B.waste_moe_prefetch(self.handle, h, T, n, stream)
 

@@ -8,7 +8,7 @@ routeur"):
   - on a side stream, layer L+1's router runs on x_L and its top-P experts are
     prefetched into L2 (waste_moe_prefetch),
   - on the main stream layer L routes x_L and applies its experts:
-    h_{L+1} = h_L + combine (waste_moe_forward, mode 1, in place).
+    h_{L+1} = h_L + combine (waste_moe_step, mode 1, in place).
 The real router of each layer decides its experts, so the lookahead changes
 neither the outputs nor the demand bytes.  x alternates between two buffers so
 the side stream can still read x_L while x_{L+1} is written; layer L+1 routes
@@ -53,10 +53,10 @@ class DecodeStack:
                 ev.record(side)
             if pending is not None:
                 main.wait_event(pending)  # layer L's prediction is in place before it routes
-            self.layers[L].route(x, T, self.idx, self.gate, stream=main)
+            # route + experts + combine (h += combine) in one launch
+            self.layers[L].step(x, T, self.idx, self.gate, self.h, 1, stream=main)
             if on_layer is not None:
                 on_layer(L, self.idx, self.gate, main)
-            self.layers[L].forward(x, T, self.idx, self.gate, self.h, 1, stream=main)
             pending = ev
         if pending is not None:
             main.wait_event(pending)

@@ -248,6 +248,32 @@ def test_bad_expert_index_flagged():
         layer.close()
 
 
+@pytest.mark.parametrize("shape", [(1032, 136, 12, 3, 5), (256, 128, 8, 2, 4), (8, 8, 2, 1, 2)])
+def test_fused_step_equals_phases(shape):
+    """The one-kernel step (route + forward) and forward through the fused kernel equal the
+    per-phase kernels bit for bit, over several launches in a row (the device queue and
+    counters must come back to zero after every launch)."""
+    d, f, E, k, T = shape
+    w, li, h, fused = small_layer(d, f, E, k, T)
+    _, _, _, phases = small_layer(d, f, E, k, T, flags=B.FLAG_UNFUSED)
+    try:
+        hd = h.cuda()
+        ref = run(phases, hd, T)
+        for _ in range(3):
+            idx, gate, logits, out = fused.alloc_outputs(T)
+            fused.step(hd, T, idx, gate, out, 0, logits)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(idx.cpu().numpy(), ref[0])
+            assert np.array_equal(gate.cpu().numpy().view(np.uint32), ref[1].view(np.uint32))
+            assert np.array_equal(out.cpu().numpy().view(np.uint32), ref[3].view(np.uint32))
+            got = run(fused, hd, T)  # route, then forward through the fused kernel
+            assert np.array_equal(got[3].view(np.uint32), ref[3].view(np.uint32))
+        fused.stats()  # no timeout or bad index recorded
+    finally:
+        fused.close()
+        phases.close()
+
+
 def test_deterministic():
     d, f, E, k, T = 1032, 136, 12, 3, 5
     w, li, h, layer = small_layer(d, f, E, k, T)
