@@ -227,6 +227,32 @@ def run_decode(args, dev, out):
         total_ms = float(t.item())
     st = layer.stats()
 
+    # the same step with each phase as its own kernel (router, top-k, gate/up, down, combine),
+    # on a second handle over the same weights, for comparison
+    ucfg = B.make_config(w.d, w.f, w.n_experts, w.top_k, w.act_dtype, 1, 0,
+                         B.FLAG_UNFUSED, layer.layer)
+    uh = B.waste_moe_create(ucfg, layer.router_w, layer.router_b, layer.records, layer.stride,
+                            layer.codebooks)
+    with torch.cuda.stream(side):
+        for i in range(3):
+            B.waste_moe_step(uh, h_in, 1, idx, gate, logits, y, 0)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ug = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ug):
+        B.waste_moe_step(uh, h_in, 1, idx, gate, logits, y, 0)
+    uev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        h_in.copy_(pool[i % DECODE_POOL])
+        flush.zero_()
+        uev[i][0].record(stream)
+        ug.replay()
+        uev[i][1].record(stream)
+    torch.cuda.synchronize()
+    unfused_ms = sum(a.elapsed_time(b) for a, b in uev) / K
+    del ug
+    B.waste_moe_destroy(uh)
+
     # per-kernel device times: the same step launched directly with CUDA events between
     # its kernels, queued behind a short spin kernel so launches never starve the GPU
     B.waste_moe_set_profiling(layer.handle, True)
@@ -250,7 +276,7 @@ def run_decode(args, dev, out):
                          gate_up_bytes=gu_bytes, down_bytes=dn_bytes,
                          hbm_gbs_step=step_bytes / (ms_per_step * 1e-3) / 1e9,
                          median_step_ms=statistics.median(step_ms),
-                         launches_per_step=1, profiled_steps=n_prof)
+                         launches_per_step=1, profiled_steps=n_prof, unfused_ms=unfused_ms)
 
     # ---- end to end through the C ABI with host buffers: h2d copy of the token from
     # pinned memory, route, forward, d2h copy of the result -- one graph per step
@@ -468,6 +494,7 @@ def native(args):
             "hbm_gbs_whole_step": d["hbm_gbs_step"],
             "algorithmic_bytes_per_step": d["step_bytes"],
             "kernels_ms": kern,
+            "ms_per_step_phase_kernels": d["unfused_ms"],
         },
         "roofline": {
             "bound": "hbm",

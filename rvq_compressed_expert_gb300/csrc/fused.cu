@@ -107,83 +107,88 @@ __device__ void combine_item(const FusedArgs &F, int r0, int r1) {
     }
 }
 
+// Queue layout helpers: item boundaries and counters are recomputed from the
+// kernel parameters where needed, so little state stays live across a unit.
+__device__ __forceinline__ int b_topk(const FusedArgs &F) { return F.n_router; }
+__device__ __forceinline__ int b_gu(const FusedArgs &F) { return F.n_router + F.n_topk; }
+__device__ __forceinline__ int b_dn(const FusedArgs &F) { return b_gu(F) + F.n_gu; }
+__device__ __forceinline__ int b_comb(const FusedArgs &F) { return b_dn(F) + F.n_dn; }
+__device__ __forceinline__ int n_total(const FusedArgs &F) { return b_comb(F) + F.n_comb; }
+__device__ __forceinline__ unsigned *gu_done(const FusedArgs &F) { return F.sync + 4; }
+__device__ __forceinline__ unsigned *dn_done(const FusedArgs &F) { return F.sync + 4 + F.A.slots; }
+
 template <bool kRecon, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs F) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ float red[kRouterRowsPerItem][4][kRouterTok];
     __shared__ int claimed;
-    const LutArgs &A = F.A;
-    unsigned *queue = F.sync, *exited = F.sync + 1, *router_done = F.sync + 2,
-             *topk_done = F.sync + 3, *gu_done = F.sync + 4, *dn_done = F.sync + 4 + A.slots;
-    const int b_topk = F.n_router, b_gu = b_topk + F.n_topk, b_dn = b_gu + F.n_gu,
-              b_comb = b_dn + F.n_dn, total = b_comb + F.n_comb;
     int par = 0;
     bool primed = false;
-    int cur = claim(queue, &claimed);
-    int nxt = claim(queue, &claimed);
-    while (cur < total) {
-        if (cur < b_topk) {
+    int cur = claim(F.sync, &claimed);
+    int nxt = claim(F.sync, &claimed);
+    while (cur < n_total(F)) {
+        if (cur < b_topk(F)) {
             // ---- router rows
-            router_block<kBf16>(F.router_w, F.router_b, A.h, F.T, A.E, F.d, cur * kRouterRowsPerItem,
+            router_block<kBf16>(F.router_w, F.router_b, F.A.h, F.T, F.A.E, F.d, cur * kRouterRowsPerItem,
                                 F.logits, F.logits_lo, red);
-            signal(router_done);
-        } else if (cur < b_gu) {
+            signal(F.sync + 2);
+        } else if (cur < b_gu(F)) {
             // ---- top-k + softmax of every token, one warp per token
-            wait_counter(router_done, (unsigned)F.n_router, A.err);
+            wait_counter(F.sync + 2, (unsigned)F.n_router, F.A.err);
             const int warp = threadIdx.x >> 5;
-            float *area = reinterpret_cast<float *>(smem) + (size_t)warp * ((A.E * 9 + 15) / 16 * 4);
+            float *area = reinterpret_cast<float *>(smem) + (size_t)warp * ((F.A.E * 9 + 15) / 16 * 4);
             for (int t = warp; t < F.T; t += kWarps)
-                topk_warp(F.logits, F.logits_lo, A.E, A.k, t, F.idx_out, F.gate_out, F.pred_idx,
-                          F.pred_count, F.pred_stride, A.stats, F.router_bytes, area);
+                topk_warp(F.logits, F.logits_lo, F.A.E, F.A.k, t, F.idx_out, F.gate_out, F.pred_idx,
+                          F.pred_count, F.pred_stride, F.A.stats, F.router_bytes, area);
             __syncthreads();
             if (threadIdx.x == 0) {
                 __threadfence();
-                atomicExch(topk_done, 1u);
+                atomicExch(F.sync + 3, 1u);
             }
-        } else if (cur < b_dn) {
+        } else if (cur < b_dn(F)) {
             // ---- gate/up unit
-            if (F.with_route) wait_counter(topk_done, 1u, A.err);
-            const Unit U = decode_unit<false>(A, cur - b_gu);
-            const bool has_next = nxt >= b_gu && nxt < b_dn;
+            if (F.with_route) wait_counter(F.sync + 3, 1u, F.A.err);
+            const Unit U = decode_unit<false>(F.A, cur - b_gu(F));
+            const bool has_next = nxt >= b_gu(F) && nxt < b_dn(F);
             Unit N;
-            if (has_next) N = decode_unit<false>(A, nxt - b_gu);
-            run_unit<false, kRecon, kBf16>(A, U, has_next, N, par, primed, nullptr, 0, smem);
-            signal(gu_done + U.slot);
-        } else if (cur < b_comb) {
+            if (has_next) N = decode_unit<false>(F.A, nxt - b_gu(F));
+            run_unit<false, kRecon, kBf16>(F.A, U, has_next, N, par, primed, nullptr, 0, smem);
+            signal(gu_done(F) + U.slot);
+        } else if (cur < b_comb(F)) {
             // ---- down unit (waits inside for the gate/up units of its slot)
-            if (F.with_route) wait_counter(topk_done, 1u, A.err);
-            const int u = cur - b_dn;
-            const Unit U = decode_unit<true>(A, u);
-            const bool has_next = nxt >= b_dn && nxt < b_comb;
+            if (F.with_route) wait_counter(F.sync + 3, 1u, F.A.err);
+            const int u = cur - b_dn(F);
+            const Unit U = decode_unit<true>(F.A, u);
+            const bool has_next = nxt >= b_dn(F) && nxt < b_comb(F);
             Unit N;
-            if (has_next) N = decode_unit<true>(A, nxt - b_dn);
-            run_unit<true, kRecon, kBf16>(A, U, has_next, N, par, primed, gu_done + U.slot,
-                                          (unsigned)A.gu.nseg, smem);
-            signal(dn_done + (u % A.nrb));
+            if (has_next) N = decode_unit<true>(F.A, nxt - b_dn(F));
+            run_unit<true, kRecon, kBf16>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot,
+                                          (unsigned)F.A.gu.nseg, smem);
+            signal(dn_done(F) + (u % F.A.nrb));
         } else {
             // ---- combine rows [r0, r1) once every down unit over them is done
-            const int r0 = (cur - b_comb) * kCombineRows;
+            const int r0 = (cur - b_comb(F)) * kCombineRows;
             const int r1 = min(F.d, r0 + kCombineRows);
-            const int rb0 = (r0 / kGroupRows) / A.rb_groups;
-            const int rb1 = ((r1 - 1) / kGroupRows) / A.rb_groups;
+            const int rb0 = (r0 / kGroupRows) / F.A.rb_groups;
+            const int rb1 = ((r1 - 1) / kGroupRows) / F.A.rb_groups;
             for (int rb = rb0; rb <= rb1; ++rb)
-                wait_counter(dn_done + rb, (unsigned)(A.slots * A.npair), A.err);
+                wait_counter(dn_done(F) + rb, (unsigned)(F.A.slots * F.A.npair), F.A.err);
             combine_item(F, r0, r1);
-            if (cur == b_comb && threadIdx.x == 0 && A.stats)
-                atomicAdd(A.stats + kStatForwardSlots, (unsigned long long)A.slots);
+            if (cur == b_comb(F) && threadIdx.x == 0 && F.A.stats)
+                atomicAdd(F.A.stats + kStatForwardSlots, (unsigned long long)F.A.slots);
         }
         cur = nxt;
-        nxt = claim(queue, &claimed);
+        nxt = claim(F.sync, &claimed);
     }
     if constexpr (!kRecon) cp_async_wait<0>();
     // the last CTA to leave puts the queue and counters back to zero
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        const unsigned left = atomicAdd(exited, 1u);
+        const unsigned left = atomicAdd(F.sync + 1, 1u);
         if (left == gridDim.x - 1) {
             __threadfence();
-            const int n = 4 + A.slots + A.nrb;
+            const int n = 4 + F.A.slots + F.A.nrb;
             for (int i = 0; i < n; ++i) F.sync[i] = 0u;
             __threadfence();
         }

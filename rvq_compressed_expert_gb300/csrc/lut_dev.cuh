@@ -217,7 +217,7 @@ __device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target,
 // into the buffers when this one returns.  For a down unit, `dep` (if not null) is a
 // completion counter that must reach dep_target before the gate/up partials are read.
 template <bool kDown, bool kRecon, bool kBf16>
-__device__ __noinline__ void run_unit(const LutArgs &A, const Unit &U, bool has_next, const Unit &N,
+__device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &U, bool has_next, const Unit &N,
                                          int &par, bool &primed, const unsigned *dep,
                                          unsigned dep_target, unsigned char *smem) {
     float *cbuf = reinterpret_cast<float *>(smem + kTabBytes);
