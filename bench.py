@@ -582,12 +582,56 @@ def profile_case(args):
     w = synth.Workload("decode-e32", 7168, 1536, 32, 16, 1, "f32", "offsets")
     layer = MoELayer(w, seed=0, layer=0, device="cuda")
     idx, gate, logits, y = layer.alloc_outputs(1)
+    trace = None
+    if args.trace:
+        trace = torch.zeros(4096 * 4, dtype=torch.int64, device="cuda")
+        B.waste_moe_set_trace(layer.handle, trace, 4096)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     for i in range(args.warmup + args.steps):
         h = synth.hidden(100 + i, 1, w.d, "f32", "cuda")
+        if trace is not None:
+            flush.zero_()
+            trace.zero_()
         layer.step(h, 1, idx, gate, y, 0, logits)
+        if trace is not None and i >= args.warmup:
+            torch.cuda.synchronize()
+            print_trace(trace.view(-1, 4).cpu(), w)
     torch.cuda.synchronize()
     layer.close()
     print("profile case done")
+
+
+def print_trace(tr, w):
+    """Phase timeline of one step-kernel launch from its item trace."""
+    import math as _m
+    n_router = (w.n_experts + 3) // 4
+    slots = w.tokens * w.top_k
+    nseg = _m.ceil(w.d / 8 / 32)
+    rows = [r for r in tr.tolist() if r[1] > 0]
+    if not rows:
+        print("no trace")
+        return
+    t0 = min(r[0] for r in rows)
+    n_gu = slots * nseg
+    bounds = [("router", 0, n_router), ("topk", n_router, n_router + 1),
+              ("gate_up", n_router + 1, n_router + 1 + n_gu)]
+    dn0 = n_router + 1 + n_gu
+    n_items = len(tr)
+    used = [i for i in range(n_items) if tr[i][1] > 0]
+    last = max(used)
+    n_comb = _m.ceil(w.d / 256)
+    bounds += [("down", dn0, last + 1 - n_comb), ("combine", last + 1 - n_comb, last + 1)]
+    out = []
+    for name, a, b in bounds:
+        its = [tr[i].tolist() for i in range(a, b) if tr[i][1] > 0]
+        if not its:
+            continue
+        st = [(x[0] - t0) / 1e3 for x in its]
+        en = [(x[1] - t0) / 1e3 for x in its]
+        du = [(x[1] - x[0]) / 1e3 for x in its]
+        out.append(f"{name}: n={len(its)} start {min(st):.1f}-{max(st):.1f} end {min(en):.1f}-{max(en):.1f} "
+                   f"dur mean {sum(du)/len(du):.2f} max {max(du):.2f} us")
+    print(" | ".join(out))
 
 
 def main():
@@ -600,6 +644,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", action="store_true",
                     help="run a small decode case for ncu captures and exit")
+    ap.add_argument("--trace", action="store_true",
+                    help="with --profile-case: print the step kernel's item timeline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

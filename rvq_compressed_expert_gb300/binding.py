@@ -33,7 +33,7 @@ EXPORTED = ["waste_moe_record_layout", "waste_moe_pack_records", "waste_moe_crea
             "waste_moe_route", "waste_moe_forward", "waste_moe_prefetch", "waste_moe_destroy",
             "waste_moe_stats", "waste_moe_reset_stats", "waste_moe_last_error",
             "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile",
-            "waste_moe_rmsnorm", "waste_moe_forward_noalloc", "waste_moe_step"]
+            "waste_moe_rmsnorm", "waste_moe_forward_noalloc", "waste_moe_step", "waste_moe_set_trace"]
 
 
 class waste_moe_config(ctypes.Structure):
@@ -99,6 +99,7 @@ def load(path: str = LIB_PATH):
     lib.waste_moe_read_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_float)]
     lib.waste_moe_rmsnorm.argtypes = [vp, vp, i32, i32, vp]
     lib.waste_moe_step.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, vp]
+    lib.waste_moe_set_trace.argtypes = [vp, vp, i32]
     lib.waste_moe_forward_noalloc.argtypes = [cfgp, vp, sz, vp, vp, i32, vp, vp, vp, i32, vp]
     for name in EXPORTED:
         if name not in ("waste_moe_destroy", "waste_moe_last_error"):
@@ -177,6 +178,11 @@ def waste_moe_forward(h, d_h, T, d_idx, d_gate, d_out, mode=0, stream=None):
 def waste_moe_step(h, d_h, T, d_idx, d_gate, d_logits, d_out, mode=0, stream=None):
     return _check(load().waste_moe_step(h, _ptr(d_h), T, _ptr(d_idx), _ptr(d_gate), _ptr(d_logits),
                                         _ptr(d_out), mode, _stream(stream)))
+
+
+def waste_moe_set_trace(h, d_trace, n_items):
+    """Record {start ns, end ns, SM, CTA} per work item of the step kernel into d_trace."""
+    return _check(load().waste_moe_set_trace(h, _ptr(d_trace), n_items))
 
 
 def waste_moe_prefetch(next_layer, d_h, T, n_prefetch=-1, side=None):

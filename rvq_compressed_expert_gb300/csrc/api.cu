@@ -21,6 +21,8 @@ struct waste_moe {
     int pred_P; // experts per token of the last prefetch into this layer
     bool profiling;
     Timing route_tm, fwd_tm, step_tm;
+    unsigned long long *trace; // caller's trace buffer for the step kernel, or null
+    int trace_cap;
 };
 
 namespace {
@@ -219,6 +221,8 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     H->max_slots = cfg->max_tokens * cfg->top_k;
     H->pred_P = 0;
     H->profiling = false;
+    H->trace = nullptr;
+    H->trace_cap = 0;
     LayerView &L = H->L;
     L.router_w = d_router_w;
     L.router_b = d_router_bias;
@@ -397,7 +401,7 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
         if (h->profiling) cudaEventRecord(h->step_tm.ev[0], s);
         e = launch_fused_step(h->L, h->W, d_h, T, false, const_cast<int32_t *>(d_idx),
                               const_cast<float *>(d_gate), nullptr, nullptr, nullptr, 1, d_out, mode,
-                              recon, h->num_sms, s);
+                              recon, h->num_sms, s, h->trace, h->trace_cap);
         if (h->profiling) {
             cudaEventRecord(h->step_tm.ev[1], s);
             h->step_tm.n = 2;
@@ -409,6 +413,14 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
         if (h->profiling) h->step_tm.n = 0;
     }
     if (e != cudaSuccess) return cuda_fail(e, "expert kernels");
+    return ok();
+}
+
+int waste_moe_set_trace(waste_moe *h, uint64_t *d_trace, int32_t n_items) {
+    if (!h) return fail(WASTE_EINVAL, "NULL handle");
+    if (n_items < 0 || (n_items > 0 && !d_trace)) return fail(WASTE_EINVAL, "bad trace buffer");
+    h->trace = n_items ? reinterpret_cast<unsigned long long *>(d_trace) : nullptr;
+    h->trace_cap = n_items;
     return ok();
 }
 
@@ -431,7 +443,8 @@ int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, flo
     if (h->profiling) cudaEventRecord(h->step_tm.ev[0], s);
     cudaError_t e = launch_fused_step(h->L, h->W, d_h, T, true, d_idx, d_gate,
                                       d_logits ? d_logits : h->W.logits, h->W.pred_idx, h->W.pred_count,
-                                      h->pred_P > 0 ? h->pred_P : 1, d_out, mode, recon, h->num_sms, s);
+                                      h->pred_P > 0 ? h->pred_P : 1, d_out, mode, recon, h->num_sms, s,
+                                      h->trace, h->trace_cap);
     if (h->profiling) {
         cudaEventRecord(h->step_tm.ev[1], s);
         h->step_tm.n = 2;

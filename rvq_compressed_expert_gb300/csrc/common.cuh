@@ -114,7 +114,8 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
                               bool with_route, int32_t *idx, float *gate, float *logits,
                               const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
                               float *out, int mode, bool reconstruct, int num_sms,
-                              cudaStream_t s);
+                              cudaStream_t s, unsigned long long *trace = nullptr,
+                              int trace_cap = 0);
 cudaError_t launch_prefetch_l2(const LayerView &L, const int32_t *pred_idx, int pred_stride,
                                int T, int P, int32_t *pred_count, unsigned long long *stats,
                                cudaStream_t s);

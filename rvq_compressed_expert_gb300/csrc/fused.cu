@@ -50,7 +50,22 @@ struct FusedArgs {
     // [4, 4 + slots) gate/up units done per slot, then down units done per row block
     unsigned *sync;
     int n_router, n_topk, n_gu, n_dn, n_comb;
+    // optional item trace: per item {start ns, end ns, SM id, CTA} (null = off)
+    unsigned long long *trace;
+    int trace_cap;
 };
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ unsigned smid() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %smid;" : "=r"(r));
+    return r;
+}
 
 __device__ __forceinline__ void signal(unsigned *c) {
     __syncthreads();
@@ -127,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
     int cur = claim(F.sync, &claimed);
     int nxt = claim(F.sync, &claimed);
     while (cur < n_total(F)) {
+        unsigned long long t_start = 0;
+        if (F.trace && threadIdx.x == 0) t_start = globaltimer();
         if (cur < b_topk(F)) {
             // ---- router rows
             router_block<kBf16>(F.router_w, F.router_b, F.A.h, F.T, F.A.E, F.d, cur * kRouterRowsPerItem,
@@ -177,6 +194,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             if (cur == b_comb(F) && threadIdx.x == 0 && F.A.stats)
                 atomicAdd(F.A.stats + kStatForwardSlots, (unsigned long long)F.A.slots);
         }
+        if (F.trace && threadIdx.x == 0 && cur < F.trace_cap) {
+            unsigned long long *e = F.trace + 4 * (size_t)cur;
+            e[0] = t_start;
+            e[1] = globaltimer();
+            e[2] = smid();
+            e[3] = blockIdx.x;
+        }
         cur = nxt;
         nxt = claim(F.sync, &claimed);
     }
@@ -223,8 +247,10 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
                               bool with_route, int32_t *idx, float *gate, float *logits,
                               const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
                               float *out, int mode, bool reconstruct, int num_sms,
-                              cudaStream_t s) {
+                              cudaStream_t s, unsigned long long *trace, int trace_cap) {
     FusedArgs F;
+    F.trace = trace;
+    F.trace_cap = trace_cap;
     LutArgs &A = F.A;
     A.records = L.records;
     A.stride = L.stride;
