@@ -82,9 +82,24 @@ __device__ __forceinline__ int claim(unsigned *q, int *slot) {
     return *slot;
 }
 
+// The cold items run out of line, so their registers do not add to the units'.
+template <bool kBf16>
+__device__ __noinline__ void router_item(const FusedArgs &F, int item, float (*red)[4][kRouterTok]) {
+    router_block<kBf16>(F.router_w, F.router_b, F.A.h, F.T, F.A.E, F.d, item * kRouterRowsPerItem,
+                        F.logits, F.logits_lo, red);
+}
+
+__device__ __noinline__ void topk_item(const FusedArgs &F, unsigned char *smem) {
+    const int warp = threadIdx.x >> 5;
+    float *area = reinterpret_cast<float *>(smem) + (size_t)warp * ((F.A.E * 9 + 15) / 16 * 4);
+    for (int t = warp; t < F.T; t += kWarps)
+        topk_warp(F.logits, F.logits_lo, F.A.E, F.A.k, t, F.idx_out, F.gate_out, F.pred_idx,
+                  F.pred_count, F.pred_stride, F.A.stats, F.router_bytes, area);
+}
+
 // combine rows [r0, r1) of every token from the down partials (same order as the
 // per-phase combine kernel)
-__device__ void combine_item(const FusedArgs &F, int r0, int r1) {
+__device__ __noinline__ void combine_item(const FusedArgs &F, int r0, int r1) {
     const LutArgs &A = F.A;
     const int d = F.d, k = A.k;
     for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
@@ -95,20 +110,17 @@ __device__ void combine_item(const FusedArgs &F, int r0, int r1) {
                 bool ok[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const int i = i0 + u;
-                    sv[u] = 0.f;
-                    gv[u] = 0.f;
-                    ok[u] = false;
-                    if (i < k) {
-                        const int e = A.idx[(size_t)t * k + i];
-                        ok[u] = e >= 0 && e < A.E;
-                        gv[u] = F.gate[(size_t)t * k + i];
-                        const float *p = A.part_dn + ((size_t)t * k + i) * A.npair * d + r;
-                        float s = 0.f;
+                    // loads of 8 slots go out together: slots past k are clamped to the last
+                    // one and masked
+                    const int i = min(i0 + u, k - 1);
+                    const int e = A.idx[(size_t)t * k + i];
+                    ok[u] = (i0 + u < k) && e >= 0 && e < A.E;
+                    gv[u] = F.gate[(size_t)t * k + i];
+                    const float *p = A.part_dn + ((size_t)t * k + i) * A.npair * d + r;
+                    float s = 0.f;
 #pragma unroll 4
-                        for (int q = 0; q < A.npair; ++q) s += p[(size_t)q * d];
-                        sv[u] = s;
-                    }
+                    for (int q = 0; q < A.npair; ++q) s += p[(size_t)q * d];
+                    sv[u] = s;
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
@@ -146,17 +158,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
         if (F.trace && threadIdx.x == 0) t_start = globaltimer();
         if (cur < b_topk(F)) {
             // ---- router rows
-            router_block<kBf16>(F.router_w, F.router_b, F.A.h, F.T, F.A.E, F.d, cur * kRouterRowsPerItem,
-                                F.logits, F.logits_lo, red);
+            router_item<kBf16>(F, cur, red);
             signal(F.sync + 2);
         } else if (cur < b_gu(F)) {
             // ---- top-k + softmax of every token, one warp per token
             wait_counter(F.sync + 2, (unsigned)F.n_router, F.A.err);
-            const int warp = threadIdx.x >> 5;
-            float *area = reinterpret_cast<float *>(smem) + (size_t)warp * ((F.A.E * 9 + 15) / 16 * 4);
-            for (int t = warp; t < F.T; t += kWarps)
-                topk_warp(F.logits, F.logits_lo, F.A.E, F.A.k, t, F.idx_out, F.gate_out, F.pred_idx,
-                          F.pred_count, F.pred_stride, F.A.stats, F.router_bytes, area);
+            topk_item(F, smem);
             __syncthreads();
             if (threadIdx.x == 0) {
                 __threadfence();

@@ -217,9 +217,13 @@ __device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target,
 // into the buffers when this one returns.  For a down unit, `dep` (if not null) is a
 // completion counter that must reach dep_target before the gate/up partials are read.
 template <bool kDown, bool kRecon, bool kBf16>
-__device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &U, bool has_next, const Unit &N,
-                                         int &par, bool &primed, const unsigned *dep,
-                                         unsigned dep_target, unsigned char *smem) {
+__device__ __noinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
+                                      int &par, bool &primed, const unsigned *dep,
+                                      unsigned dep_target, unsigned char *smem) {
+    // local copies: the caller's structs are read once, the fields then live in registers
+    const Unit U = Uin;
+    Unit N = Uin;
+    if (has_next) N = Nin;
     float *cbuf = reinterpret_cast<float *>(smem + kTabBytes);
     float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kTabBytes + 2 * kStageBuf));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

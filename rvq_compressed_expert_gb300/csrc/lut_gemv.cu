@@ -70,20 +70,16 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
         bool ok[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u;
-            sv[u] = 0.f;
-            gv[u] = 0.f;
-            ok[u] = false;
-            if (i < k) {
-                const int e = idx[(size_t)t * k + i];
-                ok[u] = e >= 0 && e < E;
-                gv[u] = gate[(size_t)t * k + i];
-                const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
-                float s = 0.f;
+            // loads of 8 slots go out together: slots past k are clamped and masked
+            const int i = min(i0 + u, k - 1);
+            const int e = idx[(size_t)t * k + i];
+            ok[u] = (i0 + u < k) && e >= 0 && e < E;
+            gv[u] = gate[(size_t)t * k + i];
+            const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
+            float s = 0.f;
 #pragma unroll 4
-                for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
-                sv[u] = s;
-            }
+            for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
+            sv[u] = s;
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)

@@ -72,24 +72,32 @@ __device__ __forceinline__ void router_block(const float *__restrict__ W, const 
         if (row < E) {
             const float4 *w4 = reinterpret_cast<const float4 *>(W + (size_t)row * d);
             for (int m0 = 0; m0 < per_lane; m0 += kRouterBatch) {
+                // every load of the batch is issued before any is used: indices past the row
+                // are clamped to its last float4 and their products masked to zero
                 float4 w[kRouterBatch];
+                float m[kRouterBatch];
 #pragma unroll
                 for (int u = 0; u < kRouterBatch; ++u) {
                     const int i4 = sub * 32 + lane + 128 * (m0 + u);
-                    w[u] = (i4 < d4) ? __ldg(w4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    m[u] = i4 < d4 ? 1.f : 0.f;
+                    w[u] = __ldg(w4 + min(i4, d4 - 1));
                 }
 #pragma unroll
-                for (int u = 0; u < kRouterBatch; ++u) {
-                    const int i4 = sub * 32 + lane + 128 * (m0 + u);
-                    if (i4 >= d4) continue;
+                for (int t = 0; t < kRouterTok; ++t) {
+                    if (t < nt) {
+                        float4 x[kRouterBatch];
 #pragma unroll
-                    for (int t = 0; t < kRouterTok; ++t) {
-                        if (t < nt) {
-                            const float4 x = load_h4<kBf16>(h, (size_t)(t0 + t) * d + (size_t)i4 * 4);
-                            acc[t] = fmaf(w[u].x, x.x, acc[t]);
-                            acc[t] = fmaf(w[u].y, x.y, acc[t]);
-                            acc[t] = fmaf(w[u].z, x.z, acc[t]);
-                            acc[t] = fmaf(w[u].w, x.w, acc[t]);
+                        for (int u = 0; u < kRouterBatch; ++u) {
+                            const int i4 = min(sub * 32 + lane + 128 * (m0 + u), d4 - 1);
+                            x[u] = load_h4<kBf16>(h, (size_t)(t0 + t) * d + (size_t)i4 * 4);
+                        }
+#pragma unroll
+                        for (int u = 0; u < kRouterBatch; ++u) {
+                            float p = w[u].x * x[u].x;
+                            p = fmaf(w[u].y, x[u].y, p);
+                            p = fmaf(w[u].z, x[u].z, p);
+                            p = fmaf(w[u].w, x[u].w, p);
+                            acc[t] = fmaf(m[u], p, acc[t]);
                         }
                     }
                 }
@@ -134,18 +142,32 @@ __device__ __forceinline__ void topk_warp(const float *__restrict__ logits,
     float *lw = lv + E;
     unsigned char *taken = reinterpret_cast<unsigned char *>(lw + E);
     const int lane = threadIdx.x & 31;
-#pragma unroll 8
-    for (int e = lane; e < E; e += 32) {
-        // canonical keys make the order total: -0 equals +0, and a NaN (outside the
-        // contract) ranks as -inf, so every lane agrees on each round's winner
-        float vh = logits[(size_t)t * E + e];
-        float vl = logits_lo ? logits_lo[(size_t)t * E + e] : 0.f;
-        if (vh != vh) vh = -INFINITY;
-        if (vh == 0.f) vh = 0.f;
-        if (vl != vl || vl == 0.f) vl = 0.f;
-        lv[e] = vh;
-        lw[e] = vl;
-        taken[e] = 0;
+    const float *lrow = logits + (size_t)t * E;
+    const float *lorow = logits_lo ? logits_lo + (size_t)t * E : lrow;
+    for (int e0 = 0; e0 < E; e0 += 32 * 8) {
+        // 8 loads of each array in flight per lane (indices clamped, stores masked)
+        float vh[8], vl[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = min(e0 + 32 * u + lane, E - 1);
+            vh[u] = lrow[e];
+            vl[u] = lorow[e];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + 32 * u + lane;
+            if (e < E) {
+                // canonical keys make the order total: -0 equals +0, and a NaN (outside
+                // the contract) ranks as -inf, so every lane agrees on each round's winner
+                float a = vh[u], b = logits_lo ? vl[u] : 0.f;
+                if (a != a) a = -INFINITY;
+                if (a == 0.f) a = 0.f;
+                if (b != b || b == 0.f) b = 0.f;
+                lv[e] = a;
+                lw[e] = b;
+                taken[e] = 0;
+            }
+        }
     }
     __syncwarp();
     constexpr int kNone = 0x7fffffff;
