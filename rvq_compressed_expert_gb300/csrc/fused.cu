@@ -27,6 +27,7 @@ namespace {
 
 constexpr int kRouterRowsPerItem = kThreads / 128; // 4 expert rows per router item
 constexpr int kCombineRows = 256;                   // output rows per combine item
+constexpr int kMaxFusedExperts = 1024;              // top-k of the step kernel sorts <= 1024 keys
 
 struct FusedArgs {
     LutArgs A; // lookup units; A.idx is where the top-k item writes the routing
@@ -85,16 +86,19 @@ __device__ __forceinline__ int claim(unsigned *q, int *slot) {
 // The cold items run out of line, so their registers do not add to the units'.
 template <bool kBf16>
 __device__ __noinline__ void router_item(const FusedArgs &F, int item, float (*red)[4][kRouterTok]) {
-    router_block<kBf16>(F.router_w, F.router_b, F.A.h, F.T, F.A.E, F.d, item * kRouterRowsPerItem,
-                        F.logits, F.logits_lo, red);
+    // hidden states staged in the (idle) table area of shared memory
+    const int hs_tokens = (int)min((size_t)kRouterTok, (size_t)kTabBytes / ((size_t)F.d * 4));
+    router_block_staged<kBf16>(F.router_w, F.router_b, F.A.h, F.T, F.A.E, F.d,
+                               item * kRouterRowsPerItem, F.logits, F.logits_lo, red,
+                               reinterpret_cast<float *>(lut_smem), hs_tokens);
 }
 
-__device__ __noinline__ void topk_item(const FusedArgs &F, unsigned char *smem) {
-    const int warp = threadIdx.x >> 5;
-    float *area = reinterpret_cast<float *>(smem) + (size_t)warp * ((F.A.E * 9 + 15) / 16 * 4);
-    for (int t = warp; t < F.T; t += kWarps)
-        topk_warp(F.logits, F.logits_lo, F.A.E, F.A.k, t, F.idx_out, F.gate_out, F.pred_idx,
-                  F.pred_count, F.pred_stride, F.A.stats, F.router_bytes, area);
+__device__ __noinline__ void topk_item(const FusedArgs &F) {
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(lut_smem);
+    int *ids = reinterpret_cast<int *>(lut_smem + 8 * kMaxFusedExperts);
+    for (int t = 0; t < F.T; ++t)
+        topk_block(F.logits, F.logits_lo, F.A.E, F.A.k, t, F.idx_out, F.gate_out, F.pred_idx,
+                   F.pred_count, F.pred_stride, F.A.stats, F.router_bytes, keys, ids);
 }
 
 // combine rows [r0, r1) of every token from the down partials (same order as the
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
         } else if (cur < b_gu(F)) {
             // ---- top-k + softmax of every token, one warp per token
             wait_counter(F.sync + 2, (unsigned)F.n_router, F.A.err);
-            topk_item(F, smem);
+            topk_item(F);
             __syncthreads();
             if (threadIdx.x == 0) {
                 __threadfence();
@@ -246,7 +250,7 @@ bool fused_eligible(const LayerView &L, int T, bool with_route, int num_sms) {
     const int slots = T * L.k;
     const int npair = (L.dn.nseg + 1) / 2;
     if (down_row_blocks(slots, npair, L.dn.groups, num_sms) > kMaxFusedRowBlocks) return false;
-    if (with_route && ((size_t)kWarps * ((L.E * 9 + 15) / 16 * 16) > (size_t)kTabBytes)) return false;
+    if (with_route && (L.E > kMaxFusedExperts || (size_t)L.d * 4 > (size_t)kTabBytes)) return false;
     return true;
 }
 

@@ -211,6 +211,9 @@ __device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target,
     __syncthreads();
 }
 
+// Dynamic shared memory of the lookup kernels (every extern __shared__ array names it).
+extern __shared__ __align__(16) unsigned char lut_smem[];
+
 // One unit: tables (or staged codebooks) for the unit's segment(s), then the stream of
 // its rows.  `par`/`primed` carry the codebook stage buffers across consecutive units of
 // one kind: when `has_next`, the next unit's stages 0 and 1 are already on their way
@@ -219,7 +222,9 @@ __device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target,
 template <bool kDown, bool kRecon, bool kBf16>
 __device__ __noinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
                                       int &par, bool &primed, const unsigned *dep,
-                                      unsigned dep_target, unsigned char *smem) {
+                                      unsigned dep_target, unsigned char *) {
+    // the dynamic shared memory named directly, so every access compiles to a shared one
+    unsigned char *smem = lut_smem;
     // local copies: the caller's structs are read once, the fields then live in registers
     const Unit U = Uin;
     Unit N = Uin;

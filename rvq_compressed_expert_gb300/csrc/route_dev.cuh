@@ -245,5 +245,185 @@ __device__ __forceinline__ void topk_warp(const float *__restrict__ logits,
     }
 }
 
+// Router logits of 4 expert rows per CTA of 512 threads, for T tokens, with the tokens'
+// hidden states staged in shared memory `hs` (room for `hs_tokens` rows of d floats):
+// each lane loads all of its float4s of W_r at once (16 per lane per pass), then takes
+// h from shared memory.  Same partial sums, in the same order, as router_block.
+template <bool kBf16>
+__device__ __forceinline__ void router_block_staged(const float *__restrict__ W,
+                                                    const float *__restrict__ bias,
+                                                    const void *__restrict__ h, int T, int E, int d,
+                                                    int row_base, float *__restrict__ logits,
+                                                    float *__restrict__ logits_lo,
+                                                    float (*red)[4][kRouterTok], float *hs,
+                                                    int hs_tokens) {
+    constexpr int kBig = 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_local = warp >> 2, sub = warp & 3;
+    const int row = row_base + row_local;
+    const int d4 = d >> 2;
+    const int per_lane = (d4 + 127) / 128;
+    const float4 *w4 = reinterpret_cast<const float4 *>(W + (size_t)min(row, E - 1) * d);
+    for (int t0 = 0; t0 < T; t0 += kRouterTok) {
+        const int nt = min(kRouterTok, T - t0);
+        float acc[kRouterTok];
+#pragma unroll
+        for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.f;
+        for (int m0 = 0; m0 < per_lane; m0 += kBig) {
+            float4 w[kBig];
+            float m[kBig];
+#pragma unroll
+            for (int u = 0; u < kBig; ++u) {
+                const int i4 = sub * 32 + lane + 128 * (m0 + u);
+                m[u] = i4 < d4 ? 1.f : 0.f;
+                w[u] = __ldg(w4 + min(i4, d4 - 1));
+            }
+            for (int tb = 0; tb < nt; tb += hs_tokens) {
+                const int ntb = min(hs_tokens, nt - tb);
+                __syncthreads(); // hs free
+                for (int i = threadIdx.x; i < ntb * d4; i += blockDim.x) {
+                    const int tt = i / d4, j = i % d4;
+                    reinterpret_cast<float4 *>(hs)[i] = load_h4<kBf16>(h, (size_t)(t0 + tb + tt) * d + (size_t)j * 4);
+                }
+                __syncthreads();
+#pragma unroll
+                for (int t = 0; t < kRouterTok; ++t) {
+                    if (t >= tb && t < tb + ntb) {
+                        const float4 *x4 = reinterpret_cast<const float4 *>(hs) + (size_t)(t - tb) * d4;
+#pragma unroll
+                        for (int u = 0; u < kBig; ++u) {
+                            const int i4 = min(sub * 32 + lane + 128 * (m0 + u), d4 - 1);
+                            const float4 x = x4[i4];
+                            float p = w[u].x * x.x;
+                            p = fmaf(w[u].y, x.y, p);
+                            p = fmaf(w[u].z, x.z, p);
+                            p = fmaf(w[u].w, x.w, p);
+                            acc[t] = fmaf(m[u], p, acc[t]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kRouterTok; ++t) {
+            float v = acc[t];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) red[row_local][sub][t] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x < (int)(blockDim.x >> 7) * kRouterTok) {
+            const int rl = threadIdx.x / kRouterTok, t = threadIdx.x % kRouterTok;
+            const int r = row_base + rl;
+            if (r < E && t < nt) {
+                float v = ((red[rl][0][t] + red[rl][1][t]) + red[rl][2][t]) + red[rl][3][t];
+                float hi = v, lo = 0.f;
+                if (bias) two_sum(v, bias[r], hi, lo);
+                logits[(size_t)(t0 + t) * E + r] = hi;
+                if (logits_lo) logits_lo[(size_t)(t0 + t) * E + r] = lo;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Top-k and softmax of token t by a whole CTA: a bitonic sort of the E experts on the key
+// (logit hi, then lo, descending; index ascending), then warp 0 forms the gates exactly
+// as topk_warp does.  keys/ids: shared scratch of >= next_pow2(E) entries each.
+__device__ __forceinline__ void topk_block(const float *__restrict__ logits,
+                                           const float *__restrict__ logits_lo, int E, int k, int t,
+                                           int32_t *__restrict__ idx, float *__restrict__ gate,
+                                           const int32_t *__restrict__ pred_idx,
+                                           int32_t *__restrict__ pred_count, int pred_stride,
+                                           unsigned long long *__restrict__ stats,
+                                           unsigned long long router_bytes,
+                                           unsigned long long *keys, int *ids) {
+    int N = 1;
+    while (N < E) N <<= 1;
+    const float *lrow = logits + (size_t)t * E;
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        unsigned long long key = 0ull; // below every real logit (-inf maps above 0)
+        if (i < E) {
+            float a = lrow[i], b = logits_lo ? logits_lo[(size_t)t * E + i] : 0.f;
+            if (a != a) a = -INFINITY;
+            if (a == 0.f) a = 0.f;
+            if (b != b || b == 0.f) b = 0.f;
+            key = ((unsigned long long)float_key(a) << 32) | float_key(b);
+        }
+        keys[i] = key;
+        ids[i] = i;
+    }
+    __syncthreads();
+    for (int size = 2; size <= N; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < N; i += blockDim.x) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const unsigned long long ki = keys[i], kj = keys[j];
+                    const int ii = ids[i], ij = ids[j];
+                    // "i before j" in the final (descending) order
+                    const bool i_first = ki > kj || (ki == kj && ii < ij);
+                    const bool desc = (i & size) == 0;
+                    if (desc != i_first) {
+                        keys[i] = kj;
+                        keys[j] = ki;
+                        ids[i] = ij;
+                        ids[j] = ii;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int my_idx = -1;
+        float my_hi = 0.f, my_lo = 0.f;
+        if (lane < k) {
+            my_idx = ids[lane];
+            float a = lrow[my_idx], b = logits_lo ? logits_lo[(size_t)t * E + my_idx] : 0.f;
+            if (a != a) a = -INFINITY;
+            if (a == 0.f) a = 0.f;
+            if (b != b || b == 0.f) b = 0.f;
+            my_hi = a;
+            my_lo = b;
+        }
+        const float h0 = __shfl_sync(0xffffffffu, my_hi, 0);
+        const float l0 = __shfl_sync(0xffffffffu, my_lo, 0);
+        const float diff = (lane == 0) ? 0.f : __fsub_rn(my_hi, h0) + __fsub_rn(my_lo, l0);
+        float ex = (lane < k) ? expf(diff) : 0.f;
+        float sum = ex;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane < k) {
+            idx[(size_t)t * k + lane] = my_idx;
+            gate[(size_t)t * k + lane] = ex / sum;
+        }
+        if (pred_count != nullptr) {
+            const int P = pred_count[t];
+            bool hit = false;
+            if (lane < k)
+                for (int p = 0; p < P; ++p) hit |= (pred_idx[(size_t)t * pred_stride + p] == my_idx);
+            const unsigned hits = __popc(__ballot_sync(0xffffffffu, hit));
+            __syncwarp();
+            if (lane == 0) {
+                if (P > 0) atomicAdd(stats + kStatPredHits, (unsigned long long)hits);
+                pred_count[t] = 0;
+            }
+        }
+        if (lane == 0 && stats) {
+            atomicAdd(stats + kStatRoutedSlots, (unsigned long long)k);
+            if (t == 0) atomicAdd(stats + kStatRouter, router_bytes);
+        }
+    }
+    __syncthreads();
+}
+
 } // namespace route
 } // namespace wm
