@@ -174,6 +174,21 @@ __device__ __forceinline__ void unit_codebooks(const LutArgs &A, const Unit &U, 
     p1 = cb_e + (kDown ? 2 : 1) * kCbFloats;
 }
 
+// fp32 -> TF32 head plus TF32 tail (x ~ head + tail to about 2^-22 relative)
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    const float rest = x - __uint_as_float(hi);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(rest));
+}
+
+// d += a (16x8, row) * b (8x8, col), TF32 inputs, fp32 accumulate
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 __device__ __forceinline__ float dot8s(const float *__restrict__ c, const float *xv) {
     const float4 c0 = reinterpret_cast<const float4 *>(c)[0];
     const float4 c1 = reinterpret_cast<const float4 *>(c)[1];
@@ -220,7 +235,7 @@ extern __shared__ __align__(16) unsigned char lut_smem[];
 // into the buffers when this one returns.  For a down unit, `dep` (if not null) is a
 // completion counter that must reach dep_target before the gate/up partials are read.
 template <bool kDown, bool kRecon, bool kBf16>
-__device__ __noinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
+__device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
                                       int &par, bool &primed, const unsigned *dep,
                                       unsigned dep_target, unsigned char *) {
     // the dynamic shared memory named directly, so every access compiles to a shared one
@@ -295,25 +310,63 @@ __device__ __noinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool ha
     for (int p = 0; p < 2; ++p)
 #pragma unroll
         for (int v = 0; v < kVec; ++v) xr[p][v] = b4 ? xv[p ^ 1][v] : xv[p][v];
-    __syncthreads(); // previous unit's lookups are done with the tables
+    if constexpr (!kDown && !kRecon) {
+        // the table build reads the column vectors X[part][j][v] from xs (both parts of a
+        // gate/up unit share x)
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+            xs[lane * kVec + v] = xv[0][v];
+            xs[kSegVec * kVec + lane * kVec + v] = xv[0][v];
+        }
+    }
+    __syncthreads(); // previous unit's lookups are done with the tables; xs is complete
     if constexpr (!kRecon) {
         // ---- tables T[s][c][part][lane], one stage at a time from the staged codebooks;
-        // the cp.async groups in flight are always the next two stage loads
+        // the cp.async groups in flight are always the next two stage loads.
+        // Per stage and part the table is the product T[j][c] = sum_v X[j][v] C[c][v]
+        // (32 columns j x 256 codes c, K = 8), taken on the tensor cores as
+        // m16n8k8 TF32 MMAs with each operand split into a TF32 head and tail
+        // (tail*head + head*tail + head*head), which keeps fp32 accuracy.  Warp w owns
+        // part (w >> 3), rows j in [16 ((w >> 2) & 1), +16) and 8 of the 32 code tiles.
         float *tab = reinterpret_cast<float *>(smem);
         const float *p0, *p1, *n0 = nullptr, *n1 = nullptr;
         unit_codebooks<kDown>(A, U, p0, p1);
         if (has_next) unit_codebooks<kDown>(A, N, n0, n1);
+        const int mp = warp >> 3, mm = (warp >> 2) & 1, mq = warp & 3;
+        const int fg = lane >> 2, ft = lane & 3;
+        uint32_t ahi[4], alo[4];
+        {
+            const float *X = xs + mp * kSegVec * kVec + (mm * 16) * kVec;
+            const float av[4] = {X[fg * kVec + ft], X[(fg + 8) * kVec + ft], X[fg * kVec + ft + 4],
+                                 X[(fg + 8) * kVec + ft + 4]};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) split_tf32(av[i], ahi[i], alo[i]);
+        }
 #pragma unroll 1
         for (int s = 0; s < kStages; ++s) {
             if (s < 2 || has_next) cp_async_wait<1>();
             else cp_async_wait<0>();
             __syncthreads();
             const float *buf = cbuf + ((s == 1) ? (par ^ 1) : par) * kStageFloats;
-            for (int c = warp; c < kCodes; c += kWarps) {
-                const float t0 = valid ? dot8s(buf + c * kVec, xv[0]) : 0.f;
-                const float t1 = valid ? dot8s(buf + kCodes * kVec + c * kVec, xv[1]) : 0.f;
-                tab[((size_t)s * kCodes + c) * 64 + lane] = t0;
-                tab[((size_t)s * kCodes + c) * 64 + 32 + lane] = t1;
+            const float *Cb = buf + mp * kCodes * kVec;
+#pragma unroll 2
+            for (int i = 0; i < 8; ++i) {
+                const int c0 = (mq + 4 * i) * 8; // first code of this n-tile
+                uint32_t bhi[2], blo[2];
+                split_tf32(Cb[(c0 + fg) * kVec + ft], bhi[0], blo[0]);
+                split_tf32(Cb[(c0 + fg) * kVec + ft + 4], bhi[1], blo[1]);
+                float dd[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_tf32(dd, alo, bhi);
+                mma_tf32(dd, ahi, blo);
+                mma_tf32(dd, ahi, bhi);
+                if (!valid) dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
+                // D rows are columns j, D columns are codes c: (fg, 2ft), (fg, 2ft+1), +8 rows
+                const int j = mm * 16 + fg, c = c0 + 2 * ft;
+                float *t0 = tab + (((size_t)s * kCodes + c) * 2 + mp) * kSegVec;
+                t0[j] = dd[0];
+                t0[2 * kSegVec + j] = dd[1];
+                t0[j + 8] = dd[2];
+                t0[2 * kSegVec + j + 8] = dd[3];
             }
             __syncthreads(); // buffer consumed: refill it
             if (s == 0) issue_stage(cbuf + par * kStageFloats, p0, p1, 2);
