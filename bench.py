@@ -580,7 +580,8 @@ def profile_case(args):
     _build.build()
     B.load()
     w = synth.Workload("decode-e32", 7168, 1536, 32, 16, 1, "f32", "offsets")
-    layer = MoELayer(w, seed=0, layer=0, device="cuda")
+    layer = MoELayer(w, seed=0, layer=0, device="cuda",
+                     flags=B.FLAG_UNFUSED if args.phases else 0)
     idx, gate, logits, y = layer.alloc_outputs(1)
     trace = None
     if args.trace:
@@ -644,6 +645,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", action="store_true",
                     help="run a small decode case for ncu captures and exit")
+    ap.add_argument("--phases", action="store_true",
+                    help="with --profile-case: run each phase as its own kernel")
     ap.add_argument("--trace", action="store_true",
                     help="with --profile-case: print the step kernel's item timeline")
     args = ap.parse_args()
