@@ -174,6 +174,15 @@ __device__ __forceinline__ void unit_codebooks(const LutArgs &A, const Unit &U, 
     p1 = cb_e + (kDown ? 2 : 1) * kCbFloats;
 }
 
+// Table load at shared-window address a + S * 64 KiB (stage S).  volatile keeps it on
+// its side of the barriers that guard the tables.
+template <int S>
+__device__ __forceinline__ float lds_stage(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(S * kTabStage));
+    return v;
+}
+
 // fp32 -> TF32 head plus TF32 tail (x ~ head + tail to about 2^-22 relative)
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
@@ -394,7 +403,9 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     // unit, for the next unit's first row groups.
     const uint8_t *pb0 = b4 ? U.base[1] : U.base[0];
     const uint8_t *pb1 = b4 ? U.base[0] : U.base[1];
-    const unsigned char *tabb = smem;
+    // 32-bit shared-window address of the tables: a lookup is PRMT, IADD and one
+    // ld.shared with the stage offset as its immediate
+    const uint32_t tab32 = (uint32_t)__cvta_generic_to_shared(smem);
     auto load = [&](int g, uint4 (&w)[2][kStages]) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
@@ -426,9 +437,9 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                         const uint32_t a0 = __byte_perm(w0, colb, sel);
                         const uint32_t a1 = __byte_perm(w1, colb, sel);
                         const uint32_t a2 = __byte_perm(w2, colb, sel);
-                        const float t0 = *reinterpret_cast<const float *>(tabb + a0);
-                        const float t1 = *reinterpret_cast<const float *>(tabb + kTabStage + a1);
-                        const float t2 = *reinterpret_cast<const float *>(tabb + 2 * kTabStage + a2);
+                        const float t0 = lds_stage<0>(tab32 + a0);
+                        const float t1 = lds_stage<1>(tab32 + a1);
+                        const float t2 = lds_stage<2>(tab32 + a2);
                         acc[16 * p + 4 * wd + b] = (t0 + t1) + t2;
                     } else {
                         const int part = p ^ b4;
