@@ -16,6 +16,7 @@ constexpr int kXsFloats = 512;               // down input staging (64 vectors x
 constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
 constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' codebooks
 constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
+constexpr bool kCodePingPong = false;             // hold the next round's codes in registers
 constexpr int kPrefetchRounds = 3;                 // L2 prefetch distance in row-group rounds
 
 struct LutArgs {
@@ -479,19 +480,30 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                 A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = v;
         }
     };
-    uint4 wa[2][kStages], wb[2][kStages];
-    int g = U.g0 + warp;
-    if (g < U.g1) load(g, wa);
-    while (g < U.g1) {
-        if (g + kWarps < U.g1) load(g + kWarps, wb);
-        ahead(g);
-        consume(wa, g);
-        g += kWarps;
-        if (g >= U.g1) break;
-        if (g + kWarps < U.g1) load(g + kWarps, wa);
-        ahead(g);
-        consume(wb, g);
-        g += kWarps;
+    if constexpr (kCodePingPong) {
+        uint4 wa[2][kStages], wb[2][kStages];
+        int g = U.g0 + warp;
+        if (g < U.g1) load(g, wa);
+        while (g < U.g1) {
+            if (g + kWarps < U.g1) load(g + kWarps, wb);
+            ahead(g);
+            consume(wa, g);
+            g += kWarps;
+            if (g >= U.g1) break;
+            if (g + kWarps < U.g1) load(g + kWarps, wa);
+            ahead(g);
+            consume(wb, g);
+            g += kWarps;
+        }
+    } else {
+        // codes loaded at the top of each round (they are already on their way into
+        // L2), leaving the registers to the lookups in flight
+        for (int g = U.g0 + warp; g < U.g1; g += kWarps) {
+            uint4 wa[2][kStages];
+            load(g, wa);
+            ahead(g);
+            consume(wa, g);
+        }
     }
     // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
     // and the slot's codebooks once
