@@ -620,7 +620,7 @@ def print_trace(tr, w):
     n_items = len(tr)
     used = [i for i in range(n_items) if tr[i][1] > 0]
     last = max(used)
-    n_comb = _m.ceil(w.d / 256)
+    n_comb = _m.ceil(w.d / 512)
     bounds += [("down", dn0, last + 1 - n_comb), ("combine", last + 1 - n_comb, last + 1)]
     out = []
     for name, a, b in bounds:

@@ -26,7 +26,7 @@ using namespace route;
 namespace {
 
 constexpr int kRouterRowsPerItem = kThreads / 128; // 4 expert rows per router item
-constexpr int kCombineRows = 256;                   // output rows per combine item
+constexpr int kCombineRows = kThreads;              // output rows per combine item
 constexpr int kMaxFusedExperts = 1024;              // top-k of the step kernel sorts <= 1024 keys
 
 struct FusedArgs {
@@ -104,10 +104,16 @@ __device__ __noinline__ void topk_item(const FusedArgs &F) {
 // combine rows [r0, r1) of every token from the down partials (same order as the
 // per-phase combine kernel)
 __device__ __noinline__ void combine_item(const FusedArgs &F, int r0, int r1) {
-    const LutArgs &A = F.A;
-    const int d = F.d, k = A.k;
+    // kernel parameters copied to registers once (read through a reference inside the
+    // loops they would be local-memory loads)
+    const int d = F.d, k = F.A.k, T = F.T, mode = F.mode, E = F.A.E, npair = F.A.npair;
+    const int32_t *__restrict__ idx = F.A.idx;
+    const float *__restrict__ gate = F.gate;
+    const float *__restrict__ part_dn = F.A.part_dn;
+    const float *__restrict__ h32 = F.h32;
+    float *__restrict__ out = F.out;
     for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-        for (int t = 0; t < F.T; ++t) {
+        for (int t = 0; t < T; ++t) {
             float y = 0.f;
             for (int i0 = 0; i0 < k; i0 += 8) {
                 float sv[8], gv[8];
@@ -117,13 +123,13 @@ __device__ __noinline__ void combine_item(const FusedArgs &F, int r0, int r1) {
                     // loads of 8 slots go out together: slots past k are clamped to the last
                     // one and masked
                     const int i = min(i0 + u, k - 1);
-                    const int e = A.idx[(size_t)t * k + i];
-                    ok[u] = (i0 + u < k) && e >= 0 && e < A.E;
-                    gv[u] = F.gate[(size_t)t * k + i];
-                    const float *p = A.part_dn + ((size_t)t * k + i) * A.npair * d + r;
+                    const int e = idx[(size_t)t * k + i];
+                    ok[u] = (i0 + u < k) && e >= 0 && e < E;
+                    gv[u] = gate[(size_t)t * k + i];
+                    const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
                     float s = 0.f;
 #pragma unroll 4
-                    for (int q = 0; q < A.npair; ++q) s += p[(size_t)q * d];
+                    for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
                     sv[u] = s;
                 }
 #pragma unroll
@@ -131,9 +137,9 @@ __device__ __noinline__ void combine_item(const FusedArgs &F, int r0, int r1) {
                     if (ok[u]) y = fmaf(gv[u], sv[u], y);
             }
             const size_t o = (size_t)t * d + r;
-            if (F.mode == 0) F.out[o] = y;
-            else if (F.mode == 1) F.out[o] = F.out[o] + y;
-            else F.out[o] = F.h32[o] + y;
+            if (mode == 0) out[o] = y;
+            else if (mode == 1) out[o] = out[o] + y;
+            else out[o] = h32[o] + y;
         }
     }
 }
