@@ -89,8 +89,10 @@ enum {
     WASTE_FLAG_K2_RECONSTRUCT = 1u << 4, /* forward: rebuild each 8-weight vector from the
                                             3 codebook entries in registers instead of the
                                             partial-dot-product table */
-    WASTE_FLAG_UNFUSED = 1u << 5 /* run each phase as its own kernel instead of the one
-                                    persistent step kernel (same results, bit for bit) */
+    WASTE_FLAG_STEP_KERNEL = 1u << 5 /* run forward / step as one persistent kernel that claims
+                                        router, top-k, expert and combine work from a device
+                                        queue, instead of one kernel per phase (same results,
+                                        bit for bit) */
 };
 
 /* Layer configuration.  d % 8 == 0, f % 8 == 0, 1 <= top_k <= n_experts <= 4096,
@@ -204,10 +206,9 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
                       const float *d_gate, float *d_out, int32_t mode, waste_stream_t stream);
 
 /* route + forward in one call: d_idx, d_gate (and d_logits if not NULL) receive the
- * routing, d_out the combined output per mode (as waste_moe_forward).  Runs as one
- * persistent kernel (router, top-k, expert units and combine claimed from a
- * device-side queue) when the layer's shapes allow it, else as route then forward.
- * Results are identical to route followed by forward. */
+ * routing, d_out the combined output per mode (as waste_moe_forward).  With
+ * WASTE_FLAG_STEP_KERNEL (and shapes that allow it: E <= 1024) it runs as one persistent
+ * kernel; otherwise as route then forward.  Results are identical either way. */
 int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
                    float *d_logits, float *d_out, int32_t mode, waste_stream_t stream);
 

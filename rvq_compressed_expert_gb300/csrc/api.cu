@@ -66,7 +66,7 @@ int check_config(const waste_moe_config *c) {
     if (c->lookahead < 0 || c->lookahead > kMaxTopK || c->lookahead > c->n_experts)
         return fail(WASTE_EINVAL, "lookahead = %d outside [0, min(n_experts, %d)]", c->lookahead, kMaxTopK);
     const uint32_t known = WASTE_FLAG_VERIFY_CRC | WASTE_FLAG_FORCE_GEMV | WASTE_FLAG_FORCE_MMA |
-                           WASTE_FLAG_K2_RECONSTRUCT | WASTE_FLAG_UNFUSED;
+                           WASTE_FLAG_K2_RECONSTRUCT | WASTE_FLAG_STEP_KERNEL;
     if (c->flags & ~known) return fail(WASTE_EINVAL, "unknown flags 0x%x", c->flags & ~known);
     return WASTE_OK;
 }
@@ -397,7 +397,7 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool recon = (h->cfg.flags & WASTE_FLAG_K2_RECONSTRUCT) != 0;
     cudaError_t e;
-    if (!(h->cfg.flags & WASTE_FLAG_UNFUSED) && fused_eligible(h->L, T, false, h->num_sms)) {
+    if ((h->cfg.flags & WASTE_FLAG_STEP_KERNEL) && fused_eligible(h->L, T, false, h->num_sms)) {
         if (h->profiling) cudaEventRecord(h->step_tm.ev[0], s);
         e = launch_fused_step(h->L, h->W, d_h, T, false, const_cast<int32_t *>(d_idx),
                               const_cast<float *>(d_gate), nullptr, nullptr, nullptr, 1, d_out, mode,
@@ -433,7 +433,7 @@ int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, flo
         return fail(WASTE_EINVAL, "mode 2 (out = h + y) needs fp32 hidden states");
     if (T == 0) return ok();
     if (!d_idx || !d_gate || !d_out) return fail(WASTE_EINVAL, "NULL idx, gate or out");
-    if ((h->cfg.flags & WASTE_FLAG_UNFUSED) || !fused_eligible(h->L, T, true, h->num_sms)) {
+    if (!(h->cfg.flags & WASTE_FLAG_STEP_KERNEL) || !fused_eligible(h->L, T, true, h->num_sms)) {
         rc = waste_moe_route(h, d_h, T, d_idx, d_gate, d_logits, stream);
         if (rc) return rc;
         return waste_moe_forward(h, d_h, T, d_idx, d_gate, d_out, mode, stream);

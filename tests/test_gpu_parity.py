@@ -254,8 +254,8 @@ def test_fused_step_equals_phases(shape):
     per-phase kernels bit for bit, over several launches in a row (the device queue and
     counters must come back to zero after every launch)."""
     d, f, E, k, T = shape
-    w, li, h, fused = small_layer(d, f, E, k, T)
-    _, _, _, phases = small_layer(d, f, E, k, T, flags=B.FLAG_UNFUSED)
+    w, li, h, fused = small_layer(d, f, E, k, T, flags=B.FLAG_STEP_KERNEL)
+    _, _, _, phases = small_layer(d, f, E, k, T)
     try:
         hd = h.cuda()
         ref = run(phases, hd, T)
