@@ -51,38 +51,61 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
 }
 
 // out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair],
-// slots in rank order and pairs in order; the loads of 8 slots are issued together.
+// slots in rank order and pairs in order.  NP = number of pairs (0: any, read in a loop):
+// with NP fixed every partial of a batch of 16 slots is loaded before any is summed.
+template <int NP>
 __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ part_dn,
                                                       const int32_t *__restrict__ idx,
                                                       const float *__restrict__ gate,
                                                       const float *__restrict__ h,
                                                       float *__restrict__ out, int d, int k, int E,
-                                                      int npair, int mode,
+                                                      int npair_rt, int mode,
                                                       unsigned long long *stats,
                                                       unsigned long long slots) {
     const int t = blockIdx.y;
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (stats && r == 0 && t == 0) atomicAdd(stats + kStatForwardSlots, slots);
     if (r >= d) return;
+    const int npair = NP ? NP : npair_rt;
     float y = 0.f;
-    for (int i0 = 0; i0 < k; i0 += 8) {
-        float sv[8], gv[8];
-        bool ok[8];
+    for (int i0 = 0; i0 < k; i0 += 16) {
+        float sv[16], gv[16];
+        bool ok[16];
+        if constexpr (NP > 0) {
+            float pv[16][NP > 0 ? NP : 1];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            // loads of 8 slots go out together: slots past k are clamped and masked
+            for (int u = 0; u < 16; ++u) {
+                const int i = min(i0 + u, k - 1);
+                const float *p = part_dn + ((size_t)t * k + i) * NP * d + r;
+#pragma unroll
+                for (int q = 0; q < NP; ++q) pv[u][q] = p[(size_t)q * d];
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                float s = 0.f;
+#pragma unroll
+                for (int q = 0; q < NP; ++q) s += pv[u][q];
+                sv[u] = s;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int i = min(i0 + u, k - 1);
+                const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
+                float s = 0.f;
+                for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
+                sv[u] = s;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
             const int i = min(i0 + u, k - 1);
             const int e = idx[(size_t)t * k + i];
             ok[u] = (i0 + u < k) && e >= 0 && e < E;
             gv[u] = gate[(size_t)t * k + i];
-            const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
-            float s = 0.f;
-#pragma unroll 4
-            for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
-            sv[u] = s;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < 16; ++u)
             if (ok[u]) y = fmaf(gv[u], sv[u], y);
     }
     const size_t o = (size_t)t * d + r;
@@ -161,9 +184,14 @@ cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const voi
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[2], s);
     dim3 grid((L.d + 127) / 128, T);
-    combine_kernel<<<grid, 128, 0, s>>>(W.part_dn, idx, gate, reinterpret_cast<const float *>(h), out,
-                                        L.d, L.k, L.E, A.npair, mode, W.stats,
-                                        (unsigned long long)A.slots);
+    const float *h32 = reinterpret_cast<const float *>(h);
+    switch (A.npair) {
+    case 1: combine_kernel<1><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
+    case 2: combine_kernel<2><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
+    case 3: combine_kernel<3><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
+    case 4: combine_kernel<4><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
+    default: combine_kernel<0><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
+    }
     if (tm) {
         cudaEventRecord(tm->ev[3], s);
         tm->n = 4;

@@ -8,6 +8,8 @@
 // equal logits; gates: softmax over the k selected logits.
 #include "route_dev.cuh"
 
+#include <algorithm>
+
 namespace wm {
 
 using namespace route;
@@ -89,6 +91,40 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const float *__restri
     }
 }
 
+// Small-T router with the tokens staged in shared memory: 4 experts per CTA of 512
+// threads, every lane's W_r loads in flight at once (same sums as the step kernel's
+// router items).
+template <bool kBf16>
+__global__ void __launch_bounds__(512) router_staged_kernel(const float *__restrict__ W,
+                                                            const float *__restrict__ bias,
+                                                            const void *__restrict__ h, int T, int E,
+                                                            int d, float *__restrict__ logits,
+                                                            float *__restrict__ logits_lo,
+                                                            int hs_tokens) {
+    extern __shared__ __align__(16) float hs_dyn[];
+    __shared__ float red[4][4][kRouterTok];
+    router_block_staged<kBf16>(W, bias, h, T, E, d, blockIdx.x * 4, logits, logits_lo, red, hs_dyn,
+                               hs_tokens);
+}
+
+// Top-k of one token per CTA of 512 threads: bitonic sort of the keys in shared memory
+// (same selection and gates as the step kernel's top-k item).
+__global__ void __launch_bounds__(512) topk_cta_kernel(const float *__restrict__ logits,
+                                                       const float *__restrict__ logits_lo, int E,
+                                                       int k, int32_t *__restrict__ idx,
+                                                       float *__restrict__ gate,
+                                                       const int32_t *__restrict__ pred_idx,
+                                                       int32_t *__restrict__ pred_count,
+                                                       int pred_stride,
+                                                       unsigned long long *__restrict__ stats,
+                                                       unsigned long long router_bytes) {
+    extern __shared__ unsigned long long keys_dyn[];
+    int N = 1;
+    while (N < E) N <<= 1;
+    topk_block(logits, logits_lo, E, k, blockIdx.x, idx, gate, pred_idx, pred_count, pred_stride,
+               stats, router_bytes, keys_dyn, reinterpret_cast<int *>(keys_dyn + N));
+}
+
 // One warp per token.
 __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logits,
                                                   const float *__restrict__ logits_lo, int E, int k,
@@ -158,9 +194,30 @@ __global__ void set_count_kernel(int32_t *count, int T, int P) {
 
 } // namespace
 
+constexpr size_t kRouterStageMax = 200 * 1024; // shared memory for staged hidden states
+
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
                           float *logits_lo, cudaStream_t s) {
-    if (T <= 16) {
+    const size_t row_bytes = (size_t)L.d * 4;
+    if (T <= 16 && row_bytes <= kRouterStageMax) {
+        const int hs_tokens = (int)std::min<size_t>({(size_t)kRouterTok, (size_t)T, kRouterStageMax / row_bytes});
+        const size_t smem = (size_t)hs_tokens * row_bytes;
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(router_staged_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kRouterStageMax);
+            cudaFuncSetAttribute(router_staged_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kRouterStageMax);
+            attr = true;
+        }
+        dim3 grid((L.E + 3) / 4);
+        if (L.act_bf16)
+            router_staged_kernel<true><<<grid, 512, smem, s>>>(L.router_w, L.router_b, h, T, L.E, L.d,
+                                                               logits, logits_lo, hs_tokens);
+        else
+            router_staged_kernel<false><<<grid, 512, smem, s>>>(L.router_w, L.router_b, h, T, L.E, L.d,
+                                                                logits, logits_lo, hs_tokens);
+    } else if (T <= 16) {
         dim3 grid((L.E + kRouterRows - 1) / kRouterRows);
         if (L.act_bf16)
             router_small_kernel<true><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
@@ -180,15 +237,17 @@ cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int 
                         int32_t *idx, float *gate, const int32_t *pred_idx, int32_t *pred_count,
                         int pred_stride, unsigned long long *stats,
                         unsigned long long router_bytes, cudaStream_t s) {
-    const size_t smem = (size_t)E * 2 * sizeof(float) + (size_t)E;
+    int N = 1;
+    while (N < E) N <<= 1;
+    const size_t smem = (size_t)N * 12;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)kMaxExperts * 9));
+        cudaFuncSetAttribute(topk_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)((size_t)kMaxExperts * 12));
         attr_set = true;
     }
-    topk_kernel<<<T, 32, smem, s>>>(logits, logits_lo, E, k, idx, gate, pred_idx, pred_count,
-                                    pred_stride, stats, router_bytes);
+    topk_cta_kernel<<<T, 512, smem, s>>>(logits, logits_lo, E, k, idx, gate, pred_idx, pred_count,
+                                         pred_stride, stats, router_bytes);
     return cudaGetLastError();
 }
 
