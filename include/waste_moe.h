@@ -85,7 +85,9 @@ enum { WASTE_ACT_F32 = 0, WASTE_ACT_BF16 = 1 };
 enum {
     WASTE_FLAG_VERIFY_CRC = 1u << 0,    /* create: check every record's payload crc32 */
     WASTE_FLAG_FORCE_GEMV = 1u << 2,    /* forward: table-lookup path for every slot */
-    WASTE_FLAG_FORCE_MMA = 1u << 3,     /* forward: grouped dequant + tensor-core path when T > 1 */
+    WASTE_FLAG_FORCE_MMA = 1u << 3,     /* forward: grouped dequant + tensor-core path for every
+                                           call and every expert with at least one token, fp32
+                                           activations included (fp16-operand accuracy) */
     WASTE_FLAG_K2_RECONSTRUCT = 1u << 4, /* forward: rebuild each 8-weight vector from the
                                             3 codebook entries in registers instead of the
                                             partial-dot-product table */
@@ -201,7 +203,18 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
  *   mode 1: out += sum_i gate_i * y_i   (residual already in out)
  *   mode 2: out  = h + sum_i gate_i * y_i (fp32 h only; out may equal h)
  * Deterministic: the same inputs give bit-identical outputs (fixed summation
- * order, no floating-point atomics). */
+ * order, no floating-point atomics).
+ * Batched calls (bf16 activations and T > 1, or WASTE_FLAG_FORCE_MMA): the slots are
+ * grouped by expert on the device; every expert chosen by at least 4 tokens of the
+ * call (environment WASTE_MMA_MIN_TOKENS overrides 4; 1 under WASTE_FLAG_FORCE_MMA)
+ * is applied as a dense product on the tensor cores -- 128-row tiles of its codes
+ * decoded into fp16 weights in shared memory, its tokens' activations as fp16,
+ * fp32 accumulation -- and the other slots take the table-lookup path.  The page
+ * "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Lecture anticipée et
+ * prédiction du routeur", puts one layer of a prefill chunk at about 550 expert
+ * slots: many tokens per expert.  Tensor-core slots carry fp16-operand error
+ * (relative L2 about 1e-3 at most on the output); WASTE_FLAG_FORCE_GEMV keeps every
+ * slot on the fp32 lookup path. */
 int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d_idx,
                       const float *d_gate, float *d_out, int32_t mode, waste_stream_t stream);
 

@@ -23,6 +23,7 @@ struct waste_moe {
     Timing route_tm, fwd_tm, step_tm;
     unsigned long long *trace; // caller's trace buffer for the step kernel, or null
     int trace_cap;
+    int mma_min_tokens; // tokens an expert needs in one call to take the tensor-core path
 };
 
 namespace {
@@ -238,9 +239,21 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     L.gu = mat_geom(cfg->f, cfg->d);
     L.dn = mat_geom(cfg->d, cfg->f);
 
+    H->mma_min_tokens = kDefaultMmaMinTokens;
+    if (const char *env = getenv("WASTE_MMA_MIN_TOKENS")) {
+        const int v = atoi(env);
+        if (v >= 1) H->mma_min_tokens = v;
+    }
+    if (cfg->flags & WASTE_FLAG_FORCE_MMA) H->mma_min_tokens = 1;
+
     // ---- workspace, one allocation carved into 256-byte aligned pieces
     const size_t T = (size_t)cfg->max_tokens, S = (size_t)H->max_slots;
     const size_t npair = (size_t)(L.dn.nseg + 1) / 2;
+    // grouping of batched calls (any call with more than one token, or every call
+    // under WASTE_FLAG_FORCE_MMA)
+    const bool grouped = cfg->max_tokens > 1 || (cfg->flags & WASTE_FLAG_FORCE_MMA);
+    const size_t max_chunks = (size_t)E + S / kGroupTokens + 1;
+    const size_t G = grouped ? 1 : 0;
     size_t sizes[] = {
         T * E * 4,                                  // logits
         T * E * 4,                                  // logits_lo
@@ -253,9 +266,17 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
         kStatCount * 8,                             // stats
         4,                                          // err
         (4 + S + kMaxFusedRowBlocks) * 4,           // sync
+        G * ((size_t)E + 1) * 4,                    // grp.offs
+        G * S * 4,                                  // grp.sorted
+        G * S * 4,                                  // grp.lut_slots
+        G * max_chunks * 16,                        // grp.chunks
+        G * 2 * 4,                                  // grp.counts
+        G * S,                                      // grp.one_part
+        G * T * (size_t)L.d * 2,                    // grp.x16
+        G * S * (size_t)L.f * 2,                    // grp.a16
     };
     const int n_parts = (int)(sizeof sizes / sizeof sizes[0]);
-    size_t offs[16], total = 0;
+    size_t offs[32], total = 0;
     for (int i = 0; i < n_parts; ++i) {
         offs[i] = total;
         total += round_up(sizes[i], 256);
@@ -283,6 +304,16 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     W.stats = reinterpret_cast<unsigned long long *>(b + offs[8]);
     W.err = reinterpret_cast<uint32_t *>(b + offs[9]);
     W.sync = reinterpret_cast<unsigned *>(b + offs[10]);
+    Grouping &Gp = W.grp;
+    Gp.offs = grouped ? reinterpret_cast<int32_t *>(b + offs[11]) : nullptr;
+    Gp.sorted = grouped ? reinterpret_cast<int32_t *>(b + offs[12]) : nullptr;
+    Gp.lut_slots = grouped ? reinterpret_cast<int32_t *>(b + offs[13]) : nullptr;
+    Gp.chunks = grouped ? reinterpret_cast<int4 *>(b + offs[14]) : nullptr;
+    Gp.counts = grouped ? reinterpret_cast<int32_t *>(b + offs[15]) : nullptr;
+    Gp.one_part = grouped ? reinterpret_cast<uint8_t *>(b + offs[16]) : nullptr;
+    Gp.x16 = grouped ? reinterpret_cast<uint16_t *>(b + offs[17]) : nullptr;
+    Gp.a16 = grouped ? reinterpret_cast<uint16_t *>(b + offs[18]) : nullptr;
+    Gp.max_chunks = grouped ? (int)max_chunks : 0;
     ce = cudaMemset(base, 0, total);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
@@ -385,6 +416,14 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
     return ok();
 }
 
+// Grouped tensor-core path: bf16 activations and more than one token, or every call
+// under WASTE_FLAG_FORCE_MMA; never under WASTE_FLAG_FORCE_GEMV.
+static bool use_grouped(const waste_moe *h, int T) {
+    if (!h->W.grp.x16 || (h->cfg.flags & WASTE_FLAG_FORCE_GEMV)) return false;
+    if (h->cfg.flags & WASTE_FLAG_FORCE_MMA) return true;
+    return h->cfg.act_dtype == WASTE_ACT_BF16 && T > 1;
+}
+
 int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d_idx,
                       const float *d_gate, float *d_out, int32_t mode, waste_stream_t stream) {
     int rc = check_tokens(h, T, d_h);
@@ -397,7 +436,11 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool recon = (h->cfg.flags & WASTE_FLAG_K2_RECONSTRUCT) != 0;
     cudaError_t e;
-    if ((h->cfg.flags & WASTE_FLAG_STEP_KERNEL) && fused_eligible(h->L, T, false, h->num_sms)) {
+    if (use_grouped(h, T)) {
+        e = launch_grouped_forward(h->L, h->W, d_h, T, d_idx, d_gate, d_out, mode, h->mma_min_tokens, recon,
+                                   h->num_sms, s, h->profiling ? &h->fwd_tm : nullptr);
+        if (h->profiling) h->step_tm.n = 0;
+    } else if ((h->cfg.flags & WASTE_FLAG_STEP_KERNEL) && fused_eligible(h->L, T, false, h->num_sms)) {
         if (h->profiling) cudaEventRecord(h->step_tm.ev[0], s);
         e = launch_fused_step(h->L, h->W, d_h, T, false, const_cast<int32_t *>(d_idx),
                               const_cast<float *>(d_gate), nullptr, nullptr, nullptr, 1, d_out, mode,
@@ -433,7 +476,8 @@ int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, flo
         return fail(WASTE_EINVAL, "mode 2 (out = h + y) needs fp32 hidden states");
     if (T == 0) return ok();
     if (!d_idx || !d_gate || !d_out) return fail(WASTE_EINVAL, "NULL idx, gate or out");
-    if (!(h->cfg.flags & WASTE_FLAG_STEP_KERNEL) || !fused_eligible(h->L, T, true, h->num_sms)) {
+    if (!(h->cfg.flags & WASTE_FLAG_STEP_KERNEL) || use_grouped(h, T) ||
+        !fused_eligible(h->L, T, true, h->num_sms)) {
         rc = waste_moe_route(h, d_h, T, d_idx, d_gate, d_logits, stream);
         if (rc) return rc;
         return waste_moe_forward(h, d_h, T, d_idx, d_gate, d_out, mode, stream);

@@ -70,6 +70,19 @@ struct LayerView {
     MatGeom dn;   // down geometry (d rows, f inputs)
 };
 
+// Slots of a batched call grouped by expert (see grouped.cu).
+struct Grouping {
+    int32_t *offs;      // [E + 1] first position of each expert in `sorted`
+    int32_t *sorted;    // [max_slots] slots grouped by expert, ascending within an expert
+    int32_t *lut_slots; // [max_slots] slots left to the lookup kernels, ascending
+    int4 *chunks;       // [max_chunks] (expert, first position in sorted, tokens, 0)
+    int32_t *counts;    // [2] chunks, lookup slots
+    uint8_t *one_part;  // [max_slots] 1: the slot's down output is partial 0 alone
+    uint16_t *x16;      // [max_T][d] fp16 copy of the hidden states
+    uint16_t *a16;      // [max_slots][f] fp16 SwiGLU output of the tensor-core slots
+    int max_chunks;
+};
+
 struct Workspace {
     float *logits;       // [max_T][E]
     float *logits_lo;    // [max_T][E]
@@ -83,6 +96,7 @@ struct Workspace {
     unsigned long long *stats; // [kStatCount]
     uint32_t *err;       // sticky error bits
     unsigned *sync;      // fused-step queue and counters [4 + max_slots + kMaxFusedRowBlocks], zero at rest
+    Grouping grp;        // batched calls only (null pointers when max_tokens == 1)
     void *base;
     size_t bytes;
 };
@@ -105,6 +119,25 @@ struct Timing {
 cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
                                const int32_t *idx, const float *gate, float *out, int mode,
                                bool reconstruct, int num_sms, cudaStream_t s, Timing *tm);
+// One lookup phase (gate/up or down) over the slots listed on the device.
+cudaError_t launch_lut_listed(const LayerView &L, const Workspace &W, const void *h, int T,
+                              const int32_t *idx, const int32_t *slot_list, const int32_t *n_list,
+                              bool down, bool reconstruct, int num_sms, cudaStream_t s);
+// out = / += / h + sum_i gate * (sum of the slot's down partials); one_part (optional)
+// marks slots whose output is partial 0 alone.
+cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h, int T,
+                           const int32_t *idx, const float *gate, float *out, int mode,
+                           const uint8_t *one_part, cudaStream_t s);
+// Tokens per chunk of the grouped tensor-core path.
+constexpr int kGroupTokens = 128;
+// Default tokens an expert needs in one call to take the tensor-core path.
+constexpr int kDefaultMmaMinTokens = 4;
+// Batched forward: slots grouped by expert; experts with at least min_tokens tokens
+// through the tensor-core kernels, the rest through the lookup kernels.
+cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const void *h, int T,
+                                   const int32_t *idx, const float *gate, float *out, int mode,
+                                   int min_tokens, bool reconstruct, int num_sms, cudaStream_t s,
+                                   Timing *tm);
 // Row blocks of the down matrix per (slot, segment pair) for the lookup kernels.
 int down_row_blocks(int slots, int npair, int groups, int num_sms);
 // Whether the fused step kernel can run this call (else the per-phase kernels do).

@@ -289,6 +289,8 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
     A.part_dn = W.part_dn;
     A.stats = W.stats;
     A.err = W.err;
+    A.slot_list = nullptr;
+    A.n_list = nullptr;
     F.router_w = L.router_w;
     F.router_b = L.router_b;
     F.logits = logits;

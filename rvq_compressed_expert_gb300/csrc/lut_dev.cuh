@@ -37,7 +37,16 @@ struct LutArgs {
     float *part_dn; // [slot][npair][d]
     unsigned long long *stats;
     uint32_t *err;
+    // optional: the slots to serve (ascending), their count on the device; null = all
+    // T * k slots in order
+    const int32_t *slot_list;
+    const int32_t *n_list;
 };
+
+// Slots this launch serves.
+__device__ __forceinline__ int lut_slot_count(const LutArgs &A) {
+    return A.slot_list ? *A.n_list : A.slots;
+}
 
 __device__ __forceinline__ uint32_t comp(const uint4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -118,12 +127,14 @@ __device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
     Unit U;
     if constexpr (!kDown) {
         U.slot = u / A.gu.nseg;
+        if (A.slot_list) U.slot = A.slot_list[U.slot];
         U.seg0 = u % A.gu.nseg;
         U.g0 = 0;
         U.g1 = A.gu.groups;
     } else {
         const int per_slot = A.npair * A.nrb;
         U.slot = u / per_slot;
+        if (A.slot_list) U.slot = A.slot_list[U.slot];
         const int rem = u % per_slot;
         U.seg0 = 2 * (rem / A.nrb);
         const int rb = rem % A.nrb;

@@ -37,7 +37,8 @@ namespace {
 template <bool kDown, bool kRecon, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
     extern __shared__ __align__(16) unsigned char smem[];
-    const int units = kDown ? A.slots * A.npair * A.nrb : A.slots * A.gu.nseg;
+    const int n_slots = lut_slot_count(A);
+    const int units = kDown ? n_slots * A.npair * A.nrb : n_slots * A.gu.nseg;
     int par = 0;
     bool primed = false;
     Unit N;
@@ -61,7 +62,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
                                                       float *__restrict__ out, int d, int k, int E,
                                                       int npair_rt, int mode,
                                                       unsigned long long *stats,
-                                                      unsigned long long slots) {
+                                                      unsigned long long slots,
+                                                      const uint8_t *__restrict__ one_part) {
     const int t = blockIdx.y;
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (stats && r == 0 && t == 0) atomicAdd(stats + kStatForwardSlots, slots);
@@ -87,13 +89,19 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
                 for (int q = 0; q < NP; ++q) s += pv[u][q];
                 sv[u] = s;
             }
+            if (one_part) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (one_part[(size_t)t * k + min(i0 + u, k - 1)]) sv[u] = pv[u][0];
+            }
         } else {
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int i = min(i0 + u, k - 1);
                 const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
+                const int nq = (one_part && one_part[(size_t)t * k + i]) ? 1 : npair;
                 float s = 0.f;
-                for (int q = 0; q < npair; ++q) s += p[(size_t)q * d];
+                for (int q = 0; q < nq; ++q) s += p[(size_t)q * d];
                 sv[u] = s;
             }
         }
@@ -151,9 +159,8 @@ int down_row_blocks(int slots, int npair, int groups, int num_sms) {
     return nrb;
 }
 
-cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
-                               const int32_t *idx, const float *gate, float *out, int mode,
-                               bool reconstruct, int num_sms, cudaStream_t s, Timing *tm) {
+LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int T,
+                      const int32_t *idx, int num_sms) {
     LutArgs A;
     A.records = L.records;
     A.stride = L.stride;
@@ -175,28 +182,66 @@ cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const voi
     A.part_dn = W.part_dn;
     A.stats = W.stats;
     A.err = W.err;
-    const bool bf16 = L.act_bf16 != 0;
-    if (tm) cudaEventRecord(tm->ev[0], s);
-    cudaError_t e = launch_var<false>(A, A.slots * A.gu.nseg, reconstruct, bf16, num_sms, s);
-    if (e != cudaSuccess) return e;
-    if (tm) cudaEventRecord(tm->ev[1], s);
-    e = launch_var<true>(A, A.slots * A.npair * A.nrb, reconstruct, bf16, num_sms, s);
-    if (e != cudaSuccess) return e;
-    if (tm) cudaEventRecord(tm->ev[2], s);
+    A.slot_list = nullptr;
+    A.n_list = nullptr;
+    return A;
+}
+
+cudaError_t launch_lut_phase(const LutArgs &A, bool down, bool reconstruct, bool bf16, int num_sms,
+                             cudaStream_t s) {
+    if (!down) return launch_var<false>(A, A.slots * A.gu.nseg, reconstruct, bf16, num_sms, s);
+    return launch_var<true>(A, A.slots * A.npair * A.nrb, reconstruct, bf16, num_sms, s);
+}
+
+cudaError_t launch_lut_listed(const LayerView &L, const Workspace &W, const void *h, int T,
+                              const int32_t *idx, const int32_t *slot_list, const int32_t *n_list,
+                              bool down, bool reconstruct, int num_sms, cudaStream_t s) {
+    LutArgs A = make_lut_args(L, W, h, T, idx, num_sms);
+    A.slot_list = slot_list;
+    A.n_list = n_list;
+    return launch_lut_phase(A, down, reconstruct, L.act_bf16 != 0, num_sms, s);
+}
+
+cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h, int T,
+                           const int32_t *idx, const float *gate, float *out, int mode,
+                           const uint8_t *one_part, cudaStream_t s) {
+    const int npair = (L.dn.nseg + 1) / 2;
+    const unsigned long long slots = (unsigned long long)T * L.k;
     dim3 grid((L.d + 127) / 128, T);
     const float *h32 = reinterpret_cast<const float *>(h);
-    switch (A.npair) {
-    case 1: combine_kernel<1><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
-    case 2: combine_kernel<2><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
-    case 3: combine_kernel<3><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
-    case 4: combine_kernel<4><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
-    default: combine_kernel<0><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, A.npair, mode, W.stats, (unsigned long long)A.slots); break;
+    switch (npair) {
+#define WM_COMBINE(NP)                                                                              \
+    combine_kernel<NP><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, npair,  \
+                                            mode, W.stats, slots, one_part)
+    case 1: WM_COMBINE(1); break;
+    case 2: WM_COMBINE(2); break;
+    case 3: WM_COMBINE(3); break;
+    case 4: WM_COMBINE(4); break;
+    default: WM_COMBINE(0); break;
+#undef WM_COMBINE
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
+                               const int32_t *idx, const float *gate, float *out, int mode,
+                               bool reconstruct, int num_sms, cudaStream_t s, Timing *tm) {
+    const LutArgs A = make_lut_args(L, W, h, T, idx, num_sms);
+    const bool bf16 = L.act_bf16 != 0;
+    if (tm) cudaEventRecord(tm->ev[0], s);
+    cudaError_t e = launch_lut_phase(A, false, reconstruct, bf16, num_sms, s);
+    if (e != cudaSuccess) return e;
+    if (tm) cudaEventRecord(tm->ev[1], s);
+    e = launch_lut_phase(A, true, reconstruct, bf16, num_sms, s);
+    if (e != cudaSuccess) return e;
+    if (tm) cudaEventRecord(tm->ev[2], s);
+    e = launch_combine(L, W, h, T, idx, gate, out, mode, nullptr, s);
+    if (e != cudaSuccess) return e;
     if (tm) {
         cudaEventRecord(tm->ev[3], s);
         tm->n = 4;
     }
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 } // namespace wm

@@ -102,7 +102,9 @@ def small_layer(d, f, E, k, T, act="f32", seed=0, flags=0, bias="none"):
 ])
 def test_layer_matches_oracle(shape, act, flags):
     d, f, E, k, T = shape
-    w, li, h, layer = small_layer(d, f, E, k, T, act, flags=flags)
+    # the lookup paths alone (batched bf16 calls would send popular experts to the
+    # tensor cores, which tests/test_gpu_grouped.py covers at their own bar)
+    w, li, h, layer = small_layer(d, f, E, k, T, act, flags=flags | B.FLAG_FORCE_GEMV)
     try:
         g_idx, g_gate, g_logits, g_out = run(layer, h.cuda(), T)
         ref = oracle.moe_layer(h, li.router_w, li.router_b, li.codebooks, li.codes, k)
