@@ -321,6 +321,99 @@ def run_decode(args, dev, out):
     out["_pool"] = pool
 
 
+def run_batched(args, dev, out, name, steps):
+    """Batched decode (128 tokens, Zipf popularity) or a prefill chunk (512 tokens): route +
+    grouped forward over all tokens per step, from a CUDA graph; the same call with every slot
+    on the lookup path (WASTE_FLAG_FORCE_GEMV) for comparison."""
+    from rvq_compressed_expert_gb300 import binding as B
+    from rvq_compressed_expert_gb300 import synth
+    from rvq_compressed_expert_gb300.layer import MoELayer
+    import oracle  # only for its byte count of one expert's codes (pinned to the pages)
+
+    w = synth.WORKLOADS[name]
+    T = w.tokens
+    layer = MoELayer(w, seed=0, layer=0, device=dev)
+    h = synth.hidden(0, T, w.d, w.act_dtype, dev)
+    idx, gate, logits, y = layer.alloc_outputs(T)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(handle, K):
+        def step():
+            B.waste_moe_step(handle, h, T, idx, gate, logits, y, 0)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            flush.zero_()
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        t0 = time.time()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        args.sampler.mark(t0, time.time())
+        del g
+        return sum(a.elapsed_time(b) for a, b in ev) / K
+
+    layer.reset_stats()
+    ms = timed(layer.handle, steps)
+    st = {k: v / (steps + 6) for k, v in layer.stats().items()}
+    # per-kernel times, launched directly with events between the phases
+    B.waste_moe_set_profiling(layer.handle, True)
+    prof = []
+    for _ in range(5):
+        flush.zero_()
+        torch.cuda._sleep(100_000)
+        B.waste_moe_step(layer.handle, h, T, idx, gate, logits, y, 0)
+        prof.append(B.waste_moe_read_profile(layer.handle))
+    B.waste_moe_set_profiling(layer.handle, False)
+    kern = {k: statistics.mean(p[k] for p in prof) for k in prof[0] if prof[0][k] >= 0}
+    counts = torch.bincount(idx.flatten().long(), minlength=w.n_experts).cpu()
+    n_distinct = int((counts > 0).sum())
+    n_tc = int((counts >= 4).sum())
+    # lookup-only comparison on a second handle over the same weights
+    gcfg = B.make_config(w.d, w.f, w.n_experts, w.top_k, w.act_dtype, T, 0, B.FLAG_FORCE_GEMV, 0)
+    gh = B.waste_moe_create(gcfg, layer.router_w, layer.router_b, layer.records, layer.stride,
+                            layer.codebooks)
+    ms_gemv = timed(gh, 3)
+    B.waste_moe_destroy(gh)
+
+    per_expert = oracle.expert_code_bytes(w.d, w.f) + 3 * 3 * 256 * 8 * 4
+    alg_bytes = n_distinct * per_expert + w.n_experts * w.d * 4 + T * w.d * (2 + 4)
+    flops = T * w.top_k * 3 * 2 * w.d * w.f
+    peak_gbs, _, pk = measured_peaks()
+    # fp16 operands run at the bf16 dense rate (nominal ratio 1:1); the burst figure, since
+    # the kernels are timed on their own
+    peak_tf = float(pk["bf16_tflops"]) if pk else 1900.0
+    out[name] = dict(
+        workload=f"{name}: d={w.d} f={w.f} E={w.n_experts} top-{w.top_k}, T={T} tokens/step, "
+                 f"{w.act_dtype} h, router bias {w.bias}",
+        tok_s=T / (ms * 1e-3), ms_per_step=ms, steps=steps,
+        kernels_ms=kern,
+        distinct_experts=n_distinct, tensor_core_experts=n_tc,
+        tokens_per_expert_max=int(counts.max()), tokens_per_expert_mean=float(counts[counts > 0].float().mean()),
+        algorithmic_bytes_per_step=alg_bytes,
+        hbm_frac_whole_step=alg_bytes / (ms * 1e-3) / 1e9 / peak_gbs,
+        tflops_whole_step=flops / (ms * 1e-3) / 1e12,
+        tensor_frac_whole_step=flops / (ms * 1e-3) / 1e12 / peak_tf,
+        lookup_only_ms_per_step=ms_gemv, speedup_over_lookup_only=ms_gemv / ms,
+        demand_code_bytes_per_step=st["demand_code_bytes"],
+    )
+    layer.close()
+
+
 def run_stack(args, dev, out):
     """92 layers x 64 experts, one token, h += combine per layer; lookahead 6 vs off."""
     from rvq_compressed_expert_gb300 import binding as B
@@ -446,6 +539,9 @@ def native(args):
         args.sampler = _Null()
     res = {}
     run_decode(args, dev, res)
+    if not args.no_batched:
+        run_batched(args, dev, res, "batched", 20)
+        run_batched(args, dev, res, "prefill", 10)
     if not args.no_stack:
         run_stack(args, dev, res)
     clocks = args.sampler.stop()
@@ -514,8 +610,9 @@ def native(args):
         "cpu_baseline": cpu,
         "stats_per_step": {k: v / args.steps for k, v in d["stats"].items()},
     }
-    if "stack" in res:
-        line["stack"] = res["stack"]
+    for extra in ("batched", "prefill", "stack"):
+        if extra in res:
+            line[extra] = res[extra]
     print(json.dumps(line), flush=True)
 
 
@@ -579,21 +676,26 @@ def profile_case(args):
     from rvq_compressed_expert_gb300.layer import MoELayer
     _build.build()
     B.load()
-    w = synth.Workload("decode-e32", 7168, 1536, 32, 16, 1, "f32", "offsets")
+    if args.prefill:
+        # the grouped tensor-core path at full d and f: 64 bf16 tokens over 32 experts
+        # (about 32 tokens per expert; 0.4 GB of records)
+        w = synth.Workload("prefill-e32", 7168, 1536, 32, 16, 64, "bf16", "none")
+    else:
+        w = synth.Workload("decode-e32", 7168, 1536, 32, 16, 1, "f32", "offsets")
     layer = MoELayer(w, seed=0, layer=0, device="cuda",
-                     flags=0 if args.phases else B.FLAG_STEP_KERNEL)
-    idx, gate, logits, y = layer.alloc_outputs(1)
+                     flags=0 if (args.phases or args.prefill) else B.FLAG_STEP_KERNEL)
+    idx, gate, logits, y = layer.alloc_outputs(w.tokens)
     trace = None
     if args.trace:
         trace = torch.zeros(4096 * 4, dtype=torch.int64, device="cuda")
         B.waste_moe_set_trace(layer.handle, trace, 4096)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     for i in range(args.warmup + args.steps):
-        h = synth.hidden(100 + i, 1, w.d, "f32", "cuda")
+        h = synth.hidden(100 + i, w.tokens, w.d, w.act_dtype, "cuda")
         if trace is not None:
             flush.zero_()
             trace.zero_()
-        layer.step(h, 1, idx, gate, y, 0, logits)
+        layer.step(h, w.tokens, idx, gate, y, 0, logits)
         if trace is not None and i >= args.warmup:
             torch.cuda.synchronize()
             print_trace(trace.view(-1, 4).cpu(), w)
@@ -642,6 +744,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--no-batched", action="store_true")
+    ap.add_argument("--prefill", action="store_true",
+                    help="with --profile-case: the grouped tensor-core path (64 bf16 tokens)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", action="store_true",
                     help="run a small decode case for ncu captures and exit")

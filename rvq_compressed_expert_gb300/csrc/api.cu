@@ -272,8 +272,9 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
         G * max_chunks * 16,                        // grp.chunks
         G * 2 * 4,                                  // grp.counts
         G * S,                                      // grp.one_part
-        G * T * (size_t)L.d * 2,                    // grp.x16
-        G * S * (size_t)L.f * 2,                    // grp.a16
+        G * grouped_tile_rows((int)S, (int)max_chunks) * ((L.d + 63) / 64) * 128, // grp.xg
+        G * grouped_tile_rows((int)S, (int)max_chunks) * ((L.f + 63) / 64) * 128, // grp.ag
+        (T > 16 ? (size_t)kRouterMaxSplits * T * E * 4 : 0), // router_part
     };
     const int n_parts = (int)(sizeof sizes / sizeof sizes[0]);
     size_t offs[32], total = 0;
@@ -311,9 +312,10 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     Gp.chunks = grouped ? reinterpret_cast<int4 *>(b + offs[14]) : nullptr;
     Gp.counts = grouped ? reinterpret_cast<int32_t *>(b + offs[15]) : nullptr;
     Gp.one_part = grouped ? reinterpret_cast<uint8_t *>(b + offs[16]) : nullptr;
-    Gp.x16 = grouped ? reinterpret_cast<uint16_t *>(b + offs[17]) : nullptr;
-    Gp.a16 = grouped ? reinterpret_cast<uint16_t *>(b + offs[18]) : nullptr;
+    Gp.xg = grouped ? reinterpret_cast<uint8_t *>(b + offs[17]) : nullptr;
+    Gp.ag = grouped ? reinterpret_cast<uint8_t *>(b + offs[18]) : nullptr;
     Gp.max_chunks = grouped ? (int)max_chunks : 0;
+    W.router_part = T > 16 ? reinterpret_cast<float *>(b + offs[19]) : nullptr;
     ce = cudaMemset(base, 0, total);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
@@ -402,7 +404,7 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *logits = d_logits ? d_logits : h->W.logits;
     if (h->profiling) cudaEventRecord(h->route_tm.ev[0], s);
-    cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s);
+    cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s, h->W.router_part, h->num_sms);
     if (e != cudaSuccess) return cuda_fail(e, "router kernel");
     if (h->profiling) cudaEventRecord(h->route_tm.ev[1], s);
     e = launch_topk(logits, h->W.logits_lo, T, h->L.E, h->L.k, d_idx, d_gate, h->W.pred_idx,
@@ -419,7 +421,7 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
 // Grouped tensor-core path: bf16 activations and more than one token, or every call
 // under WASTE_FLAG_FORCE_MMA; never under WASTE_FLAG_FORCE_GEMV.
 static bool use_grouped(const waste_moe *h, int T) {
-    if (!h->W.grp.x16 || (h->cfg.flags & WASTE_FLAG_FORCE_GEMV)) return false;
+    if (!h->W.grp.xg || (h->cfg.flags & WASTE_FLAG_FORCE_GEMV)) return false;
     if (h->cfg.flags & WASTE_FLAG_FORCE_MMA) return true;
     return h->cfg.act_dtype == WASTE_ACT_BF16 && T > 1;
 }
@@ -508,7 +510,7 @@ int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_
         return fail(WASTE_EINVAL, "n_prefetch = %d above min(n_experts, %d)", P, kMaxTopK);
     if (T == 0 || P == 0) return ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(side);
-    cudaError_t e = launch_router(h->L, d_h, T, h->W.pred_logits, nullptr, s);
+    cudaError_t e = launch_router(h->L, d_h, T, h->W.pred_logits, nullptr, s, h->W.router_part, h->num_sms);
     if (e != cudaSuccess) return cuda_fail(e, "lookahead router");
     e = launch_topk(h->W.pred_logits, nullptr, T, h->L.E, P, h->W.pred_idx, h->W.pred_gate_sel, nullptr,
                     nullptr, 1, nullptr, 0, s);

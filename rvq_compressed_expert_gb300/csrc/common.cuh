@@ -75,13 +75,15 @@ struct Grouping {
     int32_t *offs;      // [E + 1] first position of each expert in `sorted`
     int32_t *sorted;    // [max_slots] slots grouped by expert, ascending within an expert
     int32_t *lut_slots; // [max_slots] slots left to the lookup kernels, ascending
-    int4 *chunks;       // [max_chunks] (expert, first position in sorted, tokens, 0)
+    int4 *chunks;       // [max_chunks] (expert, first position in sorted, tokens, first tile row)
     int32_t *counts;    // [2] chunks, lookup slots
     uint8_t *one_part;  // [max_slots] 1: the slot's down output is partial 0 alone
-    uint16_t *x16;      // [max_T][d] fp16 copy of the hidden states
-    uint16_t *a16;      // [max_slots][f] fp16 SwiGLU output of the tensor-core slots
+    uint8_t *xg;        // fp16 activation tiles of the chunks (gate/up input), rows x ceil(d/64) x 128 B
+    uint8_t *ag;        // fp16 SwiGLU tiles of the chunks (down input), rows x ceil(f/64) x 128 B
     int max_chunks;
 };
+// Tile rows the grouped path needs at most (tokens padded to 16 per chunk).
+size_t grouped_tile_rows(int max_slots, int max_chunks);
 
 struct Workspace {
     float *logits;       // [max_T][E]
@@ -97,6 +99,7 @@ struct Workspace {
     uint32_t *err;       // sticky error bits
     unsigned *sync;      // fused-step queue and counters [4 + max_slots + kMaxFusedRowBlocks], zero at rest
     Grouping grp;        // batched calls only (null pointers when max_tokens == 1)
+    float *router_part;  // [kRouterMaxSplits][max_T][E] when max_T > 16, else null
     void *base;
     size_t bytes;
 };
@@ -104,8 +107,10 @@ struct Workspace {
 // ---- launchers (each returns cudaGetLastError() of its launches) ----
 // logits_lo (optional): exact remainder of adding the router bias, so that
 // logits + logits_lo equals W_r h + b exactly given the fp32 dot product.
+// part (optional): [kRouterMaxSplits][T][E] scratch for the split-K router of T > 16.
+constexpr int kRouterMaxSplits = 32;
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
-                          float *logits_lo, cudaStream_t s);
+                          float *logits_lo, cudaStream_t s, float *part = nullptr, int num_sms = 1);
 cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int E, int k,
                         int32_t *idx, float *gate, const int32_t *pred_idx, int32_t *pred_count,
                         int pred_stride, unsigned long long *stats,

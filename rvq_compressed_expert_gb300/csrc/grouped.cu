@@ -2,23 +2,32 @@
 // expert, and every expert that serves enough tokens applied as a dense product on
 // the tensor cores.
 //
-// Pages "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Lecture anticipée
-// et prédiction du routeur": one layer of a prefill chunk spans about 550 expert slots,
-// so one expert's weights serve many tokens at once.  The weights stay in their
-// 3-stage RVQ codes (section "Quantification et exactitude"); here a 128-row tile of
-// codes is decoded into shared memory (sum of the three 256-entry codebook rows per
-// 8-weight vector) and fed to tcgen05 MMAs with the expert's tokens as the N side.
+// Page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Lecture anticipée et
+// prédiction du routeur": one layer of a prefill chunk spans about 550 expert slots, so
+// one expert's weights serve many tokens at once.  The weights stay in their 3-stage
+// RVQ codes (section "Quantification et exactitude"); here 128-row tiles of codes are
+// decoded into shared memory (the sum of three 256-entry codebook rows per 8-weight
+// vector) and fed to tcgen05 MMAs with the expert's tokens as the N side.
 //
 // Kernels, in launch order:
-//   group_kernel  per-expert counts, the slots sorted by expert, the chunk list of the
-//                 tensor-core experts (<= 128 tokens each) and the list of the slots
-//                 left to the lookup kernels (experts with fewer than min_tokens tokens)
-//   prep_kernel   the hidden states as fp16 (the B operand)
-//   mma_kernel<0> gate and up of every (chunk, 128-row block): two K passes into two
-//                 TMEM accumulators, SwiGLU in the epilogue, fp16 result per slot
-//   mma_kernel<1> down of every (chunk, 128-row block): y per slot into partial 0
+//   group_kernel   per-expert counts, the slots sorted by expert, the chunk list of the
+//                  tensor-core experts (<= 128 tokens each, with their rows in the tiled
+//                  activation buffers) and the list of the slots left to the lookup
+//                  kernels (experts with fewer than min_tokens tokens)
+//   gather_kernel  each chunk's activations as fp16 tiles in the order the MMA reads
+//                  them (one contiguous block per K chunk), zero padding included
+//   mma_kernel<0>  gate and up of every (chunk, 128-row block): two K passes into two
+//                  TMEM accumulators, SwiGLU in the epilogue, written as the fp16 tiles
+//                  the down kernel reads
+//   mma_kernel<1>  down of every (chunk, 128-row block): y per slot into partial 0
 // The lookup kernels serve the listed slots in between, and the combine sums the k
 // slots of each token in rank order (one partial for tensor-core slots).
+//
+// mma_kernel is warp-specialised: a producer warp moves, with one bulk copy each, the
+// codes of a 32-vector segment of the row block (12 KiB) and the activation tile of each
+// 64-wide K chunk; 16 decode warps turn codes into fp16 weight tiles; one thread issues
+// the MMAs.  Full/empty mbarriers hand the buffers between them, so decoding, copies
+// and MMAs of different chunks overlap.
 //
 // Numerics: codebook rows are rounded to fp16 and summed in fp16 (stage order 0, 1, 2),
 // the activations enter as fp16, products accumulate in fp32.  The error is that of
@@ -33,17 +42,29 @@ namespace wm {
 
 namespace {
 
+constexpr int kBM = 128;  // output rows per item (MMA M)
+constexpr int kBK = 64;   // K per chunk: 8 vectors of 8 weights
+constexpr int kKcSeg = 4; // K chunks per 32-vector code segment
+
 // ---------------------------------------------------------------- grouping
 
 constexpr int kGroupThreads = 1024;
 constexpr int kExpertsPerThread = kMaxExperts / kGroupThreads; // 4
 
+__device__ __forceinline__ int pad16(int n) { return (n + 15) & ~15; }
+
+// rows the chunks of an expert with c tokens take in the tiled activation buffers
+__device__ __forceinline__ int expert_rows(int c) {
+    const int full = c / kGroupTokens, rest = c % kGroupTokens;
+    return full * kGroupTokens + (rest ? pad16(rest) : 0);
+}
+
 __global__ void __launch_bounds__(kGroupThreads) group_kernel(const int32_t *__restrict__ idx, int S,
                                                               int E, int min_tokens, Grouping G) {
     __shared__ int cnt[kMaxExperts];
     __shared__ int cur[kMaxExperts];
-    __shared__ int2 wsum[kGroupThreads / 32];
-    __shared__ int2 total;
+    __shared__ int4 wsum[kGroupThreads / 32];
+    __shared__ int4 total;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < E; e += kGroupThreads) cnt[e] = 0;
     __syncthreads();
@@ -52,49 +73,56 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(const int32_t *__r
         if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
-    // exclusive scans over experts of (slots, tensor-core chunks); thread owns experts
-    // [4 tid, 4 tid + 4)
-    int ls[kExpertsPerThread], lc[kExpertsPerThread];
-    int2 mine = make_int2(0, 0);
+    // exclusive scans over experts of (slots, tensor-core chunks, tiled rows); the thread
+    // owns experts [4 tid, 4 tid + 4)
+    int ls[kExpertsPerThread], lc[kExpertsPerThread], lr[kExpertsPerThread];
+    int4 mine = make_int4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < kExpertsPerThread; ++i) {
         const int e = kExpertsPerThread * tid + i;
         const int c = e < E ? cnt[e] : 0;
-        const int nc = c >= min_tokens ? (c + kGroupTokens - 1) / kGroupTokens : 0;
+        const bool tensor = c >= min_tokens && c > 0;
         ls[i] = mine.x;
         lc[i] = mine.y;
+        lr[i] = mine.z;
         mine.x += c;
-        mine.y += nc;
+        mine.y += tensor ? (c + kGroupTokens - 1) / kGroupTokens : 0;
+        mine.z += tensor ? expert_rows(c) : 0;
     }
-    int2 inc = mine;
+    int4 inc = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int a = __shfl_up_sync(0xffffffffu, inc.x, o);
         const int b = __shfl_up_sync(0xffffffffu, inc.y, o);
+        const int c = __shfl_up_sync(0xffffffffu, inc.z, o);
         if (lane >= o) {
             inc.x += a;
             inc.y += b;
+            inc.z += c;
         }
     }
     if (lane == 31) wsum[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        const int2 v = wsum[lane];
-        int2 w = v;
+        const int4 v = wsum[lane];
+        int4 w = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int a = __shfl_up_sync(0xffffffffu, w.x, o);
             const int b = __shfl_up_sync(0xffffffffu, w.y, o);
+            const int c = __shfl_up_sync(0xffffffffu, w.z, o);
             if (lane >= o) {
                 w.x += a;
                 w.y += b;
+                w.z += c;
             }
         }
-        wsum[lane] = make_int2(w.x - v.x, w.y - v.y);
+        wsum[lane] = make_int4(w.x - v.x, w.y - v.y, w.z - v.z, 0);
         if (lane == 31) total = w;
     }
     __syncthreads();
-    const int2 base = make_int2(wsum[warp].x + inc.x - mine.x, wsum[warp].y + inc.y - mine.y);
+    const int4 ws = wsum[warp];
+    const int4 base = make_int4(ws.x + inc.x - mine.x, ws.y + inc.y - mine.y, ws.z + inc.z - mine.z, 0);
 #pragma unroll
     for (int i = 0; i < kExpertsPerThread; ++i) {
         const int e = kExpertsPerThread * tid + i;
@@ -103,11 +131,14 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(const int32_t *__r
         G.offs[e] = off;
         cur[e] = off;
         const int c = cnt[e];
-        if (c >= min_tokens) {
+        if (c >= min_tokens && c > 0) {
             const int nc = (c + kGroupTokens - 1) / kGroupTokens;
-            for (int j = 0; j < nc; ++j)
-                G.chunks[base.y + lc[i] + j] =
-                    make_int4(e, off + j * kGroupTokens, min(kGroupTokens, c - j * kGroupTokens), 0);
+            int row = base.z + lr[i];
+            for (int j = 0; j < nc; ++j) {
+                const int n = min(kGroupTokens, c - j * kGroupTokens);
+                G.chunks[base.y + lc[i] + j] = make_int4(e, off + j * kGroupTokens, n, row);
+                row += pad16(n);
+            }
         }
     }
     if (tid == 0) {
@@ -144,56 +175,91 @@ __global__ void __launch_bounds__(kGroupThreads) group_kernel(const int32_t *__r
     }
 }
 
-// hidden states (fp32 or bf16) -> fp16, 8 elements per thread
+// Tiled fp16 activations of every chunk: for K chunk kc the npad x 64 tile is one
+// contiguous block of npad * 128 bytes made of 8x8 core matrices (token n, 8 inputs ki):
+// byte (n >> 3) * 1024 + ki * 128 + (n & 7) * 16.  xg holds the hidden states (gate/up
+// input); in ag (down input, written by the gate/up epilogue) the pieces the epilogue
+// never writes -- padding tokens, inputs past f -- are zeroed here.
+__device__ __forceinline__ uint32_t tile_off(int kc, int npad, int n, int col) {
+    return (uint32_t)kc * npad * 128 + (n >> 3) * 1024 + ((col & 63) >> 3) * 128 + (n & 7) * 16;
+}
+
 template <bool kBf16>
-__global__ void prep_kernel(const void *__restrict__ h, uint16_t *__restrict__ x16, size_t n8) {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-        float v[8];
-        if constexpr (kBf16) {
-            const uint4 raw = reinterpret_cast<const uint4 *>(h)[i];
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+__global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ h, Grouping G, int d, int f, int k) {
+    const int n_chunks = G.counts[0];
+    const int kcd = (d + kBK - 1) / kBK, kcf = (f + kBK - 1) / kBK;
+    for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const int4 ch = G.chunks[c];
+        const int start = ch.y, nt = ch.z, rb = ch.w, npad = pad16(nt);
+        uint4 *xg = reinterpret_cast<uint4 *>(G.xg + (size_t)rb * kcd * 128);
+        const int per_tile = npad * 8;
+        for (int p = threadIdx.x; p < kcd * per_tile; p += blockDim.x) {
+            const int kc = p / per_tile, o = p - kc * per_tile;
+            const int n = ((o >> 6) << 3) | (o & 7), ki = (o >> 3) & 7;
+            const int col = kc * kBK + ki * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (n < nt && col < d) {
+                const int t = G.sorted[start + n] / k;
+                float x[8];
+                if constexpr (kBf16) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(h) +
+                                                                       (size_t)t * d + col);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
-                v[2 * j] = f.x;
-                v[2 * j + 1] = f.y;
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[j]));
+                        x[2 * j] = f2.x;
+                        x[2 * j + 1] = f2.y;
+                    }
+                } else {
+                    const float4 a = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(h) +
+                                                                       (size_t)t * d + col);
+                    const float4 b = *(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(h) +
+                                                                        (size_t)t * d + col) + 1);
+                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+                }
+                uint32_t *vw = &v.x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __half2 p2 = __floats2half2_rn(x[2 * j], x[2 * j + 1]);
+                    vw[j] = *reinterpret_cast<const uint32_t *>(&p2);
+                }
             }
-        } else {
-            const float4 a = reinterpret_cast<const float4 *>(h)[2 * i];
-            const float4 b = reinterpret_cast<const float4 *>(h)[2 * i + 1];
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            xg[p] = v;
         }
-        uint4 o;
-        uint32_t *ow = &o.x;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __half2 p = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
-            ow[j] = *reinterpret_cast<const uint32_t *>(&p);
+        uint4 *ag = reinterpret_cast<uint4 *>(G.ag + (size_t)rb * kcf * 128);
+        for (int p = threadIdx.x; p < kcf * per_tile; p += blockDim.x) {
+            const int kc = p / per_tile, o = p - kc * per_tile;
+            const int n = ((o >> 6) << 3) | (o & 7), ki = (o >> 3) & 7;
+            if (n >= nt || kc * kBK + ki * 8 >= f) ag[p] = make_uint4(0, 0, 0, 0);
         }
-        reinterpret_cast<uint4 *>(x16)[i] = o;
     }
 }
 
 // ---------------------------------------------------------------- tensor-core kernels
 
-constexpr int kMmaThreads = 512;
-constexpr int kBM = 128;              // output rows per item (MMA M)
-constexpr int kBK = 64;               // K per chunk: 8 vectors of 8 weights
-constexpr int kRing = 4;              // code / activation tile stages
+constexpr int kDecWarps = 16;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kProdWarp = kDecWarps, kIssueWarp = kDecWarps + 1;
+constexpr int kMmaThreads = kDecThreads + 64;
+constexpr int kBRing = 4;             // activation tile stages
 constexpr uint32_t kCopies = 8;       // codebook copies: lane j of a quarter-warp reads copy j
 constexpr uint32_t kCbBytes = kStages * kCodes * kCopies * 16;  // 96 KiB of fp16 rows
 constexpr uint32_t kABytes = kBM * kBK * 2;                     // 16 KiB
 constexpr uint32_t kBBytes = kGroupTokens * kBK * 2;           // 16 KiB
-constexpr uint32_t kCodeBytes = 8 * kStages * 8 * 16;          // 8 groups x 3 stages x 8 chunks
+constexpr uint32_t kSegBytes = 8 * kStages * 512;              // 8 row groups x 3 stages x 32 vectors
 constexpr uint32_t kOffCb = 0;
 constexpr uint32_t kOffA = kOffCb + kCbBytes;
 constexpr uint32_t kOffB = kOffA + 2 * kABytes;
-constexpr uint32_t kOffCode = kOffB + kRing * kBBytes;
-constexpr uint32_t kOffSlot = kOffCode + kRing * kCodeBytes;
+constexpr uint32_t kOffSeg = kOffB + kBRing * kBBytes;
+constexpr uint32_t kOffSlot = kOffSeg + 2 * kSegBytes;
 constexpr uint32_t kOffBar = kOffSlot + kGroupTokens * 4;
-constexpr uint32_t kOffFlag = kOffBar + 16;
-constexpr uint32_t kMmaSmem = kOffFlag + 16;
+// barrier indices
+enum { kSegFull = 0, kSegEmpty = 2, kBFull = 4, kBEmpty = 8, kAFull = 12, kAEmpty = 14, kAccFull = 16,
+       kAccEmpty = 17, kNumBars = 18 };
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kMmaSmem = kOffMisc + 16;
 constexpr uint32_t kTmemCols = 2 * kGroupTokens; // gate and up accumulators
 static_assert(kMmaSmem <= 227 * 1024, "shared memory of the tensor-core kernel");
 
@@ -207,19 +273,12 @@ struct MmaArgs {
     const int32_t *sorted;
     const int4 *chunks;
     const int32_t *counts;
-    const uint16_t *x16; // [T][d]
-    uint16_t *a16;       // [S][f]
+    const uint8_t *bsrc; // tiled fp16 activations the MMAs read (xg or ag)
+    uint8_t *ag;         // gate/up output tiles (down input)
     float *part_dn;      // [S][npair][d]
     unsigned long long *stats;
     uint32_t *err;
 };
-
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, uint32_t bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ uint32_t half2_bits(float a, float b) {
     const __half2 p = __floats2half2_rn(a, b);
@@ -229,211 +288,274 @@ __device__ __forceinline__ uint32_t hadd2_bits(uint32_t a, uint32_t b) {
     const __half2 r = __hadd2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
     return *reinterpret_cast<const uint32_t *>(&r);
 }
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void dec_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kDecThreads) : "memory"); }
 
-// One item = (chunk of <= 128 tokens of one expert, 128-row block of the output).  K is
-// walked in chunks of 64: the codes of the tile and the chunk's activations arrive by
-// cp.async two chunks ahead (4-stage ring), all threads decode the weight tile into an
-// A buffer (two of them), one thread issues the four K=16 MMAs and commits them to the
-// A buffer's mbarrier.  The MMAs of chunk q run while the weights of chunk q+1 are decoded.
+// Wait for the phase of the given parity.  Gives up after a second (then raises the
+// CTA's abort flag) or at once when the flag is already up; with check_abort false only
+// the second bounds it (used to drain copies and MMAs in flight before exit).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           bool check_abort = true) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if ((it & 15) == 0) {
+            if (check_abort && *abort_flag) return false;
+            if (global_ns() - t0 > 1000000000ull) {
+                *abort_flag = 1;
+                return false;
+            }
+            __nanosleep(64);
+        }
+    }
+}
+
+// The same for a whole warp: every lane waits, lane 0's verdict counts for all.
+__device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                bool check_abort = true) {
+    const bool ok = wait_phase(bar, parity, abort_flag, check_abort);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// One item = (chunk of <= 128 tokens of one expert, 128-row block of the output).
 template <bool kDown>
 __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
     extern __shared__ __align__(1024) unsigned char gsm[];
     const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(gsm);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int *s_slot = reinterpret_cast<int *>(gsm + kOffSlot);
-    volatile int *s_flag = reinterpret_cast<volatile int *>(gsm + kOffFlag);
-    const uint32_t bar[2] = {sbase + kOffBar, sbase + kOffBar + 8};
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gsm + kOffMisc + 4);
+    auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
     if (tid == 0) {
-        tc::mbar_init(bar[0], 1);
-        tc::mbar_init(bar[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(kSegFull + i), 1);
+            tc::mbar_init(bar(kSegEmpty + i), kDecWarps);
+            tc::mbar_init(bar(kAFull + i), kDecWarps);
+            tc::mbar_init(bar(kAEmpty + i), 1);
+        }
+        for (int i = 0; i < kBRing; ++i) {
+            tc::mbar_init(bar(kBFull + i), 1);
+            tc::mbar_init(bar(kBEmpty + i), 1);
+        }
+        tc::mbar_init(bar(kAccFull), 1);
+        tc::mbar_init(bar(kAccEmpty), kDecWarps);
         tc::mbar_init_fence();
-        s_flag[0] = 0;
+        *abort_flag = 0;
     }
-    if (warp == 0) tc::tmem_alloc(sbase + kOffFlag + 4, kTmemCols);
+    if (warp == 0) tc::tmem_alloc(sbase + kOffMisc, kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gsm + kOffFlag + 4);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gsm + kOffMisc);
 
     const MatGeom G = A.geom;
     const int nmb = (G.n_out + kBM - 1) / kBM;
     const int KC = (G.n_in + kBK - 1) / kBK;
     const int n_items = A.counts[0] * nmb;
     constexpr int kPasses = kDown ? 1 : 2;
-    // decode role: vector column jj of the chunk, row group gq, code bytes 2 qh, 2 qh + 1
-    const int jj = lane & 7, gq = warp & 7, qh = (warp >> 3) * 4 + (lane >> 3);
-    uint32_t q = 0; // MMA batches committed by this CTA
-    bool dead = false;
 
-    for (int item = blockIdx.x; item < n_items && !dead; item += gridDim.x) {
-        const int4 ch = A.chunks[item / nmb];
-        const int mb = item % nmb;
-        const int e = ch.x, start = ch.y, nt = ch.z;
-        const int npad = (nt + 15) & ~15;
-        const uint32_t idesc = tc::idesc_f16_f32(kBM, npad);
-        const uint8_t *rec = A.records + (size_t)e * A.stride;
-        __syncthreads(); // the previous item's epilogue is done with s_slot and TMEM
-        tc::fence_after_sync();
-        if (tid < kGroupTokens) s_slot[tid] = tid < nt ? A.sorted[start + tid] : 0;
-
-        for (int pass = 0; pass < kPasses && !dead; ++pass) {
-            const int mat = kDown ? 2 : pass;
-            const uint8_t *sec = rec + A.sec[mat];
-            // codebook rows of (e, mat) as fp16, kCopies copies side by side
-            {
-                const float *cb = A.codebooks + ((size_t)e * 3 + mat) * (kStages * kCodes * kVec);
-                uint4 *dst = reinterpret_cast<uint4 *>(gsm + kOffCb);
-                for (int r = tid; r < kStages * kCodes; r += kMmaThreads) {
-                    const float4 lo = __ldg(reinterpret_cast<const float4 *>(cb) + 2 * r);
-                    const float4 hi = __ldg(reinterpret_cast<const float4 *>(cb) + 2 * r + 1);
-                    const uint4 hv = make_uint4(half2_bits(lo.x, lo.y), half2_bits(lo.z, lo.w),
-                                                half2_bits(hi.x, hi.y), half2_bits(hi.z, hi.w));
-#pragma unroll
-                    for (uint32_t c = 0; c < kCopies; ++c) dst[r * kCopies + c] = hv;
-                }
-            }
-            __syncthreads(); // s_slot (for the loads) and the codebook rows are in place
-
-            auto issue_loads = [&](int kc, uint32_t ring) {
-                if (kc < KC) {
-                    if (tid < 192) {
-                        const int g = tid / 24, s = (tid / 8) % 3, j8 = tid & 7;
-                        const int j = kc * 8 + j8, Gg = mb * 8 + g;
-                        const bool ok = Gg < G.groups;
-                        const uint8_t *src =
-                            ok ? sec + (((size_t)(j >> 5) * G.groups + Gg) * kStages + s) * 512 + (j & 31) * 16
-                               : sec;
-                        cp_async16_zfill(sbase + kOffCode + ring * kCodeBytes + tid * 16, src, ok ? 16u : 0u);
+    if (warp == kProdWarp) {
+        // ---------------- producer: codes per segment, activation tile per K chunk (the
+        // whole warp walks the loop; lane 0 issues)
+        uint32_t q = 0, gs = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            const int4 ch = A.chunks[item / nmb];
+            const int mb = item % nmb, npad = pad16(ch.z);
+            const uint32_t bbytes = (uint32_t)npad * 128;
+            const uint8_t *bsrc = A.bsrc + (size_t)ch.w * KC * 128;
+            const uint8_t *rec = A.records + (size_t)ch.x * A.stride;
+            const uint32_t seg_bytes = (uint32_t)min(8, G.groups - 8 * mb) * (kStages * 512);
+            for (int pass = 0; pass < kPasses; ++pass) {
+                const uint8_t *sec = rec + A.sec[kDown ? 2 : pass];
+                for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
+                    const int sb = gs & 1;
+                    bool ok = gs < 2 || wait_phase_warp(bar(kSegEmpty + sb), ((gs - 2) >> 1) & 1, abort_flag);
+                    if (ok && lane == 0 && !*abort_flag) {
+                        const uint8_t *src = sec + ((size_t)(kc0 / kKcSeg) * G.groups + 8 * mb) * (kStages * 512);
+                        tc::mbar_arrive_expect_tx(bar(kSegFull + sb), seg_bytes);
+                        tc::bulk_g2s(sbase + kOffSeg + sb * kSegBytes, src, seg_bytes, bar(kSegFull + sb));
                     }
-                    const int npieces = npad * 8;
-                    for (int p = tid; p < npieces; p += kMmaThreads) {
-                        const int ki = p / npad, n = p - ki * npad;
-                        const int kk = kc * kBK + ki * 8;
-                        const bool ok = n < nt && kk < G.n_in;
-                        const uint16_t *src = A.x16;
-                        if (ok) {
-                            const int slot = s_slot[n];
-                            src = kDown ? A.a16 + (size_t)slot * A.f + kk : A.x16 + (size_t)(slot / A.k) * A.d + kk;
+                    __syncwarp();
+                    for (int kc = kc0; kc < min(KC, kc0 + kKcSeg); ++kc, ++q) {
+                        const int rs = q % kBRing;
+                        ok = q < kBRing ||
+                             wait_phase_warp(bar(kBEmpty + rs), ((q - kBRing) / kBRing) & 1, abort_flag);
+                        if (ok && lane == 0 && !*abort_flag) {
+                            tc::mbar_arrive_expect_tx(bar(kBFull + rs), bbytes);
+                            tc::bulk_g2s(sbase + kOffB + rs * kBBytes, bsrc + (size_t)kc * bbytes, bbytes,
+                                         bar(kBFull + rs));
                         }
-                        cp_async16_zfill(sbase + kOffB + ring * kBBytes + (n >> 3) * 1024 + ki * 128 + (n & 7) * 16,
-                                         src, ok ? 16u : 0u);
+                        __syncwarp();
                     }
                 }
-                cp_commit();
-            };
-
-            issue_loads(0, q % kRing);
-            issue_loads(1, (q + 1) % kRing);
-            for (int kc = 0; kc < KC; ++kc, ++q) {
-                // ring slot (q + 2) % 4 and A[q & 1] were last read by the MMAs of q - 2,
-                // complete since the barrier that closed the previous chunk
-                issue_loads(kc + 2, (q + 2) % kRing);
-                cp_wait<2>();
-                __syncthreads(); // chunk kc's codes and activations are in shared memory
-                {
-                    const unsigned char *ct = gsm + kOffCode + (q % kRing) * kCodeBytes + (gq * 24 + jj) * 16 + 2 * qh;
-                    const uint32_t c0 = *reinterpret_cast<const uint16_t *>(ct);
-                    const uint32_t c1 = *reinterpret_cast<const uint16_t *>(ct + 128);
-                    const uint32_t c2 = *reinterpret_cast<const uint16_t *>(ct + 256);
-                    const int j = kc * 8 + jj, j32 = j & 31;
-                    const bool jok = j < G.nv;
-                    const uint4 *cbs = reinterpret_cast<const uint4 *>(gsm + kOffCb);
-                    unsigned char *abuf = gsm + kOffA + (q & 1) * kABytes;
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const int qq = 2 * qh + b;
-                        const int rl = 16 * gq + ((j32 ^ qq) & 15);
-                        const int row = mb * kBM + rl;
-                        const uint4 v0 = cbs[(0 * kCodes + ((c0 >> (8 * b)) & 255)) * kCopies + jj];
-                        const uint4 v1 = cbs[(1 * kCodes + ((c1 >> (8 * b)) & 255)) * kCopies + jj];
-                        const uint4 v2 = cbs[(2 * kCodes + ((c2 >> (8 * b)) & 255)) * kCopies + jj];
-                        uint4 w;
-                        w.x = hadd2_bits(hadd2_bits(v0.x, v1.x), v2.x);
-                        w.y = hadd2_bits(hadd2_bits(v0.y, v1.y), v2.y);
-                        w.z = hadd2_bits(hadd2_bits(v0.z, v1.z), v2.z);
-                        w.w = hadd2_bits(hadd2_bits(v0.w, v1.w), v2.w);
-                        if (!jok || row >= G.n_out) w = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(abuf + (rl >> 3) * 1024 + jj * 128 + (rl & 7) * 16) = w;
-                    }
-                }
-                tc::fence_proxy_async();
-                if (tid == 0 && q >= 1 && !tc::mbar_wait(bar[(q - 1) & 1], ((q - 1) >> 1) & 1)) s_flag[0] = 1;
-                __syncthreads(); // tile decoded; the MMAs of q - 1 are complete
-                if (s_flag[0]) {
-                    dead = true;
-                    break;
-                }
-                if (tid == 0) {
+            }
+        }
+        // drain: the last copies into each buffer have landed before the CTA exits
+        for (uint32_t i = 0; i < 2 && i < gs; ++i) {
+            const uint32_t g = gs - 1 - i;
+            wait_phase_warp(bar(kSegFull + (g & 1)), (g >> 1) & 1, abort_flag, false);
+        }
+        for (uint32_t i = 0; i < (uint32_t)kBRing && i < q; ++i) {
+            const uint32_t g = q - 1 - i;
+            wait_phase_warp(bar(kBFull + g % kBRing), (g / kBRing) & 1, abort_flag, false);
+        }
+    } else if (warp == kIssueWarp) {
+        // ---------------- MMA issue (the whole warp walks the loop; lane 0 issues)
+        uint32_t q = 0, it = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+            const int4 ch = A.chunks[item / nmb];
+            const int npad = pad16(ch.z);
+            const uint32_t idesc = tc::idesc_f16_f32(kBM, npad);
+            if (it >= 1) wait_phase_warp(bar(kAccEmpty), (it - 1) & 1, abort_flag);
+            tc::fence_after_sync();
+            for (int pass = 0; pass < kPasses; ++pass) {
+                for (int kc = 0; kc < KC; ++kc, ++q) {
+                    const int ab = q & 1, rs = q % kBRing;
+                    wait_phase_warp(bar(kAFull + ab), (q >> 1) & 1, abort_flag);
+                    wait_phase_warp(bar(kBFull + rs), (q / kBRing) & 1, abort_flag);
                     tc::fence_after_sync();
-                    const uint32_t a_addr = sbase + kOffA + (q & 1) * kABytes;
-                    const uint32_t b_addr = sbase + kOffB + (q % kRing) * kBBytes;
+                    if (lane == 0) {
+                        const uint32_t a_addr = sbase + kOffA + ab * kABytes;
+                        const uint32_t b_addr = sbase + kOffB + rs * kBBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc::mma_f16(tmem + pass * kGroupTokens, tc::smem_desc(a_addr + kk * 256, 128, 1024),
-                                    tc::smem_desc(b_addr + kk * 256, 128, 1024), idesc, (kc | kk) != 0);
-                    tc::mma_commit(bar[q & 1]);
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc::mma_f16(tmem + pass * kGroupTokens, tc::smem_desc(a_addr + kk * 256, 128, 1024),
+                                        tc::smem_desc(b_addr + kk * 256, 128, 1024), idesc, (kc | kk) != 0);
+                        tc::mma_commit(bar(kAEmpty + ab));
+                        tc::mma_commit(bar(kBEmpty + rs));
+                    }
+                    __syncwarp();
                 }
             }
+            if (lane == 0) {
+                tc::mma_commit(bar(kAccFull));
+                if (A.stats) {
+                    const int mb = item % nmb;
+                    const int rows = min(G.n_out - mb * kBM, kBM);
+                    atomicAdd(A.stats + kStatDemandCode, (unsigned long long)kPasses * rows * G.nv * kStages);
+                    if (mb == 0)
+                        atomicAdd(A.stats + kStatCodebook,
+                                  (unsigned long long)kPasses * kStages * kCodes * kVec * sizeof(float));
+                }
+            }
+            __syncwarp();
         }
-        if (dead) break;
-        // the item's last MMAs
-        if (tid == 0 && !tc::mbar_wait(bar[(q - 1) & 1], ((q - 1) >> 1) & 1)) s_flag[0] = 1;
-        __syncthreads();
-        if (s_flag[0]) {
-            dead = true;
-            break;
-        }
-        tc::fence_after_sync();
-        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. +32 (its output rows) and
-        // column blocks of 16 starting at 16 (w / 4), every 64
-        {
-            const int lq = warp & 3;
-            const int rl = lq * 32 + lane, row = mb * kBM + rl;
-            const uint32_t lane_addr = tmem + ((uint32_t)(lq * 32) << 16);
-            for (int c0 = (warp >> 2) * 16; c0 < npad; c0 += 64) {
-                float z[16];
-                tc::tmem_ld16(lane_addr + c0, z);
-                if constexpr (!kDown) {
-                    float u[16];
-                    tc::tmem_ld16(lane_addr + kGroupTokens + c0, u);
-                    if (row < G.n_out) {
+        // drain: every MMA issued has completed before TMEM is released
+        if (it >= 1) wait_phase_warp(bar(kAccFull), (it - 1) & 1, abort_flag, false);
+    } else {
+        // ---------------- decode warps (and the epilogue)
+        // role in a chunk: vector column jj, row group gq, code bytes 2 qh, 2 qh + 1
+        const int jj = lane & 7, gq = warp & 7, qh = (warp >> 3) * 4 + (lane >> 3);
+        const uint4 *cbs = reinterpret_cast<const uint4 *>(gsm + kOffCb);
+        uint32_t q = 0, gs = 0, it = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+            const int4 ch = A.chunks[item / nmb];
+            const int e = ch.x, nt = ch.z, npad = pad16(nt);
+            const int mb = item % nmb;
+            for (int pass = 0; pass < kPasses; ++pass) {
+                const int mat = kDown ? 2 : pass;
+                dec_barrier(); // every decode warp is past the previous pass (and epilogue)
+                if (pass == 0 && tid < kGroupTokens) s_slot[tid] = tid < nt ? A.sorted[ch.y + tid] : 0;
+                {
+                    const float *cb = A.codebooks + ((size_t)e * 3 + mat) * (kStages * kCodes * kVec);
+                    uint4 *dst = reinterpret_cast<uint4 *>(gsm + kOffCb);
+                    for (int r = tid; r < kStages * kCodes; r += kDecThreads) {
+                        const float4 lo = __ldg(reinterpret_cast<const float4 *>(cb) + 2 * r);
+                        const float4 hi = __ldg(reinterpret_cast<const float4 *>(cb) + 2 * r + 1);
+                        const uint4 hv = make_uint4(half2_bits(lo.x, lo.y), half2_bits(lo.z, lo.w),
+                                                    half2_bits(hi.x, hi.y), half2_bits(hi.z, hi.w));
 #pragma unroll
-                        for (int n = 0; n < 16; ++n)
-                            if (c0 + n < nt) {
-                                const float a = z[n] / (1.0f + expf(-z[n])) * u[n];
-                                const __half ha = __float2half_rn(a);
-                                A.a16[(size_t)s_slot[c0 + n] * A.f + row] = *reinterpret_cast<const uint16_t *>(&ha);
-                            }
+                        for (uint32_t c = 0; c < kCopies; ++c) dst[r * kCopies + c] = hv;
                     }
-                } else {
-                    if (row < G.n_out) {
+                }
+                dec_barrier(); // codebook rows and slots in place
+                for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
+                    const int sb = gs & 1;
+                    wait_phase(bar(kSegFull + sb), (gs >> 1) & 1, abort_flag);
+                    const unsigned char *seg = gsm + kOffSeg + sb * kSegBytes;
+                    for (int kc = kc0; kc < min(KC, kc0 + kKcSeg); ++kc, ++q) {
+                        const int ab = q & 1;
+                        if (q >= 2) wait_phase(bar(kAEmpty + ab), ((q - 2) >> 1) & 1, abort_flag);
+                        const int sub = kc - kc0;
+                        const unsigned char *ct = seg + ((gq * kStages) * 32 + 8 * sub + jj) * 16 + 2 * qh;
+                        const uint32_t c0 = *reinterpret_cast<const uint16_t *>(ct);
+                        const uint32_t c1 = *reinterpret_cast<const uint16_t *>(ct + 512);
+                        const uint32_t c2 = *reinterpret_cast<const uint16_t *>(ct + 1024);
+                        const int j = kc * 8 + jj, j32 = j & 31;
+                        const bool jok = j < G.nv;
+                        unsigned char *abuf = gsm + kOffA + ab * kABytes;
 #pragma unroll
-                        for (int n = 0; n < 16; ++n)
-                            if (c0 + n < nt) A.part_dn[(size_t)s_slot[c0 + n] * A.npair * A.d + row] = z[n];
+                        for (int b = 0; b < 2; ++b) {
+                            const int qq = 2 * qh + b;
+                            const int rl = 16 * gq + ((j32 ^ qq) & 15);
+                            const int row = mb * kBM + rl;
+                            const uint4 v0 = cbs[(0 * kCodes + ((c0 >> (8 * b)) & 255)) * kCopies + jj];
+                            const uint4 v1 = cbs[(1 * kCodes + ((c1 >> (8 * b)) & 255)) * kCopies + jj];
+                            const uint4 v2 = cbs[(2 * kCodes + ((c2 >> (8 * b)) & 255)) * kCopies + jj];
+                            uint4 w;
+                            w.x = hadd2_bits(hadd2_bits(v0.x, v1.x), v2.x);
+                            w.y = hadd2_bits(hadd2_bits(v0.y, v1.y), v2.y);
+                            w.z = hadd2_bits(hadd2_bits(v0.z, v1.z), v2.z);
+                            w.w = hadd2_bits(hadd2_bits(v0.w, v1.w), v2.w);
+                            if (!jok || row >= G.n_out) w = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(abuf + (rl >> 3) * 1024 + jj * 128 + (rl & 7) * 16) = w;
+                        }
+                        tc::fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(bar(kAFull + ab));
+                    }
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(bar(kSegEmpty + sb));
+                }
+            }
+            // epilogue: warp w reads TMEM lanes 32 (w % 4) .. +32 (its output rows) and the
+            // column blocks of 16 starting at 16 (w / 4), every 64
+            wait_phase(bar(kAccFull), it & 1, abort_flag);
+            tc::fence_after_sync();
+            {
+                const int lq = warp & 3;
+                const int rl = lq * 32 + lane, row = mb * kBM + rl;
+                const uint32_t lane_addr = tmem + ((uint32_t)(lq * 32) << 16);
+                const int kcf = (A.f + kBK - 1) / kBK;
+                uint8_t *ag = A.ag + (size_t)ch.w * kcf * 128;
+                for (int c0 = (warp >> 2) * 16; c0 < npad; c0 += 64) {
+                    float z[16];
+                    tc::tmem_ld16(lane_addr + c0, z);
+                    if constexpr (!kDown) {
+                        float u[16];
+                        tc::tmem_ld16(lane_addr + kGroupTokens + c0, u);
+                        if (row < G.n_out) {
+#pragma unroll
+                            for (int n = 0; n < 16; ++n)
+                                if (c0 + n < nt) {
+                                    const float a = z[n] / (1.0f + expf(-z[n])) * u[n];
+                                    const __half ha = __float2half_rn(a);
+                                    *reinterpret_cast<__half *>(ag + tile_off(row >> 6, npad, c0 + n, row) +
+                                                                (row & 7) * 2) = ha;
+                                }
+                        }
+                    } else {
+                        if (row < G.n_out) {
+#pragma unroll
+                            for (int n = 0; n < 16; ++n)
+                                if (c0 + n < nt) A.part_dn[(size_t)s_slot[c0 + n] * A.npair * A.d + row] = z[n];
+                        }
                     }
                 }
             }
-        }
-        tc::fence_before_sync();
-        if (tid == 0 && A.stats) {
-            const int rows = min(G.n_out - mb * kBM, kBM);
-            atomicAdd(A.stats + kStatDemandCode,
-                      (unsigned long long)kPasses * rows * G.nv * kStages);
-            if (mb == 0)
-                atomicAdd(A.stats + kStatCodebook,
-                          (unsigned long long)kPasses * kStages * kCodes * kVec * sizeof(float));
-        }
-    }
-    cp_wait<0>();
-    if (dead) {
-        // give the MMAs in flight a bounded chance to finish before TMEM is released
-        if (tid == 0) {
-            if (q >= 1) tc::mbar_wait(bar[(q - 1) & 1], ((q - 1) >> 1) & 1);
-            atomicOr(A.err, kErrTimeout);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(kAccEmpty));
         }
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0 && *abort_flag) atomicOr(A.err, kErrTimeout);
     if (warp == 0) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
@@ -455,6 +577,10 @@ cudaError_t launch_mma(const MmaArgs &A, int num_sms, cudaStream_t s) {
 
 } // namespace
 
+size_t grouped_tile_rows(int max_slots, int max_chunks) {
+    return (size_t)max_slots + 15 * (size_t)max_chunks;
+}
+
 cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const void *h, int T,
                                    const int32_t *idx, const float *gate, float *out, int mode,
                                    int min_tokens, bool reconstruct, int num_sms, cudaStream_t s,
@@ -463,12 +589,10 @@ cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const
     const int S = T * L.k;
     if (tm) cudaEventRecord(tm->ev[0], s);
     group_kernel<<<1, kGroupThreads, 0, s>>>(idx, S, L.E, min_tokens < 1 ? 1 : min_tokens, G);
-    const size_t n8 = (size_t)T * L.d / 8;
-    const int pgrid = (int)((n8 + 255) / 256 < (size_t)(num_sms * 8) ? (n8 + 255) / 256 : (size_t)(num_sms * 8));
     if (L.act_bf16)
-        prep_kernel<true><<<pgrid, 256, 0, s>>>(h, G.x16, n8);
+        gather_kernel<true><<<num_sms * 2, 256, 0, s>>>(h, G, L.d, L.f, L.k);
     else
-        prep_kernel<false><<<pgrid, 256, 0, s>>>(h, G.x16, n8);
+        gather_kernel<false><<<num_sms * 2, 256, 0, s>>>(h, G, L.d, L.f, L.k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -484,8 +608,7 @@ cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const
     A.sorted = G.sorted;
     A.chunks = G.chunks;
     A.counts = G.counts;
-    A.x16 = G.x16;
-    A.a16 = G.a16;
+    A.ag = G.ag;
     A.part_dn = W.part_dn;
     A.stats = W.stats;
     A.err = W.err;
@@ -494,6 +617,7 @@ cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const
     e = launch_lut_listed(L, W, h, T, idx, G.lut_slots, G.counts + 1, false, reconstruct, num_sms, s);
     if (e != cudaSuccess) return e;
     A.geom = L.gu;
+    A.bsrc = G.xg;
     e = launch_mma<false>(A, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[1], s);
@@ -501,6 +625,7 @@ cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const
     e = launch_lut_listed(L, W, h, T, idx, G.lut_slots, G.counts + 1, true, reconstruct, num_sms, s);
     if (e != cudaSuccess) return e;
     A.geom = L.dn;
+    A.bsrc = G.ag;
     e = launch_mma<true>(A, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[2], s);

@@ -91,6 +91,87 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const float *__restri
     }
 }
 
+// Larger T, split along K: CTA (E tile, T tile, split) sums the products of its K range
+// into part[split][t][e]; reduce_router_kernel adds the splits in order (then the bias,
+// with its TwoSum remainder).  Tiles of 64 tokens x 64 experts, 256 threads with 4x4
+// outputs each, K staged 32 at a time with 128-bit loads.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) router_splitk_kernel(const float *__restrict__ W,
+                                                            const void *__restrict__ h, int T, int E,
+                                                            int d, int k_per_split,
+                                                            float *__restrict__ part) {
+    __shared__ float Hs[kTileK][kTileT + 4];
+    __shared__ float Ws[kTileK][kTileE + 4];
+    const int t0 = blockIdx.y * kTileT, e0 = blockIdx.x * kTileE;
+    const int kb = blockIdx.z * k_per_split, ke = min(d, kb + k_per_split);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+    // loader role: row r (of 64), 4-element group c4 (of 8), two rows per thread
+    const int lr = threadIdx.x >> 3, lc = (threadIdx.x & 7) * 4;
+    for (int k0 = kb; k0 < ke; k0 += kTileK) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = lr + 32 * half;
+            const int kg = k0 + lc;
+            const int t = t0 + r, e = e0 + r;
+            // d % 8 == 0 and k ranges start at multiples of 32: a group of 4 is all in or out
+            float4 hv = make_float4(0.f, 0.f, 0.f, 0.f), wv = hv;
+            if (t < T && kg < ke) hv = load_h4<kBf16>(h, (size_t)t * d + kg);
+            if (e < E && kg < ke) wv = *reinterpret_cast<const float4 *>(W + (size_t)e * d + kg);
+            Hs[lc + 0][r] = hv.x;
+            Hs[lc + 1][r] = hv.y;
+            Hs[lc + 2][r] = hv.z;
+            Hs[lc + 3][r] = hv.w;
+            Ws[lc + 0][r] = wv.x;
+            Ws[lc + 1][r] = wv.y;
+            Ws[lc + 2][r] = wv.z;
+            Ws[lc + 3][r] = wv.w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < kTileK; ++kk) {
+            float hv[4], wv[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) hv[a] = Hs[kk][ty * 4 + a];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) wv[b] = Ws[kk][tx * 4 + b];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(hv[a], wv[b], acc[a][b]);
+        }
+        __syncthreads();
+    }
+    float *p = part + (size_t)blockIdx.z * T * E;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int t = t0 + ty * 4 + a;
+        if (t >= T) continue;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int e = e0 + tx * 4 + b;
+            if (e < E) p[(size_t)t * E + e] = acc[a][b];
+        }
+    }
+}
+
+__global__ void reduce_router_kernel(const float *__restrict__ part, int nsplit, const float *__restrict__ bias,
+                                     int T, int E, float *__restrict__ logits, float *__restrict__ logits_lo) {
+    const size_t n = (size_t)T * E;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        float v = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp) v += part[(size_t)sp * n + i];
+        float hi = v, lo = 0.f;
+        if (bias) two_sum(v, bias[i % E], hi, lo);
+        logits[i] = hi;
+        if (logits_lo) logits_lo[i] = lo;
+    }
+}
+
 // Small-T router with the tokens staged in shared memory: 4 experts per CTA of 512
 // threads, every lane's W_r loads in flight at once (same sums as the step kernel's
 // router items).
@@ -196,8 +277,17 @@ __global__ void set_count_kernel(int32_t *count, int T, int P) {
 
 constexpr size_t kRouterStageMax = 200 * 1024; // shared memory for staged hidden states
 
+int router_splits(int T, int E, int d, int num_sms) {
+    const int tiles = ((E + kTileE - 1) / kTileE) * ((T + kTileT - 1) / kTileT);
+    int ns = (2 * num_sms + tiles - 1) / tiles;
+    const int max_ns = (d + 255) / 256; // at least 256 of K per split
+    if (ns > max_ns) ns = max_ns;
+    if (ns > kRouterMaxSplits) ns = kRouterMaxSplits;
+    return ns < 1 ? 1 : ns;
+}
+
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
-                          float *logits_lo, cudaStream_t s) {
+                          float *logits_lo, cudaStream_t s, float *part, int num_sms) {
     const size_t row_bytes = (size_t)L.d * 4;
     if (T <= 16 && row_bytes <= kRouterStageMax) {
         const int hs_tokens = (int)std::min<size_t>({(size_t)kRouterTok, (size_t)T, kRouterStageMax / row_bytes});
@@ -223,6 +313,18 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
             router_small_kernel<true><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
         else
             router_small_kernel<false><<<grid, 256, 0, s>>>(L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo);
+    } else if (part) {
+        const int ns = router_splits(T, L.E, L.d, num_sms);
+        const int kps = ((L.d + ns - 1) / ns + kTileK - 1) / kTileK * kTileK;
+        const int nsu = (L.d + kps - 1) / kps;
+        dim3 grid((L.E + kTileE - 1) / kTileE, (T + kTileT - 1) / kTileT, nsu);
+        if (L.act_bf16)
+            router_splitk_kernel<true><<<grid, 256, 0, s>>>(L.router_w, h, T, L.E, L.d, kps, part);
+        else
+            router_splitk_kernel<false><<<grid, 256, 0, s>>>(L.router_w, h, T, L.E, L.d, kps, part);
+        const size_t n = (size_t)T * L.E;
+        const int rg = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms * 8);
+        reduce_router_kernel<<<rg, 256, 0, s>>>(part, nsu, L.router_b, T, L.E, logits, logits_lo);
     } else {
         dim3 grid((L.E + kTileE - 1) / kTileE, (T + kTileT - 1) / kTileT);
         if (L.act_bf16)
