@@ -169,6 +169,7 @@ cudaError_t launch_rmsnorm(const float *in, float *out, int T, int d, cudaStream
 
 int device_sm_count();
 
+
 // Sets the calling thread's message returned by waste_moe_last_error().
 void set_last_error(const char *msg);
 

@@ -103,6 +103,10 @@ __device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes
     }
 }
 
+// Slot of segment column j (0..31) within a table row of one part: the columns
+// j, j + 8, j + 16, j + 24 sit side by side, so the table build stores 16 bytes at a time.
+__host__ __device__ constexpr int tab_col(int j) { return 4 * (j & 7) + (j >> 3); }
+
 // Decode a unit index into (slot, first segment, part bases, row-group range).
 struct Unit {
     int slot, e, seg0, g0, g1;
@@ -168,8 +172,9 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // Codebook rows of one stage for both parts -> smem [part][256][8] (16 KiB), as
 // one cp.async group.
+template <int kNT = kThreads>
 __device__ __forceinline__ void issue_stage(float *dst, const float *cb_p0, const float *cb_p1, int s) {
-    for (int i = threadIdx.x; i < 1024; i += kThreads) {
+    for (int i = threadIdx.x; i < 1024; i += kNT) {
         const int part = i >> 9, ii = i & 511;
         const float *src = (part ? cb_p1 : cb_p0) + (size_t)s * kCodes * kVec + (size_t)ii * 4;
         cp_async16(dst + part * kCodes * kVec + ii * 4, src);
@@ -255,10 +260,15 @@ extern __shared__ __align__(16) unsigned char lut_smem[];
 // one kind: when `has_next`, the next unit's stages 0 and 1 are already on their way
 // into the buffers when this one returns.  For a down unit, `dep` (if not null) is a
 // completion counter that must reach dep_target before the gate/up partials are read.
-template <bool kDown, bool kRecon, bool kBf16>
+// kNT: threads of the CTA (a multiple of 128); kPing: codes of the next row group are
+// loaded into registers while the current one is consumed.
+template <bool kDown, bool kRecon, bool kBf16, int kNT = kThreads, bool kPing = kCodePingPong,
+          int kPf = kPrefetchRounds>
 __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
                                       int &par, bool &primed, const unsigned *dep,
                                       unsigned dep_target, unsigned char *) {
+    constexpr int kNW = kNT / 32;
+    static_assert(kNT % 128 == 0 && kNT <= 512, "CTA size of the lookup units");
     // the dynamic shared memory named directly, so every access compiles to a shared one
     unsigned char *smem = lut_smem;
     // local copies: the caller's structs are read once, the fields then live in registers
@@ -270,21 +280,22 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b4 = lane >> 4;
     const MatGeom &G = kDown ? A.dn : A.gu;
-    // table column byte offset of register-part p: column (p ^ b4), lane l
-    const uint32_t colb0 = ((uint32_t)(0 ^ b4) << 7) | ((uint32_t)lane << 2);
-    const uint32_t colb1 = ((uint32_t)(1 ^ b4) << 7) | ((uint32_t)lane << 2);
+    // table column byte offset of register-part p: part (p ^ b4), the slot of column
+    // `lane` in the permuted column order of the tables
+    const uint32_t colb0 = ((uint32_t)(0 ^ b4) << 7) | ((uint32_t)tab_col(lane) << 2);
+    const uint32_t colb1 = ((uint32_t)(1 ^ b4) << 7) | ((uint32_t)tab_col(lane) << 2);
     const bool valid = U.base[0] != nullptr;
     if (!kRecon && !primed) {
         const float *q0, *q1;
         unit_codebooks<kDown>(A, U, q0, q1);
-        issue_stage(cbuf + par * kStageFloats, q0, q1, 0);
-        issue_stage(cbuf + (par ^ 1) * kStageFloats, q0, q1, 1);
+        issue_stage<kNT>(cbuf + par * kStageFloats, q0, q1, 0);
+        issue_stage<kNT>(cbuf + (par ^ 1) * kStageFloats, q0, q1, 1);
     }
     // warm L2 with the first rounds of row groups this warp streams (the tail of the
     // previous unit already asked for them, except on a CTA's first unit)
 #pragma unroll 1
-    for (int i = 0; i < kPrefetchRounds; ++i) {
-        const int g = U.g0 + warp + i * kWarps;
+    for (int i = 0; i < kPf; ++i) {
+        const int g = U.g0 + warp + i * kNW;
         if (g < U.g1) prefetch_group(U, g, lane);
     }
     if (!valid && threadIdx.x == 0) atomicOr(A.err, kErrBadExpert);
@@ -305,8 +316,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         // gate/up segments in a fixed order
         __syncthreads(); // xs may still be read by the previous unit
         if (dep) wait_counter(dep, dep_target, A.err);
-        {
-            const int r = U.seg0 * kSegVec * kVec + threadIdx.x; // index into f
+        for (int i = threadIdx.x; i < 2 * kSegVec * kVec; i += kNT) {
+            const int r = U.seg0 * kSegVec * kVec + i; // index into f
             float a = 0.f;
             if (valid && r < A.gu.n_out) {
                 const float *pg = A.part_gu + (size_t)U.slot * A.gu.nseg * 2 * A.gu.n_out;
@@ -317,7 +328,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                 }
                 a = zg / (1.0f + expf(-zg)) * zu;
             }
-            xs[threadIdx.x] = a;
+            xs[i] = a;
         }
         __syncthreads();
 #pragma unroll
@@ -347,21 +358,28 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         // Per stage and part the table is the product T[j][c] = sum_v X[j][v] C[c][v]
         // (32 columns j x 256 codes c, K = 8), taken on the tensor cores as
         // m16n8k8 TF32 MMAs with each operand split into a TF32 head and tail
-        // (tail*head + head*tail + head*head), which keeps fp32 accuracy.  Warp w owns
-        // part (w >> 3), rows j in [16 ((w >> 2) & 1), +16) and 8 of the 32 code tiles.
+        // (tail*head + head*tail + head*head), which keeps fp32 accuracy.  The warps form
+        // 2 teams of kNW / 2, one per part; a warp takes both 16-row halves (all 32
+        // columns j) of a code tile, and its team's 32 code tiles in turn.
         float *tab = reinterpret_cast<float *>(smem);
         const float *p0, *p1, *n0 = nullptr, *n1 = nullptr;
         unit_codebooks<kDown>(A, U, p0, p1);
         if (has_next) unit_codebooks<kDown>(A, N, n0, n1);
-        const int mp = warp >> 3, mm = (warp >> 2) & 1, mq = warp & 3;
+        constexpr int kWpp = kNW / 2; // warps per part
+        const int mp = warp / kWpp, mq = warp % kWpp;
         const int fg = lane >> 2, ft = lane & 3;
-        uint32_t ahi[4], alo[4];
-        {
+        // the lane whose results this lane stores: quarter-warp q stores code pair q of the
+        // tile for the 8 row groups fg, so its 8 lanes hit 8 different bank quads
+        const int src = ((lane & 7) << 2) | (lane >> 3);
+        const int st_fg = lane & 7, st_ft = lane >> 3;
+        uint32_t ahi[2][4], alo[2][4];
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
             const float *X = xs + mp * kSegVec * kVec + (mm * 16) * kVec;
             const float av[4] = {X[fg * kVec + ft], X[(fg + 8) * kVec + ft], X[fg * kVec + ft + 4],
                                  X[(fg + 8) * kVec + ft + 4]};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) split_tf32(av[i], ahi[i], alo[i]);
+            for (int i = 0; i < 4; ++i) split_tf32(av[i], ahi[mm][i], alo[mm][i]);
         }
 #pragma unroll 1
         for (int s = 0; s < kStages; ++s) {
@@ -370,29 +388,44 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             __syncthreads();
             const float *buf = cbuf + ((s == 1) ? (par ^ 1) : par) * kStageFloats;
             const float *Cb = buf + mp * kCodes * kVec;
-#pragma unroll 2
-            for (int i = 0; i < 8; ++i) {
-                const int c0 = (mq + 4 * i) * 8; // first code of this n-tile
+#pragma unroll 1
+            for (int nt = mq; nt < kCodes / 8; nt += kWpp) {
+                const int c0 = nt * 8; // first code of this n-tile
                 uint32_t bhi[2], blo[2];
                 split_tf32(Cb[(c0 + fg) * kVec + ft], bhi[0], blo[0]);
                 split_tf32(Cb[(c0 + fg) * kVec + ft + 4], bhi[1], blo[1]);
-                float dd[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_tf32(dd, alo, bhi);
-                mma_tf32(dd, ahi, blo);
-                mma_tf32(dd, ahi, bhi);
-                if (!valid) dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
-                // D rows are columns j, D columns are codes c: (fg, 2ft), (fg, 2ft+1), +8 rows
-                const int j = mm * 16 + fg, c = c0 + 2 * ft;
-                float *t0 = tab + (((size_t)s * kCodes + c) * 2 + mp) * kSegVec;
-                t0[j] = dd[0];
-                t0[2 * kSegVec + j] = dd[1];
-                t0[j + 8] = dd[2];
-                t0[2 * kSegVec + j + 8] = dd[3];
+                float dd[2][4];
+#pragma unroll
+                for (int mm = 0; mm < 2; ++mm) {
+                    dd[mm][0] = dd[mm][1] = dd[mm][2] = dd[mm][3] = 0.f;
+                    mma_tf32(dd[mm], alo[mm], bhi);
+                    mma_tf32(dd[mm], ahi[mm], blo);
+                    mma_tf32(dd[mm], ahi[mm], bhi);
+                }
+                // D rows are columns j, D columns are codes c.  Lane (fg, ft) holds, for
+                // code c0 + 2 ft + b, the columns fg, fg + 8, fg + 16, fg + 24 -- one
+                // 16-byte slot of the permuted column order; they move to lane
+                // 8 ft + fg and are stored as two 128-bit words.
+                float v[2][4];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    v[b][0] = __shfl_sync(0xffffffffu, dd[0][b], src);
+                    v[b][1] = __shfl_sync(0xffffffffu, dd[0][2 + b], src);
+                    v[b][2] = __shfl_sync(0xffffffffu, dd[1][b], src);
+                    v[b][3] = __shfl_sync(0xffffffffu, dd[1][2 + b], src);
+                }
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    if (!valid) v[b][0] = v[b][1] = v[b][2] = v[b][3] = 0.f;
+                    const int c = c0 + 2 * st_ft + b;
+                    float *t0 = tab + (((size_t)s * kCodes + c) * 2 + mp) * kSegVec + 4 * st_fg;
+                    *reinterpret_cast<float4 *>(t0) = make_float4(v[b][0], v[b][1], v[b][2], v[b][3]);
+                }
             }
             __syncthreads(); // buffer consumed: refill it
-            if (s == 0) issue_stage(cbuf + par * kStageFloats, p0, p1, 2);
-            else if (s == 1 && has_next) issue_stage(cbuf + (par ^ 1) * kStageFloats, n0, n1, 0);
-            else if (s == 2 && has_next) issue_stage(cbuf + par * kStageFloats, n0, n1, 1);
+            if (s == 0) issue_stage<kNT>(cbuf + par * kStageFloats, p0, p1, 2);
+            else if (s == 1 && has_next) issue_stage<kNT>(cbuf + (par ^ 1) * kStageFloats, n0, n1, 0);
+            else if (s == 2 && has_next) issue_stage<kNT>(cbuf + par * kStageFloats, n0, n1, 1);
         }
         par ^= 1;
         primed = has_next;
@@ -401,7 +434,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         const float *p0, *p1;
         unit_codebooks<kDown>(A, U, p0, p1);
         float4 *cbs = reinterpret_cast<float4 *>(smem);
-        for (int i = threadIdx.x; i < 2 * kCbFloats / 4; i += kThreads) {
+        for (int i = threadIdx.x; i < 2 * kCbFloats / 4; i += kNT) {
             const float *src = (i < kCbFloats / 4) ? p0 : p1;
             const int ii = i % (kCbFloats / 4);
             cbs[i] = __ldg(reinterpret_cast<const float4 *>(src) + ii);
@@ -427,7 +460,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         }
     };
     auto ahead = [&](int g) {
-        const int ga = g + kPrefetchRounds * kWarps;
+        const int ga = g + kPf * kNW;
         if (ga < U.g1) prefetch_group(U, ga, lane);
         else if (has_next) {
             const int gn = N.g0 + (ga - U.g1);
@@ -491,25 +524,25 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                 A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = v;
         }
     };
-    if constexpr (kCodePingPong) {
+    if constexpr (kPing) {
         uint4 wa[2][kStages], wb[2][kStages];
         int g = U.g0 + warp;
         if (g < U.g1) load(g, wa);
         while (g < U.g1) {
-            if (g + kWarps < U.g1) load(g + kWarps, wb);
+            if (g + kNW < U.g1) load(g + kNW, wb);
             ahead(g);
             consume(wa, g);
-            g += kWarps;
+            g += kNW;
             if (g >= U.g1) break;
-            if (g + kWarps < U.g1) load(g + kWarps, wa);
+            if (g + kNW < U.g1) load(g + kNW, wa);
             ahead(g);
             consume(wb, g);
-            g += kWarps;
+            g += kNW;
         }
     } else {
         // codes loaded at the top of each round (they are already on their way into
         // L2), leaving the registers to the lookups in flight
-        for (int g = U.g0 + warp; g < U.g1; g += kWarps) {
+        for (int g = U.g0 + warp; g < U.g1; g += kNW) {
             uint4 wa[2][kStages];
             load(g, wa);
             ahead(g);

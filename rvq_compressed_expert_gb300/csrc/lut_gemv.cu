@@ -34,8 +34,8 @@ using namespace lut;
 
 namespace {
 
-template <bool kDown, bool kRecon, bool kBf16>
-__global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
+template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf>
+__global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int n_slots = lut_slot_count(A);
     const int units = kDown ? n_slots * A.npair * A.nrb : n_slots * A.gu.nseg;
@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
         const Unit U = decode_unit<kDown>(A, u);
         const bool has_next = u + (int)gridDim.x < units;
         if (has_next) N = decode_unit<kDown>(A, u + gridDim.x);
-        run_unit<kDown, kRecon, kBf16>(A, U, has_next, N, par, primed, nullptr, 0, smem);
+        run_unit<kDown, kRecon, kBf16, kNT, kPing && !kRecon, kPf>(A, U, has_next, N, par, primed, nullptr, 0,
+                                                                   smem);
     }
     if constexpr (!kRecon) cp_async_wait<0>();
 }
@@ -54,8 +55,10 @@ __global__ void __launch_bounds__(kThreads, 1) lut_kernel(const LutArgs A) {
 // out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair],
 // slots in rank order and pairs in order.  NP = number of pairs (0: any, read in a loop):
 // with NP fixed every partial of a batch of 16 slots is loaded before any is summed.
+constexpr int kCombineThreads = 64; // small CTAs: the partial loads spread over more SMs
+
 template <int NP>
-__global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ part_dn,
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ part_dn,
                                                       const int32_t *__restrict__ idx,
                                                       const float *__restrict__ gate,
                                                       const float *__restrict__ h,
@@ -122,19 +125,28 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
     else out[o] = h[o] + y;
 }
 
-template <bool kDown, bool kRecon, bool kBf16>
-cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
+template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf>
+cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
     const size_t smem = unit_smem<kRecon>();
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(lut_kernel<kDown, kRecon, kBf16>,
+        cudaError_t e = cudaFuncSetAttribute(lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const int grid = units < num_sms ? units : num_sms;
-    lut_kernel<kDown, kRecon, kBf16><<<grid, kThreads, smem, s>>>(A);
+    lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf><<<grid, kNT, smem, s>>>(A);
     return cudaGetLastError();
+}
+
+// The per-phase lookup kernels: 512 threads, codes loaded at the top of each round with
+// the L2 asked for them three rounds ahead.  (Measured on GB300: 384 threads with the
+// next round's codes double-buffered in registers, or a longer prefetch distance, were
+// slower -- the kernel is bound by the shared-memory pipe, not by load latency.)
+template <bool kDown, bool kRecon, bool kBf16>
+cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
+    return launch_v<kDown, kRecon, kBf16, kThreads, false, kPrefetchRounds>(A, units, num_sms, s);
 }
 
 template <bool kDown>
@@ -207,12 +219,12 @@ cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h
                            const uint8_t *one_part, cudaStream_t s) {
     const int npair = (L.dn.nseg + 1) / 2;
     const unsigned long long slots = (unsigned long long)T * L.k;
-    dim3 grid((L.d + 127) / 128, T);
+    dim3 grid((L.d + kCombineThreads - 1) / kCombineThreads, T);
     const float *h32 = reinterpret_cast<const float *>(h);
     switch (npair) {
 #define WM_COMBINE(NP)                                                                              \
-    combine_kernel<NP><<<grid, 128, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, npair,  \
-                                            mode, W.stats, slots, one_part)
+    combine_kernel<NP><<<grid, kCombineThreads, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, npair, \
+                                                        mode, W.stats, slots, one_part)
     case 1: WM_COMBINE(1); break;
     case 2: WM_COMBINE(2); break;
     case 3: WM_COMBINE(3); break;

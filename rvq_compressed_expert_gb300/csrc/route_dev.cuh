@@ -336,6 +336,68 @@ __device__ __forceinline__ uint32_t float_key(float x) {
 // Top-k and softmax of token t by a whole CTA: a bitonic sort of the E experts on the key
 // (logit hi, then lo, descending; index ascending), then warp 0 forms the gates exactly
 // as topk_warp does.  keys/ids: shared scratch of >= next_pow2(E) entries each.
+// A routing candidate: 64-bit key (total-order image of the logit, then of its
+// remainder) and the expert index; a comes before b in the selection order when its key
+// is larger, or equal with a lower index.
+struct Cand {
+    unsigned long long key;
+    int id;
+};
+__device__ __forceinline__ bool cand_before(const Cand &a, const Cand &b) {
+    return a.key > b.key || (a.key == b.key && a.id < b.id);
+}
+__device__ __forceinline__ Cand shfl_cand(const Cand &c, int src) {
+    Cand o;
+    o.key = __shfl_sync(0xffffffffu, c.key, src);
+    o.id = __shfl_sync(0xffffffffu, c.id, src);
+    return o;
+}
+// One compare-exchange step of a bitonic network across the warp: lanes l and l ^ stride
+// meet; the lower lane keeps the earlier candidate when `first_low`, else the later one.
+__device__ __forceinline__ void bitonic_step(Cand &v, int stride, bool first_low) {
+    const int lane = threadIdx.x & 31;
+    const Cand o = shfl_cand(v, lane ^ stride);
+    const bool low = (lane & stride) == 0;
+    const bool o_first = cand_before(o, v);
+    if (low == first_low ? o_first : !o_first) v = o;
+}
+// Sort the warp's 32 candidates into selection order (lane 0 first).
+__device__ __forceinline__ void warp_sort32(Cand &v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+            bitonic_step(v, stride, size == 32 || (lane & size) == 0);
+}
+// a and b in selection order (one per lane): returns the first 32 of their union, in order.
+__device__ __forceinline__ Cand warp_merge32(const Cand &a, const Cand &b) {
+    const int lane = threadIdx.x & 31;
+    const Cand rb = shfl_cand(b, 31 - lane); // b reversed: a then rb is bitonic
+    Cand v = cand_before(rb, a) ? rb : a;    // the 32 first of the 64 (itself bitonic)
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) bitonic_step(v, stride, true);
+    return v;
+}
+
+__device__ __forceinline__ Cand load_cand(const float *lrow, const float *lo_row, int E, int i) {
+    Cand c;
+    c.key = 0ull; // below every real logit (-inf maps above 0)
+    c.id = 0x7fffffff;
+    if (i < E) {
+        float a = lrow[i], b = lo_row ? lo_row[i] : 0.f;
+        if (a != a) a = -INFINITY;
+        if (a == 0.f) a = 0.f;
+        if (b != b || b == 0.f) b = 0.f;
+        c.key = ((unsigned long long)float_key(a) << 32) | float_key(b);
+        c.id = i;
+    }
+    return c;
+}
+
+// Top-k (k <= 32) of one token's logits by the whole CTA: each warp keeps the first 32
+// candidates of its 32-wide chunks (sort a chunk, merge), then the warps' lists are merged
+// pairwise through shared memory.  keys / ids: scratch of 32 entries per warp.
 __device__ __forceinline__ void topk_block(const float *__restrict__ logits,
                                            const float *__restrict__ logits_lo, int E, int k, int t,
                                            int32_t *__restrict__ idx, float *__restrict__ gate,
@@ -344,43 +406,34 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits,
                                            unsigned long long *__restrict__ stats,
                                            unsigned long long router_bytes,
                                            unsigned long long *keys, int *ids) {
-    int N = 1;
-    while (N < E) N <<= 1;
     const float *lrow = logits + (size_t)t * E;
-    for (int i = threadIdx.x; i < N; i += blockDim.x) {
-        unsigned long long key = 0ull; // below every real logit (-inf maps above 0)
-        if (i < E) {
-            float a = lrow[i], b = logits_lo ? logits_lo[(size_t)t * E + i] : 0.f;
-            if (a != a) a = -INFINITY;
-            if (a == 0.f) a = 0.f;
-            if (b != b || b == 0.f) b = 0.f;
-            key = ((unsigned long long)float_key(a) << 32) | float_key(b);
+    const float *lo_row = logits_lo ? logits_lo + (size_t)t * E : nullptr;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    Cand best;
+    best.key = 0ull;
+    best.id = 0x7fffffff;
+    for (int c0 = warp * 32; c0 < E; c0 += nw * 32) {
+        Cand v = load_cand(lrow, lo_row, E, c0 + lane);
+        warp_sort32(v);
+        best = warp_merge32(best, v);
+    }
+    keys[warp * 32 + lane] = best.key;
+    ids[warp * 32 + lane] = best.id;
+    for (int span = 1; span < nw; span <<= 1) {
+        __syncthreads();
+        if ((warp % (2 * span)) == 0 && warp + span < nw) {
+            Cand a, b;
+            a.key = keys[warp * 32 + lane];
+            a.id = ids[warp * 32 + lane];
+            b.key = keys[(warp + span) * 32 + lane];
+            b.id = ids[(warp + span) * 32 + lane];
+            const Cand m = warp_merge32(a, b);
+            __syncwarp();
+            keys[warp * 32 + lane] = m.key;
+            ids[warp * 32 + lane] = m.id;
         }
-        keys[i] = key;
-        ids[i] = i;
     }
     __syncthreads();
-    for (int size = 2; size <= N; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < N; i += blockDim.x) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const unsigned long long ki = keys[i], kj = keys[j];
-                    const int ii = ids[i], ij = ids[j];
-                    // "i before j" in the final (descending) order
-                    const bool i_first = ki > kj || (ki == kj && ii < ij);
-                    const bool desc = (i & size) == 0;
-                    if (desc != i_first) {
-                        keys[i] = kj;
-                        keys[j] = ki;
-                        ids[i] = ij;
-                        ids[j] = ii;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         int my_idx = -1;

@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(512) router_staged_kernel(const float *__restr
                                hs_tokens);
 }
 
-// Top-k of one token per CTA of 512 threads: bitonic sort of the keys in shared memory
-// (same selection and gates as the step kernel's top-k item).
+// Top-k of one token per CTA of 512 threads: per-warp sorted candidate lists merged in a
+// tree (same selection and gates as the step kernel's top-k item).
 __global__ void __launch_bounds__(512) topk_cta_kernel(const float *__restrict__ logits,
                                                        const float *__restrict__ logits_lo, int E,
                                                        int k, int32_t *__restrict__ idx,
@@ -200,10 +200,8 @@ __global__ void __launch_bounds__(512) topk_cta_kernel(const float *__restrict__
                                                        unsigned long long *__restrict__ stats,
                                                        unsigned long long router_bytes) {
     extern __shared__ unsigned long long keys_dyn[];
-    int N = 1;
-    while (N < E) N <<= 1;
     topk_block(logits, logits_lo, E, k, blockIdx.x, idx, gate, pred_idx, pred_count, pred_stride,
-               stats, router_bytes, keys_dyn, reinterpret_cast<int *>(keys_dyn + N));
+               stats, router_bytes, keys_dyn, reinterpret_cast<int *>(keys_dyn + 512));
 }
 
 // One warp per token.
@@ -339,17 +337,9 @@ cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int 
                         int32_t *idx, float *gate, const int32_t *pred_idx, int32_t *pred_count,
                         int pred_stride, unsigned long long *stats,
                         unsigned long long router_bytes, cudaStream_t s) {
-    int N = 1;
-    while (N < E) N <<= 1;
-    const size_t smem = (size_t)N * 12;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(topk_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)kMaxExperts * 12));
-        attr_set = true;
-    }
-    topk_cta_kernel<<<T, 512, smem, s>>>(logits, logits_lo, E, k, idx, gate, pred_idx, pred_count,
-                                         pred_stride, stats, router_bytes);
+    // scratch of the warp top-k: 32 candidates (8-byte key, 4-byte index) per warp
+    topk_cta_kernel<<<T, 512, 512 * 12, s>>>(logits, logits_lo, E, k, idx, gate, pred_idx, pred_count,
+                                             pred_stride, stats, router_bytes);
     return cudaGetLastError();
 }
 
