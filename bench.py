@@ -698,10 +698,40 @@ def profile_case(args):
         layer.step(h, w.tokens, idx, gate, y, 0, logits)
         if trace is not None and i >= args.warmup:
             torch.cuda.synchronize()
-            print_trace(trace.view(-1, 4).cpu(), w)
+            if args.phases:
+                print_unit_trace(trace.view(-1, 4).cpu(), w)
+            else:
+                print_trace(trace.view(-1, 4).cpu(), w)
     torch.cuda.synchronize()
     layer.close()
     print("profile case done")
+
+
+def print_unit_trace(tr, w):
+    """Per-phase summary of the lookup kernels' unit trace: table build and row streaming."""
+    import math as _m
+    slots = w.tokens * w.top_k
+    n_gu = slots * _m.ceil(w.d / 8 / 32)
+    rows = tr.tolist()
+    out = []
+    for name, a, b in (("gate_up", 0, n_gu), ("down", n_gu, len(rows))):
+        its = [r for r in rows[a:b] if r[2] > 0]
+        if not its:
+            continue
+        t0 = min(r[0] for r in its)
+        tab = [(r[1] - r[0]) / 1e3 for r in its]
+        run = [(r[2] - r[1]) / 1e3 for r in its]
+        wait = [(r[3] >> 32) / 1e3 for r in its]
+        span = (max(r[2] for r in its) - t0) / 1e3
+        per_sm = {}
+        for r in its:
+            per_sm.setdefault(r[3] & 0xffffffff, []).append(r)
+        busy = [sum((x[2] - x[0]) for x in v) / 1e3 for v in per_sm.values()]
+        out.append(f"{name}: units={len(its)} span {span:.1f} us; to barrier mean {sum(wait)/len(wait):.2f}; "
+                   f"tables mean {sum(tab)/len(tab):.2f} "
+                   f"max {max(tab):.2f}; rows mean {sum(run)/len(run):.2f} max {max(run):.2f}; "
+                   f"SM busy mean {sum(busy)/len(busy):.1f} max {max(busy):.1f} us over {len(per_sm)} SMs")
+    print(" | ".join(out))
 
 
 def print_trace(tr, w):

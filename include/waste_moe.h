@@ -225,11 +225,14 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
 int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
                    float *d_logits, float *d_out, int32_t mode, waste_stream_t stream);
 
-/* Trace the work items of the persistent step kernel into d_trace: item i (in queue
- * order: router items, the top-k item, gate/up units, down units, combine items) writes
- * {start, end} (%globaltimer, ns), the SM id and the CTA index as 4 uint64 at
- * d_trace[4 i].  n_items = capacity in items; 0 (or d_trace NULL with 0) turns it off.
- * The buffer is the caller's and must outlive the traced calls. */
+/* Trace work items into d_trace (4 uint64 per item, %globaltimer in ns).
+ * Persistent step kernel: item i in queue order (router items, the top-k item, gate/up
+ * units, down units, combine items) writes {start, end, SM id, CTA index}.
+ * Per-phase kernels: lookup unit i (gate/up units, then down units) writes
+ * {start, tables built, end, SM id | (ns from start to the barrier before the table
+ * build) << 32}.
+ * n_items = capacity in items; 0 (or d_trace NULL with 0) turns it off.  The buffer is the
+ * caller's and must outlive the traced calls. */
 int waste_moe_set_trace(waste_moe *h, uint64_t *d_trace, int32_t n_items);
 
 /* Lookahead: run next_layer's router on the current hidden states d_h [T][d],

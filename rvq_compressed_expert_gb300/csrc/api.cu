@@ -454,7 +454,7 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
         }
     } else {
         e = launch_lut_forward(h->L, h->W, d_h, T, d_idx, d_gate, d_out, mode, recon, h->num_sms, s,
-                               h->profiling ? &h->fwd_tm : nullptr);
+                               h->profiling ? &h->fwd_tm : nullptr, h->trace, h->trace_cap);
         if (h->profiling) h->step_tm.n = 0;
     }
     if (e != cudaSuccess) return cuda_fail(e, "expert kernels");

@@ -94,7 +94,7 @@ struct Workspace {
     int32_t *pred_idx_sel; // scratch for prefetch top-k
     float *pred_gate_sel;  // scratch (unused gates of the prediction)
     float *part_gu;      // [max_slots][gu.nseg][2][f]
-    float *part_dn;      // [max_slots][npair][d]
+    float *part_dn;      // [max_slots][(dn.nseg + 1) / 2][d]; tensor-core slots use part 0
     unsigned long long *stats; // [kStatCount]
     uint32_t *err;       // sticky error bits
     unsigned *sync;      // fused-step queue and counters [4 + max_slots + kMaxFusedRowBlocks], zero at rest
@@ -121,9 +121,13 @@ struct Timing {
     cudaEvent_t ev[8];
     int n;
 };
+// trace (optional): per-unit trace of the two lookup kernels, trace_cap units.
 cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
                                const int32_t *idx, const float *gate, float *out, int mode,
-                               bool reconstruct, int num_sms, cudaStream_t s, Timing *tm);
+                               bool reconstruct, int num_sms, cudaStream_t s, Timing *tm,
+                               unsigned long long *trace = nullptr, int trace_cap = 0);
+// Down partials per slot written by the lookup kernels (one per pair of segments).
+inline int down_parts(const LayerView &L) { return (L.dn.nseg + 1) / 2; }
 // One lookup phase (gate/up or down) over the slots listed on the device.
 cudaError_t launch_lut_listed(const LayerView &L, const Workspace &W, const void *h, int T,
                               const int32_t *idx, const int32_t *slot_list, const int32_t *n_list,
@@ -132,7 +136,7 @@ cudaError_t launch_lut_listed(const LayerView &L, const Workspace &W, const void
 // marks slots whose output is partial 0 alone.
 cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h, int T,
                            const int32_t *idx, const float *gate, float *out, int mode,
-                           const uint8_t *one_part, cudaStream_t s);
+                           const uint8_t *one_part, int nparts, cudaStream_t s);
 // Tokens per chunk of the grouped tensor-core path.
 constexpr int kGroupTokens = 128;
 // Default tokens an expert needs in one call to take the tensor-core path.

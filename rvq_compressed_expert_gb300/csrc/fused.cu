@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             const bool has_next = nxt >= b_gu(F) && nxt < b_dn(F);
             Unit N;
             if (has_next) N = decode_unit<false>(F.A, nxt - b_gu(F));
-            run_unit<false, kRecon, kBf16>(F.A, U, has_next, N, par, primed, nullptr, 0, smem);
+            run_unit<false, kRecon, kBf16>(F.A, U, has_next, N, par, primed, nullptr, 0);
             signal(gu_done(F) + U.slot);
         } else if (cur < b_comb(F)) {
             // ---- down unit (waits inside for the gate/up units of its slot)
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             Unit N;
             if (has_next) N = decode_unit<true>(F.A, nxt - b_dn(F));
             run_unit<true, kRecon, kBf16>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot,
-                                          (unsigned)F.A.gu.nseg, smem);
+                                          (unsigned)F.A.gu.nseg);
             signal(dn_done(F) + (u % F.A.nrb));
         } else {
             // ---- combine rows [r0, r1) once every down unit over them is done
@@ -291,6 +291,9 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
     A.err = W.err;
     A.slot_list = nullptr;
     A.n_list = nullptr;
+    A.trace = nullptr;
+    A.trace_cap = 0;
+    A.trace_base = 0;
     F.router_w = L.router_w;
     F.router_b = L.router_b;
     F.logits = logits;

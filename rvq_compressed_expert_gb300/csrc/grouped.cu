@@ -269,13 +269,13 @@ struct MmaArgs {
     size_t sec[3];
     const float *codebooks;
     MatGeom geom; // the matrix of this kernel (gate/up: f x d, down: d x f)
-    int d, f, k, npair;
+    int d, f, k, nparts;
     const int32_t *sorted;
     const int4 *chunks;
     const int32_t *counts;
     const uint8_t *bsrc; // tiled fp16 activations the MMAs read (xg or ag)
     uint8_t *ag;         // gate/up output tiles (down input)
-    float *part_dn;      // [S][npair][d]
+    float *part_dn;      // [S][nparts][d]
     unsigned long long *stats;
     uint32_t *err;
 };
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                         if (row < G.n_out) {
 #pragma unroll
                             for (int n = 0; n < 16; ++n)
-                                if (c0 + n < nt) A.part_dn[(size_t)s_slot[c0 + n] * A.npair * A.d + row] = z[n];
+                                if (c0 + n < nt) A.part_dn[(size_t)s_slot[c0 + n] * A.nparts * A.d + row] = z[n];
                         }
                     }
                 }
@@ -604,7 +604,7 @@ cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const
     A.d = L.d;
     A.f = L.f;
     A.k = L.k;
-    A.npair = (L.dn.nseg + 1) / 2;
+    A.nparts = down_parts(L);
     A.sorted = G.sorted;
     A.chunks = G.chunks;
     A.counts = G.counts;
@@ -629,7 +629,7 @@ cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const
     e = launch_mma<true>(A, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[2], s);
-    e = launch_combine(L, W, h, T, idx, gate, out, mode, G.one_part, s);
+    e = launch_combine(L, W, h, T, idx, gate, out, mode, G.one_part, A.nparts, s);
     if (e != cudaSuccess) return e;
     if (tm) {
         cudaEventRecord(tm->ev[3], s);

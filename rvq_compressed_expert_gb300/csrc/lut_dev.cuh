@@ -16,7 +16,7 @@ constexpr int kXsFloats = 512;               // down input staging (64 vectors x
 constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
 constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' codebooks
 constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
-constexpr bool kCodePingPong = false;             // hold the next round's codes in registers
+constexpr bool kCodePingPong = false;            // hold the next round's codes in registers
 constexpr int kPrefetchRounds = 3;                 // L2 prefetch distance in row-group rounds
 
 struct LutArgs {
@@ -41,7 +41,18 @@ struct LutArgs {
     // T * k slots in order
     const int32_t *slot_list;
     const int32_t *n_list;
+    // optional unit trace of the per-phase kernels: unit u of this launch writes
+    // {start, tables built, end (%globaltimer ns), SM id | (ns from start to the barrier that
+    // frees the tables) << 32} at trace[4 (trace_base + u)]
+    unsigned long long *trace;
+    int trace_cap, trace_base;
 };
+
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 // Slots this launch serves.
 __device__ __forceinline__ int lut_slot_count(const LutArgs &A) {
@@ -70,6 +81,12 @@ __device__ __forceinline__ void load_x8(const void *h, size_t elem, float *xv) {
         xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
         xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
     }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ float load_x1(const void *h, size_t elem) {
+    if constexpr (kBf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(h)[elem]);
+    else return reinterpret_cast<const float *>(h)[elem];
 }
 
 __device__ __forceinline__ float dot8(const float *__restrict__ c, const float *xv) {
@@ -266,7 +283,7 @@ template <bool kDown, bool kRecon, bool kBf16, int kNT = kThreads, bool kPing = 
           int kPf = kPrefetchRounds>
 __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
                                       int &par, bool &primed, const unsigned *dep,
-                                      unsigned dep_target, unsigned char *) {
+                                      unsigned dep_target, unsigned long long *t_tables = nullptr) {
     constexpr int kNW = kNT / 32;
     static_assert(kNT % 128 == 0 && kNT <= 512, "CTA size of the lookup units");
     // the dynamic shared memory named directly, so every access compiles to a shared one
@@ -275,28 +292,30 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     const Unit U = Uin;
     Unit N = Uin;
     if (has_next) N = Nin;
-    float *cbuf = reinterpret_cast<float *>(smem + kTabBytes);
-    float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kTabBytes + 2 * kStageBuf));
+    float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kTabBytes));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b4 = lane >> 4;
     const MatGeom &G = kDown ? A.dn : A.gu;
-    // table column byte offset of register-part p: part (p ^ b4), the slot of column
-    // `lane` in the permuted column order of the tables
-    const uint32_t colb0 = ((uint32_t)(0 ^ b4) << 7) | ((uint32_t)tab_col(lane) << 2);
-    const uint32_t colb1 = ((uint32_t)(1 ^ b4) << 7) | ((uint32_t)tab_col(lane) << 2);
+    // table column byte offset of part p: the slot of column `lane` in the permuted column
+    // order of the tables
+    const uint32_t colb0 = (0u << 7) | ((uint32_t)tab_col(lane) << 2);
+    const uint32_t colb1 = (1u << 7) | ((uint32_t)tab_col(lane) << 2);
     const bool valid = U.base[0] != nullptr;
-    if (!kRecon && !primed) {
-        const float *q0, *q1;
-        unit_codebooks<kDown>(A, U, q0, q1);
-        issue_stage<kNT>(cbuf + par * kStageFloats, q0, q1, 0);
-        issue_stage<kNT>(cbuf + (par ^ 1) * kStageFloats, q0, q1, 1);
-    }
     // warm L2 with the first rounds of row groups this warp streams (the tail of the
-    // previous unit already asked for them, except on a CTA's first unit)
+    // previous unit already asked for them, except on a CTA's first unit), and with the
+    // codebooks of the next unit, which its table build reads straight from global memory
 #pragma unroll 1
     for (int i = 0; i < kPf; ++i) {
         const int g = U.g0 + warp + i * kNW;
         if (g < U.g1) prefetch_group(U, g, lane);
+    }
+    if (!kRecon && has_next) {
+        const float *q0, *q1;
+        unit_codebooks<kDown>(A, N, q0, q1);
+        constexpr int kLines = kCbFloats / 32; // 128-byte lines of one part's codebooks
+        for (int i = threadIdx.x; i < (kDown ? 1 : 2) * kLines; i += kNT) {
+            const float *q = (i < kLines ? q0 : q1) + (size_t)(i % kLines) * 32;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+        }
     }
     if (!valid && threadIdx.x == 0) atomicOr(A.err, kErrBadExpert);
     const int t = U.slot / A.k;
@@ -312,19 +331,31 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
 #pragma unroll
         for (int v = 0; v < kVec; ++v) xv[1][v] = xv[0][v];
     } else {
-        // a = silu(gate) * up for the 64 vectors of this unit, reduced over the
-        // gate/up segments in a fixed order
+        // a = silu(gate) * up for the 64 vectors of this unit, reduced over the gate/up
+        // segments in a fixed order (the loads of 32 segments in flight at a time)
         __syncthreads(); // xs may still be read by the previous unit
         if (dep) wait_counter(dep, dep_target, A.err);
         for (int i = threadIdx.x; i < 2 * kSegVec * kVec; i += kNT) {
             const int r = U.seg0 * kSegVec * kVec + i; // index into f
             float a = 0.f;
             if (valid && r < A.gu.n_out) {
-                const float *pg = A.part_gu + (size_t)U.slot * A.gu.nseg * 2 * A.gu.n_out;
+                const float *pg = A.part_gu + (size_t)U.slot * A.gu.nseg * 2 * A.gu.n_out + r;
+                const size_t step = (size_t)2 * A.gu.n_out;
                 float zg = 0.f, zu = 0.f;
-                for (int sg = 0; sg < A.gu.nseg; ++sg) {
-                    zg += pg[((size_t)sg * 2 + 0) * A.gu.n_out + r];
-                    zu += pg[((size_t)sg * 2 + 1) * A.gu.n_out + r];
+                for (int s0 = 0; s0 < A.gu.nseg; s0 += 32) {
+                    float vg[32], vu[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int sg = min(s0 + q, A.gu.nseg - 1);
+                        vg[q] = pg[sg * step];
+                        vu[q] = pg[sg * step + A.gu.n_out];
+                    }
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        if (s0 + q < A.gu.nseg) {
+                            zg += vg[q];
+                            zu += vu[q];
+                        }
                 }
                 a = zg / (1.0f + expf(-zg)) * zu;
             }
@@ -336,64 +367,73 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
 #pragma unroll
             for (int v = 0; v < kVec; ++v) xv[p][v] = xs[p * kSegVec * kVec + lane * kVec + v];
     }
-    // x of register-part p (column p ^ b4), for the reconstruct variant
-    float xr[2][kVec];
-#pragma unroll
-    for (int p = 0; p < 2; ++p)
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) xr[p][v] = b4 ? xv[p ^ 1][v] : xv[p][v];
-    if constexpr (!kDown && !kRecon) {
-        // the table build reads the column vectors X[part][j][v] from xs (both parts of a
-        // gate/up unit share x)
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) {
-            xs[lane * kVec + v] = xv[0][v];
-            xs[kSegVec * kVec + lane * kVec + v] = xv[0][v];
-        }
-    }
-    __syncthreads(); // previous unit's lookups are done with the tables; xs is complete
     if constexpr (!kRecon) {
-        // ---- tables T[s][c][part][lane], one stage at a time from the staged codebooks;
-        // the cp.async groups in flight are always the next two stage loads.
-        // Per stage and part the table is the product T[j][c] = sum_v X[j][v] C[c][v]
-        // (32 columns j x 256 codes c, K = 8), taken on the tensor cores as
-        // m16n8k8 TF32 MMAs with each operand split into a TF32 head and tail
-        // (tail*head + head*tail + head*head), which keeps fp32 accuracy.  The warps form
-        // 2 teams of kNW / 2, one per part; a warp takes both 16-row halves (all 32
-        // columns j) of a code tile, and its team's 32 code tiles in turn.
+        // ---- tables T[s][c][part][column], one 64 KiB block per stage.  Per stage and part
+        // the table is the product T[j][c] = sum_v X[j][v] C[c][v] (32 columns j x 256
+        // codes c, K = 8), taken on the tensor cores as m16n8k8 TF32 MMAs with each operand
+        // split into a TF32 head and tail (tail*head + head*tail + head*head), which keeps
+        // fp32 accuracy.  The warps form 2 teams of kNW / 2, one per part; a warp takes
+        // both 16-row halves (all 32 columns j) of a code tile, and its team's 32 code tiles
+        // in turn.  Its operands come straight from global memory (L2), all in flight at
+        // once, before the barrier that frees the tables.
         float *tab = reinterpret_cast<float *>(smem);
-        const float *p0, *p1, *n0 = nullptr, *n1 = nullptr;
-        unit_codebooks<kDown>(A, U, p0, p1);
-        if (has_next) unit_codebooks<kDown>(A, N, n0, n1);
-        constexpr int kWpp = kNW / 2; // warps per part
+        constexpr int kWpp = kNW / 2;                       // warps per part
+        constexpr int kTiles = (kCodes / 8 + kWpp - 1) / kWpp; // code tiles per warp
         const int mp = warp / kWpp, mq = warp % kWpp;
         const int fg = lane >> 2, ft = lane & 3;
+        const float *p0, *p1;
+        unit_codebooks<kDown>(A, U, p0, p1);
+        const float *Cp = mp ? p1 : p0;
+        float bv[kStages][kTiles][2];
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+#pragma unroll
+            for (int i = 0; i < kTiles; ++i) {
+                const int nt = mq + i * kWpp;
+                const float *c = Cp + ((size_t)s * kCodes + (size_t)min(nt, kCodes / 8 - 1) * 8 + fg) * kVec;
+                bv[s][i][0] = __ldg(c + ft);
+                bv[s][i][1] = __ldg(c + ft + 4);
+            }
+        // A operand: column j = fg + 8 k of part mp (k = 0..3), inputs ft and ft + 4
+        float av[2][4];
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int j = mm * 16 + fg + 8 * h2;
+                if constexpr (!kDown) {
+                    const int jg = U.seg0 * kSegVec + j;
+                    const bool in = jg < G.nv;
+                    const size_t e0 = (size_t)t * A.gu.n_in + (size_t)min(jg, G.nv - 1) * kVec;
+                    av[mm][h2] = in ? load_x1<kBf16>(A.h, e0 + ft) : 0.f;
+                    av[mm][2 + h2] = in ? load_x1<kBf16>(A.h, e0 + ft + 4) : 0.f;
+                } else {
+                    const float *X = xs + mp * kSegVec * kVec + j * kVec;
+                    av[mm][h2] = X[ft];
+                    av[mm][2 + h2] = X[ft + 4];
+                }
+            }
+        __syncthreads(); // the previous unit's lookups are done with the tables
+        if (t_tables && threadIdx.x == 0) t_tables[1] = gtimer();
+        uint32_t ahi[2][4], alo[2][4];
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) split_tf32(av[mm][i], ahi[mm][i], alo[mm][i]);
         // the lane whose results this lane stores: quarter-warp q stores code pair q of the
         // tile for the 8 row groups fg, so its 8 lanes hit 8 different bank quads
         const int src = ((lane & 7) << 2) | (lane >> 3);
         const int st_fg = lane & 7, st_ft = lane >> 3;
-        uint32_t ahi[2][4], alo[2][4];
 #pragma unroll
-        for (int mm = 0; mm < 2; ++mm) {
-            const float *X = xs + mp * kSegVec * kVec + (mm * 16) * kVec;
-            const float av[4] = {X[fg * kVec + ft], X[(fg + 8) * kVec + ft], X[fg * kVec + ft + 4],
-                                 X[(fg + 8) * kVec + ft + 4]};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) split_tf32(av[i], ahi[mm][i], alo[mm][i]);
-        }
-#pragma unroll 1
         for (int s = 0; s < kStages; ++s) {
-            if (s < 2 || has_next) cp_async_wait<1>();
-            else cp_async_wait<0>();
-            __syncthreads();
-            const float *buf = cbuf + ((s == 1) ? (par ^ 1) : par) * kStageFloats;
-            const float *Cb = buf + mp * kCodes * kVec;
-#pragma unroll 1
-            for (int nt = mq; nt < kCodes / 8; nt += kWpp) {
+#pragma unroll
+            for (int i = 0; i < kTiles; ++i) {
+                const int nt = mq + i * kWpp;
+                if (nt >= kCodes / 8) break;
                 const int c0 = nt * 8; // first code of this n-tile
                 uint32_t bhi[2], blo[2];
-                split_tf32(Cb[(c0 + fg) * kVec + ft], bhi[0], blo[0]);
-                split_tf32(Cb[(c0 + fg) * kVec + ft + 4], bhi[1], blo[1]);
+                split_tf32(bv[s][i][0], bhi[0], blo[0]);
+                split_tf32(bv[s][i][1], bhi[1], blo[1]);
                 float dd[2][4];
 #pragma unroll
                 for (int mm = 0; mm < 2; ++mm) {
@@ -422,14 +462,10 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                     *reinterpret_cast<float4 *>(t0) = make_float4(v[b][0], v[b][1], v[b][2], v[b][3]);
                 }
             }
-            __syncthreads(); // buffer consumed: refill it
-            if (s == 0) issue_stage<kNT>(cbuf + par * kStageFloats, p0, p1, 2);
-            else if (s == 1 && has_next) issue_stage<kNT>(cbuf + (par ^ 1) * kStageFloats, n0, n1, 0);
-            else if (s == 2 && has_next) issue_stage<kNT>(cbuf + par * kStageFloats, n0, n1, 1);
         }
-        par ^= 1;
-        primed = has_next;
+        __syncthreads(); // tables complete
     } else {
+        __syncthreads(); // the previous unit's lookups are done with the codebook rows
         // ---- codebooks of both parts [2][3][256][8]
         const float *p0, *p1;
         unit_codebooks<kDown>(A, U, p0, p1);
@@ -441,13 +477,17 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         }
         __syncthreads();
     }
+    (void)par;
+    (void)primed;
+
+    if (t_tables && threadIdx.x == 0) t_tables[0] = gtimer();
 
     // ---- stream the codes of rows [g0, g1) x this unit's segment(s).  Registers hold
     // the next row group's codes while the current one is consumed (ping-pong), and L2
     // is asked for the row group kPrefetchRounds rounds ahead -- past the end of the
     // unit, for the next unit's first row groups.
-    const uint8_t *pb0 = b4 ? U.base[1] : U.base[0];
-    const uint8_t *pb1 = b4 ? U.base[0] : U.base[1];
+    const uint8_t *pb0 = U.base[0];
+    const uint8_t *pb1 = U.base[1];
     // 32-bit shared-window address of the tables: a lookup is PRMT, IADD and one
     // ld.shared with the stage offset as its immediate
     const uint32_t tab32 = (uint32_t)__cvta_generic_to_shared(smem);
@@ -467,8 +507,20 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             if (gn < N.g1) prefetch_group(N, gn, lane);
         }
     };
+    // Row group g: lane l holds, for each code byte q of its 16-byte chunks, the partial
+    // dot product of row 16 g + ((l ^ q) & 15) over its vector column.  Gate and up go one
+    // part at a time (16 partials, then a reduce-scatter over the 32 columns); the two down
+    // segments add into the same rows before a single reduce-scatter.
+    auto reduce16 = [&](float (&acc)[16]) {
+#pragma unroll
+        for (int n = 8; n >= 1; n >>= 1)
+#pragma unroll
+            for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 16);
+    };
     auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
-        float acc[32];
+        const int row = g * kGroupRows + (lane & 15);
+        float acc[16];
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
             const uint32_t colb = p ? colb1 : colb0;
@@ -477,6 +529,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                 const uint32_t w0 = comp(cw[p][0], wd), w1 = comp(cw[p][1], wd), w2 = comp(cw[p][2], wd);
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
+                    float t;
                     if constexpr (!kRecon) {
                         const uint32_t sel = 0x7604u | ((uint32_t)b << 4);
                         const uint32_t a0 = __byte_perm(w0, colb, sel);
@@ -485,17 +538,16 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                         const float t0 = lds_stage<0>(tab32 + a0);
                         const float t1 = lds_stage<1>(tab32 + a1);
                         const float t2 = lds_stage<2>(tab32 + a2);
-                        acc[16 * p + 4 * wd + b] = (t0 + t1) + t2;
+                        t = (t0 + t1) + t2;
                     } else {
-                        const int part = p ^ b4;
-                        const float *cbs = reinterpret_cast<const float *>(smem) + part * kCbFloats;
+                        const float *cbs = reinterpret_cast<const float *>(smem) + p * kCbFloats;
                         const int c0 = (w0 >> (8 * b)) & 255, c1 = (w1 >> (8 * b)) & 255,
                                   c2 = (w2 >> (8 * b)) & 255;
                         const float4 *r0 = reinterpret_cast<const float4 *>(cbs + c0 * kVec);
                         const float4 *r1 = reinterpret_cast<const float4 *>(cbs + kCodes * kVec + c1 * kVec);
                         const float4 *r2 = reinterpret_cast<const float4 *>(cbs + 2 * kCodes * kVec + c2 * kVec);
                         const float4 a0 = r0[0], a1 = r0[1], b0 = r1[0], b1 = r1[1], d0 = r2[0], d1 = r2[1];
-                        const float *x = xr[p];
+                        const float *x = xv[p];
                         float sacc = ((a0.x + b0.x) + d0.x) * x[0];
                         sacc = fmaf((a0.y + b0.y) + d0.y, x[1], sacc);
                         sacc = fmaf((a0.z + b0.z) + d0.z, x[2], sacc);
@@ -504,24 +556,22 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                         sacc = fmaf((a1.y + b1.y) + d1.y, x[5], sacc);
                         sacc = fmaf((a1.z + b1.z) + d1.z, x[6], sacc);
                         sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
-                        acc[16 * p + 4 * wd + b] = sacc;
+                        t = sacc;
                     }
+                    if (kDown && p == 1) acc[4 * wd + b] += t;
+                    else acc[4 * wd + b] = t;
                 }
             }
+            if constexpr (!kDown) {
+                reduce16(acc);
+                if (lane < 16 && row < G.n_out)
+                    A.part_gu[(((size_t)U.slot * A.gu.nseg + U.seg0) * 2 + p) * G.n_out + row] = acc[0];
+            }
         }
-        // slot i of lane l holds row (l ^ i) of the 32 (part, row) pairs: reduce-scatter
-#pragma unroll
-        for (int n = 16; n >= 1; n >>= 1)
-#pragma unroll
-            for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
-        const int row = g * kGroupRows + (lane & 15);
-        if constexpr (!kDown) {
-            if (row < G.n_out)
-                A.part_gu[(((size_t)U.slot * A.gu.nseg + U.seg0) * 2 + b4) * G.n_out + row] = acc[0];
-        } else {
-            const float v = acc[0] + __shfl_xor_sync(0xffffffffu, acc[0], 16);
+        if constexpr (kDown) {
+            reduce16(acc);
             if (lane < 16 && row < G.n_out)
-                A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = v;
+                A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = acc[0];
         }
     };
     if constexpr (kPing) {
@@ -569,7 +619,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
 // Bytes of dynamic shared memory of a unit.
 template <bool kRecon>
 constexpr size_t unit_smem() {
-    return (kRecon ? 2 * kCbFloats * 4 : kTabBytes + 2 * kStageBuf) + kXsFloats * 4;
+    return (kRecon ? 2 * kCbFloats * 4 : kTabBytes) + kXsFloats * 4;
 }
 
 } // namespace lut

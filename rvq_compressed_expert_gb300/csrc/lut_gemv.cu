@@ -46,8 +46,19 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
         const Unit U = decode_unit<kDown>(A, u);
         const bool has_next = u + (int)gridDim.x < units;
         if (has_next) N = decode_unit<kDown>(A, u + gridDim.x);
+        unsigned long long t0 = 0, t_tab[2] = {0, 0};
+        if (A.trace && threadIdx.x == 0) t0 = gtimer();
         run_unit<kDown, kRecon, kBf16, kNT, kPing && !kRecon, kPf>(A, U, has_next, N, par, primed, nullptr, 0,
-                                                                   smem);
+                                                                   A.trace ? t_tab : nullptr);
+        if (A.trace && threadIdx.x == 0 && A.trace_base + u < A.trace_cap) {
+            unsigned smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            unsigned long long *e = A.trace + 4 * (size_t)(A.trace_base + u);
+            e[0] = t0;
+            e[1] = t_tab[0];
+            e[2] = gtimer();
+            e[3] = smid | ((t_tab[1] > t0 ? (t_tab[1] - t0) : 0ull) << 32);
+        }
     }
     if constexpr (!kRecon) cp_async_wait<0>();
 }
@@ -146,7 +157,7 @@ cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
 // slower -- the kernel is bound by the shared-memory pipe, not by load latency.)
 template <bool kDown, bool kRecon, bool kBf16>
 cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
-    return launch_v<kDown, kRecon, kBf16, kThreads, false, kPrefetchRounds>(A, units, num_sms, s);
+    return launch_v<kDown, kRecon, kBf16, kThreads, kCodePingPong, kPrefetchRounds>(A, units, num_sms, s);
 }
 
 template <bool kDown>
@@ -196,6 +207,9 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
     A.err = W.err;
     A.slot_list = nullptr;
     A.n_list = nullptr;
+    A.trace = nullptr;
+    A.trace_cap = 0;
+    A.trace_base = 0;
     return A;
 }
 
@@ -216,19 +230,22 @@ cudaError_t launch_lut_listed(const LayerView &L, const Workspace &W, const void
 
 cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h, int T,
                            const int32_t *idx, const float *gate, float *out, int mode,
-                           const uint8_t *one_part, cudaStream_t s) {
-    const int npair = (L.dn.nseg + 1) / 2;
+                           const uint8_t *one_part, int nparts, cudaStream_t s) {
     const unsigned long long slots = (unsigned long long)T * L.k;
     dim3 grid((L.d + kCombineThreads - 1) / kCombineThreads, T);
     const float *h32 = reinterpret_cast<const float *>(h);
-    switch (npair) {
-#define WM_COMBINE(NP)                                                                              \
-    combine_kernel<NP><<<grid, kCombineThreads, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, npair, \
+    switch (nparts) {
+#define WM_COMBINE(NP)                                                                               \
+    combine_kernel<NP><<<grid, kCombineThreads, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, nparts, \
                                                         mode, W.stats, slots, one_part)
     case 1: WM_COMBINE(1); break;
     case 2: WM_COMBINE(2); break;
     case 3: WM_COMBINE(3); break;
     case 4: WM_COMBINE(4); break;
+    case 5: WM_COMBINE(5); break;
+    case 6: WM_COMBINE(6); break;
+    case 7: WM_COMBINE(7); break;
+    case 8: WM_COMBINE(8); break;
     default: WM_COMBINE(0); break;
 #undef WM_COMBINE
     }
@@ -237,17 +254,21 @@ cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h
 
 cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
                                const int32_t *idx, const float *gate, float *out, int mode,
-                               bool reconstruct, int num_sms, cudaStream_t s, Timing *tm) {
-    const LutArgs A = make_lut_args(L, W, h, T, idx, num_sms);
+                               bool reconstruct, int num_sms, cudaStream_t s, Timing *tm,
+                               unsigned long long *trace, int trace_cap) {
+    LutArgs A = make_lut_args(L, W, h, T, idx, num_sms);
+    A.trace = trace;
+    A.trace_cap = trace ? trace_cap : 0;
     const bool bf16 = L.act_bf16 != 0;
     if (tm) cudaEventRecord(tm->ev[0], s);
     cudaError_t e = launch_lut_phase(A, false, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[1], s);
+    A.trace_base = A.slots * A.gu.nseg; // down units follow the gate/up units
     e = launch_lut_phase(A, true, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[2], s);
-    e = launch_combine(L, W, h, T, idx, gate, out, mode, nullptr, s);
+    e = launch_combine(L, W, h, T, idx, gate, out, mode, nullptr, down_parts(L), s);
     if (e != cudaSuccess) return e;
     if (tm) {
         cudaEventRecord(tm->ev[3], s);
