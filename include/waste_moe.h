@@ -162,8 +162,10 @@ int waste_moe_record_layout(const waste_moe_config *cfg, size_t *record_stride,
  *   d_gate_codes, d_up_codes: [n_experts][f][3][d/8] uint8,
  *   d_down_codes:             [n_experts][d][3][f/8] uint8  (device, read only).
  * d_records is the bank base (4096-aligned); record_stride as above.  Headers
- * carry `layer`; with compute_crc != 0 the payload crc32 is computed on the device
- * and stored (one small synchronous copy per record).  Enqueued on stream. */
+ * carry `layer`.  Enqueued on stream.  With compute_crc != 0 the payload crc32 of each
+ * record (IEEE 802.3 / zlib crc32 of the three sections in order) is computed on the
+ * device and stored in its header; the call then allocates a temporary device buffer
+ * (4 bytes per 4 KiB of payload) and waits for the stream. */
 int waste_moe_pack_records(const waste_moe_config *cfg, int32_t layer, int32_t expert_begin,
                            int32_t n_experts, const uint8_t *d_gate_codes,
                            const uint8_t *d_up_codes, const uint8_t *d_down_codes,
@@ -177,7 +179,10 @@ int waste_moe_pack_records(const waste_moe_config *cfg, int32_t layer, int32_t e
  *   d_codebooks   [E][3 matrices: gate, up, down][3 stages][256][8] fp32 (borrowed)
  * Checks every record header (magic, version, expert id, layer, shapes, section
  * offsets inside the stride and 4096-aligned, sizes) with one synchronous copy of
- * the headers, and the payload crc32 with WASTE_FLAG_VERIFY_CRC.  On any failure
+ * the headers.  With WASTE_FLAG_VERIFY_CRC it also recomputes every record's payload
+ * crc32 on the device (page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section
+ * "Architecture de streaming depuis le disque": crc32 behind --verify) and refuses a
+ * record whose header holds 0 or a different value (WASTE_ECRC).  On any failure
  * returns < 0 and sets *out = NULL (the layer is refused rather than run on
  * suspect weights).  Allocates the workspace (sized by max_tokens). */
 int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,

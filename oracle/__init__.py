@@ -60,6 +60,8 @@ def _bind(lib):
     lib.oracle_rmsnorm.argtypes = [_i, _dp, _dp]
     lib.oracle_expert_code_bytes.argtypes = [_i, _i]
     lib.oracle_expert_code_bytes.restype = ctypes.c_uint64
+    lib.oracle_crc32.argtypes = [_u8p, ctypes.c_size_t]
+    lib.oracle_crc32.restype = ctypes.c_uint32
     return lib
 
 
@@ -171,6 +173,16 @@ def combine(gate, ys, base=None):
                            None if b is None else _ptr(b, ctypes.c_double),
                            _ptr(out, ctypes.c_double))
     return out
+
+
+def crc32(data) -> int:
+    """crc32 (IEEE 802.3 / zlib) of a byte string, numpy uint8 array or uint8 tensor."""
+    if isinstance(data, (bytes, bytearray)):
+        a = np.frombuffer(bytes(data), np.uint8)
+    else:
+        a = _np(data, np.uint8).reshape(-1)
+    a = np.ascontiguousarray(a)
+    return int(_load().oracle_crc32(_ptr(a, ctypes.c_uint8), a.size))
 
 
 def rmsnorm(x):

@@ -256,3 +256,17 @@ void oracle_rmsnorm(int d, const double *in, double *out) {
 uint64_t oracle_expert_code_bytes(int d, int f) {
     return (uint64_t)3 * (uint64_t)OR_STAGES * (uint64_t)d * (uint64_t)f / OR_V;
 }
+
+/*
+ * crc32 of a byte string as the record check uses it ([fr] "Architecture de streaming
+ * depuis le disque": crc32 behind --verify): IEEE 802.3 / zlib -- reflected polynomial
+ * 0xEDB88320, register preset to all ones, result complemented -- one bit at a time.
+ */
+uint32_t oracle_crc32(const uint8_t *p, size_t n) {
+    uint32_t c = 0xFFFFFFFFu;
+    for (size_t i = 0; i < n; ++i) {
+        c ^= p[i];
+        for (int b = 0; b < 8; ++b) c = (c >> 1) ^ (0xEDB88320u & (0u - (c & 1u)));
+    }
+    return ~c;
+}

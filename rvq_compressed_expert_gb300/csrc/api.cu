@@ -3,6 +3,7 @@
 #include "common.cuh"
 
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -132,7 +133,6 @@ int waste_moe_pack_records(const waste_moe_config *cfg, int32_t layer, int32_t e
     layout(cfg, &st, off, by);
     if (record_stride < st || record_stride % WASTE_RECORD_ALIGN)
         return fail(WASTE_ELAYOUT, "record stride %zu: needs a multiple of 4096 >= %zu", record_stride, st);
-    if (compute_crc) return fail(WASTE_ENOTIMPL, "payload crc32 is not computed by this build");
     waste_record_header hdr;
     memset(&hdr, 0, sizeof hdr);
     hdr.magic = WASTE_RECORD_MAGIC;
@@ -156,6 +156,22 @@ int waste_moe_pack_records(const waste_moe_config *cfg, int32_t layer, int32_t e
     e = launch_pack(mat_geom(cfg->f, cfg->d), mat_geom(cfg->d, cfg->f), n_experts, d_gate_codes,
                     d_up_codes, d_down_codes, first, record_stride, off, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack kernel");
+    if (compute_crc) {
+        // payload crc32 into each header: a temporary device buffer, then a wait on the stream
+        const size_t payload = by[0] + by[1] + by[2];
+        uint32_t *scratch = nullptr;
+        const size_t words = crc_scratch_words(payload, n_experts);
+        e = cudaMalloc(&scratch, words * 4);
+        if (e != cudaSuccess) return cuda_fail(e, "crc scratch");
+        uint32_t *crc = scratch + (words - (size_t)n_experts);
+        e = launch_payload_crc(first, record_stride, n_experts, off[0], payload, scratch, crc, device_sm_count(), s);
+        if (e == cudaSuccess)
+            e = launch_crc_store(crc, first, record_stride, n_experts, offsetof(waste_record_header, payload_crc32),
+                                 s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        cudaFree(scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "payload crc32");
+    }
     return ok();
 }
 
@@ -177,8 +193,6 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     layout(cfg, &st, off, by);
     if (record_stride < st || record_stride % WASTE_RECORD_ALIGN)
         return fail(WASTE_ELAYOUT, "record stride %zu: needs a multiple of 4096 >= %zu", record_stride, st);
-    if (cfg->flags & WASTE_FLAG_VERIFY_CRC)
-        return fail(WASTE_ENOTIMPL, "payload crc32 verification is not in this build");
 
     // ---- record headers: one strided copy, then every field checked
     const int E = cfg->n_experts;
@@ -208,6 +222,31 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
                 return fail(WASTE_ELAYOUT, "record %d: section %d at %llu (+%llu) outside the record", e, m,
                             (unsigned long long)h.section_offset[m], (unsigned long long)h.section_bytes[m]);
         }
+    }
+
+    // ---- payload crc32 of every record against its header (WASTE_FLAG_VERIFY_CRC)
+    if (cfg->flags & WASTE_FLAG_VERIFY_CRC) {
+        for (int e = 0; e < E; ++e)
+            if (hdrs[(size_t)e].payload_crc32 == 0)
+                return fail(WASTE_ECRC, "record %d carries no payload crc32 (packed without one)", e);
+        const size_t payload = by[0] + by[1] + by[2];
+        const size_t words = crc_scratch_words(payload, E);
+        uint32_t *scratch = nullptr;
+        ce = cudaMalloc(&scratch, words * 4);
+        if (ce != cudaSuccess) {
+            cudaGetLastError();
+            return fail(WASTE_ENOMEM, "crc scratch of %zu bytes", words * 4);
+        }
+        uint32_t *crc = scratch + (words - (size_t)E);
+        std::vector<uint32_t> got((size_t)E);
+        ce = launch_payload_crc(d_records, record_stride, E, off[0], payload, scratch, crc, device_sm_count(), 0);
+        if (ce == cudaSuccess) ce = cudaMemcpy(got.data(), crc, (size_t)E * 4, cudaMemcpyDeviceToHost);
+        cudaFree(scratch);
+        if (ce != cudaSuccess) return cuda_fail(ce, "payload crc32");
+        for (int e = 0; e < E; ++e)
+            if (got[(size_t)e] != hdrs[(size_t)e].payload_crc32)
+                return fail(WASTE_ECRC, "record %d: payload crc32 0x%08x, header says 0x%08x", e, got[(size_t)e],
+                            hdrs[(size_t)e].payload_crc32);
     }
 
     waste_moe *H = new (std::nothrow) waste_moe();

@@ -171,6 +171,17 @@ cudaError_t launch_headers(uint8_t *records, size_t stride, int n, const waste_r
 
 cudaError_t launch_rmsnorm(const float *in, float *out, int T, int d, cudaStream_t s);
 
+// crc32 (IEEE 802.3 / zlib) of bytes [payload_off, payload_off + payload_bytes) of each of
+// n_records records into crc_out[n_records]; payload_bytes a multiple of 4096; scratch of
+// crc_scratch_words(payload_bytes, n_records) words.
+cudaError_t launch_payload_crc(const uint8_t *records, size_t stride, int n_records, size_t payload_off,
+                               size_t payload_bytes, uint32_t *scratch, uint32_t *crc_out, int num_sms,
+                               cudaStream_t s);
+size_t crc_scratch_words(size_t payload_bytes, int n_records);
+// crc[i] into the 32-bit field at field_off of record i.
+cudaError_t launch_crc_store(const uint32_t *crc, uint8_t *records, size_t stride, int n_records,
+                             size_t field_off, cudaStream_t s);
+
 int device_sm_count();
 
 

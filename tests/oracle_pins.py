@@ -286,4 +286,16 @@ def pin_rmsnorm():
     np.testing.assert_allclose(oracle.rmsnorm(4 * x), out, rtol=1e-7)
 
 
+def pin_crc32():
+    """crc32: the standard check value of "123456789" (0xCBF43926), the empty string, and
+    zlib's crc32 on random byte strings of several lengths."""
+    import zlib
+    assert oracle.crc32(b"123456789") == 0xCBF43926
+    assert oracle.crc32(b"") == 0
+    rng = np.random.default_rng(14)
+    for n in (1, 7, 4096, 10000):
+        a = rng.integers(0, 256, n, dtype=np.uint8)
+        assert oracle.crc32(a) == zlib.crc32(a.tobytes())
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -36,6 +36,8 @@ MUTANTS = {
     "rmsnorm_no_mean": ("double scale = 1.0 / sqrt(ss / (double)d + 1e-6);",
                         "double scale = 1.0 / sqrt(ss + 1e-6);"),
     "code_bytes_wrong": ("return (uint64_t)3 * (uint64_t)OR_STAGES", "return (uint64_t)2 * (uint64_t)OR_STAGES"),
+    "crc_not_complemented": ("    return ~c;\n}", "    return c;\n}"),
+    "crc_wrong_polynomial": ("(0xEDB88320u & (0u - (c & 1u)))", "(0x04C11DB7u & (0u - (c & 1u)))"),
 }
 
 
