@@ -174,7 +174,16 @@ def run_decode(args, dev, out):
     from rvq_compressed_expert_gb300.layer import MoELayer
 
     w = synth.WORKLOADS["decode"]
-    layer = MoELayer(w, seed=0, layer=0, device=dev)
+    layer = MoELayer(w, seed=0, layer=0, device=dev, crc=True)
+    # opening the layer with every record's payload crc32 checked on the device
+    vcfg = B.make_config(w.d, w.f, w.n_experts, w.top_k, w.act_dtype, 1, 0, B.FLAG_VERIFY_CRC, layer.layer)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    B.waste_moe_destroy(B.waste_moe_create(vcfg, layer.router_w, layer.router_b, layer.records, layer.stride,
+                                           layer.codebooks))
+    verify_s = time.perf_counter() - t0
+    out["verify_crc"] = dict(seconds=verify_s, bank_bytes=w.n_experts * layer.stride,
+                             gb_per_s=w.n_experts * layer.stride / verify_s / 1e9)
     pool = [synth.hidden(100 + i, 1, w.d, "f32", dev) for i in range(DECODE_POOL)]
     idx, gate, logits, y = layer.alloc_outputs(1)
     h_in = torch.empty(1, w.d, dtype=torch.float32, device=dev)
@@ -610,6 +619,8 @@ def native(args):
         "cpu_baseline": cpu,
         "stats_per_step": {k: v / args.steps for k, v in d["stats"].items()},
     }
+    if "verify_crc" in res:
+        line["config"]["create_with_crc_verify"] = res["verify_crc"]
     for extra in ("batched", "prefill", "stack"):
         if extra in res:
             line[extra] = res[extra]

@@ -17,7 +17,7 @@ class MoELayer:
     def __init__(self, w: synth.Workload, seed: int, layer: int = 0, device="cuda",
                  max_tokens: int | None = None, flags: int = 0, lookahead: int | None = None,
                  keep_codes: bool = False, pack_batch: int = 32, inputs: synth.LayerInputs | None = None,
-                 gen_device: str | None = None):
+                 gen_device: str | None = None, crc: bool = False):
         self.w = w
         self.seed = seed
         self.layer = layer
@@ -36,7 +36,7 @@ class MoELayer:
         if inputs is not None and inputs.codes is not None:
             self.codes = tuple(c.to(device).contiguous() for c in inputs.codes)
             B.waste_moe_pack_records(self.cfg, layer, 0, w.n_experts, *self.codes, self.records,
-                                     self.stride)
+                                     self.stride, int(crc))
             if not keep_codes:
                 self.codes = None
         else:
@@ -48,7 +48,7 @@ class MoELayer:
                 gc, uc, dc = (torch.stack([p[i] for p in parts]).to(device).contiguous()
                               for i in range(3))
                 B.waste_moe_pack_records(self.cfg, layer, e0, n, gc, uc, dc, self.records,
-                                         self.stride)
+                                         self.stride, int(crc))
                 if kept is not None:
                     kept.append((gc, uc, dc))
                 else:
