@@ -283,6 +283,54 @@ int waste_moe_set_profiling(waste_moe *h, int32_t enable);
  * call did not run that kernel.  Waits for the events. */
 int waste_moe_read_profile(const waste_moe *h, float ms[6]);
 
+/* ---- Tiered expert bank ---------------------------------------------------------
+ * Page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", sections "Budget RAM et zone de
+ * performance étroite" and "Lecture anticipée et prédiction du routeur": the experts live
+ * in a large slow tier, a bounded cache holds some of them, a miss reads the expert's
+ * record from the slow tier, and the next layer's router fills the cache ahead of demand.
+ * Here the slow tier is host memory (pinned, read by the GPU) and the cache is HBM.  The
+ * fetch runs on the device: a plan (hits refresh their slot; each miss takes the least
+ * recently used slot not used by the call in flight) and a copy of the missing records. */
+typedef struct waste_bank waste_bank;
+
+typedef struct {
+    uint64_t demand_hits;      /* (token, expert) slots whose expert was in the cache when its
+                                  layer ran (or brought in earlier in the same call) */
+    uint64_t demand_misses;    /* experts copied in on demand */
+    uint64_t prefetch_copies;  /* experts copied in by a lookahead */
+    uint64_t prefetch_present; /* predicted experts already in the cache */
+    uint64_t copied_bytes;     /* host -> HBM bytes (demand and lookahead) */
+} waste_bank_stats_t;
+
+/* n_layers x cfg->n_experts records (written by waste_moe_pack_records into device memory,
+ * then copied out) in host memory the device can read -- pinned (cudaHostAlloc,
+ * cudaMallocHost, cudaHostRegister), or any host memory on systems whose GPU addresses it
+ * directly; cudaHostGetDevicePointer decides (WASTE_EINVAL when it refuses): layer L's
+ * expert e at host_records + (L * n_experts + e) * record_stride, host_records 4096-aligned
+ * (WASTE_ELAYOUT).  n_slots records of HBM cache.  The records are borrowed; the cache is
+ * the bank's own. */
+int waste_bank_create(const waste_moe_config *cfg, int32_t n_layers, const uint8_t *host_records,
+                      size_t record_stride, int32_t n_slots, waste_bank **out);
+void waste_bank_destroy(waste_bank *bank);
+/* Empty the cache and zero the counters (synchronous). */
+int waste_bank_reset(waste_bank *bank);
+int waste_bank_stats(const waste_bank *bank, waste_bank_stats_t *out);
+
+/* A layer handle whose expert records are layer `layer` of a bank (headers -- and the payload
+ * crc32 with WASTE_FLAG_VERIFY_CRC -- checked as by waste_moe_create).  forward / step first
+ * fetch the routed experts into the cache, then read them from their slots; prefetch copies
+ * the predicted experts into the cache instead of warming L2.  Outputs equal those of the
+ * same records held in device memory, bit for bit.  Needs n_slots >= max_tokens * top_k.
+ * Fetches of one bank never overlap: each demand fetch waits for the bank's last lookahead
+ * fetch and each lookahead fetch for its last demand fetch (events held by the bank), on
+ * whatever streams they are issued.  Issue a layer's forward before the lookahead into the
+ * next layer, so that the lookahead's copies run beside the forward's expert kernels.
+ * These waits use events recorded by earlier calls, so banked layers are not for stream
+ * capture into CUDA graphs. */
+int waste_moe_create_banked(const waste_moe_config *cfg, const float *d_router_w,
+                            const float *d_router_bias, waste_bank *bank, int32_t layer,
+                            const float *d_codebooks, waste_moe **out);
+
 /* Message of the last failure on the calling thread ("" if none). */
 const char *waste_moe_last_error(void);
 

@@ -33,7 +33,9 @@ EXPORTED = ["waste_moe_record_layout", "waste_moe_pack_records", "waste_moe_crea
             "waste_moe_route", "waste_moe_forward", "waste_moe_prefetch", "waste_moe_destroy",
             "waste_moe_stats", "waste_moe_reset_stats", "waste_moe_last_error",
             "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile",
-            "waste_moe_rmsnorm", "waste_moe_forward_noalloc", "waste_moe_step", "waste_moe_set_trace"]
+            "waste_moe_rmsnorm", "waste_moe_forward_noalloc", "waste_moe_step", "waste_moe_set_trace",
+            "waste_bank_create", "waste_bank_destroy", "waste_bank_reset", "waste_bank_stats",
+            "waste_moe_create_banked"]
 
 
 class waste_moe_config(ctypes.Structure):
@@ -58,6 +60,11 @@ class waste_moe_stats_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "demand_code_bytes", "codebook_bytes", "router_bytes", "prefetch_issued_bytes",
         "prefetch_experts", "prediction_hits", "routed_slots", "forward_slots")]
+
+
+class waste_bank_stats_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "demand_hits", "demand_misses", "prefetch_copies", "prefetch_present", "copied_bytes")]
 
 
 class WasteError(RuntimeError):
@@ -101,8 +108,14 @@ def load(path: str = LIB_PATH):
     lib.waste_moe_step.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, vp]
     lib.waste_moe_set_trace.argtypes = [vp, vp, i32]
     lib.waste_moe_forward_noalloc.argtypes = [cfgp, vp, sz, vp, vp, i32, vp, vp, vp, i32, vp]
+    lib.waste_bank_create.argtypes = [cfgp, i32, vp, sz, i32, ctypes.POINTER(vp)]
+    lib.waste_bank_destroy.argtypes = [vp]
+    lib.waste_bank_destroy.restype = None
+    lib.waste_bank_reset.argtypes = [vp]
+    lib.waste_bank_stats.argtypes = [vp, ctypes.POINTER(waste_bank_stats_t)]
+    lib.waste_moe_create_banked.argtypes = [cfgp, vp, vp, vp, i32, vp, ctypes.POINTER(vp)]
     for name in EXPORTED:
-        if name not in ("waste_moe_destroy", "waste_moe_last_error"):
+        if name not in ("waste_moe_destroy", "waste_moe_last_error", "waste_bank_destroy"):
             getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -230,6 +243,42 @@ def waste_moe_forward_noalloc(cfg, records, record_stride, codebooks, d_h, T, d_
     return _check(load().waste_moe_forward_noalloc(
         ctypes.byref(cfg), _ptr(records), record_stride, _ptr(codebooks), _ptr(d_h), T,
         _ptr(d_idx), _ptr(d_gate), _ptr(d_out), mode, _stream(stream)))
+
+
+def waste_bank_create(cfg, n_layers, host_records, record_stride, n_slots) -> int:
+    out = ctypes.c_void_p()
+    _check(load().waste_bank_create(ctypes.byref(cfg), n_layers, _ptr(host_records), record_stride, n_slots,
+                                    ctypes.byref(out)))
+    return out.value
+
+
+def waste_bank_destroy(bank):
+    if bank:
+        load().waste_bank_destroy(bank)
+
+
+def waste_bank_reset(bank):
+    return _check(load().waste_bank_reset(bank))
+
+
+def waste_bank_stats(bank) -> dict:
+    st = waste_bank_stats_t()
+    _check(load().waste_bank_stats(bank, ctypes.byref(st)))
+    return {n: getattr(st, n) for n, _ in waste_bank_stats_t._fields_}
+
+
+def waste_moe_create_banked(cfg, router_w, router_bias, bank, layer, codebooks) -> int:
+    out = ctypes.c_void_p()
+    _check(load().waste_moe_create_banked(ctypes.byref(cfg), _ptr(router_w), _ptr(router_bias), bank, layer,
+                                          _ptr(codebooks), ctypes.byref(out)))
+    return out.value
+
+
+def pinned_bytes(nbytes: int, align: int = RECORD_ALIGN) -> torch.Tensor:
+    """A uint8 pinned host buffer of nbytes whose start is align-aligned."""
+    raw = torch.empty(nbytes + align, dtype=torch.uint8, pin_memory=True)
+    off = (-raw.data_ptr()) % align
+    return raw[off:off + nbytes]
 
 
 def aligned_bytes(nbytes: int, device="cuda", align: int = RECORD_ALIGN) -> torch.Tensor:

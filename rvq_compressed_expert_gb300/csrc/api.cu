@@ -25,6 +25,8 @@ struct waste_moe {
     unsigned long long *trace; // caller's trace buffer for the step kernel, or null
     int trace_cap;
     int mma_min_tokens; // tokens an expert needs in one call to take the tensor-core path
+    waste_bank *bank;   // records live in this bank (layer bank_layer), or null
+    int bank_layer;
 };
 
 namespace {
@@ -198,7 +200,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     const int E = cfg->n_experts;
     std::vector<waste_record_header> hdrs((size_t)E);
     cudaError_t ce = cudaMemcpy2D(hdrs.data(), sizeof(waste_record_header), d_records, record_stride,
-                                  sizeof(waste_record_header), (size_t)E, cudaMemcpyDeviceToHost);
+                                  sizeof(waste_record_header), (size_t)E, cudaMemcpyDefault);
     if (ce != cudaSuccess) return cuda_fail(ce, "copying record headers");
     for (int e = 0; e < E; ++e) {
         const waste_record_header &h = hdrs[(size_t)e];
@@ -263,10 +265,13 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     H->profiling = false;
     H->trace = nullptr;
     H->trace_cap = 0;
+    H->bank = nullptr;
+    H->bank_layer = 0;
     LayerView &L = H->L;
     L.router_w = d_router_w;
     L.router_b = d_router_bias;
     L.records = d_records;
+    L.slot_map = nullptr;
     L.stride = record_stride;
     for (int m = 0; m < 3; ++m) L.sec_off[m] = off[m];
     L.codebooks = d_codebooks;
@@ -477,11 +482,16 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool recon = (h->cfg.flags & WASTE_FLAG_K2_RECONSTRUCT) != 0;
     cudaError_t e;
+    if (h->bank) {
+        // the routed experts into the bank's HBM cache before the expert kernels read them
+        e = launch_bank_fetch(h->bank, h->bank_layer, d_idx, T * h->L.k, true, h->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "bank fetch");
+    }
     if (use_grouped(h, T)) {
         e = launch_grouped_forward(h->L, h->W, d_h, T, d_idx, d_gate, d_out, mode, h->mma_min_tokens, recon,
                                    h->num_sms, s, h->profiling ? &h->fwd_tm : nullptr);
         if (h->profiling) h->step_tm.n = 0;
-    } else if ((h->cfg.flags & WASTE_FLAG_STEP_KERNEL) && fused_eligible(h->L, T, false, h->num_sms)) {
+    } else if ((h->cfg.flags & WASTE_FLAG_STEP_KERNEL) && !h->bank && fused_eligible(h->L, T, false, h->num_sms)) {
         if (h->profiling) cudaEventRecord(h->step_tm.ev[0], s);
         e = launch_fused_step(h->L, h->W, d_h, T, false, const_cast<int32_t *>(d_idx),
                               const_cast<float *>(d_gate), nullptr, nullptr, nullptr, 1, d_out, mode,
@@ -517,7 +527,7 @@ int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, flo
         return fail(WASTE_EINVAL, "mode 2 (out = h + y) needs fp32 hidden states");
     if (T == 0) return ok();
     if (!d_idx || !d_gate || !d_out) return fail(WASTE_EINVAL, "NULL idx, gate or out");
-    if (!(h->cfg.flags & WASTE_FLAG_STEP_KERNEL) || use_grouped(h, T) ||
+    if (!(h->cfg.flags & WASTE_FLAG_STEP_KERNEL) || use_grouped(h, T) || h->bank ||
         !fused_eligible(h->L, T, true, h->num_sms)) {
         rc = waste_moe_route(h, d_h, T, d_idx, d_gate, d_logits, stream);
         if (rc) return rc;
@@ -555,8 +565,44 @@ int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_
                     nullptr, 1, nullptr, 0, s);
     if (e != cudaSuccess) return cuda_fail(e, "lookahead top-k");
     h->pred_P = P;
+    if (h->bank) {
+        // the predicted experts into the bank's HBM cache
+        e = launch_bank_fetch(h->bank, h->bank_layer, h->W.pred_idx, T * P, false, h->num_sms, s);
+        if (e == cudaSuccess) e = launch_set_pred_count(h->W.pred_count, T, P, s);
+        if (e != cudaSuccess) return cuda_fail(e, "bank lookahead");
+        return ok();
+    }
     e = launch_prefetch_l2(h->L, h->W.pred_idx, P, T, P, h->W.pred_count, h->W.stats, s);
     if (e != cudaSuccess) return cuda_fail(e, "L2 prefetch");
+    return ok();
+}
+
+int waste_moe_create_banked(const waste_moe_config *cfg, const float *d_router_w,
+                            const float *d_router_bias, waste_bank *bank, int32_t layer,
+                            const float *d_codebooks, waste_moe **out) {
+    if (!out) return fail(WASTE_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (!bank) return fail(WASTE_EINVAL, "NULL bank");
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    const waste_moe_config &bc = bank_config(bank);
+    if (cfg->d != bc.d || cfg->f != bc.f || cfg->n_experts != bc.n_experts)
+        return fail(WASTE_EINVAL, "layer shapes differ from the bank's");
+    if (layer < 0 || layer >= bank_layers(bank))
+        return fail(WASTE_EINVAL, "layer %d outside the bank's [0, %d)", layer, bank_layers(bank));
+    if ((long long)cfg->max_tokens * cfg->top_k > bank_slot_count(bank))
+        return fail(WASTE_EINVAL, "the bank's %d slots cannot hold max_tokens * top_k = %d experts",
+                    bank_slot_count(bank), cfg->max_tokens * cfg->top_k);
+    // headers (and crc with the flag) checked on the host-resident records themselves
+    waste_moe *h = nullptr;
+    rc = waste_moe_create(cfg, d_router_w, d_router_bias, bank_host_records(bank, layer), bank_stride(bank),
+                          d_codebooks, &h);
+    if (rc) return rc;
+    h->bank = bank;
+    h->bank_layer = layer;
+    h->L.records = bank_slots(bank);
+    h->L.slot_map = bank_slot_map(bank, layer);
+    *out = h;
     return ok();
 }
 
@@ -576,8 +622,9 @@ int waste_moe_stats(const waste_moe *h, waste_moe_stats_t *out) {
     out->prediction_hits = v[kStatPredHits];
     out->routed_slots = v[kStatRoutedSlots];
     out->forward_slots = v[kStatForwardSlots];
-    if (err & kErrTimeout) return fail(WASTE_ETIMEOUT, "a device wait of the fused step kernel gave up");
-    if (err & kErrTimeout) return fail(WASTE_ETIMEOUT, "a bounded device wait of the step kernel gave up");
+    if (err & kErrTimeout) return fail(WASTE_ETIMEOUT, "a bounded device wait gave up");
+    if (err & kErrNotResident)
+        return fail(WASTE_EINVAL, "an expert of a banked layer had no cache slot (cache too small?)");
     if (err & kErrBadExpert) return fail(WASTE_EINVAL, "forward saw an expert index outside [0, %d)", h->L.E);
     return ok();
 }

@@ -20,7 +20,16 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxFusedRowBlocks = 64; // down row blocks the fused step kernel can track
 
 // Sticky device error bits.
-enum : uint32_t { kErrBadExpert = 1u, kErrTimeout = 2u };
+enum : uint32_t { kErrBadExpert = 1u, kErrTimeout = 2u, kErrNotResident = 4u };
+
+// Record of expert e: by index, or through a bank's slot map (null when the expert has no
+// slot -- the caller treats it as an invalid expert).
+__device__ __forceinline__ const uint8_t *expert_record(const uint8_t *records, size_t stride,
+                                                        const int32_t *slot_map, int e) {
+    if (!slot_map) return records + (size_t)e * stride;
+    const int s = slot_map[e];
+    return s >= 0 ? records + (size_t)s * stride : nullptr;
+}
 
 // Device counters, indices into the handle's uint64 counter array.
 enum {
@@ -60,7 +69,8 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct LayerView {
     const float *router_w;
     const float *router_b;
-    const uint8_t *records;
+    const uint8_t *records;   // record of expert e at records + e * stride, or (slot_map)
+    const int32_t *slot_map;  // optional [E]: record of expert e at records + slot_map[e] * stride
     size_t stride;
     size_t sec_off[3];
     const float *codebooks; // [E][3][3][256][8]
@@ -69,6 +79,21 @@ struct LayerView {
     MatGeom gu;   // gate / up geometry (f rows, d inputs)
     MatGeom dn;   // down geometry (d rows, f inputs)
 };
+
+// Device state of a tiered expert bank (see bank.cu).
+struct BankDevice {
+    void *base;
+    uint8_t *slots;       // [n_slots] records in HBM
+    int32_t *map;         // [n_layers * E] (layer, expert) -> slot, or -1
+    int32_t *key_of;      // [n_slots] slot -> layer * E + expert, or -1
+    uint32_t *tick;       // [n_slots] clock of the last call that used the slot
+    int2 *jobs;           // [n_slots] copy jobs of the last plan: (slot, key)
+    uint32_t *clock;      // advanced by every demand fetch
+    int32_t *n_jobs;
+    unsigned long long *stats;
+};
+enum { kBankDemandHits = 0, kBankDemandMisses, kBankPrefetchCopies, kBankPrefetchPresent, kBankCopiedBytes,
+       kBankStatCount };
 
 // Slots of a batched call grouped by expert (see grouped.cu).
 struct Grouping {
@@ -183,6 +208,20 @@ cudaError_t launch_crc_store(const uint32_t *crc, uint8_t *records, size_t strid
                              size_t field_off, cudaStream_t s);
 
 int device_sm_count();
+
+// Tiered bank: bring the experts ids[0..n_ids) of `layer` into the HBM cache (demand: the
+// clock advances and hits / misses are counted; lookahead: slots of the call in flight stay).
+cudaError_t launch_bank_fetch(waste_bank *b, int layer, const int32_t *ids, int n_ids, bool demand, int num_sms,
+                              cudaStream_t s);
+const uint8_t *bank_host_records(const waste_bank *b, int layer);
+const uint8_t *bank_slots(const waste_bank *b);
+const int32_t *bank_slot_map(const waste_bank *b, int layer);
+int bank_layers(const waste_bank *b);
+int bank_slot_count(const waste_bank *b);
+size_t bank_stride(const waste_bank *b);
+const waste_moe_config &bank_config(const waste_bank *b);
+// Predicted-expert count of each token (the lookahead's P), read by the next route.
+cudaError_t launch_set_pred_count(int32_t *pred_count, int T, int P, cudaStream_t s);
 
 
 // Sets the calling thread's message returned by waste_moe_last_error().

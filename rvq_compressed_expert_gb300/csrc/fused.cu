@@ -270,6 +270,7 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
     F.trace_cap = trace_cap;
     LutArgs &A = F.A;
     A.records = L.records;
+    A.slot_map = L.slot_map;
     A.stride = L.stride;
     A.codebooks = L.codebooks;
     A.idx = idx;

@@ -265,6 +265,7 @@ static_assert(kMmaSmem <= 227 * 1024, "shared memory of the tensor-core kernel")
 
 struct MmaArgs {
     const uint8_t *records;
+    const int32_t *slot_map;
     size_t stride;
     size_t sec[3];
     const float *codebooks;
@@ -368,7 +369,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             const int mb = item % nmb, npad = pad16(ch.z);
             const uint32_t bbytes = (uint32_t)npad * 128;
             const uint8_t *bsrc = A.bsrc + (size_t)ch.w * KC * 128;
-            const uint8_t *rec = A.records + (size_t)ch.x * A.stride;
+            const uint8_t *rec = expert_record(A.records, A.stride, A.slot_map, ch.x);
+            if (!rec) {
+                // not resident (a bank fetch did not place it): no copies, the row block
+                // decodes whatever the buffers hold, and the error is latched
+                if (lane == 0) atomicOr(A.err, kErrNotResident);
+                rec = A.records;
+            }
             const uint32_t seg_bytes = (uint32_t)min(8, G.groups - 8 * mb) * (kStages * 512);
             for (int pass = 0; pass < kPasses; ++pass) {
                 const uint8_t *sec = rec + A.sec[kDown ? 2 : pass];
@@ -598,6 +605,7 @@ cudaError_t launch_grouped_forward(const LayerView &L, const Workspace &W, const
 
     MmaArgs A;
     A.records = L.records;
+    A.slot_map = L.slot_map;
     A.stride = L.stride;
     for (int m = 0; m < 3; ++m) A.sec[m] = L.sec_off[m];
     A.codebooks = L.codebooks;

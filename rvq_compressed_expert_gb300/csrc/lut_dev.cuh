@@ -21,6 +21,7 @@ constexpr int kPrefetchRounds = 3;                 // L2 prefetch distance in ro
 
 struct LutArgs {
     const uint8_t *records;
+    const int32_t *slot_map; // optional expert -> record slot
     size_t stride;
     const float *codebooks;
     const int32_t *idx;
@@ -164,8 +165,8 @@ __device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
     }
     U.e = A.idx[U.slot];
     U.base[0] = U.base[1] = nullptr;
-    if (U.e >= 0 && U.e < A.E) {
-        const uint8_t *rec = A.records + (size_t)U.e * A.stride;
+    const uint8_t *rec = (U.e >= 0 && U.e < A.E) ? expert_record(A.records, A.stride, A.slot_map, U.e) : nullptr;
+    if (rec) {
         if constexpr (!kDown) {
             const size_t so = (size_t)U.seg0 * A.gu.groups * (kStages * 512);
             U.base[0] = rec + A.off_gate + so;
@@ -317,7 +318,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
         }
     }
-    if (!valid && threadIdx.x == 0) atomicOr(A.err, kErrBadExpert);
+    if (!valid && threadIdx.x == 0) atomicOr(A.err, (U.e >= 0 && U.e < A.E) ? kErrNotResident : kErrBadExpert);
     const int t = U.slot / A.k;
     // ---- input vectors of this lane's column(s)
     float xv[2][kVec];

@@ -186,6 +186,7 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
                       const int32_t *idx, int num_sms) {
     LutArgs A;
     A.records = L.records;
+    A.slot_map = L.slot_map;
     A.stride = L.stride;
     A.codebooks = L.codebooks;
     A.idx = idx;

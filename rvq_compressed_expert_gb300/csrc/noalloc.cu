@@ -101,6 +101,7 @@ int waste_moe_forward_noalloc(const waste_moe_config *cfg, const uint8_t *d_reco
     L.router_w = nullptr;
     L.router_b = nullptr;
     L.records = d_records;
+    L.slot_map = nullptr;
     L.stride = record_stride;
     L.codebooks = d_codebooks;
     L.d = cfg->d;

@@ -353,6 +353,11 @@ cudaError_t launch_rmsnorm(const float *in, float *out, int T, int d, cudaStream
     return cudaGetLastError();
 }
 
+cudaError_t launch_set_pred_count(int32_t *pred_count, int T, int P, cudaStream_t s) {
+    set_count_kernel<<<(T + 255) / 256, 256, 0, s>>>(pred_count, T, P);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefetch_l2(const LayerView &L, const int32_t *pred_idx, int pred_stride,
                                int T, int P, int32_t *pred_count, unsigned long long *stats,
                                cudaStream_t s) {

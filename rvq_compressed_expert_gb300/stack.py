@@ -23,7 +23,11 @@ from . import binding as B
 
 
 class DecodeStack:
-    def __init__(self, layers, tokens: int, device="cuda"):
+    def __init__(self, layers, tokens: int, device="cuda", banked: bool = False):
+        """banked: the layers' records live in a tiered bank (TieredStack); each layer's
+        forward is then issued before the lookahead into the next layer, whose copies into
+        the HBM cache run beside the forward's expert kernels."""
+        self.banked = banked
         self.layers = layers
         self.T = tokens
         w = layers[0].w
@@ -42,6 +46,8 @@ class DecodeStack:
         with torch.cuda.stream(main):
             self.h.copy_(h0)
         pending = None
+        if self.banked:
+            return self._run_banked(lookahead, main, side, on_layer)
         for L in range(n):
             x = self.x[L & 1]
             B.waste_moe_rmsnorm(self.h, x, T, self.d, main)
@@ -58,6 +64,30 @@ class DecodeStack:
             if on_layer is not None:
                 on_layer(L, self.idx, self.gate, main)
             pending = ev
+        if pending is not None:
+            main.wait_event(pending)
+        return self.h
+
+    def _run_banked(self, lookahead, main, side, on_layer):
+        n = len(self.layers)
+        T = self.T
+        pending = None
+        for L in range(n):
+            x = self.x[L & 1]
+            B.waste_moe_rmsnorm(self.h, x, T, self.d, main)
+            x_ready = torch.cuda.Event()
+            x_ready.record(main)
+            if pending is not None:
+                main.wait_event(pending)  # layer L's prediction is in place before it routes
+            self.layers[L].step(x, T, self.idx, self.gate, self.h, 1, stream=main)
+            if on_layer is not None:
+                on_layer(L, self.idx, self.gate, main)
+            pending = None
+            if lookahead and L + 1 < n:
+                side.wait_event(x_ready)
+                self.layers[L + 1].prefetch(x, T, lookahead, stream=side)
+                pending = torch.cuda.Event()
+                pending.record(side)
         if pending is not None:
             main.wait_event(pending)
         return self.h

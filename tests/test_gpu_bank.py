@@ -1,0 +1,110 @@
+"""Tiered expert bank: records in pinned host memory, an HBM cache, device-side fetches.
+
+Page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", sections "Budget RAM et zone de
+performance étroite" and "Lecture anticipée et prédiction du routeur": a bounded cache of
+experts over a slow tier, misses read from the slow tier, the lookahead fills the cache ahead
+of demand -- the outputs never change (the real router decides), only what is resident.
+"""
+import pytest
+import torch
+
+from rvq_compressed_expert_gb300 import binding as B
+from rvq_compressed_expert_gb300 import synth
+from rvq_compressed_expert_gb300.bank import TieredStack
+from rvq_compressed_expert_gb300.layer import MoELayer
+from rvq_compressed_expert_gb300.stack import DecodeStack
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rvq_compressed_expert_gb300 import _build
+    _build.build()
+    B.load()
+
+
+W = synth.Workload("bank", 512, 256, 16, 4, 1, "f32", "offsets", n_layers=4, lookahead=3)
+
+
+def run_tokens(stack, tokens, lookahead):
+    main = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    main.wait_stream(torch.cuda.current_stream())
+    outs = []
+    for i in range(tokens):
+        with torch.cuda.stream(main):  # the token is drawn and the output read on `main`
+            h0 = synth.hidden(50 + i, W.tokens, W.d, "f32", "cuda")
+        out = stack.run(h0, lookahead, main, side)
+        with torch.cuda.stream(main):
+            outs.append(out.clone())
+    torch.cuda.current_stream().wait_stream(main)
+    torch.cuda.synchronize()
+    return outs
+
+
+def resident_outputs(tokens, lookahead):
+    layers = [MoELayer(W, 0, L, "cuda") for L in range(W.n_layers)]
+    try:
+        return run_tokens(DecodeStack(layers, W.tokens), tokens, lookahead)
+    finally:
+        for l in layers:
+            l.close()
+
+
+@pytest.mark.parametrize("lookahead", [0, 3])
+def test_banked_equals_resident(lookahead):
+    """6 slots for 4 layers x top-4: every layer evicts; outputs equal the resident stack's bit
+    for bit; hits + misses count every routed expert; bytes copied = copies x record stride."""
+    ref = resident_outputs(5, lookahead)
+    ts = TieredStack(W, 0, W.n_layers, 6)
+    try:
+        got = run_tokens(DecodeStack(ts.layers, W.tokens, banked=True), 5, lookahead)
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
+        st = ts.stats()
+        assert st["demand_hits"] + st["demand_misses"] == 5 * W.n_layers * W.top_k
+        assert st["copied_bytes"] == (st["demand_misses"] + st["prefetch_copies"]) * ts.stride
+        for ml in ts.layers:
+            ml.stats()  # raises if an expert had no slot
+        if lookahead == 0:
+            assert st["prefetch_copies"] == 0 and st["prefetch_present"] == 0
+    finally:
+        ts.close()
+
+
+def test_lookahead_raises_demand_hits():
+    """With the router's offsets making the prediction reliable, the lookahead turns demand
+    misses into hits (16 slots: the cache holds about one layer's experts beside the next)."""
+    res = {}
+    for P in (0, 3):
+        ts = TieredStack(W, 0, W.n_layers, 8)
+        try:
+            run_tokens(DecodeStack(ts.layers, W.tokens, banked=True), 4, P)
+            res[P] = ts.stats()
+        finally:
+            ts.close()
+    assert res[3]["demand_misses"] < res[0]["demand_misses"], res
+    assert res[3]["prefetch_copies"] > 0
+
+
+def test_bank_refusals():
+    ts = TieredStack(W, 0, 1, 4)
+    try:
+        ml = ts.layers[0]
+        cfg = B.make_config(W.d, W.f, W.n_experts, W.top_k, "f32", 2, 0, 0, 0)  # 2 x 4 > 4 slots
+        with pytest.raises(B.WasteError) as ei:
+            B.waste_moe_create_banked(cfg, ml.router_w, ml.router_b, ts.bank, 0, ml.codebooks)
+        assert ei.value.status == -1
+        with pytest.raises(B.WasteError):
+            B.waste_moe_create_banked(ml.cfg, ml.router_w, ml.router_b, ts.bank, 1, ml.codebooks)  # no layer 1
+    finally:
+        ts.close()
+    cfg = B.make_config(W.d, W.f, W.n_experts, W.top_k, "f32", 1, 0, 0, 0)
+    stride, _, _ = B.waste_moe_record_layout(cfg)
+    host = B.pinned_bytes(W.n_experts * stride + 8192)
+    with pytest.raises(B.WasteError) as ei:  # not 4096-aligned
+        B.waste_bank_create(cfg, 1, host[16:], stride, 4)
+    assert ei.value.status == -4
