@@ -9,10 +9,12 @@ Per step a fresh token is taken from a pool of 64; L2 is flushed between steps
 (a 256 MiB write outside the timed events), so every step streams its ~210 MB
 from HBM.
 
-Also measured (extra keys of the same line): the full-depth decode stack (92
-layers x 64 experts, lookahead 6 vs off, captured in CUDA graphs), the
-end-to-end number through the C ABI with host buffers, and the CPU oracle on
-the host cores.
+Also measured (extra keys of the same line): batched decode (128 tokens) and a
+prefill chunk (512 tokens) on the grouped tensor-core path, the full-depth
+decode stack (92 layers x 64 experts, lookahead 6 vs off, captured in CUDA
+graphs), a tiered expert bank (16 layers x 64 experts in pinned host memory
+behind HBM caches of three sizes, lookahead 0/6/16), the end-to-end number
+through the C ABI with host buffers, and the CPU oracle on the host cores.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 For N > 1 it is launched once per GPU by torch.distributed.run; every rank
@@ -504,6 +506,118 @@ def run_stack(args, dev, out):
     torch.cuda.empty_cache()
 
 
+def measured_link_gbs(ts) -> float:
+    """The copy engines' host -> HBM rate over 64 records of the bank's pinned buffer."""
+    n = min(64, ts.host.numel() // ts.stride)
+    dst = torch.empty(n * ts.stride, dtype=torch.uint8, device="cuda")
+    src = ts.host[:n * ts.stride]
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    ts_ = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        ts_.append(a.elapsed_time(b))
+    del dst
+    return n * ts.stride / (statistics.median(ts_) * 1e-3) / 1e9
+
+
+def run_tiered(args, dev, out):
+    """16 layers x 64 experts with their records in pinned host memory behind an HBM cache;
+    one token at a time (eager: the fetch plan depends on the routing); cache sizes below,
+    near and above one token's working set (16 layers x top-16 = 256 records); lookahead
+    0, 6 and 16 experts into the next layer."""
+    from rvq_compressed_expert_gb300 import binding as B
+    from rvq_compressed_expert_gb300 import synth
+    from rvq_compressed_expert_gb300.bank import TieredStack
+    from rvq_compressed_expert_gb300.stack import DecodeStack
+
+    w = synth.WORKLOADS["tiered"]
+    stride = 12_390_400
+    host_need = w.n_layers * w.n_experts * stride
+    try:
+        host_free = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError):
+        host_free = None
+    if host_free is not None and host_free < 2 * host_need:
+        out["tiered"] = {"skipped": f"needs {2 * host_need / 1e9:.0f} GB free host memory"}
+        return
+    working_set = w.n_layers * w.top_k
+    slot_sizes = (working_set // 2, working_set * 5 // 4, working_set * 5 // 2)
+    ts = TieredStack(w, 0, w.n_layers, slot_sizes[0], dev, max_tokens=1)
+    stack = DecodeStack(ts.layers, 1, dev, banked=True)
+    n_warm, n_timed = 4, 16
+    tokens = [synth.hidden(1000 + i, 1, w.d, "f32", dev) for i in range(n_warm + n_timed)]
+    main = torch.cuda.Stream(device=dev)
+    side = torch.cuda.Stream(device=dev)
+    rows, finals, errors = [], {}, []
+    modes = (("overlap", 0), ("serial", B.FLAG_BANK_SERIAL))
+    for slots in slot_sizes:
+        for P, (mode, flags) in [(p, m) for p in (0, w.lookahead, w.top_k) for m in modes]:
+            ts.rebank(slots, flags)
+            main.wait_stream(torch.cuda.current_stream())
+            for i in range(n_warm):
+                stack.run(tokens[i], P, main, side)
+            torch.cuda.synchronize()
+            s0 = ts.stats()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_timed)]
+            outs = []
+            t_start = time.time()
+            for i in range(n_timed):
+                evs[i][0].record(main)
+                o = stack.run(tokens[n_warm + i], P, main, side)
+                evs[i][1].record(main)
+                with torch.cuda.stream(main):
+                    outs.append(o.clone())
+            torch.cuda.synchronize()
+            args.sampler.mark(t_start, time.time())
+            s1 = ts.stats()
+            for L, ml in enumerate(ts.layers):
+                try:
+                    ml.stats()
+                except Exception as e:  # an expert without a slot: reported, not hidden
+                    errors.append(f"slots {slots}, lookahead {P}, layer {L}: {e}")
+                    ml.reset_stats()
+            st = {k: s1[k] - s0[k] for k in s1}
+            ms = sum(a.elapsed_time(b) for a, b in evs) / n_timed
+            demand = st["demand_hits"] + st["demand_misses"]
+            finals[(slots, P, mode)] = torch.stack(outs)
+            rows.append(dict(
+                slots=slots, cache_gb=slots * ts.stride / 1e9, lookahead=P, copy=mode,
+                tok_s=1e3 / ms, ms_per_token=ms,
+                demand_hit_rate=st["demand_hits"] / max(demand, 1),
+                copied_gb_per_token=st["copied_bytes"] / n_timed / 1e9,
+                demand_copies_per_token=st["demand_misses"] / n_timed,
+                lookahead_copies_per_token=st["prefetch_copies"] / n_timed,
+                link_gbs_lower_bound=st["copied_bytes"] / n_timed / (ms * 1e-3) / 1e9))
+    ref = finals[(slot_sizes[0], 0, "serial")]
+    link = measured_link_gbs(ts)
+    for r in rows:
+        r["link_bound_tok_s"] = link / r["copied_gb_per_token"] if r["copied_gb_per_token"] else None
+        r["frac_of_link_bound"] = r["tok_s"] / r["link_bound_tok_s"] if r["link_bound_tok_s"] else None
+    out["tiered"] = dict(
+        workload=f"{w.n_layers} layers x {w.n_experts} experts (d={w.d} f={w.f} top-{w.top_k}, Zipf(1.1) "
+                 f"router bias), records ({host_need / 1e9:.1f} GB) in pinned host memory, HBM cache of "
+                 f"n slots; T=1, fp32, h += combine per layer; eager; {n_warm} warm-up then {n_timed} "
+                 f"timed tokens per row from an empty cache; per-token working set {working_set} records "
+                 f"({working_set * ts.stride / 1e9:.2f} GB), larger than L2",
+        link_gbs=link,
+        link_note="host->HBM copy rate of the copy engines (cudaMemcpyAsync of 64 records from the same "
+                  "pinned buffer into HBM), measured here: the bound of every row",
+        rows=rows,
+        outputs_bit_identical=all(torch.equal(v, ref) for v in finals.values()),
+    )
+    if errors:
+        out["tiered"]["device_errors"] = errors[:8]
+    ts.close()
+    del stack, finals, ref
+    torch.cuda.empty_cache()
+
+
 def cpu_baseline_decode(layer, pool, budget_s=12.0):
     """The oracle (single-threaded C, double) on a bounded sample of decode tokens."""
     import oracle
@@ -553,6 +667,8 @@ def native(args):
         run_batched(args, dev, res, "prefill", 10)
     if not args.no_stack:
         run_stack(args, dev, res)
+    if not args.no_tiered:
+        run_tiered(args, dev, res)
     clocks = args.sampler.stop()
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -621,7 +737,7 @@ def native(args):
     }
     if "verify_crc" in res:
         line["config"]["create_with_crc_verify"] = res["verify_crc"]
-    for extra in ("batched", "prefill", "stack"):
+    for extra in ("batched", "prefill", "stack", "tiered"):
         if extra in res:
             line[extra] = res[extra]
     print(json.dumps(line), flush=True)
@@ -785,6 +901,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--no-tiered", action="store_true")
     ap.add_argument("--no-batched", action="store_true")
     ap.add_argument("--prefill", action="store_true",
                     help="with --profile-case: the grouped tensor-core path (64 bf16 tokens)")

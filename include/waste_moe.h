@@ -91,10 +91,13 @@ enum {
     WASTE_FLAG_K2_RECONSTRUCT = 1u << 4, /* forward: rebuild each 8-weight vector from the
                                             3 codebook entries in registers instead of the
                                             partial-dot-product table */
-    WASTE_FLAG_STEP_KERNEL = 1u << 5 /* run forward / step as one persistent kernel that claims
+    WASTE_FLAG_STEP_KERNEL = 1u << 5, /* run forward / step as one persistent kernel that claims
                                         router, top-k, expert and combine work from a device
                                         queue, instead of one kernel per phase (same results,
                                         bit for bit) */
+    WASTE_FLAG_BANK_SERIAL = 1u << 6  /* banked layers: copy a call's missing experts first and
+                                        run the expert kernels after, instead of consuming each
+                                        expert as its copy lands (same results, bit for bit) */
 };
 
 /* Layer configuration.  d % 8 == 0, f % 8 == 0, 1 <= top_k <= n_experts <= 4096,
@@ -289,8 +292,9 @@ int waste_moe_read_profile(const waste_moe *h, float ms[6]);
  * in a large slow tier, a bounded cache holds some of them, a miss reads the expert's
  * record from the slow tier, and the next layer's router fills the cache ahead of demand.
  * Here the slow tier is host memory (pinned, read by the GPU) and the cache is HBM.  The
- * fetch runs on the device: a plan (hits refresh their slot; each miss takes the least
- * recently used slot not used by the call in flight) and a copy of the missing records. */
+ * fetch runs on the device: a plan (every requested expert already in the cache takes the
+ * call's stamp; each miss then takes the least recently used slot not stamped by the call in
+ * flight) and a copy of the missing records. */
 typedef struct waste_bank waste_bank;
 
 typedef struct {
@@ -321,6 +325,10 @@ int waste_bank_stats(const waste_bank *bank, waste_bank_stats_t *out);
  * fetch the routed experts into the cache, then read them from their slots; prefetch copies
  * the predicted experts into the cache instead of warming L2.  Outputs equal those of the
  * same records held in device memory, bit for bit.  Needs n_slots >= max_tokens * top_k.
+ * A call on the table-lookup path with T * top_k <= 64 (decode) runs its demand copy inside
+ * the persistent step kernel: a few CTAs copy the missing records in order while the others
+ * run the resident experts' units and then each missing expert's as soon as its record is in
+ * (the pages' read/compute overlap); WASTE_FLAG_BANK_SERIAL turns this off.
  * Fetches of one bank never overlap: each demand fetch waits for the bank's last lookahead
  * fetch and each lookahead fetch for its last demand fetch (events held by the bank), on
  * whatever streams they are issued.  Issue a layer's forward before the lookahead into the

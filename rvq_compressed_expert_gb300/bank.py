@@ -40,7 +40,24 @@ class TieredStack:
             ml.records = None
             self.layers.append(ml)
         torch.cuda.empty_cache()
-        self.bank = B.waste_bank_create(cfg0, n_layers, self.host, self.stride, n_slots)
+        self.cfg0 = cfg0
+        self.bank = None
+        self.rebank(n_slots)
+
+    def rebank(self, n_slots: int, flags: int | None = None):
+        """Replace the HBM cache by an empty one of n_slots records (same host records); with
+        flags, the layer handles are made again with those configuration flags."""
+        for ml in self.layers:
+            if ml.handle:
+                B.waste_moe_destroy(ml.handle)
+                ml.handle = None
+            if flags is not None:
+                ml.cfg.flags = flags
+        if self.bank:
+            B.waste_bank_destroy(self.bank)
+            self.bank = None
+        self.n_slots = n_slots
+        self.bank = B.waste_bank_create(self.cfg0, len(self.layers), self.host, self.stride, n_slots)
         for L, ml in enumerate(self.layers):
             ml.handle = B.waste_moe_create_banked(ml.cfg, ml.router_w, ml.router_b, self.bank, L,
                                                   ml.codebooks)

@@ -23,6 +23,7 @@ FLAG_FORCE_GEMV = 1 << 2
 FLAG_FORCE_MMA = 1 << 3
 FLAG_K2_RECONSTRUCT = 1 << 4
 FLAG_STEP_KERNEL = 1 << 5
+FLAG_BANK_SERIAL = 1 << 6
 RECORD_ALIGN = 4096
 RECORD_MAGIC = 0x454F4D57
 

@@ -70,7 +70,7 @@ int check_config(const waste_moe_config *c) {
     if (c->lookahead < 0 || c->lookahead > kMaxTopK || c->lookahead > c->n_experts)
         return fail(WASTE_EINVAL, "lookahead = %d outside [0, min(n_experts, %d)]", c->lookahead, kMaxTopK);
     const uint32_t known = WASTE_FLAG_VERIFY_CRC | WASTE_FLAG_FORCE_GEMV | WASTE_FLAG_FORCE_MMA |
-                           WASTE_FLAG_K2_RECONSTRUCT | WASTE_FLAG_STEP_KERNEL;
+                           WASTE_FLAG_K2_RECONSTRUCT | WASTE_FLAG_STEP_KERNEL | WASTE_FLAG_BANK_SERIAL;
     if (c->flags & ~known) return fail(WASTE_EINVAL, "unknown flags 0x%x", c->flags & ~known);
     return WASTE_OK;
 }
@@ -309,7 +309,9 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
         S * npair * (size_t)L.d * 4,                // part_dn
         kStatCount * 8,                             // stats
         4,                                          // err
-        (4 + S + kMaxFusedRowBlocks) * 4,           // sync
+        (4 + 2 * S + kMaxFusedRowBlocks) * 4,       // sync
+        S * 4,                                      // bank_wait
+        S * 4,                                      // bank_order
         G * ((size_t)E + 1) * 4,                    // grp.offs
         G * S * 4,                                  // grp.sorted
         G * S * 4,                                  // grp.lut_slots
@@ -349,17 +351,19 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     W.stats = reinterpret_cast<unsigned long long *>(b + offs[8]);
     W.err = reinterpret_cast<uint32_t *>(b + offs[9]);
     W.sync = reinterpret_cast<unsigned *>(b + offs[10]);
+    W.bank_wait = reinterpret_cast<int32_t *>(b + offs[11]);
+    W.bank_order = reinterpret_cast<int32_t *>(b + offs[12]);
     Grouping &Gp = W.grp;
-    Gp.offs = grouped ? reinterpret_cast<int32_t *>(b + offs[11]) : nullptr;
-    Gp.sorted = grouped ? reinterpret_cast<int32_t *>(b + offs[12]) : nullptr;
-    Gp.lut_slots = grouped ? reinterpret_cast<int32_t *>(b + offs[13]) : nullptr;
-    Gp.chunks = grouped ? reinterpret_cast<int4 *>(b + offs[14]) : nullptr;
-    Gp.counts = grouped ? reinterpret_cast<int32_t *>(b + offs[15]) : nullptr;
-    Gp.one_part = grouped ? reinterpret_cast<uint8_t *>(b + offs[16]) : nullptr;
-    Gp.xg = grouped ? reinterpret_cast<uint8_t *>(b + offs[17]) : nullptr;
-    Gp.ag = grouped ? reinterpret_cast<uint8_t *>(b + offs[18]) : nullptr;
+    Gp.offs = grouped ? reinterpret_cast<int32_t *>(b + offs[13]) : nullptr;
+    Gp.sorted = grouped ? reinterpret_cast<int32_t *>(b + offs[14]) : nullptr;
+    Gp.lut_slots = grouped ? reinterpret_cast<int32_t *>(b + offs[15]) : nullptr;
+    Gp.chunks = grouped ? reinterpret_cast<int4 *>(b + offs[16]) : nullptr;
+    Gp.counts = grouped ? reinterpret_cast<int32_t *>(b + offs[17]) : nullptr;
+    Gp.one_part = grouped ? reinterpret_cast<uint8_t *>(b + offs[18]) : nullptr;
+    Gp.xg = grouped ? reinterpret_cast<uint8_t *>(b + offs[19]) : nullptr;
+    Gp.ag = grouped ? reinterpret_cast<uint8_t *>(b + offs[20]) : nullptr;
     Gp.max_chunks = grouped ? (int)max_chunks : 0;
-    W.router_part = T > 16 ? reinterpret_cast<float *>(b + offs[19]) : nullptr;
+    W.router_part = T > 16 ? reinterpret_cast<float *>(b + offs[21]) : nullptr;
     ce = cudaMemset(base, 0, total);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
@@ -482,6 +486,25 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool recon = (h->cfg.flags & WASTE_FLAG_K2_RECONSTRUCT) != 0;
     cudaError_t e;
+    if (h->bank && !(h->cfg.flags & WASTE_FLAG_BANK_SERIAL) && !use_grouped(h, T) &&
+        T * h->L.k <= kOverlapMaxSlots && fused_eligible(h->L, T, false, h->num_sms)) {
+        // the routed experts' copy runs inside the step kernel, each expert consumed on arrival
+        BankLanes lanes;
+        e = launch_bank_plan_overlap(h->bank, h->bank_layer, d_idx, T * h->L.k, h->W.bank_wait, h->W.bank_order,
+                                     &lanes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "bank plan");
+        if (h->profiling) cudaEventRecord(h->step_tm.ev[0], s);
+        e = launch_fused_step(h->L, h->W, d_h, T, false, const_cast<int32_t *>(d_idx),
+                              const_cast<float *>(d_gate), nullptr, nullptr, nullptr, 1, d_out, mode,
+                              recon, h->num_sms, s, h->trace, h->trace_cap, &lanes, h->W.bank_order);
+        if (h->profiling) {
+            cudaEventRecord(h->step_tm.ev[1], s);
+            h->step_tm.n = 2;
+            h->fwd_tm.n = 0;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "banked step kernel");
+        return ok();
+    }
     if (h->bank) {
         // the routed experts into the bank's HBM cache before the expert kernels read them
         e = launch_bank_fetch(h->bank, h->bank_layer, d_idx, T * h->L.k, true, h->num_sms, s);

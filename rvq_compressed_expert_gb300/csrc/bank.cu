@@ -9,15 +9,18 @@
 // demand hit rate rises from 14% to 38% with the bytes read unchanged).  Here the slow tier
 // is Grace memory and the fast one HBM.
 //
-// A fetch is two kernels on the caller's stream: a plan (one warp: hits refresh their slot's
-// tick; each miss takes the least recently used slot whose tick is older than the current
-// clock -- slots stamped by the call in flight are never victims -- and becomes a copy job)
-// and a copy (the whole grid moves the jobs' records, 16 bytes per thread and step).  The
-// expert -> slot map is what the expert kernels read through.  Fetches must not overlap:
-// the caller orders them (one stream, or events between streams).
+// A fetch is two kernels on the caller's stream: a plan (one warp: first every requested
+// expert already resident takes the call's stamp; then each miss takes the least recently
+// used slot whose tick is older than the current clock -- slots stamped by the call in flight
+// are never victims -- and becomes a copy job) and a copy (a few CTAs, which keep the link
+// busy while leaving the SMs to the expert kernels).  A demand fetch of a decode call can
+// instead leave the copy to the persistent step kernel, which consumes each expert as its
+// copy lands (launch_bank_plan_overlap).  The expert -> slot map is what the expert kernels
+// read through.  Fetches must not overlap: the caller orders them (one stream, or events
+// between streams).
 #include <new>
 
-#include "common.cuh"
+#include "bank_dev.cuh"
 
 struct waste_bank {
     waste_moe_config cfg;
@@ -25,33 +28,69 @@ struct waste_bank {
     size_t stride;
     const uint8_t *host;  // device-usable address of the host records
     wm::BankDevice D;
-    // completion of the last demand fetch and of the last lookahead fetch: each kind waits
-    // for the other, so fetches never overlap whatever streams they are issued on
+    // the last demand fetch (for a fetch whose copy runs in the step kernel: its plan) and the
+    // last lookahead fetch: each kind waits for the other, so plans never overlap and a
+    // lookahead copies only into slots no running expert kernel reads, whatever streams the
+    // fetches are issued on
     cudaEvent_t ev_demand, ev_lookahead;
+    int2 *jobs[2];       // copy jobs of the last plan of each kind (demand, lookahead)
+    int32_t *n_jobs[2];
 };
 
 namespace wm {
 
 namespace {
 
-// one warp
+// The bank's device state with the job list of one kind of fetch (a lookahead may plan and
+// copy while the step kernel of a demand fetch still reads its own jobs).
+BankDevice device_for(const waste_bank *b, bool demand) {
+    BankDevice D = b->D;
+    D.jobs = b->jobs[demand ? 0 : 1];
+    D.n_jobs = b->n_jobs[demand ? 0 : 1];
+    return D;
+}
+
+// One warp.  With wait_job / order (n_ids <= 64): wait_job[i] = the job by which id i's record
+// arrives in this fetch, or -1 when it is already resident (or has no slot); order = the ids'
+// positions sorted by (wait_job, position), resident ones first.
 __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E, int n_slots, size_t stride,
-                                                  const int32_t *__restrict__ ids, int n_ids, int demand) {
+                                                  const int32_t *__restrict__ ids, int n_ids, int demand,
+                                                  int32_t *__restrict__ wait_job, int32_t *__restrict__ order) {
     const int lane = threadIdx.x;
     uint32_t clock = *D.clock;
     if (demand) clock += 1;
+    const uint32_t seq = *D.seq + 1;
     __syncwarp();
-    if (lane == 0) *D.clock = clock;
+    if (lane == 0) {
+        *D.clock = clock;
+        *D.seq = seq;
+    }
+    // first every requested expert already resident takes this call's stamp, so that no miss
+    // below can evict it
+    for (int i = lane; i < n_ids; i += 32) {
+        const int e = ids[i];
+        if (e < 0 || e >= E) continue;
+        const int s = D.map[layer * E + e];
+        if (s >= 0) D.tick[s] = clock;
+    }
+    __syncwarp();
     int n_jobs = 0;
     unsigned long long hits = 0, misses = 0;
     for (int i = 0; i < n_ids; ++i) {
         const int e = ids[i];
-        if (e < 0 || e >= E) continue;
+        if (e < 0 || e >= E) {
+            if (wait_job && lane == 0) wait_job[i] = -1;
+            continue;
+        }
         const int key = layer * E + e;
         const int s = D.map[key];
         __syncwarp();
         if (s >= 0) {
-            if (lane == 0) D.tick[s] = clock;
+            if (lane == 0) {
+                D.tick[s] = clock;
+                // a repeat of an expert this plan is copying waits for the same job
+                if (wait_job) wait_job[i] = D.job_seq[s] == seq ? D.job_of[s] : -1;
+            }
             ++hits;
             __syncwarp();
             continue;
@@ -70,7 +109,10 @@ __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E
             const unsigned long long b = __shfl_xor_sync(0xffffffffu, best, o);
             best = b < best ? b : best;
         }
-        if (best == ~0ull) continue; // every slot is in use by this call: left unplaced
+        if (best == ~0ull) { // every slot is in use by this call: left unplaced
+            if (wait_job && lane == 0) wait_job[i] = -1;
+            continue;
+        }
         const int v = (int)(best & 0xffffffffu);
         if (lane == 0) {
             const int old = D.key_of[v];
@@ -79,10 +121,26 @@ __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E
             D.key_of[v] = key;
             D.tick[v] = clock;
             D.jobs[n_jobs] = make_int2(v, key);
+            D.job_seq[v] = seq;
+            D.job_of[v] = n_jobs;
+            if (wait_job) wait_job[i] = n_jobs;
         }
         ++n_jobs;
         ++misses;
         __syncwarp();
+    }
+    if (order) {
+        __syncwarp();
+        // rank of each position by (wait_job, position): resident ones (-1) first
+        for (int p = lane; p < n_ids; p += 32) {
+            const int kp = wait_job[p];
+            int r = 0;
+            for (int q = 0; q < n_ids; ++q) {
+                const int kq = wait_job[q];
+                r += (kq < kp) || (kq == kp && q < p);
+            }
+            order[r] = p;
+        }
     }
     if (lane == 0) {
         *D.n_jobs = n_jobs;
@@ -97,33 +155,9 @@ __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E
     }
 }
 
-__global__ void __launch_bounds__(256) copy_kernel(BankDevice D, const uint8_t *__restrict__ host, size_t stride) {
-    const int n = *D.n_jobs;
-    const size_t per = stride / 16;
-    const size_t total = per * (size_t)n;
-    const size_t step = (size_t)gridDim.x * blockDim.x;
-    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    // four 16-byte loads in flight per thread before they are stored
-    for (; i + 3 * step < total; i += 4 * step) {
-        uint4 v[4];
-        size_t dst[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const size_t q = i + u * step;
-            const int2 job = D.jobs[q / per];
-            const size_t c = q % per;
-            v[u] = *(reinterpret_cast<const uint4 *>(host + (size_t)job.y * stride) + c);
-            dst[u] = (size_t)job.x * per + c;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) reinterpret_cast<uint4 *>(D.slots)[dst[u]] = v[u];
-    }
-    for (; i < total; i += step) {
-        const int2 job = D.jobs[i / per];
-        const size_t c = i % per;
-        reinterpret_cast<uint4 *>(D.slots)[(size_t)job.x * per + c] =
-            *(reinterpret_cast<const uint4 *>(host + (size_t)job.y * stride) + c);
-    }
+__global__ void __launch_bounds__(bank::kCopyThreads) copy_kernel(BankDevice D, const uint8_t *__restrict__ host,
+                                                                  size_t stride) {
+    bank::copy_jobs(D, host, stride, *D.n_jobs, (int)blockIdx.x, (int)gridDim.x, [](int) {});
 }
 
 } // namespace
@@ -132,11 +166,31 @@ cudaError_t launch_bank_fetch(waste_bank *b, int layer, const int32_t *ids, int 
                               cudaStream_t s) {
     cudaError_t e = cudaStreamWaitEvent(s, demand ? b->ev_lookahead : b->ev_demand, 0);
     if (e != cudaSuccess) return e;
-    plan_kernel<<<1, 32, 0, s>>>(b->D, layer, b->E, b->n_slots, b->stride, ids, n_ids, demand ? 1 : 0);
-    copy_kernel<<<num_sms * 4, 256, 0, s>>>(b->D, b->host, b->stride);
+    const BankDevice D = device_for(b, demand);
+    plan_kernel<<<1, 32, 0, s>>>(D, layer, b->E, b->n_slots, b->stride, ids, n_ids, demand ? 1 : 0, nullptr,
+                                 nullptr);
+    (void)num_sms;
+    copy_kernel<<<bank::kCopyLanes, bank::kCopyThreads, 0, s>>>(D, b->host, b->stride);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return cudaEventRecord(demand ? b->ev_demand : b->ev_lookahead, s);
+}
+
+cudaError_t launch_bank_plan_overlap(waste_bank *b, int layer, const int32_t *ids, int n_ids, int32_t *wait_job,
+                                     int32_t *order, BankLanes *lanes, cudaStream_t s) {
+    if (n_ids > kOverlapMaxSlots) return cudaErrorInvalidValue;
+    cudaError_t e = cudaStreamWaitEvent(s, b->ev_lookahead, 0);
+    if (e != cudaSuccess) return e;
+    const BankDevice D = device_for(b, true);
+    plan_kernel<<<1, 32, 0, s>>>(D, layer, b->E, b->n_slots, b->stride, ids, n_ids, 1, wait_job, order);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    lanes->D = D;
+    lanes->host = b->host;
+    lanes->wait_job = wait_job;
+    lanes->lanes = bank::kCopyLanes;
+    // a lookahead into the next layer may plan from here on: it evicts no slot of this call
+    return cudaEventRecord(b->ev_demand, s);
 }
 
 const uint8_t *bank_host_records(const waste_bank *b, int layer) {
@@ -193,7 +247,7 @@ int waste_bank_create(const waste_moe_config *cfg, int32_t n_layers, const uint8
     b->host = static_cast<const uint8_t *>(dev);
     const size_t keys = (size_t)n_layers * b->E;
     const size_t slot_bytes = (size_t)n_slots * record_stride;
-    const size_t meta = keys * 4 + (size_t)n_slots * (4 + 4 + 8) + 256 + kBankStatCount * 8;
+    const size_t meta = keys * 4 + (size_t)n_slots * (4 + 4 + 8 + 8 + 4 + 4) + 256 + kBankStatCount * 8;
     void *mem = nullptr;
     e = cudaMalloc(&mem, slot_bytes + round_up(meta, 256) + 256);
     if (e != cudaSuccess) {
@@ -211,10 +265,20 @@ int waste_bank_create(const waste_moe_config *cfg, int32_t n_layers, const uint8
     p += round_up((size_t)n_slots * 4, 16);
     b->D.tick = reinterpret_cast<uint32_t *>(p);
     p += round_up((size_t)n_slots * 4, 16);
-    b->D.jobs = reinterpret_cast<int2 *>(p);
+    b->jobs[0] = reinterpret_cast<int2 *>(p);
     p += round_up((size_t)n_slots * 8, 16);
+    b->jobs[1] = reinterpret_cast<int2 *>(p);
+    p += round_up((size_t)n_slots * 8, 16);
+    b->D.jobs = b->jobs[0];
+    b->D.job_seq = reinterpret_cast<uint32_t *>(p);
+    p += round_up((size_t)n_slots * 4, 16);
+    b->D.job_of = reinterpret_cast<int32_t *>(p);
+    p += round_up((size_t)n_slots * 4, 16);
     b->D.clock = reinterpret_cast<uint32_t *>(p);
-    b->D.n_jobs = reinterpret_cast<int32_t *>(p + 4);
+    b->n_jobs[0] = reinterpret_cast<int32_t *>(p + 4);
+    b->D.seq = reinterpret_cast<uint32_t *>(p + 8);
+    b->n_jobs[1] = reinterpret_cast<int32_t *>(p + 12);
+    b->D.n_jobs = b->n_jobs[0];
     p += 16;
     b->D.stats = reinterpret_cast<unsigned long long *>(p);
     b->ev_demand = b->ev_lookahead = nullptr;
@@ -250,6 +314,7 @@ int waste_bank_reset(waste_bank *b) {
     if (e == cudaSuccess) e = cudaMemset(b->D.map, 0xff, keys * 4);
     if (e == cudaSuccess) e = cudaMemset(b->D.key_of, 0xff, (size_t)b->n_slots * 4);
     if (e == cudaSuccess) e = cudaMemset(b->D.tick, 0, (size_t)b->n_slots * 4);
+    if (e == cudaSuccess) e = cudaMemset(b->D.job_seq, 0, (size_t)b->n_slots * 4);
     if (e == cudaSuccess) e = cudaMemset(b->D.clock, 0, 16);
     if (e == cudaSuccess) e = cudaMemset(b->D.stats, 0, kBankStatCount * 8);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();

@@ -88,9 +88,21 @@ struct BankDevice {
     int32_t *key_of;      // [n_slots] slot -> layer * E + expert, or -1
     uint32_t *tick;       // [n_slots] clock of the last call that used the slot
     int2 *jobs;           // [n_slots] copy jobs of the last plan: (slot, key)
+    uint32_t *job_seq;    // [n_slots] plan that last made the slot a copy job
+    int32_t *job_of;      // [n_slots] its job index in that plan
     uint32_t *clock;      // advanced by every demand fetch
     int32_t *n_jobs;
+    uint32_t *seq;        // advanced by every plan
     unsigned long long *stats;
+};
+// The copy of a demand fetch run by the persistent step kernel beside the expert units:
+// lanes CTAs copy the plan's jobs chunk by chunk, and every unit of a slot whose record is
+// being copied (wait_job[slot] >= 0) waits for that job's chunks first.
+struct BankLanes {
+    BankDevice D;
+    const uint8_t *host; // device-usable address of the host records
+    const int32_t *wait_job; // [slots] job the slot's record arrives by, or -1
+    int lanes;
 };
 enum { kBankDemandHits = 0, kBankDemandMisses, kBankPrefetchCopies, kBankPrefetchPresent, kBankCopiedBytes,
        kBankStatCount };
@@ -122,7 +134,9 @@ struct Workspace {
     float *part_dn;      // [max_slots][(dn.nseg + 1) / 2][d]; tensor-core slots use part 0
     unsigned long long *stats; // [kStatCount]
     uint32_t *err;       // sticky error bits
-    unsigned *sync;      // fused-step queue and counters [4 + max_slots + kMaxFusedRowBlocks], zero at rest
+    unsigned *sync;      // fused-step queue and counters [4 + 2 max_slots + kMaxFusedRowBlocks], zero at rest
+    int32_t *bank_wait;  // [max_slots] banked calls: job each slot's record arrives by, or -1
+    int32_t *bank_order; // [max_slots] banked calls: slots in the order their units run
     Grouping grp;        // batched calls only (null pointers when max_tokens == 1)
     float *router_part;  // [kRouterMaxSplits][max_T][E] when max_T > 16, else null
     void *base;
@@ -182,7 +196,8 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
                               const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
                               float *out, int mode, bool reconstruct, int num_sms,
                               cudaStream_t s, unsigned long long *trace = nullptr,
-                              int trace_cap = 0);
+                              int trace_cap = 0, const BankLanes *lanes = nullptr,
+                              const int32_t *slot_order = nullptr);
 cudaError_t launch_prefetch_l2(const LayerView &L, const int32_t *pred_idx, int pred_stride,
                                int T, int P, int32_t *pred_count, unsigned long long *stats,
                                cudaStream_t s);
@@ -213,6 +228,14 @@ int device_sm_count();
 // clock advances and hits / misses are counted; lookahead: slots of the call in flight stay).
 cudaError_t launch_bank_fetch(waste_bank *b, int layer, const int32_t *ids, int n_ids, bool demand, int num_sms,
                               cudaStream_t s);
+// A demand fetch whose copy runs inside the persistent step kernel: the plan alone (after the
+// bank's last lookahead), which also writes for each of the n_ids slots the job its record
+// arrives by (wait_job, -1: resident) and an order of the slots -- resident ones first, then
+// by job -- for the units (order).  n_ids <= kOverlapMaxSlots.  The caller then launches the
+// step kernel with *lanes on the same stream.
+constexpr int kOverlapMaxSlots = 64;
+cudaError_t launch_bank_plan_overlap(waste_bank *b, int layer, const int32_t *ids, int n_ids, int32_t *wait_job,
+                                     int32_t *order, BankLanes *lanes, cudaStream_t s);
 const uint8_t *bank_host_records(const waste_bank *b, int layer);
 const uint8_t *bank_slots(const waste_bank *b);
 const int32_t *bank_slot_map(const waste_bank *b, int layer);

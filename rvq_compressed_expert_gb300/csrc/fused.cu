@@ -3,7 +3,14 @@
 // gate-weighted combine, in one launch.
 //
 // Work items are claimed from a device-side queue in a fixed order:
-//   [router items][top-k item][gate/up units][down units][combine items]
+//   [router items][top-k item][copy lanes][gate/up units][down units][combine items]
+// Copy lanes exist for a call on a tiered bank whose demand copies run in this kernel
+// (page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Architecture de
+// streaming depuis le disque": the expert reads overlap the compute, which consumes each
+// expert as it arrives).  The lanes copy the missing records job by job, chunk by chunk,
+// and count the chunks of each job; the units of a slot whose record is on its way wait for
+// its count, while the units of resident experts -- ordered first -- run beside the copy.
+// A copy lane does not claim its next item before it finishes, so it holds no unit back.
 // A CTA claims one item ahead of the one it runs, so the next unit's codes and
 // codebooks can be fetched while the current one streams.  An item waits only on
 // items that precede it in the queue (top-k on all router items, gate/up units on
@@ -15,6 +22,9 @@
 // records kErrTimeout if it gives up.  The last CTA to leave resets the counters
 // for the next launch.  The arithmetic of each item is that of the per-phase
 // kernels, in the same order: results are bit-identical to them.
+#include <cstring>
+
+#include "bank_dev.cuh"
 #include "lut_dev.cuh"
 #include "route_dev.cuh"
 
@@ -28,6 +38,7 @@ namespace {
 constexpr int kRouterRowsPerItem = kThreads / 128; // 4 expert rows per router item
 constexpr int kCombineRows = kThreads;              // output rows per combine item
 constexpr int kMaxFusedExperts = 1024;              // top-k of the step kernel sorts <= 1024 keys
+static_assert(kThreads == bank::kCopyThreads, "a copy lane is one CTA of the step kernel");
 
 struct FusedArgs {
     LutArgs A; // lookup units; A.idx is where the top-k item writes the routing
@@ -48,9 +59,12 @@ struct FusedArgs {
     int mode;
     // queue and counters (zero at rest):
     // [0] next item, [1] CTAs that left, [2] router items done, [3] top-k done,
-    // [4, 4 + slots) gate/up units done per slot, then down units done per row block
+    // [4, 4 + slots) gate/up units done per slot, then down units done per row block, then
+    // chunks copied per copy job (banked calls)
     unsigned *sync;
-    int n_router, n_topk, n_gu, n_dn, n_comb;
+    int n_router, n_topk, n_copy, n_gu, n_dn, n_comb;
+    BankLanes bank;          // n_copy > 0 only
+    int bank_copiers;        // copy lanes that count themselves on each job
     // optional item trace: per item {start ns, end ns, SM id, CTA} (null = off)
     unsigned long long *trace;
     int trace_cap;
@@ -147,14 +161,39 @@ __device__ __noinline__ void combine_item(const FusedArgs &F, int r0, int r1) {
 // Queue layout helpers: item boundaries and counters are recomputed from the
 // kernel parameters where needed, so little state stays live across a unit.
 __device__ __forceinline__ int b_topk(const FusedArgs &F) { return F.n_router; }
-__device__ __forceinline__ int b_gu(const FusedArgs &F) { return F.n_router + F.n_topk; }
+__device__ __forceinline__ int b_copy(const FusedArgs &F) { return F.n_router + F.n_topk; }
+__device__ __forceinline__ int b_gu(const FusedArgs &F) { return b_copy(F) + F.n_copy; }
 __device__ __forceinline__ int b_dn(const FusedArgs &F) { return b_gu(F) + F.n_gu; }
 __device__ __forceinline__ int b_comb(const FusedArgs &F) { return b_dn(F) + F.n_dn; }
 __device__ __forceinline__ int n_total(const FusedArgs &F) { return b_comb(F) + F.n_comb; }
 __device__ __forceinline__ unsigned *gu_done(const FusedArgs &F) { return F.sync + 4; }
 __device__ __forceinline__ unsigned *dn_done(const FusedArgs &F) { return F.sync + 4 + F.A.slots; }
+__device__ __forceinline__ unsigned *job_done(const FusedArgs &F) { return F.sync + 4 + F.A.slots + F.A.nrb; }
+template <bool kBanked>
+__device__ __forceinline__ bool is_copy(const FusedArgs &F, int item) {
+    return kBanked && item >= b_copy(F) && item < b_gu(F);
+}
 
-template <bool kRecon, bool kBf16>
+// Copy lane `lane`: chunks lane, lane + n_copy, ... of the plan's jobs, so the lanes finish
+// the jobs in order; a lane counts itself on a job after its last chunk of the job.
+__device__ __noinline__ void copy_item(const FusedArgs &F, int lane) {
+    unsigned *done = job_done(F);
+    bank::copy_jobs(F.bank.D, F.bank.host, F.A.stride, *F.bank.D.n_jobs, lane, F.n_copy,
+                    [&](int j) { signal(done + j); });
+}
+
+// Before any code of `slot` is read: wait until its record, if it is being copied, is in.
+template <bool kBanked>
+__device__ __forceinline__ void wait_record(const FusedArgs &F, int slot) {
+    if (kBanked) {
+        const int j = F.bank.wait_job[slot];
+        if (j >= 0) wait_counter(job_done(F) + j, (unsigned)F.bank_copiers, F.A.err);
+    }
+}
+
+// kBanked: a call on a tiered bank with copy lanes (its own instance, so the copy code adds
+// nothing to the registers of the resident-record instances)
+template <bool kRecon, bool kBf16, bool kBanked>
 __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs F) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ float red[kRouterRowsPerItem][4][kRouterTok];
@@ -162,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
     int par = 0;
     bool primed = false;
     int cur = claim(F.sync, &claimed);
-    int nxt = claim(F.sync, &claimed);
+    int nxt = is_copy<kBanked>(F, cur) ? -1 : claim(F.sync, &claimed);
     while (cur < n_total(F)) {
         unsigned long long t_start = 0;
         if (F.trace && threadIdx.x == 0) t_start = globaltimer();
@@ -170,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             // ---- router rows
             router_item<kBf16>(F, cur, red);
             signal(F.sync + 2);
-        } else if (cur < b_gu(F)) {
+        } else if (cur < b_copy(F)) {
             // ---- top-k + softmax of every token, one warp per token
             wait_counter(F.sync + 2, (unsigned)F.n_router, F.A.err);
             topk_item(F);
@@ -179,10 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
                 __threadfence();
                 atomicExch(F.sync + 3, 1u);
             }
+        } else if (cur < b_gu(F)) {
+            // ---- copy lane of a banked call
+            if constexpr (kBanked) copy_item(F, cur - b_copy(F));
         } else if (cur < b_dn(F)) {
             // ---- gate/up unit
             if (F.with_route) wait_counter(F.sync + 3, 1u, F.A.err);
             const Unit U = decode_unit<false>(F.A, cur - b_gu(F));
+            wait_record<kBanked>(F, U.slot);
             const bool has_next = nxt >= b_gu(F) && nxt < b_dn(F);
             Unit N;
             if (has_next) N = decode_unit<false>(F.A, nxt - b_gu(F));
@@ -193,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             if (F.with_route) wait_counter(F.sync + 3, 1u, F.A.err);
             const int u = cur - b_dn(F);
             const Unit U = decode_unit<true>(F.A, u);
+            wait_record<kBanked>(F, U.slot);
             const bool has_next = nxt >= b_dn(F) && nxt < b_comb(F);
             Unit N;
             if (has_next) N = decode_unit<true>(F.A, nxt - b_dn(F));
@@ -218,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             e[2] = smid();
             e[3] = blockIdx.x;
         }
-        cur = nxt;
-        nxt = claim(F.sync, &claimed);
+        cur = nxt >= 0 ? nxt : claim(F.sync, &claimed);
+        nxt = is_copy<kBanked>(F, cur) ? -1 : claim(F.sync, &claimed);
     }
     if constexpr (!kRecon) cp_async_wait<0>();
     // the last CTA to leave puts the queue and counters back to zero
@@ -229,25 +273,30 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
         const unsigned left = atomicAdd(F.sync + 1, 1u);
         if (left == gridDim.x - 1) {
             __threadfence();
-            const int n = 4 + F.A.slots + F.A.nrb;
+            const int n = 4 + F.A.slots + F.A.nrb + (F.n_copy ? F.A.slots : 0);
             for (int i = 0; i < n; ++i) F.sync[i] = 0u;
             __threadfence();
         }
     }
 }
 
-template <bool kRecon, bool kBf16>
+template <bool kRecon, bool kBf16, bool kBanked>
 cudaError_t launch_fused_t(const FusedArgs &F, int grid, cudaStream_t s) {
     const size_t smem = unit_smem<kRecon>();
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(fused_step_kernel<kRecon, kBf16>,
+        cudaError_t e = cudaFuncSetAttribute(fused_step_kernel<kRecon, kBf16, kBanked>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    fused_step_kernel<kRecon, kBf16><<<grid, kThreads, smem, s>>>(F);
+    fused_step_kernel<kRecon, kBf16, kBanked><<<grid, kThreads, smem, s>>>(F);
     return cudaGetLastError();
+}
+
+template <bool kRecon, bool kBf16>
+cudaError_t launch_fused_b(const FusedArgs &F, int grid, cudaStream_t s) {
+    return F.n_copy ? launch_fused_t<kRecon, kBf16, true>(F, grid, s) : launch_fused_t<kRecon, kBf16, false>(F, grid, s);
 }
 
 } // namespace
@@ -264,7 +313,8 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
                               bool with_route, int32_t *idx, float *gate, float *logits,
                               const int32_t *pred_idx, int32_t *pred_count, int pred_stride,
                               float *out, int mode, bool reconstruct, int num_sms,
-                              cudaStream_t s, unsigned long long *trace, int trace_cap) {
+                              cudaStream_t s, unsigned long long *trace, int trace_cap,
+                              const BankLanes *lanes, const int32_t *slot_order) {
     FusedArgs F;
     F.trace = trace;
     F.trace_cap = trace_cap;
@@ -290,7 +340,7 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
     A.part_dn = W.part_dn;
     A.stats = W.stats;
     A.err = W.err;
-    A.slot_list = nullptr;
+    A.slot_list = slot_order; // a permutation of the call's slots (the unit counts stay)
     A.n_list = nullptr;
     A.trace = nullptr;
     A.trace_cap = 0;
@@ -315,14 +365,21 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
     F.sync = W.sync;
     F.n_router = with_route ? (L.E + kRouterRowsPerItem - 1) / kRouterRowsPerItem : 0;
     F.n_topk = with_route ? 1 : 0;
+    F.n_copy = lanes ? lanes->lanes : 0;
+    if (lanes) F.bank = *lanes;
+    else memset(&F.bank, 0, sizeof F.bank);
+    F.bank_copiers = bank::copiers_per_job(L.stride, F.n_copy);
     F.n_gu = A.slots * A.gu.nseg;
     F.n_dn = A.slots * A.npair * A.nrb;
     F.n_comb = (L.d + kCombineRows - 1) / kCombineRows;
-    const int total = F.n_router + F.n_topk + F.n_gu + F.n_dn + F.n_comb;
-    const int grid = total < num_sms ? total : num_sms;
+    const int total = F.n_router + F.n_topk + F.n_copy + F.n_gu + F.n_dn + F.n_comb;
+    // a banked call leaves as many SMs as it has copy lanes to the lookahead into the next
+    // layer, whose copy kernel then runs beside this one
+    const int cap = lanes ? max(1, num_sms - F.n_copy) : num_sms;
+    const int grid = total < cap ? total : cap;
     const bool bf16 = L.act_bf16 != 0;
-    if (reconstruct) return bf16 ? launch_fused_t<true, true>(F, grid, s) : launch_fused_t<true, false>(F, grid, s);
-    return bf16 ? launch_fused_t<false, true>(F, grid, s) : launch_fused_t<false, false>(F, grid, s);
+    if (reconstruct) return bf16 ? launch_fused_b<true, true>(F, grid, s) : launch_fused_b<true, false>(F, grid, s);
+    return bf16 ? launch_fused_b<false, true>(F, grid, s) : launch_fused_b<false, false>(F, grid, s);
 }
 
 } // namespace wm

@@ -79,6 +79,10 @@ WORKLOADS = {
     # 92 MoE layers x 64 resident experts, one token, residual h += combine, lookahead 6
     "stack": Workload("stack", 7168, 1536, 64, 16, 1, "f32", "offsets", n_layers=92,
                       lookahead=6, seeds=tuple(range(10))),
+    # 16 MoE layers x 64 experts behind a tiered bank (records in host memory, an HBM cache),
+    # one token, Zipf(1.1) expert popularity, lookahead 6
+    "tiered": Workload("tiered", 7168, 1536, 64, 16, 1, "f32", "zipf", n_layers=16,
+                       lookahead=6, seeds=tuple(range(10))),
     # batched decode: 128 tokens, bf16 h, Zipf(1.1) expert popularity via router bias
     "batched": Workload("batched", 7168, 1536, 384, 16, 128, "bf16", "zipf",
                         seeds=tuple(range(10))),

@@ -54,12 +54,15 @@ def resident_outputs(tokens, lookahead):
             l.close()
 
 
+@pytest.mark.parametrize("flags", [0, B.FLAG_BANK_SERIAL], ids=["overlap", "serial"])
 @pytest.mark.parametrize("lookahead", [0, 3])
-def test_banked_equals_resident(lookahead):
+def test_banked_equals_resident(lookahead, flags):
     """6 slots for 4 layers x top-4: every layer evicts; outputs equal the resident stack's bit
-    for bit; hits + misses count every routed expert; bytes copied = copies x record stride."""
+    for bit, whether each expert is consumed as its copy lands (the step kernel's copy lanes)
+    or after the whole copy; hits + misses count every routed expert; bytes copied = copies x
+    record stride."""
     ref = resident_outputs(5, lookahead)
-    ts = TieredStack(W, 0, W.n_layers, 6)
+    ts = TieredStack(W, 0, W.n_layers, 6, flags=flags)
     try:
         got = run_tokens(DecodeStack(ts.layers, W.tokens, banked=True), 5, lookahead)
         for a, b in zip(got, ref):
@@ -108,3 +111,55 @@ def test_bank_refusals():
     with pytest.raises(B.WasteError) as ei:  # not 4096-aligned
         B.waste_bank_create(cfg, 1, host[16:], stride, 4)
     assert ei.value.status == -4
+
+
+@pytest.mark.parametrize("flags", [0, B.FLAG_BANK_SERIAL], ids=["overlap", "serial"])
+def test_repeated_expert_across_tokens(flags):
+    """Two tokens share experts that are not resident: each is copied once, the second token's
+    units wait for the same copy (overlap) -- outputs equal the resident layer's."""
+    w2 = synth.Workload("bank2", 512, 256, 12, 4, 2, "f32", "none")
+    res = MoELayer(w2, 1, 0, "cuda")
+    ts = TieredStack(w2, 1, 1, 8, flags=flags)
+    try:
+        h = synth.hidden(4, 2, w2.d, "f32", "cuda")
+        gate = torch.rand(2, 4, device="cuda")
+        for ids, misses in (([[5, 1, 2, 3], [5, 6, 1, 0]], 6), ([[7, 6, 9, 5], [9, 11, 7, 2]], 9)):
+            idx = torch.tensor(ids, dtype=torch.int32, device="cuda")
+            a = torch.empty(2, w2.d, device="cuda")
+            b = torch.empty(2, w2.d, device="cuda")
+            ts.layers[0].forward(h, 2, idx, gate, a)
+            res.forward(h, 2, idx, gate, b)
+            torch.cuda.synchronize()
+            assert torch.equal(a, b)
+            assert ts.stats()["demand_misses"] == misses, (ids, ts.stats())
+        ts.layers[0].stats()
+    finally:
+        ts.close()
+        res.close()
+
+
+def test_plan_keeps_resident_experts_of_the_call():
+    """4 slots, experts given to forward: {0,1,2,3} fills the cache; [4,0,1,2] then copies
+    expert 4 alone, into the slot of 3 -- a miss listed before resident experts of the same
+    call must not evict them.  Outputs equal the resident layer's."""
+    w1 = synth.Workload("bank1", 512, 256, 8, 4, 1, "f32", "none")
+    res = MoELayer(w1, 0, 0, "cuda")
+    ts = TieredStack(w1, 0, 1, 4)
+    try:
+        h = synth.hidden(3, 1, w1.d, "f32", "cuda")
+        gate = torch.full((1, 4), 0.25, device="cuda")
+        for ids, misses in (([0, 1, 2, 3], 4), ([4, 0, 1, 2], 5), ([2, 3, 4, 1], 6)):
+            idx = torch.tensor([ids], dtype=torch.int32, device="cuda")
+            a = torch.empty(1, w1.d, device="cuda")
+            b = torch.empty(1, w1.d, device="cuda")
+            ts.layers[0].forward(h, 1, idx, gate, a)
+            res.forward(h, 1, idx, gate, b)
+            torch.cuda.synchronize()
+            assert torch.equal(a, b)
+            st = ts.stats()
+            assert st["demand_misses"] == misses, (ids, st)
+        # after [4,0,1,2] the cache held {4,0,1,2}: [2,3,4,1] misses only expert 3, evicting 0
+        assert st["demand_hits"] == 12 - 6
+    finally:
+        ts.close()
+        res.close()
