@@ -328,11 +328,14 @@ int waste_bank_stats(const waste_bank *bank, waste_bank_stats_t *out);
  * A call on the table-lookup path with T * top_k <= 64 (decode) runs its demand copy inside
  * the persistent step kernel: a few CTAs copy the missing records in order while the others
  * run the resident experts' units and then each missing expert's as soon as its record is in
- * (the pages' read/compute overlap); WASTE_FLAG_BANK_SERIAL turns this off.
- * Fetches of one bank never overlap: each demand fetch waits for the bank's last lookahead
- * fetch and each lookahead fetch for its last demand fetch (events held by the bank), on
- * whatever streams they are issued.  Issue a layer's forward before the lookahead into the
- * next layer, so that the lookahead's copies run beside the forward's expert kernels.
+ * (page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Lecture anticipée et
+ * prédiction du routeur": the compute consumes each expert as it arrives);
+ * WASTE_FLAG_BANK_SERIAL turns this off.
+ * The fetches of one bank are ordered by events the bank holds, on whatever streams they are
+ * issued: each demand fetch waits for the bank's last lookahead fetch, and each lookahead
+ * fetch for the last demand fetch (its plan, when the copy runs in the step kernel; a
+ * lookahead never evicts an expert of the call in flight).  Issue a layer's forward before
+ * the lookahead into the next layer, so that the lookahead's copies run beside the forward.
  * These waits use events recorded by earlier calls, so banked layers are not for stream
  * capture into CUDA graphs. */
 int waste_moe_create_banked(const waste_moe_config *cfg, const float *d_router_w,

@@ -5,9 +5,9 @@
 // Work items are claimed from a device-side queue in a fixed order:
 //   [router items][top-k item][copy lanes][gate/up units][down units][combine items]
 // Copy lanes exist for a call on a tiered bank whose demand copies run in this kernel
-// (page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Architecture de
-// streaming depuis le disque": the expert reads overlap the compute, which consumes each
-// expert as it arrives).  The lanes copy the missing records job by job, chunk by chunk,
+// (page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Lecture anticipée et
+// prédiction du routeur": each of a layer's expert reads is issued on its own and the
+// compute consumes each expert as it arrives, with the work and cache statistics unchanged).  The lanes copy the missing records job by job, chunk by chunk,
 // and count the chunks of each job; the units of a slot whose record is on its way wait for
 // its count, while the units of resident experts -- ordered first -- run beside the copy.
 // A copy lane does not claim its next item before it finishes, so it holds no unit back.
