@@ -61,6 +61,12 @@ def _bind(lib):
     lib.oracle_expert_code_bytes.argtypes = [_i, _i]
     lib.oracle_expert_code_bytes.restype = ctypes.c_uint64
     lib.oracle_crc32.argtypes = [_u8p, ctypes.c_size_t]
+    lib.oracle_rvq_nearest.argtypes = [_fp, _fp]
+    lib.oracle_rvq_nearest.restype = ctypes.c_int
+    lib.oracle_rvq_train.argtypes = [_i, _i, _fp, _i32p, _i, _fp, _u8p, _dp]
+    lib.oracle_rvq_train.restype = ctypes.c_int
+    lib.oracle_rvq_encode.argtypes = [_i, _i, _fp, _fp, _u8p, _dp]
+    lib.oracle_rvq_encode.restype = ctypes.c_int
     lib.oracle_crc32.restype = ctypes.c_uint32
     return lib
 
@@ -268,3 +274,43 @@ def topk_margin(logits, k):
     if m < 2:
         return float("inf")
     return float(np.min(l[: m - 1] - l[1:m]))
+
+
+def rvq_nearest(x, C) -> int:
+    """Index of the codebook row of C [256, 8] nearest to x [8] (fp32 distance, lower index on
+    ties)."""
+    x = _np(x, np.float32)
+    C = _np(C, np.float32)
+    return int(_load().oracle_rvq_nearest(_ptr(x, ctypes.c_float), _ptr(C, ctypes.c_float)))
+
+
+def rvq_train(W, init, iters: int):
+    """Greedy residual k-means of W [rows, cols] fp32: returns (codebooks [3,256,8] fp32, codes
+    [rows,3,cols/8] u8, err [3] float64 = sum of squared residuals after each stage).  init
+    [3,256] int32: the vector index each stage's centroids start from.  Raises ValueError on
+    refused inputs."""
+    W = _np(W, np.float32)
+    init = _np(init, np.int32)
+    rows, cols = W.shape
+    cb = np.zeros((3, 256, 8), np.float32)
+    codes = np.zeros((rows, 3, max(cols // 8, 0)), np.uint8)
+    err = np.zeros(3, np.float64)
+    rc = _load().oracle_rvq_train(rows, cols, _ptr(W, ctypes.c_float), _ptr(init, ctypes.c_int32), int(iters),
+                                  _ptr(cb, ctypes.c_float), _ptr(codes, ctypes.c_uint8), _ptr(err, ctypes.c_double))
+    if rc:
+        raise ValueError("rvq_train refused its inputs")
+    return cb, codes, err
+
+
+def rvq_encode(W, cb):
+    """The three nearest-codebook assignments of W with given codebooks: (codes, err)."""
+    W = _np(W, np.float32)
+    cb = _np(cb, np.float32)
+    rows, cols = W.shape
+    codes = np.zeros((rows, 3, max(cols // 8, 0)), np.uint8)
+    err = np.zeros(3, np.float64)
+    rc = _load().oracle_rvq_encode(rows, cols, _ptr(W, ctypes.c_float), _ptr(cb, ctypes.c_float),
+                                   _ptr(codes, ctypes.c_uint8), _ptr(err, ctypes.c_double))
+    if rc:
+        raise ValueError("rvq_encode refused its inputs")
+    return codes, err

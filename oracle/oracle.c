@@ -270,3 +270,137 @@ uint32_t oracle_crc32(const uint8_t *p, size_t n) {
     }
     return ~c;
 }
+
+/*
+ * RVQ encoder: codes and codebooks for a dense matrix ([fr] "Quantification et exactitude":
+ * 3 residual stages of 256 eight-dimensional vectors; the pages' converter is named there but
+ * its training is not described).  Reading taken -- greedy residual k-means:
+ *   the residual R starts as W; for stage s = 0, 1, 2:
+ *     C[c] = R[init[s][c]] for c < 256 (vector indices drawn by the caller);
+ *     `iters` Lloyd rounds: every vector goes to its nearest centroid, then every centroid
+ *       with members becomes their mean (an empty one keeps its value);
+ *     one more assignment with the final C gives the stage's codes, and R <- R - C[code].
+ * Nearest: least d(x, c) = sum over v = 0..7 of (x_v - c_v)^2, accumulated in that order in
+ *   fp32 with one fused multiply-add per term (a code is an integer decided by floating point,
+ *   so the device takes it in the same precision); ties go to the lower index.
+ * Mean: each member component in fixed point, q = round-to-nearest(x * 2^40) as int64, so
+ *   the sums are exact in any order; mean = (float)(((double)sum / count) * 2^-40).
+ * Vector j of row r of W [rows][cols] (fp32 row-major) covers columns 8j..8j+7; it is vector
+ * r*nv + j.  cb [3][256][8]; codes [rows][3][nv]; err[s] = sum of the squared residual
+ * components after stage s (double, in vector order).  Returns 0, or -1 when cols % 8 != 0,
+ * an init index is out of range, or a weight is not finite or has |w| >= 2^22.
+ */
+#define OR_FIX 1099511627776.0 /* 2^40 */
+
+int oracle_rvq_nearest(const float *x, const float *C) {
+    int best = 0;
+    float bd = INFINITY;
+    for (int c = 0; c < OR_K; ++c) {
+        float d = 0.0f;
+        for (int v = 0; v < OR_V; ++v) {
+            float t = x[v] - C[(size_t)c * OR_V + v];
+            d = fmaf(t, t, d);
+        }
+        if (d < bd) {
+            bd = d;
+            best = c;
+        }
+    }
+    return best;
+}
+
+static void rvq_means(size_t n, const float *R, const uint8_t *code, float *C) {
+    int64_t sum[OR_K][OR_V];
+    int64_t cnt[OR_K];
+    memset(sum, 0, sizeof sum);
+    memset(cnt, 0, sizeof cnt);
+    for (size_t i = 0; i < n; ++i) {
+        int c = code[i];
+        cnt[c] += 1;
+        for (int v = 0; v < OR_V; ++v) sum[c][v] += (int64_t)llrint((double)R[i * OR_V + v] * OR_FIX);
+    }
+    for (int c = 0; c < OR_K; ++c) {
+        if (cnt[c] == 0) continue;
+        for (int v = 0; v < OR_V; ++v)
+            C[(size_t)c * OR_V + v] = (float)(((double)sum[c][v] / (double)cnt[c]) * (1.0 / OR_FIX));
+    }
+}
+
+/* codes of one stage with the stage's codebook C, then R <- R - C[code]; returns sum R^2 */
+static double rvq_apply_stage(size_t n, float *R, const float *C, uint8_t *code) {
+    double e = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        int c = oracle_rvq_nearest(R + i * OR_V, C);
+        code[i] = (uint8_t)c;
+        for (int v = 0; v < OR_V; ++v) {
+            R[i * OR_V + v] = R[i * OR_V + v] - C[(size_t)c * OR_V + v];
+            e += (double)R[i * OR_V + v] * (double)R[i * OR_V + v];
+        }
+    }
+    return e;
+}
+
+static int rvq_check(int rows, int cols, const float *W) {
+    if (rows < 0 || cols < 0 || cols % OR_V) return -1;
+    for (size_t i = 0; i < (size_t)rows * (size_t)cols; ++i)
+        if (!(fabsf(W[i]) < 4194304.0f)) return -1; /* also refuses NaN */
+    return 0;
+}
+
+static void rvq_scatter_codes(int rows, int nv, int s, const uint8_t *code, uint8_t *codes) {
+    for (int r = 0; r < rows; ++r)
+        for (int j = 0; j < nv; ++j) codes[code_index(nv, r, s, j)] = code[(size_t)r * nv + j];
+}
+
+int oracle_rvq_train(int rows, int cols, const float *W, const int32_t *init, int iters, float *cb,
+                     uint8_t *codes, double *err) {
+    if (rvq_check(rows, cols, W) || iters < 0) return -1;
+    const int nv = cols / OR_V;
+    const size_t n = (size_t)rows * (size_t)nv;
+    for (int i = 0; i < OR_STAGES * OR_K; ++i)
+        if (init[i] < 0 || (size_t)init[i] >= n) return -1;
+    float *R = malloc(n * OR_V * sizeof(float) + 1);
+    uint8_t *code = malloc(n + 1);
+    if (!R || !code) {
+        free(R);
+        free(code);
+        return -1;
+    }
+    memcpy(R, W, n * OR_V * sizeof(float));
+    for (int s = 0; s < OR_STAGES; ++s) {
+        float *C = cb + (size_t)s * OR_K * OR_V;
+        for (int c = 0; c < OR_K; ++c)
+            for (int v = 0; v < OR_V; ++v) C[(size_t)c * OR_V + v] = R[(size_t)init[s * OR_K + c] * OR_V + v];
+        for (int it = 0; it < iters; ++it) {
+            for (size_t i = 0; i < n; ++i) code[i] = (uint8_t)oracle_rvq_nearest(R + i * OR_V, C);
+            rvq_means(n, R, code, C);
+        }
+        err[s] = rvq_apply_stage(n, R, C, code);
+        rvq_scatter_codes(rows, nv, s, code, codes);
+    }
+    free(R);
+    free(code);
+    return 0;
+}
+
+/* The three final assignments alone, with given codebooks cb [3][256][8]. */
+int oracle_rvq_encode(int rows, int cols, const float *W, const float *cb, uint8_t *codes, double *err) {
+    if (rvq_check(rows, cols, W)) return -1;
+    const int nv = cols / OR_V;
+    const size_t n = (size_t)rows * (size_t)nv;
+    float *R = malloc(n * OR_V * sizeof(float) + 1);
+    uint8_t *code = malloc(n + 1);
+    if (!R || !code) {
+        free(R);
+        free(code);
+        return -1;
+    }
+    memcpy(R, W, n * OR_V * sizeof(float));
+    for (int s = 0; s < OR_STAGES; ++s) {
+        err[s] = rvq_apply_stage(n, R, cb + (size_t)s * OR_K * OR_V, code);
+        rvq_scatter_codes(rows, nv, s, code, codes);
+    }
+    free(R);
+    free(code);
+    return 0;
+}

@@ -298,4 +298,122 @@ def pin_crc32():
         assert oracle.crc32(a) == zlib.crc32(a.tobytes())
 
 
+def _rvq_data(rng, rows, cols, scale=0.02):
+    return (rng.standard_normal((rows, cols)) * scale).astype(np.float32)
+
+
+def pin_rvq_nearest():
+    """Nearest codebook row: equals the float64 argmin wherever the best two distances are
+    apart by more than fp32 rounding; a row equal to x wins with distance 0; among equal rows
+    the lower index wins."""
+    rng = np.random.default_rng(21)
+    checked = 0
+    for _ in range(300):
+        C = rng.standard_normal((256, 8)).astype(np.float32)
+        x = rng.standard_normal(8).astype(np.float32)
+        d = ((x.astype(np.float64) - C.astype(np.float64)) ** 2).sum(1)
+        o = np.argsort(d)
+        if d[o[1]] - d[o[0]] > 1e-5 * d[o[1]]:
+            assert oracle.rvq_nearest(x, C) == o[0]
+            checked += 1
+    assert checked > 250
+    C = rng.standard_normal((256, 8)).astype(np.float32)
+    assert oracle.rvq_nearest(C[77], C) == 77
+    C[200] = C[31]
+    assert oracle.rvq_nearest(C[31] + np.float32(1e-3), C) == 31
+    C[:] = C[5]
+    assert oracle.rvq_nearest(rng.standard_normal(8).astype(np.float32), C) == 0
+
+
+def pin_rvq_exact_for_few_distinct_vectors():
+    """A matrix built from 200 distinct vectors, each stage-0 centroid started on one of them:
+    stage 0 reproduces every vector exactly (residual 0, later stages add zeros), so the codes
+    dequantise to W exactly and each code names a row equal to its vector."""
+    rng = np.random.default_rng(22)
+    base = (rng.standard_normal((200, 8)) * 0.05).astype(np.float32)
+    pick = rng.integers(0, 200, 24 * 40)
+    pick[:200] = rng.permutation(200)
+    W = base[pick].reshape(24, 320)
+    first = {int(b): i for i, b in reversed(list(enumerate(pick)))}
+    init = np.zeros((3, 256), np.int32)
+    init[0, :200] = [first[b] for b in range(200)]
+    init[0, 200:] = rng.integers(0, len(pick), 56)
+    init[1:] = rng.integers(0, len(pick), (2, 256))
+    cb, codes, err = oracle.rvq_train(W, init, 3)
+    assert err[0] == 0.0 and err[1] == 0.0 and err[2] == 0.0
+    assert np.array_equal(oracle.dequant(cb, codes), W.astype(np.float64))
+    for r, j in [(0, 0), (5, 17), (23, 39)]:
+        assert np.array_equal(cb[0, codes[r, 0, j]], W[r, 8 * j:8 * j + 8])
+
+
+def pin_rvq_residual_bookkeeping():
+    """err[2] equals the squared difference between W and the codes dequantised stage by stage
+    in fp32 (((w - c0) - c1) - c2), and the stage errors fall; encoding with the trained
+    codebooks gives the same codes and errors (the final assignments)."""
+    rng = np.random.default_rng(23)
+    W = _rvq_data(rng, 40, 96)
+    init = rng.integers(0, 40 * 12, (3, 256)).astype(np.int32)
+    cb, codes, err = oracle.rvq_train(W, init, 4)
+    nv = 12
+    R = W.reshape(40, nv, 8).copy()
+    for s_ in range(3):
+        R = R - cb[s_][codes[:, s_, :]]
+        e = float((R.astype(np.float64) ** 2).sum())
+        assert abs(e - err[s_]) <= 1e-12 * max(e, 1e-30)
+    assert err[0] > err[1] > err[2] >= 0
+    assert err[0] < float((W.astype(np.float64) ** 2).sum())
+    c2, e2 = oracle.rvq_encode(W, cb)
+    assert np.array_equal(c2, codes) and np.array_equal(e2, err)
+    # with no Lloyd round each stage's codebook is its residual at the init indices
+    cb0, codes0, _ = oracle.rvq_train(W, init, 0)
+    R = W.reshape(-1, 8).copy()
+    for s_ in range(3):
+        assert np.array_equal(cb0[s_], R[init[s_]])
+        R = R - cb0[s_][codes0[:, s_, :].reshape(-1)]
+
+
+def pin_rvq_lloyd_monotone_and_means():
+    """Lloyd rounds never raise the stage-0 error (beyond the 2^-40 rounding of the means);
+    after enough rounds the assignment is stable, and then every used centroid is the mean of
+    its members (float64 mean, to the fixed-point rounding)."""
+    rng = np.random.default_rng(24)
+    W = _rvq_data(rng, 64, 64)
+    init = rng.integers(0, 512, (3, 256)).astype(np.int32)
+    errs = [oracle.rvq_train(W, init, it)[2][0] for it in range(6)]
+    for a, b in zip(errs, errs[1:]):
+        assert b <= a * (1 + 1e-12)
+    assert errs[-1] < errs[0]
+    cb, codes, _ = oracle.rvq_train(W, init, 60)
+    V = W.reshape(-1, 8).astype(np.float64)
+    c0 = codes[:, 0, :].reshape(-1)
+    used = np.unique(c0)
+    assert len(used) > 100
+    for c in used[:64]:
+        m = V[c0 == c].mean(0)
+        assert np.all(np.abs(cb[0, c] - m) <= 2.0 ** -40 + 2.0 ** -24 * np.abs(m) + 1e-30)
+
+
+def pin_rvq_refusals():
+    """cols not a multiple of 8, a non-finite or too large weight, an init index outside the
+    vectors: refused."""
+    rng = np.random.default_rng(25)
+    init = np.zeros((3, 256), np.int32)
+    for W in (_rvq_data(rng, 4, 12), np.full((2, 8), np.nan, np.float32),
+              np.full((2, 8), 2.0 ** 22, np.float32)):
+        try:
+            oracle.rvq_train(W, init, 1)
+        except ValueError:
+            pass
+        else:
+            raise AssertionError("accepted")
+    bad = init.copy()
+    bad[2, 3] = 2
+    try:
+        oracle.rvq_train(_rvq_data(rng, 1, 16), bad, 1)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("accepted")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

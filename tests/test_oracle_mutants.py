@@ -38,6 +38,15 @@ MUTANTS = {
     "code_bytes_wrong": ("return (uint64_t)3 * (uint64_t)OR_STAGES", "return (uint64_t)2 * (uint64_t)OR_STAGES"),
     "crc_not_complemented": ("    return ~c;\n}", "    return c;\n}"),
     "crc_wrong_polynomial": ("(0xEDB88320u & (0u - (c & 1u)))", "(0x04C11DB7u & (0u - (c & 1u)))"),
+    "rvq_ties_to_higher": ("        if (d < bd) {\n            bd = d;", "        if (d <= bd) {\n            bd = d;"),
+    "rvq_residual_not_updated": ("R[i * OR_V + v] = R[i * OR_V + v] - C[(size_t)c * OR_V + v];",
+                                 "R[i * OR_V + v] = R[i * OR_V + v];"),
+    "rvq_mean_not_divided": ("(double)sum[c][v] / (double)cnt[c]", "(double)sum[c][v]"),
+    "rvq_init_from_weights": ("C[(size_t)c * OR_V + v] = R[(size_t)init[s * OR_K + c] * OR_V + v];",
+                              "C[(size_t)c * OR_V + v] = W[(size_t)init[s * OR_K + c] * OR_V + v];"),
+    "rvq_codes_transposed": ("codes[code_index(nv, r, s, j)] = code[(size_t)r * nv + j];",
+                             "codes[code_index(nv, r, s, j)] = code[(size_t)j * rows + r];"),
+    "rvq_distance_abs": ("d = fmaf(t, t, d);", "d = d + fabsf(t);"),
 }
 
 
