@@ -13,7 +13,8 @@ Also measured (extra keys of the same line): batched decode (128 tokens) and a
 prefill chunk (512 tokens) on the grouped tensor-core path, the full-depth
 decode stack (92 layers x 64 experts, lookahead 6 vs off, captured in CUDA
 graphs), a tiered expert bank (16 layers x 64 experts in pinned host memory
-behind HBM caches of three sizes, lookahead 0/6/16), the end-to-end number
+behind HBM caches of three sizes, lookahead 0/6/16), the RVQ encoder on one expert,
+the end-to-end number
 through the C ABI with host buffers, and the CPU oracle on the host cores.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
@@ -618,6 +619,77 @@ def run_tiered(args, dev, out):
     torch.cuda.empty_cache()
 
 
+def run_encoder(args, dev, out):
+    """RVQ encoder on one expert of the decode shape (gate and up 1536 x 7168, down 7168 x 1536),
+    8 Lloyd rounds per stage; then the encoded expert through the expert kernels against the
+    dense expert on one token."""
+    from rvq_compressed_expert_gb300 import binding as B
+    from rvq_compressed_expert_gb300 import synth
+    from rvq_compressed_expert_gb300.layer import MoELayer
+
+    d, f, iters = 7168, 1536, 8
+    shapes = [(f, d), (f, d), (d, f)]
+    Ws, codes, cbs, mats = [], [], [], []
+    total_ms, pairs = 0.0, 0
+    for k, (rows, cols) in enumerate(shapes):
+        W = synth.dense_matrix(20, 0, 0, k, rows, cols, dev)
+        n = rows * cols // 8
+        init = synth.rvq_init(21 + k, n, dev)
+        cb = torch.empty(3, 256, 8, device=dev)
+        c = torch.empty(rows, 3, cols // 8, dtype=torch.uint8, device=dev)
+        err = torch.empty(3, dtype=torch.float64, device=dev)
+        B.waste_rvq_train(W, init, 1, cb, c, err)  # warm-up (allocation paths, module load)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start = time.time()
+        a.record()
+        B.waste_rvq_train(W, init, iters, cb, c, err)
+        b.record()
+        torch.cuda.synchronize()
+        args.sampler.mark(t_start, time.time())
+        ms = a.elapsed_time(b)
+        total_ms += ms
+        pairs += n * 256 * 3 * (iters + 1)
+        norm2 = float((W.double() ** 2).sum())
+        mats.append(dict(shape=[rows, cols], ms=ms,
+                         rel_rmse_after_stage=[math.sqrt(float(e) / norm2) for e in err.cpu().tolist()]))
+        Ws.append(W)
+        codes.append(c)
+        cbs.append(cb)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clock_hz = 2.07e9
+    peak_ops = sms * 128 * clock_hz  # fp32 lane operations per second (FADD and FFMA issue)
+    ops = pairs * 16.0  # 8 subtractions + 8 fused multiply-adds per vector and centroid
+    # the encoded expert through the expert kernels, one token, against the dense expert
+    w = synth.Workload("encoded", d, f, 1, 1, 1, "f32", "none")
+    li = synth.layer_inputs(w, 0, 0, dev, with_codes=False)
+    li = synth.LayerInputs(li.router_w, li.router_b, torch.stack(cbs).unsqueeze(0).contiguous(), tuple(codes))
+    layer = MoELayer(w, 0, 0, dev, inputs=li)
+    x = synth.hidden(22, 1, d, "f32", dev)
+    y = torch.empty(1, d, device=dev)
+    layer.forward(x, 1, torch.zeros(1, 1, dtype=torch.int32, device=dev), torch.ones(1, 1, device=dev), y)
+    torch.cuda.synchronize()
+    xd = x[0].double()
+    zg, zu = Ws[0].double() @ xd, Ws[1].double() @ xd
+    yd = Ws[2].double() @ (zg / (1 + torch.exp(-zg)) * zu)
+    rel = float(torch.linalg.norm(y[0].double() - yd) / torch.linalg.norm(yd))
+    layer.close()
+    out["encoder"] = dict(
+        workload=f"one expert of the decode shape (gate, up {f}x{d}; down {d}x{f}), dense weights "
+                 f"N(0, 0.02^2); greedy residual k-means, 3 stages x 256 centroids, {iters} Lloyd rounds "
+                 f"per stage, centroids started on seeded vectors",
+        ms_per_expert=total_ms, matrices=mats,
+        vector_centroid_pairs_per_s=pairs / (total_ms * 1e-3),
+        roofline={"bound": "alu", "achieved": ops / (total_ms * 1e-3) / 1e9, "peak": peak_ops / 1e9,
+                  "unit": "Gop/s", "frac": ops / (total_ms * 1e-3) / peak_ops,
+                  "note": "fp32 lane operations (8 FADD + 8 FFMA per vector and centroid) against "
+                          f"{sms} SMs x 128 fp32 lanes x 2.07 GHz"},
+        encoded_expert_output_rel_err_vs_dense=rel,
+    )
+    del Ws, codes, cbs
+    torch.cuda.empty_cache()
+
+
 def cpu_baseline_decode(layer, pool, budget_s=12.0):
     """The oracle (single-threaded C, double) on a bounded sample of decode tokens."""
     import oracle
@@ -669,6 +741,8 @@ def native(args):
         run_stack(args, dev, res)
     if not args.no_tiered:
         run_tiered(args, dev, res)
+    if not args.no_encoder:
+        run_encoder(args, dev, res)
     clocks = args.sampler.stop()
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -737,7 +811,7 @@ def native(args):
     }
     if "verify_crc" in res:
         line["config"]["create_with_crc_verify"] = res["verify_crc"]
-    for extra in ("batched", "prefill", "stack", "tiered"):
+    for extra in ("batched", "prefill", "stack", "tiered", "encoder"):
         if extra in res:
             line[extra] = res[extra]
     print(json.dumps(line), flush=True)
@@ -902,6 +976,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-tiered", action="store_true")
+    ap.add_argument("--no-encoder", action="store_true")
     ap.add_argument("--no-batched", action="store_true")
     ap.add_argument("--prefill", action="store_true",
                     help="with --profile-case: the grouped tensor-core path (64 bf16 tokens)")

@@ -342,6 +342,32 @@ int waste_moe_create_banked(const waste_moe_config *cfg, const float *d_router_w
                             const float *d_router_bias, waste_bank *bank, int32_t layer,
                             const float *d_codebooks, waste_moe **out);
 
+/* ---- RVQ encoder (the step before the path) -------------------------------------------
+ * Page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Quantification et
+ * exactitude": expert matrices are stored as 3 residual stages of 256 eight-dimensional
+ * vectors; the converter that writes them is named there, its training is not.  This one is
+ * greedy residual k-means: the residual R starts as W; per stage s, centroid c starts as the
+ * residual vector d_init[s][c]; `iters` Lloyd rounds assign every vector to its nearest
+ * centroid and move each centroid with members to their mean (an empty one stays); a last
+ * assignment gives the stage's codes and R -= C[code].  Nearest = least sum over v = 0..7 of
+ * (x_v - c_v)^2 in fp32, in that order, one fused multiply-add per term, ties to the lower
+ * index; means are taken from exact fixed-point sums (round(x * 2^40) as int64):
+ * mean = (float)((sum / count) * 2^-40) in double.  Codes and codebooks are therefore the same
+ * on every run and equal to any implementation of these rules.
+ *
+ * d_w [rows][cols] fp32 row-major (device), cols % 8 == 0, every |w| < 2^22 and finite
+ * (WASTE_EINVAL otherwise); vector j of row r covers columns 8j..8j+7 and is vector r*(cols/8)+j.
+ * d_init [3][256] int32 vector indices in [0, rows*cols/8) (WASTE_EINVAL otherwise); iters >= 0.
+ * Outputs (device, caller-owned): d_codebooks [3][256][8] fp32, d_codes [rows][3][cols/8] uint8
+ * (the logical layout waste_moe_pack_records reads), d_err [3] double = sum of the squared
+ * residual components after each stage.  Synchronous on `stream`; allocates and frees its own
+ * scratch (rows*cols*4 bytes plus 18 KiB). */
+int waste_rvq_train(const float *d_w, int32_t rows, int32_t cols, const int32_t *d_init, int32_t iters,
+                    float *d_codebooks, uint8_t *d_codes, double *d_err, waste_stream_t stream);
+/* The three final assignments alone, with given codebooks d_codebooks [3][256][8]. */
+int waste_rvq_encode(const float *d_w, int32_t rows, int32_t cols, const float *d_codebooks, uint8_t *d_codes,
+                     double *d_err, waste_stream_t stream);
+
 /* Message of the last failure on the calling thread ("" if none). */
 const char *waste_moe_last_error(void);
 

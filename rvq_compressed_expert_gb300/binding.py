@@ -36,7 +36,7 @@ EXPORTED = ["waste_moe_record_layout", "waste_moe_pack_records", "waste_moe_crea
             "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile",
             "waste_moe_rmsnorm", "waste_moe_forward_noalloc", "waste_moe_step", "waste_moe_set_trace",
             "waste_bank_create", "waste_bank_destroy", "waste_bank_reset", "waste_bank_stats",
-            "waste_moe_create_banked"]
+            "waste_moe_create_banked", "waste_rvq_train", "waste_rvq_encode"]
 
 
 class waste_moe_config(ctypes.Structure):
@@ -115,6 +115,8 @@ def load(path: str = LIB_PATH):
     lib.waste_bank_reset.argtypes = [vp]
     lib.waste_bank_stats.argtypes = [vp, ctypes.POINTER(waste_bank_stats_t)]
     lib.waste_moe_create_banked.argtypes = [cfgp, vp, vp, vp, i32, vp, ctypes.POINTER(vp)]
+    lib.waste_rvq_train.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
+    lib.waste_rvq_encode.argtypes = [vp, i32, i32, vp, vp, vp, vp]
     for name in EXPORTED:
         if name not in ("waste_moe_destroy", "waste_moe_last_error", "waste_bank_destroy"):
             getattr(lib, name).restype = ctypes.c_int
@@ -287,3 +289,17 @@ def aligned_bytes(nbytes: int, device="cuda", align: int = RECORD_ALIGN) -> torc
     raw = torch.empty(nbytes + align, dtype=torch.uint8, device=device)
     off = (-raw.data_ptr()) % align
     return raw[off:off + nbytes]
+
+
+def waste_rvq_train(w, init, iters: int, codebooks, codes, err, stream=None):
+    """Greedy residual k-means of w [rows, cols] fp32 (device): codebooks [3,256,8] fp32, codes
+    [rows,3,cols/8] u8, err [3] float64 (device, written).  init [3,256] int32 (device)."""
+    rows, cols = w.shape
+    return _check(load().waste_rvq_train(_ptr(w), rows, cols, _ptr(init), int(iters), _ptr(codebooks),
+                                         _ptr(codes), _ptr(err), _stream(stream)))
+
+
+def waste_rvq_encode(w, codebooks, codes, err, stream=None):
+    rows, cols = w.shape
+    return _check(load().waste_rvq_encode(_ptr(w), rows, cols, _ptr(codebooks), _ptr(codes), _ptr(err),
+                                          _stream(stream)))

@@ -30,7 +30,7 @@ CODEBOOK_SIZE = 256
 VEC = 8
 
 # purposes mixed into every generator seed
-_P_ROUTER, _P_BIAS, _P_CODEBOOK, _P_GATE, _P_UP, _P_DOWN, _P_HIDDEN = range(1, 8)
+_P_ROUTER, _P_BIAS, _P_CODEBOOK, _P_GATE, _P_UP, _P_DOWN, _P_HIDDEN, _P_DENSE, _P_INIT = range(1, 10)
 _MASK64 = (1 << 64) - 1
 
 
@@ -184,3 +184,18 @@ def layer_inputs(w: Workload, seed: int, layer: int = 0, device="cpu",
         codebooks(seed, layer, w.n_experts, device),
         layer_codes(seed, layer, w.n_experts, w.d, w.f, device) if with_codes else None,
     )
+
+
+def dense_matrix(seed: int, layer: int, expert: int, which: int, rows: int, cols: int, device="cpu",
+                 std: float = 0.02) -> torch.Tensor:
+    """A dense expert matrix [rows, cols] fp32 ~ N(0, std) (which: 0 gate, 1 up, 2 down), the
+    input of the RVQ encoder."""
+    g = _gen(device, seed, layer, expert, _P_DENSE, which)
+    return torch.randn(rows, cols, generator=g, device=device, dtype=torch.float32) * std
+
+
+def rvq_init(seed: int, n_vectors: int, device="cpu") -> torch.Tensor:
+    """[3, 256] int32 vector indices, uniform over [0, n_vectors): where each stage's centroids
+    start (the encoder's only random draw)."""
+    g = _gen("cpu", seed, n_vectors, 0, _P_INIT)
+    return torch.randint(0, n_vectors, (3, CODEBOOK_SIZE), generator=g, dtype=torch.int32).to(device)

@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(waste_(?:moe|bank)_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(waste_(?:moe|bank|rvq)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
