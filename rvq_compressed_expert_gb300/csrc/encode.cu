@@ -13,7 +13,7 @@
 // in fixed point (round(x * 2^40) as int64), exact in any order, so shared-memory and global
 // atomics give the same means on every run.
 //
-// Kernels: an assignment pass (persistent CTAs of 256 threads, two vectors per thread, the 256
+// Kernels: an assignment pass (persistent CTAs of 256 threads, four vectors per thread, the 256
 // centroids in shared memory; it either adds each vector to its centroid's sums in shared
 // memory, flushed once per CTA, or applies the stage: residual update, code, squared error),
 // a mean kernel, a centroid-init gather and an input check.  Bound: fp32 issue (16 operations
@@ -29,7 +29,7 @@ namespace {
 constexpr int kK = 256;
 constexpr int kV = 8;
 constexpr int kAssignThreads = 256;
-constexpr int kPerThread = 2;
+constexpr int kPerThread = 4;
 constexpr double kFix = 1099511627776.0; // 2^40
 
 struct EncScratch {
@@ -172,11 +172,15 @@ __global__ void __launch_bounds__(kAssignThreads) assign_kernel(float *__restric
     }
 }
 
+// CTAs of an assignment pass: at most four per SM (all resident), and as many rounds for
+// each CTA as the largest of them needs, so the last round is not a partial one.
 int assign_grid(size_t n, int num_sms) {
     const size_t per_cta = (size_t)kAssignThreads * kPerThread;
     const size_t need = (n + per_cta - 1) / per_cta;
     const size_t cap = (size_t)num_sms * 4;
-    return (int)(need < cap ? (need ? need : 1) : cap);
+    if (need <= cap) return (int)(need ? need : 1);
+    const size_t rounds = (need + cap - 1) / cap;
+    return (int)((need + rounds - 1) / rounds);
 }
 
 int enc_fail(int code, const char *msg) {
