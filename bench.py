@@ -54,6 +54,15 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x: the job's time is its slowest rank's."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -232,11 +241,7 @@ def run_decode(args, dev, out):
         torch.distributed.barrier()
     args.sampler.mark(t_start, t_end)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if args.world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), args.world, dev)
     st = layer.stats()
 
     # the same step as one persistent kernel (router, top-k, expert units and combine from a
@@ -322,11 +327,7 @@ def run_decode(args, dev, out):
         ev2[i][1].record(stream)
     torch.cuda.synchronize()
     args.sampler.mark(t_start, time.time())
-    e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
-    if args.world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev2), args.world, dev)
     out["e2e"] = dict(value=args.world * K / (e2e_ms * 1e-3), unit=UNIT,
                       h2d_bytes_per_step=w.d * 4, d2h_bytes_per_step=w.d * 4)
     out["_layer"] = layer

@@ -324,7 +324,8 @@ int waste_bank_stats(const waste_bank *bank, waste_bank_stats_t *out);
  * crc32 with WASTE_FLAG_VERIFY_CRC -- checked as by waste_moe_create).  forward / step first
  * fetch the routed experts into the cache, then read them from their slots; prefetch copies
  * the predicted experts into the cache instead of warming L2.  Outputs equal those of the
- * same records held in device memory, bit for bit.  Needs n_slots >= max_tokens * top_k.
+ * same records held in device memory, bit for bit.  Needs n_slots >= min(max_tokens * top_k,
+ * n_experts), the most distinct experts one call can touch (WASTE_EINVAL otherwise).
  * A call on the table-lookup path with T * top_k <= 64 (decode) runs its demand copy inside
  * the persistent step kernel: a few CTAs copy the missing records in order while the others
  * run the resident experts' units and then each missing expert's as soon as its record is in

@@ -1,3 +1,4 @@
+#include <algorithm>
 // Host side of the C ABI declared in waste_moe.h: argument and record checks,
 // workspace, statistics, error strings, and the launch sequence of each call.
 #include "common.cuh"
@@ -613,9 +614,12 @@ int waste_moe_create_banked(const waste_moe_config *cfg, const float *d_router_w
         return fail(WASTE_EINVAL, "layer shapes differ from the bank's");
     if (layer < 0 || layer >= bank_layers(bank))
         return fail(WASTE_EINVAL, "layer %d outside the bank's [0, %d)", layer, bank_layers(bank));
-    if ((long long)cfg->max_tokens * cfg->top_k > bank_slot_count(bank))
-        return fail(WASTE_EINVAL, "the bank's %d slots cannot hold max_tokens * top_k = %d experts",
-                    bank_slot_count(bank), cfg->max_tokens * cfg->top_k);
+    // a call touches at most min(max_tokens * top_k, n_experts) distinct experts, and the plan
+    // never evicts an expert of the call in flight: all of them must fit at once
+    const long long per_call = std::min((long long)cfg->max_tokens * cfg->top_k, (long long)cfg->n_experts);
+    if (per_call > bank_slot_count(bank))
+        return fail(WASTE_EINVAL, "the bank's %d slots cannot hold the %lld distinct experts of one call",
+                    bank_slot_count(bank), per_call);
     // headers (and crc with the flag) checked on the host-resident records themselves
     waste_moe *h = nullptr;
     rc = waste_moe_create(cfg, d_router_w, d_router_bias, bank_host_records(bank, layer), bank_stride(bank),

@@ -97,7 +97,7 @@ def test_bank_refusals():
     ts = TieredStack(W, 0, 1, 4)
     try:
         ml = ts.layers[0]
-        cfg = B.make_config(W.d, W.f, W.n_experts, W.top_k, "f32", 2, 0, 0, 0)  # 2 x 4 > 4 slots
+        cfg = B.make_config(W.d, W.f, W.n_experts, W.top_k, "f32", 2, 0, 0, 0)  # min(2 x 4, 16) > 4 slots
         with pytest.raises(B.WasteError) as ei:
             B.waste_moe_create_banked(cfg, ml.router_w, ml.router_b, ts.bank, 0, ml.codebooks)
         assert ei.value.status == -1
@@ -163,3 +163,40 @@ def test_plan_keeps_resident_experts_of_the_call():
     finally:
         ts.close()
         res.close()
+
+
+def test_banked_grouped_bf16():
+    """Batched bf16 calls on a bank take the grouped tensor-core path for experts with >= 4
+    tokens (its producer reads the records through the slot map) and the lookup path for the
+    rest: routing and outputs equal the resident layers' bit for bit.  16 slots hold one layer's
+    16 experts (a call touches at most min(T * k, E) of them), so two layers evict each other."""
+    wb = synth.Workload("bankb", 512, 256, 16, 4, 32, "bf16", "zipf")
+    res = [MoELayer(wb, 2, L, "cuda") for L in range(2)]
+    ts = TieredStack(wb, 2, 2, 16)
+    try:
+        h = synth.hidden(6, wb.tokens, wb.d, "bf16", "cuda")
+        T, k = wb.tokens, wb.top_k
+        first_seen = 0
+        for rep in range(2):
+            for L in range(2):
+                outs = []
+                for ml in (res[L], ts.layers[L]):
+                    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+                    gate = torch.empty(T, k, device="cuda")
+                    out = torch.empty(T, wb.d, device="cuda")
+                    ml.step(h, T, idx, gate, out, 0)
+                    outs.append((idx, gate, out))
+                torch.cuda.synchronize()
+                for a, b in zip(*outs):
+                    assert torch.equal(a, b)
+                if rep == 0:
+                    first_seen += len(torch.unique(outs[1][0]))
+        st = ts.stats()
+        assert st["demand_hits"] + st["demand_misses"] == 2 * 2 * T * k
+        assert st["demand_misses"] >= first_seen  # every expert came in when first routed
+        for ml in ts.layers:
+            ml.stats()
+    finally:
+        ts.close()
+        for l in res:
+            l.close()
