@@ -313,6 +313,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
         (4 + 2 * S + kMaxFusedRowBlocks) * 4,       // sync
         S * 4,                                      // bank_wait
         S * 4,                                      // bank_order
+        4,                                          // route_done
         G * ((size_t)E + 1) * 4,                    // grp.offs
         G * S * 4,                                  // grp.sorted
         G * S * 4,                                  // grp.lut_slots
@@ -354,17 +355,18 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     W.sync = reinterpret_cast<unsigned *>(b + offs[10]);
     W.bank_wait = reinterpret_cast<int32_t *>(b + offs[11]);
     W.bank_order = reinterpret_cast<int32_t *>(b + offs[12]);
+    W.route_done = reinterpret_cast<unsigned *>(b + offs[13]);
     Grouping &Gp = W.grp;
-    Gp.offs = grouped ? reinterpret_cast<int32_t *>(b + offs[13]) : nullptr;
-    Gp.sorted = grouped ? reinterpret_cast<int32_t *>(b + offs[14]) : nullptr;
-    Gp.lut_slots = grouped ? reinterpret_cast<int32_t *>(b + offs[15]) : nullptr;
-    Gp.chunks = grouped ? reinterpret_cast<int4 *>(b + offs[16]) : nullptr;
-    Gp.counts = grouped ? reinterpret_cast<int32_t *>(b + offs[17]) : nullptr;
-    Gp.one_part = grouped ? reinterpret_cast<uint8_t *>(b + offs[18]) : nullptr;
-    Gp.xg = grouped ? reinterpret_cast<uint8_t *>(b + offs[19]) : nullptr;
-    Gp.ag = grouped ? reinterpret_cast<uint8_t *>(b + offs[20]) : nullptr;
+    Gp.offs = grouped ? reinterpret_cast<int32_t *>(b + offs[14]) : nullptr;
+    Gp.sorted = grouped ? reinterpret_cast<int32_t *>(b + offs[15]) : nullptr;
+    Gp.lut_slots = grouped ? reinterpret_cast<int32_t *>(b + offs[16]) : nullptr;
+    Gp.chunks = grouped ? reinterpret_cast<int4 *>(b + offs[17]) : nullptr;
+    Gp.counts = grouped ? reinterpret_cast<int32_t *>(b + offs[18]) : nullptr;
+    Gp.one_part = grouped ? reinterpret_cast<uint8_t *>(b + offs[19]) : nullptr;
+    Gp.xg = grouped ? reinterpret_cast<uint8_t *>(b + offs[20]) : nullptr;
+    Gp.ag = grouped ? reinterpret_cast<uint8_t *>(b + offs[21]) : nullptr;
     Gp.max_chunks = grouped ? (int)max_chunks : 0;
-    W.router_part = T > 16 ? reinterpret_cast<float *>(b + offs[21]) : nullptr;
+    W.router_part = T > 16 ? reinterpret_cast<float *>(b + offs[22]) : nullptr;
     ce = cudaMemset(base, 0, total);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
@@ -453,13 +455,19 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     float *logits = d_logits ? d_logits : h->W.logits;
     if (h->profiling) cudaEventRecord(h->route_tm.ev[0], s);
-    cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s, h->W.router_part, h->num_sms);
+    const unsigned long long router_bytes = (unsigned long long)h->L.E * (unsigned long long)h->L.d * 4ull;
+    const int pred_stride = h->pred_P > 0 ? h->pred_P : 1;
+    RouteTopk F{h->W.route_done, h->L.k, d_idx, d_gate, h->W.pred_idx, h->W.pred_count, pred_stride, h->W.stats,
+                router_bytes};
+    bool fused = false;
+    cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s, h->W.router_part, h->num_sms, &F, &fused);
     if (e != cudaSuccess) return cuda_fail(e, "router kernel");
     if (h->profiling) cudaEventRecord(h->route_tm.ev[1], s);
-    e = launch_topk(logits, h->W.logits_lo, T, h->L.E, h->L.k, d_idx, d_gate, h->W.pred_idx,
-                    h->W.pred_count, h->pred_P > 0 ? h->pred_P : 1, h->W.stats,
-                    (unsigned long long)h->L.E * (unsigned long long)h->L.d * 4ull, s);
-    if (e != cudaSuccess) return cuda_fail(e, "top-k kernel");
+    if (!fused) {
+        e = launch_topk(logits, h->W.logits_lo, T, h->L.E, h->L.k, d_idx, d_gate, h->W.pred_idx,
+                        h->W.pred_count, pred_stride, h->W.stats, router_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "top-k kernel");
+    }
     if (h->profiling) {
         cudaEventRecord(h->route_tm.ev[2], s);
         h->route_tm.n = 3;

@@ -107,6 +107,19 @@ struct BankLanes {
 enum { kBankDemandHits = 0, kBankDemandMisses, kBankPrefetchCopies, kBankPrefetchPresent, kBankCopiedBytes,
        kBankStatCount };
 
+// Top-k taken by the last CTA of the router launch (router.cu); done = null: router only.
+struct RouteTopk {
+    unsigned *done; // CTAs finished, zero at rest
+    int k;
+    int32_t *idx;
+    float *gate;
+    const int32_t *pred_idx;
+    int32_t *pred_count;
+    int pred_stride;
+    unsigned long long *stats;
+    unsigned long long router_bytes;
+};
+
 // Slots of a batched call grouped by expert (see grouped.cu).
 struct Grouping {
     int32_t *offs;      // [E + 1] first position of each expert in `sorted`
@@ -137,6 +150,7 @@ struct Workspace {
     unsigned *sync;      // fused-step queue and counters [4 + 2 max_slots + kMaxFusedRowBlocks], zero at rest
     int32_t *bank_wait;  // [max_slots] banked calls: job each slot's record arrives by, or -1
     int32_t *bank_order; // [max_slots] banked calls: slots in the order their units run
+    unsigned *route_done; // router CTAs finished (the router launch that also takes the top-k)
     Grouping grp;        // batched calls only (null pointers when max_tokens == 1)
     float *router_part;  // [kRouterMaxSplits][max_T][E] when max_T > 16, else null
     void *base;
@@ -148,8 +162,11 @@ struct Workspace {
 // logits + logits_lo equals W_r h + b exactly given the fp32 dot product.
 // part (optional): [kRouterMaxSplits][T][E] scratch for the split-K router of T > 16.
 constexpr int kRouterMaxSplits = 32;
+// With fuse (and T <= 16): the staged router's last CTA also takes the top-k, and *fused
+// says so (else the caller launches the top-k).
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
-                          float *logits_lo, cudaStream_t s, float *part = nullptr, int num_sms = 1);
+                          float *logits_lo, cudaStream_t s, float *part = nullptr, int num_sms = 1,
+                          const RouteTopk *fuse = nullptr, bool *fused = nullptr);
 cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int E, int k,
                         int32_t *idx, float *gate, const int32_t *pred_idx, int32_t *pred_count,
                         int pred_stride, unsigned long long *stats,

@@ -385,7 +385,8 @@ __device__ __forceinline__ Cand load_cand(const float *lrow, const float *lo_row
     c.key = 0ull; // below every real logit (-inf maps above 0)
     c.id = 0x7fffffff;
     if (i < E) {
-        float a = lrow[i], b = lo_row ? lo_row[i] : 0.f;
+        // L2 loads: the logits may come from other CTAs of the same launch
+        float a = __ldcg(lrow + i), b = lo_row ? __ldcg(lo_row + i) : 0.f;
         if (a != a) a = -INFINITY;
         if (a == 0.f) a = 0.f;
         if (b != b || b == 0.f) b = 0.f;
@@ -440,7 +441,7 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits,
         float my_hi = 0.f, my_lo = 0.f;
         if (lane < k) {
             my_idx = ids[lane];
-            float a = lrow[my_idx], b = logits_lo ? logits_lo[(size_t)t * E + my_idx] : 0.f;
+            float a = __ldcg(lrow + my_idx), b = logits_lo ? __ldcg(logits_lo + (size_t)t * E + my_idx) : 0.f;
             if (a != a) a = -INFINITY;
             if (a == 0.f) a = 0.f;
             if (b != b || b == 0.f) b = 0.f;

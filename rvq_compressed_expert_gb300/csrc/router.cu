@@ -175,18 +175,33 @@ __global__ void reduce_router_kernel(const float *__restrict__ part, int nsplit,
 // Small-T router with the tokens staged in shared memory: 4 experts per CTA of 512
 // threads, every lane's W_r loads in flight at once (same sums as the step kernel's
 // router items).
-// kRows expert rows per CTA (128 threads each).
+// kRows expert rows per CTA (128 threads each).  With F.done set, the last CTA to finish its
+// rows (a counter, zero at rest, put back by that CTA) also takes the top-k and gates of
+// every token, in the kernel's shared memory: the routing in one launch.
 template <bool kBf16, int kRows>
 __global__ void __launch_bounds__(128 * kRows) router_staged_kernel(const float *__restrict__ W,
                                                                     const float *__restrict__ bias,
                                                                     const void *__restrict__ h, int T, int E,
                                                                     int d, float *__restrict__ logits,
                                                                     float *__restrict__ logits_lo,
-                                                                    int hs_tokens) {
+                                                                    int hs_tokens, const RouteTopk F) {
     extern __shared__ __align__(16) float hs_dyn[];
     __shared__ float red[kRows][4][kRouterTok];
+    __shared__ int last;
     router_block_staged<kBf16>(W, bias, h, T, E, d, blockIdx.x * kRows, logits, logits_lo, red, hs_dyn,
                                hs_tokens);
+    if (!F.done) return;
+    __threadfence(); // this CTA's logits before its count
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(F.done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence(); // every CTA's logits after their counts
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(hs_dyn);
+    for (int t = 0; t < T; ++t)
+        topk_block(logits, logits_lo, E, F.k, t, F.idx, F.gate, F.pred_idx, F.pred_count, F.pred_stride, F.stats,
+                   F.router_bytes, keys, reinterpret_cast<int *>(keys + 512));
+    if (threadIdx.x == 0) *F.done = 0u;
 }
 
 // Top-k of one token per CTA of 512 threads: per-warp sorted candidate lists merged in a
@@ -290,11 +305,18 @@ int router_splits(int T, int E, int d, int num_sms) {
 }
 
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
-                          float *logits_lo, cudaStream_t s, float *part, int num_sms) {
+                          float *logits_lo, cudaStream_t s, float *part, int num_sms, const RouteTopk *fuse,
+                          bool *fused) {
     const size_t row_bytes = (size_t)L.d * 4;
+    if (fused) *fused = false;
     if (T <= 16 && row_bytes <= kRouterStageMax) {
         const int hs_tokens = (int)std::min<size_t>({(size_t)kRouterTok, (size_t)T, kRouterStageMax / row_bytes});
-        const size_t smem = (size_t)hs_tokens * row_bytes;
+        // the staged tokens' space, which the last CTA reuses for the top-k's candidate lists
+        const size_t smem = std::max((size_t)hs_tokens * row_bytes, (size_t)kStagedRows * 128 / 32 * 32 * 12);
+        // one token (decode): the top-k rides on the router launch; more tokens keep the
+        // top-k kernel, which takes them in parallel
+        if (fuse && fused && T == 1) *fused = true;
+        else fuse = nullptr;
         static bool attr = false;
         if (!attr) {
             cudaFuncSetAttribute(router_staged_kernel<true, kStagedRows>,
@@ -306,10 +328,10 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
         dim3 grid((L.E + kStagedRows - 1) / kStagedRows);
         if (L.act_bf16)
             router_staged_kernel<true, kStagedRows><<<grid, 128 * kStagedRows, smem, s>>>(
-                L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo, hs_tokens);
+                L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo, hs_tokens, fuse ? *fuse : RouteTopk{});
         else
             router_staged_kernel<false, kStagedRows><<<grid, 128 * kStagedRows, smem, s>>>(
-                L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo, hs_tokens);
+                L.router_w, L.router_b, h, T, L.E, L.d, logits, logits_lo, hs_tokens, fuse ? *fuse : RouteTopk{});
     } else if (T <= 16) {
         dim3 grid((L.E + kRouterRows - 1) / kRouterRows);
         if (L.act_bf16)

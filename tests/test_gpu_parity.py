@@ -287,6 +287,29 @@ def test_deterministic():
         layer.close()
 
 
+@pytest.mark.parametrize("E, k", [(384, 16), (12, 3), (4, 4)])
+def test_one_token_routing_in_one_launch(E, k):
+    """One token is routed in a single launch (the router's last CTA takes the top-k); the same
+    token inside a batch of three goes through the router and the top-k kernel: indices,
+    gates and logits agree bit for bit, and the counter is back at rest for the next call."""
+    d = 512
+    w = synth.Workload("r1", d, 64, E, k, 3, "f32", "offsets")
+    li = synth.layer_inputs(w, 4, 0, "cpu", with_codes=True)
+    h = synth.hidden(9, 3, d, "f32", "cpu").cuda()
+    layer = MoELayer(w, 4, 0, "cuda", inputs=li)
+    try:
+        for rep in range(3):
+            i3, g3, l3 = layer.alloc_outputs(3)[:3]
+            layer.route(h, 3, i3, g3, l3)
+            for t in range(3):
+                i1, g1, l1 = layer.alloc_outputs(1)[:3]
+                layer.route(h[t:t + 1].contiguous(), 1, i1, g1, l1)
+                torch.cuda.synchronize()
+                assert torch.equal(i1[0], i3[t]) and torch.equal(g1[0], g3[t]) and torch.equal(l1[0], l3[t])
+    finally:
+        layer.close()
+
+
 def test_bad_record_header_refused():
     """create refuses a bank whose header has a wrong magic, expert id, layer or offset."""
     d, f, E, k, T = 256, 128, 8, 2, 1
