@@ -1,8 +1,8 @@
-#include <algorithm>
 // Host side of the C ABI declared in waste_moe.h: argument and record checks,
 // workspace, statistics, error strings, and the launch sequence of each call.
 #include "common.cuh"
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstddef>
 #include <cstdio>
@@ -122,6 +122,7 @@ int waste_moe_pack_records(const waste_moe_config *cfg, int32_t layer, int32_t e
                            const uint8_t *d_up_codes, const uint8_t *d_down_codes,
                            uint8_t *d_records, size_t record_stride, int32_t compute_crc,
                            waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
     int rc = check_config(cfg);
     if (rc) return rc;
     if (n_experts < 0 || expert_begin < 0 || expert_begin + n_experts > cfg->n_experts)
@@ -181,6 +182,7 @@ int waste_moe_pack_records(const waste_moe_config *cfg, int32_t layer, int32_t e
 int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
                      const float *d_router_bias, const uint8_t *d_records, size_t record_stride,
                      const float *d_codebooks, waste_moe **out) {
+    const NvtxRange nvtx_range(__func__);
     if (!out) return fail(WASTE_EINVAL, "out is NULL");
     *out = nullptr;
     int rc = check_config(cfg);
@@ -448,6 +450,7 @@ static int check_tokens(const waste_moe *h, int32_t T, const void *d_h) {
 
 int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
                     float *d_logits, waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
     int rc = check_tokens(h, T, d_h);
     if (rc) return rc;
     if (T == 0) return ok();
@@ -485,6 +488,7 @@ static bool use_grouped(const waste_moe *h, int T) {
 
 int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d_idx,
                       const float *d_gate, float *d_out, int32_t mode, waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
     int rc = check_tokens(h, T, d_h);
     if (rc) return rc;
     if (mode < 0 || mode > 2) return fail(WASTE_EINVAL, "mode = %d", mode);
@@ -552,6 +556,7 @@ int waste_moe_set_trace(waste_moe *h, uint64_t *d_trace, int32_t n_items) {
 
 int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
                    float *d_logits, float *d_out, int32_t mode, waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
     int rc = check_tokens(h, T, d_h);
     if (rc) return rc;
     if (mode < 0 || mode > 2) return fail(WASTE_EINVAL, "mode = %d", mode);
@@ -583,6 +588,7 @@ int waste_moe_step(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, flo
 
 int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_t n_prefetch,
                        waste_stream_t side) {
+    const NvtxRange nvtx_range(__func__);
     int rc = check_tokens(next_layer, T, d_h);
     if (rc) return rc;
     waste_moe *h = next_layer;
@@ -612,6 +618,7 @@ int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_
 int waste_moe_create_banked(const waste_moe_config *cfg, const float *d_router_w,
                             const float *d_router_bias, waste_bank *bank, int32_t layer,
                             const float *d_codebooks, waste_moe **out) {
+    const NvtxRange nvtx_range(__func__);
     if (!out) return fail(WASTE_EINVAL, "out is NULL");
     *out = nullptr;
     if (!bank) return fail(WASTE_EINVAL, "NULL bank");
@@ -687,6 +694,7 @@ int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int3
 }
 
 int waste_moe_rmsnorm(const float *d_in, float *d_out, int32_t T, int32_t d, waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
     if (T < 0 || d < 1) return fail(WASTE_EINVAL, "T = %d, d = %d out of range", T, d);
     if (T == 0) return ok();
     if (!d_in || !d_out) return fail(WASTE_EINVAL, "NULL pointer");

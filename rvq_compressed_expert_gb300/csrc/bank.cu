@@ -218,6 +218,7 @@ extern "C" {
 
 int waste_bank_create(const waste_moe_config *cfg, int32_t n_layers, const uint8_t *host_records,
                       size_t record_stride, int32_t n_slots, waste_bank **out) {
+    const NvtxRange nvtx_range(__func__);
     if (!out) return bank_fail(WASTE_EINVAL, "out is NULL");
     *out = nullptr;
     size_t min_stride = 0;

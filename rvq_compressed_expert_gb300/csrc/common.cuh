@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libwaste_moe.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -266,5 +267,14 @@ cudaError_t launch_set_pred_count(int32_t *pred_count, int T, int P, cudaStream_
 
 // Sets the calling thread's message returned by waste_moe_last_error().
 void set_last_error(const char *msg);
+
+// A range named after a C-ABI call on the profiler's timeline for the call's duration (NVTX;
+// nothing is recorded unless a profiler is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 } // namespace wm

@@ -262,6 +262,7 @@ extern "C" {
 
 int waste_rvq_train(const float *d_w, int32_t rows, int32_t cols, const int32_t *d_init, int32_t iters,
                     float *d_codebooks, uint8_t *d_codes, double *d_err, waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
     if (!d_init || !d_codebooks || !d_codes || !d_err || iters < 0)
         return enc_fail(WASTE_EINVAL, "NULL init, codebooks, codes or err, or iters < 0");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -290,6 +291,7 @@ int waste_rvq_train(const float *d_w, int32_t rows, int32_t cols, const int32_t 
 
 int waste_rvq_encode(const float *d_w, int32_t rows, int32_t cols, const float *d_codebooks, uint8_t *d_codes,
                      double *d_err, waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
     if (!d_codebooks || !d_codes || !d_err) return enc_fail(WASTE_EINVAL, "NULL codebooks, codes or err");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     EncScratch S;

@@ -55,6 +55,7 @@ int waste_moe_forward_noalloc(const waste_moe_config *cfg, const uint8_t *d_reco
                               size_t record_stride, const float *d_codebooks, const void *d_h,
                               int32_t T, const int32_t *d_idx, const float *d_gate,
                               float *d_out, int32_t mode, waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
     if (!cfg || cfg->abi_version != WASTE_MOE_ABI_VERSION)
         return fail_na(WASTE_EINVAL, "config is NULL or of another ABI version");
     if (cfg->d <= 0 || cfg->d % kVec || cfg->f <= 0 || cfg->f % kVec || cfg->n_experts < 1 ||

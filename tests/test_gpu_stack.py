@@ -144,3 +144,34 @@ def test_stack_graph_replay_equals_eager():
     finally:
         for l in layers:
             l.close()
+
+
+def test_route_trace_jsonl(tmp_path):
+    """The routing trace of two tokens through the stack: one JSON line per (token, layer) with
+    the experts the oracle's chain picks and gates summing to one."""
+    import json
+    from rvq_compressed_expert_gb300.trace import RouteTrace
+    w = SMALL
+    pairs = make_layers(w)
+    layers = [p[0] for p in pairs]
+    try:
+        stack = DecodeStack(layers, w.tokens)
+        tr = RouteTrace()
+        h0s = [synth.hidden(3 + i, w.tokens, w.d, "f32", "cpu") for i in range(2)]
+        for h0 in h0s:
+            run_eager(stack, h0.cuda(), 0, tr.on_layer)
+            tr.next_token()
+        path = tmp_path / "route.jsonl"
+        assert tr.write(str(path)) == 2 * w.n_layers
+        rows = [json.loads(l) for l in open(path)]
+        assert [(r["token"], r["layer"]) for r in rows] == [(t, L) for t in range(2) for L in range(w.n_layers)]
+        for t, h0 in enumerate(h0s):
+            _, ref_idx, _ = oracle.stack_chain(
+                h0, [(li.router_w, li.router_b, li.codebooks, li.codes) for _, li in pairs], w.top_k)
+            for L in range(w.n_layers):
+                r = rows[t * w.n_layers + L]
+                assert r["experts"] == np.asarray(ref_idx[L]).tolist()
+                assert all(abs(sum(g) - 1.0) < 1e-6 for g in r["gates"])
+    finally:
+        for l in layers:
+            l.close()
