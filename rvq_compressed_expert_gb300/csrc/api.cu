@@ -520,7 +520,7 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
     }
     if (h->bank) {
         // the routed experts into the bank's HBM cache before the expert kernels read them
-        e = launch_bank_fetch(h->bank, h->bank_layer, d_idx, T * h->L.k, true, h->num_sms, s);
+        e = launch_bank_fetch(h->bank, h->bank_layer, d_idx, T * h->L.k, true, s);
         if (e != cudaSuccess) return cuda_fail(e, "bank fetch");
     }
     if (use_grouped(h, T)) {
@@ -605,7 +605,7 @@ int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_
     h->pred_P = P;
     if (h->bank) {
         // the predicted experts into the bank's HBM cache
-        e = launch_bank_fetch(h->bank, h->bank_layer, h->W.pred_idx, T * P, false, h->num_sms, s);
+        e = launch_bank_fetch(h->bank, h->bank_layer, h->W.pred_idx, T * P, false, s);
         if (e == cudaSuccess) e = launch_set_pred_count(h->W.pred_count, T, P, s);
         if (e != cudaSuccess) return cuda_fail(e, "bank lookahead");
         return ok();

@@ -162,14 +162,13 @@ __global__ void __launch_bounds__(bank::kCopyThreads) copy_kernel(BankDevice D, 
 
 } // namespace
 
-cudaError_t launch_bank_fetch(waste_bank *b, int layer, const int32_t *ids, int n_ids, bool demand, int num_sms,
+cudaError_t launch_bank_fetch(waste_bank *b, int layer, const int32_t *ids, int n_ids, bool demand,
                               cudaStream_t s) {
     cudaError_t e = cudaStreamWaitEvent(s, demand ? b->ev_lookahead : b->ev_demand, 0);
     if (e != cudaSuccess) return e;
     const BankDevice D = device_for(b, demand);
     plan_kernel<<<1, 32, 0, s>>>(D, layer, b->E, b->n_slots, b->stride, ids, n_ids, demand ? 1 : 0, nullptr,
                                  nullptr);
-    (void)num_sms;
     copy_kernel<<<bank::kCopyLanes, bank::kCopyThreads, 0, s>>>(D, b->host, b->stride);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

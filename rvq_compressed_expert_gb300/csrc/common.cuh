@@ -244,7 +244,7 @@ int device_sm_count();
 
 // Tiered bank: bring the experts ids[0..n_ids) of `layer` into the HBM cache (demand: the
 // clock advances and hits / misses are counted; lookahead: slots of the call in flight stay).
-cudaError_t launch_bank_fetch(waste_bank *b, int layer, const int32_t *ids, int n_ids, bool demand, int num_sms,
+cudaError_t launch_bank_fetch(waste_bank *b, int layer, const int32_t *ids, int n_ids, bool demand,
                               cudaStream_t s);
 // A demand fetch whose copy runs inside the persistent step kernel: the plan alone (after the
 // bank's last lookahead), which also writes for each of the n_ids slots the job its record
