@@ -279,9 +279,11 @@ extern __shared__ __align__(16) unsigned char lut_smem[];
 // into the buffers when this one returns.  For a down unit, `dep` (if not null) is a
 // completion counter that must reach dep_target before the gate/up partials are read.
 // kNT: threads of the CTA (a multiple of 128); kPing: codes of the next row group are
-// loaded into registers while the current one is consumed.
+// loaded into registers while the current one is consumed; kPartLoads: the next row group's
+// codes of a part are asked for as soon as that part's lookups are issued (else at the top
+// of each round -- the persistent step kernel, whose other items leave no registers for it).
 template <bool kDown, bool kRecon, bool kBf16, int kNT = kThreads, bool kPing = kCodePingPong,
-          int kPf = kPrefetchRounds>
+          int kPf = kPrefetchRounds, bool kPartLoads = true>
 __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
                                       int &par, bool &primed, const unsigned *dep,
                                       unsigned dep_target, unsigned long long *t_tables = nullptr) {
@@ -492,13 +494,17 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     // 32-bit shared-window address of the tables: a lookup is PRMT, IADD and one
     // ld.shared with the stage offset as its immediate
     const uint32_t tab32 = (uint32_t)__cvta_generic_to_shared(smem);
-    auto load = [&](int g, uint4 (&w)[2][kStages]) {
+    auto load_part = [&](int g, int p, uint4 (&w)[2][kStages]) {
+        const uint8_t *pb = p ? pb1 : pb0;
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
             const size_t co = ((size_t)g * kStages + s) * 512 + (size_t)lane * 16;
-            w[0][s] = pb0 ? ld_stream(pb0 + co) : make_uint4(0, 0, 0, 0);
-            w[1][s] = pb1 ? ld_stream(pb1 + co) : make_uint4(0, 0, 0, 0);
+            w[p][s] = pb ? ld_stream(pb + co) : make_uint4(0, 0, 0, 0);
         }
+    };
+    auto load = [&](int g, uint4 (&w)[2][kStages]) {
+        load_part(g, 0, w);
+        load_part(g, 1, w);
     };
     auto ahead = [&](int g) {
         const int ga = g + kPf * kNW;
@@ -519,63 +525,68 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
         acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 16);
     };
-    auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
-        const int row = g * kGroupRows + (lane & 15);
-        float acc[16];
+    // the lookups of part p of one row group: acc = (or, for the second down segment, +=)
+    // the 16 partials
+    auto lookups = [&](const uint4 (&cwp)[kStages], int p, float (&acc)[16]) {
+        const uint32_t colb = p ? colb1 : colb0;
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            const uint32_t colb = p ? colb1 : colb0;
+        for (int wd = 0; wd < 4; ++wd) {
+            const uint32_t w0 = comp(cwp[0], wd), w1 = comp(cwp[1], wd), w2 = comp(cwp[2], wd);
 #pragma unroll
-            for (int wd = 0; wd < 4; ++wd) {
-                const uint32_t w0 = comp(cw[p][0], wd), w1 = comp(cw[p][1], wd), w2 = comp(cw[p][2], wd);
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    float t;
-                    if constexpr (!kRecon) {
-                        const uint32_t sel = 0x7604u | ((uint32_t)b << 4);
-                        const uint32_t a0 = __byte_perm(w0, colb, sel);
-                        const uint32_t a1 = __byte_perm(w1, colb, sel);
-                        const uint32_t a2 = __byte_perm(w2, colb, sel);
-                        const float t0 = lds_stage<0>(tab32 + a0);
-                        const float t1 = lds_stage<1>(tab32 + a1);
-                        const float t2 = lds_stage<2>(tab32 + a2);
-                        t = (t0 + t1) + t2;
-                    } else {
-                        const float *cbs = reinterpret_cast<const float *>(smem) + p * kCbFloats;
-                        const int c0 = (w0 >> (8 * b)) & 255, c1 = (w1 >> (8 * b)) & 255,
-                                  c2 = (w2 >> (8 * b)) & 255;
-                        const float4 *r0 = reinterpret_cast<const float4 *>(cbs + c0 * kVec);
-                        const float4 *r1 = reinterpret_cast<const float4 *>(cbs + kCodes * kVec + c1 * kVec);
-                        const float4 *r2 = reinterpret_cast<const float4 *>(cbs + 2 * kCodes * kVec + c2 * kVec);
-                        const float4 a0 = r0[0], a1 = r0[1], b0 = r1[0], b1 = r1[1], d0 = r2[0], d1 = r2[1];
-                        const float *x = xv[p];
-                        float sacc = ((a0.x + b0.x) + d0.x) * x[0];
-                        sacc = fmaf((a0.y + b0.y) + d0.y, x[1], sacc);
-                        sacc = fmaf((a0.z + b0.z) + d0.z, x[2], sacc);
-                        sacc = fmaf((a0.w + b0.w) + d0.w, x[3], sacc);
-                        sacc = fmaf((a1.x + b1.x) + d1.x, x[4], sacc);
-                        sacc = fmaf((a1.y + b1.y) + d1.y, x[5], sacc);
-                        sacc = fmaf((a1.z + b1.z) + d1.z, x[6], sacc);
-                        sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
-                        t = sacc;
-                    }
-                    if (kDown && p == 1) acc[4 * wd + b] += t;
-                    else acc[4 * wd + b] = t;
+            for (int b = 0; b < 4; ++b) {
+                float t;
+                if constexpr (!kRecon) {
+                    const uint32_t sel = 0x7604u | ((uint32_t)b << 4);
+                    const uint32_t a0 = __byte_perm(w0, colb, sel);
+                    const uint32_t a1 = __byte_perm(w1, colb, sel);
+                    const uint32_t a2 = __byte_perm(w2, colb, sel);
+                    const float t0 = lds_stage<0>(tab32 + a0);
+                    const float t1 = lds_stage<1>(tab32 + a1);
+                    const float t2 = lds_stage<2>(tab32 + a2);
+                    t = (t0 + t1) + t2;
+                } else {
+                    const float *cbs = reinterpret_cast<const float *>(smem) + p * kCbFloats;
+                    const int c0 = (w0 >> (8 * b)) & 255, c1 = (w1 >> (8 * b)) & 255,
+                              c2 = (w2 >> (8 * b)) & 255;
+                    const float4 *r0 = reinterpret_cast<const float4 *>(cbs + c0 * kVec);
+                    const float4 *r1 = reinterpret_cast<const float4 *>(cbs + kCodes * kVec + c1 * kVec);
+                    const float4 *r2 = reinterpret_cast<const float4 *>(cbs + 2 * kCodes * kVec + c2 * kVec);
+                    const float4 a0 = r0[0], a1 = r0[1], b0 = r1[0], b1 = r1[1], d0 = r2[0], d1 = r2[1];
+                    const float *x = xv[p];
+                    float sacc = ((a0.x + b0.x) + d0.x) * x[0];
+                    sacc = fmaf((a0.y + b0.y) + d0.y, x[1], sacc);
+                    sacc = fmaf((a0.z + b0.z) + d0.z, x[2], sacc);
+                    sacc = fmaf((a0.w + b0.w) + d0.w, x[3], sacc);
+                    sacc = fmaf((a1.x + b1.x) + d1.x, x[4], sacc);
+                    sacc = fmaf((a1.y + b1.y) + d1.y, x[5], sacc);
+                    sacc = fmaf((a1.z + b1.z) + d1.z, x[6], sacc);
+                    sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
+                    t = sacc;
                 }
-            }
-            if constexpr (!kDown) {
-                reduce16(acc);
-                if (lane < 16 && row < G.n_out)
-                    A.part_gu[(((size_t)U.slot * A.gu.nseg + U.seg0) * 2 + p) * G.n_out + row] = acc[0];
+                if (kDown && p == 1) acc[4 * wd + b] += t;
+                else acc[4 * wd + b] = t;
             }
         }
-        if constexpr (kDown) {
-            reduce16(acc);
-            if (lane < 16 && row < G.n_out)
+    };
+    // reduce-scatter and store: gate/up per part, down once for both segments
+    auto finish = [&](float (&acc)[16], int p, int g) {
+        const int row = g * kGroupRows + (lane & 15);
+        reduce16(acc);
+        if (lane < 16 && row < G.n_out) {
+            if constexpr (!kDown)
+                A.part_gu[(((size_t)U.slot * A.gu.nseg + U.seg0) * 2 + p) * G.n_out + row] = acc[0];
+            else
                 A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = acc[0];
         }
     };
     if constexpr (kPing) {
+        auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
+            float acc[16];
+            lookups(cw[0], 0, acc);
+            if constexpr (!kDown) finish(acc, 0, g);
+            lookups(cw[1], 1, acc);
+            finish(acc, 1, g);
+        };
         uint4 wa[2][kStages], wb[2][kStages];
         int g = U.g0 + warp;
         if (g < U.g1) load(g, wa);
@@ -590,14 +601,34 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             consume(wb, g);
             g += kNW;
         }
-    } else {
-        // codes loaded at the top of each round (they are already on their way into
-        // L2), leaving the registers to the lookups in flight
+    } else if constexpr (!kPartLoads) {
         for (int g = U.g0 + warp; g < U.g1; g += kNW) {
             uint4 wa[2][kStages];
             load(g, wa);
             ahead(g);
-            consume(wa, g);
+            float acc[16];
+            lookups(wa[0], 0, acc);
+            if constexpr (!kDown) finish(acc, 0, g);
+            lookups(wa[1], 1, acc);
+            finish(acc, 1, g);
+        }
+    } else {
+        // one set of code registers: as soon as a part's lookups are issued, the next row
+        // group's codes of that part are asked for into its registers, so each load has the
+        // rest of the round in front of it (lines are already on their way into L2)
+        uint4 wa[2][kStages];
+        int g = U.g0 + warp;
+        if (g < U.g1) load(g, wa);
+        for (; g < U.g1; g += kNW) {
+            const int gn = g + kNW;
+            ahead(g);
+            float acc[16];
+            lookups(wa[0], 0, acc);
+            if (gn < U.g1) load_part(gn, 0, wa);
+            if constexpr (!kDown) finish(acc, 0, g);
+            lookups(wa[1], 1, acc);
+            if (gn < U.g1) load_part(gn, 1, wa);
+            finish(acc, 1, g);
         }
     }
     // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
