@@ -39,6 +39,9 @@ constexpr int kRouterRowsPerItem = kThreads / 128; // 4 expert rows per router i
 constexpr int kCombineRows = kThreads;              // output rows per combine item
 constexpr int kMaxFusedExperts = 1024;              // top-k of the step kernel sorts <= 1024 keys
 static_assert(kThreads == bank::kCopyThreads, "a copy lane is one CTA of the step kernel");
+// L2 prefetch distance of the step kernel's units, which load a whole round of codes at the
+// top of each round (three rounds measured best for that order)
+constexpr int kStepPrefetchRounds = 3;
 
 struct FusedArgs {
     LutArgs A; // lookup units; A.idx is where the top-k item writes the routing
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             const bool has_next = nxt >= b_gu(F) && nxt < b_dn(F);
             Unit N;
             if (has_next) N = decode_unit<false>(F.A, nxt - b_gu(F));
-            run_unit<false, kRecon, kBf16, kThreads, kCodePingPong, kPrefetchRounds, false>(F.A, U, has_next, N, par, primed, nullptr, 0);
+            run_unit<false, kRecon, kBf16, kThreads, kCodePingPong, kStepPrefetchRounds, false>(F.A, U, has_next, N, par, primed, nullptr, 0);
             signal(gu_done(F) + U.slot);
         } else if (cur < b_comb(F)) {
             // ---- down unit (waits inside for the gate/up units of its slot)
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             const bool has_next = nxt >= b_dn(F) && nxt < b_comb(F);
             Unit N;
             if (has_next) N = decode_unit<true>(F.A, nxt - b_dn(F));
-            run_unit<true, kRecon, kBf16, kThreads, kCodePingPong, kPrefetchRounds, false>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot,
+            run_unit<true, kRecon, kBf16, kThreads, kCodePingPong, kStepPrefetchRounds, false>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot,
                                           (unsigned)F.A.gu.nseg);
             signal(dn_done(F) + (u % F.A.nrb));
         } else {

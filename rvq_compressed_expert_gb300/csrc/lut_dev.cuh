@@ -17,7 +17,7 @@ constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
 constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' codebooks
 constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
 constexpr bool kCodePingPong = false;            // hold the next round's codes in registers
-constexpr int kPrefetchRounds = 3;                 // L2 prefetch distance in row-group rounds
+constexpr int kPrefetchRounds = 1;                 // L2 prefetch distance in row-group rounds
 
 struct LutArgs {
     const uint8_t *records;

@@ -151,10 +151,11 @@ cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// The per-phase lookup kernels: 512 threads, codes loaded at the top of each round with
-// the L2 asked for them three rounds ahead.  (Measured on GB300: 384 threads with the
-// next round's codes double-buffered in registers, or a longer prefetch distance, were
-// slower -- the kernel is bound by the shared-memory pipe, not by load latency.)
+// The per-phase lookup kernels: 512 threads; the next round's codes of a part are loaded
+// as soon as that part's lookups are issued, and L2 is asked for the round after (measured
+// on GB300 at the decode shape: step 85.0 us with a prefetch distance of one round, 86.9
+// with two, 87.9 with three, 97.0 with none; 384 threads with a second register set for
+// the codes were slower).
 template <bool kDown, bool kRecon, bool kBf16>
 cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
     return launch_v<kDown, kRecon, kBf16, kThreads, kCodePingPong, kPrefetchRounds>(A, units, num_sms, s);
