@@ -208,18 +208,23 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
     while (cur < n_total(F)) {
         unsigned long long t_start = 0;
         if (F.trace && threadIdx.x == 0) t_start = globaltimer();
-        if (cur < b_topk(F)) {
-            // ---- router rows
-            router_item<kBf16>(F, cur, red);
-            signal(F.sync + 2);
-        } else if (cur < b_copy(F)) {
-            // ---- top-k + softmax of every token, one warp per token
-            wait_counter(F.sync + 2, (unsigned)F.n_router, F.A.err);
-            topk_item(F);
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                __threadfence();
-                atomicExch(F.sync + 3, 1u);
+        if (cur < b_copy(F)) {
+            // a banked call is routed before the kernel: its instance has no routing items
+            if constexpr (!kBanked) {
+                if (cur < b_topk(F)) {
+                    // ---- router rows
+                    router_item<kBf16>(F, cur, red);
+                    signal(F.sync + 2);
+                } else {
+                    // ---- top-k + softmax of every token, one warp per token
+                    wait_counter(F.sync + 2, (unsigned)F.n_router, F.A.err);
+                    topk_item(F);
+                    __syncthreads();
+                    if (threadIdx.x == 0) {
+                        __threadfence();
+                        atomicExch(F.sync + 3, 1u);
+                    }
+                }
             }
         } else if (cur < b_gu(F)) {
             // ---- copy lane of a banked call
@@ -232,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             const bool has_next = nxt >= b_gu(F) && nxt < b_dn(F);
             Unit N;
             if (has_next) N = decode_unit<false>(F.A, nxt - b_gu(F));
-            run_unit<false, kRecon, kBf16, kThreads, kCodePingPong, kStepPrefetchRounds, false>(F.A, U, has_next, N, par, primed, nullptr, 0);
+            run_unit<false, kRecon, kBf16, kThreads, kCodePingPong, kBanked ? kPrefetchRounds : kStepPrefetchRounds,
+                     kBanked>(F.A, U, has_next, N, par, primed, nullptr, 0);
             signal(gu_done(F) + U.slot);
         } else if (cur < b_comb(F)) {
             // ---- down unit (waits inside for the gate/up units of its slot)
@@ -243,8 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             const bool has_next = nxt >= b_dn(F) && nxt < b_comb(F);
             Unit N;
             if (has_next) N = decode_unit<true>(F.A, nxt - b_dn(F));
-            run_unit<true, kRecon, kBf16, kThreads, kCodePingPong, kStepPrefetchRounds, false>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot,
-                                          (unsigned)F.A.gu.nseg);
+            run_unit<true, kRecon, kBf16, kThreads, kCodePingPong, kBanked ? kPrefetchRounds : kStepPrefetchRounds,
+                     kBanked>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot, (unsigned)F.A.gu.nseg);
             signal(dn_done(F) + (u % F.A.nrb));
         } else {
             // ---- combine rows [r0, r1) once every down unit over them is done
