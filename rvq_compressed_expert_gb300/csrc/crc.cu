@@ -7,9 +7,12 @@
 // CRC-32 as in IEEE 802.3 / zlib: reflected polynomial 0xEDB88320, register preset to
 // all ones, result complemented.  The register update over a byte string is affine in the
 // register: R(S, data) = M_len S xor R(0, data), with M_len the GF(2) matrix of "advance
-// over len zero bytes".  So the payload is cut into 4 KiB chunks, one thread computes
-// R(0, chunk) of each, and one thread per record folds the chunks in order:
-// S <- M_4096 S xor R(0, chunk_i) from S = 0xFFFFFFFF; crc = ~S.
+// over len zero bytes", and R(0, .) ignores leading zero bytes.  So the payload is cut into
+// 4 KiB chunks and a thread computes R(0, chunk) of each, four bytes per dependent step
+// (four 256-entry tables); then one warp per record folds its chunks: each lane folds an
+// equal run of chunks (the record padded in front with zero chunks to 32 equal runs), the
+// lanes combine in a shuffle tree, R(0, A||B) = M_len(B) R(0, A) xor R(0, B), and
+// crc = ~(M_payload 0xFFFFFFFF xor R(0, payload)).
 #include <vector>
 
 #include "common.cuh"
@@ -27,55 +30,75 @@ __host__ __device__ inline uint32_t crc_table_entry(uint32_t i) {
     return c;
 }
 
-// R(0, chunk) of every 4 KiB chunk of every record's payload
+// R(0, chunk) of every 4 KiB chunk of every record's payload: per 32-bit little-endian word
+// w, x = S ^ w and S = T3[x & 255] ^ T2[x >> 8 & 255] ^ T1[x >> 16 & 255] ^ T0[x >> 24], with
+// T0 the byte table and T_k[i] = (T_{k-1}[i] >> 8) ^ T0[T_{k-1}[i] & 255] (the same update as
+// four byte steps).
 __global__ void __launch_bounds__(256) crc_chunk_kernel(const uint8_t *__restrict__ records, size_t stride,
                                                         size_t payload_off, size_t n_chunks, int n_records,
                                                         uint32_t *__restrict__ out) {
-    __shared__ uint32_t table[256];
-    table[threadIdx.x] = crc_table_entry(threadIdx.x);
+    __shared__ uint32_t table[4][256];
+    table[0][threadIdx.x] = crc_table_entry(threadIdx.x);
     __syncthreads();
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+        const uint32_t t = table[k - 1][threadIdx.x];
+        table[k][threadIdx.x] = (t >> 8) ^ table[0][t & 0xFFu];
+        __syncthreads();
+    }
     const size_t total = n_chunks * (size_t)n_records;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
         const size_t rec = i / n_chunks, ch = i % n_chunks;
         const uint4 *p = reinterpret_cast<const uint4 *>(records + rec * stride + payload_off + ch * kCrcChunk);
         uint32_t s = 0;
+        uint4 v = __ldg(p);
         for (size_t w = 0; w < kCrcChunk / 16; ++w) {
-            const uint4 v = __ldg(p + w);
+            const uint4 nv = w + 1 < kCrcChunk / 16 ? __ldg(p + w + 1) : v; // the next 16 bytes in flight
             const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint32_t x = words[q];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    s = table[(s ^ x) & 0xFFu] ^ (s >> 8);
-                    x >>= 8;
-                }
+                const uint32_t x = s ^ words[q];
+                s = table[3][x & 0xFFu] ^ table[2][(x >> 8) & 0xFFu] ^ table[1][(x >> 16) & 0xFFu] ^ table[0][x >> 24];
             }
+            v = nv;
         }
         out[i] = s;
     }
 }
 
-__device__ inline uint32_t gf2_apply(const uint32_t *cols, uint32_t v) {
+__host__ __device__ inline uint32_t gf2_apply(const uint32_t *cols, uint32_t v) {
     uint32_t r = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) r ^= cols[i] & (0u - ((v >> i) & 1u));
     return r;
 }
 
-struct AdvanceMatrix {
-    uint32_t cols[32];
+// Matrices of one fold: advance over one chunk, over 2^k lane runs (k = 0..4), and the
+// preset register advanced over the whole payload.
+struct FoldArgs {
+    uint32_t chunk[32];
+    uint32_t tree[5][32];
+    uint32_t preset;
+    int run;  // chunks per lane
+    int pad;  // zero chunks in front of the record
 };
 
-// crc of each record from its chunks, in order
-__global__ void crc_fold_kernel(const uint32_t *__restrict__ chunk_crc, size_t n_chunks, int n_records,
-                                AdvanceMatrix m, uint32_t *__restrict__ out) {
-    const int rec = blockIdx.x * blockDim.x + threadIdx.x;
-    if (rec >= n_records) return;
-    uint32_t s = 0xFFFFFFFFu;
+// crc of each record from its chunks: one warp per record
+__global__ void __launch_bounds__(128) crc_fold_kernel(const uint32_t *__restrict__ chunk_crc, size_t n_chunks,
+                                                       int n_records, const FoldArgs F, uint32_t *__restrict__ out) {
+    const int rec = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (rec >= n_records) return; // whole warps leave together
     const uint32_t *c = chunk_crc + (size_t)rec * n_chunks;
-    for (size_t i = 0; i < n_chunks; ++i) s = gf2_apply(m.cols, s) ^ c[i];
-    out[rec] = ~s;
+    uint32_t s = 0;
+    const long long first = (long long)lane * F.run - F.pad;
+    for (long long i = first < 0 ? 0 : first; i < first + F.run; ++i) s = gf2_apply(F.chunk, s) ^ c[i];
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, s, 1 << k);
+        const uint32_t m = gf2_apply(F.tree[k], s) ^ t;
+        if ((lane & ((2 << k) - 1)) == 0) s = m;
+    }
+    if (lane == 0) out[rec] = ~(F.preset ^ s);
 }
 
 // the folded crc into each record's header field
@@ -95,23 +118,45 @@ void gf2_square(const uint32_t *a, uint32_t *out) {
     }
 }
 
-AdvanceMatrix advance_matrix(size_t bytes) {
+// a * b (apply b, then a)
+void gf2_mul(const uint32_t *a, const uint32_t *b, uint32_t *out) {
+    uint32_t r[32];
+    for (int i = 0; i < 32; ++i) r[i] = gf2_apply(a, b[i]);
+    for (int i = 0; i < 32; ++i) out[i] = r[i];
+}
+
+// m^n by squaring
+void gf2_pow(const uint32_t *m, size_t n, uint32_t *out) {
+    uint32_t r[32], b[32], t[32];
+    for (int i = 0; i < 32; ++i) {
+        r[i] = 1u << i;
+        b[i] = m[i];
+    }
+    while (n) {
+        if (n & 1) gf2_mul(b, r, r);
+        gf2_square(b, t);
+        for (int i = 0; i < 32; ++i) b[i] = t[i];
+        n >>= 1;
+    }
+    for (int i = 0; i < 32; ++i) out[i] = r[i];
+}
+
+FoldArgs fold_args(size_t n_chunks) {
     // one zero byte: S -> table[S & 0xFF] ^ (S >> 8), linear in S
-    uint32_t m[32], t[32];
+    uint32_t byte[32];
     for (int i = 0; i < 32; ++i) {
         const uint32_t s = 1u << i;
-        m[i] = crc_table_entry(s & 0xFFu) ^ (s >> 8);
+        byte[i] = crc_table_entry(s & 0xFFu) ^ (s >> 8);
     }
-    // bytes is a power of two here: square log2(bytes) times
-    size_t n = 1;
-    while (n < bytes) {
-        gf2_square(m, t);
-        for (int i = 0; i < 32; ++i) m[i] = t[i];
-        n <<= 1;
-    }
-    AdvanceMatrix A;
-    for (int i = 0; i < 32; ++i) A.cols[i] = m[i];
-    return A;
+    FoldArgs F;
+    gf2_pow(byte, kCrcChunk, F.chunk);
+    F.run = (int)((n_chunks + 31) / 32);
+    F.pad = (int)(32 * (size_t)F.run - n_chunks);
+    for (int k = 0; k < 5; ++k) gf2_pow(F.chunk, (size_t)F.run << k, F.tree[k]);
+    uint32_t all[32];
+    gf2_pow(F.chunk, n_chunks, all);
+    F.preset = gf2_apply(all, 0xFFFFFFFFu);
+    return F;
 }
 
 } // namespace
@@ -124,8 +169,8 @@ cudaError_t launch_payload_crc(const uint8_t *records, size_t stride, int n_reco
     const size_t total = n_chunks * (size_t)n_records;
     const int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms * 8);
     crc_chunk_kernel<<<grid, 256, 0, s>>>(records, stride, payload_off, n_chunks, n_records, scratch);
-    static const AdvanceMatrix m = advance_matrix(kCrcChunk);
-    crc_fold_kernel<<<(n_records + 127) / 128, 128, 0, s>>>(scratch, n_chunks, n_records, m, crc_out);
+    const FoldArgs F = fold_args(n_chunks);
+    crc_fold_kernel<<<(n_records + 3) / 4, 128, 0, s>>>(scratch, n_chunks, n_records, F, crc_out);
     return cudaGetLastError();
 }
 
