@@ -801,6 +801,9 @@ def native(args):
                   "each step also uses a different token (pool of 64)",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
             "hbm_gbs_whole_step": d["hbm_gbs_step"],
+            "hbm_frac_whole_step": d["hbm_gbs_step"] / peak,
+            "hbm_frac_expert_kernels": (d["gate_up_bytes"] + d["down_bytes"])
+            / ((kern["gate_up"] + kern["down"]) * 1e-3) / 1e9 / peak if "gate_up" in kern else None,
             "algorithmic_bytes_per_step": d["step_bytes"],
             "kernels_ms": kern,
             "ms_per_step_persistent_step_kernel": d["unfused_ms"],

@@ -30,15 +30,34 @@ __host__ __device__ inline uint32_t crc_table_entry(uint32_t i) {
     return c;
 }
 
-// R(0, chunk) of every 4 KiB chunk of every record's payload: per 32-bit little-endian word
-// w, x = S ^ w and S = T3[x & 255] ^ T2[x >> 8 & 255] ^ T1[x >> 16 & 255] ^ T0[x >> 24], with
-// T0 the byte table and T_k[i] = (T_{k-1}[i] >> 8) ^ T0[T_{k-1}[i] & 255] (the same update as
-// four byte steps).
+// One chunk per warp, read coalesced: lane l takes the 16-byte pieces l, l + 32, ..., l + 224.
+// Piece p's contribution to R(0, chunk) is M_{16 (255 - p)} R(0, piece) = M_{512 (7 - j)}
+// M_{16 (31 - l)} R(0, piece) for p = 32 j + l, so a lane folds its pieces with the advance
+// over 512 bytes (four byte tables of that matrix) and the lanes combine in a shuffle tree,
+// R(0, A||B) = M_{16 |B|} R(0, A) xor R(0, B).  R(0, piece) four bytes per step: for each
+// 32-bit little-endian word w, x = S ^ w and S = T3[x & 255] ^ T2[x >> 8 & 255] ^
+// T1[x >> 16 & 255] ^ T0[x >> 24], with T0 the byte table and T_k[i] = (T_{k-1}[i] >> 8) ^
+// T0[T_{k-1}[i] & 255] (the same update as four byte steps).
+struct ChunkArgs {
+    uint32_t adv512[32];   // advance over 512 zero bytes
+    uint32_t tree[5][32];  // advance over 16 * 2^k zero bytes
+};
+
+__device__ __forceinline__ uint32_t gf2_cols(const uint32_t *cols, uint32_t v) {
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r ^= cols[i] & (0u - ((v >> i) & 1u));
+    return r;
+}
+
 __global__ void __launch_bounds__(256) crc_chunk_kernel(const uint8_t *__restrict__ records, size_t stride,
                                                         size_t payload_off, size_t n_chunks, int n_records,
-                                                        uint32_t *__restrict__ out) {
+                                                        const ChunkArgs C, uint32_t *__restrict__ out) {
     __shared__ uint32_t table[4][256];
+    __shared__ uint32_t adv[4][256];
     table[0][threadIdx.x] = crc_table_entry(threadIdx.x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) adv[k][threadIdx.x] = gf2_cols(C.adv512, threadIdx.x << (8 * k));
     __syncthreads();
 #pragma unroll
     for (int k = 1; k < 4; ++k) {
@@ -46,23 +65,34 @@ __global__ void __launch_bounds__(256) crc_chunk_kernel(const uint8_t *__restric
         table[k][threadIdx.x] = (t >> 8) ^ table[0][t & 0xFFu];
         __syncthreads();
     }
+    const int lane = threadIdx.x & 31;
     const size_t total = n_chunks * (size_t)n_records;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
+    for (size_t i = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < total; i += warps) {
         const size_t rec = i / n_chunks, ch = i % n_chunks;
         const uint4 *p = reinterpret_cast<const uint4 *>(records + rec * stride + payload_off + ch * kCrcChunk);
-        uint32_t s = 0;
-        uint4 v = __ldg(p);
-        for (size_t w = 0; w < kCrcChunk / 16; ++w) {
-            const uint4 nv = w + 1 < kCrcChunk / 16 ? __ldg(p + w + 1) : v; // the next 16 bytes in flight
-            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        uint4 v[kCrcChunk / 512];
+#pragma unroll
+        for (int j = 0; j < (int)(kCrcChunk / 512); ++j) v[j] = __ldg(p + 32 * j + lane); // all in flight
+        uint32_t acc = 0;
+#pragma unroll
+        for (int j = 0; j < (int)(kCrcChunk / 512); ++j) {
+            const uint32_t words[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t s = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t x = s ^ words[q];
                 s = table[3][x & 0xFFu] ^ table[2][(x >> 8) & 0xFFu] ^ table[1][(x >> 16) & 0xFFu] ^ table[0][x >> 24];
             }
-            v = nv;
+            acc = adv[0][acc & 0xFFu] ^ adv[1][(acc >> 8) & 0xFFu] ^ adv[2][(acc >> 16) & 0xFFu] ^ adv[3][acc >> 24] ^ s;
         }
-        out[i] = s;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+            const uint32_t t = __shfl_down_sync(0xffffffffu, acc, 1 << k);
+            const uint32_t m = gf2_cols(C.tree[k], acc) ^ t;
+            if ((lane & ((2 << k) - 1)) == 0) acc = m;
+        }
+        if (lane == 0) out[i] = acc;
     }
 }
 
@@ -141,6 +171,23 @@ void gf2_pow(const uint32_t *m, size_t n, uint32_t *out) {
     for (int i = 0; i < 32; ++i) out[i] = r[i];
 }
 
+void byte_matrix(uint32_t *m) {
+    // one zero byte: S -> table[S & 0xFF] ^ (S >> 8), linear in S
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t s = 1u << i;
+        m[i] = crc_table_entry(s & 0xFFu) ^ (s >> 8);
+    }
+}
+
+ChunkArgs chunk_args() {
+    uint32_t byte[32];
+    byte_matrix(byte);
+    ChunkArgs C;
+    gf2_pow(byte, 512, C.adv512);
+    for (int k = 0; k < 5; ++k) gf2_pow(byte, (size_t)16 << k, C.tree[k]);
+    return C;
+}
+
 FoldArgs fold_args(size_t n_chunks) {
     // one zero byte: S -> table[S & 0xFF] ^ (S >> 8), linear in S
     uint32_t byte[32];
@@ -167,8 +214,9 @@ cudaError_t launch_payload_crc(const uint8_t *records, size_t stride, int n_reco
     if (payload_bytes % kCrcChunk) return cudaErrorInvalidValue;
     const size_t n_chunks = payload_bytes / kCrcChunk;
     const size_t total = n_chunks * (size_t)n_records;
-    const int grid = (int)std::min<size_t>((total + 255) / 256, (size_t)num_sms * 8);
-    crc_chunk_kernel<<<grid, 256, 0, s>>>(records, stride, payload_off, n_chunks, n_records, scratch);
+    const int grid = (int)std::min<size_t>((total + 7) / 8, (size_t)num_sms * 8); // 8 chunks (warps) per CTA
+    static const ChunkArgs C = chunk_args();
+    crc_chunk_kernel<<<grid, 256, 0, s>>>(records, stride, payload_off, n_chunks, n_records, C, scratch);
     const FoldArgs F = fold_args(n_chunks);
     crc_fold_kernel<<<(n_records + 3) / 4, 128, 0, s>>>(scratch, n_chunks, n_records, F, crc_out);
     return cudaGetLastError();
