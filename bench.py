@@ -925,6 +925,25 @@ def profile_case(args):
     print("profile case done")
 
 
+def profile_encoder():
+    """One encoder training of a dense 1536 x 7168 matrix (the gate matrix of the decode shape),
+    two Lloyd rounds per stage: a small case for ncu captures of the assignment kernels."""
+    from rvq_compressed_expert_gb300 import _build
+    from rvq_compressed_expert_gb300 import binding as B
+    from rvq_compressed_expert_gb300 import synth
+    _build.build()
+    B.load()
+    rows, cols = 1536, 7168
+    W = synth.dense_matrix(20, 0, 0, 0, rows, cols, "cuda")
+    init = synth.rvq_init(21, rows * cols // 8, "cuda")
+    cb = torch.empty(3, 256, 8, device="cuda")
+    codes = torch.empty(rows, 3, cols // 8, dtype=torch.uint8, device="cuda")
+    err = torch.empty(3, dtype=torch.float64, device="cuda")
+    B.waste_rvq_train(W, init, 2, cb, codes, err)
+    torch.cuda.synchronize()
+    print("encoder profile case: squared error after each stage", err.tolist())
+
+
 def print_unit_trace(tr, w):
     """Per-phase summary of the lookup kernels' unit trace: table build and row streaming."""
     import math as _m
@@ -1004,11 +1023,16 @@ def main():
                     help="with --profile-case: one kernel per phase instead of the step kernel")
     ap.add_argument("--trace", action="store_true",
                     help="with --profile-case: print the step kernel's item timeline")
+    ap.add_argument("--profile-encoder", action="store_true",
+                    help="train one 1536 x 7168 matrix with the RVQ encoder (2 Lloyd rounds) for ncu and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.profile_case:
         profile_case(args)
+        return
+    if args.profile_encoder:
+        profile_encoder()
         return
     if args.impl == "reference":
         reference(args)

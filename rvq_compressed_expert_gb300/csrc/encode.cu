@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kAssignThreads) assign_kernel(float *__restric
             bd[u] = __int_as_float(0x7f800000); // +inf
             best[u] = 0;
         }
-#pragma unroll 2
+#pragma unroll 4
         for (int c = 0; c < kK; ++c) {
             const float4 ca = reinterpret_cast<const float4 *>(C)[2 * c];
             const float4 cb = reinterpret_cast<const float4 *>(C)[2 * c + 1];
