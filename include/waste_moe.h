@@ -49,7 +49,11 @@
  *     checked again on the device: an index outside [0, E) contributes zero
  *     and sets a sticky device error reported by waste_moe_stats as
  *     WASTE_EINVAL.
- *   - A handle is not safe for concurrent use from two host threads.
+ *   - A handle is not safe for concurrent use from two host threads, and its
+ *     route/forward/step calls must not run at the same time on two streams
+ *     (they share the handle's workspace, including the counter by which the
+ *     router's last CTA takes the top-k of a one-token call).  The lookahead
+ *     goes through the next layer's handle, so it may run beside this one's.
  */
 #ifndef WASTE_MOE_H
 #define WASTE_MOE_H
