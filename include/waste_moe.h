@@ -81,7 +81,7 @@ typedef enum {
     WASTE_ELAYOUT = -4,  /* record header: bad magic / version / expert id / offset / alignment */
     WASTE_ECRC = -5,     /* record payload crc32 mismatch (WASTE_FLAG_VERIFY_CRC) */
     WASTE_ETIMEOUT = -6, /* a bounded device wait gave up */
-    WASTE_ENOTIMPL = -7  /* combination not supported by this build */
+    WASTE_ENOTIMPL = -7  /* combination the library does not implement */
 } waste_status;
 
 enum { WASTE_ACT_F32 = 0, WASTE_ACT_BF16 = 1 };
