@@ -50,10 +50,144 @@ BankDevice device_for(const waste_bank *b, bool demand) {
     return D;
 }
 
-// One warp.  With wait_job / order (n_ids <= 64): wait_job[i] = the job by which id i's record
-// arrives in this fetch, or -1 when it is already resident (or has no slot); order = the ids'
-// positions sorted by (wait_job, position), resident ones first.
+// Ranks of positions by (wait_job, position), resident ones (-1) first: order[rank] = position.
+__device__ __forceinline__ void plan_order(const int32_t *wait_job, int32_t *order, int n_ids, int lane) {
+    for (int p = lane; p < n_ids; p += 32) {
+        const int kp = wait_job[p];
+        int r = 0;
+        for (int q = 0; q < n_ids; ++q) {
+            const int kq = wait_job[q];
+            r += (kq < kp) || (kq == kp && q < p);
+        }
+        order[r] = p;
+    }
+}
+
+// One warp; the slots' ticks and keys in shared memory (2 x n_slots words).  With wait_job /
+// order (n_ids <= 64): wait_job[i] = the job by which id i's record arrives in this fetch, or -1
+// when it is already resident (or has no slot); order = the ids' positions sorted by (wait_job,
+// position), resident ones first.
+//  1. every requested expert already resident takes this call's stamp (no miss evicts it);
+//  2. the ids in order, 32 at a time with their slots loaded together: a resident one is a hit;
+//     a miss takes the least (tick, index) slot older than the call -- each lane keeps the least
+//     of its own slots (v = lane mod 32), so a miss is a warp minimum and one lane's rescan --
+//     and becomes a job; a later id of the same expert sees the placement (a hit on that job).
 __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E, int n_slots, size_t stride,
+                                                  const int32_t *__restrict__ ids, int n_ids, int demand,
+                                                  int32_t *__restrict__ wait_job, int32_t *__restrict__ order) {
+    extern __shared__ uint32_t plan_smem[];
+    uint32_t *tick = plan_smem;                                   // [n_slots]
+    int32_t *key_of = reinterpret_cast<int32_t *>(plan_smem + n_slots); // [n_slots]
+    const int lane = threadIdx.x;
+    uint32_t clock = *D.clock;
+    if (demand) clock += 1;
+    const uint32_t seq = *D.seq + 1;
+    for (int v = lane; v < n_slots; v += 32) {
+        tick[v] = D.tick[v];
+        key_of[v] = D.key_of[v];
+    }
+    __syncwarp();
+    if (lane == 0) {
+        *D.clock = clock;
+        *D.seq = seq;
+    }
+    for (int i = lane; i < n_ids; i += 32) {
+        const int e = ids[i];
+        if (e < 0 || e >= E) continue;
+        const int s = D.map[layer * E + e];
+        if (s >= 0) {
+            tick[s] = clock;
+            D.tick[s] = clock;
+        }
+    }
+    __syncwarp();
+    // this lane's least (tick, index) among its slots older than the call
+    auto lane_min = [&]() {
+        unsigned long long best = ~0ull;
+        for (int v = lane; v < n_slots; v += 32) {
+            const uint32_t t = tick[v];
+            if (t < clock) {
+                const unsigned long long c = ((unsigned long long)t << 32) | (unsigned)v;
+                best = c < best ? c : best;
+            }
+        }
+        return best;
+    };
+    unsigned long long mine = lane_min();
+    int n_jobs = 0;
+    unsigned long long hits = 0, misses = 0;
+    for (int i0 = 0; i0 < n_ids; i0 += 32) {
+        const int i = i0 + lane;
+        int key = -1, slot = -1, wj = -1;
+        if (i < n_ids) {
+            const int e = ids[i];
+            if (e >= 0 && e < E) {
+                key = layer * E + e;
+                slot = D.map[key];
+                // placed by an earlier chunk of this plan: waits for that job
+                if (i0 > 0 && slot >= 0 && D.job_seq[slot] == seq) wj = D.job_of[slot];
+            }
+        }
+        const int n = min(32, n_ids - i0);
+        for (int j = 0; j < n; ++j) {
+            const int kj = __shfl_sync(0xffffffffu, key, j);
+            const int sj = __shfl_sync(0xffffffffu, slot, j);
+            if (kj < 0) continue;
+            if (sj >= 0) {
+                ++hits;
+                continue;
+            }
+            unsigned long long best = mine;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const unsigned long long b = __shfl_xor_sync(0xffffffffu, best, o);
+                best = b < best ? b : best;
+            }
+            if (best == ~0ull) continue; // every slot is in use by this call: left unplaced
+            const int v = (int)(best & 0xffffffffu);
+            if (lane == 0) {
+                const int old = key_of[v];
+                if (old >= 0) D.map[old] = -1;
+                D.map[kj] = v;
+                D.key_of[v] = kj;
+                D.tick[v] = clock;
+                D.jobs[n_jobs] = make_int2(v, kj);
+                D.job_seq[v] = seq;
+                D.job_of[v] = n_jobs;
+                key_of[v] = kj;
+                tick[v] = clock;
+            }
+            __syncwarp();
+            if ((v & 31) == lane) mine = lane_min(); // the owner of slot v looks again
+            if (key == kj) { // this id and every later one of the same expert: on this job
+                slot = v;
+                wj = n_jobs;
+            }
+            ++n_jobs;
+            ++misses;
+        }
+        if (wait_job && i < n_ids) wait_job[i] = wj;
+    }
+    if (order) {
+        __syncwarp();
+        plan_order(wait_job, order, n_ids, lane);
+    }
+    if (lane == 0) {
+        *D.n_jobs = n_jobs;
+        if (demand) {
+            D.stats[kBankDemandHits] += hits;
+            D.stats[kBankDemandMisses] += misses;
+        } else {
+            D.stats[kBankPrefetchPresent] += hits;
+            D.stats[kBankPrefetchCopies] += misses;
+        }
+        D.stats[kBankCopiedBytes] += (unsigned long long)n_jobs * stride;
+    }
+}
+
+// The plan with the slot state read from global memory, for banks whose ticks and keys do not
+// fit in shared memory (same decisions as plan_kernel).
+__global__ void __launch_bounds__(32) plan_kernel_global(BankDevice D, int layer, int E, int n_slots, size_t stride,
                                                   const int32_t *__restrict__ ids, int n_ids, int demand,
                                                   int32_t *__restrict__ wait_job, int32_t *__restrict__ order) {
     const int lane = threadIdx.x;
@@ -131,16 +265,7 @@ __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E
     }
     if (order) {
         __syncwarp();
-        // rank of each position by (wait_job, position): resident ones (-1) first
-        for (int p = lane; p < n_ids; p += 32) {
-            const int kp = wait_job[p];
-            int r = 0;
-            for (int q = 0; q < n_ids; ++q) {
-                const int kq = wait_job[q];
-                r += (kq < kp) || (kq == kp && q < p);
-            }
-            order[r] = p;
-        }
+        plan_order(wait_job, order, n_ids, lane);
     }
     if (lane == 0) {
         *D.n_jobs = n_jobs;
@@ -162,13 +287,25 @@ __global__ void __launch_bounds__(bank::kCopyThreads) copy_kernel(BankDevice D, 
 
 } // namespace
 
+// The plan: with the slots' ticks and keys in shared memory when they fit in 48 KiB, else
+// read from global memory (same decisions).
+void launch_plan(const waste_bank *b, const BankDevice &D, int layer, const int32_t *ids, int n_ids, bool demand,
+                 int32_t *wait_job, int32_t *order, cudaStream_t s) {
+    const size_t smem = (size_t)b->n_slots * 8;
+    if (smem <= 48 * 1024)
+        plan_kernel<<<1, 32, smem, s>>>(D, layer, b->E, b->n_slots, b->stride, ids, n_ids, demand ? 1 : 0, wait_job,
+                                        order);
+    else
+        plan_kernel_global<<<1, 32, 0, s>>>(D, layer, b->E, b->n_slots, b->stride, ids, n_ids, demand ? 1 : 0,
+                                            wait_job, order);
+}
+
 cudaError_t launch_bank_fetch(waste_bank *b, int layer, const int32_t *ids, int n_ids, bool demand,
                               cudaStream_t s) {
     cudaError_t e = cudaStreamWaitEvent(s, demand ? b->ev_lookahead : b->ev_demand, 0);
     if (e != cudaSuccess) return e;
     const BankDevice D = device_for(b, demand);
-    plan_kernel<<<1, 32, 0, s>>>(D, layer, b->E, b->n_slots, b->stride, ids, n_ids, demand ? 1 : 0, nullptr,
-                                 nullptr);
+    launch_plan(b, D, layer, ids, n_ids, demand, nullptr, nullptr, s);
     copy_kernel<<<bank::kCopyLanes, bank::kCopyThreads, 0, s>>>(D, b->host, b->stride);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -181,7 +318,7 @@ cudaError_t launch_bank_plan_overlap(waste_bank *b, int layer, const int32_t *id
     cudaError_t e = cudaStreamWaitEvent(s, b->ev_lookahead, 0);
     if (e != cudaSuccess) return e;
     const BankDevice D = device_for(b, true);
-    plan_kernel<<<1, 32, 0, s>>>(D, layer, b->E, b->n_slots, b->stride, ids, n_ids, 1, wait_job, order);
+    launch_plan(b, D, layer, ids, n_ids, true, wait_job, order, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     lanes->D = D;

@@ -138,6 +138,35 @@ def test_repeated_expert_across_tokens(flags):
         res.close()
 
 
+@pytest.mark.parametrize("flags", [0, B.FLAG_BANK_SERIAL], ids=["overlap", "serial"])
+def test_many_ids_across_plan_chunks(flags):
+    """16 tokens x top-4 = 64 ids, planned 32 at a time: experts repeated inside and across the
+    two halves are copied once each, the repeats wait for those copies (overlap), and outputs
+    equal the resident layer's; a second call with the same routing copies nothing."""
+    w3 = synth.Workload("bank3", 512, 256, 20, 4, 16, "f32", "none")
+    res = MoELayer(w3, 3, 0, "cuda")
+    ts = TieredStack(w3, 3, 1, 20, flags=flags)
+    try:
+        h = synth.hidden(8, 16, w3.d, "f32", "cuda")
+        g = torch.Generator().manual_seed(5)
+        ids = torch.stack([torch.randperm(20, generator=g)[:4] for _ in range(16)]).to(torch.int32).cuda()
+        gate = torch.rand(16, 4, generator=g).cuda()
+        for rep in range(2):
+            a = torch.empty(16, w3.d, device="cuda")
+            b = torch.empty(16, w3.d, device="cuda")
+            ts.layers[0].forward(h, 16, ids, gate, a)
+            res.forward(h, 16, ids, gate, b)
+            torch.cuda.synchronize()
+            assert torch.equal(a, b)
+            st = ts.stats()
+            assert st["demand_misses"] == len(torch.unique(ids)), st
+            assert st["demand_hits"] == (rep + 1) * 64 - st["demand_misses"]
+        ts.layers[0].stats()
+    finally:
+        ts.close()
+        res.close()
+
+
 def test_plan_keeps_resident_experts_of_the_call():
     """4 slots, experts given to forward: {0,1,2,3} fills the cache; [4,0,1,2] then copies
     expert 4 alone, into the slot of 3 -- a miss listed before resident experts of the same
