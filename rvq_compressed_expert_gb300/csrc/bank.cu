@@ -82,16 +82,27 @@ __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E
     uint32_t clock = *D.clock;
     if (demand) clock += 1;
     const uint32_t seq = *D.seq + 1;
+    // the first 32 ids and their slots, loaded beside the slot state
+    int key0 = -1, slot0 = -1;
+    const int e0 = lane < n_ids ? ids[lane] : -1;
     for (int v = lane; v < n_slots; v += 32) {
         tick[v] = D.tick[v];
         key_of[v] = D.key_of[v];
+    }
+    if (e0 >= 0 && e0 < E) {
+        key0 = layer * E + e0;
+        slot0 = D.map[key0];
     }
     __syncwarp();
     if (lane == 0) {
         *D.clock = clock;
         *D.seq = seq;
     }
-    for (int i = lane; i < n_ids; i += 32) {
+    if (slot0 >= 0) {
+        tick[slot0] = clock;
+        D.tick[slot0] = clock;
+    }
+    for (int i = 32 + lane; i < n_ids; i += 32) {
         const int e = ids[i];
         if (e < 0 || e >= E) continue;
         const int s = D.map[layer * E + e];
@@ -118,14 +129,18 @@ __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E
     unsigned long long hits = 0, misses = 0;
     for (int i0 = 0; i0 < n_ids; i0 += 32) {
         const int i = i0 + lane;
-        int key = -1, slot = -1, wj = -1;
-        if (i < n_ids) {
-            const int e = ids[i];
-            if (e >= 0 && e < E) {
-                key = layer * E + e;
-                slot = D.map[key];
-                // placed by an earlier chunk of this plan: waits for that job
-                if (i0 > 0 && slot >= 0 && D.job_seq[slot] == seq) wj = D.job_of[slot];
+        int key = key0, slot = slot0, wj = -1;
+        if (i0 > 0) {
+            key = -1;
+            slot = -1;
+            if (i < n_ids) {
+                const int e = ids[i];
+                if (e >= 0 && e < E) {
+                    key = layer * E + e;
+                    slot = D.map[key];
+                    // placed by an earlier chunk of this plan: waits for that job
+                    if (slot >= 0 && D.job_seq[slot] == seq) wj = D.job_of[slot];
+                }
             }
         }
         const int n = min(32, n_ids - i0);
@@ -172,16 +187,11 @@ __global__ void __launch_bounds__(32) plan_kernel(BankDevice D, int layer, int E
         __syncwarp();
         plan_order(wait_job, order, n_ids, lane);
     }
-    if (lane == 0) {
+    if (lane == 0) { // reductions, so the warp does not wait for the counters' old values
         *D.n_jobs = n_jobs;
-        if (demand) {
-            D.stats[kBankDemandHits] += hits;
-            D.stats[kBankDemandMisses] += misses;
-        } else {
-            D.stats[kBankPrefetchPresent] += hits;
-            D.stats[kBankPrefetchCopies] += misses;
-        }
-        D.stats[kBankCopiedBytes] += (unsigned long long)n_jobs * stride;
+        atomicAdd(D.stats + (demand ? kBankDemandHits : kBankPrefetchPresent), hits);
+        atomicAdd(D.stats + (demand ? kBankDemandMisses : kBankPrefetchCopies), misses);
+        atomicAdd(D.stats + kBankCopiedBytes, (unsigned long long)n_jobs * stride);
     }
 }
 
@@ -267,16 +277,11 @@ __global__ void __launch_bounds__(32) plan_kernel_global(BankDevice D, int layer
         __syncwarp();
         plan_order(wait_job, order, n_ids, lane);
     }
-    if (lane == 0) {
+    if (lane == 0) { // reductions, so the warp does not wait for the counters' old values
         *D.n_jobs = n_jobs;
-        if (demand) {
-            D.stats[kBankDemandHits] += hits;
-            D.stats[kBankDemandMisses] += misses;
-        } else {
-            D.stats[kBankPrefetchPresent] += hits;
-            D.stats[kBankPrefetchCopies] += misses;
-        }
-        D.stats[kBankCopiedBytes] += (unsigned long long)n_jobs * stride;
+        atomicAdd(D.stats + (demand ? kBankDemandHits : kBankPrefetchPresent), hits);
+        atomicAdd(D.stats + (demand ? kBankDemandMisses : kBankPrefetchCopies), misses);
+        atomicAdd(D.stats + kBankCopiedBytes, (unsigned long long)n_jobs * stride);
     }
 }
 
