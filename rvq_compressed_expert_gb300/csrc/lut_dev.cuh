@@ -622,13 +622,22 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         for (; g < U.g1; g += kNW) {
             const int gn = g + kNW;
             ahead(g);
-            float acc[16];
-            lookups(wa[0], 0, acc);
-            if (gn < U.g1) load_part(gn, 0, wa);
-            if constexpr (!kDown) finish(acc, 0, g);
-            lookups(wa[1], 1, acc);
-            if (gn < U.g1) load_part(gn, 1, wa);
-            finish(acc, 1, g);
+            if constexpr (!kDown) {
+                float acc0[16], acc1[16];
+                lookups(wa[0], 0, acc0);
+                if (gn < U.g1) load_part(gn, 0, wa);
+                lookups(wa[1], 1, acc1);
+                if (gn < U.g1) load_part(gn, 1, wa);
+                finish(acc0, 0, g);
+                finish(acc1, 1, g);
+            } else {
+                float acc[16];
+                lookups(wa[0], 0, acc);
+                if (gn < U.g1) load_part(gn, 0, wa);
+                lookups(wa[1], 1, acc);
+                if (gn < U.g1) load_part(gn, 1, wa);
+                finish(acc, 1, g);
+            }
         }
     }
     // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
