@@ -167,6 +167,24 @@ def test_many_ids_across_plan_chunks(flags):
         res.close()
 
 
+def test_large_cache_plan_from_global_memory():
+    """7,000 slots (their ticks and keys do not fit the plan's shared memory, so it reads them
+    from global memory): outputs equal the resident stack's, every expert is copied once, and a
+    second token through the same layers only hits or copies the experts it has not seen."""
+    ts = TieredStack(W, 0, W.n_layers, 7000)
+    try:
+        ref = resident_outputs(3, 0)
+        got = run_tokens(DecodeStack(ts.layers, W.tokens, banked=True), 3, 0)
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
+        st = ts.stats()
+        assert st["demand_hits"] + st["demand_misses"] == 3 * W.n_layers * W.top_k
+        assert st["demand_misses"] <= W.n_layers * W.n_experts  # nothing is ever evicted
+        assert st["copied_bytes"] == st["demand_misses"] * ts.stride
+    finally:
+        ts.close()
+
+
 def test_plan_keeps_resident_experts_of_the_call():
     """4 slots, experts given to forward: {0,1,2,3} fills the cache; [4,0,1,2] then copies
     expert 4 alone, into the slot of 3 -- a miss listed before resident experts of the same
