@@ -210,7 +210,9 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
 /* Apply the selected experts and combine (0 <= T <= max_tokens).
  *   d_h      [T][d] hidden states (fp32 or bf16 per act_dtype)
  *   d_idx    [T][k] int32, d_gate [T][k] fp32 (usually route's outputs)
- *   d_out    [T][d] fp32
+ *   d_out    [T][d] fp32, any memory the device can write: device memory, or pinned
+ *            (or, where the GPU addresses it, any) host memory, which the combine then
+ *            writes over the CPU-GPU link with no separate copy
  *   mode 0: out  = sum_i gate_i * y_i
  *   mode 1: out += sum_i gate_i * y_i   (residual already in out)
  *   mode 2: out  = h + sum_i gate_i * y_i (fp32 h only; out may equal h)

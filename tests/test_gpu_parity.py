@@ -310,6 +310,26 @@ def test_one_token_routing_in_one_launch(E, k):
         layer.close()
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_output_in_pinned_host_memory(mode):
+    """The step's output written straight into pinned host memory equals the device-memory
+    output bit for bit (mode 0 =, mode 1 +=, the residual already in the host buffer)."""
+    d, f, E, k, T = 512, 264, 20, 5, 3
+    w, li, h, layer = small_layer(d, f, E, k, T)
+    try:
+        hd = h.cuda()
+        base = torch.randn(T, d, generator=torch.Generator().manual_seed(11))
+        out_dev = base.cuda()
+        out_host = base.clone().pin_memory()
+        for out in (out_dev, out_host):
+            idx, gate, logits, _ = layer.alloc_outputs(T)
+            layer.step(hd, T, idx, gate, out, mode, logits=logits)
+        torch.cuda.synchronize()
+        assert torch.equal(out_dev.cpu(), out_host)
+    finally:
+        layer.close()
+
+
 def test_bad_record_header_refused():
     """create refuses a bank whose header has a wrong magic, expert id, layer or offset."""
     d, f, E, k, T = 256, 128, 8, 2, 1
