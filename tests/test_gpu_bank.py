@@ -185,6 +185,48 @@ def test_large_cache_plan_from_global_memory():
         ts.close()
 
 
+@pytest.mark.parametrize("flags", [0, B.FLAG_BANK_SERIAL], ids=["overlap", "serial"])
+def test_full_size_records(flags):
+    """The decode shape (d=7168, f=1536, 12.4 MB records, 190 copy chunks each): 2 layers x 20
+    experts, top-16, behind 24 slots (each layer's 16 experts evict the other's); four tokens
+    through the banked stack equal the resident stack bit for bit."""
+    wf = synth.Workload("bankf", 7168, 1536, 20, 16, 1, "f32", "offsets", n_layers=2, lookahead=4)
+    layers = [MoELayer(wf, 0, L, "cuda") for L in range(2)]
+    try:
+        ref = run_tokens_w(DecodeStack(layers, 1), wf, 4, 0)
+    finally:
+        for l in layers:
+            l.close()
+    ts = TieredStack(wf, 0, 2, 24, flags=flags)
+    try:
+        got = run_tokens_w(DecodeStack(ts.layers, 1, banked=True), wf, 4, 0)
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
+        st = ts.stats()
+        assert st["demand_hits"] + st["demand_misses"] == 4 * 2 * 16
+        assert st["demand_misses"] >= 16 + 16
+        for ml in ts.layers:
+            ml.stats()
+    finally:
+        ts.close()
+
+
+def run_tokens_w(stack, w, tokens, lookahead):
+    main = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    main.wait_stream(torch.cuda.current_stream())
+    outs = []
+    for i in range(tokens):
+        with torch.cuda.stream(main):
+            h0 = synth.hidden(70 + i, w.tokens, w.d, "f32", "cuda")
+        out = stack.run(h0, lookahead, main, side)
+        with torch.cuda.stream(main):
+            outs.append(out.clone())
+    torch.cuda.current_stream().wait_stream(main)
+    torch.cuda.synchronize()
+    return outs
+
+
 def test_plan_keeps_resident_experts_of_the_call():
     """4 slots, experts given to forward: {0,1,2,3} fills the cache; [4,0,1,2] then copies
     expert 4 alone, into the slot of 3 -- a miss listed before resident experts of the same
