@@ -330,6 +330,37 @@ def test_output_in_pinned_host_memory(mode):
         layer.close()
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_largest_expert_count_and_top_k(T):
+    """The configuration's limits: E = 4096 experts, top-32 (1,024 router CTAs; for one token the
+    last of them takes the top-k, for three the top-k kernel does): logits, routing, gates and
+    outputs against the oracle; plus the top-k alone on tied integer logits over 4096 experts."""
+    d, f, E, k = 64, 16, 4096, 32
+    w = synth.Workload("maxE", d, f, E, k, T, "f32", "offsets", bias_spacing=40.0)
+    li = synth.layer_inputs(w, 5, 0, "cpu", with_codes=True)
+    h = synth.hidden(6, T, d, "f32", "cpu")
+    layer = MoELayer(w, 5, 0, "cuda", inputs=li)
+    try:
+        g_idx, g_gate, g_logits, g_out = run(layer, h.cuda(), T)
+        ref = oracle.moe_layer(h, li.router_w, li.router_b, li.codebooks, li.codes, k)
+        np.testing.assert_allclose(g_logits, ref["logits"], rtol=1e-5, atol=1e-5)
+        ok = check_routing(g_idx, g_gate, ref["logits"], k)
+        assert ok, "no well-separated token"
+        assert_close(g_out[ok], ref["out"][ok])
+    finally:
+        layer.close()
+    L = np.random.default_rng(1).integers(-4, 5, (2, E)).astype(np.float32)
+    dl = torch.tensor(L).cuda()
+    idx = torch.empty(2, k, dtype=torch.int32, device="cuda")
+    gate = torch.empty(2, k, dtype=torch.float32, device="cuda")
+    B.waste_moe_topk_from_logits(dl, 2, E, k, idx, gate)
+    torch.cuda.synchronize()
+    for t in range(2):
+        ridx, rg = oracle.topk_softmax(L[t].astype(np.float64), k)
+        np.testing.assert_array_equal(idx[t].cpu().numpy(), ridx)
+        np.testing.assert_allclose(gate[t].cpu().numpy(), rg, rtol=1e-6, atol=1e-7)
+
+
 def test_bad_record_header_refused():
     """create refuses a bank whose header has a wrong magic, expert id, layer or offset."""
     d, f, E, k, T = 256, 128, 8, 2, 1
