@@ -227,6 +227,72 @@ def run_tokens_w(stack, w, tokens, lookahead):
     return outs
 
 
+class LruModel:
+    """The bank's replacement policy as documented: a demand call advances the clock; every
+    requested expert already cached takes the call's stamp; then, in order, each miss takes the
+    least (tick, slot) among slots stamped before the call (none left: not placed)."""
+
+    def __init__(self, n_slots):
+        self.tick = [0] * n_slots
+        self.key_of = [-1] * n_slots
+        self.slot_of = {}
+        self.clock = 0
+        self.hits = self.misses = 0
+
+    def demand(self, keys):
+        self.clock += 1
+        c = self.clock
+        for k in keys:
+            if k in self.slot_of:
+                self.tick[self.slot_of[k]] = c
+        for k in keys:
+            if k in self.slot_of:
+                self.hits += 1
+                continue
+            free = [(t, v) for v, t in enumerate(self.tick) if t < c]
+            if not free:
+                continue
+            _, v = min(free)
+            if self.key_of[v] >= 0:
+                del self.slot_of[self.key_of[v]]
+            self.slot_of[k] = v
+            self.key_of[v] = k
+            self.tick[v] = c
+            self.misses += 1
+
+
+@pytest.mark.parametrize("flags", [0, B.FLAG_BANK_SERIAL], ids=["overlap", "serial"])
+def test_replacement_follows_the_lru_model(flags):
+    """40 random calls (1-2 tokens, top-4 of 12 experts, repeats within and across tokens) on
+    2 layers sharing 8 slots: after every call the device's hit and miss counts equal the
+    model's, and the outputs equal the resident layers'."""
+    w4 = synth.Workload("bank4", 512, 256, 12, 4, 2, "f32", "none", n_layers=2)
+    res = [MoELayer(w4, 4, L, "cuda") for L in range(2)]
+    ts = TieredStack(w4, 4, 2, 8, flags=flags)
+    model = LruModel(8)
+    g = torch.Generator().manual_seed(9)
+    try:
+        for call in range(40):
+            L = int(torch.randint(0, 2, (1,), generator=g))
+            T = int(torch.randint(1, 3, (1,), generator=g))
+            ids = torch.stack([torch.randperm(12, generator=g)[:4] for _ in range(T)]).to(torch.int32)
+            gate = torch.rand(T, 4, generator=g).cuda()
+            h = synth.hidden(100 + call, T, w4.d, "f32", "cuda")
+            a = torch.empty(T, w4.d, device="cuda")
+            b = torch.empty(T, w4.d, device="cuda")
+            ts.layers[L].forward(h, T, ids.cuda(), gate, a)
+            res[L].forward(h, T, ids.cuda(), gate, b)
+            torch.cuda.synchronize()
+            assert torch.equal(a, b), call
+            model.demand([L * 12 + int(e) for e in ids.reshape(-1)])
+            st = ts.stats()
+            assert (st["demand_hits"], st["demand_misses"]) == (model.hits, model.misses), (call, st)
+    finally:
+        ts.close()
+        for l in res:
+            l.close()
+
+
 def test_plan_keeps_resident_experts_of_the_call():
     """4 slots, experts given to forward: {0,1,2,3} fills the cache; [4,0,1,2] then copies
     expert 4 alone, into the slot of 3 -- a miss listed before resident experts of the same
