@@ -238,16 +238,29 @@ class LruModel:
         self.slot_of = {}
         self.clock = 0
         self.hits = self.misses = 0
+        self.present = self.copies = 0
 
     def demand(self, keys):
         self.clock += 1
+        h, m = self._plan(keys)
+        self.hits += h
+        self.misses += m
+
+    def lookahead(self, keys):
+        """A lookahead fetch plans at the current clock (it does not advance it)."""
+        h, m = self._plan(keys)
+        self.present += h
+        self.copies += m
+
+    def _plan(self, keys):
         c = self.clock
+        hits = misses = 0
         for k in keys:
             if k in self.slot_of:
                 self.tick[self.slot_of[k]] = c
         for k in keys:
             if k in self.slot_of:
-                self.hits += 1
+                hits += 1
                 continue
             free = [(t, v) for v, t in enumerate(self.tick) if t < c]
             if not free:
@@ -258,14 +271,16 @@ class LruModel:
             self.slot_of[k] = v
             self.key_of[v] = k
             self.tick[v] = c
-            self.misses += 1
+            misses += 1
+        return hits, misses
 
 
 @pytest.mark.parametrize("flags", [0, B.FLAG_BANK_SERIAL], ids=["overlap", "serial"])
 def test_replacement_follows_the_lru_model(flags):
     """40 random calls (1-2 tokens, top-4 of 12 experts, repeats within and across tokens) on
-    2 layers sharing 8 slots: after every call the device's hit and miss counts equal the
-    model's, and the outputs equal the resident layers'."""
+    2 layers sharing 8 slots, most followed by a lookahead of 1-3 experts into the other layer:
+    after every call the device's hit / miss and present / copied counts equal the model's, and
+    the outputs equal the resident layers'."""
     w4 = synth.Workload("bank4", 512, 256, 12, 4, 2, "f32", "none", n_layers=2)
     res = [MoELayer(w4, 4, L, "cuda") for L in range(2)]
     ts = TieredStack(w4, 4, 2, 8, flags=flags)
@@ -285,8 +300,19 @@ def test_replacement_follows_the_lru_model(flags):
             torch.cuda.synchronize()
             assert torch.equal(a, b), call
             model.demand([L * 12 + int(e) for e in ids.reshape(-1)])
+            # now and then a lookahead into the other layer: its top-P of the same token
+            P = int(torch.randint(0, 4, (1,), generator=g))
+            if P:
+                o = 1 - L
+                pidx = torch.empty(T, 4, dtype=torch.int32, device="cuda")
+                pgate = torch.empty(T, 4, device="cuda")
+                ts.layers[o].route(h, T, pidx, pgate)
+                ts.layers[o].prefetch(h, T, P)
+                torch.cuda.synchronize()
+                model.lookahead([o * 12 + int(e) for e in pidx[:, :P].reshape(-1).cpu()])
             st = ts.stats()
             assert (st["demand_hits"], st["demand_misses"]) == (model.hits, model.misses), (call, st)
+            assert (st["prefetch_present"], st["prefetch_copies"]) == (model.present, model.copies), (call, st)
     finally:
         ts.close()
         for l in res:
