@@ -463,7 +463,8 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
     RouteTopk F{h->W.route_done, h->L.k, d_idx, d_gate, h->W.pred_idx, h->W.pred_count, pred_stride, h->W.stats,
                 router_bytes};
     bool fused = false;
-    cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s, h->W.router_part, h->num_sms, &F, &fused);
+    cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s, h->W.router_part, h->num_sms, &F, &fused,
+                                  h->W.err);
     if (e != cudaSuccess) return cuda_fail(e, "router kernel");
     if (h->profiling) cudaEventRecord(h->route_tm.ev[1], s);
     if (!fused) {
@@ -597,7 +598,8 @@ int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_
         return fail(WASTE_EINVAL, "n_prefetch = %d above min(n_experts, %d)", P, kMaxTopK);
     if (T == 0 || P == 0) return ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(side);
-    cudaError_t e = launch_router(h->L, d_h, T, h->W.pred_logits, nullptr, s, h->W.router_part, h->num_sms);
+    cudaError_t e = launch_router(h->L, d_h, T, h->W.pred_logits, nullptr, s, h->W.router_part, h->num_sms,
+                                  nullptr, nullptr, h->W.err);
     if (e != cudaSuccess) return cuda_fail(e, "lookahead router");
     e = launch_topk(h->W.pred_logits, nullptr, T, h->L.E, P, h->W.pred_idx, h->W.pred_gate_sel, nullptr,
                     nullptr, 1, nullptr, 0, s);

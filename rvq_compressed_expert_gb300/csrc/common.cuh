@@ -163,11 +163,12 @@ struct Workspace {
 // logits + logits_lo equals W_r h + b exactly given the fp32 dot product.
 // part (optional): [kRouterMaxSplits][T][E] scratch for the split-K router of T > 16.
 constexpr int kRouterMaxSplits = 32;
-// With fuse (and T <= 16): the staged router's last CTA also takes the top-k, and *fused
-// says so (else the caller launches the top-k).
+// With fuse (and T == 1): the router's last CTA also takes the top-k, and *fused says so
+// (else the caller launches the top-k).  err (optional): sticky device error bits (a bounded
+// wait that gave up sets kErrTimeout).
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
                           float *logits_lo, cudaStream_t s, float *part = nullptr, int num_sms = 1,
-                          const RouteTopk *fuse = nullptr, bool *fused = nullptr);
+                          const RouteTopk *fuse = nullptr, bool *fused = nullptr, uint32_t *err = nullptr);
 cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int E, int k,
                         int32_t *idx, float *gate, const int32_t *pred_idx, int32_t *pred_count,
                         int pred_stride, unsigned long long *stats,

@@ -332,6 +332,10 @@ __device__ __forceinline__ uint32_t float_key(float x) {
     const uint32_t b = __float_as_uint(x);
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+// Its inverse: the float whose key is k.
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
 
 // Top-k and softmax of token t by a whole CTA: a bitonic sort of the E experts on the key
 // (logit hi, then lo, descending; index ascending), then warp 0 forms the gates exactly
@@ -410,13 +414,28 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits,
     const float *lrow = logits + (size_t)t * E;
     const float *lo_row = logits_lo ? logits_lo + (size_t)t * E : nullptr;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    // warp 0 asks for the token's predicted experts now; they arrive during the sort
+    int P = 0, pred_l = -1;
+    if (warp == 0 && pred_count != nullptr) {
+        P = pred_count[t];
+        if (lane < pred_stride && lane < P) pred_l = pred_idx[(size_t)t * pred_stride + lane];
+    }
     Cand best;
     best.key = 0ull;
     best.id = 0x7fffffff;
-    for (int c0 = warp * 32; c0 < E; c0 += nw * 32) {
-        Cand v = load_cand(lrow, lo_row, E, c0 + lane);
-        warp_sort32(v);
-        best = warp_merge32(best, v);
+    // the warp's chunks c0, c0 + nw * 32, ...: the loads of three chunks in flight at once
+    // (the selection is a total order, so the merge order does not change the result)
+    constexpr int kAhead = 3;
+    for (int c0 = warp * 32; c0 < E; c0 += kAhead * nw * 32) {
+        Cand v[kAhead];
+#pragma unroll
+        for (int q = 0; q < kAhead; ++q) v[q] = load_cand(lrow, lo_row, E, c0 + q * nw * 32 + lane);
+#pragma unroll
+        for (int q = 0; q < kAhead; ++q)
+            if (c0 + q * nw * 32 < E) {
+                warp_sort32(v[q]);
+                best = warp_merge32(best, v[q]);
+            }
     }
     keys[warp * 32 + lane] = best.key;
     ids[warp * 32 + lane] = best.id;
@@ -440,13 +459,11 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits,
         int my_idx = -1;
         float my_hi = 0.f, my_lo = 0.f;
         if (lane < k) {
+            // the selected logit and remainder, as load_cand normalised them, back from the key
             my_idx = ids[lane];
-            float a = __ldcg(lrow + my_idx), b = logits_lo ? __ldcg(logits_lo + (size_t)t * E + my_idx) : 0.f;
-            if (a != a) a = -INFINITY;
-            if (a == 0.f) a = 0.f;
-            if (b != b || b == 0.f) b = 0.f;
-            my_hi = a;
-            my_lo = b;
+            const unsigned long long key = keys[lane];
+            my_hi = key_float((uint32_t)(key >> 32));
+            my_lo = key_float((uint32_t)key);
         }
         const float h0 = __shfl_sync(0xffffffffu, my_hi, 0);
         const float l0 = __shfl_sync(0xffffffffu, my_lo, 0);
@@ -460,10 +477,9 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits,
             gate[(size_t)t * k + lane] = ex / sum;
         }
         if (pred_count != nullptr) {
-            const int P = pred_count[t];
             bool hit = false;
-            if (lane < k)
-                for (int p = 0; p < P; ++p) hit |= (pred_idx[(size_t)t * pred_stride + p] == my_idx);
+            for (int p = 0; p < P && p < 32; ++p) hit |= (__shfl_sync(0xffffffffu, pred_l, p) == my_idx);
+            hit = hit && lane < k;
             const unsigned hits = __popc(__ballot_sync(0xffffffffu, hit));
             __syncwarp();
             if (lane == 0) {

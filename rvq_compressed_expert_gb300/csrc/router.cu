@@ -7,6 +7,7 @@
 // prédiction du routeur").  Order: logit descending, lowest index first on
 // equal logits; gates: softmax over the k selected logits.
 #include "route_dev.cuh"
+#include "tc_dev.cuh"
 
 #include <algorithm>
 
@@ -204,6 +205,109 @@ __global__ void __launch_bounds__(128 * kRows) router_staged_kernel(const float 
     if (threadIdx.x == 0) *F.done = 0u;
 }
 
+// Adds one to a counter with acquire-release semantics at GPU scope and returns the old value:
+// the calling CTA's writes ordered before it by a barrier are published with it, and every
+// CTA that counted before is visible after it.
+__device__ __forceinline__ unsigned count_acq_rel(unsigned *c) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(c) : "memory");
+    return old;
+}
+
+// One token (decode): kRows expert rows per CTA of 128 threads (4 warps) per row.  Thread 0
+// moves the rows of W_r and the token's h into shared memory with bulk copies (all of the
+// rows' bytes in flight at once); the lanes then form router_block_staged's products in its
+// order (per lane the float4s sub * 32 + lane + 128 u in turn, the warp's xor tree, the 4
+// warps' sums in order), so the logits equal the staged kernel's bit for bit.  With F.done
+// set, the last CTA to count itself also takes the top-k and gates; the count is one
+// acquire-release atomic (no separate fences).  A copy that does not land within the
+// bounded wait sets kErrTimeout in err; the CTA still counts itself, so the counter comes
+// back to rest.
+template <bool kBf16, int kRows>
+__global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__restrict__ W,
+                                                                const float *__restrict__ bias,
+                                                                const void *__restrict__ h, int E, int d,
+                                                                float *__restrict__ logits,
+                                                                float *__restrict__ logits_lo, const RouteTopk F,
+                                                                uint32_t *err) {
+    constexpr int kBig = 16;
+    extern __shared__ __align__(16) unsigned char t1_smem[];
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ float red[kRows][4];
+    __shared__ unsigned long long keys[128 * kRows];
+    __shared__ int ids[128 * kRows];
+    __shared__ int last;
+    const int row0 = blockIdx.x * kRows;
+    const int rows = min(kRows, E - row0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rl = warp >> 2, sub = warp & 3;
+    const uint32_t wbytes = (uint32_t)d * 4u, hbytes = (uint32_t)d * (kBf16 ? 2u : 4u);
+    const unsigned char *hs = t1_smem + (size_t)kRows * wbytes;
+    const uint32_t mb = (uint32_t)__cvta_generic_to_shared(&bar);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(mb, 1);
+        tc::mbar_init_fence();
+        tc::mbar_arrive_expect_tx(mb, (uint32_t)rows * wbytes + hbytes);
+        const uint32_t s0 = (uint32_t)__cvta_generic_to_shared(t1_smem);
+        tc::bulk_g2s(s0 + (uint32_t)kRows * wbytes, h, hbytes, mb);
+        for (int r = 0; r < rows; ++r) tc::bulk_g2s(s0 + (uint32_t)r * wbytes, W + (size_t)(row0 + r) * d, wbytes, mb);
+    }
+    __syncthreads(); // the barrier is initialised
+    if (!tc::mbar_wait(mb, 0)) {
+        if (threadIdx.x == 0 && err) atomicOr(err, kErrTimeout);
+        tc::mbar_wait(mb, 0); // the copies in flight target this CTA's shared memory
+    }
+    const float4 *ws = reinterpret_cast<const float4 *>(t1_smem + (size_t)rl * wbytes);
+    const int d4 = d >> 2;
+    const int per_lane = (d4 + 127) / 128;
+    float acc = 0.f;
+    if (rl < rows) {
+        for (int m0 = 0; m0 < per_lane; m0 += kBig) {
+#pragma unroll
+            for (int u = 0; u < kBig; ++u) {
+                const int i4 = sub * 32 + lane + 128 * (m0 + u);
+                const int ic = min(i4, d4 - 1);
+                const float4 w = ws[ic];
+                float4 x;
+                if constexpr (kBf16) {
+                    const uint2 raw = reinterpret_cast<const uint2 *>(hs)[ic];
+                    const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+                    const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+                    x = make_float4(fa.x, fa.y, fb.x, fb.y);
+                } else {
+                    x = reinterpret_cast<const float4 *>(hs)[ic];
+                }
+                float p = w.x * x.x;
+                p = fmaf(w.y, x.y, p);
+                p = fmaf(w.z, x.z, p);
+                p = fmaf(w.w, x.w, p);
+                acc = fmaf(i4 < d4 ? 1.f : 0.f, p, acc);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) red[rl][sub] = acc;
+    __syncthreads();
+    if (threadIdx.x < rows) {
+        const int r = row0 + (int)threadIdx.x;
+        const float *q = red[threadIdx.x];
+        const float v = ((q[0] + q[1]) + q[2]) + q[3];
+        float hi = v, lo = 0.f;
+        if (bias) two_sum(v, bias[r], hi, lo);
+        logits[r] = hi;
+        if (logits_lo) logits_lo[r] = lo;
+    }
+    if (!F.done) return;
+    __syncthreads(); // this CTA's logits before its count
+    if (threadIdx.x == 0) last = count_acq_rel(F.done) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    topk_block(logits, logits_lo, E, F.k, 0, F.idx, F.gate, F.pred_idx, F.pred_count, F.pred_stride, F.stats,
+               F.router_bytes, keys, ids);
+    if (threadIdx.x == 0) *F.done = 0u;
+}
+
 // Top-k of one token per CTA of 512 threads: per-warp sorted candidate lists merged in a
 // tree (same selection and gates as the step kernel's top-k item).
 __global__ void __launch_bounds__(512) topk_cta_kernel(const float *__restrict__ logits,
@@ -294,6 +398,15 @@ constexpr size_t kRouterStageMax = 200 * 1024; // shared memory for staged hidde
 // Expert rows per CTA of the staged router (measured on GB300 at E = 384: four rows per
 // CTA of 512 threads ran faster than two per CTA of 256).
 constexpr int kStagedRows = 4;
+// Expert rows per CTA of the one-token router, and its shared memory (the rows of W_r and h):
+// up to d = 10,240 with fp32 hidden states.
+#ifndef WM_T1_ROWS
+#define WM_T1_ROWS 3
+#endif
+constexpr int kT1Rows = WM_T1_ROWS;
+constexpr size_t kT1SmemMax = 160 * 1024;
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
 int router_splits(int T, int E, int d, int num_sms) {
     const int tiles = ((E + kTileE - 1) / kTileE) * ((T + kTileT - 1) / kTileT);
@@ -306,7 +419,7 @@ int router_splits(int T, int E, int d, int num_sms) {
 
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
                           float *logits_lo, cudaStream_t s, float *part, int num_sms, const RouteTopk *fuse,
-                          bool *fused) {
+                          bool *fused, uint32_t *err) {
     const size_t row_bytes = (size_t)L.d * 4;
     if (fused) *fused = false;
     if (T <= 16 && row_bytes <= kRouterStageMax) {
@@ -324,6 +437,26 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
             cudaFuncSetAttribute(router_staged_kernel<false, kStagedRows>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterStageMax);
             attr = true;
+        }
+        const size_t t1_smem = (size_t)L.d * (4 * kT1Rows + (L.act_bf16 ? 2 : 4));
+        if (T == 1 && t1_smem <= kT1SmemMax && aligned16(L.router_w) && aligned16(h)) {
+            static bool attr1 = false;
+            if (!attr1) {
+                cudaFuncSetAttribute(router_t1_kernel<true, kT1Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kT1SmemMax);
+                cudaFuncSetAttribute(router_t1_kernel<false, kT1Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kT1SmemMax);
+                attr1 = true;
+            }
+            const RouteTopk F = fuse ? *fuse : RouteTopk{};
+            const dim3 grid1((L.E + kT1Rows - 1) / kT1Rows);
+            if (L.act_bf16)
+                router_t1_kernel<true, kT1Rows><<<grid1, 128 * kT1Rows, t1_smem, s>>>(
+                    L.router_w, L.router_b, h, L.E, L.d, logits, logits_lo, F, err);
+            else
+                router_t1_kernel<false, kT1Rows><<<grid1, 128 * kT1Rows, t1_smem, s>>>(
+                    L.router_w, L.router_b, h, L.E, L.d, logits, logits_lo, F, err);
+            return cudaGetLastError();
         }
         dim3 grid((L.E + kStagedRows - 1) / kStagedRows);
         if (L.act_bf16)

@@ -287,15 +287,16 @@ def test_deterministic():
         layer.close()
 
 
-@pytest.mark.parametrize("E, k", [(384, 16), (12, 3), (4, 4)])
-def test_one_token_routing_in_one_launch(E, k):
-    """One token is routed in a single launch (the router's last CTA takes the top-k); the same
-    token inside a batch of three goes through the router and the top-k kernel: indices,
+@pytest.mark.parametrize("d, E, k, act", [(512, 384, 16, "f32"), (512, 12, 3, "f32"), (512, 4, 4, "f32"),
+                                          (7168, 384, 16, "f32"), (7168, 384, 16, "bf16"), (8, 4, 2, "bf16")])
+def test_one_token_routing_in_one_launch(d, E, k, act):
+    """One token is routed in a single launch (one CTA per expert row, the row and the token
+    moved into shared memory by bulk copies; the last CTA takes the top-k); the same token
+    inside a batch of three goes through the staged router and the top-k kernel: indices,
     gates and logits agree bit for bit, and the counter is back at rest for the next call."""
-    d = 512
-    w = synth.Workload("r1", d, 64, E, k, 3, "f32", "offsets")
+    w = synth.Workload("r1", d, 64, E, k, 3, act, "offsets")
     li = synth.layer_inputs(w, 4, 0, "cpu", with_codes=True)
-    h = synth.hidden(9, 3, d, "f32", "cpu").cuda()
+    h = synth.hidden(9, 3, d, act, "cpu").cuda()
     layer = MoELayer(w, 4, 0, "cuda", inputs=li)
     try:
         for rep in range(3):
