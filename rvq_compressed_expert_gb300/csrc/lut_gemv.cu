@@ -64,72 +64,56 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
 }
 
 // out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair],
-// slots in rank order and pairs in order.  NP = number of pairs (0: any, read in a loop):
-// with NP fixed every partial of a batch of 16 slots is loaded before any is summed.
-constexpr int kCombineThreads = 64; // small CTAs: the partial loads spread over more SMs
-
+// slots in rank order and pairs in order.  A CTA takes 32 rows of one token with one warp per
+// slot: lane l of warp i sums slot i's pairs of row l (every load of the launch in flight at
+// once, one round trip), and warp 0 adds the slots in rank order.  NP = number of pairs (0:
+// any, read in a loop).  one_part: slots whose single partial is their whole output (the
+// tensor-core slots of a batched call).
 template <int NP>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ part_dn,
-                                                      const int32_t *__restrict__ idx,
-                                                      const float *__restrict__ gate,
-                                                      const float *__restrict__ h,
-                                                      float *__restrict__ out, int d, int k, int E,
-                                                      int npair_rt, int mode,
-                                                      unsigned long long *stats,
-                                                      unsigned long long slots,
-                                                      const uint8_t *__restrict__ one_part) {
+__global__ void __launch_bounds__(32 * kMaxTopK) combine_kernel(const float *__restrict__ part_dn,
+                                                                const int32_t *__restrict__ idx,
+                                                                const float *__restrict__ gate,
+                                                                const float *__restrict__ h,
+                                                                float *__restrict__ out, int d, int k, int E,
+                                                                int npair_rt, int mode,
+                                                                unsigned long long *stats,
+                                                                unsigned long long slots,
+                                                                const uint8_t *__restrict__ one_part) {
+    __shared__ float sv[kMaxTopK][32];
+    __shared__ float gs[kMaxTopK];
+    __shared__ int oks[kMaxTopK];
     const int t = blockIdx.y;
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (stats && r == 0 && t == 0) atomicAdd(stats + kStatForwardSlots, slots);
-    if (r >= d) return;
+    const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 32 + lane;
+    if (stats && blockIdx.x == 0 && t == 0 && threadIdx.x == 0) atomicAdd(stats + kStatForwardSlots, slots);
     const int npair = NP ? NP : npair_rt;
-    float y = 0.f;
-    for (int i0 = 0; i0 < k; i0 += 16) {
-        float sv[16], gv[16];
-        bool ok[16];
+    const size_t si = (size_t)t * k + i;
+    if (r < d) {
+        const float *p = part_dn + si * npair * d + r;
+        float s = 0.f;
         if constexpr (NP > 0) {
-            float pv[16][NP > 0 ? NP : 1];
+            float pv[NP];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int i = min(i0 + u, k - 1);
-                const float *p = part_dn + ((size_t)t * k + i) * NP * d + r;
+            for (int q = 0; q < NP; ++q) pv[q] = p[(size_t)q * d];
 #pragma unroll
-                for (int q = 0; q < NP; ++q) pv[u][q] = p[(size_t)q * d];
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                float s = 0.f;
-#pragma unroll
-                for (int q = 0; q < NP; ++q) s += pv[u][q];
-                sv[u] = s;
-            }
-            if (one_part) {
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (one_part[(size_t)t * k + min(i0 + u, k - 1)]) sv[u] = pv[u][0];
-            }
+            for (int q = 0; q < NP; ++q) s += pv[q];
+            if (one_part && one_part[si]) s = pv[0];
         } else {
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int i = min(i0 + u, k - 1);
-                const float *p = part_dn + ((size_t)t * k + i) * npair * d + r;
-                const int nq = (one_part && one_part[(size_t)t * k + i]) ? 1 : npair;
-                float s = 0.f;
-                for (int q = 0; q < nq; ++q) s += p[(size_t)q * d];
-                sv[u] = s;
-            }
+            const int nq = (one_part && one_part[si]) ? 1 : npair;
+            for (int q = 0; q < nq; ++q) s += p[(size_t)q * d];
         }
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int i = min(i0 + u, k - 1);
-            const int e = idx[(size_t)t * k + i];
-            ok[u] = (i0 + u < k) && e >= 0 && e < E;
-            gv[u] = gate[(size_t)t * k + i];
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-            if (ok[u]) y = fmaf(gv[u], sv[u], y);
+        sv[i][lane] = s;
     }
+    if (lane == 0) {
+        const int e = idx[si];
+        oks[i] = e >= 0 && e < E;
+        gs[i] = gate[si];
+    }
+    __syncthreads();
+    if (i != 0 || r >= d) return;
+    float y = 0.f;
+    for (int j = 0; j < k; ++j)
+        if (oks[j]) y = fmaf(gs[j], sv[j][lane], y);
     const size_t o = (size_t)t * d + r;
     if (mode == 0) out[o] = y;
     else if (mode == 1) out[o] = out[o] + y;
@@ -234,11 +218,11 @@ cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h
                            const int32_t *idx, const float *gate, float *out, int mode,
                            const uint8_t *one_part, int nparts, cudaStream_t s) {
     const unsigned long long slots = (unsigned long long)T * L.k;
-    dim3 grid((L.d + kCombineThreads - 1) / kCombineThreads, T);
+    dim3 grid((L.d + 31) / 32, T);
     const float *h32 = reinterpret_cast<const float *>(h);
     switch (nparts) {
 #define WM_COMBINE(NP)                                                                               \
-    combine_kernel<NP><<<grid, kCombineThreads, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, nparts, \
+    combine_kernel<NP><<<grid, 32 * L.k, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, nparts, \
                                                         mode, W.stats, slots, one_part)
     case 1: WM_COMBINE(1); break;
     case 2: WM_COMBINE(2); break;
