@@ -438,8 +438,11 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterStageMax);
             attr = true;
         }
+        // the one-token kernel only for the demand route (fuse): its CTAs hold ~113 KiB of
+        // shared memory and cannot run beside the expert kernels, which the lookahead's router
+        // (another stream, no fuse) does on the staged kernel's 28 KiB (the same logits)
         const size_t t1_smem = (size_t)L.d * (4 * kT1Rows + (L.act_bf16 ? 2 : 4));
-        if (T == 1 && t1_smem <= kT1SmemMax && aligned16(L.router_w) && aligned16(h)) {
+        if (T == 1 && fuse && fused && t1_smem <= kT1SmemMax && aligned16(L.router_w) && aligned16(h)) {
             static bool attr1 = false;
             if (!attr1) {
                 cudaFuncSetAttribute(router_t1_kernel<true, kT1Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
