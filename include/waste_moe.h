@@ -203,7 +203,10 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
  *   d_logits [T][E] fp32 out, or NULL (then kept in the workspace)
  * If waste_moe_prefetch ran for this layer (ordered before this call by the
  * caller), the number of predicted experts among the selected ones is added to
- * the prediction_hits statistic. */
+ * the prediction_hits statistic.  One token (T == 1) is routed in one launch whose
+ * CTAs move their rows of W_r and the token into shared memory with bulk copies;
+ * a copy that does not land within a bounded wait (about a second) leaves the
+ * outputs undefined and makes waste_moe_stats return WASTE_ETIMEOUT. */
 int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, float *d_gate,
                     float *d_logits, waste_stream_t stream);
 
