@@ -955,6 +955,39 @@ def profile_encoder():
     print("encoder profile case: squared error after each stage", err.tolist())
 
 
+def profile_route(args):
+    """Small case for ncu captures of the one-token router: the decode layer's router (d=7168,
+    E=384, top-16, fp32 h) over narrow experts (f=256, 0.8 GB of records), `--warmup` then
+    `--steps` one-token routes, each a CUDA-graph replay after an L2 flush."""
+    from rvq_compressed_expert_gb300 import _build
+    from rvq_compressed_expert_gb300 import binding as B
+    from rvq_compressed_expert_gb300 import synth
+    from rvq_compressed_expert_gb300.layer import MoELayer
+    _build.build()
+    B.load()
+    w = synth.Workload("route-e384", 7168, 256, 384, 16, 1, "f32", "offsets")
+    layer = MoELayer(w, seed=0, layer=0, device="cuda")
+    idx, gate, logits, _ = layer.alloc_outputs(1)
+    h = synth.hidden(3, 1, w.d, "f32", "cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer.route(h, 1, idx, gate, logits)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.route(h, 1, idx, gate, logits)
+    for _ in range(args.warmup + args.steps):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    layer.stats()  # raises if a device wait gave up
+    layer.close()
+    print("route profile case done")
+
+
 def print_unit_trace(tr, w):
     """Per-phase summary of the lookup kernels' unit trace: table build and row streaming."""
     import math as _m
@@ -1036,6 +1069,8 @@ def main():
                     help="with --profile-case: print the step kernel's item timeline")
     ap.add_argument("--profile-encoder", action="store_true",
                     help="train one 1536 x 7168 matrix with the RVQ encoder (2 Lloyd rounds) for ncu and exit")
+    ap.add_argument("--profile-route", action="store_true",
+                    help="route one token through the decode layer's router (graph replays) for ncu and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1044,6 +1079,9 @@ def main():
         return
     if args.profile_encoder:
         profile_encoder()
+        return
+    if args.profile_route:
+        profile_route(args)
         return
     if args.impl == "reference":
         reference(args)
