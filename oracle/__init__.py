@@ -58,6 +58,8 @@ def _bind(lib):
     lib.oracle_moe_layer.argtypes = [_i, _i, _i, _i, _i, _fp, _fp, _fp, _u8p, _u8p, _u8p,
                                      _dp, _i, _i, _dp, _dp, _i32p, _dp]
     lib.oracle_rmsnorm.argtypes = [_i, _dp, _dp]
+    lib.oracle_residual_layer.argtypes = [_i, _i, _i, _i, _i, _fp, _fp, _fp, _u8p, _u8p, _u8p,
+                                          _dp, _i, _dp, _i32p, _dp]
     lib.oracle_expert_code_bytes.argtypes = [_i, _i]
     lib.oracle_expert_code_bytes.restype = ctypes.c_uint64
     lib.oracle_crc32.argtypes = [_u8p, ctypes.c_size_t]
@@ -199,21 +201,65 @@ def rmsnorm(x):
     return out
 
 
+def residual_layer(h, Wr, bias, cbs, codes, k, use_lut=True):
+    """One layer of the decode chain on all tokens: h_t <- h_t + MoE(rmsnorm(h_t)).
+
+    h [T,d] (not modified); codes = (gate [E,f,3,d/8], up [E,f,3,d/8], down [E,d,3,f/8]).
+    Returns dict(h [T,d] after the layer, logits [T,E], idx [T,k], gate [T,k]).
+    """
+    h = _np(h, np.float64).copy()
+    Wr = _np(Wr, np.float32)
+    cbs = _np(cbs, np.float32)
+    gc, uc, dc = (_np(c, np.uint8) for c in codes)
+    b = None if bias is None else _np(bias, np.float32)
+    T, d = h.shape
+    E = Wr.shape[0]
+    f = gc.shape[1]
+    logits = np.empty((T, E), np.float64)
+    idx = np.empty((T, k), np.int32)
+    gate = np.empty((T, k), np.float64)
+    _load().oracle_residual_layer(T, d, f, E, k, _ptr(Wr, ctypes.c_float),
+                                  None if b is None else _ptr(b, ctypes.c_float),
+                                  _ptr(cbs, ctypes.c_float), _ptr(gc, ctypes.c_uint8),
+                                  _ptr(uc, ctypes.c_uint8), _ptr(dc, ctypes.c_uint8),
+                                  _ptr(h, ctypes.c_double), int(bool(use_lut)),
+                                  _ptr(logits, ctypes.c_double), _ptr(idx, ctypes.c_int32),
+                                  _ptr(gate, ctypes.c_double))
+    return dict(h=h, logits=logits, idx=idx, gate=gate)
+
+
 def stack_chain(h0, layers, k, n_layers=None):
-    """Decode chain h <- h + MoE_L(rmsnorm(h)) over the given layers, per token.
+    """Decode chain h <- h + MoE_L(rmsnorm(h)) over the given layers, in order.
 
     layers: list of (Wr, bias, cbs, codes) with codes = (gate, up, down) for all experts.
     Returns (final h [T,d], list of idx [T,k] per layer, list of logits [T,E] per layer).
     """
     h = _np(h0, np.float64).copy()
     idxs, logits = [], []
-    for L, (Wr, bias, cbs, codes) in enumerate(layers[:n_layers]):
-        x = np.stack([rmsnorm(h[t]) for t in range(h.shape[0])])
-        r = moe_layer(x, Wr, bias, cbs, codes, k)
-        h = h + r["out"]
+    for Wr, bias, cbs, codes in layers[:n_layers]:
+        r = residual_layer(h, Wr, bias, cbs, codes, k)
+        h = r["h"]
         idxs.append(r["idx"])
         logits.append(r["logits"])
     return h, idxs, logits
+
+
+def stack_token(h_t, layers, k):
+    """The same chain for one token, fetching only the selected experts' codes.
+
+    layers: iterable of (Wr, bias, cbs, get_expert_codes) per layer, where cbs is
+    [E,3,3,256,8] or a callable e -> [3,3,256,8] and get_expert_codes(e) returns
+    (gate [f,3,d/8], up [f,3,d/8], down [d,3,f/8]).  Returns (final h [d], list of idx [k]
+    per layer, list of gate [k] per layer).
+    """
+    h = _np(h_t, np.float64).copy()
+    idxs, gates = [], []
+    for Wr, bias, cbs, get_codes in layers:
+        r = moe_token(rmsnorm(h), Wr, bias, cbs, get_codes, k)
+        h = h + r["out"]
+        idxs.append(r["idx"])
+        gates.append(r["gate"])
+    return h, idxs, gates
 
 
 def expert_code_bytes(d: int, f: int) -> int:

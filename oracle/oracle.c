@@ -249,6 +249,49 @@ void oracle_rmsnorm(int d, const double *in, double *out) {
 }
 
 /*
+ * One layer of the decode chain, applied in place to h [T][d]: per token,
+ * x = rmsnorm(h_t) feeds the router and the experts, and the gate-weighted
+ * combine is added back, h_t <- h_t + sum_i g_i y_i(x).  The pages stack 92
+ * MoE layers per token, each layer's routing decided on the hidden state the
+ * previous layer left ([fr] "Budget RAM et zone de performance étroite": 16
+ * experts x 92 layers per token; "Lecture anticipée et prédiction du
+ * routeur": layer L+1's router reads layer L's residual).  The residual add
+ * is the pages' "h += combine"; the norm in front of the layer stands in for
+ * the trunk, which is out of scope (see oracle_rmsnorm).  Arrays as in
+ * oracle_moe_layer; logits [T][E], idx [T][k], gate [T][k] are outputs.
+ */
+void oracle_residual_layer(int T, int d, int f, int n_experts, int k, const float *Wr,
+                           const float *bias, const float *cbs, const uint8_t *gate_codes,
+                           const uint8_t *up_codes, const uint8_t *down_codes, double *h,
+                           int use_lut, double *logits, int32_t *idx, double *gate) {
+    const size_t cb_exp = (size_t)3 * OR_STAGES * OR_K * OR_V;
+    const size_t gu_exp = (size_t)f * OR_STAGES * (size_t)(d / OR_V);
+    const size_t dn_exp = (size_t)d * OR_STAGES * (size_t)(f / OR_V);
+    double *x = (double *)malloc(sizeof(double) * (size_t)d);
+    double *ys = (double *)malloc(sizeof(double) * (size_t)k * (size_t)d);
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!x || !ys || !y) { free(x); free(ys); free(y); return; }
+    for (int t = 0; t < T; ++t) {
+        double *ht = h + (size_t)t * d;
+        double *lt = logits + (size_t)t * n_experts;
+        int32_t *it = idx + (size_t)t * k;
+        double *gt = gate + (size_t)t * k;
+        oracle_rmsnorm(d, ht, x);
+        oracle_router(n_experts, d, Wr, bias, x, lt);
+        oracle_topk_softmax(n_experts, k, lt, it, gt);
+        for (int i = 0; i < k; ++i) {
+            int e = it[i];
+            oracle_expert_ffn(d, f, cbs + (size_t)e * cb_exp, gate_codes + (size_t)e * gu_exp,
+                              up_codes + (size_t)e * gu_exp, down_codes + (size_t)e * dn_exp, x,
+                              ys + (size_t)i * d, use_lut);
+        }
+        oracle_combine(d, k, gt, ys, NULL, y);
+        for (int i = 0; i < d; ++i) ht[i] = ht[i] + y[i];
+    }
+    free(x); free(ys); free(y);
+}
+
+/*
  * Bytes of codes per expert: 3 matrices (gate, up, down) of d*f weights at
  * 3 stages x 1 byte per 8 weights = 3.00 bits per weight ([fr]
  * "Quantification et exactitude").

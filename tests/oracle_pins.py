@@ -92,6 +92,47 @@ def pin_hand_example_experts():
             np.testing.assert_allclose(y, ex["expect"][f"y_expert{e}"], rtol=1e-14, atol=1e-14)
 
 
+def pin_chain_hand_example():
+    """Two chained copies of the hand example (h <- h + MoE(rmsnorm(h))), worked by hand in
+    the golden file: layer-by-layer h, layer 2's logits, gates and routing, k = 2 and k = 1."""
+    ex = load_hand_example()
+    X = ex["expect"]
+    layer = (ex["Wr"], None, ex["cbs"], ex["codes"])
+    for k in (2, 1):
+        r1 = oracle.residual_layer(ex["h"][None], *layer, k)
+        np.testing.assert_array_equal(r1["idx"][0], np.arange(k, dtype=np.int32))
+        np.testing.assert_allclose(r1["h"][0], X[f"chain_h1_k{k}"], rtol=1e-14, atol=1e-14)
+        r2 = oracle.residual_layer(r1["h"], *layer, k)
+        np.testing.assert_array_equal(r2["idx"][0], np.arange(k, dtype=np.int32))
+        np.testing.assert_allclose(r2["logits"][0], X[f"chain_logits2_k{k}"], rtol=1e-14, atol=1e-14)
+        if k == 2:
+            np.testing.assert_allclose(r2["gate"][0], X["chain_gate2_k2"], rtol=1e-14, atol=1e-15)
+        np.testing.assert_allclose(r2["h"][0], X[f"chain_h2_k{k}"], rtol=1e-14, atol=1e-14)
+        h2, idxs, logits = oracle.stack_chain(ex["h"][None], [layer, layer], k)
+        np.testing.assert_allclose(h2[0], X[f"chain_h2_k{k}"], rtol=1e-14, atol=1e-14)
+        assert len(idxs) == 2 and len(logits) == 2
+
+
+def pin_chain_zero_codebooks():
+    """Layers whose codebooks are all zero give zero expert outputs, so the chain leaves h
+    exactly as it was (whatever the routing)."""
+    rng = np.random.default_rng(11)
+    T, d, f, E, k = 3, 64, 32, 6, 2
+    layers = []
+    for _ in range(3):
+        Wr = rng.standard_normal((E, d)).astype(np.float32)
+        b = rng.standard_normal(E).astype(np.float32)
+        cbs = np.zeros((E, 3, 3, 256, 8), np.float32)
+        codes = (rng.integers(0, 256, (E, f, 3, d // 8), dtype=np.uint8),
+                 rng.integers(0, 256, (E, f, 3, d // 8), dtype=np.uint8),
+                 rng.integers(0, 256, (E, d, 3, f // 8), dtype=np.uint8))
+        layers.append((Wr, b, cbs, codes))
+    h0 = rng.standard_normal((T, d))
+    h, idxs, _ = oracle.stack_chain(h0, layers, k)
+    np.testing.assert_array_equal(h, h0)
+    assert len(idxs) == 3
+
+
 def pin_dequant_stage_placement():
     """Closed form: with stage-s codebook entry c equal to c * 256**s on component s
     (zero elsewhere), W[r][8j+s] is code_s(r, j) * 256**s and every other weight is 0."""

@@ -47,6 +47,11 @@ MUTANTS = {
     "rvq_codes_transposed": ("codes[code_index(nv, r, s, j)] = code[(size_t)r * nv + j];",
                              "codes[code_index(nv, r, s, j)] = code[(size_t)j * rows + r];"),
     "rvq_distance_abs": ("d = fmaf(t, t, d);", "d = d + fabsf(t);"),
+    "chain_router_on_h": ("oracle_router(n_experts, d, Wr, bias, x, lt);",
+                          "oracle_router(n_experts, d, Wr, bias, ht, lt);"),
+    "chain_experts_on_h": ("down_codes + (size_t)e * dn_exp, x,", "down_codes + (size_t)e * dn_exp, ht,"),
+    "chain_drops_residual": ("ht[i] = ht[i] + y[i];", "ht[i] = y[i];"),
+    "chain_norm_written_back": ("oracle_rmsnorm(d, ht, x);", "oracle_rmsnorm(d, ht, x);\n        memcpy(ht, x, sizeof(double) * (size_t)d);"),
 }
 
 

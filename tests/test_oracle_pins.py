@@ -39,3 +39,22 @@ def test_per_token_composition_matches_layer(oracle_mod):
                                  w.top_k, residual=True)
         assert (r["idx"] == full["idx"][t]).all()
         assert abs(r["out"] - full["out"][t]).max() < 1e-12
+
+
+def test_stack_token_matches_chain(oracle_mod):
+    """stack_token (one token, fetching only the selected experts) equals stack_chain on every
+    token of a three-layer chain of the tiny workload's shapes."""
+    from rvq_compressed_expert_gb300 import synth
+    w = synth.WORKLOADS["tiny"]
+    layers = [synth.layer_inputs(w, seed=0, layer=L) for L in range(3)]
+    h = synth.hidden(0, w.tokens, w.d, w.act_dtype)
+    full = [(li.router_w, li.router_b, li.codebooks, li.codes) for li in layers]
+    h_all, idx_all, _ = oracle_mod.stack_chain(h, full, w.top_k)
+    lazy = [(li.router_w, li.router_b, li.codebooks,
+             (lambda li: lambda e: (li.codes[0][e], li.codes[1][e], li.codes[2][e]))(li)) for li in layers]
+    for t in range(w.tokens):
+        h_t, idxs, gates = oracle_mod.stack_token(h[t], lazy, w.top_k)
+        for L in range(3):
+            assert (idxs[L] == idx_all[L][t]).all()
+            assert abs(gates[L].sum() - 1.0) < 1e-12
+        assert abs(h_t - h_all[t]).max() < 1e-12 * max(1.0, abs(h_all[t]).max())
