@@ -392,15 +392,34 @@ int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int3
  * layers driven by h += combine keeps its inputs at unit scale. */
 int waste_moe_rmsnorm(const float *d_in, float *d_out, int32_t T, int32_t d, waste_stream_t stream);
 
+/* Test aid for the refusal path of the library's device waits.  Work items of the
+ * persistent step kernel wait on one another through device counters (thread 0 polls with
+ * acquire loads and a growing sleep, then its CTA proceeds); every such wait is bounded, and
+ * one that gives up latches a timeout in the handle's error word, which waste_moe_stats
+ * reports as WASTE_ETIMEOUT (the pages' rule: refuse rather than degrade, page "Exécuter
+ * Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Budget RAM et zone de performance
+ * étroite").  This call runs that same wait, in one CTA on `stream`, on a counter the caller
+ * owns: it returns once *d_counter >= target, or after limit_ns nanoseconds (1 us .. 10 s)
+ * with the timeout latched in h.  A test withholds the counter to see the refusal without
+ * hanging or faulting the GPU; the context stays usable.  The library never calls it.
+ *   d_counter   device (or device-accessible) uint32, 4-byte aligned; only read
+ * Returns WASTE_EINVAL for a NULL handle or counter or a limit outside the range. */
+int waste_moe_debug_wait(waste_moe *h, const uint32_t *d_counter, uint32_t target, uint64_t limit_ns,
+                         waste_stream_t stream);
+
 /* waste_moe_forward without a handle and without allocating anything.
  *
  * The pages have no counterpart to this call; it exists for callers that cannot
  * allocate device memory -- for example a host that only receives device pointers
  * from an engine which owns all of the GPU's memory, or code running where
- * cudaMalloc is not allowed.  It computes what waste_moe_forward computes for the
- * same records, codebooks, hidden states, experts and gates, but keeps its
- * partial sums in one fixed 8 MiB array inside the library's device image
- * (every GPU that loads the library holds it until the process exits).
+ * cudaMalloc is not allowed.  It always runs the fp32 table-lookup kernels on the
+ * same records, codebooks, hidden states, experts and gates, and keeps its partial
+ * sums in one fixed 8 MiB array inside the library's device image (every GPU that
+ * loads the library holds it until the process exits).  Its output therefore equals
+ * waste_moe_forward's within the fp32 bar wherever the handle's forward also runs the
+ * lookup kernels (fp32 hidden states, one token, or WASTE_FLAG_FORCE_GEMV); for a
+ * batched bf16 call, whose experts with several tokens the handle's forward sends to
+ * the fp16 tensor-core path, the two agree only to the bf16 bar (relative L2 2e-3).
  *   cfg          shapes and act_dtype (d, f, n_experts, top_k, act_dtype, flags as
  *                for create; max_tokens, lookahead and layer are ignored)
  *   d_records    bank of records, 4096-aligned; not re-validated here (validate

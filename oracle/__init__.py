@@ -249,17 +249,18 @@ def stack_token(h_t, layers, k):
 
     layers: iterable of (Wr, bias, cbs, get_expert_codes) per layer, where cbs is
     [E,3,3,256,8] or a callable e -> [3,3,256,8] and get_expert_codes(e) returns
-    (gate [f,3,d/8], up [f,3,d/8], down [d,3,f/8]).  Returns (final h [d], list of idx [k]
-    per layer, list of gate [k] per layer).
+    (gate [f,3,d/8], up [f,3,d/8], down [d,3,f/8]).  Returns (final h [d], and per layer the
+    lists of idx [k], gate [k] and logits [E]).
     """
     h = _np(h_t, np.float64).copy()
-    idxs, gates = [], []
+    idxs, gates, logits = [], [], []
     for Wr, bias, cbs, get_codes in layers:
         r = moe_token(rmsnorm(h), Wr, bias, cbs, get_codes, k)
         h = h + r["out"]
         idxs.append(r["idx"])
         gates.append(r["gate"])
-    return h, idxs, gates
+        logits.append(r["logits"])
+    return h, idxs, gates, logits
 
 
 def expert_code_bytes(d: int, f: int) -> int:

@@ -36,7 +36,7 @@ EXPORTED = ["waste_moe_record_layout", "waste_moe_pack_records", "waste_moe_crea
             "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile",
             "waste_moe_rmsnorm", "waste_moe_forward_noalloc", "waste_moe_step", "waste_moe_set_trace",
             "waste_bank_create", "waste_bank_destroy", "waste_bank_reset", "waste_bank_stats",
-            "waste_moe_create_banked", "waste_rvq_train", "waste_rvq_encode"]
+            "waste_moe_create_banked", "waste_rvq_train", "waste_rvq_encode", "waste_moe_debug_wait"]
 
 
 class waste_moe_config(ctypes.Structure):
@@ -117,6 +117,7 @@ def load(path: str = LIB_PATH):
     lib.waste_moe_create_banked.argtypes = [cfgp, vp, vp, vp, i32, vp, ctypes.POINTER(vp)]
     lib.waste_rvq_train.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
     lib.waste_rvq_encode.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+    lib.waste_moe_debug_wait.argtypes = [vp, vp, ctypes.c_uint32, ctypes.c_uint64, vp]
     for name in EXPORTED:
         if name not in ("waste_moe_destroy", "waste_moe_last_error", "waste_bank_destroy"):
             getattr(lib, name).restype = ctypes.c_int
@@ -234,6 +235,11 @@ def waste_moe_read_profile(h) -> dict:
     ms = (ctypes.c_float * 6)()
     _check(load().waste_moe_read_profile(h, ms))
     return dict(zip(("router", "topk", "gate_up", "down", "combine", "step"), list(ms)))
+
+
+def waste_moe_debug_wait(h, d_counter, target, limit_ns, stream=None):
+    """The library's bounded device wait on a caller-owned uint32 counter (test aid)."""
+    return _check(load().waste_moe_debug_wait(h, _ptr(d_counter), target, limit_ns, _stream(stream)))
 
 
 def waste_moe_rmsnorm(d_in, d_out, T, d, stream=None):

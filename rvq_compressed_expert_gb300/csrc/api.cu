@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in waste_moe.h: argument and record checks,
 // workspace, statistics, error strings, and the launch sequence of each call.
 #include "common.cuh"
+#include "lut_dev.cuh"
 
 #include <algorithm>
 #include <cstdarg>
@@ -90,6 +91,13 @@ void layout(const waste_moe_config *c, size_t *stride, size_t off[3], size_t byt
 
 namespace wm {
 void set_last_error(const char *msg) { g_err = msg; }
+
+// One CTA running the bounded wait that the step kernel's work items use between one
+// another, on a caller-owned counter.
+__global__ void __launch_bounds__(32) debug_wait_kernel(const unsigned *c, unsigned target, uint32_t *err,
+                                                        unsigned long long limit_ns) {
+    lut::wait_counter(c, target, err, limit_ns);
+}
 
 int device_sm_count() {
     int dev = 0, n = 0;
@@ -692,6 +700,20 @@ int waste_moe_topk_from_logits(const float *d_logits, int32_t T, int32_t E, int3
     cudaError_t e = launch_topk(d_logits, nullptr, T, E, k, d_idx, d_gate, nullptr, nullptr, 1, nullptr, 0,
                                 reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "top-k kernel");
+    return ok();
+}
+
+int waste_moe_debug_wait(waste_moe *h, const uint32_t *d_counter, uint32_t target, uint64_t limit_ns,
+                         waste_stream_t stream) {
+    const NvtxRange nvtx_range(__func__);
+    if (!h) return fail(WASTE_EINVAL, "NULL handle");
+    if (!d_counter || !aligned(d_counter, 4)) return fail(WASTE_EINVAL, "counter pointer NULL or not 4-byte aligned");
+    if (limit_ns < 1000 || limit_ns > 10000000000ull)
+        return fail(WASTE_EINVAL, "limit_ns = %llu outside [1 us, 10 s]", (unsigned long long)limit_ns);
+    debug_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(d_counter, target, h->W.err,
+                                                                            (unsigned long long)limit_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "wait kernel");
     return ok();
 }
 

@@ -7,6 +7,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <atomic>
+
 #include "waste_moe.h"
 
 namespace wm {
@@ -65,6 +67,26 @@ inline MatGeom mat_geom(int n_out, int n_in) {
 }
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Devices the per-device host caches below track (ordinals past it are served uncached).
+constexpr int kMaxDevices = 64;
+
+// The dynamic shared memory a kernel may ask for is an attribute of the kernel on each
+// device: it is set on the current device the first time a launcher needs `bytes` there
+// (a cheap driver call; the cache only avoids repeating it).  One SmemAttr per kernel.
+struct SmemAttr {
+    std::atomic<int> bytes[kMaxDevices] = {};
+};
+inline cudaError_t ensure_smem(SmemAttr &a, const void *kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached && a.bytes[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && cached) a.bytes[dev].store(bytes, std::memory_order_release);
+    return e;
+}
 
 // Everything a kernel needs to reach one layer's weights.
 struct LayerView {

@@ -292,13 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
 template <bool kRecon, bool kBf16, bool kBanked>
 cudaError_t launch_fused_t(const FusedArgs &F, int grid, cudaStream_t s) {
     const size_t smem = unit_smem<kRecon>();
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(fused_step_kernel<kRecon, kBf16, kBanked>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static SmemAttr attr;
+    cudaError_t e = ensure_smem(attr, (const void *)fused_step_kernel<kRecon, kBf16, kBanked>, (int)smem);
+    if (e != cudaSuccess) return e;
     fused_step_kernel<kRecon, kBf16, kBanked><<<grid, kThreads, smem, s>>>(F);
     return cudaGetLastError();
 }

@@ -571,13 +571,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
 
 template <bool kDown>
 cudaError_t launch_mma(const MmaArgs &A, int num_sms, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(mma_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kMmaSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static SmemAttr attr;
+    cudaError_t e = ensure_smem(attr, (const void *)mma_kernel<kDown>, (int)kMmaSmem);
+    if (e != cudaSuccess) return e;
     mma_kernel<kDown><<<num_sms, kMmaThreads, kMmaSmem, s>>>(A);
     return cudaGetLastError();
 }

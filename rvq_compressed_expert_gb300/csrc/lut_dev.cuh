@@ -248,18 +248,22 @@ __device__ __forceinline__ float dot8s(const float *__restrict__ c, const float 
 }
 
 // Wait (thread 0 polls, the CTA then proceeds together) until *c >= target.  The wait
-// is bounded: after about a second it records kErrTimeout and gives up.
+// is bounded: after limit_ns (by default about a second) it records kErrTimeout and gives up.
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
-__device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target, uint32_t *err) {
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target, uint32_t *err,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
     if (threadIdx.x == 0) {
         unsigned ns = 32;
-        for (long it = 0; ld_acquire(c) < target; ++it) {
-            if (it > (1l << 22)) {
+        const unsigned long long t0 = gtimer();
+        while (ld_acquire(c) < target) {
+            if (gtimer() - t0 > limit_ns) {
                 atomicOr(err, kErrTimeout);
                 break;
             }

@@ -123,13 +123,9 @@ __global__ void __launch_bounds__(32 * kMaxTopK) combine_kernel(const float *__r
 template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf>
 cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
     const size_t smem = unit_smem<kRecon>();
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static SmemAttr attr;
+    cudaError_t e = ensure_smem(attr, (const void *)lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf>, (int)smem);
+    if (e != cudaSuccess) return e;
     const int grid = units < num_sms ? units : num_sms;
     lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf><<<grid, kNT, smem, s>>>(A);
     return cudaGetLastError();

@@ -18,7 +18,6 @@ namespace {
 // the library until the process exits.  Layout: [256 B: device error word][gate/up
 // partials][down partials].
 constexpr size_t kStaticScratchBytes = 8u << 20;
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_forward_scratch[kStaticScratchBytes];
 

@@ -253,9 +253,21 @@ __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__r
         for (int r = 0; r < rows; ++r) tc::bulk_g2s(s0 + (uint32_t)r * wbytes, W + (size_t)(row0 + r) * d, wbytes, mb);
     }
     __syncthreads(); // the barrier is initialised
-    if (!tc::mbar_wait(mb, 0)) {
-        if (threadIdx.x == 0 && err) atomicOr(err, kErrTimeout);
-        tc::mbar_wait(mb, 0); // the copies in flight target this CTA's shared memory
+    bool landed = tc::mbar_wait(mb, 0);
+    if (!landed) {
+        if (err) atomicOr(err, kErrTimeout);
+        landed = tc::mbar_wait(mb, 0); // the copies in flight target this CTA's shared memory
+    }
+    landed = __syncthreads_and(landed ? 1 : 0) != 0; // one verdict for the whole CTA
+    if (!landed) {
+        // The copies never landed: the staged rows are not to be read.  No logits are
+        // written; the CTA still counts itself so the counter returns to rest, and the last
+        // CTA leaves the top-k alone (the timeout is latched; the copies may still be in
+        // flight, so the context is to be treated as unusable).
+        if (!F.done) return;
+        __syncthreads();
+        if (threadIdx.x == 0 && count_acq_rel(F.done) == gridDim.x - 1) *F.done = 0u;
+        return;
     }
     const float4 *ws = reinterpret_cast<const float4 *>(t1_smem + (size_t)rl * wbytes);
     const int d4 = d >> 2;
@@ -300,7 +312,15 @@ __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__r
     }
     if (!F.done) return;
     __syncthreads(); // this CTA's logits before its count
-    if (threadIdx.x == 0) last = count_acq_rel(F.done) == gridDim.x - 1;
+    if (threadIdx.x == 0) {
+        last = count_acq_rel(F.done) == gridDim.x - 1;
+        // some CTA's rows never arrived (the timeout it latched precedes its count): its
+        // logits are missing, so the last CTA takes no top-k
+        if (last && err && (atomicOr(err, 0u) & kErrTimeout)) {
+            *F.done = 0u;
+            last = 0;
+        }
+    }
     __syncthreads();
     if (!last) return;
     topk_block(logits, logits_lo, E, F.k, 0, F.idx, F.gate, F.pred_idx, F.pred_count, F.pred_stride, F.stats,
@@ -430,27 +450,23 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
         // top-k kernel, which takes them in parallel
         if (fuse && fused && T == 1) *fused = true;
         else fuse = nullptr;
-        static bool attr = false;
-        if (!attr) {
-            cudaFuncSetAttribute(router_staged_kernel<true, kStagedRows>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterStageMax);
-            cudaFuncSetAttribute(router_staged_kernel<false, kStagedRows>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRouterStageMax);
-            attr = true;
-        }
+        static SmemAttr attr_s[2];
+        cudaError_t ea = ensure_smem(attr_s[L.act_bf16 ? 1 : 0],
+                                     L.act_bf16 ? (const void *)router_staged_kernel<true, kStagedRows>
+                                                : (const void *)router_staged_kernel<false, kStagedRows>,
+                                     (int)kRouterStageMax);
+        if (ea != cudaSuccess) return ea;
         // the one-token kernel only for the demand route (fuse): its CTAs hold ~113 KiB of
         // shared memory and cannot run beside the expert kernels, which the lookahead's router
         // (another stream, no fuse) does on the staged kernel's 28 KiB (the same logits)
         const size_t t1_smem = (size_t)L.d * (4 * kT1Rows + (L.act_bf16 ? 2 : 4));
         if (T == 1 && fuse && fused && t1_smem <= kT1SmemMax && aligned16(L.router_w) && aligned16(h)) {
-            static bool attr1 = false;
-            if (!attr1) {
-                cudaFuncSetAttribute(router_t1_kernel<true, kT1Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kT1SmemMax);
-                cudaFuncSetAttribute(router_t1_kernel<false, kT1Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kT1SmemMax);
-                attr1 = true;
-            }
+            static SmemAttr attr_t1[2];
+            ea = ensure_smem(attr_t1[L.act_bf16 ? 1 : 0],
+                             L.act_bf16 ? (const void *)router_t1_kernel<true, kT1Rows>
+                                        : (const void *)router_t1_kernel<false, kT1Rows>,
+                             (int)kT1SmemMax);
+            if (ea != cudaSuccess) return ea;
             const RouteTopk F = fuse ? *fuse : RouteTopk{};
             const dim3 grid1((L.E + kT1Rows - 1) / kT1Rows);
             if (L.act_bf16)

@@ -103,4 +103,6 @@ def test_null_handle_rejected(lib):
         B.waste_moe_prefetch(None, None, 1, side=0)
     with pytest.raises(B.WasteError):
         B.waste_moe_stats(None)
+    with pytest.raises(B.WasteError):
+        B.waste_moe_debug_wait(None, 4096, 1, 1_000_000, stream=0)
     B.waste_moe_destroy(None)

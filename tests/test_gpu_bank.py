@@ -5,9 +5,11 @@ performance étroite" and "Lecture anticipée et prédiction du routeur": a boun
 experts over a slow tier, misses read from the slow tier, the lookahead fills the cache ahead
 of demand -- the outputs never change (the real router decides), only what is resident.
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from rvq_compressed_expert_gb300 import binding as B
 from rvq_compressed_expert_gb300 import synth
 from rvq_compressed_expert_gb300.bank import TieredStack
@@ -24,6 +26,29 @@ def _built():
     from rvq_compressed_expert_gb300 import _build
     _build.build()
     B.load()
+    oracle.build()
+
+
+def assert_oracle_chain(outs, w, hidden_seed0, n_layers, gen_device="cuda", seed=0):
+    """Each token's output (the banked stack's) against the oracle's decode chain run on its own
+    from the same token and weights: h <- h + MoE_L(rmsnorm(h)) over the layers, only the
+    selected experts' codes fetched.  The bounded cache and the lookahead never change what a
+    layer computes (page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", sections "Budget RAM
+    et zone de performance étroite" and "Lecture anticipée et prédiction du routeur"), so the
+    fp32 bar holds: relative L2 <= 1e-5 and |err| <= 1e-4 max|y|."""
+    lis = [synth.layer_inputs(w, seed, L, gen_device, with_codes=False) for L in range(n_layers)]
+    layers = []
+    for L, li in enumerate(lis):
+        get = (lambda L: lambda e: tuple(c.cpu() for c in synth.expert_codes(seed, L, e, w.d, w.f, gen_device)))(L)
+        layers.append((li.router_w.cpu(), None if li.router_b is None else li.router_b.cpu(),
+                       li.codebooks.cpu(), get))
+    for i, got in enumerate(outs):
+        h0 = synth.hidden(hidden_seed0 + i, w.tokens, w.d, "f32", "cuda")[0].cpu()
+        ref, _, _, _ = oracle.stack_token(h0, layers, w.top_k)
+        g = got[0].cpu().double().numpy()
+        rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+        assert rel <= 1e-5, f"token {i}: relative L2 {rel:.3e}"
+        assert np.abs(g - ref).max() <= 1e-4 * np.abs(ref).max(), f"token {i}"
 
 
 W = synth.Workload("bank", 512, 256, 16, 4, 1, "f32", "offsets", n_layers=4, lookahead=3)
@@ -67,6 +92,7 @@ def test_banked_equals_resident(lookahead, flags):
         got = run_tokens(DecodeStack(ts.layers, W.tokens, banked=True), 5, lookahead)
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+        assert_oracle_chain(got, W, 50, W.n_layers)
         st = ts.stats()
         assert st["demand_hits"] + st["demand_misses"] == 5 * W.n_layers * W.top_k
         assert st["copied_bytes"] == (st["demand_misses"] + st["prefetch_copies"]) * ts.stride
@@ -202,6 +228,7 @@ def test_full_size_records(flags):
         got = run_tokens_w(DecodeStack(ts.layers, 1, banked=True), wf, 4, 0)
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+        assert_oracle_chain(got, wf, 70, 2)
         st = ts.stats()
         assert st["demand_hits"] + st["demand_misses"] == 4 * 2 * 16
         assert st["demand_misses"] >= 16 + 16

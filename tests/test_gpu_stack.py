@@ -175,3 +175,46 @@ def test_route_trace_jsonl(tmp_path):
     finally:
         for l in layers:
             l.close()
+
+
+def test_full_depth_token_matches_oracle():
+    """One token through the full-depth stack -- 92 layers x 64 resident experts at d=7168,
+    f=1536, top-16, lookahead 6 -- against the oracle's decode chain run on its own (only the 16
+    selected experts' codes of each layer handed to it): every layer's experts bit-exact, the
+    final h within the fp32 bar (relative L2 <= 1e-5, |err| <= 1e-4 max|h|).  Page "Exécuter
+    Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section "Budget RAM et zone de performance
+    étroite": 16 experts x 92 layers per token."""
+    w = synth.WORKLOADS["stack"]
+    free, _ = torch.cuda.mem_get_info()
+    need = w.n_layers * w.n_experts * 12_390_400 * 1.05 + (4 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
+    layers = [MoELayer(w, 0, L, "cuda", max_tokens=1) for L in range(w.n_layers)]
+    try:
+        h0 = synth.hidden(7, 1, w.d, "f32", "cuda")
+        stack = DecodeStack(layers, 1)
+        routed = {}
+
+        def record(L, idx, gate, main):
+            with torch.cuda.stream(main):
+                routed[L] = idx.clone()
+
+        out = run_eager(stack, h0, w.lookahead, record)
+        for l in layers:
+            l.stats()  # raises on a latched device error
+        ref_layers = []
+        for L, ml in enumerate(layers):
+            get = (lambda ml: lambda e: ml.expert_codes_host(e))(ml)
+            ref_layers.append((ml.router_w.cpu(), ml.router_b.cpu(), ml.codebooks.cpu(), get))
+        h, ref_idx, _, ref_logits = oracle.stack_token(h0[0].cpu(), ref_layers, w.top_k)
+        for L in range(w.n_layers):
+            assert oracle.topk_margin(ref_logits[L], w.top_k) > 1e-4, f"layer {L}: near-tie in the oracle"
+            np.testing.assert_array_equal(routed[L][0].cpu().numpy(), ref_idx[L], err_msg=f"layer {L}")
+        got = out[0].cpu().double().numpy()
+        rel = np.linalg.norm(got - h) / np.linalg.norm(h)
+        assert rel <= 1e-5, rel
+        assert np.abs(got - h).max() <= 1e-4 * np.abs(h).max()
+    finally:
+        for l in layers:
+            l.close()
+        torch.cuda.empty_cache()

@@ -53,7 +53,7 @@ def test_stack_token_matches_chain(oracle_mod):
     lazy = [(li.router_w, li.router_b, li.codebooks,
              (lambda li: lambda e: (li.codes[0][e], li.codes[1][e], li.codes[2][e]))(li)) for li in layers]
     for t in range(w.tokens):
-        h_t, idxs, gates = oracle_mod.stack_token(h[t], lazy, w.top_k)
+        h_t, idxs, gates, _ = oracle_mod.stack_token(h[t], lazy, w.top_k)
         for L in range(3):
             assert (idxs[L] == idx_all[L][t]).all()
             assert abs(gates[L].sum() - 1.0) < 1e-12
