@@ -992,7 +992,7 @@ def print_unit_trace(tr, w):
     """Per-phase summary of the lookup kernels' unit trace: table build and row streaming."""
     import math as _m
     slots = w.tokens * w.top_k
-    n_gu = slots * _m.ceil(w.d / 8 / 32)
+    n_gu = slots * 2 * _m.ceil(_m.ceil(w.d / 8 / 32) / 2)  # (slot, segment pair, matrix) units
     rows = tr.tolist()
     out = []
     for name, a, b in (("gate_up", 0, n_gu), ("down", n_gu, len(rows))):
@@ -1026,7 +1026,7 @@ def print_trace(tr, w):
         print("no trace")
         return
     t0 = min(r[0] for r in rows)
-    n_gu = slots * nseg
+    n_gu = slots * 2 * _m.ceil(nseg / 2)  # (slot, segment pair, matrix) units
     bounds = [("router", 0, n_router), ("topk", n_router, n_router + 1),
               ("gate_up", n_router + 1, n_router + 1 + n_gu)]
     dn0 = n_router + 1 + n_gu

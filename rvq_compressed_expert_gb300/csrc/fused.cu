@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             Unit N;
             if (has_next) N = decode_unit<true>(F.A, nxt - b_dn(F));
             run_unit<true, kRecon, kBf16, kThreads, kCodePingPong, kBanked ? kPrefetchRounds : kStepPrefetchRounds,
-                     kBanked>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot, (unsigned)F.A.gu.nseg);
+                     kBanked>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot, (unsigned)(2 * F.A.gu_pairs));
             signal(dn_done(F) + (u % F.A.nrb));
         } else {
             // ---- combine rows [r0, r1) once every down unit over them is done
@@ -336,6 +336,7 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
     A.gu = L.gu;
     A.off_gate = L.sec_off[0];
     A.off_up = L.sec_off[1];
+    A.gu_pairs = (L.gu.nseg + 1) / 2;
     A.part_gu = W.part_gu;
     A.dn = L.dn;
     A.off_down = L.sec_off[2];
@@ -374,7 +375,7 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
     if (lanes) F.bank = *lanes;
     else memset(&F.bank, 0, sizeof F.bank);
     F.bank_copiers = bank::copiers_per_job(L.stride, F.n_copy);
-    F.n_gu = A.slots * A.gu.nseg;
+    F.n_gu = A.slots * 2 * A.gu_pairs;
     F.n_dn = A.slots * A.npair * A.nrb;
     F.n_comb = (L.d + kCombineRows - 1) / kCombineRows;
     const int total = F.n_router + F.n_topk + F.n_copy + F.n_gu + F.n_dn + F.n_comb;

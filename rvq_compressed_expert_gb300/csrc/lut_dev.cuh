@@ -27,10 +27,11 @@ struct LutArgs {
     const int32_t *idx;
     const void *h;
     int E, k, slots;
-    // gate / up
+    // gate / up: a unit is (slot, pair of consecutive 32-vector segments, matrix)
     MatGeom gu;
     size_t off_gate, off_up;
-    float *part_gu; // [slot][gu.nseg][2][f]
+    int gu_pairs;   // segment pairs of the gate/up input, (gu.nseg + 1) / 2
+    float *part_gu; // [slot][gu_pairs][2 matrices: gate, up][f]
     // down
     MatGeom dn;
     size_t off_down;
@@ -125,10 +126,12 @@ __device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes
 // j, j + 8, j + 16, j + 24 sit side by side, so the table build stores 16 bytes at a time.
 __host__ __device__ constexpr int tab_col(int j) { return 4 * (j & 7) + (j >> 3); }
 
-// Decode a unit index into (slot, first segment, part bases, row-group range).
+// Decode a unit index into (slot, matrix, first segment, segment bases, row-group range).
+// Every unit covers two consecutive 32-vector segments of one matrix (its two "parts"):
+// the same rows, so both segments' lookups add into one set of row partials.
 struct Unit {
-    int slot, e, seg0, g0, g1;
-    const uint8_t *base[2]; // chunk (seg, g=0, s=0, jj=0) of each part, or null
+    int slot, e, mat, seg0, g0, g1;
+    const uint8_t *base[2]; // chunk (seg0 + p, g=0, s=0, jj=0) of each part, or null
 };
 
 // Ask L2 for row group g of both parts of a unit: 2 parts x 3 stages x 512 B = 24 lines
@@ -148,9 +151,11 @@ template <bool kDown>
 __device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
     Unit U;
     if constexpr (!kDown) {
-        U.slot = u / A.gu.nseg;
+        U.slot = u / (2 * A.gu_pairs);
         if (A.slot_list) U.slot = A.slot_list[U.slot];
-        U.seg0 = u % A.gu.nseg;
+        const int rem = u % (2 * A.gu_pairs);
+        U.seg0 = 2 * (rem >> 1);
+        U.mat = rem & 1;
         U.g0 = 0;
         U.g1 = A.gu.groups;
     } else {
@@ -162,20 +167,16 @@ __device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
         const int rb = rem % A.nrb;
         U.g0 = rb * A.rb_groups;
         U.g1 = min(A.dn.groups, U.g0 + A.rb_groups);
+        U.mat = 2;
     }
     U.e = A.idx[U.slot];
     U.base[0] = U.base[1] = nullptr;
     const uint8_t *rec = (U.e >= 0 && U.e < A.E) ? expert_record(A.records, A.stride, A.slot_map, U.e) : nullptr;
     if (rec) {
-        if constexpr (!kDown) {
-            const size_t so = (size_t)U.seg0 * A.gu.groups * (kStages * 512);
-            U.base[0] = rec + A.off_gate + so;
-            U.base[1] = rec + A.off_up + so;
-        } else {
-            for (int p = 0; p < 2; ++p)
-                if (U.seg0 + p < A.dn.nseg)
-                    U.base[p] = rec + A.off_down + (size_t)(U.seg0 + p) * A.dn.groups * (kStages * 512);
-        }
+        const MatGeom &G = kDown ? A.dn : A.gu;
+        const size_t off = kDown ? A.off_down : (U.mat ? A.off_up : A.off_gate);
+        for (int p = 0; p < 2; ++p)
+            if (U.seg0 + p < G.nseg) U.base[p] = rec + off + (size_t)(U.seg0 + p) * G.groups * (kStages * 512);
     }
     return U;
 }
@@ -200,13 +201,12 @@ __device__ __forceinline__ void issue_stage(float *dst, const float *cb_p0, cons
     cp_async_commit();
 }
 
+// The unit's matrix codebooks (both parts: the parts are two segments of one matrix).
 template <bool kDown>
 __device__ __forceinline__ void unit_codebooks(const LutArgs &A, const Unit &U, const float *&p0,
                                                const float *&p1) {
     const int e = (U.e >= 0 && U.e < A.E) ? U.e : 0;
-    const float *cb_e = A.codebooks + (size_t)e * 3 * kCbFloats;
-    p0 = cb_e + (kDown ? 2 : 0) * kCbFloats;
-    p1 = cb_e + (kDown ? 2 : 1) * kCbFloats;
+    p0 = p1 = A.codebooks + ((size_t)e * 3 + (size_t)U.mat) * kCbFloats;
 }
 
 // Table load at shared-window address a + S * 64 KiB (stage S).  volatile keeps it on
@@ -319,8 +319,9 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         const float *q0, *q1;
         unit_codebooks<kDown>(A, N, q0, q1);
         constexpr int kLines = kCbFloats / 32; // 128-byte lines of one part's codebooks
-        for (int i = threadIdx.x; i < (kDown ? 1 : 2) * kLines; i += kNT) {
-            const float *q = (i < kLines ? q0 : q1) + (size_t)(i % kLines) * 32;
+        (void)q1;
+        for (int i = threadIdx.x; i < kLines; i += kNT) {
+            const float *q = q0 + (size_t)i * 32;
             asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
         }
     }
@@ -329,37 +330,38 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     // ---- input vectors of this lane's column(s)
     float xv[2][kVec];
     if constexpr (!kDown) {
-        const int j = U.seg0 * kSegVec + lane;
-        if (j < G.nv) load_x8<kBf16>(A.h, (size_t)t * A.gu.n_in + (size_t)j * kVec, xv[0]);
-        else {
 #pragma unroll
-            for (int v = 0; v < kVec; ++v) xv[0][v] = 0.f;
+        for (int p = 0; p < 2; ++p) {
+            const int j = (U.seg0 + p) * kSegVec + lane;
+            if (j < G.nv) load_x8<kBf16>(A.h, (size_t)t * A.gu.n_in + (size_t)j * kVec, xv[p]);
+            else {
+#pragma unroll
+                for (int v = 0; v < kVec; ++v) xv[p][v] = 0.f;
+            }
         }
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) xv[1][v] = xv[0][v];
     } else {
         // a = silu(gate) * up for the 64 vectors of this unit, reduced over the gate/up
-        // segments in a fixed order (the loads of 32 segments in flight at a time)
+        // segment pairs in a fixed order (the loads of 32 pairs in flight at a time)
         __syncthreads(); // xs may still be read by the previous unit
         if (dep) wait_counter(dep, dep_target, A.err);
         for (int i = threadIdx.x; i < 2 * kSegVec * kVec; i += kNT) {
             const int r = U.seg0 * kSegVec * kVec + i; // index into f
             float a = 0.f;
             if (valid && r < A.gu.n_out) {
-                const float *pg = A.part_gu + (size_t)U.slot * A.gu.nseg * 2 * A.gu.n_out + r;
+                const float *pg = A.part_gu + (size_t)U.slot * A.gu_pairs * 2 * A.gu.n_out + r;
                 const size_t step = (size_t)2 * A.gu.n_out;
                 float zg = 0.f, zu = 0.f;
-                for (int s0 = 0; s0 < A.gu.nseg; s0 += 32) {
+                for (int s0 = 0; s0 < A.gu_pairs; s0 += 32) {
                     float vg[32], vu[32];
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
-                        const int sg = min(s0 + q, A.gu.nseg - 1);
+                        const int sg = min(s0 + q, A.gu_pairs - 1);
                         vg[q] = pg[sg * step];
                         vu[q] = pg[sg * step + A.gu.n_out];
                     }
 #pragma unroll
                     for (int q = 0; q < 32; ++q)
-                        if (s0 + q < A.gu.nseg) {
+                        if (s0 + q < A.gu_pairs) {
                             zg += vg[q];
                             zu += vu[q];
                         }
@@ -409,7 +411,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int j = mm * 16 + fg + 8 * h2;
                 if constexpr (!kDown) {
-                    const int jg = U.seg0 * kSegVec + j;
+                    const int jg = (U.seg0 + mp) * kSegVec + j;
                     const bool in = jg < G.nv;
                     const size_t e0 = (size_t)t * A.gu.n_in + (size_t)min(jg, G.nv - 1) * kVec;
                     av[mm][h2] = in ? load_x1<kBf16>(A.h, e0 + ft) : 0.f;
@@ -519,9 +521,9 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         }
     };
     // Row group g: lane l holds, for each code byte q of its 16-byte chunks, the partial
-    // dot product of row 16 g + ((l ^ q) & 15) over its vector column.  Gate and up go one
-    // part at a time (16 partials, then a reduce-scatter over the 32 columns); the two down
-    // segments add into the same rows before a single reduce-scatter.
+    // dot product of row 16 g + ((l ^ q) & 15) over its vector column.  The unit's two
+    // segments add into the same 16 row partials before a single reduce-scatter over the 32
+    // columns.
     auto reduce16 = [&](float (&acc)[16]) {
 #pragma unroll
         for (int n = 8; n >= 1; n >>= 1)
@@ -529,8 +531,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
         acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 16);
     };
-    // the lookups of part p of one row group: acc = (or, for the second down segment, +=)
-    // the 16 partials
+    // the lookups of part p of one row group: acc = (part 0) or += (part 1) the 16 partials
     auto lookups = [&](const uint4 (&cwp)[kStages], int p, float (&acc)[16]) {
         const uint32_t colb = p ? colb1 : colb0;
 #pragma unroll
@@ -567,18 +568,18 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                     sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
                     t = sacc;
                 }
-                if (kDown && p == 1) acc[4 * wd + b] += t;
+                if (p == 1) acc[4 * wd + b] += t;
                 else acc[4 * wd + b] = t;
             }
         }
     };
-    // reduce-scatter and store: gate/up per part, down once for both segments
-    auto finish = [&](float (&acc)[16], int p, int g) {
+    // reduce-scatter of the row partials (both segments added) and store
+    auto finish = [&](float (&acc)[16], int g) {
         const int row = g * kGroupRows + (lane & 15);
         reduce16(acc);
         if (lane < 16 && row < G.n_out) {
             if constexpr (!kDown)
-                A.part_gu[(((size_t)U.slot * A.gu.nseg + U.seg0) * 2 + p) * G.n_out + row] = acc[0];
+                A.part_gu[(((size_t)U.slot * A.gu_pairs + U.seg0 / 2) * 2 + U.mat) * G.n_out + row] = acc[0];
             else
                 A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = acc[0];
         }
@@ -587,9 +588,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
             float acc[16];
             lookups(cw[0], 0, acc);
-            if constexpr (!kDown) finish(acc, 0, g);
             lookups(cw[1], 1, acc);
-            finish(acc, 1, g);
+            finish(acc, g);
         };
         uint4 wa[2][kStages], wb[2][kStages];
         int g = U.g0 + warp;
@@ -612,9 +612,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             ahead(g);
             float acc[16];
             lookups(wa[0], 0, acc);
-            if constexpr (!kDown) finish(acc, 0, g);
             lookups(wa[1], 1, acc);
-            finish(acc, 1, g);
+            finish(acc, g);
         }
     } else {
         // one set of code registers: as soon as a part's lookups are issued, the next row
@@ -626,22 +625,12 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         for (; g < U.g1; g += kNW) {
             const int gn = g + kNW;
             ahead(g);
-            if constexpr (!kDown) {
-                float acc0[16], acc1[16];
-                lookups(wa[0], 0, acc0);
-                if (gn < U.g1) load_part(gn, 0, wa);
-                lookups(wa[1], 1, acc1);
-                if (gn < U.g1) load_part(gn, 1, wa);
-                finish(acc0, 0, g);
-                finish(acc1, 1, g);
-            } else {
-                float acc[16];
-                lookups(wa[0], 0, acc);
-                if (gn < U.g1) load_part(gn, 0, wa);
-                lookups(wa[1], 1, acc);
-                if (gn < U.g1) load_part(gn, 1, wa);
-                finish(acc, 1, g);
-            }
+            float acc[16];
+            lookups(wa[0], 0, acc);
+            if (gn < U.g1) load_part(gn, 0, wa);
+            lookups(wa[1], 1, acc);
+            if (gn < U.g1) load_part(gn, 1, wa);
+            finish(acc, g);
         }
     }
     // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
@@ -649,15 +638,13 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     if (threadIdx.x == 0 && valid && A.stats) {
         unsigned long long vecs = 0;
         for (int p = 0; p < 2; ++p) {
-            const int seg = kDown ? U.seg0 + p : U.seg0;
+            const int seg = U.seg0 + p;
             if (seg < G.nseg) vecs += (unsigned long long)min(kSegVec, G.nv - seg * kSegVec);
         }
         const int rows = min(G.n_out, U.g1 * kGroupRows) - U.g0 * kGroupRows;
         atomicAdd(A.stats + kStatDemandCode, vecs * (unsigned long long)rows * kStages);
-        const bool first = kDown ? (U.seg0 == 0 && U.g0 == 0) : (U.seg0 == 0);
-        if (first)
-            atomicAdd(A.stats + kStatCodebook,
-                      (unsigned long long)(kDown ? 1 : 2) * kCbFloats * sizeof(float));
+        if (U.seg0 == 0 && U.g0 == 0)
+            atomicAdd(A.stats + kStatCodebook, (unsigned long long)kCbFloats * sizeof(float));
     }
 }
 

@@ -38,7 +38,7 @@ template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf>
 __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int n_slots = lut_slot_count(A);
-    const int units = kDown ? n_slots * A.npair * A.nrb : n_slots * A.gu.nseg;
+    const int units = kDown ? n_slots * A.npair * A.nrb : n_slots * 2 * A.gu_pairs;
     int par = 0;
     bool primed = false;
     Unit N;
@@ -178,6 +178,7 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
     A.gu = L.gu;
     A.off_gate = L.sec_off[0];
     A.off_up = L.sec_off[1];
+    A.gu_pairs = (L.gu.nseg + 1) / 2;
     A.part_gu = W.part_gu;
     A.dn = L.dn;
     A.off_down = L.sec_off[2];
@@ -197,7 +198,7 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
 
 cudaError_t launch_lut_phase(const LutArgs &A, bool down, bool reconstruct, bool bf16, int num_sms,
                              cudaStream_t s) {
-    if (!down) return launch_var<false>(A, A.slots * A.gu.nseg, reconstruct, bf16, num_sms, s);
+    if (!down) return launch_var<false>(A, A.slots * 2 * A.gu_pairs, reconstruct, bf16, num_sms, s);
     return launch_var<true>(A, A.slots * A.npair * A.nrb, reconstruct, bf16, num_sms, s);
 }
 
@@ -246,7 +247,7 @@ cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const voi
     cudaError_t e = launch_lut_phase(A, false, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[1], s);
-    A.trace_base = A.slots * A.gu.nseg; // down units follow the gate/up units
+    A.trace_base = A.slots * 2 * A.gu_pairs; // down units follow the gate/up units
     e = launch_lut_phase(A, true, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[2], s);
