@@ -74,11 +74,15 @@ def test_noalloc_matches_forward_decode_shape():
 
 
 def test_noalloc_rejects_what_does_not_fit():
+    """64 tokens x top-16 at the decode shape need about 264 MB of partial-sum scratch, far past
+    the fixed array: refused on the host before anything is launched (the dummy buffers are
+    never read)."""
     w = synth.Workload("decode-e32", 7168, 1536, 32, 16, 1, "f32", "offsets")
-    cfg = B.make_config(w.d, w.f, w.n_experts, w.top_k, "f32", 2)
+    T = 64
+    cfg = B.make_config(w.d, w.f, w.n_experts, w.top_k, "f32", T)
     stride, _, _ = B.waste_moe_record_layout(cfg)
     dummy = B.aligned_bytes(4096, "cuda")
     with pytest.raises(B.WasteError) as ei:
-        B.waste_moe_forward_noalloc(cfg, dummy, stride, dummy, dummy, 2, dummy, dummy, dummy, 0)
+        B.waste_moe_forward_noalloc(cfg, dummy, stride, dummy, dummy, T, dummy, dummy, dummy, 0)
     assert ei.value.status == -1
     assert "scratch" in ei.value.message
