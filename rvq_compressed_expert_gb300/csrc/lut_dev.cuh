@@ -296,9 +296,9 @@ __device__ __forceinline__ void init_stage_barrier() {
 
 // Operands of unit U's table build into shared memory: the codebooks of its matrix, and for
 // a gate/up unit the token's input vectors of its two segments (raw, fp32 or bf16; vectors
-// past the input are zero-filled here, then a CTA barrier).  Every thread of the CTA calls
-// it; thread 0 issues the bulk copies on the staging mbarrier.  Nobody may be reading the
-// staged operands or x (the previous unit's tables are built).
+// past the input are zero-filled here).  Every thread calls it (the zero fill); thread 0
+// issues the bulk copies on the staging mbarrier.  Nobody may be reading the staged
+// operands or x (the previous unit's tables are built).
 template <bool kDown, bool kBf16, int kNT>
 __device__ __forceinline__ void stage_unit(const LutArgs &A, const Unit &U) {
     const float *cb, *cb1;
@@ -315,7 +315,6 @@ __device__ __forceinline__ void stage_unit(const LutArgs &A, const Unit &U) {
         xsrc = reinterpret_cast<const unsigned char *>(A.h) + ((size_t)t * A.gu.n_in + (size_t)j0 * kVec) * kEs;
         uint32_t *xw = reinterpret_cast<uint32_t *>(lut_smem + kOffXs);
         for (int i = (int)(xbytes / 4) + (int)threadIdx.x; i < 2 * kSegVec * kVec * kEs / 4; i += kNT) xw[i] = 0u;
-        __syncthreads(); // the zeros are in place before any thread reads x
     }
     if (threadIdx.x == 0) {
         const uint32_t s0 = (uint32_t)__cvta_generic_to_shared(lut_smem);
