@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
     __shared__ int claimed;
     int par = 0;
     bool primed = false;
-    if constexpr (!kRecon) init_stage_barrier();
     int cur = claim(F.sync, &claimed);
     int nxt = is_copy<kBanked>(F, cur) ? -1 : claim(F.sync, &claimed);
     while (cur < n_total(F)) {

@@ -3,7 +3,6 @@
 #pragma once
 
 #include "common.cuh"
-#include "tc_dev.cuh"
 
 
 namespace wm {
@@ -17,13 +16,6 @@ constexpr int kXsFloats = 512;               // down input staging (64 vectors x
 constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
 constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' codebooks
 constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
-constexpr int kXsBytes = kXsFloats * 4;
-// Shared memory of the table-form units: [tables][input vectors x][staged codebooks of the
-// unit's matrix][the staging mbarrier].  A unit's codebooks (and, for gate/up, its 64 input
-// vectors) are brought in by one bulk copy, issued while the previous unit streams.
-constexpr int kOffXs = kTabBytes;
-constexpr int kOffCbStage = kOffXs + kXsBytes;
-constexpr int kOffStageBar = kOffCbStage + kCbFloats * 4;
 constexpr bool kCodePingPong = false;            // hold the next round's codes in registers
 constexpr int kPrefetchRounds = 1;                 // L2 prefetch distance in row-group rounds
 
@@ -285,56 +277,6 @@ __device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target,
 // Dynamic shared memory of the lookup kernels (every extern __shared__ array names it).
 extern __shared__ __align__(16) unsigned char lut_smem[];
 
-// The staging mbarrier of the table-form units, set up once per CTA before its first unit.
-__device__ __forceinline__ void init_stage_barrier() {
-    if (threadIdx.x == 0) {
-        tc::mbar_init((uint32_t)__cvta_generic_to_shared(lut_smem + kOffStageBar), 1);
-        tc::mbar_init_fence();
-    }
-    __syncthreads();
-}
-
-// Operands of unit U's table build into shared memory: the codebooks of its matrix, and for
-// a gate/up unit the token's input vectors of its two segments (raw, fp32 or bf16; vectors
-// past the input are zero-filled here).  Every thread calls it (the zero fill); thread 0
-// issues the bulk copies on the staging mbarrier.  Nobody may be reading the staged
-// operands or x (the previous unit's tables are built).
-template <bool kDown, bool kBf16, int kNT>
-__device__ __forceinline__ void stage_unit(const LutArgs &A, const Unit &U) {
-    const float *cb, *cb1;
-    unit_codebooks<kDown>(A, U, cb, cb1);
-    (void)cb1;
-    uint32_t xbytes = 0;
-    const unsigned char *xsrc = nullptr;
-    if constexpr (!kDown) {
-        constexpr int kEs = kBf16 ? 2 : 4;
-        const int j0 = U.seg0 * kSegVec;
-        const int nvalid = max(0, min(2 * kSegVec, A.gu.nv - j0));
-        xbytes = (uint32_t)nvalid * kVec * kEs;
-        const int t = U.slot / A.k;
-        xsrc = reinterpret_cast<const unsigned char *>(A.h) + ((size_t)t * A.gu.n_in + (size_t)j0 * kVec) * kEs;
-        uint32_t *xw = reinterpret_cast<uint32_t *>(lut_smem + kOffXs);
-        for (int i = (int)(xbytes / 4) + (int)threadIdx.x; i < 2 * kSegVec * kVec * kEs / 4; i += kNT) xw[i] = 0u;
-    }
-    if (threadIdx.x == 0) {
-        const uint32_t s0 = (uint32_t)__cvta_generic_to_shared(lut_smem);
-        const uint32_t bar = s0 + kOffStageBar;
-        tc::mbar_arrive_expect_tx(bar, (uint32_t)kCbFloats * 4 + xbytes);
-        tc::bulk_g2s(s0 + kOffCbStage, cb, (uint32_t)kCbFloats * 4, bar);
-        if (xbytes) tc::bulk_g2s(s0 + kOffXs, xsrc, xbytes, bar);
-    }
-}
-
-// Every thread waits (bounded) for the staged operands of the current unit (phase `par`).
-__device__ __forceinline__ void wait_stage(int &par, uint32_t *err) {
-    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(lut_smem + kOffStageBar);
-    if (!tc::mbar_wait(bar, (uint32_t)par)) {
-        atomicOr(err, kErrTimeout);
-        tc::mbar_wait(bar, (uint32_t)par); // the copies target this CTA's shared memory
-    }
-    par ^= 1;
-}
-
 // One unit: tables (or staged codebooks) for the unit's segment(s), then the stream of
 // its rows.  `par`/`primed` carry the codebook stage buffers across consecutive units of
 // one kind: when `has_next`, the next unit's stages 0 and 1 are already on their way
@@ -357,10 +299,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     const Unit U = Uin;
     Unit N = Uin;
     if (has_next) N = Nin;
-    float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kOffXs));
-    // the table operands of this unit, unless the previous unit already asked for them
-    if constexpr (!kRecon)
-        if (!primed) stage_unit<kDown, kBf16, kNT>(A, U);
+    float *xs = reinterpret_cast<float *>(smem + (kRecon ? 2 * kCbFloats * 4 : kTabBytes));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const MatGeom &G = kDown ? A.dn : A.gu;
     // table column byte offset of part p: the slot of column `lane` in the permuted column
@@ -369,18 +308,17 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     const uint32_t colb1 = (1u << 7) | ((uint32_t)tab_col(lane) << 2);
     const bool valid = U.base[0] != nullptr;
     // warm L2 with the first rounds of row groups this warp streams (the tail of the
-    // previous unit already asked for them, except on a CTA's first unit), and (codebooks
-    // staged in shared memory by the table form) for the reconstruct form with the
-    // codebooks of the next unit, which it reads straight from global memory
+    // previous unit already asked for them, except on a CTA's first unit), and with the
+    // codebooks of the next unit, which its table build reads straight from global memory
 #pragma unroll 1
     for (int i = 0; i < kPf; ++i) {
         const int g = U.g0 + warp + i * kNW;
         if (g < U.g1) prefetch_group(U, g, lane);
     }
-    if (kRecon && has_next) {
+    if (!kRecon && has_next) {
         const float *q0, *q1;
         unit_codebooks<kDown>(A, N, q0, q1);
-        constexpr int kLines = kCbFloats / 32; // 128-byte lines of one matrix's codebooks
+        constexpr int kLines = kCbFloats / 32; // 128-byte lines of one part's codebooks
         (void)q1;
         for (int i = threadIdx.x; i < kLines; i += kNT) {
             const float *q = q0 + (size_t)i * 32;
@@ -443,17 +381,18 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         // the table is the product T[j][c] = sum_v X[j][v] C[c][v] (32 columns j x 256
         // codes c, K = 8), taken on the tensor cores as m16n8k8 TF32 MMAs with each operand
         // split into a TF32 head and tail (tail*head + head*tail + head*head), which keeps
-        // fp32 accuracy.  The warps form 2 teams of kNW / 2, one per part (segment); a warp
-        // takes both 16-row halves (all 32 columns j) of a code tile, and its team's 32 code
-        // tiles in turn.  Its operands -- the unit's codebooks and input vectors, staged in
-        // shared memory by a bulk copy -- are read before the barrier that frees the tables.
+        // fp32 accuracy.  The warps form 2 teams of kNW / 2, one per part; a warp takes
+        // both 16-row halves (all 32 columns j) of a code tile, and its team's 32 code tiles
+        // in turn.  Its operands come straight from global memory (L2), all in flight at
+        // once, before the barrier that frees the tables.
         float *tab = reinterpret_cast<float *>(smem);
         constexpr int kWpp = kNW / 2;                       // warps per part
         constexpr int kTiles = (kCodes / 8 + kWpp - 1) / kWpp; // code tiles per warp
         const int mp = warp / kWpp, mq = warp % kWpp;
         const int fg = lane >> 2, ft = lane & 3;
-        wait_stage(par, A.err);
-        const float *Cp = reinterpret_cast<const float *>(smem + kOffCbStage);
+        const float *p0, *p1;
+        unit_codebooks<kDown>(A, U, p0, p1);
+        const float *Cp = mp ? p1 : p0;
         float bv[kStages][kTiles][2];
 #pragma unroll
         for (int s = 0; s < kStages; ++s)
@@ -461,8 +400,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             for (int i = 0; i < kTiles; ++i) {
                 const int nt = mq + i * kWpp;
                 const float *c = Cp + ((size_t)s * kCodes + (size_t)min(nt, kCodes / 8 - 1) * 8 + fg) * kVec;
-                bv[s][i][0] = c[ft];
-                bv[s][i][1] = c[ft + 4];
+                bv[s][i][0] = __ldg(c + ft);
+                bv[s][i][1] = __ldg(c + ft + 4);
             }
         // A operand: column j = fg + 8 k of part mp (k = 0..3), inputs ft and ft + 4
         float av[2][4];
@@ -471,14 +410,16 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int j = mm * 16 + fg + 8 * h2;
-                const int xi = (mp * kSegVec + j) * kVec + ft;
-                if constexpr (!kDown && kBf16) {
-                    const __nv_bfloat16 *X = reinterpret_cast<const __nv_bfloat16 *>(xs);
-                    av[mm][h2] = __bfloat162float(X[xi]);
-                    av[mm][2 + h2] = __bfloat162float(X[xi + 4]);
+                if constexpr (!kDown) {
+                    const int jg = (U.seg0 + mp) * kSegVec + j;
+                    const bool in = jg < G.nv;
+                    const size_t e0 = (size_t)t * A.gu.n_in + (size_t)min(jg, G.nv - 1) * kVec;
+                    av[mm][h2] = in ? load_x1<kBf16>(A.h, e0 + ft) : 0.f;
+                    av[mm][2 + h2] = in ? load_x1<kBf16>(A.h, e0 + ft + 4) : 0.f;
                 } else {
-                    av[mm][h2] = xs[xi];
-                    av[mm][2 + h2] = xs[xi + 4];
+                    const float *X = xs + mp * kSegVec * kVec + j * kVec;
+                    av[mm][h2] = X[ft];
+                    av[mm][2 + h2] = X[ft + 4];
                 }
             }
         __syncthreads(); // the previous unit's lookups are done with the tables
@@ -531,10 +472,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                 }
             }
         }
-        __syncthreads(); // tables complete (and the staged operands read)
-        // the next unit's table operands come in while this one streams
-        if (has_next) stage_unit<kDown, kBf16, kNT>(A, N);
-        primed = has_next;
+        __syncthreads(); // tables complete
     } else {
         __syncthreads(); // the previous unit's lookups are done with the codebook rows
         // ---- codebooks of both parts [2][3][256][8]
@@ -548,6 +486,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         }
         __syncthreads();
     }
+    (void)par;
+    (void)primed;
 
     if (t_tables && threadIdx.x == 0) t_tables[0] = gtimer();
 
@@ -711,7 +651,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
 // Bytes of dynamic shared memory of a unit.
 template <bool kRecon>
 constexpr size_t unit_smem() {
-    return kRecon ? 2 * kCbFloats * 4 + kXsFloats * 4 : kOffStageBar + 16;
+    return (kRecon ? 2 * kCbFloats * 4 : kTabBytes) + kXsFloats * 4;
 }
 
 } // namespace lut

@@ -41,7 +41,6 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
     const int units = kDown ? n_slots * A.npair * A.nrb : n_slots * 2 * A.gu_pairs;
     int par = 0;
     bool primed = false;
-    if constexpr (!kRecon) init_stage_barrier();
     Unit N;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const Unit U = decode_unit<kDown>(A, u);
