@@ -378,97 +378,93 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     }
     if constexpr (!kRecon) {
         // ---- tables T[s][c][part][column], one 64 KiB block per stage.  Per stage and part
-        // the table is the product T[j][c] = sum_v X[j][v] C[c][v] (32 columns j x 256
-        // codes c, K = 8), taken on the tensor cores as m16n8k8 TF32 MMAs with each operand
-        // split into a TF32 head and tail (tail*head + head*tail + head*head), which keeps
-        // fp32 accuracy.  The warps form 2 teams of kNW / 2, one per part; a warp takes
-        // both 16-row halves (all 32 columns j) of a code tile, and its team's 32 code tiles
-        // in turn.  Its operands come straight from global memory (L2), all in flight at
-        // once, before the barrier that frees the tables.
+        // the table is the product T[c][j] = sum_v C[c][v] X[j][v] (256 codes c x 32
+        // columns j, K = 8), taken on the tensor cores as m16n8k8 TF32 MMAs (M = 16 codes,
+        // N = 8 columns) with each operand split into a TF32 head and tail (head*tail +
+        // tail*head + head*head), which keeps fp32 accuracy.  The warps form 2 teams of
+        // kNW / 2, one per part; a warp takes kMt 16-code tiles of every stage, each across
+        // all 32 columns.  Its operands come straight from global memory (L2), all in flight
+        // at once, before the barrier that frees the tables.  The MMA's D fragment already
+        // holds, per lane, 16-byte slots of the permuted column order, so the stores need no
+        // shuffles.
         float *tab = reinterpret_cast<float *>(smem);
-        constexpr int kWpp = kNW / 2;                       // warps per part
-        constexpr int kTiles = (kCodes / 8 + kWpp - 1) / kWpp; // code tiles per warp
+        constexpr int kWpp = kNW / 2;                 // warps per part
+        constexpr int kMt = (kCodes / 16) / kWpp;     // 16-code tiles per warp and stage
+        static_assert((kCodes / 16) % kWpp == 0, "code tiles per warp");
         const int mp = warp / kWpp, mq = warp % kWpp;
         const int fg = lane >> 2, ft = lane & 3;
         const float *p0, *p1;
         unit_codebooks<kDown>(A, U, p0, p1);
         const float *Cp = mp ? p1 : p0;
-        float bv[kStages][kTiles][2];
+        // A operand (codebook rows c0 + fg and c0 + fg + 8 of tile (s, i); inputs ft, ft + 4)
+        float av[kStages][kMt][4];
 #pragma unroll
         for (int s = 0; s < kStages; ++s)
 #pragma unroll
-            for (int i = 0; i < kTiles; ++i) {
-                const int nt = mq + i * kWpp;
-                const float *c = Cp + ((size_t)s * kCodes + (size_t)min(nt, kCodes / 8 - 1) * 8 + fg) * kVec;
-                bv[s][i][0] = __ldg(c + ft);
-                bv[s][i][1] = __ldg(c + ft + 4);
+            for (int i = 0; i < kMt; ++i) {
+                const float *r0 = Cp + ((size_t)s * kCodes + (size_t)(mq * kMt + i) * 16 + fg) * kVec;
+                const float *r1 = r0 + 8 * kVec;
+                av[s][i][0] = __ldg(r0 + ft);
+                av[s][i][1] = __ldg(r1 + ft);
+                av[s][i][2] = __ldg(r0 + ft + 4);
+                av[s][i][3] = __ldg(r1 + ft + 4);
             }
-        // A operand: column j = fg + 8 k of part mp (k = 0..3), inputs ft and ft + 4
-        float av[2][4];
+        // B operand: column j = 8 nt + fg of part mp (nt = 0..3), inputs ft and ft + 4
+        float bv[4][2];
 #pragma unroll
-        for (int mm = 0; mm < 2; ++mm)
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int j = mm * 16 + fg + 8 * h2;
-                if constexpr (!kDown) {
-                    const int jg = (U.seg0 + mp) * kSegVec + j;
-                    const bool in = jg < G.nv;
-                    const size_t e0 = (size_t)t * A.gu.n_in + (size_t)min(jg, G.nv - 1) * kVec;
-                    av[mm][h2] = in ? load_x1<kBf16>(A.h, e0 + ft) : 0.f;
-                    av[mm][2 + h2] = in ? load_x1<kBf16>(A.h, e0 + ft + 4) : 0.f;
-                } else {
-                    const float *X = xs + mp * kSegVec * kVec + j * kVec;
-                    av[mm][h2] = X[ft];
-                    av[mm][2 + h2] = X[ft + 4];
-                }
+        for (int nt = 0; nt < 4; ++nt) {
+            const int j = 8 * nt + fg;
+            if constexpr (!kDown) {
+                const int jg = (U.seg0 + mp) * kSegVec + j;
+                const bool in = jg < G.nv;
+                const size_t e0 = (size_t)t * A.gu.n_in + (size_t)min(jg, G.nv - 1) * kVec;
+                bv[nt][0] = in ? load_x1<kBf16>(A.h, e0 + ft) : 0.f;
+                bv[nt][1] = in ? load_x1<kBf16>(A.h, e0 + ft + 4) : 0.f;
+            } else {
+                const float *X = xs + mp * kSegVec * kVec + j * kVec;
+                bv[nt][0] = X[ft];
+                bv[nt][1] = X[ft + 4];
             }
+        }
         __syncthreads(); // the previous unit's lookups are done with the tables
         if (t_tables && threadIdx.x == 0) t_tables[1] = gtimer();
-        uint32_t ahi[2][4], alo[2][4];
+        uint32_t bhi[4][2], blo[4][2];
 #pragma unroll
-        for (int mm = 0; mm < 2; ++mm)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) split_tf32(av[mm][i], ahi[mm][i], alo[mm][i]);
-        // the lane whose results this lane stores: quarter-warp q stores code pair q of the
-        // tile for the 8 row groups fg, so its 8 lanes hit 8 different bank quads
-        const int src = ((lane & 7) << 2) | (lane >> 3);
-        const int st_fg = lane & 7, st_ft = lane >> 3;
+            for (int q = 0; q < 2; ++q) split_tf32(bv[nt][q], bhi[nt][q], blo[nt][q]);
+        // Lane (fg, ft) ends with, for code c0 + fg (and c0 + fg + 8), the columns 2 ft + 8 nt
+        // (nt = 0..3) -- the slots of column group 2 ft -- and 2 ft + 1 + 8 nt (group 2 ft + 1).
+        // Lanes of odd fg store group 2 ft + 1 first, so each quarter-warp's 8 lanes hit 8
+        // different bank quads in both stores.
+        const int odd = fg & 1;
+        const int g_first = 2 * ft + odd, g_second = 2 * ft + 1 - odd;
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
 #pragma unroll
-            for (int i = 0; i < kTiles; ++i) {
-                const int nt = mq + i * kWpp;
-                if (nt >= kCodes / 8) break;
-                const int c0 = nt * 8; // first code of this n-tile
-                uint32_t bhi[2], blo[2];
-                split_tf32(bv[s][i][0], bhi[0], blo[0]);
-                split_tf32(bv[s][i][1], bhi[1], blo[1]);
-                float dd[2][4];
+            for (int i = 0; i < kMt; ++i) {
+                const int c0 = (mq * kMt + i) * 16;
+                uint32_t ahi[4], alo[4];
 #pragma unroll
-                for (int mm = 0; mm < 2; ++mm) {
-                    dd[mm][0] = dd[mm][1] = dd[mm][2] = dd[mm][3] = 0.f;
-                    mma_tf32(dd[mm], alo[mm], bhi);
-                    mma_tf32(dd[mm], ahi[mm], blo);
-                    mma_tf32(dd[mm], ahi[mm], bhi);
-                }
-                // D rows are columns j, D columns are codes c.  Lane (fg, ft) holds, for
-                // code c0 + 2 ft + b, the columns fg, fg + 8, fg + 16, fg + 24 -- one
-                // 16-byte slot of the permuted column order; they move to lane
-                // 8 ft + fg and are stored as two 128-bit words.
-                float v[2][4];
+                for (int q = 0; q < 4; ++q) split_tf32(av[s][i][q], ahi[q], alo[q]);
+                float dd[4][4];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    v[b][0] = __shfl_sync(0xffffffffu, dd[0][b], src);
-                    v[b][1] = __shfl_sync(0xffffffffu, dd[0][2 + b], src);
-                    v[b][2] = __shfl_sync(0xffffffffu, dd[1][b], src);
-                    v[b][3] = __shfl_sync(0xffffffffu, dd[1][2 + b], src);
+                for (int nt = 0; nt < 4; ++nt) {
+                    dd[nt][0] = dd[nt][1] = dd[nt][2] = dd[nt][3] = 0.f;
+                    mma_tf32(dd[nt], ahi, blo[nt]);
+                    mma_tf32(dd[nt], alo, bhi[nt]);
+                    mma_tf32(dd[nt], ahi, bhi[nt]);
                 }
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    if (!valid) v[b][0] = v[b][1] = v[b][2] = v[b][3] = 0.f;
-                    const int c = c0 + 2 * st_ft + b;
-                    float *t0 = tab + (((size_t)s * kCodes + c) * 2 + mp) * kSegVec + 4 * st_fg;
-                    *reinterpret_cast<float4 *>(t0) = make_float4(v[b][0], v[b][1], v[b][2], v[b][3]);
+                for (int hh = 0; hh < 2; ++hh) {
+                    float4 ev = make_float4(dd[0][2 * hh], dd[1][2 * hh], dd[2][2 * hh], dd[3][2 * hh]);
+                    float4 ov = make_float4(dd[0][2 * hh + 1], dd[1][2 * hh + 1], dd[2][2 * hh + 1],
+                                            dd[3][2 * hh + 1]);
+                    if (!valid) ev = ov = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int c = c0 + fg + 8 * hh;
+                    float *row = tab + (((size_t)s * kCodes + c) * 2 + mp) * kSegVec;
+                    *reinterpret_cast<float4 *>(row + 4 * g_first) = odd ? ov : ev;
+                    *reinterpret_cast<float4 *>(row + 4 * g_second) = odd ? ev : ov;
                 }
             }
         }
