@@ -168,10 +168,39 @@ def ncu_traffic(kernel_tag: str):
 
 # ---------------------------------------------------------------- native arm
 
+def expert_code_bytes(d: int, f: int) -> int:
+    """Code bytes of one expert: 3 matrices of d x f weights, 3 stages x 1 byte per 8 weights
+    (12,386,304 B at d=7168, f=1536)."""
+    return 3 * 3 * d * f // 8
+
+
+def host_description() -> dict:
+    """The host cores the CPU baseline runs on: count and model name."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":", 1)[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for line in fh:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model, "machine": platform.machine()}
+
+
 def decode_algorithmic_bytes(w):
     """Algorithmic bytes per decode step and per gate/up and down launch."""
-    import oracle  # only for its byte count of one expert's codes (pinned to the pages)
-    codes = oracle.expert_code_bytes(w.d, w.f)  # 12,386,304 B at d=7168, f=1536
+    codes = expert_code_bytes(w.d, w.f)
     cb_mat = 3 * 256 * 8 * 4
     gate_up = w.top_k * (2 * codes // 3 + 2 * cb_mat) + w.d * 4
     down = w.top_k * (codes // 3 + cb_mat)
@@ -301,11 +330,36 @@ def run_decode(args, dev, out):
     step_bytes, gu_bytes, dn_bytes = decode_algorithmic_bytes(w)
     kern = {k: statistics.mean(p[k] for p in prof) for k in prof[0] if prof[0][k] >= 0}
     ms_per_step = total_ms / K
+
+    # the register-reconstruct form of the expert kernels (WASTE_FLAG_K2_RECONSTRUCT: each
+    # 8-weight vector rebuilt from its 3 codebook rows in shared memory, then an 8-term dot
+    # product) on the same weights, per-kernel times as above
+    rcfg = B.make_config(w.d, w.f, w.n_experts, w.top_k, w.act_dtype, 1, 0, B.FLAG_K2_RECONSTRUCT, layer.layer)
+    rh = B.waste_moe_create(rcfg, layer.router_w, layer.router_b, layer.records, layer.stride, layer.codebooks)
+    B.waste_moe_set_profiling(rh, True)
+    rprof = []
+    for i in range(max(8, min(K, 40))):
+        h_in.copy_(pool[i % DECODE_POOL])
+        flush.zero_()
+        torch.cuda._sleep(100_000)
+        B.waste_moe_step(rh, h_in, 1, idx, gate, logits, y, 0)
+        if i >= 3:
+            rprof.append(B.waste_moe_read_profile(rh))
+    torch.cuda.synchronize()
+    B.waste_moe_destroy(rh)
+    rk = {k: statistics.mean(p[k] for p in rprof) for k in rprof[0] if rprof[0][k] >= 0}
+    peak_k2, _, _ = measured_peaks()
+    k2a = dict(kernels_ms=rk, steps_profiled=len(rprof),
+               gate_up_gbs=gu_bytes / (rk["gate_up"] * 1e-3) / 1e9,
+               gate_up_frac=gu_bytes / (rk["gate_up"] * 1e-3) / 1e9 / peak_k2,
+               down_frac=dn_bytes / (rk["down"] * 1e-3) / 1e9 / peak_k2,
+               table_form_gate_up_ms=kern.get("gate_up"), table_form_down_ms=kern.get("down"))
     out["decode"] = dict(step_ms=ms_per_step, kernels_ms=kern, stats=st, step_bytes=step_bytes,
                          gate_up_bytes=gu_bytes, down_bytes=dn_bytes,
                          hbm_gbs_step=step_bytes / (ms_per_step * 1e-3) / 1e9,
                          median_step_ms=statistics.median(step_ms),
-                         launches_per_step=4, profiled_steps=n_prof, unfused_ms=unfused_ms)
+                         launches_per_step=4, profiled_steps=n_prof, unfused_ms=unfused_ms,
+                         k2a_reconstruct=k2a)
 
     # ---- end to end through the C ABI with host buffers: h2d copy of the token from
     # pinned memory, then route + forward with the result written by the combine straight
@@ -344,13 +398,30 @@ def run_decode(args, dev, out):
     torch.cuda.synchronize()
     args.sampler.mark(t_start, time.time())
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev2), args.world, dev)
+    # the same loop timed by the host's clock, one step at a time: the copy of the next token
+    # into the pinned buffer, the launch, and the wait for the result in host memory are all
+    # inside
+    torch.cuda.synchronize()
+    t_w = time.perf_counter()
+    for i in range(K):
+        h_host.copy_(host_pool[i % 8])
+        g2.replay()
+        torch.cuda.current_stream().synchronize()
+    wall_s = time.perf_counter() - t_w
     # the last token's result in host memory equals the same step written to device memory
     step()
     torch.cuda.synchronize()
     same = bool(torch.equal(y.cpu(), y_host))
     out["e2e"] = dict(value=args.world * K / (e2e_ms * 1e-3), unit=UNIT,
                       h2d_bytes_per_step=w.d * 4, d2h_bytes_per_step=w.d * 4,
-                      output_equals_device_path=same)
+                      output_equals_device_path=same,
+                      timing="CUDA events on the stream around each step's graph (H2D copy of the token "
+                             "from pinned memory, route + experts, result written into pinned host memory); "
+                             "host launch cost outside",
+                      wall_clock_value=args.world * K / wall_s,
+                      wall_clock_timing="host clock over the whole loop, each step: host copy of the "
+                                        "token into the pinned buffer, graph launch, wait for the result "
+                                        "(no L2 flush)")
     out["_layer"] = layer
     out["_pool"] = pool
 
@@ -362,7 +433,6 @@ def run_batched(args, dev, out, name, steps):
     from rvq_compressed_expert_gb300 import binding as B
     from rvq_compressed_expert_gb300 import synth
     from rvq_compressed_expert_gb300.layer import MoELayer
-    import oracle  # only for its byte count of one expert's codes (pinned to the pages)
 
     w = synth.WORKLOADS[name]
     T = w.tokens
@@ -424,13 +494,15 @@ def run_batched(args, dev, out, name, steps):
     ms_gemv = timed(gh, 3)
     B.waste_moe_destroy(gh)
 
-    per_expert = oracle.expert_code_bytes(w.d, w.f) + 3 * 3 * 256 * 8 * 4
+    per_expert = expert_code_bytes(w.d, w.f) + 3 * 3 * 256 * 8 * 4
     alg_bytes = n_distinct * per_expert + w.n_experts * w.d * 4 + T * w.d * (2 + 4)
     flops = T * w.top_k * 3 * 2 * w.d * w.f
     peak_gbs, _, pk = measured_peaks()
-    # fp16 operands run at the bf16 dense rate (nominal ratio 1:1); the burst figure, since
-    # the kernels are timed on their own
-    peak_tf = float(pk["bf16_tflops"]) if pk else 1900.0
+    # fp16 operands run at the bf16 dense rate (nominal ratio 1:1).  A step lasts milliseconds
+    # and is replayed back to back, so the sustained figure is its peak; the burst one is
+    # reported beside it
+    peak_tf = float(pk["bf16_tflops_sustained"]) if pk else 1700.0
+    peak_tf_burst = float(pk["bf16_tflops"]) if pk else 1900.0
     out[name] = dict(
         workload=f"{name}: d={w.d} f={w.f} E={w.n_experts} top-{w.top_k}, T={T} tokens/step, "
                  f"{w.act_dtype} h, router bias {w.bias}",
@@ -442,24 +514,27 @@ def run_batched(args, dev, out, name, steps):
         hbm_frac_whole_step=alg_bytes / (ms * 1e-3) / 1e9 / peak_gbs,
         tflops_whole_step=flops / (ms * 1e-3) / 1e12,
         tensor_frac_whole_step=flops / (ms * 1e-3) / 1e12 / peak_tf,
+        tensor_peak="bf16_tflops_sustained of MEASURED_PEAKS.json" if pk else "fallback 1.7 PFLOP/s sustained",
+        tensor_frac_whole_step_of_burst=flops / (ms * 1e-3) / 1e12 / peak_tf_burst,
         lookup_only_ms_per_step=ms_gemv, speedup_over_lookup_only=ms_gemv / ms,
         demand_code_bytes_per_step=st["demand_code_bytes"],
     )
     layer.close()
 
 
-def run_stack(args, dev, out):
-    """92 layers x 64 experts, one token, h += combine per layer; lookahead 6 vs off."""
+def run_stack(args, dev, out, w=None, key="stack"):
+    """92 layers x 64 experts, one token, h += combine per layer; lookahead 6 vs off.  With w and
+    key: another stack workload reported under key."""
     from rvq_compressed_expert_gb300 import binding as B
     from rvq_compressed_expert_gb300 import synth
     from rvq_compressed_expert_gb300.layer import MoELayer
     from rvq_compressed_expert_gb300.stack import DecodeStack
 
-    w = synth.WORKLOADS["stack"]
+    w = w or synth.WORKLOADS["stack"]
     free, _ = torch.cuda.mem_get_info()
     need = w.n_layers * w.n_experts * 12_390_400 * 1.05 + (4 << 30)
     if free < need:
-        out["stack"] = {"skipped": f"needs {need / 1e9:.0f} GB free, {free / 1e9:.0f} GB available"}
+        out[key] = {"skipped": f"needs {need / 1e9:.0f} GB free, {free / 1e9:.0f} GB available"}
         return
     layers = [MoELayer(w, seed=0, layer=L, device=dev, max_tokens=1) for L in range(w.n_layers)]
     h0 = synth.hidden(7, 1, w.d, "f32", dev)
@@ -510,9 +585,9 @@ def run_stack(args, dev, out):
             prediction_hits_per_token=sum(s["prediction_hits"] for s in sts) / n)
         del g
     on, off = res[w.lookahead], res[0]
-    out["stack"] = dict(
+    out[key] = dict(
         workload=f"{w.n_layers} layers x {w.n_experts} experts, d={w.d} f={w.f} top-{w.top_k}, T=1, fp32, "
-                 f"h += combine per layer; CUDA graph per token; L2 flushed between tokens",
+                 f"router bias {w.bias}, h += combine per layer; CUDA graph per token; L2 flushed between tokens",
         tok_s_lookahead_off=off["tok_s"], tok_s_lookahead_on=on["tok_s"],
         lookahead_speedup=on["tok_s"] / off["tok_s"],
         outputs_bit_identical=bool(torch.equal(final[0], final[w.lookahead])),
@@ -522,7 +597,7 @@ def run_stack(args, dev, out):
         prediction_accuracy=on["prediction_hits_per_token"] / ((w.n_layers - 1) * w.lookahead),
     )
     if errors:
-        out["stack"]["device_errors"] = errors[:8]
+        out[key]["device_errors"] = errors[:8]
     for L in layers:
         L.close()
     del layers
@@ -731,7 +806,45 @@ def cpu_baseline_decode(layer, pool, budget_s=12.0):
         done += 1
     return dict(value=done / spent, unit=UNIT, cores=1, kind="oracle",
                 sample=f"{done} decode tokens (full layer each: router over 384 experts, top-16, "
-                       f"16 expert FFNs from codes, combine), single-threaded C oracle")
+                       f"16 expert FFNs from codes, combine), single-threaded C oracle",
+                host=host_description())
+
+
+def _oracle_worker(job):
+    """One process of the parallel CPU baseline: the single-threaded oracle on up to n decode
+    tokens of a layer drawn on the CPU (the same shapes and distributions); only the oracle's
+    own call is timed.  Returns (tokens, seconds)."""
+    seed0, n = job
+    import oracle
+    from rvq_compressed_expert_gb300 import synth
+    w = synth.WORKLOADS["decode"]
+    li = synth.layer_inputs(w, 0, 0, "cpu", with_codes=False)
+    cbs = li.codebooks.numpy()
+    done, spent = 0, 0.0
+    for i in range(n):
+        h = synth.hidden(seed0 + i, 1, w.d, "f32", "cpu")[0]
+        logits = oracle.router(li.router_w, li.router_b, h)
+        idx, _ = oracle.topk_softmax(logits, w.top_k)
+        codes = {int(e): synth.expert_codes(0, 0, int(e), w.d, w.f, "cpu") for e in idx}
+        t0 = time.perf_counter()
+        oracle.moe_token(h, li.router_w, li.router_b, cbs, lambda e: codes[int(e)], w.top_k)
+        spent += time.perf_counter() - t0
+        done += 1
+    return done, spent
+
+
+def cpu_baseline_parallel(tokens_per_proc=3):
+    """The same oracle in one process per host core (spawned, so no GPU state is inherited),
+    each timing its own tokens: the aggregate rate is the sum of the processes' rates."""
+    import multiprocessing as mp
+    n = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_oracle_worker, [(5000 + 100 * i, tokens_per_proc) for i in range(n)])
+    rate = sum(d / s for d, s in res if s > 0)
+    return dict(value=rate, unit=UNIT, cores=n, kind="oracle",
+                sample=f"{sum(d for d, _ in res)} decode tokens over {n} processes of the single-threaded "
+                       f"C oracle ({tokens_per_proc} each, layer drawn on the CPU); sum of per-process rates",
+                host=host_description())
 
 
 def native(args):
@@ -763,14 +876,22 @@ def native(args):
         run_batched(args, dev, res, "prefill", 10)
     if rank == 0 and not args.no_stack:
         run_stack(args, dev, res)
+        # a shorter stack whose Zipf-like router bias makes the lookahead's predictions miss
+        from rvq_compressed_expert_gb300 import synth as _s
+        zw = _s.Workload("stack-zipf", 7168, 1536, 64, 16, 1, "f32", "zipf", n_layers=16, lookahead=6)
+        run_stack(args, dev, res, zw, "stack_zipf")
     if rank == 0 and not args.no_tiered:
         run_tiered(args, dev, res)
     if rank == 0 and not args.no_encoder:
         run_encoder(args, dev, res)
     clocks = args.sampler.stop()
-    cpu = None
+    cpu = cpu_par = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_decode(res["_layer"], res["_pool"])
+        try:
+            cpu_par = cpu_baseline_parallel()
+        except Exception as e:  # the parallel line is optional; the single-core one stands
+            cpu_par = {"unavailable": f"{type(e).__name__}: {e}"}
     if rank != 0:
         return
     from rvq_compressed_expert_gb300 import synth
@@ -818,6 +939,7 @@ def native(args):
             "algorithmic_bytes_per_step": d["step_bytes"],
             "kernels_ms": kern,
             "ms_per_step_persistent_step_kernel": d["unfused_ms"],
+            "k2a_register_reconstruct": d["k2a_reconstruct"],
         },
         "roofline": {
             "bound": "hbm",
@@ -835,11 +957,12 @@ def native(args):
         "gpu_launches": args.steps * d["launches_per_step"],
         "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
         "cpu_baseline": cpu,
+        "cpu_baseline_parallel": cpu_par,
         "stats_per_step": {k: v / args.steps for k, v in d["stats"].items()},
     }
     if "verify_crc" in res:
         line["config"]["create_with_crc_verify"] = res["verify_crc"]
-    for extra in ("batched", "prefill", "stack", "tiered", "encoder"):
+    for extra in ("batched", "prefill", "stack", "stack_zipf", "tiered", "encoder"):
         if extra in res:
             line[extra] = res[extra]
     print(json.dumps(line), flush=True)
@@ -889,7 +1012,8 @@ def reference(args):
         "config": {"workload": "decode layer: d=7168 f=1536 E=384 experts top-16, T=1 token/step, fp32 h",
                    "parallelism": "host cores, single thread"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{K} decode tokens, one per step (capped at 20 steps)"},
+                         "sample": f"{K} decode tokens, one per step (capped at 20 steps)",
+                         "host": host_description()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -254,8 +254,12 @@ int waste_moe_set_trace(waste_moe *h, uint64_t *d_trace, int32_t n_items);
 
 /* Lookahead: run next_layer's router on the current hidden states d_h [T][d],
  * take its top n_prefetch experts per token (n_prefetch < 0: the handle's
- * lookahead; 0: nothing) and prefetch their records into L2.  Writes no
- * user-visible buffer and never changes any output.  The caller orders it after
+ * lookahead; 0: nothing) and prefetch into L2 what their gate/up units read
+ * first: the first 16 row groups of every 32-vector segment of gate and up, and
+ * the gate and up codebooks (about 1.4 MB per expert at d = 7168, f = 1536; the
+ * whole record would not survive the current layer's stream in L2).  On a
+ * banked handle the predicted records are copied into the HBM cache instead.
+ * Writes no user-visible buffer and never changes any output.  The caller orders it after
  * d_h is ready and before next_layer's route (events), and must not overwrite
  * d_h until it has run. */
 int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_t n_prefetch,
@@ -268,7 +272,7 @@ typedef struct {
     uint64_t demand_code_bytes;     /* code bytes the expert kernels read (algorithmic) */
     uint64_t codebook_bytes;        /* codebook bytes used by the expert kernels */
     uint64_t router_bytes;          /* router weight bytes read by route */
-    uint64_t prefetch_issued_bytes; /* record bytes named in L2 prefetches */
+    uint64_t prefetch_issued_bytes; /* record and codebook bytes named in L2 prefetches */
     uint64_t prefetch_experts;      /* (token, expert) prefetches issued */
     uint64_t prediction_hits;       /* routed experts that had been predicted */
     uint64_t routed_slots;          /* (token, expert) slots routed */

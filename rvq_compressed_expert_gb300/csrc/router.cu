@@ -359,27 +359,38 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
               stats, router_bytes, smem_topk);
 }
 
-// L2 prefetch of predicted experts' records: one CTA per (token, rank);
-// each thread names 64 KiB pieces of the record's three sections.
-__global__ void __launch_bounds__(128) prefetch_l2_kernel(const uint8_t *__restrict__ records,
-                                                          size_t stride, size_t payload_off,
-                                                          size_t payload_bytes, int E,
+// L2 prefetch of predicted experts: one CTA per (token, rank).  With every expert resident in
+// HBM the only gain is the first read of each unit, so the prefetch asks L2 for what the
+// gate/up units of the expert read first -- the first kLookaheadGroups row groups of each
+// 32-vector segment of gate and up (one round of a 16-warp unit's row stream) -- and the
+// expert's gate and up codebooks: about 1.4 MB per expert at d = 7168, f = 1536, small enough
+// to stay in L2 while the current layer streams, where whole records (12.4 MB each) were
+// evicted before use and read twice.
+constexpr int kLookaheadGroups = 16;
+
+__global__ void __launch_bounds__(128) prefetch_l2_kernel(const uint8_t *__restrict__ records, size_t stride,
+                                                          size_t off_gate, size_t off_up, int nseg, int groups,
+                                                          const float *__restrict__ codebooks, int E,
                                                           const int32_t *__restrict__ pred_idx,
                                                           int pred_stride, int P,
                                                           unsigned long long *stats) {
     const int t = blockIdx.x / P, p = blockIdx.x % P;
     const int e = pred_idx[(size_t)t * pred_stride + p];
     if (e < 0 || e >= E) return;
-    const uint8_t *base = records + (size_t)e * stride + payload_off;
-    constexpr size_t kPiece = 65536;
-    for (size_t off = (size_t)threadIdx.x * kPiece; off < payload_bytes; off += 128 * kPiece) {
-        const uint32_t n = (uint32_t)min(kPiece, payload_bytes - off);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n)
-                     : "memory");
+    const uint8_t *rec = records + (size_t)e * stride;
+    const uint32_t seg_bytes = (uint32_t)min(groups, kLookaheadGroups) * (kStages * 512);
+    for (int i = threadIdx.x; i < 2 * nseg; i += blockDim.x) {
+        const uint8_t *q = rec + (i < nseg ? off_gate : off_up) + (size_t)(i % nseg) * groups * (kStages * 512);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(q), "r"(seg_bytes) : "memory");
     }
-    if (threadIdx.x == 0 && stats) {
-        atomicAdd(stats + kStatPrefetchBytes, (unsigned long long)payload_bytes);
-        atomicAdd(stats + kStatPrefetchExperts, 1ull);
+    constexpr uint32_t kCbBytes = 2 * kStages * kCodes * kVec * 4; // gate and up codebooks
+    if (threadIdx.x == 0) {
+        const float *cb = codebooks + (size_t)e * 3 * kStages * kCodes * kVec;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cb), "r"(kCbBytes) : "memory");
+        if (stats) {
+            atomicAdd(stats + kStatPrefetchBytes, (unsigned long long)2 * nseg * seg_bytes + kCbBytes);
+            atomicAdd(stats + kStatPrefetchExperts, 1ull);
+        }
     }
 }
 
@@ -535,10 +546,8 @@ cudaError_t launch_set_pred_count(int32_t *pred_count, int T, int P, cudaStream_
 cudaError_t launch_prefetch_l2(const LayerView &L, const int32_t *pred_idx, int pred_stride,
                                int T, int P, int32_t *pred_count, unsigned long long *stats,
                                cudaStream_t s) {
-    const size_t payload_off = L.sec_off[0];
-    const size_t payload_bytes = L.sec_off[2] + L.dn.chunk_bytes() - L.sec_off[0];
-    prefetch_l2_kernel<<<T * P, 128, 0, s>>>(L.records, L.stride, payload_off, payload_bytes, L.E,
-                                             pred_idx, pred_stride, P, stats);
+    prefetch_l2_kernel<<<T * P, 128, 0, s>>>(L.records, L.stride, L.sec_off[0], L.sec_off[1], L.gu.nseg,
+                                             L.gu.groups, L.codebooks, L.E, pred_idx, pred_stride, P, stats);
     set_count_kernel<<<(T + 255) / 256, 256, 0, s>>>(pred_count, T, P);
     return cudaGetLastError();
 }

@@ -218,3 +218,36 @@ def test_full_depth_token_matches_oracle():
         for l in layers:
             l.close()
         torch.cuda.empty_cache()
+
+
+def test_lookahead_with_mispredictions():
+    """A stack whose router bias gives Zipf-like expert popularity: the lookahead's predictions
+    (layer L+1's router on layer L's input) miss some experts.  Outputs are still bit-identical
+    with the lookahead on and off, demand bytes equal, and each prediction names the first row
+    groups of gate and up plus their codebooks, whatever it hits."""
+    w = synth.Workload("zipf-stack", 512, 256, 32, 4, 4, "f32", "zipf", n_layers=6, lookahead=3)
+    pairs = make_layers(w)
+    layers = [p[0] for p in pairs]
+    try:
+        hd = synth.hidden(5, w.tokens, w.d, "f32", "cuda")
+        stack = DecodeStack(layers, w.tokens)
+        res = {}
+        for P in (0, w.lookahead):
+            for l in layers:
+                l.reset_stats()
+            out = run_eager(stack, hd, P)
+            sts = [l.stats() for l in layers]
+            res[P] = (out, {k: sum(s[k] for s in sts) for k in sts[0]})
+        (out0, s0), (out1, s1) = res[0], res[w.lookahead]
+        assert torch.equal(out0, out1)
+        assert s0["demand_code_bytes"] == s1["demand_code_bytes"]
+        n_pred = (w.n_layers - 1) * w.tokens * w.lookahead
+        assert s1["prefetch_experts"] == n_pred
+        nseg = -(-w.d // 256)
+        groups = -(-w.f // 16)
+        per_expert = 2 * nseg * min(groups, 16) * 3 * 512 + 2 * 3 * 256 * 8 * 4
+        assert s1["prefetch_issued_bytes"] == n_pred * per_expert
+        assert 0 < s1["prediction_hits"] < n_pred, s1["prediction_hits"]
+    finally:
+        for l in layers:
+            l.close()
