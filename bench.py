@@ -876,9 +876,10 @@ def native(args):
         run_batched(args, dev, res, "prefill", 10)
     if rank == 0 and not args.no_stack:
         run_stack(args, dev, res)
-        # a shorter stack whose Zipf-like router bias makes the lookahead's predictions miss
+        # a shorter stack whose router bias follows a weak Zipf law (s = 0.3), so the
+        # lookahead's predictions miss some experts
         from rvq_compressed_expert_gb300 import synth as _s
-        zw = _s.Workload("stack-zipf", 7168, 1536, 64, 16, 1, "f32", "zipf", n_layers=16, lookahead=6)
+        zw = _s.Workload("stack-zipf", 7168, 1536, 64, 16, 1, "f32", "zipf", n_layers=16, lookahead=6, zipf_s=0.3)
         run_stack(args, dev, res, zw, "stack_zipf")
     if rank == 0 and not args.no_tiered:
         run_tiered(args, dev, res)
