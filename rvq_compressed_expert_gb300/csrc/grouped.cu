@@ -244,24 +244,29 @@ constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kProdWarp = kDecWarps, kIssueWarp = kDecWarps + 1;
 constexpr int kMmaThreads = kDecThreads + 64;
 constexpr int kBRing = 4;             // activation tile stages
+constexpr int kARing = 4;             // weight tile stages (in tensor memory)
 constexpr uint32_t kCopies = 8;       // codebook copies: lane j of a quarter-warp reads copy j
 constexpr uint32_t kCbBytes = kStages * kCodes * kCopies * 16;  // 96 KiB of fp16 rows
-constexpr uint32_t kABytes = kBM * kBK * 2;                     // 16 KiB
 constexpr uint32_t kBBytes = kGroupTokens * kBK * 2;           // 16 KiB
-constexpr uint32_t kSegBytes = 8 * kStages * 512;              // 8 row groups x 3 stages x 32 vectors
+constexpr uint32_t kGroupBytes = kStages * 512;                // one row group of a segment
+constexpr uint32_t kGroupStride = kGroupBytes + 16;            // padded in shared memory
+constexpr uint32_t kSegBytes = 8 * kGroupStride;               // 8 row groups x 3 stages x 32 vectors
 constexpr uint32_t kOffCb = 0;
-constexpr uint32_t kOffA = kOffCb + kCbBytes;
-constexpr uint32_t kOffB = kOffA + 2 * kABytes;
+constexpr uint32_t kOffB = kOffCb + kCbBytes;
 constexpr uint32_t kOffSeg = kOffB + kBRing * kBBytes;
 constexpr uint32_t kOffSlot = kOffSeg + 2 * kSegBytes;
-constexpr uint32_t kOffBar = kOffSlot + kGroupTokens * 4;
+constexpr uint32_t kOffBar = (kOffSlot + kGroupTokens * 4 + 7) & ~7u;
 // barrier indices
-enum { kSegFull = 0, kSegEmpty = 2, kBFull = 4, kBEmpty = 8, kAFull = 12, kAEmpty = 14, kAccFull = 16,
-       kAccEmpty = 17, kNumBars = 18 };
+enum { kSegFull = 0, kSegEmpty = 2, kBFull = 4, kBEmpty = kBFull + kBRing, kAFull = kBEmpty + kBRing,
+       kAEmpty = kAFull + kARing, kAccFull = kAEmpty + kARing, kAccEmpty = kAccFull + 1, kNumBars = kAccEmpty + 1 };
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kMmaSmem = kOffMisc + 16;
-constexpr uint32_t kTmemCols = 2 * kGroupTokens; // gate and up accumulators
+// tensor memory: [0, 256) the gate and up accumulators (128 columns each), [256, 384) the
+// weight tiles (kARing x 32 columns: 128 rows x 64 fp16 weights each)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemA = 2 * kGroupTokens;
 static_assert(kMmaSmem <= 227 * 1024, "shared memory of the tensor-core kernel");
+static_assert(kTmemA + kARing * (kBK / 2) <= kTmemCols, "tensor memory of the tensor-core kernel");
 
 struct MmaArgs {
     const uint8_t *records;
@@ -323,7 +328,25 @@ __device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity, v
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// The items of this CTA: a contiguous range of the (chunk, 128-row block) items, so that
+// consecutive items mostly share their expert and its codebooks stay in shared memory.
+__device__ __forceinline__ void cta_items(int n_items, int &i0, int &i1) {
+    const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
+    i0 = min(n_items, (int)blockIdx.x * per);
+    i1 = min(n_items, i0 + per);
+}
+
+// Matrix of pass `pass` of the CTA's it-th item: down has one pass; gate/up alternate their
+// order from item to item, so the last pass's codebooks serve the next item's first pass.
+template <bool kDown>
+__device__ __forceinline__ int pass_mat(int it, int pass) {
+    if constexpr (kDown) return 2;
+    return (pass ^ (it & 1));
+}
+
 // One item = (chunk of <= 128 tokens of one expert, 128-row block of the output).
+// Weights are decoded from their codes into tensor memory (the MMA's A operand); the
+// activation tiles come from shared memory (B operand).
 template <bool kDown>
 __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
     extern __shared__ __align__(1024) unsigned char gsm[];
@@ -336,12 +359,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(bar(kSegFull + i), 1);
             tc::mbar_init(bar(kSegEmpty + i), kDecWarps);
-            tc::mbar_init(bar(kAFull + i), kDecWarps);
-            tc::mbar_init(bar(kAEmpty + i), 1);
         }
         for (int i = 0; i < kBRing; ++i) {
             tc::mbar_init(bar(kBFull + i), 1);
             tc::mbar_init(bar(kBEmpty + i), 1);
+        }
+        for (int i = 0; i < kARing; ++i) {
+            tc::mbar_init(bar(kAFull + i), kDecWarps);
+            tc::mbar_init(bar(kAEmpty + i), 1);
         }
         tc::mbar_init(bar(kAccFull), 1);
         tc::mbar_init(bar(kAccEmpty), kDecWarps);
@@ -358,13 +383,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
     const int nmb = (G.n_out + kBM - 1) / kBM;
     const int KC = (G.n_in + kBK - 1) / kBK;
     const int n_items = A.counts[0] * nmb;
+    int i0, i1;
+    cta_items(n_items, i0, i1);
     constexpr int kPasses = kDown ? 1 : 2;
 
     if (warp == kProdWarp) {
-        // ---------------- producer: codes per segment, activation tile per K chunk (the
-        // whole warp walks the loop; lane 0 issues)
+        // ---------------- producer: codes per segment (one bulk copy per row group, into
+        // padded slots), activation tile per K chunk (the whole warp walks the loop; lane 0
+        // issues)
         uint32_t q = 0, gs = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        for (int item = i0; item < i1; ++item) {
             const int4 ch = A.chunks[item / nmb];
             const int mb = item % nmb, npad = pad16(ch.z);
             const uint32_t bbytes = (uint32_t)npad * 128;
@@ -376,16 +404,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                 if (lane == 0) atomicOr(A.err, kErrNotResident);
                 rec = A.records;
             }
-            const uint32_t seg_bytes = (uint32_t)min(8, G.groups - 8 * mb) * (kStages * 512);
+            const int n_groups = min(8, G.groups - 8 * mb);
             for (int pass = 0; pass < kPasses; ++pass) {
-                const uint8_t *sec = rec + A.sec[kDown ? 2 : pass];
+                const uint8_t *sec = rec + A.sec[pass_mat<kDown>(item - i0, pass)];
                 for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
                     const int sb = gs & 1;
                     bool ok = gs < 2 || wait_phase_warp(bar(kSegEmpty + sb), ((gs - 2) >> 1) & 1, abort_flag);
                     if (ok && lane == 0 && !*abort_flag) {
-                        const uint8_t *src = sec + ((size_t)(kc0 / kKcSeg) * G.groups + 8 * mb) * (kStages * 512);
-                        tc::mbar_arrive_expect_tx(bar(kSegFull + sb), seg_bytes);
-                        tc::bulk_g2s(sbase + kOffSeg + sb * kSegBytes, src, seg_bytes, bar(kSegFull + sb));
+                        const uint8_t *src = sec + ((size_t)(kc0 / kKcSeg) * G.groups + 8 * mb) * kGroupBytes;
+                        tc::mbar_arrive_expect_tx(bar(kSegFull + sb), (uint32_t)n_groups * kGroupBytes);
+                        for (int g = 0; g < n_groups; ++g)
+                            tc::bulk_g2s(sbase + kOffSeg + sb * kSegBytes + g * kGroupStride, src + g * kGroupBytes,
+                                         kGroupBytes, bar(kSegFull + sb));
                     }
                     __syncwarp();
                     for (int kc = kc0; kc < min(KC, kc0 + kKcSeg); ++kc, ++q) {
@@ -414,25 +444,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
     } else if (warp == kIssueWarp) {
         // ---------------- MMA issue (the whole warp walks the loop; lane 0 issues)
         uint32_t q = 0, it = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+        for (int item = i0; item < i1; ++item, ++it) {
             const int4 ch = A.chunks[item / nmb];
             const int npad = pad16(ch.z);
             const uint32_t idesc = tc::idesc_f16_f32(kBM, npad);
             if (it >= 1) wait_phase_warp(bar(kAccEmpty), (it - 1) & 1, abort_flag);
             tc::fence_after_sync();
             for (int pass = 0; pass < kPasses; ++pass) {
+                const uint32_t acc = tmem + (uint32_t)(kDown ? 0 : pass_mat<kDown>(it, pass)) * kGroupTokens;
                 for (int kc = 0; kc < KC; ++kc, ++q) {
-                    const int ab = q & 1, rs = q % kBRing;
-                    wait_phase_warp(bar(kAFull + ab), (q >> 1) & 1, abort_flag);
+                    const int ab = q % kARing, rs = q % kBRing;
+                    wait_phase_warp(bar(kAFull + ab), (q / kARing) & 1, abort_flag);
                     wait_phase_warp(bar(kBFull + rs), (q / kBRing) & 1, abort_flag);
                     tc::fence_after_sync();
                     if (lane == 0) {
-                        const uint32_t a_addr = sbase + kOffA + ab * kABytes;
+                        const uint32_t a_tm = tmem + kTmemA + (uint32_t)ab * (kBK / 2);
                         const uint32_t b_addr = sbase + kOffB + rs * kBBytes;
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
-                            tc::mma_f16(tmem + pass * kGroupTokens, tc::smem_desc(a_addr + kk * 256, 128, 1024),
-                                        tc::smem_desc(b_addr + kk * 256, 128, 1024), idesc, (kc | kk) != 0);
+                            tc::mma_f16_ta(acc, a_tm + kk * 8, tc::smem_desc(b_addr + kk * 256, 128, 1024), idesc,
+                                           (kc | kk) != 0);
                         tc::mma_commit(bar(kAEmpty + ab));
                         tc::mma_commit(bar(kBEmpty + rs));
                     }
@@ -455,64 +486,78 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
         // drain: every MMA issued has completed before TMEM is released
         if (it >= 1) wait_phase_warp(bar(kAccFull), (it - 1) & 1, abort_flag, false);
     } else {
-        // ---------------- decode warps (and the epilogue)
-        // role in a chunk: vector column jj, row group gq, code bytes 2 qh, 2 qh + 1
-        const int jj = lane & 7, gq = warp & 7, qh = (warp >> 3) * 4 + (lane >> 3);
+        // ---------------- decode warps (and the epilogue).  Warp w writes the weight rows of
+        // TMEM lane quarter w % 4 (rows 32 (w % 4) + lane of the block) for the K slice w / 4
+        // of each 64-wide chunk: vectors 2 (w / 4) and 2 (w / 4) + 1 of the chunk's 8.
+        const int lq = warp & 3, wg = warp >> 2;
+        const int rl = lq * 32 + lane;                  // row of the 128-row block
+        const int rr = rl & 15, gl = rl >> 4;           // row in its group, group in the block
         const uint4 *cbs = reinterpret_cast<const uint4 *>(gsm + kOffCb);
+        const uint32_t copy = (uint32_t)(lane & 7);
+        const uint32_t a_lane = (uint32_t)(lq * 32) << 16;
+        int loaded = -1; // (expert * 3 + matrix) whose codebooks are in shared memory
         uint32_t q = 0, gs = 0, it = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+        for (int item = i0; item < i1; ++item, ++it) {
             const int4 ch = A.chunks[item / nmb];
             const int e = ch.x, nt = ch.z, npad = pad16(nt);
             const int mb = item % nmb;
+            const int row = mb * kBM + rl;
+            const bool row_ok = row < G.n_out;
             for (int pass = 0; pass < kPasses; ++pass) {
-                const int mat = kDown ? 2 : pass;
-                dec_barrier(); // every decode warp is past the previous pass (and epilogue)
-                if (pass == 0 && tid < kGroupTokens) s_slot[tid] = tid < nt ? A.sorted[ch.y + tid] : 0;
-                {
-                    const float *cb = A.codebooks + ((size_t)e * 3 + mat) * (kStages * kCodes * kVec);
-                    uint4 *dst = reinterpret_cast<uint4 *>(gsm + kOffCb);
-                    for (int r = tid; r < kStages * kCodes; r += kDecThreads) {
-                        const float4 lo = __ldg(reinterpret_cast<const float4 *>(cb) + 2 * r);
-                        const float4 hi = __ldg(reinterpret_cast<const float4 *>(cb) + 2 * r + 1);
-                        const uint4 hv = make_uint4(half2_bits(lo.x, lo.y), half2_bits(lo.z, lo.w),
-                                                    half2_bits(hi.x, hi.y), half2_bits(hi.z, hi.w));
+                const int mat = pass_mat<kDown>(it, pass);
+                const int key = e * 3 + mat;
+                // the same for every decode thread: the down epilogue's slot list changes with
+                // the item, the codebooks with the (expert, matrix)
+                const bool new_slots = kDown && pass == 0, reload = key != loaded;
+                if (new_slots || reload) {
+                    dec_barrier(); // every decode warp is past the previous pass (and epilogue)
+                    if (new_slots && tid < kGroupTokens) s_slot[tid] = tid < nt ? A.sorted[ch.y + tid] : 0;
+                    if (reload) {
+                        // codebook rows as fp16, 8 copies each; a thread writes its row's copies
+                        // starting at its own, so a quarter-warp's stores hit 8 bank quads
+                        const float *cb = A.codebooks + (size_t)key * (kStages * kCodes * kVec);
+                        uint4 *dst = reinterpret_cast<uint4 *>(gsm + kOffCb);
+                        for (int r = tid; r < kStages * kCodes; r += kDecThreads) {
+                            const float4 lo = __ldg(reinterpret_cast<const float4 *>(cb) + 2 * r);
+                            const float4 hi = __ldg(reinterpret_cast<const float4 *>(cb) + 2 * r + 1);
+                            const uint4 hv = make_uint4(half2_bits(lo.x, lo.y), half2_bits(lo.z, lo.w),
+                                                        half2_bits(hi.x, hi.y), half2_bits(hi.z, hi.w));
 #pragma unroll
-                        for (uint32_t c = 0; c < kCopies; ++c) dst[r * kCopies + c] = hv;
+                            for (uint32_t c = 0; c < kCopies; ++c) dst[r * kCopies + ((c + r) & (kCopies - 1))] = hv;
+                        }
+                        loaded = key;
                     }
+                    dec_barrier(); // codebook rows and slots in place
                 }
-                dec_barrier(); // codebook rows and slots in place
                 for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
                     const int sb = gs & 1;
                     wait_phase(bar(kSegFull + sb), (gs >> 1) & 1, abort_flag);
-                    const unsigned char *seg = gsm + kOffSeg + sb * kSegBytes;
+                    const unsigned char *seg = gsm + kOffSeg + sb * kSegBytes + gl * kGroupStride;
                     for (int kc = kc0; kc < min(KC, kc0 + kKcSeg); ++kc, ++q) {
-                        const int ab = q & 1;
-                        if (q >= 2) wait_phase(bar(kAEmpty + ab), ((q - 2) >> 1) & 1, abort_flag);
-                        const int sub = kc - kc0;
-                        const unsigned char *ct = seg + ((gq * kStages) * 32 + 8 * sub + jj) * 16 + 2 * qh;
-                        const uint32_t c0 = *reinterpret_cast<const uint16_t *>(ct);
-                        const uint32_t c1 = *reinterpret_cast<const uint16_t *>(ct + 512);
-                        const uint32_t c2 = *reinterpret_cast<const uint16_t *>(ct + 1024);
-                        const int j = kc * 8 + jj, j32 = j & 31;
-                        const bool jok = j < G.nv;
-                        unsigned char *abuf = gsm + kOffA + ab * kABytes;
-#pragma unroll
-                        for (int b = 0; b < 2; ++b) {
-                            const int qq = 2 * qh + b;
-                            const int rl = 16 * gq + ((j32 ^ qq) & 15);
-                            const int row = mb * kBM + rl;
-                            const uint4 v0 = cbs[(0 * kCodes + ((c0 >> (8 * b)) & 255)) * kCopies + jj];
-                            const uint4 v1 = cbs[(1 * kCodes + ((c1 >> (8 * b)) & 255)) * kCopies + jj];
-                            const uint4 v2 = cbs[(2 * kCodes + ((c2 >> (8 * b)) & 255)) * kCopies + jj];
-                            uint4 w;
-                            w.x = hadd2_bits(hadd2_bits(v0.x, v1.x), v2.x);
-                            w.y = hadd2_bits(hadd2_bits(v0.y, v1.y), v2.y);
-                            w.z = hadd2_bits(hadd2_bits(v0.z, v1.z), v2.z);
-                            w.w = hadd2_bits(hadd2_bits(v0.w, v1.w), v2.w);
-                            if (!jok || row >= G.n_out) w = make_uint4(0, 0, 0, 0);
-                            *reinterpret_cast<uint4 *>(abuf + (rl >> 3) * 1024 + jj * 128 + (rl & 7) * 16) = w;
+                        const int ab = q % kARing;
+                        if (q >= kARing) {
+                            wait_phase(bar(kAEmpty + ab), ((q - kARing) / kARing) & 1, abort_flag);
+                            tc::fence_after_sync(); // the MMAs that read this stage are complete
                         }
-                        tc::fence_proxy_async();
+                        uint32_t w[8];
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            const int jj = 8 * (kc - kc0) + 2 * wg + v; // vector within the segment
+                            const int j = kc * 8 + 2 * wg + v;          // vector within the row
+                            const unsigned char *cp = seg + jj * 16 + ((rr ^ jj) & 15);
+                            const uint32_t c0 = cp[0], c1 = cp[512], c2 = cp[1024];
+                            const uint4 v0 = cbs[(0 * kCodes + c0) * kCopies + copy];
+                            const uint4 v1 = cbs[(1 * kCodes + c1) * kCopies + copy];
+                            const uint4 v2 = cbs[(2 * kCodes + c2) * kCopies + copy];
+                            const bool ok = row_ok && j < G.nv;
+                            w[4 * v + 0] = ok ? hadd2_bits(hadd2_bits(v0.x, v1.x), v2.x) : 0u;
+                            w[4 * v + 1] = ok ? hadd2_bits(hadd2_bits(v0.y, v1.y), v2.y) : 0u;
+                            w[4 * v + 2] = ok ? hadd2_bits(hadd2_bits(v0.z, v1.z), v2.z) : 0u;
+                            w[4 * v + 3] = ok ? hadd2_bits(hadd2_bits(v0.w, v1.w), v2.w) : 0u;
+                        }
+                        tc::tmem_st8(tmem + a_lane + kTmemA + (uint32_t)ab * (kBK / 2) + (uint32_t)wg * 8, w);
+                        tc::tmem_wait_st();
+                        tc::fence_before_sync();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(bar(kAFull + ab));
                     }
@@ -525,18 +570,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             wait_phase(bar(kAccFull), it & 1, abort_flag);
             tc::fence_after_sync();
             {
-                const int lq = warp & 3;
-                const int rl = lq * 32 + lane, row = mb * kBM + rl;
-                const uint32_t lane_addr = tmem + ((uint32_t)(lq * 32) << 16);
+                const uint32_t lane_addr = tmem + a_lane;
                 const int kcf = (A.f + kBK - 1) / kBK;
                 uint8_t *ag = A.ag + (size_t)ch.w * kcf * 128;
-                for (int c0 = (warp >> 2) * 16; c0 < npad; c0 += 64) {
+                for (int c0 = wg * 16; c0 < npad; c0 += 64) {
                     float z[16];
                     tc::tmem_ld16(lane_addr + c0, z);
                     if constexpr (!kDown) {
                         float u[16];
                         tc::tmem_ld16(lane_addr + kGroupTokens + c0, u);
-                        if (row < G.n_out) {
+                        if (row_ok) {
 #pragma unroll
                             for (int n = 0; n < 16; ++n)
                                 if (c0 + n < nt) {
@@ -547,7 +590,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                                 }
                         }
                     } else {
-                        if (row < G.n_out) {
+                        if (row_ok) {
 #pragma unroll
                             for (int n = 0; n < 16; ++n)
                                 if (c0 + n < nt) A.part_dn[(size_t)s_slot[c0 + n] * A.nparts * A.d + row] = z[n];
