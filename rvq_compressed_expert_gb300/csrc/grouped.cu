@@ -244,7 +244,8 @@ constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kProdWarp = kDecWarps, kIssueWarp = kDecWarps + 1;
 constexpr int kMmaThreads = kDecThreads + 64;
 constexpr int kBRing = 4;             // activation tile stages
-constexpr int kARing = 4;             // weight tile stages (in tensor memory)
+constexpr int kARing = 8;             // weight tile stages (in tensor memory)
+constexpr int kSegRing = 4;           // code segment stages
 constexpr uint32_t kCopies = 8;       // codebook copies: lane j of a quarter-warp reads copy j
 constexpr uint32_t kCbBytes = kStages * kCodes * kCopies * 16;  // 96 KiB of fp16 rows
 constexpr uint32_t kBBytes = kGroupTokens * kBK * 2;           // 16 KiB
@@ -254,14 +255,14 @@ constexpr uint32_t kSegBytes = 8 * kGroupStride;               // 8 row groups x
 constexpr uint32_t kOffCb = 0;
 constexpr uint32_t kOffB = kOffCb + kCbBytes;
 constexpr uint32_t kOffSeg = kOffB + kBRing * kBBytes;
-constexpr uint32_t kOffSlot = kOffSeg + 2 * kSegBytes;
+constexpr uint32_t kOffSlot = kOffSeg + kSegRing * kSegBytes;
 constexpr uint32_t kOffBar = (kOffSlot + kGroupTokens * 4 + 7) & ~7u;
 // barrier indices
-enum { kSegFull = 0, kSegEmpty = 2, kBFull = 4, kBEmpty = kBFull + kBRing, kAFull = kBEmpty + kBRing,
+enum { kSegFull = 0, kSegEmpty = kSegRing, kBFull = 2 * kSegRing, kBEmpty = kBFull + kBRing, kAFull = kBEmpty + kBRing,
        kAEmpty = kAFull + kARing, kAccFull = kAEmpty + kARing, kAccEmpty = kAccFull + 1, kNumBars = kAccEmpty + 1 };
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kMmaSmem = kOffMisc + 16;
-// tensor memory: [0, 256) the gate and up accumulators (128 columns each), [256, 384) the
+// tensor memory: [0, 256) the gate and up accumulators (128 columns each), [256, 512) the
 // weight tiles (kARing x 32 columns: 128 rows x 64 fp16 weights each)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemA = 2 * kGroupTokens;
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gsm + kOffMisc + 4);
     auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSegRing; ++i) {
             tc::mbar_init(bar(kSegFull + i), 1);
             tc::mbar_init(bar(kSegEmpty + i), kDecWarps);
         }
@@ -390,8 +391,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
     if (warp == kProdWarp) {
         // ---------------- producer: codes per segment (one bulk copy per row group, into
         // padded slots), activation tile per K chunk (the whole warp walks the loop; lane 0
-        // issues)
+        // issues).  At the start of each (item, pass) the codes of the next one are asked of
+        // L2, so the segment copies find them there.
         uint32_t q = 0, gs = 0;
+        auto l2_ahead = [&](int item, int pass) {
+            if (item >= i1) return;
+            const int4 c = A.chunks[item / nmb];
+            const uint8_t *r = expert_record(A.records, A.stride, A.slot_map, c.x);
+            if (!r) return;
+            const int mb = item % nmb;
+            const uint32_t bytes = (uint32_t)min(8, G.groups - 8 * mb) * kGroupBytes;
+            const uint8_t *sec = r + A.sec[pass_mat<kDown>(item - i0, pass)];
+            for (int sg = lane; sg < G.nseg; sg += 32) {
+                const uint8_t *src = sec + ((size_t)sg * G.groups + 8 * mb) * kGroupBytes;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+            }
+        };
+        l2_ahead(i0, 0);
         for (int item = i0; item < i1; ++item) {
             const int4 ch = A.chunks[item / nmb];
             const int mb = item % nmb, npad = pad16(ch.z);
@@ -406,10 +422,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             }
             const int n_groups = min(8, G.groups - 8 * mb);
             for (int pass = 0; pass < kPasses; ++pass) {
+                if (pass + 1 < kPasses) l2_ahead(item, pass + 1);
+                else l2_ahead(item + 1, 0);
                 const uint8_t *sec = rec + A.sec[pass_mat<kDown>(item - i0, pass)];
                 for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
-                    const int sb = gs & 1;
-                    bool ok = gs < 2 || wait_phase_warp(bar(kSegEmpty + sb), ((gs - 2) >> 1) & 1, abort_flag);
+                    const int sb = gs % kSegRing;
+                    bool ok = gs < kSegRing ||
+                              wait_phase_warp(bar(kSegEmpty + sb), ((gs - kSegRing) / kSegRing) & 1, abort_flag);
                     if (ok && lane == 0 && !*abort_flag) {
                         const uint8_t *src = sec + ((size_t)(kc0 / kKcSeg) * G.groups + 8 * mb) * kGroupBytes;
                         tc::mbar_arrive_expect_tx(bar(kSegFull + sb), (uint32_t)n_groups * kGroupBytes);
@@ -433,9 +452,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             }
         }
         // drain: the last copies into each buffer have landed before the CTA exits
-        for (uint32_t i = 0; i < 2 && i < gs; ++i) {
+        for (uint32_t i = 0; i < (uint32_t)kSegRing && i < gs; ++i) {
             const uint32_t g = gs - 1 - i;
-            wait_phase_warp(bar(kSegFull + (g & 1)), (g >> 1) & 1, abort_flag, false);
+            wait_phase_warp(bar(kSegFull + g % kSegRing), (g / kSegRing) & 1, abort_flag, false);
         }
         for (uint32_t i = 0; i < (uint32_t)kBRing && i < q; ++i) {
             const uint32_t g = q - 1 - i;
@@ -530,8 +549,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                     dec_barrier(); // codebook rows and slots in place
                 }
                 for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
-                    const int sb = gs & 1;
-                    wait_phase(bar(kSegFull + sb), (gs >> 1) & 1, abort_flag);
+                    const int sb = gs % kSegRing;
+                    wait_phase(bar(kSegFull + sb), (gs / kSegRing) & 1, abort_flag);
                     const unsigned char *seg = gsm + kOffSeg + sb * kSegBytes + gl * kGroupStride;
                     for (int kc = kc0; kc < min(KC, kc0 + kKcSeg); ++kc, ++q) {
                         const int ab = q % kARing;
