@@ -548,6 +548,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                     }
                     dec_barrier(); // codebook rows and slots in place
                 }
+                // a stage's tensor-memory stores are waited for one chunk later, so the decode of
+                // the next chunk runs under them; `pend` is the stage still to be handed over
+                int pend = -1;
                 for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
                     const int sb = gs % kSegRing;
                     wait_phase(bar(kSegFull + sb), (gs / kSegRing) & 1, abort_flag);
@@ -575,13 +578,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                             w[4 * v + 3] = ok ? hadd2_bits(hadd2_bits(v0.w, v1.w), v2.w) : 0u;
                         }
                         tc::tmem_st8(tmem + a_lane + kTmemA + (uint32_t)ab * (kBK / 2) + (uint32_t)wg * 8, w);
-                        tc::tmem_wait_st();
-                        tc::fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(bar(kAFull + ab));
+                        if (pend >= 0) {
+                            tc::tmem_wait_st(); // both stages' stores are complete
+                            tc::fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tc::mbar_arrive(bar(kAFull + pend));
+                                tc::mbar_arrive(bar(kAFull + ab));
+                            }
+                            pend = -1;
+                        } else {
+                            pend = ab;
+                        }
                     }
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(bar(kSegEmpty + sb));
+                    if (lane == 0) tc::mbar_arrive(bar(kSegEmpty + sb)); // its codes are read
+                }
+                if (pend >= 0) {
+                    tc::tmem_wait_st();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(bar(kAFull + pend));
                 }
             }
             // epilogue: warp w reads TMEM lanes 32 (w % 4) .. +32 (its output rows) and the
