@@ -300,6 +300,17 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Explicit shared-memory loads at 32-bit shared-window addresses (never generic accesses).
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
 __device__ __forceinline__ void dec_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kDecThreads) : "memory"); }
 
 // Wait for the phase of the given parity.  Gives up after a second (then raises the
@@ -511,8 +522,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
         const int lq = warp & 3, wg = warp >> 2;
         const int rl = lq * 32 + lane;                  // row of the 128-row block
         const int rr = rl & 15, gl = rl >> 4;           // row in its group, group in the block
-        const uint4 *cbs = reinterpret_cast<const uint4 *>(gsm + kOffCb);
-        const uint32_t copy = (uint32_t)(lane & 7);
+        // shared-window address of this lane's codebook copy (stage 0, code 0)
+        const uint32_t cb_lane = sbase + kOffCb + (uint32_t)(lane & 7) * 16;
         const uint32_t a_lane = (uint32_t)(lq * 32) << 16;
         int loaded = -1; // (expert * 3 + matrix) whose codebooks are in shared memory
         uint32_t q = 0, gs = 0, it = 0;
@@ -554,24 +565,36 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                 for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
                     const int sb = gs % kSegRing;
                     wait_phase(bar(kSegFull + sb), (gs / kSegRing) & 1, abort_flag);
-                    const unsigned char *seg = gsm + kOffSeg + sb * kSegBytes + gl * kGroupStride;
+                    const uint32_t seg = sbase + kOffSeg + (uint32_t)sb * kSegBytes + (uint32_t)gl * kGroupStride;
                     for (int kc = kc0; kc < min(KC, kc0 + kKcSeg); ++kc, ++q) {
                         const int ab = q % kARing;
                         if (q >= kARing) {
                             wait_phase(bar(kAEmpty + ab), ((q - kARing) / kARing) & 1, abort_flag);
                             tc::fence_after_sync(); // the MMAs that read this stage are complete
                         }
-                        uint32_t w[8];
+                        // both vectors' codes first, then their codebook rows (the loads are
+                        // volatile: issued in this order, all in flight before their uses)
+                        uint32_t c[2][3];
 #pragma unroll
                         for (int v = 0; v < 2; ++v) {
                             const int jj = 8 * (kc - kc0) + 2 * wg + v; // vector within the segment
-                            const int j = kc * 8 + 2 * wg + v;          // vector within the row
-                            const unsigned char *cp = seg + jj * 16 + ((rr ^ jj) & 15);
-                            const uint32_t c0 = cp[0], c1 = cp[512], c2 = cp[1024];
-                            const uint4 v0 = cbs[(0 * kCodes + c0) * kCopies + copy];
-                            const uint4 v1 = cbs[(1 * kCodes + c1) * kCopies + copy];
-                            const uint4 v2 = cbs[(2 * kCodes + c2) * kCopies + copy];
+                            const uint32_t cp = seg + (uint32_t)(jj * 16 + ((rr ^ jj) & 15));
+                            c[v][0] = lds_u8(cp);
+                            c[v][1] = lds_u8(cp + 512);
+                            c[v][2] = lds_u8(cp + 1024);
+                        }
+                        uint4 cv[2][3];
+#pragma unroll
+                        for (int v = 0; v < 2; ++v)
+#pragma unroll
+                            for (int st = 0; st < kStages; ++st)
+                                cv[v][st] = lds_v4(cb_lane + ((uint32_t)st * kCodes + c[v][st]) * (kCopies * 16));
+                        uint32_t w[8];
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            const int j = kc * 8 + 2 * wg + v; // vector within the row
                             const bool ok = row_ok && j < G.nv;
+                            const uint4 &v0 = cv[v][0], &v1 = cv[v][1], &v2 = cv[v][2];
                             w[4 * v + 0] = ok ? hadd2_bits(hadd2_bits(v0.x, v1.x), v2.x) : 0u;
                             w[4 * v + 1] = ok ? hadd2_bits(hadd2_bits(v0.y, v1.y), v2.y) : 0u;
                             w[4 * v + 2] = ok ? hadd2_bits(hadd2_bits(v0.z, v1.z), v2.z) : 0u;
