@@ -6,7 +6,7 @@
 // prédiction du routeur": one layer of a prefill chunk spans about 550 expert slots, so
 // one expert's weights serve many tokens at once.  The weights stay in their 3-stage
 // RVQ codes (section "Quantification et exactitude"); here 128-row tiles of codes are
-// decoded into shared memory (the sum of three 256-entry codebook rows per 8-weight
+// decoded into tensor memory (the sum of three 256-entry codebook rows per 8-weight
 // vector) and fed to tcgen05 MMAs with the expert's tokens as the N side.
 //
 // Kernels, in launch order:
@@ -23,11 +23,13 @@
 // The lookup kernels serve the listed slots in between, and the combine sums the k
 // slots of each token in rank order (one partial for tensor-core slots).
 //
-// mma_kernel is warp-specialised: a producer warp moves, with one bulk copy each, the
-// codes of a 32-vector segment of the row block (12 KiB) and the activation tile of each
-// 64-wide K chunk; 16 decode warps turn codes into fp16 weight tiles; one thread issues
-// the MMAs.  Full/empty mbarriers hand the buffers between them, so decoding, copies
-// and MMAs of different chunks overlap.
+// mma_kernel is warp-specialised: one producer warp moves the codes of each 32-vector
+// segment of the row block (12 KiB, a bulk copy per row group), another the activation tile
+// of each 64-wide K chunk; 16 decode warps turn codes into fp16 weights and store them into
+// tensor memory (tcgen05.st), where the MMA reads its A operand; one thread issues the MMAs.
+// Full/empty mbarriers hand the buffers between them, so decoding, copies and MMAs of
+// different chunks overlap.  A CTA takes a contiguous range of items, so an expert's
+// codebooks stay in shared memory across its row blocks.
 //
 // Numerics: codebook rows are rounded to fp16 and summed in fp16 (stage order 0, 1, 2),
 // the activations enter as fp16, products accumulate in fp32.  The error is that of
@@ -241,8 +243,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const void *__restrict__ h,
 
 constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kProdWarp = kDecWarps, kIssueWarp = kDecWarps + 1;
-constexpr int kMmaThreads = kDecThreads + 64;
+// producers: one warp for the code segments, one for the activation tiles, so neither ring's
+// progress holds the other's copies back
+constexpr int kProdWarp = kDecWarps, kIssueWarp = kDecWarps + 1, kProdBWarp = kDecWarps + 2;
+constexpr int kMmaThreads = kDecThreads + 96;
 constexpr int kBRing = 4;             // activation tile stages
 constexpr int kARing = 8;             // weight tile stages (in tensor memory)
 constexpr int kSegRing = 4;           // code segment stages
@@ -400,11 +404,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
     constexpr int kPasses = kDown ? 1 : 2;
 
     if (warp == kProdWarp) {
-        // ---------------- producer: codes per segment (one bulk copy per row group, into
-        // padded slots), activation tile per K chunk (the whole warp walks the loop; lane 0
-        // issues).  At the start of each (item, pass) the codes of the next one are asked of
-        // L2, so the segment copies find them there.
-        uint32_t q = 0, gs = 0;
+        // ---------------- code producer: the codes of each 32-vector segment of the row
+        // block, one bulk copy per row group into padded slots (the whole warp walks the loop;
+        // lane 0 issues).  At the start of each (item, pass) the codes of the next one are
+        // asked of L2, so the segment copies find them there.
+        uint32_t gs = 0;
         auto l2_ahead = [&](int item, int pass) {
             if (item >= i1) return;
             const int4 c = A.chunks[item / nmb];
@@ -421,9 +425,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
         l2_ahead(i0, 0);
         for (int item = i0; item < i1; ++item) {
             const int4 ch = A.chunks[item / nmb];
-            const int mb = item % nmb, npad = pad16(ch.z);
-            const uint32_t bbytes = (uint32_t)npad * 128;
-            const uint8_t *bsrc = A.bsrc + (size_t)ch.w * KC * 128;
+            const int mb = item % nmb;
             const uint8_t *rec = expert_record(A.records, A.stride, A.slot_map, ch.x);
             if (!rec) {
                 // not resident (a bank fetch did not place it): no copies, the row block
@@ -438,8 +440,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                 const uint8_t *sec = rec + A.sec[pass_mat<kDown>(item - i0, pass)];
                 for (int kc0 = 0; kc0 < KC; kc0 += kKcSeg, ++gs) {
                     const int sb = gs % kSegRing;
-                    bool ok = gs < kSegRing ||
-                              wait_phase_warp(bar(kSegEmpty + sb), ((gs - kSegRing) / kSegRing) & 1, abort_flag);
+                    const bool ok = gs < kSegRing ||
+                                    wait_phase_warp(bar(kSegEmpty + sb), ((gs - kSegRing) / kSegRing) & 1, abort_flag);
                     if (ok && lane == 0 && !*abort_flag) {
                         const uint8_t *src = sec + ((size_t)(kc0 / kKcSeg) * G.groups + 8 * mb) * kGroupBytes;
                         tc::mbar_arrive_expect_tx(bar(kSegFull + sb), (uint32_t)n_groups * kGroupBytes);
@@ -448,17 +450,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                                          kGroupBytes, bar(kSegFull + sb));
                     }
                     __syncwarp();
-                    for (int kc = kc0; kc < min(KC, kc0 + kKcSeg); ++kc, ++q) {
-                        const int rs = q % kBRing;
-                        ok = q < kBRing ||
-                             wait_phase_warp(bar(kBEmpty + rs), ((q - kBRing) / kBRing) & 1, abort_flag);
-                        if (ok && lane == 0 && !*abort_flag) {
-                            tc::mbar_arrive_expect_tx(bar(kBFull + rs), bbytes);
-                            tc::bulk_g2s(sbase + kOffB + rs * kBBytes, bsrc + (size_t)kc * bbytes, bbytes,
-                                         bar(kBFull + rs));
-                        }
-                        __syncwarp();
-                    }
                 }
             }
         }
@@ -466,6 +457,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
         for (uint32_t i = 0; i < (uint32_t)kSegRing && i < gs; ++i) {
             const uint32_t g = gs - 1 - i;
             wait_phase_warp(bar(kSegFull + g % kSegRing), (g / kSegRing) & 1, abort_flag, false);
+        }
+    } else if (warp == kProdBWarp) {
+        // ---------------- activation producer: the tile of each 64-wide K chunk
+        uint32_t q = 0;
+        for (int item = i0; item < i1; ++item) {
+            const int4 ch = A.chunks[item / nmb];
+            const uint32_t bbytes = (uint32_t)pad16(ch.z) * 128;
+            const uint8_t *bsrc = A.bsrc + (size_t)ch.w * KC * 128;
+            for (int pass = 0; pass < kPasses; ++pass) {
+                for (int kc = 0; kc < KC; ++kc, ++q) {
+                    const int rs = q % kBRing;
+                    const bool ok = q < kBRing ||
+                                    wait_phase_warp(bar(kBEmpty + rs), ((q - kBRing) / kBRing) & 1, abort_flag);
+                    if (ok && lane == 0 && !*abort_flag) {
+                        tc::mbar_arrive_expect_tx(bar(kBFull + rs), bbytes);
+                        tc::bulk_g2s(sbase + kOffB + rs * kBBytes, bsrc + (size_t)kc * bbytes, bbytes, bar(kBFull + rs));
+                    }
+                    __syncwarp();
+                }
+            }
         }
         for (uint32_t i = 0; i < (uint32_t)kBRing && i < q; ++i) {
             const uint32_t g = q - 1 - i;
