@@ -247,13 +247,12 @@ constexpr int kDecThreads = kDecWarps * 32;
 // progress holds the other's copies back
 constexpr int kProdWarp = kDecWarps, kIssueWarp = kDecWarps + 1, kProdBWarp = kDecWarps + 2;
 constexpr int kMmaThreads = kDecThreads + 96;
-constexpr int kBRing = 8;             // activation half-tile stages (<= 64 tokens each)
-constexpr int kBHalf = 64;            // tokens per activation stage (an MMA's N at most)
+constexpr int kBRing = 4;             // activation tile stages
 constexpr int kARing = 8;             // weight tile stages (in tensor memory)
 constexpr int kSegRing = 4;           // code segment stages
 constexpr uint32_t kCopies = 8;       // codebook copies: lane j of a quarter-warp reads copy j
 constexpr uint32_t kCbBytes = kStages * kCodes * kCopies * 16;  // 96 KiB of fp16 rows
-constexpr uint32_t kBBytes = kBHalf * kBK * 2;                 // 8 KiB
+constexpr uint32_t kBBytes = kGroupTokens * kBK * 2;           // 16 KiB
 constexpr uint32_t kGroupBytes = kStages * 512;                // one row group of a segment
 constexpr uint32_t kGroupStride = kGroupBytes + 16;            // padded in shared memory
 constexpr uint32_t kSegBytes = 8 * kGroupStride;               // 8 row groups x 3 stages x 32 vectors
@@ -460,40 +459,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             wait_phase_warp(bar(kSegFull + g % kSegRing), (g / kSegRing) & 1, abort_flag, false);
         }
     } else if (warp == kProdBWarp) {
-        // ---------------- activation producer: the tile of each 64-wide K chunk; L2 is asked
-        // for the tile kBPrefetch chunks ahead (the tiles of a chunk are read once per row
-        // block, and the first read comes from DRAM)
-        constexpr int kBPrefetch = 12;
+        // ---------------- activation producer: the tile of each 64-wide K chunk
         uint32_t q = 0;
         for (int item = i0; item < i1; ++item) {
             const int4 ch = A.chunks[item / nmb];
             const uint32_t bbytes = (uint32_t)pad16(ch.z) * 128;
             const uint8_t *bsrc = A.bsrc + (size_t)ch.w * KC * 128;
-            const int nh = (pad16(ch.z) + kBHalf - 1) / kBHalf; // stages per chunk
             for (int pass = 0; pass < kPasses; ++pass) {
-                if (lane == 0)
-                    for (int kc = 0; kc < min(KC, kBPrefetch); ++kc)
-                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(bsrc + (size_t)kc * bbytes),
-                                     "r"(bbytes) : "memory");
-                for (int kc = 0; kc < KC; ++kc) {
-                    if (lane == 0 && kc + kBPrefetch < KC)
-                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                                         bsrc + (size_t)(kc + kBPrefetch) * bbytes),
-                                     "r"(bbytes) : "memory");
-                    // the tile of chunk kc in stages of up to 64 tokens: tokens 64 h .. of a
-                    // tile are its bytes from 8 KiB h on
-                    for (int hh = 0; hh < nh; ++hh, ++q) {
-                        const int rs = q % kBRing;
-                        const bool ok = q < kBRing ||
-                                        wait_phase_warp(bar(kBEmpty + rs), ((q - kBRing) / kBRing) & 1, abort_flag);
-                        if (ok && lane == 0 && !*abort_flag) {
-                            const uint32_t hb = min(kBBytes, bbytes - (uint32_t)hh * kBBytes);
-                            tc::mbar_arrive_expect_tx(bar(kBFull + rs), hb);
-                            tc::bulk_g2s(sbase + kOffB + rs * kBBytes, bsrc + (size_t)kc * bbytes + (size_t)hh * kBBytes,
-                                         hb, bar(kBFull + rs));
-                        }
-                        __syncwarp();
+                for (int kc = 0; kc < KC; ++kc, ++q) {
+                    const int rs = q % kBRing;
+                    const bool ok = q < kBRing ||
+                                    wait_phase_warp(bar(kBEmpty + rs), ((q - kBRing) / kBRing) & 1, abort_flag);
+                    if (ok && lane == 0 && !*abort_flag) {
+                        tc::mbar_arrive_expect_tx(bar(kBFull + rs), bbytes);
+                        tc::bulk_g2s(sbase + kOffB + rs * kBBytes, bsrc + (size_t)kc * bbytes, bbytes, bar(kBFull + rs));
                     }
+                    __syncwarp();
                 }
             }
         }
@@ -503,36 +484,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
         }
     } else if (warp == kIssueWarp) {
         // ---------------- MMA issue (the whole warp walks the loop; lane 0 issues)
-        uint32_t q = 0, qb = 0, it = 0;
+        uint32_t q = 0, it = 0;
         for (int item = i0; item < i1; ++item, ++it) {
             const int4 ch = A.chunks[item / nmb];
             const int npad = pad16(ch.z);
-            const int nh = (npad + kBHalf - 1) / kBHalf;
+            const uint32_t idesc = tc::idesc_f16_f32(kBM, npad);
             if (it >= 1) wait_phase_warp(bar(kAccEmpty), (it - 1) & 1, abort_flag);
             tc::fence_after_sync();
             for (int pass = 0; pass < kPasses; ++pass) {
                 const uint32_t acc = tmem + (uint32_t)(kDown ? 0 : pass_mat<kDown>(it, pass)) * kGroupTokens;
                 for (int kc = 0; kc < KC; ++kc, ++q) {
-                    const int ab = q % kARing;
+                    const int ab = q % kARing, rs = q % kBRing;
                     wait_phase_warp(bar(kAFull + ab), (q / kARing) & 1, abort_flag);
-                    const uint32_t a_tm = tmem + kTmemA + (uint32_t)ab * (kBK / 2);
-                    // one stage of up to 64 tokens at a time, each into its own columns
-                    for (int hh = 0; hh < nh; ++hh, ++qb) {
-                        const int rs = qb % kBRing;
-                        wait_phase_warp(bar(kBFull + rs), (qb / kBRing) & 1, abort_flag);
-                        tc::fence_after_sync();
-                        if (lane == 0) {
-                            const uint32_t idesc = tc::idesc_f16_f32(kBM, min(kBHalf, npad - hh * kBHalf));
-                            const uint32_t b_addr = sbase + kOffB + rs * kBBytes;
+                    wait_phase_warp(bar(kBFull + rs), (q / kBRing) & 1, abort_flag);
+                    tc::fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t a_tm = tmem + kTmemA + (uint32_t)ab * (kBK / 2);
+                        const uint32_t b_addr = sbase + kOffB + rs * kBBytes;
 #pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk)
-                                tc::mma_f16_ta(acc + (uint32_t)hh * kBHalf, a_tm + kk * 8,
-                                               tc::smem_desc(b_addr + kk * 256, 128, 1024), idesc, (kc | kk) != 0);
-                            tc::mma_commit(bar(kBEmpty + rs));
-                            if (hh == nh - 1) tc::mma_commit(bar(kAEmpty + ab));
-                        }
-                        __syncwarp();
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc::mma_f16_ta(acc, a_tm + kk * 8, tc::smem_desc(b_addr + kk * 256, 128, 1024), idesc,
+                                           (kc | kk) != 0);
+                        tc::mma_commit(bar(kAEmpty + ab));
+                        tc::mma_commit(bar(kBEmpty + rs));
                     }
+                    __syncwarp();
                 }
             }
             if (lane == 0) {
