@@ -327,32 +327,6 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     }
     if (!valid && threadIdx.x == 0) atomicOr(A.err, (U.e >= 0 && U.e < A.E) ? kErrNotResident : kErrBadExpert);
     const int t = U.slot / A.k;
-    // ---- the table build's codebook operand, loaded first so that its latency runs under
-    // the input-vector phase (for down units, the SwiGLU of the gate/up partials).  The warps
-    // form 2 teams of kNW / 2, one per part; a warp takes kMt 16-code tiles of every stage;
-    // lane (fg, ft) holds codebook rows c0 + fg and c0 + fg + 8 of each tile, inputs ft, ft + 4.
-    constexpr int kWpp = kNW / 2;                 // warps per part
-    constexpr int kMt = (kCodes / 16) / kWpp;     // 16-code tiles per warp and stage
-    static_assert((kCodes / 16) % kWpp == 0, "code tiles per warp");
-    const int mp = warp / kWpp, mq = warp % kWpp;
-    const int fg = lane >> 2, ft = lane & 3;
-    float av[kRecon ? 1 : kStages][kRecon ? 1 : kMt][4];
-    if constexpr (!kRecon) {
-        const float *p0, *p1;
-        unit_codebooks<kDown>(A, U, p0, p1);
-        const float *Cp = mp ? p1 : p0;
-#pragma unroll
-        for (int s = 0; s < kStages; ++s)
-#pragma unroll
-            for (int i = 0; i < kMt; ++i) {
-                const float *r0 = Cp + ((size_t)s * kCodes + (size_t)(mq * kMt + i) * 16 + fg) * kVec;
-                const float *r1 = r0 + 8 * kVec;
-                av[s][i][0] = __ldg(r0 + ft);
-                av[s][i][1] = __ldg(r1 + ft);
-                av[s][i][2] = __ldg(r0 + ft + 4);
-                av[s][i][3] = __ldg(r1 + ft + 4);
-            }
-    }
     // ---- input vectors of this lane's column(s)
     float xv[2][kVec];
     if constexpr (!kDown) {
@@ -414,6 +388,27 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         // holds, per lane, 16-byte slots of the permuted column order, so the stores need no
         // shuffles.
         float *tab = reinterpret_cast<float *>(smem);
+        constexpr int kWpp = kNW / 2;                 // warps per part
+        constexpr int kMt = (kCodes / 16) / kWpp;     // 16-code tiles per warp and stage
+        static_assert((kCodes / 16) % kWpp == 0, "code tiles per warp");
+        const int mp = warp / kWpp, mq = warp % kWpp;
+        const int fg = lane >> 2, ft = lane & 3;
+        const float *p0, *p1;
+        unit_codebooks<kDown>(A, U, p0, p1);
+        const float *Cp = mp ? p1 : p0;
+        // A operand (codebook rows c0 + fg and c0 + fg + 8 of tile (s, i); inputs ft, ft + 4)
+        float av[kStages][kMt][4];
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+#pragma unroll
+            for (int i = 0; i < kMt; ++i) {
+                const float *r0 = Cp + ((size_t)s * kCodes + (size_t)(mq * kMt + i) * 16 + fg) * kVec;
+                const float *r1 = r0 + 8 * kVec;
+                av[s][i][0] = __ldg(r0 + ft);
+                av[s][i][1] = __ldg(r1 + ft);
+                av[s][i][2] = __ldg(r0 + ft + 4);
+                av[s][i][3] = __ldg(r1 + ft + 4);
+            }
         // B operand: column j = 8 nt + fg of part mp (nt = 0..3), inputs ft and ft + 4
         float bv[4][2];
 #pragma unroll
