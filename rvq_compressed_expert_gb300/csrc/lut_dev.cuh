@@ -31,7 +31,7 @@ struct LutArgs {
     MatGeom gu;
     size_t off_gate, off_up;
     int gu_pairs;   // segment pairs of the gate/up input, (gu.nseg + 1) / 2
-    int gu_parts;   // gate/up partials per (slot, matrix): gu_pairs (pair units) or gu.nseg (half units)
+    int gu_parts;   // gate/up partials per (slot, matrix): one per segment, gu.nseg
     float *part_gu; // [slot][gu_parts][2 matrices: gate, up][f]
     // down
     MatGeom dn;
@@ -528,7 +528,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
         acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 16);
     };
-    // the lookups of part p of one row group: acc = (part 0) or += (part 1) the 16 partials
+    // the lookups of part p of one row group: acc = (part 0, and every gate/up part) or +=
+    // (part 1 of down) the 16 partials
     auto lookups = [&](const uint4 (&cwp)[kStages], int p, float (&acc)[16]) {
         const uint32_t colb = p ? colb1 : colb0;
 #pragma unroll
@@ -565,28 +566,32 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                     sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
                     t = sacc;
                 }
-                if (p == 1) acc[4 * wd + b] += t;
+                if (kDown && p == 1) acc[4 * wd + b] += t;
                 else acc[4 * wd + b] = t;
             }
         }
     };
-    // reduce-scatter of the row partials (both segments added) and store
-    auto finish = [&](float (&acc)[16], int g) {
+    // reduce-scatter of the row partials and store: gate/up one partial per segment (part p),
+    // down one for both segments added
+    auto finish = [&](float (&acc)[16], int p, int g) {
         const int row = g * kGroupRows + (lane & 15);
         reduce16(acc);
         if (lane < 16 && row < G.n_out) {
-            if constexpr (!kDown)
-                A.part_gu[(((size_t)U.slot * A.gu_parts + U.seg0 / 2) * 2 + U.mat) * G.n_out + row] = acc[0];
-            else
+            if constexpr (!kDown) {
+                if (U.seg0 + p < G.nseg)
+                    A.part_gu[(((size_t)U.slot * A.gu_parts + U.seg0 + p) * 2 + U.mat) * G.n_out + row] = acc[0];
+            } else {
                 A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = acc[0];
+            }
         }
     };
     if constexpr (kPing) {
         auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
             float acc[16];
             lookups(cw[0], 0, acc);
+            if constexpr (!kDown) finish(acc, 0, g);
             lookups(cw[1], 1, acc);
-            finish(acc, g);
+            finish(acc, 1, g);
         };
         uint4 wa[2][kStages], wb[2][kStages];
         int g = U.g0 + warp;
@@ -609,8 +614,9 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             ahead(g);
             float acc[16];
             lookups(wa[0], 0, acc);
+            if constexpr (!kDown) finish(acc, 0, g);
             lookups(wa[1], 1, acc);
-            finish(acc, g);
+            finish(acc, 1, g);
         }
     } else {
         // one set of code registers: as soon as a part's lookups are issued, the next row
@@ -622,12 +628,22 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         for (; g < U.g1; g += kNW) {
             const int gn = g + kNW;
             ahead(g);
-            float acc[16];
-            lookups(wa[0], 0, acc);
-            if (gn < U.g1) load_part(gn, 0, wa);
-            lookups(wa[1], 1, acc);
-            if (gn < U.g1) load_part(gn, 1, wa);
-            finish(acc, g);
+            if constexpr (!kDown) {
+                float acc0[16], acc1[16];
+                lookups(wa[0], 0, acc0);
+                if (gn < U.g1) load_part(gn, 0, wa);
+                lookups(wa[1], 1, acc1);
+                if (gn < U.g1) load_part(gn, 1, wa);
+                finish(acc0, 0, g);
+                finish(acc1, 1, g);
+            } else {
+                float acc[16];
+                lookups(wa[0], 0, acc);
+                if (gn < U.g1) load_part(gn, 0, wa);
+                lookups(wa[1], 1, acc);
+                if (gn < U.g1) load_part(gn, 1, wa);
+                finish(acc, 1, g);
+            }
         }
     }
     // algorithmic bytes of this unit: codes of its real (row, vector) pairs,

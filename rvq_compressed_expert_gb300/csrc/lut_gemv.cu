@@ -216,7 +216,7 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
     A.off_gate = L.sec_off[0];
     A.off_up = L.sec_off[1];
     A.gu_pairs = (L.gu.nseg + 1) / 2;
-    A.gu_parts = L.gu.nseg; // the per-phase table-form gate/up kernel runs half-CTA units
+    A.gu_parts = L.gu.nseg;
     A.part_gu = W.part_gu;
     A.dn = L.dn;
     A.off_down = L.sec_off[2];
@@ -236,10 +236,9 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
 
 cudaError_t launch_lut_phase(const LutArgs &A_in, bool down, bool reconstruct, bool bf16, int num_sms,
                              cudaStream_t s) {
-    // the table form's gate/up: half-CTA units, one partial per segment; the reconstruct
-    // form: pair units, one partial per pair of segments
+    // the table form's gate/up: half-CTA units; the reconstruct form: pair units (both write
+    // one partial per segment, summed alike)
     LutArgs A = A_in;
-    A.gu_parts = reconstruct ? A.gu_pairs : A.gu.nseg;
     if (!down && !reconstruct)
         return bf16 ? launch_gu_half<true>(A, A.slots * 2 * A.gu.nseg, num_sms, s)
                     : launch_gu_half<false>(A, A.slots * 2 * A.gu.nseg, num_sms, s);
