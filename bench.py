@@ -1117,7 +1117,7 @@ def print_unit_trace(tr, w):
     """Per-phase summary of the lookup kernels' unit trace: table build and row streaming."""
     import math as _m
     slots = w.tokens * w.top_k
-    n_gu = slots * 2 * _m.ceil(w.d / 8 / 32)  # (slot, segment, matrix) half-CTA units
+    n_gu = slots * 2 * _m.ceil(_m.ceil(w.d / 8 / 32) / 2)  # (slot, segment pair, matrix) units
     rows = tr.tolist()
     out = []
     for name, a, b in (("gate_up", 0, n_gu), ("down", n_gu, len(rows))):

@@ -429,8 +429,8 @@ int waste_moe_debug_wait(waste_moe *h, const uint32_t *d_counter, uint32_t targe
  *   d_records    bank of records, 4096-aligned; not re-validated here (validate
  *                once, e.g. with waste_moe_create)
  *   d_codebooks, d_h, d_idx, d_gate, d_out, mode: as for waste_moe_forward
- * Limits: the T * top_k slots need (f * 2 * ceil(d/256) + d * ceil(f/512)) * 4 bytes
- * of scratch each (about 0.43 MB at d = 7168, f = 1536, i.e. T * top_k <= 19 there);
+ * Limits: the T * top_k slots need (f * 2 * ceil(d/512) + d * ceil(f/512)) * 4 bytes
+ * of scratch each (about 0.26 MB at d = 7168, f = 1536, i.e. T * top_k <= 32 there);
  * a call beyond 8 MiB in total is rejected with WASTE_EINVAL and launches nothing.
  * No cudaMalloc, cudaFree or other allocating routine is called.
  * The first call on a device looks up the array's device address

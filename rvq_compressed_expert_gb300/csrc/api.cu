@@ -316,7 +316,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
         T * kMaxTopK * 4,                           // pred_idx
         T * 4,                                      // pred_count
         T * kMaxTopK * 4,                           // pred_gate_sel
-        S * (size_t)L.gu.nseg * 2 * (size_t)L.f * 4, // part_gu
+        S * (size_t)((L.gu.nseg + 1) / 2) * 2 * (size_t)L.f * 4, // part_gu
         S * npair * (size_t)L.d * 4,                // part_dn
         kStatCount * 8,                             // stats
         4,                                          // err

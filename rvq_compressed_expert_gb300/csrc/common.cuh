@@ -166,7 +166,7 @@ struct Workspace {
     int32_t *pred_count; // [max_T]
     int32_t *pred_idx_sel; // scratch for prefetch top-k
     float *pred_gate_sel;  // scratch (unused gates of the prediction)
-    float *part_gu;      // [max_slots][gu.nseg][2][f]
+    float *part_gu;      // [max_slots][(gu.nseg + 1) / 2][2][f]
     float *part_dn;      // [max_slots][(dn.nseg + 1) / 2][d]; tensor-core slots use part 0
     unsigned long long *stats; // [kStatCount]
     uint32_t *err;       // sticky error bits

@@ -337,7 +337,6 @@ cudaError_t launch_fused_step(const LayerView &L, const Workspace &W, const void
     A.off_gate = L.sec_off[0];
     A.off_up = L.sec_off[1];
     A.gu_pairs = (L.gu.nseg + 1) / 2;
-    A.gu_parts = L.gu.nseg;
     A.part_gu = W.part_gu;
     A.dn = L.dn;
     A.off_down = L.sec_off[2];

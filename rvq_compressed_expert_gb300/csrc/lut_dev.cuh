@@ -31,8 +31,7 @@ struct LutArgs {
     MatGeom gu;
     size_t off_gate, off_up;
     int gu_pairs;   // segment pairs of the gate/up input, (gu.nseg + 1) / 2
-    int gu_parts;   // gate/up partials per (slot, matrix): one per segment, gu.nseg
-    float *part_gu; // [slot][gu_parts][2 matrices: gate, up][f]
+    float *part_gu; // [slot][gu_pairs][2 matrices: gate, up][f]
     // down
     MatGeom dn;
     size_t off_down;
@@ -349,20 +348,20 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             const int r = U.seg0 * kSegVec * kVec + i; // index into f
             float a = 0.f;
             if (valid && r < A.gu.n_out) {
-                const float *pg = A.part_gu + (size_t)U.slot * A.gu_parts * 2 * A.gu.n_out + r;
+                const float *pg = A.part_gu + (size_t)U.slot * A.gu_pairs * 2 * A.gu.n_out + r;
                 const size_t step = (size_t)2 * A.gu.n_out;
                 float zg = 0.f, zu = 0.f;
-                for (int s0 = 0; s0 < A.gu_parts; s0 += 32) {
+                for (int s0 = 0; s0 < A.gu_pairs; s0 += 32) {
                     float vg[32], vu[32];
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
-                        const int sg = min(s0 + q, A.gu_parts - 1);
+                        const int sg = min(s0 + q, A.gu_pairs - 1);
                         vg[q] = pg[sg * step];
                         vu[q] = pg[sg * step + A.gu.n_out];
                     }
 #pragma unroll
                     for (int q = 0; q < 32; ++q)
-                        if (s0 + q < A.gu_parts) {
+                        if (s0 + q < A.gu_pairs) {
                             zg += vg[q];
                             zu += vu[q];
                         }
@@ -528,8 +527,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
         acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 16);
     };
-    // the lookups of part p of one row group: acc = (part 0, and every gate/up part) or +=
-    // (part 1 of down) the 16 partials
+    // the lookups of part p of one row group: acc = (part 0) or += (part 1) the 16 partials
     auto lookups = [&](const uint4 (&cwp)[kStages], int p, float (&acc)[16]) {
         const uint32_t colb = p ? colb1 : colb0;
 #pragma unroll
@@ -566,32 +564,28 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                     sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
                     t = sacc;
                 }
-                if (kDown && p == 1) acc[4 * wd + b] += t;
+                if (p == 1) acc[4 * wd + b] += t;
                 else acc[4 * wd + b] = t;
             }
         }
     };
-    // reduce-scatter of the row partials and store: gate/up one partial per segment (part p),
-    // down one for both segments added
-    auto finish = [&](float (&acc)[16], int p, int g) {
+    // reduce-scatter of the row partials (both segments added) and store
+    auto finish = [&](float (&acc)[16], int g) {
         const int row = g * kGroupRows + (lane & 15);
         reduce16(acc);
         if (lane < 16 && row < G.n_out) {
-            if constexpr (!kDown) {
-                if (U.seg0 + p < G.nseg)
-                    A.part_gu[(((size_t)U.slot * A.gu_parts + U.seg0 + p) * 2 + U.mat) * G.n_out + row] = acc[0];
-            } else {
+            if constexpr (!kDown)
+                A.part_gu[(((size_t)U.slot * A.gu_pairs + U.seg0 / 2) * 2 + U.mat) * G.n_out + row] = acc[0];
+            else
                 A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = acc[0];
-            }
         }
     };
     if constexpr (kPing) {
         auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
             float acc[16];
             lookups(cw[0], 0, acc);
-            if constexpr (!kDown) finish(acc, 0, g);
             lookups(cw[1], 1, acc);
-            finish(acc, 1, g);
+            finish(acc, g);
         };
         uint4 wa[2][kStages], wb[2][kStages];
         int g = U.g0 + warp;
@@ -614,9 +608,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             ahead(g);
             float acc[16];
             lookups(wa[0], 0, acc);
-            if constexpr (!kDown) finish(acc, 0, g);
             lookups(wa[1], 1, acc);
-            finish(acc, 1, g);
+            finish(acc, g);
         }
     } else {
         // one set of code registers: as soon as a part's lookups are issued, the next row
@@ -628,22 +621,12 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         for (; g < U.g1; g += kNW) {
             const int gn = g + kNW;
             ahead(g);
-            if constexpr (!kDown) {
-                float acc0[16], acc1[16];
-                lookups(wa[0], 0, acc0);
-                if (gn < U.g1) load_part(gn, 0, wa);
-                lookups(wa[1], 1, acc1);
-                if (gn < U.g1) load_part(gn, 1, wa);
-                finish(acc0, 0, g);
-                finish(acc1, 1, g);
-            } else {
-                float acc[16];
-                lookups(wa[0], 0, acc);
-                if (gn < U.g1) load_part(gn, 0, wa);
-                lookups(wa[1], 1, acc);
-                if (gn < U.g1) load_part(gn, 1, wa);
-                finish(acc, 1, g);
-            }
+            float acc[16];
+            lookups(wa[0], 0, acc);
+            if (gn < U.g1) load_part(gn, 0, wa);
+            lookups(wa[1], 1, acc);
+            if (gn < U.g1) load_part(gn, 1, wa);
+            finish(acc, g);
         }
     }
     // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
@@ -658,176 +641,6 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         atomicAdd(A.stats + kStatDemandCode, vecs * (unsigned long long)rows * kStages);
         if (U.seg0 == 0 && U.g0 == 0)
             atomicAdd(A.stats + kStatCodebook, (unsigned long long)kCbFloats * sizeof(float));
-    }
-}
-
-// ---------------------------------------------------------------- half-CTA gate/up units
-//
-// The per-phase gate/up kernel runs each half of its CTA (8 warps, named barrier 1 + half) as
-// an independent worker over units (slot, 32-vector segment, matrix): a half builds its unit's
-// table in its own half of every table row (T[s][c][half][column], the part slot of the
-// layout above) and streams the unit's rows, while the other half does the same for its own
-// units.  The halves drift apart, so one half's table build (tensor-core MMAs and stores) runs
-// beside the other half's row stream instead of stopping the whole SM.
-
-// Unit u of the half-unit order: (slot, segment, matrix), the matrix fastest.
-__device__ __forceinline__ Unit decode_gu_half(const LutArgs &A, int u) {
-    Unit U;
-    U.slot = u / (2 * A.gu.nseg);
-    if (A.slot_list) U.slot = A.slot_list[U.slot];
-    const int rem = u % (2 * A.gu.nseg);
-    U.seg0 = rem >> 1;
-    U.mat = rem & 1;
-    U.g0 = 0;
-    U.g1 = A.gu.groups;
-    U.e = A.idx[U.slot];
-    U.base[0] = U.base[1] = nullptr;
-    const uint8_t *rec = (U.e >= 0 && U.e < A.E) ? expert_record(A.records, A.stride, A.slot_map, U.e) : nullptr;
-    if (rec)
-        U.base[0] = rec + (U.mat ? A.off_up : A.off_gate) + (size_t)U.seg0 * A.gu.groups * (kStages * 512);
-    return U;
-}
-
-// Ask L2 for row group g of a one-segment unit: 3 stages x 512 B = 12 lines, lanes 0..11.
-__device__ __forceinline__ void prefetch_group1(const Unit &U, int g, int lane) {
-    if (lane < 12 && U.base[0]) {
-        const uint8_t *p = U.base[0] + ((size_t)g * kStages + lane / 4) * 512 + (size_t)(lane % 4) * 128;
-        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
-    }
-}
-
-__device__ __forceinline__ void half_barrier(int half) {
-    asm volatile("bar.sync %0, 256;" ::"r"(1 + half) : "memory");
-}
-
-template <bool kBf16>
-__device__ __forceinline__ void run_gu_half(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
-                                            int half, unsigned long long *t_tables) {
-    constexpr int kHW = 8;                    // warps of a half
-    unsigned char *smem = lut_smem;
-    const Unit U = Uin;
-    Unit N = Uin;
-    if (has_next) N = Nin;
-    const int wh = (threadIdx.x >> 5) & 7, lane = threadIdx.x & 31;
-    const int htid = threadIdx.x & 255;       // thread of the half
-    const MatGeom &G = A.gu;
-    const bool valid = U.base[0] != nullptr;
-    const uint32_t colb = ((uint32_t)half << 7) | ((uint32_t)tab_col(lane) << 2);
-    // warm L2 with the first round of row groups this warp streams
-    if (U.g0 + wh < U.g1) prefetch_group1(U, U.g0 + wh, lane);
-    if (!valid && htid == 0) atomicOr(A.err, (U.e >= 0 && U.e < A.E) ? kErrNotResident : kErrBadExpert);
-    const int t = U.slot / A.k;
-    // ---- table T[s][c][half][column] of the unit's segment and matrix: as in run_unit, the
-    // 8 warps each take 2 of the 16 code tiles of every stage
-    {
-        float *tab = reinterpret_cast<float *>(smem);
-        constexpr int kMt = (kCodes / 16) / kHW;
-        const int fg = lane >> 2, ft = lane & 3;
-        const float *Cp = A.codebooks + ((size_t)((U.e >= 0 && U.e < A.E) ? U.e : 0) * 3 + U.mat) * kCbFloats;
-        float av[kStages][kMt][4];
-#pragma unroll
-        for (int s = 0; s < kStages; ++s)
-#pragma unroll
-            for (int i = 0; i < kMt; ++i) {
-                const float *r0 = Cp + ((size_t)s * kCodes + (size_t)(wh * kMt + i) * 16 + fg) * kVec;
-                const float *r1 = r0 + 8 * kVec;
-                av[s][i][0] = __ldg(r0 + ft);
-                av[s][i][1] = __ldg(r1 + ft);
-                av[s][i][2] = __ldg(r0 + ft + 4);
-                av[s][i][3] = __ldg(r1 + ft + 4);
-            }
-        float bv[4][2];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int jg = U.seg0 * kSegVec + 8 * nt + fg;
-            const bool in = jg < G.nv;
-            const size_t e0 = (size_t)t * G.n_in + (size_t)min(jg, G.nv - 1) * kVec;
-            bv[nt][0] = in ? load_x1<kBf16>(A.h, e0 + ft) : 0.f;
-            bv[nt][1] = in ? load_x1<kBf16>(A.h, e0 + ft + 4) : 0.f;
-        }
-        half_barrier(half); // this half's previous lookups are done with its table
-        if (t_tables && htid == 0) t_tables[1] = gtimer();
-        uint32_t bhi[4][2], blo[4][2];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) split_tf32(bv[nt][q], bhi[nt][q], blo[nt][q]);
-        const int odd = fg & 1;
-        const int g_first = 2 * ft + odd, g_second = 2 * ft + 1 - odd;
-#pragma unroll
-        for (int s = 0; s < kStages; ++s) {
-#pragma unroll
-            for (int i = 0; i < kMt; ++i) {
-                const int c0 = (wh * kMt + i) * 16;
-                uint32_t ahi[4], alo[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) split_tf32(av[s][i][q], ahi[q], alo[q]);
-                float dd[4][4];
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    dd[nt][0] = dd[nt][1] = dd[nt][2] = dd[nt][3] = 0.f;
-                    mma_tf32(dd[nt], ahi, blo[nt]);
-                    mma_tf32(dd[nt], alo, bhi[nt]);
-                    mma_tf32(dd[nt], ahi, bhi[nt]);
-                }
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float4 ev = make_float4(dd[0][2 * hh], dd[1][2 * hh], dd[2][2 * hh], dd[3][2 * hh]);
-                    float4 ov = make_float4(dd[0][2 * hh + 1], dd[1][2 * hh + 1], dd[2][2 * hh + 1],
-                                            dd[3][2 * hh + 1]);
-                    if (!valid) ev = ov = make_float4(0.f, 0.f, 0.f, 0.f);
-                    float *row = tab + (((size_t)s * kCodes + c0 + fg + 8 * hh) * 2 + half) * kSegVec;
-                    *reinterpret_cast<float4 *>(row + 4 * g_first) = odd ? ov : ev;
-                    *reinterpret_cast<float4 *>(row + 4 * g_second) = odd ? ev : ov;
-                }
-            }
-        }
-        half_barrier(half); // table complete
-    }
-    if (t_tables && htid == 0) t_tables[0] = gtimer();
-    // ---- stream rows [g0, g1) of the segment: row group g per warp round, 48 lookups per
-    // lane, one reduce-scatter; the next round's codes are asked for right after the lookups
-    const uint8_t *pb = U.base[0];
-    const uint32_t tab32 = (uint32_t)__cvta_generic_to_shared(smem);
-    auto load = [&](int g, uint4 (&w)[kStages]) {
-#pragma unroll
-        for (int s = 0; s < kStages; ++s)
-            w[s] = pb ? ld_stream(pb + ((size_t)g * kStages + s) * 512 + (size_t)lane * 16) : make_uint4(0, 0, 0, 0);
-    };
-    uint4 wa[kStages];
-    int g = U.g0 + wh;
-    if (g < U.g1) load(g, wa);
-    for (; g < U.g1; g += kHW) {
-        const int gn = g + kHW;
-        if (gn < U.g1) prefetch_group1(U, gn, lane);
-        else if (has_next && N.g0 + (gn - U.g1) < N.g1) prefetch_group1(N, N.g0 + (gn - U.g1), lane);
-        float acc[16];
-#pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-            const uint32_t w0 = comp(wa[0], wd), w1 = comp(wa[1], wd), w2 = comp(wa[2], wd);
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const uint32_t sel = 0x7604u | ((uint32_t)b << 4);
-                const float t0 = lds_stage<0>(tab32 + __byte_perm(w0, colb, sel));
-                const float t1 = lds_stage<1>(tab32 + __byte_perm(w1, colb, sel));
-                const float t2 = lds_stage<2>(tab32 + __byte_perm(w2, colb, sel));
-                acc[4 * wd + b] = (t0 + t1) + t2;
-            }
-        }
-        if (gn < U.g1) load(gn, wa);
-#pragma unroll
-        for (int n = 8; n >= 1; n >>= 1)
-#pragma unroll
-            for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
-        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 16);
-        const int row = g * kGroupRows + (lane & 15);
-        if (lane < 16 && row < G.n_out)
-            A.part_gu[(((size_t)U.slot * A.gu_parts + U.seg0) * 2 + U.mat) * G.n_out + row] = acc[0];
-    }
-    if (htid == 0 && valid && A.stats) {
-        const unsigned long long vecs = (unsigned long long)min(kSegVec, G.nv - U.seg0 * kSegVec);
-        atomicAdd(A.stats + kStatDemandCode, vecs * (unsigned long long)G.n_out * kStages);
-        if (U.seg0 == 0) atomicAdd(A.stats + kStatCodebook, (unsigned long long)kCbFloats * sizeof(float));
     }
 }
 

@@ -63,32 +63,6 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
     if constexpr (!kRecon) cp_async_wait<0>();
 }
 
-// Gate/up with each half of the CTA running its own (slot, segment, matrix) units.
-template <bool kBf16>
-__global__ void __launch_bounds__(kThreads, 1) lut_gu_half_kernel(const LutArgs A) {
-    const int half = threadIdx.x >> 8;
-    const int units = lut_slot_count(A) * 2 * A.gu.nseg;
-    const int stride = 2 * (int)gridDim.x;
-    Unit N;
-    for (int u = 2 * (int)blockIdx.x + half; u < units; u += stride) {
-        const Unit U = decode_gu_half(A, u);
-        const bool has_next = u + stride < units;
-        if (has_next) N = decode_gu_half(A, u + stride);
-        unsigned long long t0 = 0, t_tab[2] = {0, 0};
-        if (A.trace && (threadIdx.x & 255) == 0) t0 = gtimer();
-        run_gu_half<kBf16>(A, U, has_next, N, half, A.trace ? t_tab : nullptr);
-        if (A.trace && (threadIdx.x & 255) == 0 && A.trace_base + u < A.trace_cap) {
-            unsigned smid;
-            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-            unsigned long long *e = A.trace + 4 * (size_t)(A.trace_base + u);
-            e[0] = t0;
-            e[1] = t_tab[0];
-            e[2] = gtimer();
-            e[3] = smid | ((t_tab[1] > t0 ? (t_tab[1] - t0) : 0ull) << 32);
-        }
-    }
-}
-
 // out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair],
 // slots in rank order and pairs in order.  A CTA takes 32 rows of one token with one warp per
 // slot: lane l of warp i sums slot i's pairs of row l (every load of the launch in flight at
@@ -167,17 +141,6 @@ cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s)
     return launch_v<kDown, kRecon, kBf16, kThreads, kCodePingPong, kPrefetchRounds>(A, units, num_sms, s);
 }
 
-template <bool kBf16>
-cudaError_t launch_gu_half(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
-    const size_t smem = unit_smem<false>();
-    static SmemAttr attr;
-    cudaError_t e = ensure_smem(attr, (const void *)lut_gu_half_kernel<kBf16>, (int)smem);
-    if (e != cudaSuccess) return e;
-    const int ctas = (units + 1) / 2;
-    lut_gu_half_kernel<kBf16><<<ctas < num_sms ? ctas : num_sms, kThreads, smem, s>>>(A);
-    return cudaGetLastError();
-}
-
 template <bool kDown>
 cudaError_t launch_var(const LutArgs &A, int units, bool recon, bool bf16, int num_sms, cudaStream_t s) {
     if (recon) return bf16 ? launch_one<kDown, true, true>(A, units, num_sms, s)
@@ -216,7 +179,6 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
     A.off_gate = L.sec_off[0];
     A.off_up = L.sec_off[1];
     A.gu_pairs = (L.gu.nseg + 1) / 2;
-    A.gu_parts = L.gu.nseg;
     A.part_gu = W.part_gu;
     A.dn = L.dn;
     A.off_down = L.sec_off[2];
@@ -234,14 +196,8 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
     return A;
 }
 
-cudaError_t launch_lut_phase(const LutArgs &A_in, bool down, bool reconstruct, bool bf16, int num_sms,
+cudaError_t launch_lut_phase(const LutArgs &A, bool down, bool reconstruct, bool bf16, int num_sms,
                              cudaStream_t s) {
-    // the table form's gate/up: half-CTA units; the reconstruct form: pair units (both write
-    // one partial per segment, summed alike)
-    LutArgs A = A_in;
-    if (!down && !reconstruct)
-        return bf16 ? launch_gu_half<true>(A, A.slots * 2 * A.gu.nseg, num_sms, s)
-                    : launch_gu_half<false>(A, A.slots * 2 * A.gu.nseg, num_sms, s);
     if (!down) return launch_var<false>(A, A.slots * 2 * A.gu_pairs, reconstruct, bf16, num_sms, s);
     return launch_var<true>(A, A.slots * A.npair * A.nrb, reconstruct, bf16, num_sms, s);
 }
@@ -291,7 +247,7 @@ cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const voi
     cudaError_t e = launch_lut_phase(A, false, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[1], s);
-    A.trace_base = A.slots * 2 * (reconstruct ? A.gu_pairs : A.gu.nseg); // down units follow the gate/up units
+    A.trace_base = A.slots * 2 * A.gu_pairs; // down units follow the gate/up units
     e = launch_lut_phase(A, true, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[2], s);

@@ -87,7 +87,7 @@ int waste_moe_forward_noalloc(const waste_moe_config *cfg, const uint8_t *d_reco
     // scratch demand of this call against the fixed array
     const size_t slots = (size_t)T * (size_t)cfg->top_k;
     const size_t npair = (size_t)down_parts(L);
-    const size_t gu_bytes = round_up(slots * (size_t)L.gu.nseg * 2 * (size_t)cfg->f * 4, 256);
+    const size_t gu_bytes = round_up(slots * (size_t)((L.gu.nseg + 1) / 2) * 2 * (size_t)cfg->f * 4, 256);
     const size_t dn_bytes = round_up(slots * npair * (size_t)cfg->d * 4, 256);
     if (256 + gu_bytes + dn_bytes > kStaticScratchBytes)
         return fail_na(WASTE_EINVAL,
