@@ -1061,6 +1061,38 @@ def profile_case(args):
     print("profile case done")
 
 
+def profile_stack(args):
+    """Small stack for ncu captures of the lookahead's DRAM bytes: 8 layers x 32 resident
+    experts at d=7168, f=1536, top-16, one token per pass through the stack (eager launches),
+    with the lookahead of --lookahead experts (0 = off).  The last --steps tokens are the ones
+    to capture (each token: per layer rmsnorm, route, experts, combine, and with the lookahead
+    the next layer's router, top-k and prefetch)."""
+    from rvq_compressed_expert_gb300 import _build
+    from rvq_compressed_expert_gb300 import binding as B
+    from rvq_compressed_expert_gb300 import synth
+    from rvq_compressed_expert_gb300.layer import MoELayer
+    from rvq_compressed_expert_gb300.stack import DecodeStack
+    _build.build()
+    B.load()
+    w = synth.Workload("stack-e32", 7168, 1536, 32, 16, 1, "f32", "offsets", n_layers=8, lookahead=6)
+    layers = [MoELayer(w, seed=0, layer=L, device="cuda", max_tokens=1) for L in range(w.n_layers)]
+    stack = DecodeStack(layers, 1)
+    main = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for i in range(args.warmup + args.steps):
+        h = synth.hidden(200 + i, 1, w.d, "f32", "cuda")
+        flush.zero_()
+        main.wait_stream(torch.cuda.current_stream())
+        stack.run(h, args.lookahead, main, side)
+        torch.cuda.current_stream().wait_stream(main)
+        torch.cuda.synchronize()
+    for l in layers:
+        l.stats()
+        l.close()
+    print("stack profile case done")
+
+
 def profile_encoder():
     """One encoder training of a dense 1536 x 7168 matrix (the gate matrix of the decode shape),
     two Lloyd rounds per stage: a small case for ncu captures of the assignment kernels."""
@@ -1194,6 +1226,9 @@ def main():
                     help="with --profile-case: print the step kernel's item timeline")
     ap.add_argument("--profile-encoder", action="store_true",
                     help="train one 1536 x 7168 matrix with the RVQ encoder (2 Lloyd rounds) for ncu and exit")
+    ap.add_argument("--profile-stack", action="store_true",
+                    help="pass tokens through an 8-layer stack (32 experts each) for ncu and exit")
+    ap.add_argument("--lookahead", type=int, default=6, help="with --profile-stack: experts predicted per layer")
     ap.add_argument("--profile-route", action="store_true",
                     help="route one token through the decode layer's router (graph replays) for ncu and exit")
     args = ap.parse_args()
@@ -1207,6 +1242,9 @@ def main():
         return
     if args.profile_route:
         profile_route(args)
+        return
+    if args.profile_stack:
+        profile_stack(args)
         return
     if args.impl == "reference":
         reference(args)

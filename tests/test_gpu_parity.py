@@ -63,6 +63,7 @@ def check_routing(g_idx, g_gate, ref_logits, k):
         ridx, rg = oracle.topk_softmax(l, k)
         if oracle.topk_margin(l, k) > tau:
             np.testing.assert_array_equal(g_idx[t], ridx, err_msg=f"token {t}")
+            # the gates are an fp32 output of the path: held to the fp32 bar (relative 1e-5)
             np.testing.assert_allclose(g_gate[t], rg, rtol=1e-5, atol=1e-7)
             ok_tokens.append(t)
         else:
@@ -429,8 +430,24 @@ def test_decode_layer_full_size(seed):
         np.testing.assert_array_equal(g_idx[0], ref["idx"])
         np.testing.assert_allclose(g_gate[0], ref["gate"], rtol=1e-5, atol=1e-7)
         assert_close(g_out[0], ref["out"])
-        # reconstruct variant on the same weights gives the same answer within tolerance
         st = layer.stats()
         assert st["demand_code_bytes"] == w.top_k * oracle.expert_code_bytes(w.d, w.f)
+        # the register-reconstruct form of the expert kernels on the same records: the same
+        # experts and the same output within the fp32 bar
+        rcfg = B.make_config(w.d, w.f, w.n_experts, w.top_k, "f32", 1, 0, B.FLAG_K2_RECONSTRUCT, 0)
+        rh = B.waste_moe_create(rcfg, layer.router_w, layer.router_b, layer.records, layer.stride,
+                                layer.codebooks)
+        try:
+            idx = torch.empty(1, w.top_k, dtype=torch.int32, device="cuda")
+            gate = torch.empty(1, w.top_k, dtype=torch.float32, device="cuda")
+            out = torch.empty(1, w.d, dtype=torch.float32, device="cuda")
+            B.waste_moe_route(rh, h, 1, idx, gate)
+            B.waste_moe_forward(rh, h, 1, idx, gate, out, 0)
+            torch.cuda.synchronize()
+            B.waste_moe_stats(rh)
+            np.testing.assert_array_equal(idx[0].cpu().numpy(), ref["idx"])
+            assert_close(out[0].cpu().numpy(), ref["out"])
+        finally:
+            B.waste_moe_destroy(rh)
     finally:
         layer.close()
