@@ -311,33 +311,11 @@ def run_decode(args, dev, out):
     del ug
     B.waste_moe_destroy(uh)
 
-    # per-kernel device times.  First inside a CUDA graph of the step captured with the
-    # library's profiling events on (the events become nodes of the graph, between its
-    # kernels), replayed as the timed steps are; then the same step launched directly with
-    # the events between its kernels, queued behind a short spin kernel so launches never
-    # starve the GPU
+    # per-kernel device times: the same step launched directly with CUDA events between
+    # its kernels, queued behind a short spin kernel so launches never starve the GPU
     B.waste_moe_set_profiling(layer.handle, True)
-    n_prof = max(8, min(K, 200))
-    kern_graph, graph_err = None, None
-    try:
-        pg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(pg):
-            step()
-        gprof = []
-        t_start = time.time()
-        for i in range(n_prof):
-            h_in.copy_(pool[i % DECODE_POOL])
-            flush.zero_()
-            pg.replay()
-            gprof.append(B.waste_moe_read_profile(layer.handle))
-        torch.cuda.synchronize()
-        args.sampler.mark(t_start, time.time())
-        del pg
-        kern_graph = {k: statistics.mean(p[k] for p in gprof) for k in gprof[0] if gprof[0][k] >= 0}
-    except Exception as e:  # an event that cannot be timed inside a graph: eager times only
-        graph_err = f"{type(e).__name__}: {e}"
-        torch.cuda.synchronize()
     prof = []
+    n_prof = max(8, min(K, 200))
     t_start = time.time()
     for i in range(n_prof):
         h_in.copy_(pool[i % DECODE_POOL])
@@ -350,8 +328,7 @@ def run_decode(args, dev, out):
     B.waste_moe_set_profiling(layer.handle, False)
 
     step_bytes, gu_bytes, dn_bytes = decode_algorithmic_bytes(w)
-    kern_eager = {k: statistics.mean(p[k] for p in prof) for k in prof[0] if prof[0][k] >= 0}
-    kern = kern_graph if kern_graph else kern_eager
+    kern = {k: statistics.mean(p[k] for p in prof) for k in prof[0] if prof[0][k] >= 0}
     ms_per_step = total_ms / K
 
     # the register-reconstruct form of the expert kernels (WASTE_FLAG_K2_RECONSTRUCT: each
@@ -377,10 +354,7 @@ def run_decode(args, dev, out):
                gate_up_frac=gu_bytes / (rk["gate_up"] * 1e-3) / 1e9 / peak_k2,
                down_frac=dn_bytes / (rk["down"] * 1e-3) / 1e9 / peak_k2,
                table_form_gate_up_ms=kern.get("gate_up"), table_form_down_ms=kern.get("down"))
-    out["decode"] = dict(step_ms=ms_per_step, kernels_ms=kern, kernels_ms_eager=kern_eager,
-                         kernels_timing="graph replay with event nodes between the kernels" if kern_graph
-                         else f"eager launches with events between the kernels ({graph_err})",
-                         stats=st, step_bytes=step_bytes,
+    out["decode"] = dict(step_ms=ms_per_step, kernels_ms=kern, stats=st, step_bytes=step_bytes,
                          gate_up_bytes=gu_bytes, down_bytes=dn_bytes,
                          hbm_gbs_step=step_bytes / (ms_per_step * 1e-3) / 1e9,
                          median_step_ms=statistics.median(step_ms),
@@ -965,8 +939,6 @@ def native(args):
             / ((kern["gate_up"] + kern["down"]) * 1e-3) / 1e9 / peak if "gate_up" in kern else None,
             "algorithmic_bytes_per_step": d["step_bytes"],
             "kernels_ms": kern,
-            "kernels_ms_eager": d["kernels_ms_eager"],
-            "kernels_timing": d["kernels_timing"],
             "ms_per_step_persistent_step_kernel": d["unfused_ms"],
             "k2a_register_reconstruct": d["k2a_reconstruct"],
         },
