@@ -8,7 +8,6 @@
 #include <stddef.h>
 
 #include <atomic>
-#include <utility>
 
 #include "waste_moe.h"
 
@@ -68,30 +67,6 @@ inline MatGeom mat_geom(int n_out, int n_in) {
 }
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// Programmatic dependent launch.  A kernel launched with pdl = true (launch_k) may be scheduled
-// while the kernel before it on the stream is still finishing; before reading anything that
-// kernel wrote it calls grid_dep_wait(), which returns once that kernel has completed and its
-// writes are visible (at once for a kernel launched without the attribute).  grid_dep_launch()
-// lets the next kernel on the stream be scheduled early.
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                     Args &&...args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
 
 // Devices the per-device host caches below track (ordinals past it are served uncached).
 constexpr int kMaxDevices = 64;
@@ -239,10 +214,9 @@ cudaError_t launch_lut_listed(const LayerView &L, const Workspace &W, const void
                               bool down, bool reconstruct, int num_sms, cudaStream_t s);
 // out = / += / h + sum_i gate * (sum of the slot's down partials); one_part (optional)
 // marks slots whose output is partial 0 alone.
-// pdl: launched as a programmatic dependent of the kernel before it (the down kernel)
 cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h, int T,
                            const int32_t *idx, const float *gate, float *out, int mode,
-                           const uint8_t *one_part, int nparts, cudaStream_t s, bool pdl = false);
+                           const uint8_t *one_part, int nparts, cudaStream_t s);
 // Tokens per chunk of the grouped tensor-core path.
 constexpr int kGroupTokens = 128;
 // Default tokens an expert needs in one call to take the tensor-core path.

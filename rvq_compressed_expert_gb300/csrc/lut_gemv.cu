@@ -37,8 +37,6 @@ namespace {
 template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf>
 __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
     extern __shared__ __align__(16) unsigned char smem[];
-    grid_dep_wait();   // the routing (gate/up) or the gate/up partials (down) are complete
-    grid_dep_launch(); // the next phase may be scheduled as this one's CTAs leave
     const int n_slots = lut_slot_count(A);
     const int units = kDown ? n_slots * A.npair * A.nrb : n_slots * 2 * A.gu_pairs;
     int par = 0;
@@ -87,7 +85,6 @@ __global__ void __launch_bounds__(32 * kMaxTopK) combine_kernel(const float *__r
     const int t = blockIdx.y;
     const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 32 + lane;
-    grid_dep_wait(); // the down partials are complete
     if (stats && blockIdx.x == 0 && t == 0 && threadIdx.x == 0) atomicAdd(stats + kStatForwardSlots, slots);
     const int npair = NP ? NP : npair_rt;
     const size_t si = (size_t)t * k + i;
@@ -124,14 +121,13 @@ __global__ void __launch_bounds__(32 * kMaxTopK) combine_kernel(const float *__r
 }
 
 template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf>
-cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s, bool pdl) {
+cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
     const size_t smem = unit_smem<kRecon>();
     static SmemAttr attr;
     cudaError_t e = ensure_smem(attr, (const void *)lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf>, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = units < num_sms ? units : num_sms;
-    e = launch_k(lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf>, dim3(grid), dim3(kNT), smem, s, pdl, A);
-    if (e != cudaSuccess) return e;
+    lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf><<<grid, kNT, smem, s>>>(A);
     return cudaGetLastError();
 }
 
@@ -141,17 +137,16 @@ cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s, b
 // with two, 87.9 with three, 97.0 with none; 384 threads with a second register set for
 // the codes were slower).
 template <bool kDown, bool kRecon, bool kBf16>
-cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s, bool pdl) {
-    return launch_v<kDown, kRecon, kBf16, kThreads, kCodePingPong, kPrefetchRounds>(A, units, num_sms, s, pdl);
+cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
+    return launch_v<kDown, kRecon, kBf16, kThreads, kCodePingPong, kPrefetchRounds>(A, units, num_sms, s);
 }
 
 template <bool kDown>
-cudaError_t launch_var(const LutArgs &A, int units, bool recon, bool bf16, int num_sms, cudaStream_t s,
-                       bool pdl) {
-    if (recon) return bf16 ? launch_one<kDown, true, true>(A, units, num_sms, s, pdl)
-                           : launch_one<kDown, true, false>(A, units, num_sms, s, pdl);
-    return bf16 ? launch_one<kDown, false, true>(A, units, num_sms, s, pdl)
-                : launch_one<kDown, false, false>(A, units, num_sms, s, pdl);
+cudaError_t launch_var(const LutArgs &A, int units, bool recon, bool bf16, int num_sms, cudaStream_t s) {
+    if (recon) return bf16 ? launch_one<kDown, true, true>(A, units, num_sms, s)
+                           : launch_one<kDown, true, false>(A, units, num_sms, s);
+    return bf16 ? launch_one<kDown, false, true>(A, units, num_sms, s)
+                : launch_one<kDown, false, false>(A, units, num_sms, s);
 }
 
 } // namespace
@@ -202,9 +197,9 @@ LutArgs make_lut_args(const LayerView &L, const Workspace &W, const void *h, int
 }
 
 cudaError_t launch_lut_phase(const LutArgs &A, bool down, bool reconstruct, bool bf16, int num_sms,
-                             cudaStream_t s, bool pdl = false) {
-    if (!down) return launch_var<false>(A, A.slots * 2 * A.gu_pairs, reconstruct, bf16, num_sms, s, pdl);
-    return launch_var<true>(A, A.slots * A.npair * A.nrb, reconstruct, bf16, num_sms, s, pdl);
+                             cudaStream_t s) {
+    if (!down) return launch_var<false>(A, A.slots * 2 * A.gu_pairs, reconstruct, bf16, num_sms, s);
+    return launch_var<true>(A, A.slots * A.npair * A.nrb, reconstruct, bf16, num_sms, s);
 }
 
 cudaError_t launch_lut_listed(const LayerView &L, const Workspace &W, const void *h, int T,
@@ -218,15 +213,14 @@ cudaError_t launch_lut_listed(const LayerView &L, const Workspace &W, const void
 
 cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h, int T,
                            const int32_t *idx, const float *gate, float *out, int mode,
-                           const uint8_t *one_part, int nparts, cudaStream_t s, bool pdl) {
+                           const uint8_t *one_part, int nparts, cudaStream_t s) {
     const unsigned long long slots = (unsigned long long)T * L.k;
     dim3 grid((L.d + 31) / 32, T);
     const float *h32 = reinterpret_cast<const float *>(h);
     switch (nparts) {
 #define WM_COMBINE(NP)                                                                               \
-    if (cudaError_t e = launch_k(combine_kernel<NP>, grid, dim3(32 * L.k), 0, s, pdl, W.part_dn, idx, gate, h32, out, \
-                                 L.d, L.k, L.E, nparts, mode, W.stats, slots, one_part))                 \
-        return e
+    combine_kernel<NP><<<grid, 32 * L.k, 0, s>>>(W.part_dn, idx, gate, h32, out, L.d, L.k, L.E, nparts, \
+                                                        mode, W.stats, slots, one_part)
     case 1: WM_COMBINE(1); break;
     case 2: WM_COMBINE(2); break;
     case 3: WM_COMBINE(3); break;
@@ -249,19 +243,15 @@ cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const voi
     A.trace = trace;
     A.trace_cap = trace ? trace_cap : 0;
     const bool bf16 = L.act_bf16 != 0;
-    // the three launches as programmatic dependents, each scheduled while the kernel before it
-    // finishes (each waits for it before reading its output); not when per-kernel events are
-    // recorded between them
-    const bool pdl = tm == nullptr;
     if (tm) cudaEventRecord(tm->ev[0], s);
-    cudaError_t e = launch_lut_phase(A, false, reconstruct, bf16, num_sms, s, pdl);
+    cudaError_t e = launch_lut_phase(A, false, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[1], s);
     A.trace_base = A.slots * 2 * A.gu_pairs; // down units follow the gate/up units
-    e = launch_lut_phase(A, true, reconstruct, bf16, num_sms, s, pdl);
+    e = launch_lut_phase(A, true, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[2], s);
-    e = launch_combine(L, W, h, T, idx, gate, out, mode, nullptr, down_parts(L), s, pdl);
+    e = launch_combine(L, W, h, T, idx, gate, out, mode, nullptr, down_parts(L), s);
     if (e != cudaSuccess) return e;
     if (tm) {
         cudaEventRecord(tm->ev[3], s);

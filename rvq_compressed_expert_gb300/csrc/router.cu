@@ -237,7 +237,6 @@ __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__r
     __shared__ unsigned long long keys[128 * kRows];
     __shared__ int ids[128 * kRows];
     __shared__ int last;
-    grid_dep_launch(); // the expert kernels may be scheduled as this launch's CTAs leave
     const int row0 = blockIdx.x * kRows;
     const int rows = min(kRows, E - row0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
