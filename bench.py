@@ -1036,8 +1036,10 @@ def profile_case(args):
         w = synth.Workload("prefill-e32", 7168, 1536, 32, 16, 64, "bf16", "none")
     else:
         w = synth.Workload("decode-e32", 7168, 1536, 32, 16, 1, "f32", "offsets")
-    layer = MoELayer(w, seed=0, layer=0, device="cuda",
-                     flags=0 if (args.phases or args.prefill) else B.FLAG_STEP_KERNEL)
+    flags = 0 if (args.phases or args.prefill) else B.FLAG_STEP_KERNEL
+    if args.recon:
+        flags = B.FLAG_K2_RECONSTRUCT
+    layer = MoELayer(w, seed=0, layer=0, device="cuda", flags=flags)
     idx, gate, logits, y = layer.alloc_outputs(w.tokens)
     trace = None
     if args.trace:
@@ -1222,6 +1224,8 @@ def main():
                     help="run a small decode case for ncu captures and exit")
     ap.add_argument("--phases", action="store_true",
                     help="with --profile-case: one kernel per phase instead of the step kernel")
+    ap.add_argument("--recon", action="store_true",
+                    help="with --profile-case: the register-reconstruct form of the expert kernels")
     ap.add_argument("--trace", action="store_true",
                     help="with --profile-case: print the step kernel's item timeline")
     ap.add_argument("--profile-encoder", action="store_true",
