@@ -678,6 +678,8 @@ int waste_moe_stats(const waste_moe *h, waste_moe_stats_t *out) {
     if (err & kErrNotResident)
         return fail(WASTE_EINVAL, "an expert of a banked layer had no cache slot (cache too small?)");
     if (err & kErrBadExpert) return fail(WASTE_EINVAL, "forward saw an expert index outside [0, %d)", h->L.E);
+    if (err & kErrSmemLayout)
+        return fail(WASTE_ECUDA, "a lookup kernel found its shared memory at another address than probed");
     return ok();
 }
 

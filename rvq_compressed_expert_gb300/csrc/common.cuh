@@ -23,7 +23,7 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxFusedRowBlocks = 64; // down row blocks the fused step kernel can track
 
 // Sticky device error bits.
-enum : uint32_t { kErrBadExpert = 1u, kErrTimeout = 2u, kErrNotResident = 4u };
+enum : uint32_t { kErrBadExpert = 1u, kErrTimeout = 2u, kErrNotResident = 4u, kErrSmemLayout = 8u };
 
 // Record of expert e: by index, or through a bank's slot map (null when the expert has no
 // slot -- the caller treats it as an invalid expert).

@@ -4,6 +4,8 @@
 
 #include "common.cuh"
 
+#include <type_traits>
+
 
 namespace wm {
 namespace lut {
@@ -18,6 +20,7 @@ constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' c
 constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
 constexpr bool kCodePingPong = false;            // hold the next round's codes in registers
 constexpr int kPrefetchRounds = 1;                 // L2 prefetch distance in row-group rounds
+constexpr int kPrefetchRoundsGu = 2;               // the same for the per-phase gate/up kernel
 
 struct LutArgs {
     const uint8_t *records;
@@ -218,11 +221,41 @@ __device__ __forceinline__ float lds_stage(uint32_t a) {
     return v;
 }
 
+// Where the dynamic shared memory of a kernel without static shared memory starts in the
+// CTA's shared window.  A lookup kernel that finds its tables there folds the table base into
+// each table load's immediate offset (one instruction less per lookup); elsewhere it adds it.
+constexpr uint32_t kDynSmemBase = 1024;
+
+// Table load at shared-window address a + kDynSmemBase + S * 64 KiB: a is the PRMT result
+// alone (code byte and column offset), the base and stage offset the load's immediate.
+template <int S>
+__device__ __forceinline__ float lds_fixed(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(S * kTabStage + (int)kDynSmemBase));
+    return v;
+}
+
+// (d0, d1) = (a0 + b0, a1 + b1) as one packed fp32 addition, each lane rounded to nearest
+// like a scalar add.
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// fp32 -> TF32 by rounding the 13 dropped mantissa bits to nearest, ties away from zero:
+// adding half of the kept last place to the magnitude bits and clearing the dropped bits.
+// Exact for every finite input (a carry moves into the exponent as it should); the operands
+// here are finite.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+}
+
 // fp32 -> TF32 head plus TF32 tail (x ~ head + tail to about 2^-22 relative)
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-    const float rest = x - __uint_as_float(hi);
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(rest));
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - __uint_as_float(hi));
 }
 
 // d += a (16x8, row) * b (8x8, col), TF32 inputs, fp32 accumulate
@@ -287,7 +320,7 @@ extern __shared__ __align__(16) unsigned char lut_smem[];
 // codes of a part are asked for as soon as that part's lookups are issued (else at the top
 // of each round -- the persistent step kernel, whose other items leave no registers for it).
 template <bool kDown, bool kRecon, bool kBf16, int kNT = kThreads, bool kPing = kCodePingPong,
-          int kPf = kPrefetchRounds, bool kPartLoads = true>
+          int kPf = kPrefetchRounds, bool kPartLoads = true, bool kFixed = false>
 __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
                                       int &par, bool &primed, const unsigned *dep,
                                       unsigned dep_target, unsigned long long *t_tables = nullptr) {
@@ -325,7 +358,18 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
         }
     }
-    if (!valid && threadIdx.x == 0) atomicOr(A.err, (U.e >= 0 && U.e < A.E) ? kErrNotResident : kErrBadExpert);
+    if (!valid) {
+        // no codes to stream: the unit's rows get zero partials (the step reports the error)
+        if (threadIdx.x == 0) atomicOr(A.err, (U.e >= 0 && U.e < A.E) ? kErrNotResident : kErrBadExpert);
+        const int r1 = min(G.n_out, U.g1 * kGroupRows);
+        for (int row = U.g0 * kGroupRows + threadIdx.x; row < r1; row += kNT) {
+            if constexpr (!kDown)
+                A.part_gu[(((size_t)U.slot * A.gu_pairs + U.seg0 / 2) * 2 + U.mat) * G.n_out + row] = 0.f;
+            else
+                A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = 0.f;
+        }
+        return;
+    }
     const int t = U.slot / A.k;
     // ---- input vectors of this lane's column(s)
     float xv[2][kVec];
@@ -460,7 +504,6 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                     float4 ev = make_float4(dd[0][2 * hh], dd[1][2 * hh], dd[2][2 * hh], dd[3][2 * hh]);
                     float4 ov = make_float4(dd[0][2 * hh + 1], dd[1][2 * hh + 1], dd[2][2 * hh + 1],
                                             dd[3][2 * hh + 1]);
-                    if (!valid) ev = ov = make_float4(0.f, 0.f, 0.f, 0.f);
                     const int c = c0 + fg + 8 * hh;
                     float *row = tab + (((size_t)s * kCodes + c) * 2 + mp) * kSegVec;
                     *reinterpret_cast<float4 *>(row + 4 * g_first) = odd ? ov : ev;
@@ -491,8 +534,10 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     // the next row group's codes while the current one is consumed (ping-pong), and L2
     // is asked for the row group kPrefetchRounds rounds ahead -- past the end of the
     // unit, for the next unit's first row groups.
+    // a unit whose second segment lies past the matrix (an odd segment count) reads the first
+    // segment's codes again for it: that part's tables are zero (its inputs are)
     const uint8_t *pb0 = U.base[0];
-    const uint8_t *pb1 = U.base[1];
+    const uint8_t *pb1 = U.base[1] ? U.base[1] : U.base[0];
     // 32-bit shared-window address of the tables: a lookup is PRMT, IADD and one
     // ld.shared with the stage offset as its immediate
     const uint32_t tab32 = (uint32_t)__cvta_generic_to_shared(smem);
@@ -501,7 +546,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
             const size_t co = ((size_t)g * kStages + s) * 512 + (size_t)lane * 16;
-            w[p][s] = pb ? ld_stream(pb + co) : make_uint4(0, 0, 0, 0);
+            w[p][s] = ld_stream(pb + co);
         }
     };
     auto load = [&](int g, uint4 (&w)[2][kStages]) {
@@ -522,33 +567,61 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     // columns.
     auto reduce16 = [&](float (&acc)[16]) {
 #pragma unroll
-        for (int n = 8; n >= 1; n >>= 1)
+        for (int n = 8; n >= 2; n >>= 1)
 #pragma unroll
-            for (int i = 0; i < n; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + n], n);
+            for (int i = 0; i < n; i += 2) {
+                const float r0 = __shfl_xor_sync(0xffffffffu, acc[i + n], n);
+                const float r1 = __shfl_xor_sync(0xffffffffu, acc[i + n + 1], n);
+                add2(acc[i], acc[i + 1], acc[i], acc[i + 1], r0, r1);
+            }
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[1], 1);
         acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 16);
     };
-    // the lookups of part p of one row group: acc = (part 0) or += (part 1) the 16 partials
-    auto lookups = [&](const uint4 (&cwp)[kStages], int p, float (&acc)[16]) {
+    // the lookups of part p of one row group: acc = (part 0) or += (part 1) the 16 partials.
+    // Two code bytes at a time: their three stage entries are added pairwise with packed
+    // additions, in the order (T0 + T1) + T2, then into the partials.  fixed: the tables sit
+    // at kDynSmemBase, so a table address is the PRMT result alone.
+    auto lookups = [&](auto fixed, const uint4 (&cwp)[kStages], int p, float (&acc)[16]) {
+        constexpr bool kFixed = decltype(fixed)::value;
         const uint32_t colb = p ? colb1 : colb0;
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
             const uint32_t w0 = comp(cwp[0], wd), w1 = comp(cwp[1], wd), w2 = comp(cwp[2], wd);
+            if constexpr (!kRecon) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                float t;
-                if constexpr (!kRecon) {
-                    const uint32_t sel = 0x7604u | ((uint32_t)b << 4);
-                    const uint32_t a0 = __byte_perm(w0, colb, sel);
-                    const uint32_t a1 = __byte_perm(w1, colb, sel);
-                    const uint32_t a2 = __byte_perm(w2, colb, sel);
-                    const float t0 = lds_stage<0>(tab32 + a0);
-                    const float t1 = lds_stage<1>(tab32 + a1);
-                    const float t2 = lds_stage<2>(tab32 + a2);
-                    t = (t0 + t1) + t2;
-                } else {
-                    const float *cbs = reinterpret_cast<const float *>(smem) + p * kCbFloats;
-                    const int c0 = (w0 >> (8 * b)) & 255, c1 = (w1 >> (8 * b)) & 255,
-                              c2 = (w2 >> (8 * b)) & 255;
+                for (int bp = 0; bp < 2; ++bp) {
+                    float t0[2], t1[2], t2[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t sel = 0x7604u | ((uint32_t)(2 * bp + h) << 4);
+                        const uint32_t a0 = __byte_perm(w0, colb, sel);
+                        const uint32_t a1 = __byte_perm(w1, colb, sel);
+                        const uint32_t a2 = __byte_perm(w2, colb, sel);
+                        if constexpr (kFixed) {
+                            t0[h] = lds_fixed<0>(a0);
+                            t1[h] = lds_fixed<1>(a1);
+                            t2[h] = lds_fixed<2>(a2);
+                        } else {
+                            t0[h] = lds_stage<0>(tab32 + a0);
+                            t1[h] = lds_stage<1>(tab32 + a1);
+                            t2[h] = lds_stage<2>(tab32 + a2);
+                        }
+                    }
+                    float s0, s1;
+                    add2(s0, s1, t0[0], t0[1], t1[0], t1[1]);
+                    add2(s0, s1, s0, s1, t2[0], t2[1]);
+                    const int i = 4 * wd + 2 * bp;
+                    if (p == 1) add2(acc[i], acc[i + 1], acc[i], acc[i + 1], s0, s1);
+                    else {
+                        acc[i] = s0;
+                        acc[i + 1] = s1;
+                    }
+                }
+            } else {
+                const float *cbs = reinterpret_cast<const float *>(smem) + p * kCbFloats;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int c0 = (w0 >> (8 * b)) & 255, c1 = (w1 >> (8 * b)) & 255, c2 = (w2 >> (8 * b)) & 255;
                     const float4 *r0 = reinterpret_cast<const float4 *>(cbs + c0 * kVec);
                     const float4 *r1 = reinterpret_cast<const float4 *>(cbs + kCodes * kVec + c1 * kVec);
                     const float4 *r2 = reinterpret_cast<const float4 *>(cbs + 2 * kCodes * kVec + c2 * kVec);
@@ -562,10 +635,9 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                     sacc = fmaf((a1.y + b1.y) + d1.y, x[5], sacc);
                     sacc = fmaf((a1.z + b1.z) + d1.z, x[6], sacc);
                     sacc = fmaf((a1.w + b1.w) + d1.w, x[7], sacc);
-                    t = sacc;
+                    if (p == 1) acc[4 * wd + b] += sacc;
+                    else acc[4 * wd + b] = sacc;
                 }
-                if (p == 1) acc[4 * wd + b] += t;
-                else acc[4 * wd + b] = t;
             }
         }
     };
@@ -580,54 +652,71 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                 A.part_dn[((size_t)U.slot * A.npair + U.seg0 / 2) * G.n_out + row] = acc[0];
         }
     };
-    if constexpr (kPing) {
-        auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
-            float acc[16];
-            lookups(cw[0], 0, acc);
-            lookups(cw[1], 1, acc);
-            finish(acc, g);
-        };
-        uint4 wa[2][kStages], wb[2][kStages];
-        int g = U.g0 + warp;
-        if (g < U.g1) load(g, wa);
-        while (g < U.g1) {
-            if (g + kNW < U.g1) load(g + kNW, wb);
-            ahead(g);
-            consume(wa, g);
-            g += kNW;
-            if (g >= U.g1) break;
-            if (g + kNW < U.g1) load(g + kNW, wa);
-            ahead(g);
-            consume(wb, g);
-            g += kNW;
-        }
-    } else if constexpr (!kPartLoads) {
-        for (int g = U.g0 + warp; g < U.g1; g += kNW) {
+    auto stream = [&](auto fixed) {
+        if constexpr (kPing) {
+            auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
+                float acc[16];
+                lookups(fixed, cw[0], 0, acc);
+                lookups(fixed, cw[1], 1, acc);
+                finish(acc, g);
+            };
+            uint4 wa[2][kStages], wb[2][kStages];
+            int g = U.g0 + warp;
+            if (g < U.g1) load(g, wa);
+            while (g < U.g1) {
+                if (g + kNW < U.g1) load(g + kNW, wb);
+                ahead(g);
+                consume(wa, g);
+                g += kNW;
+                if (g >= U.g1) break;
+                if (g + kNW < U.g1) load(g + kNW, wa);
+                ahead(g);
+                consume(wb, g);
+                g += kNW;
+            }
+        } else if constexpr (!kPartLoads) {
+            for (int g = U.g0 + warp; g < U.g1; g += kNW) {
+                uint4 wa[2][kStages];
+                load(g, wa);
+                ahead(g);
+                float acc[16];
+                lookups(fixed, wa[0], 0, acc);
+                lookups(fixed, wa[1], 1, acc);
+                finish(acc, g);
+            }
+        } else {
+            // one set of code registers: as soon as a part's lookups are issued, the next row
+            // group's codes of that part are asked for into its registers, so each load has the
+            // rest of the round in front of it (lines are already on their way into L2).  The
+            // last round, which loads nothing, is peeled off the loop.
             uint4 wa[2][kStages];
-            load(g, wa);
-            ahead(g);
-            float acc[16];
-            lookups(wa[0], 0, acc);
-            lookups(wa[1], 1, acc);
-            finish(acc, g);
+            int g = U.g0 + warp;
+            if (g < U.g1) load(g, wa);
+            for (; g + kNW < U.g1; g += kNW) {
+                ahead(g);
+                float acc[16];
+                lookups(fixed, wa[0], 0, acc);
+                load_part(g + kNW, 0, wa);
+                lookups(fixed, wa[1], 1, acc);
+                load_part(g + kNW, 1, wa);
+                finish(acc, g);
+            }
+            if (g < U.g1) {
+                ahead(g);
+                float acc[16];
+                lookups(fixed, wa[0], 0, acc);
+                lookups(fixed, wa[1], 1, acc);
+                finish(acc, g);
+            }
         }
+    };
+    if constexpr (!kRecon && kFixed) {
+        // launched only where the tables were found at kDynSmemBase; anywhere else the
+        // unit reports the mismatch and streams nothing
+        if (tab32 == kDynSmemBase) stream(std::integral_constant<bool, true>{});
+        else if (threadIdx.x == 0) atomicOr(A.err, kErrSmemLayout);
     } else {
-        // one set of code registers: as soon as a part's lookups are issued, the next row
-        // group's codes of that part are asked for into its registers, so each load has the
-        // rest of the round in front of it (lines are already on their way into L2)
-        uint4 wa[2][kStages];
-        int g = U.g0 + warp;
-        if (g < U.g1) load(g, wa);
-        for (; g < U.g1; g += kNW) {
-            const int gn = g + kNW;
-            ahead(g);
-            float acc[16];
-            lookups(wa[0], 0, acc);
-            if (gn < U.g1) load_part(gn, 0, wa);
-            lookups(wa[1], 1, acc);
-            if (gn < U.g1) load_part(gn, 1, wa);
-            finish(acc, g);
-        }
+        stream(std::integral_constant<bool, false>{});
     }
     // algorithmic bytes of this unit: codes of its real (row, vector) pairs,
     // and the slot's codebooks once

@@ -34,7 +34,7 @@ using namespace lut;
 
 namespace {
 
-template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf>
+template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf, bool kFixed>
 __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int n_slots = lut_slot_count(A);
@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
         if (has_next) N = decode_unit<kDown>(A, u + gridDim.x);
         unsigned long long t0 = 0, t_tab[2] = {0, 0};
         if (A.trace && threadIdx.x == 0) t0 = gtimer();
-        run_unit<kDown, kRecon, kBf16, kNT, kPing && !kRecon, kPf>(A, U, has_next, N, par, primed, nullptr, 0,
-                                                                   A.trace ? t_tab : nullptr);
+        run_unit<kDown, kRecon, kBf16, kNT, kPing && !kRecon, kPf, true, kFixed>(A, U, has_next, N, par, primed,
+                                                                                 nullptr, 0, A.trace ? t_tab : nullptr);
         if (A.trace && threadIdx.x == 0 && A.trace_base + u < A.trace_cap) {
             unsigned smid;
             asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -120,25 +120,65 @@ __global__ void __launch_bounds__(32 * kMaxTopK) combine_kernel(const float *__r
     else out[o] = h[o] + y;
 }
 
-template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf>
+// Where a kernel without static shared memory finds its dynamic shared memory: written by a
+// one-thread probe, read once per device.
+__device__ unsigned g_dyn_smem_base;
+
+__global__ void smem_base_probe_kernel() {
+    if (threadIdx.x == 0) g_dyn_smem_base = (unsigned)__cvta_generic_to_shared(lut_smem);
+}
+
+// 0: not probed yet, 1: the tables sit at kDynSmemBase, 2: elsewhere.
+std::atomic<int> g_tables_fixed[kMaxDevices];
+
+// Whether the lookup kernels of the current device find their tables at kDynSmemBase (then
+// they take the table base as a load immediate).  Probed on stream s the first time it is
+// asked outside a stream capture; a captured call before that takes the general kernels.
+bool tables_at_fixed_base(cudaStream_t s) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    const int known = g_tables_fixed[dev].load(std::memory_order_acquire);
+    if (known) return known == 1;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return false;
+    const int smem = (int)unit_smem<false>();
+    static SmemAttr attr;
+    if (ensure_smem(attr, (const void *)smem_base_probe_kernel, smem) != cudaSuccess) return false;
+    smem_base_probe_kernel<<<1, 32, smem, s>>>();
+    unsigned base = ~0u;
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyFromSymbolAsync(&base, g_dyn_smem_base, sizeof base, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return false;
+    g_tables_fixed[dev].store(base == kDynSmemBase ? 1 : 2, std::memory_order_release);
+    return base == kDynSmemBase;
+}
+
+template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf, bool kFixed>
 cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
     const size_t smem = unit_smem<kRecon>();
     static SmemAttr attr;
-    cudaError_t e = ensure_smem(attr, (const void *)lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf>, (int)smem);
+    cudaError_t e =
+        ensure_smem(attr, (const void *)lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf, kFixed>, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = units < num_sms ? units : num_sms;
-    lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf><<<grid, kNT, smem, s>>>(A);
+    lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf, kFixed><<<grid, kNT, smem, s>>>(A);
     return cudaGetLastError();
 }
 
 // The per-phase lookup kernels: 512 threads; the next round's codes of a part are loaded
-// as soon as that part's lookups are issued, and L2 is asked for the round after (measured
-// on GB300 at the decode shape: step 85.0 us with a prefetch distance of one round, 86.9
-// with two, 87.9 with three, 97.0 with none; 384 threads with a second register set for
-// the codes were slower).
+// as soon as that part's lookups are issued, and L2 is asked for the rounds ahead (measured
+// on GB300 at the decode shape, same box, interleaved runs: gate/up 42.9 us with L2 two
+// rounds ahead against 44.3 with one; down 24.6 us with one against 26.6 with two; earlier,
+// before the lookups took fewer instructions, one round was best for both; 384 threads with
+// a second register set for the codes were slower).
 template <bool kDown, bool kRecon, bool kBf16>
 cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
-    return launch_v<kDown, kRecon, kBf16, kThreads, kCodePingPong, kPrefetchRounds>(A, units, num_sms, s);
+    constexpr int kPf = kDown ? kPrefetchRounds : kPrefetchRoundsGu;
+    if constexpr (!kRecon)
+        if (tables_at_fixed_base(s))
+            return launch_v<kDown, false, kBf16, kThreads, kCodePingPong, kPf, true>(A, units, num_sms, s);
+    return launch_v<kDown, kRecon, kBf16, kThreads, kCodePingPong, kPf, false>(A, units, num_sms, s);
 }
 
 template <bool kDown>
