@@ -333,6 +333,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
         G * grouped_tile_rows((int)S, (int)max_chunks) * ((L.d + 63) / 64) * 128, // grp.xg
         G * grouped_tile_rows((int)S, (int)max_chunks) * ((L.f + 63) / 64) * 128, // grp.ag
         (T > 16 ? (size_t)kRouterMaxSplits * T * E * 4 : 0), // router_part
+        (size_t)E * 8,                              // route_slots
     };
     const int n_parts = (int)(sizeof sizes / sizeof sizes[0]);
     size_t offs[32], total = 0;
@@ -377,6 +378,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     Gp.ag = grouped ? reinterpret_cast<uint8_t *>(b + offs[21]) : nullptr;
     Gp.max_chunks = grouped ? (int)max_chunks : 0;
     W.router_part = T > 16 ? reinterpret_cast<float *>(b + offs[22]) : nullptr;
+    W.route_slots = reinterpret_cast<unsigned long long *>(b + offs[23]);
     ce = cudaMemset(base, 0, total);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
     if (ce != cudaSuccess) {
@@ -469,7 +471,7 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
     const unsigned long long router_bytes = (unsigned long long)h->L.E * (unsigned long long)h->L.d * 4ull;
     const int pred_stride = h->pred_P > 0 ? h->pred_P : 1;
     RouteTopk F{h->W.route_done, h->L.k, d_idx, d_gate, h->W.pred_idx, h->W.pred_count, pred_stride, h->W.stats,
-                router_bytes};
+                router_bytes, h->W.route_slots};
     bool fused = false;
     cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s, h->W.router_part, h->num_sms, &F, &fused,
                                   h->W.err);
@@ -688,6 +690,8 @@ int waste_moe_reset_stats(waste_moe *h) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemset(h->W.stats, 0, kStatCount * 8);
     if (e == cudaSuccess) e = cudaMemset(h->W.err, 0, 4);
+    // a timed-out call may have left selection keys behind
+    if (e == cudaSuccess) e = cudaMemset(h->W.route_slots, 0, (size_t)h->L.E * 8);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "resetting statistics");
     return ok();

@@ -141,6 +141,7 @@ struct RouteTopk {
     int pred_stride;
     unsigned long long *stats;
     unsigned long long router_bytes;
+    unsigned long long *slots; // [E] one-token router: each expert's selection key, 0 at rest
 };
 
 // Slots of a batched call grouped by expert (see grouped.cu).
@@ -174,6 +175,7 @@ struct Workspace {
     int32_t *bank_wait;  // [max_slots] banked calls: job each slot's record arrives by, or -1
     int32_t *bank_order; // [max_slots] banked calls: slots in the order their units run
     unsigned *route_done; // router CTAs finished (the router launch that also takes the top-k)
+    unsigned long long *route_slots; // [E] one-token router's selection keys, zero at rest
     Grouping grp;        // batched calls only (null pointers when max_tokens == 1)
     float *router_part;  // [kRouterMaxSplits][max_T][E] when max_T > 16, else null
     void *base;

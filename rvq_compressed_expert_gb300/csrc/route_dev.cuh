@@ -337,9 +337,6 @@ __device__ __forceinline__ float key_float(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
 }
 
-// Top-k and softmax of token t by a whole CTA: a bitonic sort of the E experts on the key
-// (logit hi, then lo, descending; index ascending), then warp 0 forms the gates exactly
-// as topk_warp does.  keys/ids: shared scratch of >= next_pow2(E) entries each.
 // A routing candidate: 64-bit key (total-order image of the logit, then of its
 // remainder) and the expert index; a comes before b in the selection order when its key
 // is larger, or equal with a lower index.
@@ -384,20 +381,100 @@ __device__ __forceinline__ Cand warp_merge32(const Cand &a, const Cand &b) {
     return v;
 }
 
+// Selection key of a logit a and its remainder b: NaN ranks as -inf, -0 as +0, and a NaN or
+// zero remainder as +0.  Never 0 (the key of -inf is above it), so 0 marks "no key yet".
+__device__ __forceinline__ unsigned long long cand_key(float a, float b) {
+    if (a != a) a = -INFINITY;
+    if (a == 0.f) a = 0.f;
+    if (b != b || b == 0.f) b = 0.f;
+    return ((unsigned long long)float_key(a) << 32) | float_key(b);
+}
+
 __device__ __forceinline__ Cand load_cand(const float *lrow, const float *lo_row, int E, int i) {
     Cand c;
     c.key = 0ull; // below every real logit (-inf maps above 0)
     c.id = 0x7fffffff;
     if (i < E) {
         // L2 loads: the logits may come from other CTAs of the same launch
-        float a = __ldcg(lrow + i), b = lo_row ? __ldcg(lo_row + i) : 0.f;
-        if (a != a) a = -INFINITY;
-        if (a == 0.f) a = 0.f;
-        if (b != b || b == 0.f) b = 0.f;
-        c.key = ((unsigned long long)float_key(a) << 32) | float_key(b);
+        const float a = __ldcg(lrow + i), b = lo_row ? __ldcg(lo_row + i) : 0.f;
+        c.key = cand_key(a, b);
         c.id = i;
     }
     return c;
+}
+
+// The gates of a selected list: keys / ids hold the k first candidates in selection order;
+// warp 0 forms the softmax over them and writes idx and gate of token t (and, with a
+// prediction, counts its hits: P and pred_l as warp 0 read them).  real = false runs the very
+// same instructions (a pass that only brings the code into the instruction caches): its idx
+// and gate stores are overwritten by the real pass, and it adds zero to the counters.
+__device__ __forceinline__ void topk_emit(const unsigned long long *keys, const int *ids, int k, int t,
+                                          int32_t *__restrict__ idx, float *__restrict__ gate, int P, int pred_l,
+                                          int32_t *__restrict__ pred_count, unsigned long long *__restrict__ stats,
+                                          unsigned long long router_bytes, bool real = true) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int my_idx = -1;
+        float my_hi = 0.f, my_lo = 0.f;
+        if (lane < k) {
+            // the selected logit and remainder, as load_cand normalised them, back from the key
+            my_idx = ids[lane];
+            const unsigned long long key = keys[lane];
+            my_hi = key_float((uint32_t)(key >> 32));
+            my_lo = key_float((uint32_t)key);
+        }
+        const float h0 = __shfl_sync(0xffffffffu, my_hi, 0);
+        const float l0 = __shfl_sync(0xffffffffu, my_lo, 0);
+        const float diff = (lane == 0) ? 0.f : __fsub_rn(my_hi, h0) + __fsub_rn(my_lo, l0);
+        float ex = (lane < k) ? expf(diff) : 0.f;
+        float sum = ex;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane < k) {
+            idx[(size_t)t * k + lane] = my_idx;
+            gate[(size_t)t * k + lane] = ex / sum;
+        }
+        if (pred_count != nullptr) {
+            bool hit = false;
+            for (int p = 0; p < P && p < 32; ++p) hit |= (__shfl_sync(0xffffffffu, pred_l, p) == my_idx);
+            hit = hit && lane < k;
+            const unsigned hits = __popc(__ballot_sync(0xffffffffu, hit));
+            __syncwarp();
+            if (lane == 0) {
+                if (P > 0) atomicAdd(stats + kStatPredHits, real ? (unsigned long long)hits : 0ull);
+                pred_count[t] = 0;
+            }
+        }
+        if (lane == 0 && stats) {
+            atomicAdd(stats + kStatRoutedSlots, real ? (unsigned long long)k : 0ull);
+            if (t == 0) atomicAdd(stats + kStatRouter, real ? router_bytes : 0ull);
+        }
+    }
+    __syncthreads();
+}
+
+// The warps' lists (each warp's 32 candidates in selection order, one per lane) merged
+// pairwise through shared memory: keys / ids (32 entries per warp) end with the first 32 of
+// all, in order, at entries 0..31.
+__device__ __forceinline__ void merge_warp_lists(const Cand &best, unsigned long long *keys, int *ids) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    keys[warp * 32 + lane] = best.key;
+    ids[warp * 32 + lane] = best.id;
+    for (int span = 1; span < nw; span <<= 1) {
+        __syncthreads();
+        if ((warp % (2 * span)) == 0 && warp + span < nw) {
+            Cand a, b;
+            a.key = keys[warp * 32 + lane];
+            a.id = ids[warp * 32 + lane];
+            b.key = keys[(warp + span) * 32 + lane];
+            b.id = ids[(warp + span) * 32 + lane];
+            const Cand m = warp_merge32(a, b);
+            __syncwarp();
+            keys[warp * 32 + lane] = m.key;
+            ids[warp * 32 + lane] = m.id;
+        }
+    }
+    __syncthreads();
 }
 
 // Top-k (k <= 32) of one token's logits by the whole CTA: each warp keeps the first 32
@@ -437,63 +514,8 @@ __device__ __forceinline__ void topk_block(const float *__restrict__ logits,
                 best = warp_merge32(best, v[q]);
             }
     }
-    keys[warp * 32 + lane] = best.key;
-    ids[warp * 32 + lane] = best.id;
-    for (int span = 1; span < nw; span <<= 1) {
-        __syncthreads();
-        if ((warp % (2 * span)) == 0 && warp + span < nw) {
-            Cand a, b;
-            a.key = keys[warp * 32 + lane];
-            a.id = ids[warp * 32 + lane];
-            b.key = keys[(warp + span) * 32 + lane];
-            b.id = ids[(warp + span) * 32 + lane];
-            const Cand m = warp_merge32(a, b);
-            __syncwarp();
-            keys[warp * 32 + lane] = m.key;
-            ids[warp * 32 + lane] = m.id;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int my_idx = -1;
-        float my_hi = 0.f, my_lo = 0.f;
-        if (lane < k) {
-            // the selected logit and remainder, as load_cand normalised them, back from the key
-            my_idx = ids[lane];
-            const unsigned long long key = keys[lane];
-            my_hi = key_float((uint32_t)(key >> 32));
-            my_lo = key_float((uint32_t)key);
-        }
-        const float h0 = __shfl_sync(0xffffffffu, my_hi, 0);
-        const float l0 = __shfl_sync(0xffffffffu, my_lo, 0);
-        const float diff = (lane == 0) ? 0.f : __fsub_rn(my_hi, h0) + __fsub_rn(my_lo, l0);
-        float ex = (lane < k) ? expf(diff) : 0.f;
-        float sum = ex;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane < k) {
-            idx[(size_t)t * k + lane] = my_idx;
-            gate[(size_t)t * k + lane] = ex / sum;
-        }
-        if (pred_count != nullptr) {
-            bool hit = false;
-            for (int p = 0; p < P && p < 32; ++p) hit |= (__shfl_sync(0xffffffffu, pred_l, p) == my_idx);
-            hit = hit && lane < k;
-            const unsigned hits = __popc(__ballot_sync(0xffffffffu, hit));
-            __syncwarp();
-            if (lane == 0) {
-                if (P > 0) atomicAdd(stats + kStatPredHits, (unsigned long long)hits);
-                pred_count[t] = 0;
-            }
-        }
-        if (lane == 0 && stats) {
-            atomicAdd(stats + kStatRoutedSlots, (unsigned long long)k);
-            if (t == 0) atomicAdd(stats + kStatRouter, router_bytes);
-        }
-    }
-    __syncthreads();
+    merge_warp_lists(best, keys, ids);
+    topk_emit(keys, ids, k, t, idx, gate, P, pred_l, pred_count, stats, router_bytes);
 }
-
 } // namespace route
 } // namespace wm

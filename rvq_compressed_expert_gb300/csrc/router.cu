@@ -214,6 +214,76 @@ __device__ __forceinline__ unsigned count_acq_rel(unsigned *c) {
     return old;
 }
 
+__device__ __forceinline__ unsigned long long route_gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// The top-k CTA of the polled one-token router: thread i waits (bounded, about a second) for
+// expert i's selection key in slots[i] (0 = not yet written; one 64-bit store by the CTA that
+// owns the row, read as one), clears the slot for the next call, and the CTA selects and
+// gates (each warp sorts its 32 candidates, the lists are merged pairwise, as topk_block
+// does).  While the row CTAs still work, a first pass runs the same selection on placeholder
+// keys and stores nothing: only this CTA runs that code, which otherwise comes cold from
+// memory (measured on GB300: the selection 0.6 us faster after the pass).  If a key never arrives, the timeout is latched, the token's experts are set
+// to -1 (no expert: its slots contribute nothing) and no gates are formed.
+__device__ __forceinline__ void route_poll_topk(int E, const RouteTopk F, uint32_t *err, unsigned long long *lk,
+                                                int *li) {
+    // warp 0 asks for the token's predicted experts now; they arrive during the wait
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int P = 0, pred_l = -1;
+    if (warp == 0 && F.pred_count != nullptr) {
+        P = F.pred_count[0];
+        if (lane < F.pred_stride && lane < P) pred_l = F.pred_idx[lane];
+    }
+    const int i = threadIdx.x;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool real = pass == 1;
+        Cand c;
+        c.key = 0ull;
+        c.id = 0x7fffffff;
+        bool got = true;
+        if (i < E) {
+            unsigned long long v = 1ull + (unsigned long long)i; // placeholder key of the first pass
+            if (real) {
+                const unsigned long long t0 = route_gtimer();
+                while ((v = ld_relaxed_u64(F.slots + i)) == 0ull) {
+                    if (route_gtimer() - t0 > 1000000000ull) {
+                        got = false;
+                        break;
+                    }
+                }
+                if (got) st_relaxed_u64(F.slots + i, 0ull);
+            }
+            if (got) {
+                c.key = v;
+                c.id = i;
+            }
+        }
+        if (!__syncthreads_and(got ? 1 : 0)) {
+            if (threadIdx.x == 0 && err) atomicOr(err, kErrTimeout);
+            if (threadIdx.x < F.k) {
+                F.idx[threadIdx.x] = -1;
+                F.gate[threadIdx.x] = 0.f;
+            }
+            return;
+        }
+        warp_sort32(c);
+        merge_warp_lists(c, lk, li);
+        topk_emit(lk, li, F.k, 0, F.idx, F.gate, P, pred_l, F.pred_count, F.stats, F.router_bytes, real);
+    }
+}
+
 // One token (decode): kRows expert rows per CTA of 128 threads (4 warps) per row.  Thread 0
 // moves the rows of W_r and the token's h into shared memory with bulk copies (all of the
 // rows' bytes in flight at once); the lanes then form router_block_staged's products in its
@@ -222,8 +292,10 @@ __device__ __forceinline__ unsigned count_acq_rel(unsigned *c) {
 // set, the last CTA to count itself also takes the top-k and gates; the count is one
 // acquire-release atomic (no separate fences).  A copy that does not land within the
 // bounded wait sets kErrTimeout in err; the CTA still counts itself, so the counter comes
-// back to rest.
-template <bool kBf16, int kRows>
+// back to rest.  kPoll (a cooperative launch: every CTA resident at once): the row CTAs
+// instead store each row's selection key into F.slots, and one more CTA (the last) waits for
+// them and takes the top-k (route_poll_topk): no counter round trip, no re-read of the logits.
+template <bool kBf16, int kRows, bool kPoll>
 __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__restrict__ W,
                                                                 const float *__restrict__ bias,
                                                                 const void *__restrict__ h, int E, int d,
@@ -237,6 +309,12 @@ __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__r
     __shared__ unsigned long long keys[128 * kRows];
     __shared__ int ids[128 * kRows];
     __shared__ int last;
+    if constexpr (kPoll) {
+        if (blockIdx.x == gridDim.x - 1) {
+            route_poll_topk(E, F, err, keys, ids);
+            return;
+        }
+    }
     const int row0 = blockIdx.x * kRows;
     const int rows = min(kRows, E - row0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -263,8 +341,9 @@ __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__r
         // The copies never landed: the staged rows are not to be read.  No logits are
         // written; the CTA still counts itself so the counter returns to rest, and the last
         // CTA leaves the top-k alone (the timeout is latched; the copies may still be in
-        // flight, so the context is to be treated as unusable).
-        if (!F.done) return;
+        // flight, so the context is to be treated as unusable).  Polled: the top-k CTA's wait
+        // for this CTA's keys runs out instead.
+        if (kPoll || !F.done) return;
         __syncthreads();
         if (threadIdx.x == 0 && count_acq_rel(F.done) == gridDim.x - 1) *F.done = 0u;
         return;
@@ -309,8 +388,9 @@ __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__r
         if (bias) two_sum(v, bias[r], hi, lo);
         logits[r] = hi;
         if (logits_lo) logits_lo[r] = lo;
+        if constexpr (kPoll) st_relaxed_u64(F.slots + r, cand_key(hi, lo));
     }
-    if (!F.done) return;
+    if (kPoll || !F.done) return;
     __syncthreads(); // this CTA's logits before its count
     if (threadIdx.x == 0) {
         last = count_acq_rel(F.done) == gridDim.x - 1;
@@ -439,6 +519,23 @@ constexpr size_t kT1SmemMax = 160 * 1024;
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
+// Whether `ctas` CTAs of the one-token router can all be resident at once on the current
+// device (one per SM: each holds over 100 KiB of shared memory) and the device takes
+// cooperative launches: the polled form's top-k CTA waits for the others.
+static bool t1_poll_fits(int ctas, int num_sms) {
+    static std::atomic<int> coop[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    int c = coop[dev].load(std::memory_order_acquire);
+    if (c == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) v = 0;
+        c = v ? 1 : 2;
+        coop[dev].store(c, std::memory_order_release);
+    }
+    return c == 1 && ctas <= num_sms;
+}
+
 int router_splits(int T, int E, int d, int num_sms) {
     const int tiles = ((E + kTileE - 1) / kTileE) * ((T + kTileT - 1) / kTileT);
     int ns = (2 * num_sms + tiles - 1) / tiles;
@@ -472,19 +569,42 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
         // (another stream, no fuse) does on the staged kernel's 28 KiB (the same logits)
         const size_t t1_smem = (size_t)L.d * (4 * kT1Rows + (L.act_bf16 ? 2 : 4));
         if (T == 1 && fuse && fused && t1_smem <= kT1SmemMax && aligned16(L.router_w) && aligned16(h)) {
+            const RouteTopk F = *fuse;
+            const int grid1 = (L.E + kT1Rows - 1) / kT1Rows;
+            if (F.slots && L.E <= 128 * kT1Rows && t1_poll_fits(grid1 + 1, num_sms)) {
+                // polled: the row CTAs and one top-k CTA, resident together
+                static SmemAttr attr_p[2];
+                const void *kfn = L.act_bf16 ? (const void *)router_t1_kernel<true, kT1Rows, true>
+                                             : (const void *)router_t1_kernel<false, kT1Rows, true>;
+                ea = ensure_smem(attr_p[L.act_bf16 ? 1 : 0], kfn, (int)kT1SmemMax);
+                if (ea != cudaSuccess) return ea;
+                cudaLaunchConfig_t lc = {};
+                lc.gridDim = dim3(grid1 + 1);
+                lc.blockDim = dim3(128 * kT1Rows);
+                lc.dynamicSmemBytes = t1_smem;
+                lc.stream = s;
+                cudaLaunchAttribute at[1];
+                at[0].id = cudaLaunchAttributeCooperative;
+                at[0].val.cooperative = 1;
+                lc.attrs = at;
+                lc.numAttrs = 1;
+                if (L.act_bf16)
+                    return cudaLaunchKernelEx(&lc, router_t1_kernel<true, kT1Rows, true>, L.router_w, L.router_b, h,
+                                              L.E, L.d, logits, logits_lo, F, err);
+                return cudaLaunchKernelEx(&lc, router_t1_kernel<false, kT1Rows, true>, L.router_w, L.router_b, h,
+                                          L.E, L.d, logits, logits_lo, F, err);
+            }
             static SmemAttr attr_t1[2];
             ea = ensure_smem(attr_t1[L.act_bf16 ? 1 : 0],
-                             L.act_bf16 ? (const void *)router_t1_kernel<true, kT1Rows>
-                                        : (const void *)router_t1_kernel<false, kT1Rows>,
+                             L.act_bf16 ? (const void *)router_t1_kernel<true, kT1Rows, false>
+                                        : (const void *)router_t1_kernel<false, kT1Rows, false>,
                              (int)kT1SmemMax);
             if (ea != cudaSuccess) return ea;
-            const RouteTopk F = fuse ? *fuse : RouteTopk{};
-            const dim3 grid1((L.E + kT1Rows - 1) / kT1Rows);
             if (L.act_bf16)
-                router_t1_kernel<true, kT1Rows><<<grid1, 128 * kT1Rows, t1_smem, s>>>(
+                router_t1_kernel<true, kT1Rows, false><<<grid1, 128 * kT1Rows, t1_smem, s>>>(
                     L.router_w, L.router_b, h, L.E, L.d, logits, logits_lo, F, err);
             else
-                router_t1_kernel<false, kT1Rows><<<grid1, 128 * kT1Rows, t1_smem, s>>>(
+                router_t1_kernel<false, kT1Rows, false><<<grid1, 128 * kT1Rows, t1_smem, s>>>(
                     L.router_w, L.router_b, h, L.E, L.d, logits, logits_lo, F, err);
             return cudaGetLastError();
         }
