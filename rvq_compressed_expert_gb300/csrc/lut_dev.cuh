@@ -311,7 +311,9 @@ __device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target,
 extern __shared__ __align__(16) unsigned char lut_smem[];
 
 // One unit: tables (or staged codebooks) for the unit's segment(s), then the stream of
-// its rows.  `par`/`primed` carry the codebook stage buffers across consecutive units of
+// its rows.  `primed`: this unit's codebooks were already asked for by the previous unit of
+// the CTA (else they are asked for at the start, ahead of the down units' input and the
+// table build).  `par` carries the codebook stage buffers across consecutive units of
 // one kind: when `has_next`, the next unit's stages 0 and 1 are already on their way
 // into the buffers when this one returns.  For a down unit, `dep` (if not null) is a
 // completion counter that must reach dep_target before the gate/up partials are read.
@@ -348,6 +350,15 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         const int g = U.g0 + warp + i * kNW;
         if (g < U.g1) prefetch_group(U, g, lane);
     }
+    if (!kRecon && !primed && warp == 1) {
+        // the CTA's first unit: its codebooks come from HBM; ask for them now, so that they
+        // arrive under the down units' input and the loads of the table build hit L2
+        const float *q0, *q1;
+        unit_codebooks<kDown>(A, U, q0, q1);
+        (void)q1;
+        prefetch_l2_range(reinterpret_cast<const uint8_t *>(q0), (size_t)kCbFloats * sizeof(float), lane);
+    }
+    primed = !kRecon && has_next;
     if (!kRecon && has_next) {
         const float *q0, *q1;
         unit_codebooks<kDown>(A, N, q0, q1);
@@ -358,6 +369,45 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
         }
     }
+    // down: a = silu(gate) * up for the 64 vectors of this unit into xs, reduced over the
+    // gate/up segment pairs in a fixed order (the loads of 16 pairs in flight at a time).  It
+    // reads only the slot's gate/up partials, so where nothing is waited for (the per-phase
+    // kernels) it goes first, under the load of the expert index that the rest needs.
+    bool input_done = false;
+    auto swiglu_input = [&]() {
+        __syncthreads(); // xs may still be read by the previous unit
+        if (dep) wait_counter(dep, dep_target, A.err);
+        for (int i = threadIdx.x; i < 2 * kSegVec * kVec; i += kNT) {
+            const int r = U.seg0 * kSegVec * kVec + i; // index into f
+            float a = 0.f;
+            if (r < A.gu.n_out) {
+                const float *pg = A.part_gu + (size_t)U.slot * A.gu_pairs * 2 * A.gu.n_out + r;
+                const size_t step = (size_t)2 * A.gu.n_out;
+                float zg = 0.f, zu = 0.f;
+                for (int s0 = 0; s0 < A.gu_pairs; s0 += 16) {
+                    float vg[16], vu[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int sg = min(s0 + q, A.gu_pairs - 1);
+                        vg[q] = pg[sg * step];
+                        vu[q] = pg[sg * step + A.gu.n_out];
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (s0 + q < A.gu_pairs) {
+                            zg += vg[q];
+                            zu += vu[q];
+                        }
+                }
+                a = zg / (1.0f + expf(-zg)) * zu;
+            }
+            xs[i] = a;
+        }
+        __syncthreads();
+        input_done = true;
+    };
+    if constexpr (kDown)
+        if (!dep) swiglu_input();
     if (!valid) {
         // no codes to stream: the unit's rows get zero partials (the step reports the error)
         if (threadIdx.x == 0) atomicOr(A.err, (U.e >= 0 && U.e < A.E) ? kErrNotResident : kErrBadExpert);
@@ -384,37 +434,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             }
         }
     } else {
-        // a = silu(gate) * up for the 64 vectors of this unit, reduced over the gate/up
-        // segment pairs in a fixed order (the loads of 32 pairs in flight at a time)
-        __syncthreads(); // xs may still be read by the previous unit
-        if (dep) wait_counter(dep, dep_target, A.err);
-        for (int i = threadIdx.x; i < 2 * kSegVec * kVec; i += kNT) {
-            const int r = U.seg0 * kSegVec * kVec + i; // index into f
-            float a = 0.f;
-            if (valid && r < A.gu.n_out) {
-                const float *pg = A.part_gu + (size_t)U.slot * A.gu_pairs * 2 * A.gu.n_out + r;
-                const size_t step = (size_t)2 * A.gu.n_out;
-                float zg = 0.f, zu = 0.f;
-                for (int s0 = 0; s0 < A.gu_pairs; s0 += 32) {
-                    float vg[32], vu[32];
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int sg = min(s0 + q, A.gu_pairs - 1);
-                        vg[q] = pg[sg * step];
-                        vu[q] = pg[sg * step + A.gu.n_out];
-                    }
-#pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        if (s0 + q < A.gu_pairs) {
-                            zg += vg[q];
-                            zu += vu[q];
-                        }
-                }
-                a = zg / (1.0f + expf(-zg)) * zu;
-            }
-            xs[i] = a;
-        }
-        __syncthreads();
+        if (!input_done) swiglu_input();
 #pragma unroll
         for (int p = 0; p < 2; ++p)
 #pragma unroll
@@ -526,7 +546,6 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         __syncthreads();
     }
     (void)par;
-    (void)primed;
 
     if (t_tables && threadIdx.x == 0) t_tables[0] = gtimer();
 
