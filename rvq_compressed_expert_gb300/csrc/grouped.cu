@@ -260,14 +260,16 @@ constexpr uint32_t kOffCb = 0;
 constexpr uint32_t kOffB = kOffCb + kCbBytes;
 constexpr uint32_t kOffSeg = kOffB + kBRing * kBBytes;
 constexpr uint32_t kOffSlot = kOffSeg + kSegRing * kSegBytes;
-constexpr uint32_t kOffBar = (kOffSlot + kGroupTokens * 4 + 7) & ~7u;
-// barrier indices
+// two slot lists: the down kernel takes an item's epilogue under the next item's decode
+constexpr uint32_t kOffBar = (kOffSlot + 2 * kGroupTokens * 4 + 7) & ~7u;
+// barrier indices (two accumulators' full / empty pairs: gate/up uses the first only)
 enum { kSegFull = 0, kSegEmpty = kSegRing, kBFull = 2 * kSegRing, kBEmpty = kBFull + kBRing, kAFull = kBEmpty + kBRing,
-       kAEmpty = kAFull + kARing, kAccFull = kAEmpty + kARing, kAccEmpty = kAccFull + 1, kNumBars = kAccEmpty + 1 };
+       kAEmpty = kAFull + kARing, kAccFull = kAEmpty + kARing, kAccEmpty = kAccFull + 2, kNumBars = kAccEmpty + 2 };
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kMmaSmem = kOffMisc + 16;
-// tensor memory: [0, 256) the gate and up accumulators (128 columns each), [256, 512) the
-// weight tiles (kARing x 32 columns: 128 rows x 64 fp16 weights each)
+// tensor memory: [0, 256) the gate and up accumulators (128 columns each; down: two
+// accumulators used by alternate items), [256, 512) the weight tiles (kARing x 32 columns:
+// 128 rows x 64 fp16 weights each)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemA = 2 * kGroupTokens;
 static_assert(kMmaSmem <= 227 * 1024, "shared memory of the tensor-core kernel");
@@ -384,8 +386,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             tc::mbar_init(bar(kAFull + i), kDecWarps);
             tc::mbar_init(bar(kAEmpty + i), 1);
         }
-        tc::mbar_init(bar(kAccFull), 1);
-        tc::mbar_init(bar(kAccEmpty), kDecWarps);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(kAccFull + i), 1);
+            tc::mbar_init(bar(kAccEmpty + i), kDecWarps);
+        }
         tc::mbar_init_fence();
         *abort_flag = 0;
     }
@@ -489,10 +493,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             const int4 ch = A.chunks[item / nmb];
             const int npad = pad16(ch.z);
             const uint32_t idesc = tc::idesc_f16_f32(kBM, npad);
-            if (it >= 1) wait_phase_warp(bar(kAccEmpty), (it - 1) & 1, abort_flag);
+            // down: item it accumulates into buffer it & 1, free once item it - 2's epilogue is done
+            const int ba = kDown ? (int)(it & 1) : 0;
+            if (kDown ? it >= 2 : it >= 1)
+                wait_phase_warp(bar(kAccEmpty + ba), kDown ? ((it - 2) >> 1) & 1 : (it - 1) & 1, abort_flag);
             tc::fence_after_sync();
             for (int pass = 0; pass < kPasses; ++pass) {
-                const uint32_t acc = tmem + (uint32_t)(kDown ? 0 : pass_mat<kDown>(it, pass)) * kGroupTokens;
+                const uint32_t acc = tmem + (uint32_t)(kDown ? ba : pass_mat<kDown>(it, pass)) * kGroupTokens;
                 for (int kc = 0; kc < KC; ++kc, ++q) {
                     const int ab = q % kARing, rs = q % kBRing;
                     wait_phase_warp(bar(kAFull + ab), (q / kARing) & 1, abort_flag);
@@ -512,7 +519,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                 }
             }
             if (lane == 0) {
-                tc::mma_commit(bar(kAccFull));
+                tc::mma_commit(bar(kAccFull + ba));
                 if (A.stats) {
                     const int mb = item % nmb;
                     const int rows = min(G.n_out - mb * kBM, kBM);
@@ -525,7 +532,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             __syncwarp();
         }
         // drain: every MMA issued has completed before TMEM is released
-        if (it >= 1) wait_phase_warp(bar(kAccFull), (it - 1) & 1, abort_flag, false);
+        if (it >= 1) {
+            const uint32_t last = it - 1;
+            wait_phase_warp(bar(kAccFull + (kDown ? (int)(last & 1) : 0)), kDown ? (last >> 1) & 1 : last & 1,
+                            abort_flag, false);
+        }
     } else {
         // ---------------- decode warps (and the epilogue).  Warp w writes the weight rows of
         // TMEM lane quarter w % 4 (rows 32 (w % 4) + lane of the block) for the K slice w / 4
@@ -537,6 +548,55 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
         const uint32_t cb_lane = sbase + kOffCb + (uint32_t)(lane & 7) * 16;
         const uint32_t a_lane = (uint32_t)(lq * 32) << 16;
         int loaded = -1; // (expert * 3 + matrix) whose codebooks are in shared memory
+        // An item's epilogue: warp w reads TMEM lanes 32 (w % 4) .. +32 (its output rows) and the
+        // column blocks of 16 starting at 16 (w / 4), every 64.  Down: item j's accumulator is
+        // buffer j & 1 and its slot list the list j & 1; it runs under the next item's decode.
+        struct Ep {
+            uint32_t j;
+            int row, nt, npad;
+            bool row_ok;
+            int4 ch;
+        };
+        auto epilogue = [&](const Ep &E) {
+            const int ba = kDown ? (int)(E.j & 1) : 0;
+            wait_phase(bar(kAccFull + ba), kDown ? (E.j >> 1) & 1 : E.j & 1, abort_flag);
+            tc::fence_after_sync();
+            const int *slots = s_slot + (kDown ? ba * kGroupTokens : 0);
+            const uint32_t lane_addr = tmem + a_lane + (uint32_t)ba * kGroupTokens;
+            const int kcf = (A.f + kBK - 1) / kBK;
+            uint8_t *ag = A.ag + (size_t)E.ch.w * kcf * 128;
+            const int row = E.row, nt = E.nt, npad = E.npad;
+            for (int c0 = wg * 16; c0 < npad; c0 += 64) {
+                float z[16];
+                tc::tmem_ld16(lane_addr + c0, z);
+                if constexpr (!kDown) {
+                    float u[16];
+                    tc::tmem_ld16(lane_addr + kGroupTokens + c0, u);
+                    if (E.row_ok) {
+#pragma unroll
+                        for (int n = 0; n < 16; ++n)
+                            if (c0 + n < nt) {
+                                const float a = z[n] / (1.0f + expf(-z[n])) * u[n];
+                                const __half ha = __float2half_rn(a);
+                                *reinterpret_cast<__half *>(ag + tile_off(row >> 6, npad, c0 + n, row) +
+                                                            (row & 7) * 2) = ha;
+                            }
+                    }
+                } else {
+                    if (E.row_ok) {
+#pragma unroll
+                        for (int n = 0; n < 16; ++n)
+                            if (c0 + n < nt) A.part_dn[(size_t)slots[c0 + n] * A.nparts * A.d + row] = z[n];
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(kAccEmpty + ba));
+        };
+        Ep pend_ep;
+        bool have_ep = false;           // down: an epilogue waits for the next item's first chunks
+        const int defer_at = min(kARing, KC); // chunks of an item decoded before it runs
         uint32_t q = 0, gs = 0, it = 0;
         for (int item = i0; item < i1; ++item, ++it) {
             const int4 ch = A.chunks[item / nmb];
@@ -544,6 +604,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             const int mb = item % nmb;
             const int row = mb * kBM + rl;
             const bool row_ok = row < G.n_out;
+            int *slots_it = s_slot + (kDown ? (int)(it & 1) * kGroupTokens : 0);
+            int kc_item = 0; // chunks of this item decoded (down's deferred epilogue)
             for (int pass = 0; pass < kPasses; ++pass) {
                 const int mat = pass_mat<kDown>(it, pass);
                 const int key = e * 3 + mat;
@@ -552,7 +614,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                 const bool new_slots = kDown && pass == 0, reload = key != loaded;
                 if (new_slots || reload) {
                     dec_barrier(); // every decode warp is past the previous pass (and epilogue)
-                    if (new_slots && tid < kGroupTokens) s_slot[tid] = tid < nt ? A.sorted[ch.y + tid] : 0;
+                    if (new_slots && tid < kGroupTokens) slots_it[tid] = tid < nt ? A.sorted[ch.y + tid] : 0;
                     if (reload) {
                         // codebook rows as fp16, 8 copies each; a thread writes its row's copies
                         // starting at its own, so a quarter-warp's stores hit 8 bank quads
@@ -624,6 +686,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                         } else {
                             pend = ab;
                         }
+                        if (kDown && have_ep && ++kc_item == defer_at) {
+                            // the MMAs have defer_at chunks of this item queued: the previous
+                            // item's epilogue now (its stage handed over first)
+                            if (pend >= 0) {
+                                tc::tmem_wait_st();
+                                tc::fence_before_sync();
+                                __syncwarp();
+                                if (lane == 0) tc::mbar_arrive(bar(kAFull + pend));
+                                pend = -1;
+                            }
+                            epilogue(pend_ep);
+                            have_ep = false;
+                        }
                     }
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(bar(kSegEmpty + sb)); // its codes are read
@@ -635,43 +710,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
                     if (lane == 0) tc::mbar_arrive(bar(kAFull + pend));
                 }
             }
-            // epilogue: warp w reads TMEM lanes 32 (w % 4) .. +32 (its output rows) and the
-            // column blocks of 16 starting at 16 (w / 4), every 64
-            wait_phase(bar(kAccFull), it & 1, abort_flag);
-            tc::fence_after_sync();
-            {
-                const uint32_t lane_addr = tmem + a_lane;
-                const int kcf = (A.f + kBK - 1) / kBK;
-                uint8_t *ag = A.ag + (size_t)ch.w * kcf * 128;
-                for (int c0 = wg * 16; c0 < npad; c0 += 64) {
-                    float z[16];
-                    tc::tmem_ld16(lane_addr + c0, z);
-                    if constexpr (!kDown) {
-                        float u[16];
-                        tc::tmem_ld16(lane_addr + kGroupTokens + c0, u);
-                        if (row_ok) {
-#pragma unroll
-                            for (int n = 0; n < 16; ++n)
-                                if (c0 + n < nt) {
-                                    const float a = z[n] / (1.0f + expf(-z[n])) * u[n];
-                                    const __half ha = __float2half_rn(a);
-                                    *reinterpret_cast<__half *>(ag + tile_off(row >> 6, npad, c0 + n, row) +
-                                                                (row & 7) * 2) = ha;
-                                }
-                        }
-                    } else {
-                        if (row_ok) {
-#pragma unroll
-                            for (int n = 0; n < 16; ++n)
-                                if (c0 + n < nt) A.part_dn[(size_t)s_slot[c0 + n] * A.nparts * A.d + row] = z[n];
-                        }
-                    }
-                }
+            const Ep cur{it, row, nt, npad, row_ok, ch};
+            if constexpr (kDown) {
+                pend_ep = cur;
+                have_ep = true;
+            } else {
+                epilogue(cur);
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(kAccEmpty));
         }
+        if (have_ep) epilogue(pend_ep);
     }
     tc::fence_before_sync();
     __syncthreads();
