@@ -201,7 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ float red[kRouterRowsPerItem][4][kRouterTok];
     __shared__ int claimed;
-    int par = 0;
     bool primed = false;
     int cur = claim(F.sync, &claimed);
     int nxt = is_copy<kBanked>(F, cur) ? -1 : claim(F.sync, &claimed);
@@ -237,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             const bool has_next = nxt >= b_gu(F) && nxt < b_dn(F);
             Unit N;
             if (has_next) N = decode_unit<false>(F.A, nxt - b_gu(F));
-            run_unit<false, kRecon, kBf16, kThreads, kCodePingPong, kBanked ? kPrefetchRounds : kStepPrefetchRounds,
-                     kBanked>(F.A, U, has_next, N, par, primed, nullptr, 0);
+            run_unit<false, kRecon, kBf16, kThreads, kBanked ? kPrefetchRounds : kStepPrefetchRounds, kBanked>(
+                F.A, U, has_next, N, primed, nullptr, 0);
             signal(gu_done(F) + U.slot);
         } else if (cur < b_comb(F)) {
             // ---- down unit (waits inside for the gate/up units of its slot)
@@ -249,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             const bool has_next = nxt >= b_dn(F) && nxt < b_comb(F);
             Unit N;
             if (has_next) N = decode_unit<true>(F.A, nxt - b_dn(F));
-            run_unit<true, kRecon, kBf16, kThreads, kCodePingPong, kBanked ? kPrefetchRounds : kStepPrefetchRounds,
-                     kBanked>(F.A, U, has_next, N, par, primed, gu_done(F) + U.slot, (unsigned)(2 * F.A.gu_pairs));
+            run_unit<true, kRecon, kBf16, kThreads, kBanked ? kPrefetchRounds : kStepPrefetchRounds, kBanked>(
+                F.A, U, has_next, N, primed, gu_done(F) + U.slot, (unsigned)(2 * F.A.gu_pairs));
             signal(dn_done(F) + (u % F.A.nrb));
         } else {
             // ---- combine rows [r0, r1) once every down unit over them is done
@@ -274,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
         cur = nxt >= 0 ? nxt : claim(F.sync, &claimed);
         nxt = is_copy<kBanked>(F, cur) ? -1 : claim(F.sync, &claimed);
     }
-    if constexpr (!kRecon) cp_async_wait<0>();
+
     // the last CTA to leave puts the queue and counters back to zero
     __syncthreads();
     if (threadIdx.x == 0) {

@@ -16,9 +16,6 @@ constexpr int kTabStage = 65536;             // bytes per stage: 256 codes x 256
 constexpr int kTabBytes = kStages * kTabStage; // 192 KiB
 constexpr int kXsFloats = 512;               // down input staging (64 vectors x 8)
 constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
-constexpr int kStageFloats = 2 * kCodes * kVec;    // one stage of both parts' codebooks
-constexpr int kStageBuf = kStageFloats * 4;        // 16 KiB
-constexpr bool kCodePingPong = false;            // hold the next round's codes in registers
 constexpr int kPrefetchRounds = 1;                 // L2 prefetch distance in row-group rounds
 constexpr int kPrefetchRoundsGu = 2;               // the same for the per-phase gate/up kernel
 
@@ -92,20 +89,6 @@ template <bool kBf16>
 __device__ __forceinline__ float load_x1(const void *h, size_t elem) {
     if constexpr (kBf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(h)[elem]);
     else return reinterpret_cast<const float *>(h)[elem];
-}
-
-__device__ __forceinline__ float dot8(const float *__restrict__ c, const float *xv) {
-    const float4 c0 = __ldg(reinterpret_cast<const float4 *>(c));
-    const float4 c1 = __ldg(reinterpret_cast<const float4 *>(c) + 1);
-    float t = c0.x * xv[0];
-    t = fmaf(c0.y, xv[1], t);
-    t = fmaf(c0.z, xv[2], t);
-    t = fmaf(c0.w, xv[3], t);
-    t = fmaf(c1.x, xv[4], t);
-    t = fmaf(c1.y, xv[5], t);
-    t = fmaf(c1.z, xv[6], t);
-    t = fmaf(c1.w, xv[7], t);
-    return t;
 }
 
 // Streaming load of 16 code bytes: read once, so kept out of L1.
@@ -184,26 +167,6 @@ __device__ __forceinline__ Unit decode_unit(const LutArgs &A, int u) {
     return U;
 }
 
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Codebook rows of one stage for both parts -> smem [part][256][8] (16 KiB), as
-// one cp.async group.
-template <int kNT = kThreads>
-__device__ __forceinline__ void issue_stage(float *dst, const float *cb_p0, const float *cb_p1, int s) {
-    for (int i = threadIdx.x; i < 1024; i += kNT) {
-        const int part = i >> 9, ii = i & 511;
-        const float *src = (part ? cb_p1 : cb_p0) + (size_t)s * kCodes * kVec + (size_t)ii * 4;
-        cp_async16(dst + part * kCodes * kVec + ii * 4, src);
-    }
-    cp_async_commit();
-}
-
 // The unit's matrix codebooks (both parts: the parts are two segments of one matrix).
 template <bool kDown>
 __device__ __forceinline__ void unit_codebooks(const LutArgs &A, const Unit &U, const float *&p0,
@@ -266,20 +229,6 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__device__ __forceinline__ float dot8s(const float *__restrict__ c, const float *xv) {
-    const float4 c0 = reinterpret_cast<const float4 *>(c)[0];
-    const float4 c1 = reinterpret_cast<const float4 *>(c)[1];
-    float t = c0.x * xv[0];
-    t = fmaf(c0.y, xv[1], t);
-    t = fmaf(c0.z, xv[2], t);
-    t = fmaf(c0.w, xv[3], t);
-    t = fmaf(c1.x, xv[4], t);
-    t = fmaf(c1.y, xv[5], t);
-    t = fmaf(c1.z, xv[6], t);
-    t = fmaf(c1.w, xv[7], t);
-    return t;
-}
-
 // Wait (thread 0 polls, the CTA then proceeds together) until *c >= target.  The wait
 // is bounded: after limit_ns (by default about a second) it records kErrTimeout and gives up.
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
@@ -310,22 +259,20 @@ __device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target,
 // Dynamic shared memory of the lookup kernels (every extern __shared__ array names it).
 extern __shared__ __align__(16) unsigned char lut_smem[];
 
-// One unit: tables (or staged codebooks) for the unit's segment(s), then the stream of
-// its rows.  `primed`: this unit's codebooks were already asked for by the previous unit of
-// the CTA (else they are asked for at the start, ahead of the down units' input and the
-// table build).  `par` carries the codebook stage buffers across consecutive units of
-// one kind: when `has_next`, the next unit's stages 0 and 1 are already on their way
-// into the buffers when this one returns.  For a down unit, `dep` (if not null) is a
-// completion counter that must reach dep_target before the gate/up partials are read.
-// kNT: threads of the CTA (a multiple of 128); kPing: codes of the next row group are
-// loaded into registers while the current one is consumed; kPartLoads: the next row group's
-// codes of a part are asked for as soon as that part's lookups are issued (else at the top
-// of each round -- the persistent step kernel, whose other items leave no registers for it).
-template <bool kDown, bool kRecon, bool kBf16, int kNT = kThreads, bool kPing = kCodePingPong,
-          int kPf = kPrefetchRounds, bool kPartLoads = true, bool kFixed = false>
+// One unit: tables (or, for the register-reconstruct form, the codebooks) for the unit's
+// segments, then the stream of its rows.  `primed`: this unit's codebooks were already asked
+// for by the previous unit of the CTA (else they are asked for at the start, ahead of the down
+// units' input and the table build).  For a down unit, `dep` (if not null) is a completion
+// counter that must reach dep_target before the gate/up partials are read.  kNT: threads of
+// the CTA (a multiple of 128); kPf: L2 prefetch distance in rounds; kPartLoads: the next row
+// group's codes of a part are asked for as soon as that part's lookups are issued (else at the
+// top of each round -- the persistent step kernel, whose other items leave no registers for
+// it); kFixed: the tables sit at kDynSmemBase (the lookups' immediate base).
+template <bool kDown, bool kRecon, bool kBf16, int kNT = kThreads, int kPf = kPrefetchRounds,
+          bool kPartLoads = true, bool kFixed = false>
 __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
-                                      int &par, bool &primed, const unsigned *dep,
-                                      unsigned dep_target, unsigned long long *t_tables = nullptr) {
+                                         bool &primed, const unsigned *dep, unsigned dep_target,
+                                         unsigned long long *t_tables = nullptr) {
     constexpr int kNW = kNT / 32;
     static_assert(kNT % 128 == 0 && kNT <= 512, "CTA size of the lookup units");
     // the dynamic shared memory named directly, so every access compiles to a shared one
@@ -545,14 +492,11 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         }
         __syncthreads();
     }
-    (void)par;
 
     if (t_tables && threadIdx.x == 0) t_tables[0] = gtimer();
 
-    // ---- stream the codes of rows [g0, g1) x this unit's segment(s).  Registers hold
-    // the next row group's codes while the current one is consumed (ping-pong), and L2
-    // is asked for the row group kPrefetchRounds rounds ahead -- past the end of the
-    // unit, for the next unit's first row groups.
+    // ---- stream the codes of rows [g0, g1) x this unit's segments.  L2 is asked for the row
+    // group kPf rounds ahead -- past the end of the unit, for the next unit's first row groups.
     // a unit whose second segment lies past the matrix (an odd segment count) reads the first
     // segment's codes again for it: that part's tables are zero (its inputs are)
     const uint8_t *pb0 = U.base[0];
@@ -672,28 +616,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
         }
     };
     auto stream = [&](auto fixed) {
-        if constexpr (kPing) {
-            auto consume = [&](const uint4 (&cw)[2][kStages], int g) {
-                float acc[16];
-                lookups(fixed, cw[0], 0, acc);
-                lookups(fixed, cw[1], 1, acc);
-                finish(acc, g);
-            };
-            uint4 wa[2][kStages], wb[2][kStages];
-            int g = U.g0 + warp;
-            if (g < U.g1) load(g, wa);
-            while (g < U.g1) {
-                if (g + kNW < U.g1) load(g + kNW, wb);
-                ahead(g);
-                consume(wa, g);
-                g += kNW;
-                if (g >= U.g1) break;
-                if (g + kNW < U.g1) load(g + kNW, wa);
-                ahead(g);
-                consume(wb, g);
-                g += kNW;
-            }
-        } else if constexpr (!kPartLoads) {
+        if constexpr (!kPartLoads) {
             for (int g = U.g0 + warp; g < U.g1; g += kNW) {
                 uint4 wa[2][kStages];
                 load(g, wa);

@@ -9,15 +9,16 @@
 // additions per vector.
 //
 // GB300 mapping.  A CTA (512 threads, one per SM, persistent) owns a "unit":
-// one slot and one 32-vector segment of the input (two matrices' worth: gate
-// and up at the same segment, or two consecutive segments of down).  It builds
-// the unit's tables in shared memory -- T[s][c][part][lane], 3 x 64 KiB, so
-// that lane l always reads bank l whatever the code -- then streams all rows'
-// codes of that segment with 128-bit loads.  Each lane owns one vector column
-// and 16 rows per 16-byte chunk; the chunk's bytes are pre-permuted (row
-// (lane ^ q) & 15 at byte q) so the cross-lane reduction of 32 row partials is
-// a select-free butterfly.  One PRMT turns a code byte plus the lane's column
-// offset into the table address, so a lookup costs PRMT + LDS + FADD.
+// one slot, one matrix and two consecutive 32-vector segments of its input (for
+// down also a block of rows).  It builds the unit's tables in shared memory --
+// T[s][c][part][lane], 3 x 64 KiB, so that lane l always reads bank l whatever
+// the code -- then streams all rows' codes of those segments with 128-bit
+// loads.  Each lane owns one vector column of each segment and 16 rows per
+// 16-byte chunk; the chunk's bytes are pre-permuted (row (lane ^ q) & 15 at byte
+// q) so the cross-lane reduction of 32 row partials is a select-free butterfly.
+// One PRMT turns a code byte plus the lane's column offset into the table
+// address (the tables' base and the stage in the load's immediate), so a lookup
+// costs PRMT + LDS and half of a packed fp32 addition.
 // Partials of each segment go to a scratch buffer; the down kernel reduces the
 // gate/up partials in a fixed order, applies SwiGLU and builds its own tables;
 // a last kernel combines the k expert outputs with their gates.  Every sum has a
@@ -34,12 +35,10 @@ using namespace lut;
 
 namespace {
 
-template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf, bool kFixed>
+template <bool kDown, bool kRecon, bool kBf16, int kNT, int kPf, bool kFixed>
 __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
-    extern __shared__ __align__(16) unsigned char smem[];
     const int n_slots = lut_slot_count(A);
     const int units = kDown ? n_slots * A.npair * A.nrb : n_slots * 2 * A.gu_pairs;
-    int par = 0;
     bool primed = false;
     Unit N;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -48,8 +47,8 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
         if (has_next) N = decode_unit<kDown>(A, u + gridDim.x);
         unsigned long long t0 = 0, t_tab[2] = {0, 0};
         if (A.trace && threadIdx.x == 0) t0 = gtimer();
-        run_unit<kDown, kRecon, kBf16, kNT, kPing && !kRecon, kPf, true, kFixed>(A, U, has_next, N, par, primed,
-                                                                                 nullptr, 0, A.trace ? t_tab : nullptr);
+        run_unit<kDown, kRecon, kBf16, kNT, kPf, true, kFixed>(A, U, has_next, N, primed, nullptr, 0,
+                                                               A.trace ? t_tab : nullptr);
         if (A.trace && threadIdx.x == 0 && A.trace_base + u < A.trace_cap) {
             unsigned smid;
             asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -60,7 +59,6 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
             e[3] = smid | ((t_tab[1] > t0 ? (t_tab[1] - t0) : 0ull) << 32);
         }
     }
-    if constexpr (!kRecon) cp_async_wait<0>();
 }
 
 // out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair],
@@ -154,15 +152,15 @@ bool tables_at_fixed_base(cudaStream_t s) {
     return base == kDynSmemBase;
 }
 
-template <bool kDown, bool kRecon, bool kBf16, int kNT, bool kPing, int kPf, bool kFixed>
+template <bool kDown, bool kRecon, bool kBf16, int kNT, int kPf, bool kFixed>
 cudaError_t launch_v(const LutArgs &A, int units, int num_sms, cudaStream_t s) {
     const size_t smem = unit_smem<kRecon>();
     static SmemAttr attr;
     cudaError_t e =
-        ensure_smem(attr, (const void *)lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf, kFixed>, (int)smem);
+        ensure_smem(attr, (const void *)lut_kernel<kDown, kRecon, kBf16, kNT, kPf, kFixed>, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = units < num_sms ? units : num_sms;
-    lut_kernel<kDown, kRecon, kBf16, kNT, kPing, kPf, kFixed><<<grid, kNT, smem, s>>>(A);
+    lut_kernel<kDown, kRecon, kBf16, kNT, kPf, kFixed><<<grid, kNT, smem, s>>>(A);
     return cudaGetLastError();
 }
 
@@ -177,8 +175,8 @@ cudaError_t launch_one(const LutArgs &A, int units, int num_sms, cudaStream_t s)
     constexpr int kPf = kDown ? kPrefetchRounds : kPrefetchRoundsGu;
     if constexpr (!kRecon)
         if (tables_at_fixed_base(s))
-            return launch_v<kDown, false, kBf16, kThreads, kCodePingPong, kPf, true>(A, units, num_sms, s);
-    return launch_v<kDown, kRecon, kBf16, kThreads, kCodePingPong, kPf, false>(A, units, num_sms, s);
+            return launch_v<kDown, false, kBf16, kThreads, kPf, true>(A, units, num_sms, s);
+    return launch_v<kDown, kRecon, kBf16, kThreads, kPf, false>(A, units, num_sms, s);
 }
 
 template <bool kDown>
