@@ -353,12 +353,13 @@ def run_decode(args, dev, out):
                gate_up_gbs=gu_bytes / (rk["gate_up"] * 1e-3) / 1e9,
                gate_up_frac=gu_bytes / (rk["gate_up"] * 1e-3) / 1e9 / peak_k2,
                down_frac=dn_bytes / (rk["down"] * 1e-3) / 1e9 / peak_k2,
-               table_form_gate_up_ms=kern.get("gate_up"), table_form_down_ms=kern.get("down"))
+               table_form_gate_up_ms=kern.get("gate_up"), table_form_down_ms=kern.get("down"),
+               table_form_experts_ms=kern.get("experts"))
     out["decode"] = dict(step_ms=ms_per_step, kernels_ms=kern, stats=st, step_bytes=step_bytes,
                          gate_up_bytes=gu_bytes, down_bytes=dn_bytes,
                          hbm_gbs_step=step_bytes / (ms_per_step * 1e-3) / 1e9,
                          median_step_ms=statistics.median(step_ms),
-                         launches_per_step=4, profiled_steps=n_prof, unfused_ms=unfused_ms,
+                         launches_per_step=len(kern), profiled_steps=n_prof, unfused_ms=unfused_ms,
                          k2a_reconstruct=k2a)
 
     # ---- end to end through the C ABI with host buffers: h2d copy of the token from
@@ -904,6 +905,10 @@ def native(args):
         dominant, alg = "fused_step_kernel", d["step_bytes"]
         achieved = alg / (kern["step"] * 1e-3) / 1e9
         traffic = ncu_traffic("fused_step_decode")
+    elif "experts" in kern:  # the gate/up and down units in one launch
+        dominant, alg = "lut_experts_kernel", d["gate_up_bytes"] + d["down_bytes"]
+        achieved = alg / (kern["experts"] * 1e-3) / 1e9
+        traffic = ncu_traffic("lut_experts_decode")
     else:
         dominant = max(("gate_up", "down"), key=lambda k: kern[k])
         alg = d["gate_up_bytes"] if dominant == "gate_up" else d["down_bytes"]
@@ -927,16 +932,19 @@ def native(args):
             "workload": "decode layer: d=7168 f=1536 E=384 experts top-16, T=1 token/step, fp32 h; "
                         "RVQ 3x256 codebooks per matrix, 8-weight vectors, 12.39 MB codes per expert",
             "step": "router GEMV + top-16 + softmax + RVQ gate/up table-lookup GEMV + SwiGLU + down "
-                    "table-lookup GEMV + gate-weighted combine (waste_moe_step: 4 kernels, the router's last "
-                    "CTA taking the top-k) replayed "
-                    "from a CUDA graph",
+                    "table-lookup GEMV + gate-weighted combine (waste_moe_step: "
+                    f"{d['launches_per_step']} kernels: the router, its last CTA taking the top-k; "
+                    + ("the gate/up and down units in one launch; " if "experts" in kern else
+                       "gate/up; down; ") + "the combine) replayed from a CUDA graph",
             "l2": "flushed between steps (256 MiB write outside the per-step CUDA events); "
                   "each step also uses a different token (pool of 64)",
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
             "hbm_gbs_whole_step": d["hbm_gbs_step"],
             "hbm_frac_whole_step": d["hbm_gbs_step"] / peak,
             "hbm_frac_expert_kernels": (d["gate_up_bytes"] + d["down_bytes"])
-            / ((kern["gate_up"] + kern["down"]) * 1e-3) / 1e9 / peak if "gate_up" in kern else None,
+            / ((kern["gate_up"] + kern["down"]) * 1e-3) / 1e9 / peak if "gate_up" in kern
+            else (d["gate_up_bytes"] + d["down_bytes"]) / (kern["experts"] * 1e-3) / 1e9 / peak
+            if "experts" in kern else None,
             "algorithmic_bytes_per_step": d["step_bytes"],
             "kernels_ms": kern,
             "ms_per_step_persistent_step_kernel": d["unfused_ms"],
@@ -1171,6 +1179,9 @@ def print_unit_trace(tr, w):
                    f"tables mean {sum(tab)/len(tab):.2f} "
                    f"max {max(tab):.2f}; rows mean {sum(run)/len(run):.2f} max {max(run):.2f}; "
                    f"SM busy mean {sum(busy)/len(busy):.1f} max {max(busy):.1f} us over {len(per_sm)} SMs")
+    live = [r for r in rows if r[2] > 0]
+    if live:
+        out.append(f"all units: span {(max(r[2] for r in live) - min(r[0] for r in live)) / 1e3:.1f} us")
     print(" | ".join(out))
 
 

@@ -294,7 +294,8 @@ int waste_moe_reset_stats(waste_moe *h);
 int waste_moe_set_profiling(waste_moe *h, int32_t enable);
 
 /* Milliseconds of each kernel of the last profiled calls: ms[0] router, ms[1] top-k
- * (route); ms[2] gate/up, ms[3] down, ms[4] combine (forward as separate kernels);
+ * (route; -1 where the router's last CTA took the top-k); ms[2] gate/up, ms[3] down, ms[4] combine (forward as separate kernels; where
+ * the gate/up and down units ran in one launch, ms[2] is that launch and ms[3] is -1);
  * ms[5] the persistent step kernel (step, or forward when fused); -1 where the last
  * call did not run that kernel.  Waits for the events. */
 int waste_moe_read_profile(const waste_moe *h, float ms[6]);

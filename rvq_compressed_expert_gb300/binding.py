@@ -234,7 +234,10 @@ def waste_moe_read_profile(h) -> dict:
     """Milliseconds per kernel of the last profiled route and forward."""
     ms = (ctypes.c_float * 6)()
     _check(load().waste_moe_read_profile(h, ms))
-    return dict(zip(("router", "topk", "gate_up", "down", "combine", "step"), list(ms)))
+    out = dict(zip(("router", "topk", "gate_up", "down", "combine", "step"), list(ms)))
+    if out["down"] < 0 <= out["gate_up"]:  # gate/up and down units in one launch
+        out["experts"] = out.pop("gate_up")
+    return out
 
 
 def waste_moe_debug_wait(h, d_counter, target, limit_ns, stream=None):

@@ -436,11 +436,17 @@ int waste_moe_read_profile(const waste_moe *h, float ms[6]) {
     int o = 0;
     for (int j = 0; j < 3; ++j) {
         const int n = count[j];
-        if (t[j]->n == n) {
-            cudaError_t e = cudaEventSynchronize(t[j]->ev[n - 1]);
+        // the forward with its gate/up and down units in one launch records 3 events:
+        // that launch into ms[2], the combine into ms[4], ms[3] stays -1; a route whose
+        // router took the top-k records 2 (ms[1] stays -1)
+        const bool one_launch = j == 1 && t[j]->n == 3;
+        if (t[j]->n == n || one_launch || (j == 0 && t[j]->n == 2)) {
+            const int m = t[j]->n;
+            cudaError_t e = cudaEventSynchronize(t[j]->ev[m - 1]);
             if (e != cudaSuccess) return cuda_fail(e, "waiting for profiling events");
-            for (int i = 0; i + 1 < n; ++i) {
-                e = cudaEventElapsedTime(&ms[o + i], t[j]->ev[i], t[j]->ev[i + 1]);
+            for (int i = 0; i + 1 < m; ++i) {
+                const int at = one_launch && i == 1 ? o + 2 : o + i;
+                e = cudaEventElapsedTime(&ms[at], t[j]->ev[i], t[j]->ev[i + 1]);
                 if (e != cudaSuccess) return cuda_fail(e, "reading profiling events");
             }
         }
@@ -483,8 +489,12 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
         if (e != cudaSuccess) return cuda_fail(e, "top-k kernel");
     }
     if (h->profiling) {
-        cudaEventRecord(h->route_tm.ev[2], s);
-        h->route_tm.n = 3;
+        if (fused) {
+            h->route_tm.n = 2; // the router's last CTA took the top-k: no top-k kernel
+        } else {
+            cudaEventRecord(h->route_tm.ev[2], s);
+            h->route_tm.n = 3;
+        }
     }
     return ok();
 }

@@ -271,8 +271,9 @@ extern __shared__ __align__(16) unsigned char lut_smem[];
 template <bool kDown, bool kRecon, bool kBf16, int kNT = kThreads, int kPf = kPrefetchRounds,
           bool kPartLoads = true, bool kFixed = false>
 __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
-                                         bool &primed, const unsigned *dep, unsigned dep_target,
-                                         unsigned long long *t_tables = nullptr) {
+                                         bool &primed, unsigned *dep, unsigned dep_target,
+                                         unsigned long long *t_tables = nullptr, unsigned *done_prev = nullptr,
+                                         unsigned *dep_used = nullptr, unsigned dep_users = 0) {
     constexpr int kNW = kNT / 32;
     static_assert(kNT % 128 == 0 && kNT <= 512, "CTA size of the lookup units");
     // the dynamic shared memory named directly, so every access compiles to a shared one
@@ -355,8 +356,30 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     };
     if constexpr (kDown)
         if (!dep) swiglu_input();
+    // Counters of a launch that runs gate/up and down units together, kept from the last warp
+    // once every thread is past a barrier that follows the previous unit's partial stores (and,
+    // for a down unit, its wait): done_prev counts the CTA's previous unit as finished; dep_used
+    // counts this unit as a reader of dep, and the slot's last reader puts both back to zero
+    // (every writer and reader of dep in this launch is then past it).
+    auto counters = [&]() {
+        if (threadIdx.x == kNT - 32) {
+            if (done_prev) {
+                __threadfence();
+                atomicAdd(done_prev, 1u);
+            }
+            if (dep_used && atomicAdd(dep_used, 1u) == dep_users - 1) {
+                *dep_used = 0u;
+                *dep = 0u;
+            }
+        }
+    };
     if (!valid) {
         // no codes to stream: the unit's rows get zero partials (the step reports the error)
+        if (done_prev || dep_used) {
+            if (kDown && dep && !input_done) wait_counter(dep, dep_target, A.err);
+            else __syncthreads();
+            counters();
+        }
         if (threadIdx.x == 0) atomicOr(A.err, (U.e >= 0 && U.e < A.E) ? kErrNotResident : kErrBadExpert);
         const int r1 = min(G.n_out, U.g1 * kGroupRows);
         for (int row = U.g0 * kGroupRows + threadIdx.x; row < r1; row += kNT) {
@@ -494,6 +517,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     }
 
     if (t_tables && threadIdx.x == 0) t_tables[0] = gtimer();
+    // after the table barriers: the last warp's fence and atomics overlap the other warps' rows
+    counters();
 
     // ---- stream the codes of rows [g0, g1) x this unit's segments.  L2 is asked for the row
     // group kPf rounds ahead -- past the end of the unit, for the next unit's first row groups.

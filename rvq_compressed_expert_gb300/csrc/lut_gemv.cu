@@ -19,10 +19,14 @@
 // One PRMT turns a code byte plus the lane's column offset into the table
 // address (the tables' base and the stage in the load's immediate), so a lookup
 // costs PRMT + LDS and half of a packed fp32 addition.
-// Partials of each segment go to a scratch buffer; the down kernel reduces the
-// gate/up partials in a fixed order, applies SwiGLU and builds its own tables;
-// a last kernel combines the k expert outputs with their gates.  Every sum has a
-// fixed order: results are bit-reproducible.
+// Partials of each segment go to a scratch buffer; a down unit reduces the
+// gate/up partials of its slot in a fixed order, applies SwiGLU and builds its
+// own tables; a last kernel combines the k expert outputs with their gates.  A
+// handle's forward runs the gate/up and the down units in one launch (each down
+// unit waits for its slot's gate/up units); the per-phase kernels, one launch
+// per phase, serve the listed slots of batched calls, the reconstruct form and
+// the no-allocation entry point.  Every sum has a fixed order: results are
+// bit-reproducible, and the same in either form.
 //
 // The K2_RECONSTRUCT variant instead stages the codebooks in shared memory and
 // rebuilds each 8-weight vector in registers (3 codebook rows summed) before an
@@ -34,6 +38,20 @@ namespace wm {
 using namespace lut;
 
 namespace {
+
+// Per-unit trace entry {start, tables ready, end, SM | table-barrier wait << 32}.
+__device__ __forceinline__ void trace_unit(const LutArgs &A, int item, unsigned long long t0,
+                                           const unsigned long long (&t_tab)[2]) {
+    if (A.trace && threadIdx.x == 0 && A.trace_base + item < A.trace_cap) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        unsigned long long *e = A.trace + 4 * (size_t)(A.trace_base + item);
+        e[0] = t0;
+        e[1] = t_tab[0];
+        e[2] = gtimer();
+        e[3] = smid | ((t_tab[1] > t0 ? (t_tab[1] - t0) : 0ull) << 32);
+    }
+}
 
 template <bool kDown, bool kRecon, bool kBf16, int kNT, int kPf, bool kFixed>
 __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
@@ -49,15 +67,69 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
         if (A.trace && threadIdx.x == 0) t0 = gtimer();
         run_unit<kDown, kRecon, kBf16, kNT, kPf, true, kFixed>(A, U, has_next, N, primed, nullptr, 0,
                                                                A.trace ? t_tab : nullptr);
-        if (A.trace && threadIdx.x == 0 && A.trace_base + u < A.trace_cap) {
-            unsigned smid;
-            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-            unsigned long long *e = A.trace + 4 * (size_t)(A.trace_base + u);
-            e[0] = t0;
-            e[1] = t_tab[0];
-            e[2] = gtimer();
-            e[3] = smid | ((t_tab[1] > t0 ? (t_tab[1] - t0) : 0ull) << 32);
+        trace_unit(A, u, t0, t_tab);
+    }
+}
+
+// The gate/up and the down units of one call in one launch, so that a CTA starts its down
+// unit as soon as its own gate/up units and those of the down unit's slot are done, with no
+// kernel boundary between the two phases.  CTA b runs gate/up units b, b + G, ... and then
+// down units G - 1 - b, 2 G - 1 - b, ...: the CTAs with one gate/up unit fewer take the
+// first slots' down units, whose gate/up units finish first.  A down unit waits (bounded) on
+// its slot's count of finished gate/up units, so every CTA must be resident at once: the
+// launch is cooperative.  sync: [4 + slot] gate/up units of the slot finished, [4 + slots +
+// slot] its down units past that wait; zero at rest, and the slot's last down unit puts both
+// back.  A finished gate/up unit is counted inside the CTA's next unit, once its tables are
+// built, so that the fence of the count runs beside that unit's rows (the CTA's last gate/up
+// unit is counted before its first down unit).  Same unit arithmetic as the per-phase kernels:
+// the results are bit-identical to theirs.
+template <bool kBf16, bool kFixed>
+__global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs A, unsigned *sync) {
+    const int n_gu = A.slots * 2 * A.gu_pairs;
+    const int n_dn = A.slots * A.npair * A.nrb;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int mine_gu = b < n_gu ? (n_gu - 1 - b) / G + 1 : 0;
+    const int d0 = G - 1 - b;
+    const int mine_dn = d0 < n_dn ? (n_dn - 1 - d0) / G + 1 : 0;
+    bool primed = false;
+    // slot counter of the CTA's last finished gate/up unit, bumped inside the next unit (once
+    // its tables are built), or before the first down unit
+    int pending = -1;
+    for (int i = 0; i < mine_gu; ++i) {
+        const int u = b + i * G;
+        // the next unit: the CTA's next gate/up unit, else its first down unit
+        const bool has_next = i + 1 < mine_gu || mine_dn > 0;
+        Unit N;
+        if (i + 1 < mine_gu) N = decode_unit<false>(A, u + G);
+        else if (mine_dn > 0) N = decode_unit<true>(A, d0);
+        unsigned long long t0 = 0, t_tab[2] = {0, 0};
+        if (A.trace && threadIdx.x == 0) t0 = gtimer();
+        const Unit U = decode_unit<false>(A, u);
+        run_unit<false, false, kBf16, kThreads, kPrefetchRoundsGu, true, kFixed>(
+            A, U, has_next, N, primed, nullptr, 0, A.trace ? t_tab : nullptr,
+            pending >= 0 ? sync + 4 + pending : nullptr);
+        trace_unit(A, u, t0, t_tab);
+        pending = U.slot;
+    }
+    if (pending >= 0) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(sync + 4 + pending, 1u);
         }
+    }
+    for (int i = 0; i < mine_dn; ++i) {
+        const int u = d0 + i * G;
+        const bool has_next = i + 1 < mine_dn;
+        Unit N;
+        if (has_next) N = decode_unit<true>(A, u + G);
+        unsigned long long t0 = 0, t_tab[2] = {0, 0};
+        if (A.trace && threadIdx.x == 0) t0 = gtimer();
+        const Unit U = decode_unit<true>(A, u);
+        run_unit<true, false, kBf16, kThreads, kPrefetchRounds, true, kFixed>(
+            A, U, has_next, N, primed, sync + 4 + U.slot, (unsigned)(2 * A.gu_pairs), A.trace ? t_tab : nullptr,
+            nullptr, sync + 4 + A.slots + U.slot, (unsigned)(A.npair * A.nrb));
+        trace_unit(A, n_gu + u, t0, t_tab);
     }
 }
 
@@ -187,6 +259,50 @@ cudaError_t launch_var(const LutArgs &A, int units, bool recon, bool bf16, int n
                 : launch_one<kDown, false, false>(A, units, num_sms, s);
 }
 
+// Whether the current device takes cooperative launches (asked once per device).
+bool coop_launch_ok() {
+    static std::atomic<int> coop[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    int c = coop[dev].load(std::memory_order_acquire);
+    if (c == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) v = 0;
+        c = v ? 1 : 2;
+        coop[dev].store(c, std::memory_order_release);
+    }
+    return c == 1;
+}
+
+template <bool kBf16, bool kFixed>
+cudaError_t launch_experts_v(const LutArgs &A, unsigned *sync, int grid, cudaStream_t s) {
+    const size_t smem = unit_smem<false>();
+    static SmemAttr attr;
+    cudaError_t e = ensure_smem(attr, (const void *)lut_experts_kernel<kBf16, kFixed>, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, lut_experts_kernel<kBf16, kFixed>, A, sync);
+}
+
+// The gate/up and down units in one cooperative launch of at most one CTA per SM.
+cudaError_t launch_experts(const LutArgs &A, unsigned *sync, bool bf16, int num_sms, cudaStream_t s) {
+    const int n_gu = A.slots * 2 * A.gu_pairs, n_dn = A.slots * A.npair * A.nrb;
+    const int units = n_gu > n_dn ? n_gu : n_dn;
+    const int grid = units < num_sms ? units : num_sms;
+    if (tables_at_fixed_base(s))
+        return bf16 ? launch_experts_v<true, true>(A, sync, grid, s) : launch_experts_v<false, true>(A, sync, grid, s);
+    return bf16 ? launch_experts_v<true, false>(A, sync, grid, s) : launch_experts_v<false, false>(A, sync, grid, s);
+}
+
 } // namespace
 
 // Row blocks of the down matrix per (slot, segment pair): enough units to fill
@@ -282,6 +398,20 @@ cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const voi
     A.trace_cap = trace ? trace_cap : 0;
     const bool bf16 = L.act_bf16 != 0;
     if (tm) cudaEventRecord(tm->ev[0], s);
+    if (!reconstruct && W.sync && coop_launch_ok()) {
+        // gate/up and down units in one launch, then the combine
+        A.trace_base = 0;
+        cudaError_t e = launch_experts(A, W.sync, bf16, num_sms, s);
+        if (e != cudaSuccess) return e;
+        if (tm) cudaEventRecord(tm->ev[1], s);
+        e = launch_combine(L, W, h, T, idx, gate, out, mode, nullptr, down_parts(L), s);
+        if (e != cudaSuccess) return e;
+        if (tm) {
+            cudaEventRecord(tm->ev[2], s);
+            tm->n = 3;
+        }
+        return cudaSuccess;
+    }
     cudaError_t e = launch_lut_phase(A, false, reconstruct, bf16, num_sms, s);
     if (e != cudaSuccess) return e;
     if (tm) cudaEventRecord(tm->ev[1], s);

@@ -5,15 +5,20 @@ avec 29 Go de RAM à 0,50 tok/s", section "Lecture anticipée et prédiction du
 routeur"):
   - x_L = rmsnorm(h_L)  (stand-in for the trunk's normalisation of the MoE
     input; without it the chain h <- h + MoE(h) diverges at these scales),
-  - on a side stream, layer L+1's router runs on x_L and its top-P experts are
-    prefetched into L2 (waste_moe_prefetch),
-  - on the main stream layer L routes x_L and applies its experts:
-    h_{L+1} = h_L + combine (waste_moe_step, mode 1, in place).
+  - on the main stream layer L routes x_L (waste_moe_route),
+  - on a side stream, once that route is done, layer L+1's router runs on x_L and
+    its top-P experts are prefetched into L2 (waste_moe_prefetch),
+  - on the main stream layer L applies its experts:
+    h_{L+1} = h_L + combine (waste_moe_forward, mode 1, in place).
 The real router of each layer decides its experts, so the lookahead changes
-neither the outputs nor the demand bytes.  x alternates between two buffers so
-the side stream can still read x_L while x_{L+1} is written; layer L+1 routes
-only after its prefetch has finished (an event), which also keeps the next
-write of x_L's buffer behind the read.
+neither the outputs nor the demand bytes.  The side stream starts behind layer
+L's route, not beside it: the expert kernel is one cooperative launch that
+needs every SM at once, and side-stream kernels still running when it is due
+would hold it back; behind the route they fill the SMs that the expert kernel's
+tail and the combine leave free.  x alternates between two buffers so the side
+stream can still read x_L while x_{L+1} is written; layer L+1 routes only after
+its prefetch has finished (an event), which also keeps the next write of x_L's
+buffer behind the read.
 """
 from __future__ import annotations
 
@@ -51,16 +56,17 @@ class DecodeStack:
         for L in range(n):
             x = self.x[L & 1]
             B.waste_moe_rmsnorm(self.h, x, T, self.d, main)
+            if pending is not None:
+                main.wait_event(pending)  # layer L's prediction is in place before it routes
+            self.layers[L].route(x, T, self.idx, self.gate, stream=main)
             ev = None
             if lookahead and L + 1 < n:
-                side.wait_stream(main)  # x_L is ready
+                side.wait_stream(main)  # x_L is ready and layer L has routed
                 self.layers[L + 1].prefetch(x, T, lookahead, stream=side)
                 ev = torch.cuda.Event()
                 ev.record(side)
-            if pending is not None:
-                main.wait_event(pending)  # layer L's prediction is in place before it routes
-            # route + experts + combine (h += combine) in one launch
-            self.layers[L].step(x, T, self.idx, self.gate, self.h, 1, stream=main)
+            # experts + combine (h += combine)
+            self.layers[L].forward(x, T, self.idx, self.gate, self.h, 1, stream=main)
             if on_layer is not None:
                 on_layer(L, self.idx, self.gate, main)
             pending = ev

@@ -247,6 +247,15 @@ def test_bad_expert_index_flagged():
             layer.stats()
         layer.reset_stats()
         layer.stats()
+        # the launch's completion counters came back to zero around the invalid slot: the
+        # next calls wait for their own gate/up units again
+        for e in (5, 1):
+            idx = torch.tensor([[e, 3]], dtype=torch.int32, device="cuda")
+            layer.forward(hd, T, idx, gate, out, 0)
+            torch.cuda.synchronize()
+            ee = oracle.expert_ffn(li.codebooks[e], li.codes[0][e], li.codes[1][e], li.codes[2][e], h[0])
+            assert_close(out[0].cpu().numpy(), 0.5 * ee + 0.5 * e3)
+        layer.stats()
     finally:
         layer.close()
 
