@@ -202,6 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
     __shared__ float red[kRouterRowsPerItem][4][kRouterTok];
     __shared__ int claimed;
     bool primed = false;
+    TabTc tcs;
+    tab_tc_open<kRecon>(tcs);
     int cur = claim(F.sync, &claimed);
     int nxt = is_copy<kBanked>(F, cur) ? -1 : claim(F.sync, &claimed);
     while (cur < n_total(F)) {
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             Unit N;
             if (has_next) N = decode_unit<false>(F.A, nxt - b_gu(F));
             run_unit<false, kRecon, kBf16, kThreads, kBanked ? kPrefetchRounds : kStepPrefetchRounds, kBanked>(
-                F.A, U, has_next, N, primed, nullptr, 0);
+                F.A, U, has_next, N, primed, tcs, nullptr, 0);
             signal(gu_done(F) + U.slot);
         } else if (cur < b_comb(F)) {
             // ---- down unit (waits inside for the gate/up units of its slot)
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
             Unit N;
             if (has_next) N = decode_unit<true>(F.A, nxt - b_dn(F));
             run_unit<true, kRecon, kBf16, kThreads, kBanked ? kPrefetchRounds : kStepPrefetchRounds, kBanked>(
-                F.A, U, has_next, N, primed, gu_done(F) + U.slot, (unsigned)(2 * F.A.gu_pairs));
+                F.A, U, has_next, N, primed, tcs, gu_done(F) + U.slot, (unsigned)(2 * F.A.gu_pairs));
             signal(dn_done(F) + (u % F.A.nrb));
         } else {
             // ---- combine rows [r0, r1) once every down unit over them is done
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_step_kernel(const FusedArgs
         nxt = is_copy<kBanked>(F, cur) ? -1 : claim(F.sync, &claimed);
     }
 
+    tab_tc_close<kRecon>(tcs);
     // the last CTA to leave puts the queue and counters back to zero
     __syncthreads();
     if (threadIdx.x == 0) {

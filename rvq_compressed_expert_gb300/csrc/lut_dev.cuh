@@ -3,6 +3,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "tc_dev.cuh"
 
 #include <type_traits>
 
@@ -16,6 +17,16 @@ constexpr int kTabStage = 65536;             // bytes per stage: 256 codes x 256
 constexpr int kTabBytes = kStages * kTabStage; // 192 KiB
 constexpr int kXsFloats = 512;               // down input staging (64 vectors x 8)
 constexpr int kCbFloats = kStages * kCodes * kVec; // 6144 floats per matrix
+// Table build on the tensor cores: tensor-memory columns of a lookup CTA (the 3 stages' tables as
+// 6 code tiles x 64 columns, then the codebook rows' TF32 heads and tails, 6 x 16 columns); one
+// half (head or tail) of the B operand, which sits at the start of the last stage's table (that
+// table is written only after every MMA has read it); the 3 mbarriers and the tensor-memory
+// address behind the down input.  (Shared memory stays within the 196 KiB carveout: 4 KiB more
+// there took the L1 cache from 60 to 28 KiB, and the decode step from 74.1 to 76.6 us.)
+constexpr uint32_t kTmCols = 512;
+constexpr uint32_t kTmA = 384;
+constexpr uint32_t kBHalf = 2 * 32 * 8 * 4;
+constexpr int kTcBytes = 32;
 constexpr int kPrefetchRounds = 1;                 // L2 prefetch distance in row-group rounds
 constexpr int kPrefetchRoundsGu = 2;               // the same for the per-phase gate/up kernel
 
@@ -221,13 +232,6 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) 
     lo = tf32_rna(x - __uint_as_float(hi));
 }
 
-// d += a (16x8, row) * b (8x8, col), TF32 inputs, fp32 accumulate
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
-                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 
 // Wait (thread 0 polls, the CTA then proceeds together) until *c >= target.  The wait
 // is bounded: after limit_ns (by default about a second) it records kErrTimeout and gives up.
@@ -259,6 +263,49 @@ __device__ __forceinline__ void wait_counter(const unsigned *c, unsigned target,
 // Dynamic shared memory of the lookup kernels (every extern __shared__ array names it).
 extern __shared__ __align__(16) unsigned char lut_smem[];
 
+// Tensor-core state of a lookup CTA across its units.
+struct TabTc {
+    uint32_t tmem;   // tensor-memory base (kTmCols columns)
+    uint32_t bar;    // shared-window address of the 3 mbarriers, one per stage
+    uint32_t bbuf;   // shared-window address of the B operand (head, then tail)
+    uint32_t builds; // table builds so far: the mbarriers' phase parity
+};
+
+// Every thread of the CTA, before its first unit: the mbarriers, and the tensor memory (warp 0
+// allocates; one lookup CTA per SM, so the columns are free).
+template <bool kRecon>
+__device__ __forceinline__ void tab_tc_open(TabTc &t) {
+    if constexpr (!kRecon) {
+        const uint32_t off = (uint32_t)kTabBytes + (uint32_t)kXsFloats * 4;
+        const uint32_t base = (uint32_t)__cvta_generic_to_shared(lut_smem);
+        t.bbuf = base + (uint32_t)(kStages - 1) * kTabStage;
+        t.bar = base + off;
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < kStages; ++s) tc::mbar_init(t.bar + 8u * (uint32_t)s, 1);
+            tc::mbar_init_fence();
+        }
+        if (threadIdx.x < 32) tc::tmem_alloc(t.bar + 8u * kStages, kTmCols);
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        t.tmem = *reinterpret_cast<volatile uint32_t *>(lut_smem + off + 8 * kStages);
+        t.builds = 0;
+    }
+}
+
+// Every thread of the CTA, after its last unit (every table build's MMAs were waited for).
+template <bool kRecon>
+__device__ __forceinline__ void tab_tc_close(const TabTc &t) {
+    if constexpr (!kRecon) {
+        tc::fence_before_sync();
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            tc::fence_after_sync();
+            tc::tmem_dealloc(t.tmem, kTmCols);
+        }
+    }
+}
+
 // One unit: tables (or, for the register-reconstruct form, the codebooks) for the unit's
 // segments, then the stream of its rows.  `primed`: this unit's codebooks were already asked
 // for by the previous unit of the CTA (else they are asked for at the start, ahead of the down
@@ -271,7 +318,7 @@ extern __shared__ __align__(16) unsigned char lut_smem[];
 template <bool kDown, bool kRecon, bool kBf16, int kNT = kThreads, int kPf = kPrefetchRounds,
           bool kPartLoads = true, bool kFixed = false>
 __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool has_next, const Unit &Nin,
-                                         bool &primed, unsigned *dep, unsigned dep_target,
+                                         bool &primed, TabTc &tcs, unsigned *dep, unsigned dep_target,
                                          unsigned long long *t_tables = nullptr, unsigned *done_prev = nullptr,
                                          unsigned *dep_used = nullptr, unsigned dep_users = 0) {
     constexpr int kNW = kNT / 32;
@@ -411,89 +458,123 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
             for (int v = 0; v < kVec; ++v) xv[p][v] = xs[p * kSegVec * kVec + lane * kVec + v];
     }
     if constexpr (!kRecon) {
-        // ---- tables T[s][c][part][column], one 64 KiB block per stage.  Per stage and part
-        // the table is the product T[c][j] = sum_v C[c][v] X[j][v] (256 codes c x 32
-        // columns j, K = 8), taken on the tensor cores as m16n8k8 TF32 MMAs (M = 16 codes,
-        // N = 8 columns) with each operand split into a TF32 head and tail (head*tail +
-        // tail*head + head*head), which keeps fp32 accuracy.  The warps form 2 teams of
-        // kNW / 2, one per part; a warp takes kMt 16-code tiles of every stage, each across
-        // all 32 columns.  Its operands come straight from global memory (L2), all in flight
-        // at once, before the barrier that frees the tables.  The MMA's D fragment already
-        // holds, per lane, 16-byte slots of the permuted column order, so the stores need no
-        // shuffles.
+        // ---- tables T[s][c][part][column], one 64 KiB block per stage.  Per stage the tables
+        // are the product T[c][n] = sum_v C[c][v] X[n][v] (256 codes c x 64 columns n of both
+        // parts, K = 8), taken on the tensor cores by tcgen05.mma kind::tf32 into tensor memory
+        // (M = 128 codes per MMA, N = 64), each operand split into a TF32 head and tail
+        // (head*tail + tail*head + head*head, in that order: fp32 accuracy).  A, the codebook
+        // rows, goes into tensor memory (row = lane): warp w stores the rows of its lane quarter
+        // for the (stage, code tile) pairs w/4 and w/4 + 4; B, the unit's 64 input vectors, goes
+        // into shared memory in the no-swizzle K-major layout, at the start of the last stage's
+        // table.  Their loads are in flight across the barrier that frees the tables; the stores
+        // follow it, and a second barrier precedes the MMAs.  One thread then issues the 18
+        // MMAs stage by stage, each stage completing its own mbarrier,
+        // and the warps copy each stage out as soon as it is complete: a 16x256b load gives the
+        // registers of an mma.sync accumulator (lanes fg and fg + 8, column pairs 2 ft), so each
+        // lane stores 16-byte slots of the permuted column order, conflict-free.
+        static_assert(kNT == 512, "the table build maps 16 warps onto the lane quarters");
         float *tab = reinterpret_cast<float *>(smem);
-        constexpr int kWpp = kNW / 2;                 // warps per part
-        constexpr int kMt = (kCodes / 16) / kWpp;     // 16-code tiles per warp and stage
-        static_assert((kCodes / 16) % kWpp == 0, "code tiles per warp");
-        const int mp = warp / kWpp, mq = warp % kWpp;
+        const int q = warp & 3, wg = warp >> 2;
         const int fg = lane >> 2, ft = lane & 3;
         const float *p0, *p1;
         unit_codebooks<kDown>(A, U, p0, p1);
-        const float *Cp = mp ? p1 : p0;
-        // A operand (codebook rows c0 + fg and c0 + fg + 8 of tile (s, i); inputs ft, ft + 4)
-        float av[kStages][kMt][4];
+        (void)p1;
+        // A: codebook row mt * 128 + 32 q + lane of stage s for the pairs j = (s, mt) = wg, wg + 4
+        float4 ca[2][2];
 #pragma unroll
-        for (int s = 0; s < kStages; ++s)
-#pragma unroll
-            for (int i = 0; i < kMt; ++i) {
-                const float *r0 = Cp + ((size_t)s * kCodes + (size_t)(mq * kMt + i) * 16 + fg) * kVec;
-                const float *r1 = r0 + 8 * kVec;
-                av[s][i][0] = __ldg(r0 + ft);
-                av[s][i][1] = __ldg(r1 + ft);
-                av[s][i][2] = __ldg(r0 + ft + 4);
-                av[s][i][3] = __ldg(r1 + ft + 4);
+        for (int jj = 0; jj < 2; ++jj) {
+            const int j = wg + 4 * jj;
+            if (j < 2 * kStages) {
+                const int c = (j & 1) * 128 + q * 32 + lane;
+                const float4 *r = reinterpret_cast<const float4 *>(p0 + ((size_t)(j >> 1) * kCodes + c) * kVec);
+                ca[jj][0] = __ldg(r);
+                ca[jj][1] = __ldg(r + 1);
             }
-        // B operand: column j = 8 nt + fg of part mp (nt = 0..3), inputs ft and ft + 4
-        float bv[4][2];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int j = 8 * nt + fg;
+        }
+        // B: element k = threadIdx.x % 8 of column n = threadIdx.x / 8 (part n / 32, vector n % 32)
+        float xb;
+        {
+            const int n = threadIdx.x >> 3, k = threadIdx.x & 7;
             if constexpr (!kDown) {
-                const int jg = (U.seg0 + mp) * kSegVec + j;
-                const bool in = jg < G.nv;
-                const size_t e0 = (size_t)t * A.gu.n_in + (size_t)min(jg, G.nv - 1) * kVec;
-                bv[nt][0] = in ? load_x1<kBf16>(A.h, e0 + ft) : 0.f;
-                bv[nt][1] = in ? load_x1<kBf16>(A.h, e0 + ft + 4) : 0.f;
+                const int jg = (U.seg0 + (n >> 5)) * kSegVec + (n & 31);
+                xb = jg < G.nv ? load_x1<kBf16>(A.h, (size_t)t * A.gu.n_in + (size_t)jg * kVec + k) : 0.f;
             } else {
-                const float *X = xs + mp * kSegVec * kVec + j * kVec;
-                bv[nt][0] = X[ft];
-                bv[nt][1] = X[ft + 4];
+                xb = xs[threadIdx.x];
             }
         }
         __syncthreads(); // the previous unit's lookups are done with the tables
         if (t_tables && threadIdx.x == 0) t_tables[1] = gtimer();
-        uint32_t bhi[4][2], blo[4][2];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int jj = 0; jj < 2; ++jj) {
+            const int j = wg + 4 * jj;
+            if (j < 2 * kStages) {
+                const float v[8] = {ca[jj][0].x, ca[jj][0].y, ca[jj][0].z, ca[jj][0].w,
+                                    ca[jj][1].x, ca[jj][1].y, ca[jj][1].z, ca[jj][1].w};
+                uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) split_tf32(bv[nt][q], bhi[nt][q], blo[nt][q]);
-        // Lane (fg, ft) ends with, for code c0 + fg (and c0 + fg + 8), the columns 2 ft + 8 nt
-        // (nt = 0..3) -- the slots of column group 2 ft -- and 2 ft + 1 + 8 nt (group 2 ft + 1).
-        // Lanes of odd fg store group 2 ft + 1 first, so each quarter-warp's 8 lanes hit 8
-        // different bank quads in both stores.
+                for (int k = 0; k < 8; ++k) split_tf32(v[k], hi[k], lo[k]);
+                const uint32_t ta = tcs.tmem + ((uint32_t)(q * 32) << 16) + kTmA + (uint32_t)j * 16;
+                tc::tmem_st8(ta, hi);
+                tc::tmem_st8(ta + 8, lo);
+            }
+        }
+        {
+            uint32_t hi, lo;
+            split_tf32(xb, hi, lo);
+            const int n = threadIdx.x >> 3, k = threadIdx.x & 7;
+            const uint32_t off = (uint32_t)((n >> 3) * 256 + (k >> 2) * 128 + (n & 7) * 16 + (k & 3) * 4);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tcs.bbuf + off), "r"(hi) : "memory");
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(tcs.bbuf + kBHalf + off), "r"(lo) : "memory");
+        }
+        tc::tmem_wait_st();
+        tc::fence_proxy_async(); // B's stores, seen by the tensor core
+        tc::fence_before_sync();
+        __syncthreads(); // A and B staged
+        tc::fence_after_sync();
+        if (threadIdx.x == 0) {
+            const uint32_t idesc = tc::idesc_tf32_f32(128, 2 * kSegVec);
+            const uint64_t bh = tc::smem_desc(tcs.bbuf, 128, 256);
+            const uint64_t bl = tc::smem_desc(tcs.bbuf + kBHalf, 128, 256);
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const uint32_t d = tcs.tmem + (uint32_t)(s * 2 + mt) * 64;
+                    const uint32_t a = tcs.tmem + kTmA + (uint32_t)(s * 2 + mt) * 16;
+                    tc::mma_tf32_ta(d, a, bl, idesc, 0);
+                    tc::mma_tf32_ta(d, a + 8, bh, idesc, 1);
+                    tc::mma_tf32_ta(d, a, bh, idesc, 1);
+                }
+                tc::mma_commit(tcs.bar + 8u * (uint32_t)s);
+            }
+        }
+        __syncwarp();
+        // Lane (fg, ft) holds, for codes c0 + fg and c0 + fg + 8, the columns 2 ft + 8 nt (nt =
+        // 0..3) -- the slots of column group 2 ft -- and 2 ft + 1 + 8 nt (group 2 ft + 1).  Lanes
+        // of odd fg store group 2 ft + 1 first, so each quarter-warp's 8 lanes hit 8 different
+        // bank quads in both stores.
         const int odd = fg & 1;
         const int g_first = 2 * ft + odd, g_second = 2 * ft + 1 - odd;
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
+            if (!tc::mbar_wait(tcs.bar + 8u * (uint32_t)s, tcs.builds & 1u)) {
+                if (lane == 0) atomicOr(A.err, kErrTimeout);
+                tc::mbar_wait(tcs.bar + 8u * (uint32_t)s, tcs.builds & 1u);
+            }
+            tc::fence_after_sync();
 #pragma unroll
-            for (int i = 0; i < kMt; ++i) {
-                const int c0 = (mq * kMt + i) * 16;
-                uint32_t ahi[4], alo[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) split_tf32(av[s][i][q], ahi[q], alo[q]);
-                float dd[4][4];
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    dd[nt][0] = dd[nt][1] = dd[nt][2] = dd[nt][3] = 0.f;
-                    mma_tf32(dd[nt], ahi, blo[nt]);
-                    mma_tf32(dd[nt], alo, bhi[nt]);
-                    mma_tf32(dd[nt], ahi, bhi[nt]);
-                }
+            for (int i = 0; i < 2; ++i) {
+                // this warp's 16 codes x 32 columns: code tile mt, half blk of its lane quarter, part mp
+                const int cb = wg * 2 + i, mt = cb >> 2, blk = (cb >> 1) & 1, mp = cb & 1;
+                float dd[16];
+                tc::tmem_ld16x256_x4(tcs.tmem + ((uint32_t)(q * 32 + blk * 16) << 16) +
+                                         (uint32_t)(s * 2 + mt) * 64 + (uint32_t)mp * kSegVec,
+                                     dd);
+                const int c0 = mt * 128 + q * 32 + blk * 16;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    float4 ev = make_float4(dd[0][2 * hh], dd[1][2 * hh], dd[2][2 * hh], dd[3][2 * hh]);
-                    float4 ov = make_float4(dd[0][2 * hh + 1], dd[1][2 * hh + 1], dd[2][2 * hh + 1],
-                                            dd[3][2 * hh + 1]);
+                    float4 ev = make_float4(dd[2 * hh], dd[4 + 2 * hh], dd[8 + 2 * hh], dd[12 + 2 * hh]);
+                    float4 ov = make_float4(dd[2 * hh + 1], dd[4 + 2 * hh + 1], dd[8 + 2 * hh + 1], dd[12 + 2 * hh + 1]);
                     const int c = c0 + fg + 8 * hh;
                     float *row = tab + (((size_t)s * kCodes + c) * 2 + mp) * kSegVec;
                     *reinterpret_cast<float4 *>(row + 4 * g_first) = odd ? ov : ev;
@@ -501,6 +582,8 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
                 }
             }
         }
+        ++tcs.builds;
+        tc::fence_before_sync();
         __syncthreads(); // tables complete
     } else {
         __syncthreads(); // the previous unit's lookups are done with the codebook rows
@@ -703,7 +786,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
 // Bytes of dynamic shared memory of a unit.
 template <bool kRecon>
 constexpr size_t unit_smem() {
-    return (kRecon ? 2 * kCbFloats * 4 : kTabBytes) + kXsFloats * 4;
+    return (kRecon ? 2 * kCbFloats * 4 : kTabBytes) + kXsFloats * 4 + (kRecon ? 0 : kTcBytes);
 }
 
 } // namespace lut

@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
     const int n_slots = lut_slot_count(A);
     const int units = kDown ? n_slots * A.npair * A.nrb : n_slots * 2 * A.gu_pairs;
     bool primed = false;
+    TabTc tcs;
+    tab_tc_open<kRecon>(tcs);
     Unit N;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const Unit U = decode_unit<kDown>(A, u);
@@ -65,10 +67,11 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
         if (has_next) N = decode_unit<kDown>(A, u + gridDim.x);
         unsigned long long t0 = 0, t_tab[2] = {0, 0};
         if (A.trace && threadIdx.x == 0) t0 = gtimer();
-        run_unit<kDown, kRecon, kBf16, kNT, kPf, true, kFixed>(A, U, has_next, N, primed, nullptr, 0,
+        run_unit<kDown, kRecon, kBf16, kNT, kPf, true, kFixed>(A, U, has_next, N, primed, tcs, nullptr, 0,
                                                                A.trace ? t_tab : nullptr);
         trace_unit(A, u, t0, t_tab);
     }
+    tab_tc_close<kRecon>(tcs);
 }
 
 // The gate/up and the down units of one call in one launch, so that a CTA starts its down
@@ -92,6 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs 
     const int d0 = G - 1 - b;
     const int mine_dn = d0 < n_dn ? (n_dn - 1 - d0) / G + 1 : 0;
     bool primed = false;
+    TabTc tcs;
+    tab_tc_open<false>(tcs);
     // slot counter of the CTA's last finished gate/up unit, bumped inside the next unit (once
     // its tables are built), or before the first down unit
     int pending = -1;
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs 
         if (A.trace && threadIdx.x == 0) t0 = gtimer();
         const Unit U = decode_unit<false>(A, u);
         run_unit<false, false, kBf16, kThreads, kPrefetchRoundsGu, true, kFixed>(
-            A, U, has_next, N, primed, nullptr, 0, A.trace ? t_tab : nullptr,
+            A, U, has_next, N, primed, tcs, nullptr, 0, A.trace ? t_tab : nullptr,
             pending >= 0 ? sync + 4 + pending : nullptr);
         trace_unit(A, u, t0, t_tab);
         pending = U.slot;
@@ -127,10 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs 
         if (A.trace && threadIdx.x == 0) t0 = gtimer();
         const Unit U = decode_unit<true>(A, u);
         run_unit<true, false, kBf16, kThreads, kPrefetchRounds, true, kFixed>(
-            A, U, has_next, N, primed, sync + 4 + U.slot, (unsigned)(2 * A.gu_pairs), A.trace ? t_tab : nullptr,
+            A, U, has_next, N, primed, tcs, sync + 4 + U.slot, (unsigned)(2 * A.gu_pairs), A.trace ? t_tab : nullptr,
             nullptr, sync + 4 + A.slots + U.slot, (unsigned)(A.npair * A.nrb));
         trace_unit(A, n_gu + u, t0, t_tab);
     }
+    tab_tc_close<false>(tcs);
 }
 
 // out[t] (mode 0: =, 1: +=, 2: = h +) sum_i gate[t][i] * sum_pair part_dn[t*k+i][pair],

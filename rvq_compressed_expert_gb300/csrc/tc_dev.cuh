@@ -99,6 +99,14 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor of kind::tf32: TF32 A and B (both K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+    return (1u << 4)                       // D format: f32
+           | (2u << 7) | (2u << 10)        // A, B format: tf32
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -119,6 +127,17 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uin
                  "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T with TF32 operands, issued by one thread: A (M = 128 rows x
+// K = 8) read from tensor memory -- row m in lane m, one element per 32-bit column -- starting at
+// column a_tmem.
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
 // The mbarrier at addr receives one arrival once every tcgen05 operation this thread
 // issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t mbar_addr) {
@@ -132,6 +151,24 @@ __device__ __forceinline__ void mma_commit(uint32_t mbar_addr) {
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+                   "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 lanes x 32 columns from lane base `taddr` (within the warp's lane quarter), in the
+// register layout of an mma.sync m16n8 accumulator repeated over 4 groups of 8 columns: thread
+// t holds, for group r, v[4r .. 4r+3] = (lane t/4, columns 8r + 2(t%4) and + 1), then the same
+// columns of lane t/4 + 8.  The wait sits in the same statement.
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x4.b32 "
                  "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
                  "tcgen05.wait::ld.sync.aligned;"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
