@@ -265,6 +265,23 @@ int waste_moe_set_trace(waste_moe *h, uint64_t *d_trace, int32_t n_items);
 int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_t n_prefetch,
                        waste_stream_t side);
 
+/* Lookahead inside the step (page "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s", section
+ * "Lecture anticipée et prédiction du routeur": layer L+1's router runs on layer L's input and its
+ * top experts are fetched ahead), for one-token calls on resident layers, with no extra launch
+ * and no side stream.  After this call, a one-token waste_moe_route on h also runs next_layer's
+ * router rows on the same input (the extra rows ride on h's router launch), and the
+ * waste_moe_forward that follows it (or waste_moe_step) takes next_layer's top n_prefetch experts
+ * from those logits -- the order of next_layer's own top-k -- as its prediction (scored by
+ * next_layer's next route, as after waste_moe_prefetch) and asks L2 for the same pieces as
+ * waste_moe_prefetch, from the CTAs of h's expert kernel that have no down unit once their
+ * gate/up units are done.  Outputs and demand bytes are unchanged.  next_layer = NULL or
+ * n_prefetch = 0 turns it off.  Errors: WASTE_EINVAL for NULL h, n_prefetch outside
+ * [0, min(n_experts, 32)], a next layer with another hidden size or activation type or more than
+ * 512 experts, or banked handles (they take waste_moe_prefetch).  A call whose shapes do not
+ * allow it (several tokens, a router launch that would not fit with the extra rows) runs without
+ * it.  h's step and next_layer's route must be ordered on one stream (or by events). */
+int waste_moe_set_lookahead(waste_moe *h, waste_moe *next_layer, int32_t n_prefetch);
+
 /* Free the workspace and the handle (NULL is ignored).  Synchronises the device. */
 void waste_moe_destroy(waste_moe *h);
 

@@ -36,6 +36,7 @@ EXPORTED = ["waste_moe_record_layout", "waste_moe_pack_records", "waste_moe_crea
             "waste_moe_topk_from_logits", "waste_moe_set_profiling", "waste_moe_read_profile",
             "waste_moe_rmsnorm", "waste_moe_forward_noalloc", "waste_moe_step", "waste_moe_set_trace",
             "waste_bank_create", "waste_bank_destroy", "waste_bank_reset", "waste_bank_stats",
+            "waste_moe_set_lookahead",
             "waste_moe_create_banked", "waste_rvq_train", "waste_rvq_encode", "waste_moe_debug_wait"]
 
 
@@ -108,6 +109,7 @@ def load(path: str = LIB_PATH):
     lib.waste_moe_rmsnorm.argtypes = [vp, vp, i32, i32, vp]
     lib.waste_moe_step.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, vp]
     lib.waste_moe_set_trace.argtypes = [vp, vp, i32]
+    lib.waste_moe_set_lookahead.argtypes = [vp, vp, i32]
     lib.waste_moe_forward_noalloc.argtypes = [cfgp, vp, sz, vp, vp, i32, vp, vp, vp, i32, vp]
     lib.waste_bank_create.argtypes = [cfgp, i32, vp, sz, i32, ctypes.POINTER(vp)]
     lib.waste_bank_destroy.argtypes = [vp]
@@ -228,6 +230,11 @@ def waste_moe_topk_from_logits(d_logits, T, E, k, d_idx, d_gate, stream=None):
 
 def waste_moe_set_profiling(h, enable=True):
     return _check(load().waste_moe_set_profiling(h, int(bool(enable))))
+
+
+def waste_moe_set_lookahead(h, next_layer, n_prefetch):
+    """The lookahead inside h's one-token steps into next_layer (None or 0: off)."""
+    return _check(load().waste_moe_set_lookahead(h, next_layer, n_prefetch))
 
 
 def waste_moe_read_profile(h) -> dict:

@@ -29,6 +29,11 @@ struct waste_moe {
     int mma_min_tokens; // tokens an expert needs in one call to take the tensor-core path
     waste_bank *bank;   // records live in this bank (layer bank_layer), or null
     int bank_layer;
+    // the lookahead inside the step (waste_moe_set_lookahead): the next layer and P, and whether
+    // the last route also ran the next layer's router rows (the forward then predicts)
+    waste_moe *ahead_next;
+    int ahead_P;
+    bool ahead_routed;
 };
 
 namespace {
@@ -278,6 +283,9 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     H->trace_cap = 0;
     H->bank = nullptr;
     H->bank_layer = 0;
+    H->ahead_next = nullptr;
+    H->ahead_P = 0;
+    H->ahead_routed = false;
     LayerView &L = H->L;
     L.router_w = d_router_w;
     L.router_b = d_router_bias;
@@ -334,6 +342,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
         G * grouped_tile_rows((int)S, (int)max_chunks) * ((L.f + 63) / 64) * 128, // grp.ag
         (T > 16 ? (size_t)kRouterMaxSplits * T * E * 4 : 0), // router_part
         (size_t)E * 8,                              // route_slots
+        (size_t)E * 8,                              // ahead_keys
     };
     const int n_parts = (int)(sizeof sizes / sizeof sizes[0]);
     size_t offs[32], total = 0;
@@ -378,6 +387,7 @@ int waste_moe_create(const waste_moe_config *cfg, const float *d_router_w,
     Gp.ag = grouped ? reinterpret_cast<uint8_t *>(b + offs[21]) : nullptr;
     Gp.max_chunks = grouped ? (int)max_chunks : 0;
     W.router_part = T > 16 ? reinterpret_cast<float *>(b + offs[22]) : nullptr;
+    W.ahead_keys = reinterpret_cast<unsigned long long *>(b + offs[24]);
     W.route_slots = reinterpret_cast<unsigned long long *>(b + offs[23]);
     ce = cudaMemset(base, 0, total);
     if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
@@ -478,6 +488,17 @@ int waste_moe_route(waste_moe *h, const void *d_h, int32_t T, int32_t *d_idx, fl
     const int pred_stride = h->pred_P > 0 ? h->pred_P : 1;
     RouteTopk F{h->W.route_done, h->L.k, d_idx, d_gate, h->W.pred_idx, h->W.pred_count, pred_stride, h->W.stats,
                 router_bytes, h->W.route_slots};
+    // the lookahead inside the step: the next layer's router rows ride on this launch
+    const waste_moe *nx = h->ahead_next;
+    h->ahead_routed = false;
+    if (nx && h->ahead_P > 0 && T == 1 && nx->L.d == h->L.d && nx->L.act_bf16 == h->L.act_bf16 &&
+        ((uintptr_t)nx->L.router_w & 15) == 0 && route_polled_fits(h->L, d_h, T, nx->L.E, h->num_sms)) {
+        F.ahead_w = nx->L.router_w;
+        F.ahead_b = nx->L.router_b;
+        F.ahead_E = nx->L.E;
+        F.ahead_keys = nx->W.ahead_keys;
+        h->ahead_routed = true;
+    }
     bool fused = false;
     cudaError_t e = launch_router(h->L, d_h, T, logits, h->W.logits_lo, s, h->W.router_part, h->num_sms, &F, &fused,
                                   h->W.err);
@@ -515,6 +536,9 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
     if (mode < 0 || mode > 2) return fail(WASTE_EINVAL, "mode = %d", mode);
     if (mode == 2 && h->cfg.act_dtype != WASTE_ACT_F32)
         return fail(WASTE_EINVAL, "mode 2 (out = h + y) needs fp32 hidden states");
+    // whether the route in front of this call ran the next layer's router rows (consumed here)
+    const bool ahead = h->ahead_routed;
+    h->ahead_routed = false;
     if (T == 0) return ok();
     if (!d_idx || !d_gate || !d_out) return fail(WASTE_EINVAL, "NULL idx, gate or out");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -559,8 +583,29 @@ int waste_moe_forward(waste_moe *h, const void *d_h, int32_t T, const int32_t *d
             h->fwd_tm.n = 0;
         }
     } else {
+        // the lookahead inside the step, when the route that produced d_idx also ran the next
+        // layer's router rows
+        LutAhead LA{};
+        if (ahead && h->ahead_next && T == 1) {
+            waste_moe *nx = h->ahead_next;
+            LA.keys = nx->W.ahead_keys;
+            LA.E = nx->L.E;
+            LA.P = h->ahead_P;
+            LA.pred_idx = nx->W.pred_idx;
+            LA.pred_count = nx->W.pred_count;
+            LA.records = nx->L.records;
+            LA.stride = nx->L.stride;
+            LA.off_gate = nx->L.sec_off[0];
+            LA.off_up = nx->L.sec_off[1];
+            LA.nseg = nx->L.gu.nseg;
+            LA.groups = nx->L.gu.groups;
+            LA.codebooks = nx->L.codebooks;
+            LA.stats = nx->W.stats;
+            nx->pred_P = h->ahead_P;
+        }
         e = launch_lut_forward(h->L, h->W, d_h, T, d_idx, d_gate, d_out, mode, recon, h->num_sms, s,
-                               h->profiling ? &h->fwd_tm : nullptr, h->trace, h->trace_cap);
+                               h->profiling ? &h->fwd_tm : nullptr, h->trace, h->trace_cap,
+                               LA.keys ? &LA : nullptr);
         if (h->profiling) h->step_tm.n = 0;
     }
     if (e != cudaSuccess) return cuda_fail(e, "expert kernels");
@@ -634,6 +679,27 @@ int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_
     }
     e = launch_prefetch_l2(h->L, h->W.pred_idx, P, T, P, h->W.pred_count, h->W.stats, s);
     if (e != cudaSuccess) return cuda_fail(e, "L2 prefetch");
+    return ok();
+}
+
+int waste_moe_set_lookahead(waste_moe *h, waste_moe *next_layer, int32_t n_prefetch) {
+    const NvtxRange nvtx_range(__func__);
+    if (!h) return fail(WASTE_EINVAL, "NULL handle");
+    if (!next_layer || n_prefetch == 0) {
+        h->ahead_next = nullptr;
+        h->ahead_P = 0;
+        h->ahead_routed = false;
+        return ok();
+    }
+    if (n_prefetch < 0 || n_prefetch > next_layer->L.E || n_prefetch > kMaxTopK)
+        return fail(WASTE_EINVAL, "n_prefetch = %d outside [0, min(n_experts, %d)]", n_prefetch, kMaxTopK);
+    if (next_layer->L.d != h->L.d || next_layer->L.act_bf16 != h->L.act_bf16)
+        return fail(WASTE_EINVAL, "the next layer's hidden size or activation type differs");
+    if (next_layer->L.E > 512) return fail(WASTE_EINVAL, "the next layer has more than 512 experts");
+    if (h->bank || next_layer->bank) return fail(WASTE_EINVAL, "banked layers take waste_moe_prefetch");
+    h->ahead_next = next_layer;
+    h->ahead_P = n_prefetch;
+    h->ahead_routed = false;
     return ok();
 }
 

@@ -142,7 +142,43 @@ struct RouteTopk {
     unsigned long long *stats;
     unsigned long long router_bytes;
     unsigned long long *slots; // [E] one-token router: each expert's selection key, 0 at rest
+    // optional, polled one-token router only: the next layer's router rows on the same input
+    // (ahead_E experts, weights ahead_w, bias ahead_b), whose selection keys go to ahead_keys
+    const float *ahead_w, *ahead_b;
+    int ahead_E;
+    unsigned long long *ahead_keys;
 };
+
+// L2 prefetch of a predicted expert (the lookahead).  With every expert resident in HBM the only
+// gain is the first read of each unit, so the lookahead asks L2 for what the gate/up units of
+// the expert read first -- the first kLookaheadGroups row groups of each 32-vector segment of
+// gate and up (one round of a 16-warp unit's row stream) -- and the expert's gate and up
+// codebooks: about 1.4 MB per expert at d = 7168, f = 1536, small enough to stay in L2 while the
+// current layer streams, where whole records (12.4 MB each) were evicted before use and read
+// twice.  Piece i of an expert: the segments of gate (i < nseg) and up, then the codebooks.
+constexpr int kLookaheadGroups = 16;
+constexpr uint32_t kLookaheadCbBytes = 2 * kStages * kCodes * kVec * 4; // gate and up codebooks
+
+__host__ __device__ inline int lookahead_pieces(int nseg) { return 2 * nseg + 1; }
+__host__ __device__ inline unsigned long long lookahead_bytes(int nseg, int groups) {
+    const int g = groups < kLookaheadGroups ? groups : kLookaheadGroups;
+    return (unsigned long long)2 * nseg * (unsigned long long)(g * (kStages * 512)) + kLookaheadCbBytes;
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ void lookahead_piece(const uint8_t *records, size_t stride, size_t off_gate,
+                                                size_t off_up, int nseg, int groups, const float *codebooks,
+                                                int e, int i) {
+    if (i < 2 * nseg) {
+        const uint32_t seg_bytes = (uint32_t)min(groups, kLookaheadGroups) * (kStages * 512);
+        const uint8_t *q = records + (size_t)e * stride + (i < nseg ? off_gate : off_up) +
+                           (size_t)(i % nseg) * groups * (kStages * 512);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(q), "r"(seg_bytes) : "memory");
+    } else {
+        const float *cb = codebooks + (size_t)e * 3 * kStages * kCodes * kVec;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cb), "r"(kLookaheadCbBytes) : "memory");
+    }
+}
+#endif
 
 // Slots of a batched call grouped by expert (see grouped.cu).
 struct Grouping {
@@ -176,6 +212,7 @@ struct Workspace {
     int32_t *bank_order; // [max_slots] banked calls: slots in the order their units run
     unsigned *route_done; // router CTAs finished (the router launch that also takes the top-k)
     unsigned long long *route_slots; // [E] one-token router's selection keys, zero at rest
+    unsigned long long *ahead_keys;  // [E] this layer's selection keys from the previous layer's router launch
     Grouping grp;        // batched calls only (null pointers when max_tokens == 1)
     float *router_part;  // [kRouterMaxSplits][max_T][E] when max_T > 16, else null
     void *base;
@@ -193,6 +230,8 @@ constexpr int kRouterMaxSplits = 32;
 cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logits,
                           float *logits_lo, cudaStream_t s, float *part = nullptr, int num_sms = 1,
                           const RouteTopk *fuse = nullptr, bool *fused = nullptr, uint32_t *err = nullptr);
+// Whether the polled one-token router fits with ahead_E more expert rows (the next layer's).
+bool route_polled_fits(const LayerView &L, const void *h, int T, int ahead_E, int num_sms);
 cudaError_t launch_topk(const float *logits, const float *logits_lo, int T, int E, int k,
                         int32_t *idx, float *gate, const int32_t *pred_idx, int32_t *pred_count,
                         int pred_stride, unsigned long long *stats,
@@ -203,11 +242,27 @@ struct Timing {
     cudaEvent_t ev[8];
     int n;
 };
-// trace (optional): per-unit trace of the two lookup kernels, trace_cap units.
+// The lookahead inside a one-token expert launch: the next layer's top-P experts, chosen from the
+// selection keys its router rows produced in this layer's router launch (same input), and their
+// first pieces asked of L2 (lookahead_piece) by the CTAs that have no down unit, once their
+// gate/up units are done.
+struct LutAhead {
+    const unsigned long long *keys; // [E] the next layer's selection keys; null: no lookahead
+    int E, P;
+    int32_t *pred_idx, *pred_count;  // the next layer's prediction (P experts, rank order)
+    const uint8_t *records;          // the next layer's records and codebooks
+    size_t stride, off_gate, off_up;
+    int nseg, groups;
+    const float *codebooks;
+    unsigned long long *stats;       // the next layer's counters (prefetched bytes and experts)
+};
+// trace (optional): per-unit trace of the two lookup kernels, trace_cap units.  ahead
+// (optional): the lookahead of a one-token call (taken by the one-launch expert kernel only).
 cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
                                const int32_t *idx, const float *gate, float *out, int mode,
                                bool reconstruct, int num_sms, cudaStream_t s, Timing *tm,
-                               unsigned long long *trace = nullptr, int trace_cap = 0);
+                               unsigned long long *trace = nullptr, int trace_cap = 0,
+                               const LutAhead *ahead = nullptr);
 // Down partials per slot written by the lookup kernels (one per pair of segments).
 inline int down_parts(const LayerView &L) { return (L.dn.nseg + 1) / 2; }
 // One lookup phase (gate/up or down) over the slots listed on the device.

@@ -32,6 +32,7 @@
 // rebuilds each 8-weight vector in registers (3 codebook rows summed) before an
 // 8-term dot product.
 #include "lut_dev.cuh"
+#include "route_dev.cuh"
 
 namespace wm {
 
@@ -86,8 +87,55 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
 // built, so that the fence of the count runs beside that unit's rows (the CTA's last gate/up
 // unit is counted before its first down unit).  Same unit arithmetic as the per-phase kernels:
 // the results are bit-identical to theirs.
+// The lookahead's share of lookahead CTA k of n_la (inside the one-launch expert kernel): CTA 0
+// selects the next layer's top-P experts from its selection keys (warp sorts merged in a tree,
+// the order of the router's own selection), stores them as that layer's prediction and
+// publishes it on sync[2]; every lookahead CTA then waits for it (bounded) and asks L2 for its
+// share of the predicted experts' pieces.  The last one to finish puts sync[2..3] back to zero.
+__device__ __noinline__ void lookahead_item(const LutAhead LA, unsigned *sync, int k, int n_la, uint32_t *err) {
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(lut_smem);
+    int *ids = reinterpret_cast<int *>(lut_smem + 8 * kThreads);
+    __syncthreads(); // the CTA's last unit is done with its shared memory
+    if (k == 0) {
+        route::Cand c;
+        c.key = 0ull;
+        c.id = 0x7fffffff;
+        if ((int)threadIdx.x < LA.E) {
+            c.key = LA.keys[threadIdx.x];
+            c.id = threadIdx.x;
+        }
+        route::warp_sort32(c);
+        route::merge_warp_lists(c, keys, ids);
+        __syncthreads();
+        if ((int)threadIdx.x < LA.P) LA.pred_idx[threadIdx.x] = ids[threadIdx.x];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            *LA.pred_count = LA.P;
+            if (LA.stats) {
+                atomicAdd(LA.stats + kStatPrefetchBytes, (unsigned long long)LA.P * lookahead_bytes(LA.nseg, LA.groups));
+                atomicAdd(LA.stats + kStatPrefetchExperts, (unsigned long long)LA.P);
+            }
+            __threadfence();
+            atomicExch(sync + 2, 1u);
+        }
+    }
+    wait_counter(sync + 2, 1u, err);
+    const int per = lookahead_pieces(LA.nseg);
+    for (int j = k + n_la * (int)threadIdx.x; j < LA.P * per; j += n_la * (int)blockDim.x) {
+        const int e = __ldcg(LA.pred_idx + j / per);
+        if (e >= 0 && e < LA.E)
+            lookahead_piece(LA.records, LA.stride, LA.off_gate, LA.off_up, LA.nseg, LA.groups, LA.codebooks, e,
+                            j % per);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(sync + 3, 1u) == (unsigned)n_la - 1) {
+        sync[2] = 0u;
+        sync[3] = 0u;
+    }
+}
+
 template <bool kBf16, bool kFixed>
-__global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs A, unsigned *sync) {
+__global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs A, unsigned *sync, const LutAhead LA) {
     const int n_gu = A.slots * 2 * A.gu_pairs;
     const int n_dn = A.slots * A.npair * A.nrb;
     const int G = gridDim.x, b = blockIdx.x;
@@ -123,6 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs 
             atomicAdd(sync + 4 + pending, 1u);
         }
     }
+    // the lookahead: the CTAs without a down unit (or, if every CTA has one, CTA 0 at its end)
+    const int n_la = n_dn < G ? G - n_dn : 1;
+    if (LA.keys && n_dn < G && mine_dn == 0) lookahead_item(LA, sync, b, n_la, A.err);
     for (int i = 0; i < mine_dn; ++i) {
         const int u = d0 + i * G;
         const bool has_next = i + 1 < mine_dn;
@@ -136,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs 
             nullptr, sync + 4 + A.slots + U.slot, (unsigned)(A.npair * A.nrb));
         trace_unit(A, n_gu + u, t0, t_tab);
     }
+    if (LA.keys && n_dn >= G && b == 0) lookahead_item(LA, sync, 0, 1, A.err);
     tab_tc_close<false>(tcs);
 }
 
@@ -281,7 +333,7 @@ bool coop_launch_ok() {
 }
 
 template <bool kBf16, bool kFixed>
-cudaError_t launch_experts_v(const LutArgs &A, unsigned *sync, int grid, cudaStream_t s) {
+cudaError_t launch_experts_v(const LutArgs &A, unsigned *sync, const LutAhead &LA, int grid, cudaStream_t s) {
     const size_t smem = unit_smem<false>();
     static SmemAttr attr;
     cudaError_t e = ensure_smem(attr, (const void *)lut_experts_kernel<kBf16, kFixed>, (int)smem);
@@ -296,17 +348,20 @@ cudaError_t launch_experts_v(const LutArgs &A, unsigned *sync, int grid, cudaStr
     at[0].val.cooperative = 1;
     lc.attrs = at;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, lut_experts_kernel<kBf16, kFixed>, A, sync);
+    return cudaLaunchKernelEx(&lc, lut_experts_kernel<kBf16, kFixed>, A, sync, LA);
 }
 
 // The gate/up and down units in one cooperative launch of at most one CTA per SM.
-cudaError_t launch_experts(const LutArgs &A, unsigned *sync, bool bf16, int num_sms, cudaStream_t s) {
+cudaError_t launch_experts(const LutArgs &A, unsigned *sync, const LutAhead &LA, bool bf16, int num_sms,
+                           cudaStream_t s) {
     const int n_gu = A.slots * 2 * A.gu_pairs, n_dn = A.slots * A.npair * A.nrb;
     const int units = n_gu > n_dn ? n_gu : n_dn;
     const int grid = units < num_sms ? units : num_sms;
     if (tables_at_fixed_base(s))
-        return bf16 ? launch_experts_v<true, true>(A, sync, grid, s) : launch_experts_v<false, true>(A, sync, grid, s);
-    return bf16 ? launch_experts_v<true, false>(A, sync, grid, s) : launch_experts_v<false, false>(A, sync, grid, s);
+        return bf16 ? launch_experts_v<true, true>(A, sync, LA, grid, s)
+                    : launch_experts_v<false, true>(A, sync, LA, grid, s);
+    return bf16 ? launch_experts_v<true, false>(A, sync, LA, grid, s)
+                : launch_experts_v<false, false>(A, sync, LA, grid, s);
 }
 
 } // namespace
@@ -398,7 +453,7 @@ cudaError_t launch_combine(const LayerView &L, const Workspace &W, const void *h
 cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const void *h, int T,
                                const int32_t *idx, const float *gate, float *out, int mode,
                                bool reconstruct, int num_sms, cudaStream_t s, Timing *tm,
-                               unsigned long long *trace, int trace_cap) {
+                               unsigned long long *trace, int trace_cap, const LutAhead *ahead) {
     LutArgs A = make_lut_args(L, W, h, T, idx, num_sms);
     A.trace = trace;
     A.trace_cap = trace ? trace_cap : 0;
@@ -407,7 +462,10 @@ cudaError_t launch_lut_forward(const LayerView &L, const Workspace &W, const voi
     if (!reconstruct && W.sync && coop_launch_ok()) {
         // gate/up and down units in one launch, then the combine
         A.trace_base = 0;
-        cudaError_t e = launch_experts(A, W.sync, bf16, num_sms, s);
+        LutAhead LA{};
+        if (ahead && ahead->keys && T == 1 && ahead->E <= kThreads && ahead->P >= 1 && ahead->P <= kMaxTopK)
+            LA = *ahead;
+        cudaError_t e = launch_experts(A, W.sync, LA, bf16, num_sms, s);
         if (e != cudaSuccess) return e;
         if (tm) cudaEventRecord(tm->ev[1], s);
         e = launch_combine(L, W, h, T, idx, gate, out, mode, nullptr, down_parts(L), s);

@@ -315,8 +315,15 @@ __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__r
             return;
         }
     }
-    const int row0 = blockIdx.x * kRows;
-    const int rows = min(kRows, E - row0);
+    // the CTAs past this layer's rows take the next layer's rows (F.ahead_w: the lookahead)
+    const int grid1 = (E + kRows - 1) / kRows;
+    const bool ahead = kPoll && (int)blockIdx.x >= grid1;
+    if (ahead) {
+        W = F.ahead_w;
+        bias = F.ahead_b;
+    }
+    const int row0 = (ahead ? (int)blockIdx.x - grid1 : (int)blockIdx.x) * kRows;
+    const int rows = min(kRows, (ahead ? F.ahead_E : E) - row0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rl = warp >> 2, sub = warp & 3;
     const uint32_t wbytes = (uint32_t)d * 4u, hbytes = (uint32_t)d * (kBf16 ? 2u : 4u);
@@ -386,9 +393,13 @@ __global__ void __launch_bounds__(128 * kRows) router_t1_kernel(const float *__r
         const float v = ((q[0] + q[1]) + q[2]) + q[3];
         float hi = v, lo = 0.f;
         if (bias) two_sum(v, bias[r], hi, lo);
-        logits[r] = hi;
-        if (logits_lo) logits_lo[r] = lo;
-        if constexpr (kPoll) st_relaxed_u64(F.slots + r, cand_key(hi, lo));
+        if (ahead) {
+            F.ahead_keys[r] = cand_key(hi, lo);
+        } else {
+            logits[r] = hi;
+            if (logits_lo) logits_lo[r] = lo;
+            if constexpr (kPoll) st_relaxed_u64(F.slots + r, cand_key(hi, lo));
+        }
     }
     if (kPoll || !F.done) return;
     __syncthreads(); // this CTA's logits before its count
@@ -439,15 +450,7 @@ __global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logi
               stats, router_bytes, smem_topk);
 }
 
-// L2 prefetch of predicted experts: one CTA per (token, rank).  With every expert resident in
-// HBM the only gain is the first read of each unit, so the prefetch asks L2 for what the
-// gate/up units of the expert read first -- the first kLookaheadGroups row groups of each
-// 32-vector segment of gate and up (one round of a 16-warp unit's row stream) -- and the
-// expert's gate and up codebooks: about 1.4 MB per expert at d = 7168, f = 1536, small enough
-// to stay in L2 while the current layer streams, where whole records (12.4 MB each) were
-// evicted before use and read twice.
-constexpr int kLookaheadGroups = 16;
-
+// L2 prefetch of predicted experts: one CTA per (token, rank), the pieces of lookahead_piece.
 __global__ void __launch_bounds__(128) prefetch_l2_kernel(const uint8_t *__restrict__ records, size_t stride,
                                                           size_t off_gate, size_t off_up, int nseg, int groups,
                                                           const float *__restrict__ codebooks, int E,
@@ -457,20 +460,11 @@ __global__ void __launch_bounds__(128) prefetch_l2_kernel(const uint8_t *__restr
     const int t = blockIdx.x / P, p = blockIdx.x % P;
     const int e = pred_idx[(size_t)t * pred_stride + p];
     if (e < 0 || e >= E) return;
-    const uint8_t *rec = records + (size_t)e * stride;
-    const uint32_t seg_bytes = (uint32_t)min(groups, kLookaheadGroups) * (kStages * 512);
-    for (int i = threadIdx.x; i < 2 * nseg; i += blockDim.x) {
-        const uint8_t *q = rec + (i < nseg ? off_gate : off_up) + (size_t)(i % nseg) * groups * (kStages * 512);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(q), "r"(seg_bytes) : "memory");
-    }
-    constexpr uint32_t kCbBytes = 2 * kStages * kCodes * kVec * 4; // gate and up codebooks
-    if (threadIdx.x == 0) {
-        const float *cb = codebooks + (size_t)e * 3 * kStages * kCodes * kVec;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cb), "r"(kCbBytes) : "memory");
-        if (stats) {
-            atomicAdd(stats + kStatPrefetchBytes, (unsigned long long)2 * nseg * seg_bytes + kCbBytes);
-            atomicAdd(stats + kStatPrefetchExperts, 1ull);
-        }
+    for (int i = threadIdx.x; i < lookahead_pieces(nseg); i += blockDim.x)
+        lookahead_piece(records, stride, off_gate, off_up, nseg, groups, codebooks, e, i);
+    if (threadIdx.x == 0 && stats) {
+        atomicAdd(stats + kStatPrefetchBytes, lookahead_bytes(nseg, groups));
+        atomicAdd(stats + kStatPrefetchExperts, 1ull);
     }
 }
 
@@ -522,6 +516,15 @@ static bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 // Whether `ctas` CTAs of the one-token router can all be resident at once on the current
 // device (one per SM: each holds over 100 KiB of shared memory) and the device takes
 // cooperative launches: the polled form's top-k CTA waits for the others.
+static bool t1_poll_fits(int ctas, int num_sms);
+
+bool route_polled_fits(const LayerView &L, const void *h, int T, int ahead_E, int num_sms) {
+    const size_t t1_smem = (size_t)L.d * (4 * kT1Rows + (L.act_bf16 ? 2 : 4));
+    const int ctas = (L.E + kT1Rows - 1) / kT1Rows + (ahead_E + kT1Rows - 1) / kT1Rows + 1;
+    return T == 1 && (size_t)L.d * 4 <= kRouterStageMax && t1_smem <= kT1SmemMax && aligned16(L.router_w) &&
+           aligned16(h) && L.E <= 128 * kT1Rows && t1_poll_fits(ctas, num_sms);
+}
+
 static bool t1_poll_fits(int ctas, int num_sms) {
     static std::atomic<int> coop[kMaxDevices];
     int dev = 0;
@@ -571,7 +574,8 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
         if (T == 1 && fuse && fused && t1_smem <= kT1SmemMax && aligned16(L.router_w) && aligned16(h)) {
             const RouteTopk F = *fuse;
             const int grid1 = (L.E + kT1Rows - 1) / kT1Rows;
-            if (F.slots && L.E <= 128 * kT1Rows && t1_poll_fits(grid1 + 1, num_sms)) {
+            const int grid2 = F.ahead_w ? (F.ahead_E + kT1Rows - 1) / kT1Rows : 0;
+            if (F.slots && L.E <= 128 * kT1Rows && t1_poll_fits(grid1 + grid2 + 1, num_sms)) {
                 // polled: the row CTAs and one top-k CTA, resident together
                 static SmemAttr attr_p[2];
                 const void *kfn = L.act_bf16 ? (const void *)router_t1_kernel<true, kT1Rows, true>
@@ -579,7 +583,7 @@ cudaError_t launch_router(const LayerView &L, const void *h, int T, float *logit
                 ea = ensure_smem(attr_p[L.act_bf16 ? 1 : 0], kfn, (int)kT1SmemMax);
                 if (ea != cudaSuccess) return ea;
                 cudaLaunchConfig_t lc = {};
-                lc.gridDim = dim3(grid1 + 1);
+                lc.gridDim = dim3(grid1 + grid2 + 1);
                 lc.blockDim = dim3(128 * kT1Rows);
                 lc.dynamicSmemBytes = t1_smem;
                 lc.stream = s;

@@ -10,8 +10,9 @@ routeur"):
     its top-P experts are prefetched into L2 (waste_moe_prefetch),
   - on the main stream layer L applies its experts:
     h_{L+1} = h_L + combine (waste_moe_forward, mode 1, in place).
-The real router of each layer decides its experts, so the lookahead changes
-neither the outputs nor the demand bytes.  The side stream starts behind layer
+For one token the lookahead instead runs inside each layer's step, with no side
+stream (waste_moe_set_lookahead).  The real router of each layer decides its
+experts, so the lookahead changes neither the outputs nor the demand bytes.  The side stream starts behind layer
 L's route, not beside it: the expert kernel is one cooperative launch that
 needs every SM at once, and side-stream kernels still running when it is due
 would hold it back; behind the route they fill the SMs that the expert kernel's
@@ -53,6 +54,8 @@ class DecodeStack:
         pending = None
         if self.banked:
             return self._run_banked(lookahead, main, side, on_layer)
+        if T == 1:
+            return self._run_one_token(lookahead, main, on_layer)
         for L in range(n):
             x = self.x[L & 1]
             B.waste_moe_rmsnorm(self.h, x, T, self.d, main)
@@ -72,6 +75,23 @@ class DecodeStack:
             pending = ev
         if pending is not None:
             main.wait_event(pending)
+        return self.h
+
+    def _run_one_token(self, lookahead, main, on_layer):
+        """One token: the lookahead runs inside each layer's step (waste_moe_set_lookahead): layer
+        L's router launch also runs layer L+1's router rows on x_L, and layer L's expert kernel
+        predicts L+1's top-P experts and asks L2 for them with the SMs it leaves idle at its end.
+        No side stream."""
+        n = len(self.layers)
+        for L in range(n):
+            nxt = self.layers[L + 1].handle if lookahead and L + 1 < n else None
+            B.waste_moe_set_lookahead(self.layers[L].handle, nxt, lookahead if nxt is not None else 0)
+        for L in range(n):
+            x = self.x[L & 1]
+            B.waste_moe_rmsnorm(self.h, x, 1, self.d, main)
+            self.layers[L].step(x, 1, self.idx, self.gate, self.h, 1, stream=main)
+            if on_layer is not None:
+                on_layer(L, self.idx, self.gate, main)
         return self.h
 
     def _run_banked(self, lookahead, main, side, on_layer):

@@ -29,6 +29,8 @@ def _built():
 
 
 SMALL = synth.Workload("small-stack", 512, 256, 16, 4, 2, "f32", "offsets", n_layers=6, lookahead=3)
+# one token: the lookahead runs inside each layer's step (no side stream)
+SMALL_ONE = synth.Workload("small-stack-1", 512, 256, 16, 4, 1, "f32", "offsets", n_layers=6, lookahead=3)
 
 
 def make_layers(w, seed=0, device="cuda"):
@@ -49,8 +51,8 @@ def run_eager(stack, h0, P, record=None):
     return out.clone()
 
 
-def test_stack_lookahead_invariant_and_matches_oracle():
-    w = SMALL
+@pytest.mark.parametrize("w", [SMALL, SMALL_ONE], ids=["two-tokens", "one-token"])
+def test_stack_lookahead_invariant_and_matches_oracle(w):
     pairs = make_layers(w)
     layers = [p[0] for p in pairs]
     try:
@@ -252,3 +254,61 @@ def test_lookahead_with_mispredictions():
     finally:
         for l in layers:
             l.close()
+
+
+def test_lookahead_inside_the_step_predicts_its_own_route():
+    """waste_moe_set_lookahead with the layer as its own next layer: the step's router launch runs
+    the layer's rows twice on the same input, its expert kernel predicts the top-P from the second
+    set and prefetches them; the next step on the same input scores that prediction: every one of
+    the P experts is among its top-k.  Outputs equal those without the lookahead, bit for bit."""
+    w = synth.Workload("la-self", 1032, 136, 40, 6, 1, "f32", "none")
+    layer = MoELayer(w, 0, 0, "cuda")
+    plain = MoELayer(w, 0, 0, "cuda")
+    try:
+        idx, gate, logits, out = layer.alloc_outputs(1)
+        idx2, gate2, logits2, out2 = plain.alloc_outputs(1)
+        nseg = -(-w.d // 256)
+        groups = -(-w.f // 16)
+        per_expert = 2 * nseg * min(groups, 16) * 3 * 512 + 2 * 3 * 256 * 8 * 4
+        for seed, P in ((1, 4), (2, 1), (3, 6)):
+            x = synth.hidden(seed, 1, w.d, "f32", "cuda")
+            B.waste_moe_set_lookahead(layer.handle, layer.handle, P)
+            layer.route(x, 1, idx, gate, logits)  # scores (and so clears) a pending prediction
+            layer.reset_stats()
+            layer.step(x, 1, idx, gate, out, 0, logits)
+            layer.step(x, 1, idx, gate, out, 0, logits)
+            plain.step(x, 1, idx2, gate2, out2, 0, logits2)
+            torch.cuda.synchronize()
+            st = layer.stats()
+            assert st["prefetch_experts"] == 2 * P
+            assert st["prefetch_issued_bytes"] == 2 * P * per_expert
+            assert st["prediction_hits"] == P
+            assert torch.equal(idx, idx2)
+            assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
+        B.waste_moe_set_lookahead(layer.handle, None, 0)
+        layer.route(x, 1, idx, gate, logits)
+        layer.reset_stats()
+        layer.step(x, 1, idx, gate, out, 0, logits)
+        torch.cuda.synchronize()
+        st = layer.stats()
+        assert st["prefetch_experts"] == 0 and st["prediction_hits"] == 0
+    finally:
+        layer.close()
+        plain.close()
+
+
+def test_set_lookahead_rejects_bad_arguments():
+    w = synth.Workload("la-bad", 512, 256, 16, 4, 1, "f32", "none")
+    a = MoELayer(w, 0, 0, "cuda")
+    b = MoELayer(synth.Workload("la-bad2", 1024, 256, 16, 4, 1, "f32", "none"), 0, 1, "cuda")
+    try:
+        with pytest.raises(B.WasteError):
+            B.waste_moe_set_lookahead(a.handle, a.handle, 17)  # more than the next layer's experts
+        with pytest.raises(B.WasteError):
+            B.waste_moe_set_lookahead(a.handle, b.handle, 2)  # another hidden size
+        with pytest.raises(B.WasteError):
+            B.waste_moe_set_lookahead(None, a.handle, 2)
+        B.waste_moe_set_lookahead(a.handle, None, 0)
+    finally:
+        a.close()
+        b.close()
