@@ -32,7 +32,6 @@
 // rebuilds each 8-weight vector in registers (3 codebook rows summed) before an
 // 8-term dot product.
 #include "lut_dev.cuh"
-#include "route_dev.cuh"
 
 namespace wm {
 
@@ -87,54 +86,47 @@ __global__ void __launch_bounds__(kNT, 1) lut_kernel(const LutArgs A) {
 // built, so that the fence of the count runs beside that unit's rows (the CTA's last gate/up
 // unit is counted before its first down unit).  Same unit arithmetic as the per-phase kernels:
 // the results are bit-identical to theirs.
-// The lookahead's share of lookahead CTA k of n_la (inside the one-launch expert kernel): CTA 0
-// selects the next layer's top-P experts from its selection keys (warp sorts merged in a tree,
-// the order of the router's own selection), stores them as that layer's prediction and
-// publishes it on sync[2]; every lookahead CTA then waits for it (bounded) and asks L2 for its
-// share of the predicted experts' pieces.  The last one to finish puts sync[2..3] back to zero.
-__device__ __noinline__ void lookahead_item(const LutAhead LA, unsigned *sync, int k, int n_la, uint32_t *err) {
-    unsigned long long *keys = reinterpret_cast<unsigned long long *>(lut_smem);
-    int *ids = reinterpret_cast<int *>(lut_smem + 8 * kThreads);
+// The lookahead's share of lookahead CTA k of n_la (inside the one-launch expert kernel): the
+// next layer's top-P experts, selected from its selection keys by rank (the number of keys that
+// come first in the router's own order: larger key, or equal key and smaller index) -- each
+// lookahead CTA takes the same selection by itself, so none waits for another -- then CTA k's
+// share of the predicted experts' pieces asked of L2.  CTA 0 also stores the prediction.
+__device__ __noinline__ void lookahead_item(const LutAhead LA, int k, int n_la) {
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(lut_smem); // [E]
+    int *sel = reinterpret_cast<int *>(lut_smem + 8 * kThreads);                 // [P]
     __syncthreads(); // the CTA's last unit is done with its shared memory
-    if (k == 0) {
-        route::Cand c;
-        c.key = 0ull;
-        c.id = 0x7fffffff;
-        if ((int)threadIdx.x < LA.E) {
-            c.key = LA.keys[threadIdx.x];
-            c.id = threadIdx.x;
+    for (int i = threadIdx.x; i < LA.E; i += kThreads) keys[i] = LA.keys[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < LA.E; i += kThreads) {
+        const unsigned long long ki = keys[i];
+        int rank = 0;
+        for (int j = 0; j < LA.E; ++j) {
+            const unsigned long long kj = keys[j];
+            rank += (kj > ki || (kj == ki && j < i)) ? 1 : 0;
         }
-        route::warp_sort32(c);
-        route::merge_warp_lists(c, keys, ids);
-        __syncthreads();
-        if ((int)threadIdx.x < LA.P) LA.pred_idx[threadIdx.x] = ids[threadIdx.x];
-        __syncthreads();
+        if (rank < LA.P) sel[rank] = i;
+    }
+    __syncthreads();
+    if (k == 0) {
+        if ((int)threadIdx.x < LA.P) LA.pred_idx[threadIdx.x] = sel[threadIdx.x];
         if (threadIdx.x == 0) {
             *LA.pred_count = LA.P;
             if (LA.stats) {
                 atomicAdd(LA.stats + kStatPrefetchBytes, (unsigned long long)LA.P * lookahead_bytes(LA.nseg, LA.groups));
                 atomicAdd(LA.stats + kStatPrefetchExperts, (unsigned long long)LA.P);
             }
-            __threadfence();
-            atomicExch(sync + 2, 1u);
         }
     }
-    wait_counter(sync + 2, 1u, err);
     const int per = lookahead_pieces(LA.nseg);
-    for (int j = k + n_la * (int)threadIdx.x; j < LA.P * per; j += n_la * (int)blockDim.x) {
-        const int e = __ldcg(LA.pred_idx + j / per);
-        if (e >= 0 && e < LA.E)
-            lookahead_piece(LA.records, LA.stride, LA.off_gate, LA.off_up, LA.nseg, LA.groups, LA.codebooks, e,
-                            j % per);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && atomicAdd(sync + 3, 1u) == (unsigned)n_la - 1) {
-        sync[2] = 0u;
-        sync[3] = 0u;
-    }
+    for (int j = k + n_la * (int)threadIdx.x; j < LA.P * per; j += n_la * kThreads)
+        lookahead_piece(LA.records, LA.stride, LA.off_gate, LA.off_up, LA.nseg, LA.groups, LA.codebooks, sel[j / per],
+                        j % per);
 }
 
-template <bool kBf16, bool kFixed>
+// kAhead: the launch carries the lookahead, in its own instance and out of line (its code inside
+// every instance cost 1.5 us of the one-layer step; inlined into its own instance, 0.2 us per
+// layer of the stack)
+template <bool kBf16, bool kFixed, bool kAhead>
 __global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs A, unsigned *sync, const LutAhead LA) {
     const int n_gu = A.slots * 2 * A.gu_pairs;
     const int n_dn = A.slots * A.npair * A.nrb;
@@ -173,7 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs 
     }
     // the lookahead: the CTAs without a down unit (or, if every CTA has one, CTA 0 at its end)
     const int n_la = n_dn < G ? G - n_dn : 1;
-    if (LA.keys && n_dn < G && mine_dn == 0) lookahead_item(LA, sync, b, n_la, A.err);
+    if constexpr (kAhead)
+        if (n_dn < G && mine_dn == 0) lookahead_item(LA, b, n_la);
     for (int i = 0; i < mine_dn; ++i) {
         const int u = d0 + i * G;
         const bool has_next = i + 1 < mine_dn;
@@ -187,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1) lut_experts_kernel(const LutArgs 
             nullptr, sync + 4 + A.slots + U.slot, (unsigned)(A.npair * A.nrb));
         trace_unit(A, n_gu + u, t0, t_tab);
     }
-    if (LA.keys && n_dn >= G && b == 0) lookahead_item(LA, sync, 0, 1, A.err);
+    if constexpr (kAhead)
+        if (n_dn >= G && b == 0) lookahead_item(LA, 0, 1);
     tab_tc_close<false>(tcs);
 }
 
@@ -332,11 +326,11 @@ bool coop_launch_ok() {
     return c == 1;
 }
 
-template <bool kBf16, bool kFixed>
+template <bool kBf16, bool kFixed, bool kAhead>
 cudaError_t launch_experts_v(const LutArgs &A, unsigned *sync, const LutAhead &LA, int grid, cudaStream_t s) {
     const size_t smem = unit_smem<false>();
     static SmemAttr attr;
-    cudaError_t e = ensure_smem(attr, (const void *)lut_experts_kernel<kBf16, kFixed>, (int)smem);
+    cudaError_t e = ensure_smem(attr, (const void *)lut_experts_kernel<kBf16, kFixed, kAhead>, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(grid);
@@ -348,7 +342,7 @@ cudaError_t launch_experts_v(const LutArgs &A, unsigned *sync, const LutAhead &L
     at[0].val.cooperative = 1;
     lc.attrs = at;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, lut_experts_kernel<kBf16, kFixed>, A, sync, LA);
+    return cudaLaunchKernelEx(&lc, lut_experts_kernel<kBf16, kFixed, kAhead>, A, sync, LA);
 }
 
 // The gate/up and down units in one cooperative launch of at most one CTA per SM.
@@ -357,11 +351,19 @@ cudaError_t launch_experts(const LutArgs &A, unsigned *sync, const LutAhead &LA,
     const int n_gu = A.slots * 2 * A.gu_pairs, n_dn = A.slots * A.npair * A.nrb;
     const int units = n_gu > n_dn ? n_gu : n_dn;
     const int grid = units < num_sms ? units : num_sms;
-    if (tables_at_fixed_base(s))
-        return bf16 ? launch_experts_v<true, true>(A, sync, LA, grid, s)
-                    : launch_experts_v<false, true>(A, sync, LA, grid, s);
-    return bf16 ? launch_experts_v<true, false>(A, sync, LA, grid, s)
-                : launch_experts_v<false, false>(A, sync, LA, grid, s);
+    const bool ahead = LA.keys != nullptr;
+    if (tables_at_fixed_base(s)) {
+        if (ahead)
+            return bf16 ? launch_experts_v<true, true, true>(A, sync, LA, grid, s)
+                        : launch_experts_v<false, true, true>(A, sync, LA, grid, s);
+        return bf16 ? launch_experts_v<true, true, false>(A, sync, LA, grid, s)
+                    : launch_experts_v<false, true, false>(A, sync, LA, grid, s);
+    }
+    if (ahead)
+        return bf16 ? launch_experts_v<true, false, true>(A, sync, LA, grid, s)
+                    : launch_experts_v<false, false, true>(A, sync, LA, grid, s);
+    return bf16 ? launch_experts_v<true, false, false>(A, sync, LA, grid, s)
+                : launch_experts_v<false, false, false>(A, sync, LA, grid, s);
 }
 
 } // namespace
