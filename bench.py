@@ -589,6 +589,8 @@ def run_stack(args, dev, out, w=None, key="stack"):
     out[key] = dict(
         workload=f"{w.n_layers} layers x {w.n_experts} experts, d={w.d} f={w.f} top-{w.top_k}, T=1, fp32, "
                  f"router bias {w.bias}, h += combine per layer; CUDA graph per token; L2 flushed between tokens",
+        lookahead_form="inside the step (waste_moe_set_lookahead): layer L+1's router rows on layer L's "
+                       "router launch, its top-P selected and prefetched by layer L's expert kernel",
         tok_s_lookahead_off=off["tok_s"], tok_s_lookahead_on=on["tok_s"],
         lookahead_speedup=on["tok_s"] / off["tok_s"],
         outputs_bit_identical=bool(torch.equal(final[0], final[w.lookahead])),

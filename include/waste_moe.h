@@ -299,7 +299,9 @@ typedef struct {
 /* Copy the handle's counters (one synchronous copy on the legacy stream after a
  * device synchronise).  Returns WASTE_ETIMEOUT if a bounded device wait gave up,
  * WASTE_EINVAL if a kernel saw an expert index out of range (since create or the
- * last reset), else WASTE_OK. */
+ * last reset), else WASTE_OK.  After WASTE_ETIMEOUT the outputs of the calls since the
+ * last reset are not to be used, and the context is to be treated as unusable: a kernel
+ * that gave up may have left asynchronous copies or tensor-core operations behind it. */
 int waste_moe_stats(const waste_moe *h, waste_moe_stats_t *out);
 
 /* Zero the counters (synchronous). */
