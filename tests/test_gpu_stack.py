@@ -312,3 +312,33 @@ def test_set_lookahead_rejects_bad_arguments():
     finally:
         a.close()
         b.close()
+
+
+def test_lookahead_inside_the_step_into_a_wider_layer():
+    """The next layer may have more experts than the current one: its router rows ride on the
+    current router launch all the same; its own route on the same input scores every one of the P
+    predicted experts as a hit, and the current layer's outputs are unchanged."""
+    wa = synth.Workload("la-a", 512, 256, 16, 4, 1, "f32", "none")
+    wb = synth.Workload("la-b", 512, 256, 40, 6, 1, "f32", "none")
+    a = MoELayer(wa, 0, 0, "cuda")
+    b = MoELayer(wb, 0, 1, "cuda")
+    try:
+        ia, ga, la, oa = a.alloc_outputs(1)
+        ib, gb, lb, ob = b.alloc_outputs(1)
+        x = synth.hidden(9, 1, wa.d, "f32", "cuda")
+        a.step(x, 1, ia, ga, oa, 0, la)
+        torch.cuda.synchronize()
+        ref = oa.clone()
+        b.route(x, 1, ib, gb, lb)  # no prediction pending
+        B.waste_moe_set_lookahead(a.handle, b.handle, 3)
+        b.reset_stats()
+        a.step(x, 1, ia, ga, oa, 0, la)
+        b.route(x, 1, ib, gb, lb)
+        torch.cuda.synchronize()
+        st = b.stats()
+        assert st["prefetch_experts"] == 3 and st["prediction_hits"] == 3
+        assert torch.equal(oa.view(torch.int32), ref.view(torch.int32))
+        B.waste_moe_set_lookahead(a.handle, None, 0)
+    finally:
+        a.close()
+        b.close()
