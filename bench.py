@@ -758,7 +758,7 @@ def run_encoder(args, dev, out):
         cbs.append(cb)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clock_hz = 2.07e9
-    peak_ops = sms * 128 * clock_hz  # fp32 lane operations per second (FADD and FFMA issue)
+    peak_ops = sms * 128 * clock_hz  # fp32 lane operations per second (adds and fused multiply-adds)
     ops = pairs * 16.0  # 8 subtractions + 8 fused multiply-adds per vector and centroid
     # the encoded expert through the expert kernels, one token, against the dense expert
     w = synth.Workload("encoded", d, f, 1, 1, 1, "f32", "none")
@@ -782,7 +782,7 @@ def run_encoder(args, dev, out):
         vector_centroid_pairs_per_s=pairs / (total_ms * 1e-3),
         roofline={"bound": "alu", "achieved": ops / (total_ms * 1e-3) / 1e9, "peak": peak_ops / 1e9,
                   "unit": "Gop/s", "frac": ops / (total_ms * 1e-3) / peak_ops,
-                  "note": "fp32 lane operations (8 FADD + 8 FFMA per vector and centroid) against "
+                  "note": "fp32 lane operations (8 adds + 8 fused multiply-adds per vector and centroid) against "
                           f"{sms} SMs x 128 fp32 lanes x 2.07 GHz"},
         encoded_expert_output_rel_err_vs_dense=rel,
     )

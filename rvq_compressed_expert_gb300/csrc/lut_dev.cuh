@@ -200,7 +200,7 @@ __device__ __forceinline__ float lds_stage(uint32_t a) {
 // each table load's immediate offset (one instruction less per lookup); elsewhere it adds it.
 constexpr uint32_t kDynSmemBase = 1024;
 
-// Table load at shared-window address a + kDynSmemBase + S * 64 KiB: a is the PRMT result
+// Table load at shared-window address a + kDynSmemBase + S * 64 KiB: a is the prmt result
 // alone (code byte and column offset), the base and stage offset the load's immediate.
 template <int S>
 __device__ __forceinline__ float lds_fixed(uint32_t a) {
@@ -609,7 +609,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     // segment's codes again for it: that part's tables are zero (its inputs are)
     const uint8_t *pb0 = U.base[0];
     const uint8_t *pb1 = U.base[1] ? U.base[1] : U.base[0];
-    // 32-bit shared-window address of the tables: a lookup is PRMT, IADD and one
+    // 32-bit shared-window address of the tables: a lookup is prmt, an integer add and one
     // ld.shared with the stage offset as its immediate
     const uint32_t tab32 = (uint32_t)__cvta_generic_to_shared(smem);
     auto load_part = [&](int g, int p, uint4 (&w)[2][kStages]) {
@@ -651,7 +651,7 @@ __device__ __forceinline__ void run_unit(const LutArgs &A, const Unit &Uin, bool
     // the lookups of part p of one row group: acc = (part 0) or += (part 1) the 16 partials.
     // Two code bytes at a time: their three stage entries are added pairwise with packed
     // additions, in the order (T0 + T1) + T2, then into the partials.  fixed: the tables sit
-    // at kDynSmemBase, so a table address is the PRMT result alone.
+    // at kDynSmemBase, so a table address is the prmt result alone.
     auto lookups = [&](auto fixed, const uint4 (&cwp)[kStages], int p, float (&acc)[16]) {
         constexpr bool kFixed = decltype(fixed)::value;
         const uint32_t colb = p ? colb1 : colb0;

@@ -16,9 +16,9 @@
 // loads.  Each lane owns one vector column of each segment and 16 rows per
 // 16-byte chunk; the chunk's bytes are pre-permuted (row (lane ^ q) & 15 at byte
 // q) so the cross-lane reduction of 32 row partials is a select-free butterfly.
-// One PRMT turns a code byte plus the lane's column offset into the table
+// One prmt turns a code byte plus the lane's column offset into the table
 // address (the tables' base and the stage in the load's immediate), so a lookup
-// costs PRMT + LDS and half of a packed fp32 addition.
+// costs a prmt, an ld.shared and half of a packed fp32 addition.
 // Partials of each segment go to a scratch buffer; a down unit reduces the
 // gate/up partials of its slot in a fixed order, applies SwiGLU and builds its
 // own tables; a last kernel combines the k expert outputs with their gates.  A
