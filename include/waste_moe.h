@@ -279,7 +279,9 @@ int waste_moe_prefetch(waste_moe *next_layer, const void *d_h, int32_t T, int32_
  * [0, min(n_experts, 32)], a next layer with another hidden size or activation type or more than
  * 512 experts, or banked handles (they take waste_moe_prefetch).  A call whose shapes do not
  * allow it (several tokens, a router launch that would not fit with the extra rows) runs without
- * it.  h's step and next_layer's route must be ordered on one stream (or by events). */
+ * it.  h's step and next_layer's route must be ordered on one stream (or by events); h keeps a
+ * pointer to next_layer, which must stay alive while the setting holds (turn it off, or destroy
+ * h, first). */
 int waste_moe_set_lookahead(waste_moe *h, waste_moe *next_layer, int32_t n_prefetch);
 
 /* Free the workspace and the handle (NULL is ignored).  Synchronises the device. */
