@@ -28,7 +28,7 @@ constexpr uint32_t kTmA = 384;
 constexpr uint32_t kBHalf = 2 * 32 * 8 * 4;
 constexpr int kTcBytes = 32;
 constexpr int kPrefetchRounds = 1;                 // L2 prefetch distance in row-group rounds
-constexpr int kPrefetchRoundsGu = 2;               // the same for the per-phase gate/up kernel
+constexpr int kPrefetchRoundsGu = 2;               // the same for the per-phase gate/up kernel and the one-launch kernel's units
 
 struct LutArgs {
     const uint8_t *records;
