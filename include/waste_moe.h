@@ -12,7 +12,10 @@
  *      weight), a = silu(G h) * (U h), y = D a, and
  *   4. adds the gate-weighted sum of the k expert outputs into the output.
  * A lookahead call runs the NEXT layer's router on the current hidden state
- * and prefetches the experts it predicts into L2; it never changes outputs.
+ * and prefetches the experts it predicts into L2; it never changes outputs.  For
+ * one token it can instead ride on the current layer's step (waste_moe_set_lookahead:
+ * the next layer's router rows in this layer's router launch, the prediction and
+ * the prefetches in its expert launch), with no extra launch.
  *
  * Sources (web pages about the WASTE engine; page titles and sections):
  *   "Exécuter Kimi K3 avec 29 Go de RAM à 0,50 tok/s"
