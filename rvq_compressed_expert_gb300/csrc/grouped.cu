@@ -26,7 +26,9 @@
 // mma_kernel is warp-specialised: one producer warp moves the codes of each 32-vector
 // segment of the row block (12 KiB, a bulk copy per row group), another the activation tile
 // of each 64-wide K chunk; 16 decode warps turn codes into fp16 weights and store them into
-// tensor memory (tcgen05.st), where the MMA reads its A operand; one thread issues the MMAs.
+// tensor memory (tcgen05.st), where the MMA reads its A operand; two threads, in two warps,
+// issue the MMAs (a chunk of <= 64 tokens: alternate K chunks, into two accumulators the
+// epilogue adds; a larger one: half of its tokens each).
 // Full/empty mbarriers hand the buffers between them, so decoding, copies and MMAs of
 // different chunks overlap.  A CTA takes a contiguous range of items, so an expert's
 // codebooks stay in shared memory across its row blocks.
@@ -245,8 +247,21 @@ constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
 // producers: one warp for the code segments, one for the activation tiles, so neither ring's
 // progress holds the other's copies back
-constexpr int kProdWarp = kDecWarps, kIssueWarp = kDecWarps + 1, kProdBWarp = kDecWarps + 2;
-constexpr int kMmaThreads = kDecThreads + 96;
+// Two MMA-issuing warps: a thread waits ~55-80 cycles for each tcgen05.mma it issues, whatever
+// the MMA's N up to 64 (~100 at N = 128), so with ~20-30 tokens per expert the issue rate of one
+// thread bounds the MMAs; two threads taking alternate K chunks into separate accumulators
+// issue twice as many.  A chunk too wide for two accumulators is split by its tokens instead
+// (the same MMA count per thread, each of half the N).
+constexpr int kProdWarp = kDecWarps, kIssueWarp = kDecWarps + 1, kProdBWarp = kDecWarps + 2,
+              kIssue2Warp = kDecWarps + 3;
+constexpr int kIssuers = 2;
+constexpr int kMmaThreads = kDecThreads + 128;
+// A chunk of at most kSplitMax tokens (and >= 2 K chunks) is split by K between the two
+// issuers: the second's accumulator takes the upper half of each 128-column accumulator.
+constexpr int kSplitTokens = kGroupTokens / 2;
+constexpr int kSplitMax = 64;
+static_assert(kSplitMax <= kSplitTokens, "a split chunk fits half an accumulator");
+__device__ __forceinline__ bool split_issue(int npad, int KC) { return npad <= kSplitMax && KC >= 2; }
 constexpr int kBRing = 4;             // activation tile stages
 constexpr int kARing = 8;             // weight tile stages (in tensor memory)
 constexpr int kSegRing = 4;           // code segment stages
@@ -378,16 +393,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             tc::mbar_init(bar(kSegFull + i), 1);
             tc::mbar_init(bar(kSegEmpty + i), kDecWarps);
         }
+        // a stage is free, and an accumulator full, once both issuers have committed it (a
+        // commit covers that issuer's own MMAs issued so far, or none)
         for (int i = 0; i < kBRing; ++i) {
             tc::mbar_init(bar(kBFull + i), 1);
-            tc::mbar_init(bar(kBEmpty + i), 1);
+            tc::mbar_init(bar(kBEmpty + i), kIssuers);
         }
         for (int i = 0; i < kARing; ++i) {
             tc::mbar_init(bar(kAFull + i), kDecWarps);
-            tc::mbar_init(bar(kAEmpty + i), 1);
+            tc::mbar_init(bar(kAEmpty + i), kIssuers);
         }
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar(kAccFull + i), 1);
+            tc::mbar_init(bar(kAccFull + i), kIssuers);
             tc::mbar_init(bar(kAccEmpty + i), kDecWarps);
         }
         tc::mbar_init_fence();
@@ -486,41 +503,60 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             const uint32_t g = q - 1 - i;
             wait_phase_warp(bar(kBFull + g % kBRing), (g / kBRing) & 1, abort_flag, false);
         }
-    } else if (warp == kIssueWarp) {
-        // ---------------- MMA issue (the whole warp walks the loop; lane 0 issues)
+    } else if (warp == kIssueWarp || warp == kIssue2Warp) {
+        // ---------------- MMA issue (each issuing warp walks the loop; its lane 0 issues).  A
+        // K-split item: the first issuer takes the even chunks of the CTA's chunk sequence, the
+        // second the odd ones (every pass of >= 2 chunks gives each at least one), each into its
+        // own accumulator.  Otherwise both take every chunk, the first for the accumulator
+        // columns (tokens) [0, n0), the second for [n0, npad): B rows from n0 on, n0 a multiple
+        // of 16 (the MMA's N for M = 128); a chunk of 16 tokens is the first issuer's alone.
+        // Both wait for every stage and commit every stage and item, so neither runs more than a
+        // ring ahead of the other or of the producers, and no parity wait is ever two phases off.
+        const uint32_t mine = warp == kIssue2Warp ? 1u : 0u;
         uint32_t q = 0, it = 0;
         for (int item = i0; item < i1; ++item, ++it) {
             const int4 ch = A.chunks[item / nmb];
             const int npad = pad16(ch.z);
-            const uint32_t idesc = tc::idesc_f16_f32(kBM, npad);
+            const bool split = split_issue(npad, KC);
+            const int n0 = npad >= 32 ? ((npad / 2 + 15) & ~15) : npad;
+            const int c0 = split || mine == 0u ? 0 : n0;                 // first token column
+            const int nb = split ? npad : (mine == 0u ? n0 : npad - n0); // 0 or a multiple of 16
+            const uint32_t idesc = tc::idesc_f16_f32(kBM, nb > 0 ? nb : 16);
             // down: item it accumulates into buffer it & 1, free once item it - 2's epilogue is done
             const int ba = kDown ? (int)(it & 1) : 0;
             if (kDown ? it >= 2 : it >= 1)
                 wait_phase_warp(bar(kAccEmpty + ba), kDown ? ((it - 2) >> 1) & 1 : (it - 1) & 1, abort_flag);
             tc::fence_after_sync();
             for (int pass = 0; pass < kPasses; ++pass) {
-                const uint32_t acc = tmem + (uint32_t)(kDown ? ba : pass_mat<kDown>(it, pass)) * kGroupTokens;
+                const uint32_t acc = tmem + (uint32_t)(kDown ? ba : pass_mat<kDown>(it, pass)) * kGroupTokens +
+                                     (split ? mine * (uint32_t)kSplitTokens : (uint32_t)c0);
+                bool fresh = true; // this issuer's first chunk of the pass starts its accumulator
                 for (int kc = 0; kc < KC; ++kc, ++q) {
+                    const bool take = split ? (q & 1u) == mine : nb > 0;
                     const int ab = q % kARing, rs = q % kBRing;
                     wait_phase_warp(bar(kAFull + ab), (q / kARing) & 1, abort_flag);
                     wait_phase_warp(bar(kBFull + rs), (q / kBRing) & 1, abort_flag);
                     tc::fence_after_sync();
                     if (lane == 0) {
-                        const uint32_t a_tm = tmem + kTmemA + (uint32_t)ab * (kBK / 2);
-                        const uint32_t b_addr = sbase + kOffB + rs * kBBytes;
+                        if (take) {
+                            const uint32_t a_tm = tmem + kTmemA + (uint32_t)ab * (kBK / 2);
+                            // B rows of 8 tokens are 1024 bytes apart (the descriptor's SBO)
+                            const uint32_t b_addr = sbase + kOffB + rs * kBBytes + (uint32_t)(c0 / 8) * 1024;
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)
-                            tc::mma_f16_ta(acc, a_tm + kk * 8, tc::smem_desc(b_addr + kk * 256, 128, 1024), idesc,
-                                           (kc | kk) != 0);
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                tc::mma_f16_ta(acc, a_tm + kk * 8, tc::smem_desc(b_addr + kk * 256, 128, 1024),
+                                               idesc, !fresh || kk != 0);
+                        }
                         tc::mma_commit(bar(kAEmpty + ab));
                         tc::mma_commit(bar(kBEmpty + rs));
                     }
+                    if (take) fresh = false;
                     __syncwarp();
                 }
             }
             if (lane == 0) {
                 tc::mma_commit(bar(kAccFull + ba));
-                if (A.stats) {
+                if (A.stats && mine == 0u) {
                     const int mb = item % nmb;
                     const int rows = min(G.n_out - mb * kBM, kBM);
                     atomicAdd(A.stats + kStatDemandCode, (unsigned long long)kPasses * rows * G.nv * kStages);
@@ -531,7 +567,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             }
             __syncwarp();
         }
-        // drain: every MMA issued has completed before TMEM is released
+        // drain: every MMA issued (by either issuer) has completed before TMEM is released
         if (it >= 1) {
             const uint32_t last = it - 1;
             wait_phase_warp(bar(kAccFull + (kDown ? (int)(last & 1) : 0)), kDown ? (last >> 1) & 1 : last & 1,
@@ -566,12 +602,25 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_kernel(const MmaArgs A) {
             const int kcf = (A.f + kBK - 1) / kBK;
             uint8_t *ag = A.ag + (size_t)E.ch.w * kcf * 128;
             const int row = E.row, nt = E.nt, npad = E.npad;
+            const bool split = split_issue(npad, KC);
             for (int c0 = wg * 16; c0 < npad; c0 += 64) {
                 float z[16];
                 tc::tmem_ld16(lane_addr + c0, z);
+                if (split) {
+                    float z2[16];
+                    tc::tmem_ld16(lane_addr + kSplitTokens + c0, z2);
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) z[n] += z2[n];
+                }
                 if constexpr (!kDown) {
                     float u[16];
                     tc::tmem_ld16(lane_addr + kGroupTokens + c0, u);
+                    if (split) {
+                        float u2[16];
+                        tc::tmem_ld16(lane_addr + kGroupTokens + kSplitTokens + c0, u2);
+#pragma unroll
+                        for (int n = 0; n < 16; ++n) u[n] += u2[n];
+                    }
                     if (E.row_ok) {
 #pragma unroll
                         for (int n = 0; n < 16; ++n)
