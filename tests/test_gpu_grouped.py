@@ -80,6 +80,23 @@ def test_forced_tensor_core_path_matches_oracle(shape, act):
     assert st["forward_slots"] == T * k
 
 
+@pytest.mark.parametrize("shape,npads", [
+    ((64, 64, 2, 1, 48), {32}),         # one K chunk: each issuer takes 16 of the 32 token columns
+    ((64, 64, 2, 1, 80), {48}),         # one K chunk, 48 columns: 32 + 16
+    ((128, 128, 4, 2, 60), {32}),       # two K chunks: each issuer one chunk per pass
+    ((256, 136, 2, 1, 128), {64, 80}),  # 64 tokens: alternate K chunks; 80: 48 + 32 token columns;
+                                        # down has 3 K chunks (the last one ragged)
+])
+def test_two_issuer_splits(shape, npads):
+    """The MMAs of a chunk shared by two issuing threads: by alternate K chunks into two
+    accumulators (<= 64 tokens, >= 2 K chunks) or by halves of the tokens."""
+    d, f, E, k, T = shape
+    g_idx, _, st = run_small(d, f, E, k, T, "bf16", B.FLAG_FORCE_MMA)
+    counts = np.bincount(g_idx.ravel(), minlength=E)
+    assert {(int(c) + 15) // 16 * 16 for c in counts if c > 0} == npads, counts
+    assert st["forward_slots"] == T * k
+
+
 def test_batched_bf16_mixed_paths():
     """bf16, 48 tokens, Zipf router bias: popular experts on the tensor cores, rare ones on
     the lookup path, combined per token in rank order."""
